@@ -1,0 +1,227 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache decode-attention library for GB300 (sm_103a).
+ *
+ * One decode step of an LLM attends one new query token per sequence to all of that
+ * sequence's cached keys and values.  The cache is paged: K and V live in fixed-size
+ * blocks of 16 tokens, and a per-sequence block table maps logical block i of a
+ * sequence to a physical block anywhere in a shared pool ("KV Cache primer",
+ * cf-1.com/news/5988169, section 4.1 "PagedAttention"; vLLM's --block-size 16 in
+ * section 5.2).  The layer-wise sparse variant ("How KV Sparsity Achieves 1.5x
+ * Acceleration for vLLM", blogs.novita.ai, sections "System model" and "Key technique 1")
+ * keeps only sink tokens, a recent window and the top-scored tokens of a layer.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument that names tensor data is a DEVICE pointer owned by the
+ *    caller.  The library never allocates, frees or keeps a pointer after a call returns.
+ *  - Calls are asynchronous: they only enqueue kernels on `stream` (a cudaStream_t passed
+ *    as void*; NULL = the legacy default stream) and never synchronise, except
+ *    pkv_read_error.  The first call on a device performs one-time per-device set-up
+ *    (kernel attributes, SM count); make it before capturing a stream into a CUDA graph.
+ *  - Element types: K, V, q, out are bf16 (IEEE binary16-bfloat, 2 bytes); block tables,
+ *    lengths and index lists are int32; slot mappings are int64.
+ *  - Layouts are dense row-major with the shapes stated per argument (no strides).
+ *  - Paged pool layout: k_cache and v_cache are [num_blocks, num_kv_heads, 16, head_dim];
+ *    token `off` of physical block `p` for kv head `g` is row ((p*Hkv + g)*16 + off).
+ *    One (block, kv-head) tile is 16*head_dim*2 bytes and contiguous (4 KiB at d=128).
+ *  - A slot is a physical token position: slot = p*16 + off.  Slot < 0 means "skip".
+ *  - GQA: query head h reads kv head h / G, G = num_q_heads / num_kv_heads.
+ *  - Return value: PKV_OK (0) on success; a negative PKV_ERR_* for an argument the host
+ *    rejects (nothing is enqueued then); PKV_ERR_CUDA_BASE + cudaError_t (>= 1000) if a
+ *    launch failed.
+ *  - Errors only the device can see (a block id outside the pool, a kept index outside
+ *    the context, a slot outside the pool, a TMA wait that timed out) never trap: the
+ *    offending access is skipped and the first such PKV_DEV_* code is stored into
+ *    *error_word (a device int32 the caller zero-initialises; NULL disables reporting).
+ *    Output rows touched by a device-detected error are unspecified but finite-safe.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_BLOCK_SIZE 16
+
+/* Host-side status codes. */
+#define PKV_OK 0
+#define PKV_ERR_NULL_POINTER (-1)   /* a required pointer is NULL */
+#define PKV_ERR_DIMS (-2)           /* a size is negative/zero where it must be positive */
+#define PKV_ERR_BLOCK_SIZE (-3)     /* block_size != 16 */
+#define PKV_ERR_HEAD_DIM (-4)       /* head_dim not in {64, 128} */
+#define PKV_ERR_GQA (-5)            /* num_q_heads % num_kv_heads != 0 or unsupported G */
+#define PKV_ERR_WORKSPACE (-6)      /* workspace NULL or smaller than the *_workspace_bytes query */
+#define PKV_ERR_ALIGNMENT (-7)      /* a tensor pointer is not 16-byte aligned */
+#define PKV_ERR_ARGUMENT (-8)       /* any other invalid scalar argument */
+#define PKV_ERR_NO_DEVICE (-9)      /* no current CUDA device could be queried */
+#define PKV_ERR_CUDA_BASE 1000      /* + cudaError_t of a failed launch */
+
+/* Device-side error codes stored into *error_word (first one wins). */
+#define PKV_DEV_OK 0
+#define PKV_DEV_BAD_BLOCK_ID 1      /* block table entry outside [0, num_blocks) */
+#define PKV_DEV_BAD_SLOT 2          /* slot >= num_blocks*16 */
+#define PKV_DEV_BAD_KEPT_INDEX 3    /* kept index outside [0, context_len) */
+#define PKV_DEV_BAD_CONTEXT_LEN 4   /* context_len < 0 or > max_blocks_per_seq*16 */
+#define PKV_DEV_WAIT_TIMEOUT 5      /* an mbarrier wait exceeded its bound (kernel gave up) */
+#define PKV_DEV_BAD_SCORE 6         /* NaN score given to top-k selection */
+
+/* Shape record shared by the calls. */
+typedef struct pkv_dims {
+  int32_t batch;              /* B: sequences in this decode step */
+  int32_t num_q_heads;        /* Hq */
+  int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0 */
+  int32_t head_dim;           /* d: 64 or 128 */
+  int32_t block_size;         /* tokens per physical block; must be 16 */
+  int32_t num_blocks;         /* NB: physical blocks in each of the K and V pools */
+  int32_t max_blocks_per_seq; /* MB: row length of block_tables */
+} pkv_dims;
+
+/*
+ * pkv_kv_append -- write this step's new key/value rows into their cache slots.
+ * Defines: the decode stage computes K,V of the new token only and appends them to the
+ * cache ("KV Cache primer", cf-1.com/news/5988169, section 2.2); all layers of one step
+ * share one write position ("naive KV cache", koas-w.github.io/posts/20260325-kvcache,
+ * the seq_len pitfall), so one slot_mapping serves every layer.
+ *   k_cache, v_cache : [NB, Hkv, 16, d] bf16, updated in place.
+ *   k, v             : [num_tokens, Hkv, d] bf16, the new rows.
+ *   slot_mapping     : [num_tokens] int64; token i goes to slot slot_mapping[i]
+ *                      (block slot/16, offset slot%16) for every kv head; < 0 skips it.
+ *                      Two tokens with the same slot in one call is invalid input.
+ *   num_tokens       : >= 0 (0 enqueues nothing).
+ *   dims             : uses num_kv_heads, head_dim, block_size, num_blocks.
+ *   error_word       : optional; receives PKV_DEV_BAD_SLOT for slot >= NB*16.
+ * Bit-exact: the cache rows become exactly the input bits.
+ */
+int pkv_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
+                  const int64_t* slot_mapping, int64_t num_tokens, const pkv_dims* dims,
+                  int32_t* error_word, void* stream);
+
+/*
+ * pkv_decode_workspace_bytes -- bytes of device workspace pkv_paged_decode_attention
+ * needs for these dims on the current device (split-K partial results).  The workspace
+ * needs no initialisation and may be reused by consecutive calls on one stream.
+ * Returns 0 if dims are invalid.
+ */
+size_t pkv_decode_workspace_bytes(const pkv_dims* dims);
+
+/*
+ * pkv_paged_decode_attention -- out = softmax(scale * q K^T) V per sequence and query head.
+ * Defines: the attention formula ("Transformer模型中的KV Cache优化推理策略",
+ * yutianautomatic.com, section "为什么传统推理方式难以为继"), evaluated at decode time
+ * with the new token's query against all cached keys ("KV Cache primer" section 2.2), K/V
+ * gathered through the block table (section 4.1); the optional sliding window keeps only
+ * the most recent `window` tokens (section 4.3).  Computed with the one-pass online softmax
+ * (running max and running sum, output divided by the sum at the end) of "How KV Sparsity
+ * Achieves 1.5x Acceleration for vLLM", section "2. Attention modification" (Fig. 7),
+ * split over context blocks and merged by log-sum-exp.
+ *   out            : [B, Hq, d] bf16 (round-to-nearest-even of the fp32 result).
+ *   q              : [B, Hq, d] bf16.
+ *   k_cache,v_cache: [NB, Hkv, 16, d] bf16.
+ *   block_tables   : [B, MB] int32; entry [b][i] = physical block of logical block i.
+ *                    Only the entries covering the attended tokens are read.
+ *   context_lens   : [B] int32; L_b = tokens of sequence b INCLUDING this step's token;
+ *                    0 <= L_b <= MB*16.  L_b == 0 gives a zero output row.
+ *   scale          : logit scale (normally 1/sqrt(d)).
+ *   window         : > 0 attends tokens [max(0, L_b - window), L_b); <= 0 attends all.
+ *   workspace      : >= pkv_decode_workspace_bytes(dims) bytes, 16-byte aligned.
+ *   error_word     : optional; PKV_DEV_BAD_BLOCK_ID / _BAD_CONTEXT_LEN / _WAIT_TIMEOUT.
+ * Supported: d in {64, 128}; G in {1, 2, 4, 6, 8}.
+ */
+int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               const int32_t* context_lens, float scale, int32_t window,
+                               void* workspace, size_t workspace_bytes, const pkv_dims* dims,
+                               int32_t* error_word, void* stream);
+
+/*
+ * pkv_sparse_decode_workspace_bytes -- workspace for pkv_sparse_decode_attention with
+ * kept lists of row length max_kept.  Returns 0 if the arguments are invalid.
+ */
+size_t pkv_sparse_decode_workspace_bytes(const pkv_dims* dims, int32_t max_kept);
+
+/*
+ * pkv_sparse_decode_attention -- decode attention over a kept subset of each sequence's
+ * tokens (the layer-wise sparse variant: a layer keeps high-score and recent KV and drops
+ * the rest, "How KV Sparsity Achieves 1.5x Acceleration for vLLM", sections "System
+ * model" and "Key technique 1").  Same formula as pkv_paged_decode_attention, with the
+ * attended set of (b, kv head g) = kept_index_lists[b][g][0 : kept_lens[b]], gathered row
+ * by row from the full paged pool through block_tables.
+ *   kept_index_lists : [B, Hkv, max_kept] int32 logical token positions, strictly
+ *                      ascending, each in [0, context_lens[b]).
+ *   kept_lens        : [B] int32 in [0, max_kept]; every kv head of b keeps that many.
+ *   other arguments  : as pkv_paged_decode_attention (no window).
+ */
+int pkv_sparse_decode_attention(void* out, const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                const int32_t* context_lens,
+                                const int32_t* kept_index_lists, const int32_t* kept_lens,
+                                int32_t max_kept, float scale, void* workspace,
+                                size_t workspace_bytes, const pkv_dims* dims,
+                                int32_t* error_word, void* stream);
+
+/*
+ * pkv_kv_select_topk -- choose the tokens a sparse layer keeps, per (sequence, kv head):
+ * the first n_sink tokens (attention sinks: the start token carries massive activations,
+ * "How KV Sparsity..." introduction, Fig. 1), the n_recent most recent tokens, and the
+ * k_top highest-scoring tokens among the rest (pruning drops low-score KV pairs and
+ * retains high-score and nearby ones, section "System model"; the score is per layer and
+ * head, a sum of softmax probabilities, section "2. Attention modification").
+ *   kept_out       : [B, Hkv, n_sink + k_top + n_recent] int32, ascending token positions;
+ *                    entries past kept_lens_out[b] are left untouched.
+ *   kept_lens_out  : [B] int32 = min(L_b, n_sink + k_top + n_recent).
+ *   score_accum    : [B, Hkv, score_stride] fp32; score of token t is [b][g][t], t < L_b.
+ *   context_lens   : [B] int32, 0 <= L_b <= score_stride.
+ * Rule: if L_b <= n_sink + k_top + n_recent every token is kept.  Otherwise candidates are
+ * [n_sink, L_b - n_recent), ordered by score descending, equal scores by lower position
+ * first (-0.0 equals +0.0); the first k_top candidates are kept.  Bit-exact.  NaN scores are
+ * invalid (PKV_DEV_BAD_SCORE).  Supports score_stride <= 262144.
+ */
+int pkv_kv_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* score_accum,
+                       int32_t score_stride, const int32_t* context_lens, int32_t n_sink,
+                       int32_t n_recent, int32_t k_top, const pkv_dims* dims,
+                       int32_t* error_word, void* stream);
+
+/*
+ * pkv_kv_compact -- copy each (sequence, kv head)'s kept tokens into a compact paged pool:
+ * compact position j of (b, g) receives source token kept_index_lists[b][g][j], so that
+ * the compact pool holds the layer's retained KV in 16-token blocks and plain paged decode
+ * over it with context length kept_lens[b] equals sparse decode over the full pool (the
+ * per-layer block-table policy of "How KV Sparsity...", section "Key technique 1", Fig. 5).
+ *   dst_k_cache, dst_v_cache : [dst_num_blocks, Hkv, 16, d] bf16, written at the slots the
+ *                              copy addresses; other slots untouched.
+ *   dst_block_tables         : [B, dst_max_blocks_per_seq] int32.
+ *   src_*                    : the full pool and its block table, shapes per src_dims.
+ *   context_lens             : [B] int32 source context lengths (for index validation).
+ *   kept_index_lists, kept_lens, max_kept : as pkv_sparse_decode_attention.
+ * Bit-exact.
+ */
+int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_block_tables,
+                   int32_t dst_num_blocks, int32_t dst_max_blocks_per_seq,
+                   const void* src_k_cache, const void* src_v_cache,
+                   const int32_t* src_block_tables, const int32_t* context_lens,
+                   const int32_t* kept_index_lists, const int32_t* kept_lens,
+                   int32_t max_kept, const pkv_dims* src_dims, int32_t* error_word,
+                   void* stream);
+
+/*
+ * pkv_read_error -- synchronise `stream`, then return the device error word's value
+ * (PKV_DEV_*), or a negative host status if it cannot be read.  If `clear` is non-zero
+ * the word is reset to 0 afterwards.  Diagnostic; not for the hot loop.
+ */
+int pkv_read_error(int32_t* error_word, int32_t clear, void* stream);
+
+/* Human-readable text for a host status (PKV_OK / PKV_ERR_*) or >= PKV_ERR_CUDA_BASE. */
+const char* pkv_status_string(int status);
+
+/* Human-readable text for a device error code (PKV_DEV_*). */
+const char* pkv_device_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,206 @@
+"""fp64 CPU oracle for the paged KV-cache decode path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg (and its
+``--impl reference`` arm) may import this package.  The library under
+``paged_kv_cache_mapped_gb300`` never does, and shares no code with it: the arithmetic
+lives in ``pkv_oracle.c`` (plain C, fp64), this module only compiles it with gcc and
+marshals numpy arrays through ctypes.
+
+bf16 tensors are passed as their raw bits (numpy ``uint16``).  Every function raises
+``OracleError`` when the C side refuses its input.
+
+Parity status of each function (what pins it; see ``tests/test_oracle_*.py``):
+  kv_cache_bytes   -- pinned by the worked examples of the KV-cache primer page (golden file)
+  kv_append        -- pinned by a brute-force dict-of-slots model and untouched-slot checks
+  paged_decode     -- pinned by closed forms (q=0, one token, equal rows, two tokens, W=1),
+                      block-permutation invariance and torch SDPA (fp64) on contiguous K/V
+  sparse_decode    -- pinned by kept=all == paged, and gather == compact-then-paged
+  select_topk      -- pinned by a hand-worked golden case, exhaustive subset search on tiny
+                      inputs and the selection invariants
+  compact          -- pinned by a brute-force dict-of-slots model
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+_CODES = {
+    -1: "invalid argument",
+    -2: "slot outside the pool",
+    -3: "block id outside the pool",
+    -4: "token index outside the context / not ascending",
+    -5: "invalid length",
+    -6: "NaN score",
+    -7: "out of memory",
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile pkv_oracle.c into liboracle.so (with OpenMP when gcc supports it)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.oracle_num_threads.restype = i32
+            lib.oracle_kv_cache_bytes.restype = i64
+            lib.oracle_kv_cache_bytes.argtypes = [i64] * 6
+            lib.oracle_kv_append.argtypes = [P, P, P, P, P, i64, i32, i32, i64]
+            lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, i32,
+                                                f64, i32, P, i64]
+            lib.oracle_sparse_decode.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                                 i64, i32, f64, P, i64]
+            lib.oracle_select_topk.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, i32]
+            lib.oracle_compact.argtypes = [P, P, P, i64, i32, P, P, P, P, P, P, i32, i32, i32,
+                                           i32, i64, i32]
+            for name in ("oracle_kv_append", "oracle_paged_decode", "oracle_sparse_decode",
+                         "oracle_select_topk", "oracle_compact"):
+                getattr(lib, name).restype = i32
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise OracleError(f"{what}: {_CODES.get(status, status)}")
+
+
+def _arr(x, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(x)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def kv_cache_bytes(batch, layers, heads, head_dim, seq_len, dtype_bytes) -> int:
+    return int(_load().oracle_kv_cache_bytes(batch, layers, heads, head_dim, seq_len, dtype_bytes))
+
+
+def kv_append(k_cache, v_cache, k, v, slot_mapping):
+    """Return copies of the uint16 pools [NB,Hkv,16,d] after writing k, v [T,Hkv,d] at the slots."""
+    kc = np.array(_arr(k_cache, np.uint16), copy=True)
+    vc = np.array(_arr(v_cache, np.uint16), copy=True)
+    k = _arr(k, np.uint16)
+    v = _arr(v, np.uint16)
+    slots = _arr(slot_mapping, np.int64)
+    nb, hkv, bs, d = kc.shape
+    assert bs == 16 and k.shape == (slots.shape[0], hkv, d) and v.shape == k.shape
+    _check(_load().oracle_kv_append(_ptr(kc), _ptr(vc), _ptr(k), _ptr(v), _ptr(slots),
+                                    slots.shape[0], hkv, d, nb), "kv_append")
+    return kc, vc
+
+
+def _rows(rows, batch, hq):
+    if rows is None:
+        return None, batch * hq
+    r = _arr(np.asarray(rows, dtype=np.int64), np.int64)
+    return r, r.shape[0]
+
+
+def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale, window=0, rows=None):
+    """fp64 attention.  rows=None -> [B,Hq,d]; else a list of b*Hq+h -> [len(rows), d]."""
+    q = _arr(q, np.uint16)
+    kc = _arr(k_cache, np.uint16)
+    vc = _arr(v_cache, np.uint16)
+    bt = _arr(block_tables, np.int32)
+    lens = _arr(context_lens, np.int32)
+    b, hq, d = q.shape
+    nb, hkv, bs, d2 = kc.shape
+    assert bs == 16 and d2 == d and vc.shape == kc.shape and bt.shape[0] == b
+    r, n = _rows(rows, b, hq)
+    out = np.zeros((n, d), dtype=np.float64)
+    _check(_load().oracle_paged_decode(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(lens),
+                                       b, hq, hkv, d, nb, bt.shape[1], float(scale), int(window),
+                                       None if r is None else _ptr(r), n), "paged_decode")
+    return out.reshape(b, hq, d) if rows is None else out
+
+
+def sparse_decode(q, k_cache, v_cache, block_tables, context_lens, kept, kept_lens, scale, rows=None):
+    """fp64 attention over kept[b][g][:kept_lens[b]]."""
+    q = _arr(q, np.uint16)
+    kc = _arr(k_cache, np.uint16)
+    vc = _arr(v_cache, np.uint16)
+    bt = _arr(block_tables, np.int32)
+    lens = _arr(context_lens, np.int32)
+    kept = _arr(kept, np.int32)
+    kl = _arr(kept_lens, np.int32)
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = kc.shape
+    assert kept.shape[:2] == (b, hkv)
+    r, n = _rows(rows, b, hq)
+    out = np.zeros((n, d), dtype=np.float64)
+    _check(_load().oracle_sparse_decode(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(lens),
+                                        _ptr(kept), _ptr(kl), kept.shape[2], b, hq, hkv, d, nb,
+                                        bt.shape[1], float(scale), None if r is None else _ptr(r), n),
+           "sparse_decode")
+    return out.reshape(b, hq, d) if rows is None else out
+
+
+def select_topk(scores, context_lens, n_sink, n_recent, k_top):
+    """Return (kept [B,Hkv,K] int32 with -1 past kept_lens, kept_lens [B])."""
+    s = _arr(scores, np.float32)
+    lens = _arr(context_lens, np.int32)
+    b, hkv, stride = s.shape
+    kmax = n_sink + k_top + n_recent
+    kept = np.full((b, hkv, kmax), -1, dtype=np.int32)
+    kl = np.zeros((b,), dtype=np.int32)
+    _check(_load().oracle_select_topk(_ptr(kept), _ptr(kl), _ptr(s), stride, _ptr(lens), b, hkv,
+                                      n_sink, n_recent, k_top), "select_topk")
+    return kept, kl
+
+
+def compact(dst_k, dst_v, dst_block_tables, src_k, src_v, src_block_tables, context_lens, kept,
+            kept_lens):
+    """Return copies of the destination pools after the compaction copy."""
+    dk = np.array(_arr(dst_k, np.uint16), copy=True)
+    dv = np.array(_arr(dst_v, np.uint16), copy=True)
+    dbt = _arr(dst_block_tables, np.int32)
+    sk = _arr(src_k, np.uint16)
+    sv = _arr(src_v, np.uint16)
+    sbt = _arr(src_block_tables, np.int32)
+    lens = _arr(context_lens, np.int32)
+    kept = _arr(kept, np.int32)
+    kl = _arr(kept_lens, np.int32)
+    b, hkv, max_kept = kept.shape
+    d = sk.shape[3]
+    _check(_load().oracle_compact(_ptr(dk), _ptr(dv), _ptr(dbt), dk.shape[0], dbt.shape[1],
+                                  _ptr(sk), _ptr(sv), _ptr(sbt), _ptr(lens), _ptr(kept), _ptr(kl),
+                                  max_kept, b, hkv, d, sk.shape[0], sbt.shape[1]), "compact")
+    return dk, dv

@@ -1,0 +1,378 @@
+/*
+ * pkv_oracle.c -- plain, slow, fp64 CPU restatement of what the paged KV-cache decode path
+ * computes.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the bench's CPU
+ * baseline load it; the library's own path never does.  It shares no code, header, table
+ * or constant with the CUDA library: every operation is written here straight from its
+ * definition, in the order the definition states it, with no blocking, fusion or
+ * reordering.  bf16 values are widened exactly to double; sums and exponentials are fp64.
+ *
+ * Page names used in the citations below:
+ *   [primer]  KV-cache primer article, cf-1.com/news/5988169 (sections numbered as on the page)
+ *   [novita]  "How KV Sparsity Achieves 1.5x Acceleration for vLLM", blogs.novita.ai
+ *   [naive]   naive KV cache post, koas-w.github.io/posts/20260325-kvcache
+ *   [tfcache] "Transformer模型中的KV Cache优化推理策略", yutianautomatic.com
+ *
+ * Return codes: 0 = ok, negative = the input breaks the stated contract (the oracle
+ * refuses to guess).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_BLOCK 16 /* tokens per block: [primer] section 4.1 and section 5.2 (--block-size 16) */
+
+#define ORC_OK 0
+#define ORC_ERR_ARG (-1)
+#define ORC_ERR_SLOT (-2)
+#define ORC_ERR_BLOCK (-3)
+#define ORC_ERR_INDEX (-4)
+#define ORC_ERR_LEN (-5)
+#define ORC_ERR_NAN (-6)
+#define ORC_ERR_MEM (-7)
+
+/* bfloat16 is the upper half of an IEEE binary32: widening is exact. */
+static double bf16_to_double(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/*
+ * KV-cache size in bytes: 2 (K and V) x batch x layers x heads x head_dim x seq_len x
+ * bytes per element.  [primer] section 3.1 (size formula).
+ */
+int64_t oracle_kv_cache_bytes(int64_t batch, int64_t layers, int64_t heads, int64_t head_dim,
+                              int64_t seq_len, int64_t dtype_bytes) {
+  return 2 * batch * layers * heads * head_dim * seq_len * dtype_bytes;
+}
+
+/*
+ * Append: each new token's K and V rows are stored at its slot, for every kv head.
+ * A slot is physical block * 16 + offset inside the block ([primer] section 4.1: blocks of
+ * 16 tokens mapped through a block table); the decode step stores only the new token's K,V
+ * ([primer] section 2.2).  Slot < 0 skips the token.
+ * Pools are [NB][Hkv][16][d] uint16 (bf16 bits); k, v are [T][Hkv][d].
+ */
+int oracle_kv_append(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k, const uint16_t* v,
+                     const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                     int head_dim, int64_t num_blocks) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return ORC_ERR_ARG;
+  for (int64_t i = 0; i < num_tokens; ++i) {
+    int64_t slot = slot_mapping[i];
+    if (slot < 0) continue;
+    if (slot >= num_blocks * ORC_BLOCK) return ORC_ERR_SLOT;
+    int64_t block = slot / ORC_BLOCK;
+    int64_t offset = slot % ORC_BLOCK;
+    for (int g = 0; g < num_kv_heads; ++g) {
+      int64_t dst = ((block * num_kv_heads + g) * ORC_BLOCK + offset) * head_dim;
+      int64_t src = (i * num_kv_heads + g) * head_dim;
+      for (int e = 0; e < head_dim; ++e) {
+        k_cache[dst + e] = k[src + e];
+        v_cache[dst + e] = v[src + e];
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+/*
+ * Attention of one query row over an explicit list of logical token positions:
+ *   s_t = scale * sum_e q[e] * K_t[e]           (dot product with each cached key)
+ *   out = sum_t exp(s_t - max s) V_t / sum_t exp(s_t - max s)     (softmax, then weighted V)
+ * [tfcache] section on why plain recomputation fails (the Attention formula);
+ * [primer] section 2.2 (the new token's Q against all cached K, weights applied to V).
+ * Logical token t of the sequence lives in physical block block_row[t / 16], offset t % 16
+ * ([primer] section 4.1).  Subtracting the max is the textbook stable softmax; it does not
+ * change the value.  An empty list gives a zero row.
+ */
+static int attend_one_row(double* out, const uint16_t* q_row, const uint16_t* k_cache,
+                          const uint16_t* v_cache, const int32_t* block_row,
+                          int max_blocks_per_seq, int64_t num_blocks, int num_kv_heads,
+                          int head_dim, int kv_head, double scale, const int64_t* tokens,
+                          int64_t n_tokens) {
+  for (int e = 0; e < head_dim; ++e) out[e] = 0.0;
+  if (n_tokens == 0) return ORC_OK;
+  double* logits = (double*)malloc((size_t)n_tokens * sizeof(double));
+  if (!logits) return ORC_ERR_MEM;
+  int64_t* rows = (int64_t*)malloc((size_t)n_tokens * sizeof(int64_t));
+  if (!rows) {
+    free(logits);
+    return ORC_ERR_MEM;
+  }
+  for (int64_t j = 0; j < n_tokens; ++j) {
+    int64_t t = tokens[j];
+    int64_t logical_block = t / ORC_BLOCK;
+    int64_t offset = t % ORC_BLOCK;
+    if (t < 0 || logical_block >= max_blocks_per_seq) {
+      free(logits);
+      free(rows);
+      return ORC_ERR_INDEX;
+    }
+    int64_t physical = block_row[logical_block];
+    if (physical < 0 || physical >= num_blocks) {
+      free(logits);
+      free(rows);
+      return ORC_ERR_BLOCK;
+    }
+    rows[j] = ((physical * num_kv_heads + kv_head) * ORC_BLOCK + offset) * head_dim;
+    double dot = 0.0;
+    for (int e = 0; e < head_dim; ++e)
+      dot += bf16_to_double(q_row[e]) * bf16_to_double(k_cache[rows[j] + e]);
+    logits[j] = scale * dot;
+  }
+  double m = logits[0];
+  for (int64_t j = 1; j < n_tokens; ++j)
+    if (logits[j] > m) m = logits[j];
+  double denom = 0.0;
+  for (int64_t j = 0; j < n_tokens; ++j) {
+    logits[j] = exp(logits[j] - m); /* now the unnormalised weight */
+    denom += logits[j];
+  }
+  for (int64_t j = 0; j < n_tokens; ++j)
+    for (int e = 0; e < head_dim; ++e)
+      out[e] += logits[j] * bf16_to_double(v_cache[rows[j] + e]);
+  for (int e = 0; e < head_dim; ++e) out[e] /= denom;
+  free(logits);
+  free(rows);
+  return ORC_OK;
+}
+
+/*
+ * Paged decode attention for the rows listed in `row_ids` (each = b * Hq + h), or for all
+ * B*Hq rows when row_ids is NULL; out has one d-vector per computed row, in list order.
+ * Query head h reads kv head h / (Hq / Hkv) (grouped-query attention, as [novita] section
+ * "Key technique 1" requires the sparse path to stay compatible with).  The attended tokens
+ * are [start, L_b), start = max(0, L_b - window) when window > 0, else 0: the sliding window
+ * keeps only the most recent `window` tokens ([primer] section 4.3).  L_b counts the token
+ * appended this step.
+ */
+int oracle_paged_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
+                        const uint16_t* v_cache, const int32_t* block_tables,
+                        const int32_t* context_lens, int batch, int num_q_heads,
+                        int num_kv_heads, int head_dim, int64_t num_blocks,
+                        int max_blocks_per_seq, double scale, int window,
+                        const int64_t* row_ids, int64_t n_rows) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return ORC_ERR_ARG;
+  if (num_q_heads % num_kv_heads != 0) return ORC_ERR_ARG;
+  int group = num_q_heads / num_kv_heads;
+  int64_t total = row_ids ? n_rows : (int64_t)batch * num_q_heads;
+  int status = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < total; ++r) {
+    int64_t row = row_ids ? row_ids[r] : r;
+    int b = (int)(row / num_q_heads);
+    int h = (int)(row % num_q_heads);
+    int st = ORC_OK;
+    if (b < 0 || b >= batch) {
+      st = ORC_ERR_ARG;
+    } else {
+      int64_t len = context_lens[b];
+      if (len < 0 || len > (int64_t)max_blocks_per_seq * ORC_BLOCK) {
+        st = ORC_ERR_LEN;
+      } else {
+        int64_t start = 0;
+        if (window > 0 && len > window) start = len - window;
+        int64_t n = len - start;
+        int64_t* tokens = (int64_t*)malloc((size_t)(n > 0 ? n : 1) * sizeof(int64_t));
+        if (!tokens) {
+          st = ORC_ERR_MEM;
+        } else {
+          for (int64_t j = 0; j < n; ++j) tokens[j] = start + j;
+          st = attend_one_row(out + r * head_dim, q + row * head_dim, k_cache, v_cache,
+                              block_tables + (int64_t)b * max_blocks_per_seq,
+                              max_blocks_per_seq, num_blocks, num_kv_heads, head_dim,
+                              h / group, scale, tokens, n);
+          free(tokens);
+        }
+      }
+    }
+    if (st != ORC_OK) {
+#pragma omp critical
+      status = st;
+    }
+  }
+  return status;
+}
+
+/*
+ * Sparse decode attention: the attended set of (b, kv head g) is the kept list
+ * kept[b][g][0 : kept_lens[b]] ([novita] section "System model": the layer attends only the
+ * KV pairs it retained).  The list must be strictly ascending and inside [0, L_b).
+ */
+int oracle_sparse_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
+                         const uint16_t* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, const int32_t* kept, const int32_t* kept_lens,
+                         int max_kept, int batch, int num_q_heads, int num_kv_heads,
+                         int head_dim, int64_t num_blocks, int max_blocks_per_seq, double scale,
+                         const int64_t* row_ids, int64_t n_rows) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kept < 0)
+    return ORC_ERR_ARG;
+  if (num_q_heads % num_kv_heads != 0) return ORC_ERR_ARG;
+  int group = num_q_heads / num_kv_heads;
+  int64_t total = row_ids ? n_rows : (int64_t)batch * num_q_heads;
+  int status = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < total; ++r) {
+    int64_t row = row_ids ? row_ids[r] : r;
+    int b = (int)(row / num_q_heads);
+    int h = (int)(row % num_q_heads);
+    int g = h / group;
+    int st = ORC_OK;
+    int64_t n = (b >= 0 && b < batch) ? kept_lens[b] : -1;
+    if (n < 0 || n > max_kept) {
+      st = ORC_ERR_LEN;
+    } else {
+      const int32_t* list = kept + ((int64_t)b * num_kv_heads + g) * max_kept;
+      int64_t* tokens = (int64_t*)malloc((size_t)(n > 0 ? n : 1) * sizeof(int64_t));
+      if (!tokens) {
+        st = ORC_ERR_MEM;
+      } else {
+        for (int64_t j = 0; j < n && st == ORC_OK; ++j) {
+          tokens[j] = list[j];
+          if (list[j] < 0 || list[j] >= context_lens[b]) st = ORC_ERR_INDEX;
+          if (j > 0 && list[j] <= list[j - 1]) st = ORC_ERR_INDEX;
+        }
+        if (st == ORC_OK)
+          st = attend_one_row(out + r * head_dim, q + row * head_dim, k_cache, v_cache,
+                              block_tables + (int64_t)b * max_blocks_per_seq,
+                              max_blocks_per_seq, num_blocks, num_kv_heads, head_dim, g,
+                              scale, tokens, n);
+        free(tokens);
+      }
+    }
+    if (st != ORC_OK) {
+#pragma omp critical
+      status = st;
+    }
+  }
+  return status;
+}
+
+/* Candidate ordering for the top-k: higher score first; equal scores, lower position first. */
+typedef struct {
+  double score;
+  int32_t position;
+} orc_candidate;
+
+static int candidate_order(const void* a, const void* b) {
+  const orc_candidate* x = (const orc_candidate*)a;
+  const orc_candidate* y = (const orc_candidate*)b;
+  if (x->score > y->score) return -1;
+  if (x->score < y->score) return 1;
+  return (x->position < y->position) ? -1 : (x->position > y->position);
+}
+
+/*
+ * Kept-token selection per (sequence b, kv head g) ([novita] section "System model": drop
+ * low-score KV, retain high-score and recent KV; section "2. Attention modification": per
+ * layer and head, keep the top-k tokens by score; the introduction's attention sinks: the
+ * start token is always important):
+ *   K = n_sink + k_top + n_recent.  If L <= K keep every position 0..L-1.
+ *   Otherwise keep [0, n_sink), the k_top best candidates of [n_sink, L - n_recent) by
+ *   (score descending, position ascending), and [L - n_recent, L); output ascending.
+ * Scores are compared as the fp32 values given (widening to double is exact; -0 == +0).
+ */
+int oracle_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* scores,
+                       int score_stride, const int32_t* context_lens, int batch,
+                       int num_kv_heads, int n_sink, int n_recent, int k_top) {
+  if (batch < 0 || num_kv_heads <= 0 || n_sink < 0 || n_recent < 0 || k_top < 0)
+    return ORC_ERR_ARG;
+  int64_t keep_max = (int64_t)n_sink + k_top + n_recent;
+  int status = ORC_OK;
+  for (int b = 0; b < batch; ++b) {
+    int64_t len = context_lens[b];
+    if (len < 0 || len > score_stride) return ORC_ERR_LEN;
+    kept_lens_out[b] = (int32_t)(len < keep_max ? len : keep_max);
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t pair = 0; pair < (int64_t)batch * num_kv_heads; ++pair) {
+    int b = (int)(pair / num_kv_heads);
+    int64_t len = context_lens[b];
+    const float* row = scores + pair * score_stride;
+    int32_t* dst = kept_out + pair * keep_max;
+    if (len <= keep_max) {
+      for (int64_t t = 0; t < len; ++t) dst[t] = (int32_t)t;
+      continue;
+    }
+    int64_t first = n_sink, last = len - n_recent; /* candidate range [first, last) */
+    int64_t n_cand = last - first;
+    orc_candidate* cand = (orc_candidate*)malloc((size_t)n_cand * sizeof(orc_candidate));
+    unsigned char* chosen = (unsigned char*)calloc((size_t)len, 1);
+    int st = (cand && chosen) ? ORC_OK : ORC_ERR_MEM;
+    for (int64_t c = 0; c < n_cand && st == ORC_OK; ++c) {
+      float s = row[first + c];
+      if (isnan(s)) st = ORC_ERR_NAN;
+      cand[c].score = (double)s;
+      cand[c].position = (int32_t)(first + c);
+    }
+    if (st == ORC_OK) {
+      qsort(cand, (size_t)n_cand, sizeof(orc_candidate), candidate_order);
+      for (int64_t t = 0; t < n_sink; ++t) chosen[t] = 1;
+      for (int64_t c = 0; c < k_top; ++c) chosen[cand[c].position] = 1;
+      for (int64_t t = last; t < len; ++t) chosen[t] = 1;
+      int64_t w = 0;
+      for (int64_t t = 0; t < len; ++t)
+        if (chosen[t]) dst[w++] = (int32_t)t;
+      if (w != keep_max) st = ORC_ERR_ARG;
+    }
+    free(cand);
+    free(chosen);
+    if (st != ORC_OK) {
+#pragma omp critical
+      status = st;
+    }
+  }
+  return status;
+}
+
+/*
+ * Compaction: compact position j of (b, g) -- slot dst_block_tables[b][j / 16]*16 + j % 16
+ * of the destination pool -- receives source token kept[b][g][j] (found through the source
+ * block table).  This realises the per-layer block-table policy of [novita] section "Key
+ * technique 1" (Fig. 5): a sparse layer's retained KV lives in its own 16-token blocks.
+ */
+int oracle_compact(uint16_t* dst_k, uint16_t* dst_v, const int32_t* dst_block_tables,
+                   int64_t dst_num_blocks, int dst_max_blocks_per_seq, const uint16_t* src_k,
+                   const uint16_t* src_v, const int32_t* src_block_tables,
+                   const int32_t* context_lens, const int32_t* kept, const int32_t* kept_lens,
+                   int max_kept, int batch, int num_kv_heads, int head_dim,
+                   int64_t src_num_blocks, int src_max_blocks_per_seq) {
+  if (batch < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kept < 0) return ORC_ERR_ARG;
+  for (int b = 0; b < batch; ++b) {
+    int64_t n = kept_lens[b];
+    if (n < 0 || n > max_kept || n > (int64_t)dst_max_blocks_per_seq * ORC_BLOCK)
+      return ORC_ERR_LEN;
+    for (int g = 0; g < num_kv_heads; ++g) {
+      const int32_t* list = kept + ((int64_t)b * num_kv_heads + g) * max_kept;
+      for (int64_t j = 0; j < n; ++j) {
+        int64_t t = list[j];
+        if (t < 0 || t >= context_lens[b] || t / ORC_BLOCK >= src_max_blocks_per_seq)
+          return ORC_ERR_INDEX;
+        int64_t src_block = src_block_tables[(int64_t)b * src_max_blocks_per_seq + t / ORC_BLOCK];
+        int64_t dst_block = dst_block_tables[(int64_t)b * dst_max_blocks_per_seq + j / ORC_BLOCK];
+        if (src_block < 0 || src_block >= src_num_blocks) return ORC_ERR_BLOCK;
+        if (dst_block < 0 || dst_block >= dst_num_blocks) return ORC_ERR_BLOCK;
+        int64_t src = ((src_block * num_kv_heads + g) * ORC_BLOCK + t % ORC_BLOCK) * head_dim;
+        int64_t dst = ((dst_block * num_kv_heads + g) * ORC_BLOCK + j % ORC_BLOCK) * head_dim;
+        for (int e = 0; e < head_dim; ++e) {
+          dst_k[dst + e] = src_k[src + e];
+          dst_v[dst + e] = src_v[src + e];
+        }
+      }
+    }
+  }
+  return ORC_OK;
+}

@@ -1,0 +1,418 @@
+"""Decode-attention benchmark: tokens/s and KV-read HBM GB/s of one paged decode step.
+
+Default workload (the one the headline metric is quoted on): the Llama-3-8B-shaped decode
+layer -- batch 32, 32 query / 8 kv heads (GQA 4), head_dim 128, block 16, context lengths
+U[3500, 4500] + 1, physical blocks shuffled over a shared pool.  One step = kv_append of the
+new token of every sequence + paged_decode_attention over all cached tokens.  Inputs are
+resident in HBM and rotate over 4 independent pool copies (2.3 GB in total, far above the
+129 MB L2) so no step reads K/V that a previous step left in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-secondary]
+
+With torchrun (N > 1) every rank runs an independent replica of the workload (the path
+shards by sequence with no exchange: weak scaling); rank 0 prints the JSON line with the
+max time over ranks.  `--impl reference` times the fp64 CPU oracle on host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn tokens/s and KV-read HBM GB/s (% of GB300 peak), 1 GPU"
+WORKLOAD = "llama8b"
+ROTATE = 4
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def kv_bytes(lens: torch.Tensor, hkv: int, d: int, window: int = 0) -> int:
+    """Algorithmic bytes of K and V one decode reads: attended tokens x Hkv x d x 2 x 2 B."""
+    L = lens.to(torch.int64)
+    att = torch.minimum(L, torch.full_like(L, window)) if window > 0 else L
+    return int(att.sum()) * hkv * d * 2 * 2
+
+
+def decode_bytes(lens, B, hq, hkv, d, window=0) -> int:
+    """KV + q + out + the block-table entries and lengths the step needs."""
+    blocks = int(((lens.to(torch.int64) + 15) // 16).sum())
+    return kv_bytes(lens, hkv, d, window) + 2 * B * hq * d * 2 + blocks * 4 + B * 4
+
+
+# ------------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import paged_kv_cache_mapped_gb300 as pkv
+    from paged_kv_cache_mapped_gb300 import inputs as W
+
+    dist, rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[WORKLOAD]
+    lens = W.context_lengths(wl)
+    B, hq, hkv, d = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+
+    # pool copy 0 from the CPU generator (also feeds the CPU baseline), 1..3 drawn on device
+    host0 = W.make_layer(wl, layer=0, device="cpu")
+    copies = [{k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in host0.items()}]
+    for r in range(1, ROTATE):
+        copies.append(W.make_layer(wl, layer=r, device=dev, device_rng=True))
+    nb, mb = copies[0]["num_blocks"], copies[0]["max_blocks_per_seq"]
+    for c in copies:
+        assert c["num_blocks"] == nb and c["max_blocks_per_seq"] == mb
+    ws_bytes = pkv.decode_workspace_bytes(B, hq, hkv, d, nb, mb)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=dev)
+    err = pkv.new_error_word(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(c):
+        pkv.kv_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["slot_mapping"],
+                      error_word=err, stream=stream)
+        pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                   c["context_lens"], c["scale"], out=out, workspace=ws,
+                                   error_word=err, stream=stream)
+
+    for i in range(args.warmup):
+        step(copies[i % ROTATE])
+    torch.cuda.synchronize(dev)
+    if pkv.read_error(err) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    _barrier(dist)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            c = copies[i % ROTATE]
+            pkv.kv_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["slot_mapping"],
+                          error_word=err, stream=stream)
+            dec[i][0].record(stream)
+            pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                       c["context_lens"], c["scale"], out=out, workspace=ws,
+                                       error_word=err, stream=stream)
+            dec[i][1].record(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    _barrier(dist)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = _max_over_ranks(dist, ms, dev)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec)
+    if pkv.read_error(err) != 0:
+        raise RuntimeError("device error during the timed region")
+
+    # end to end through the public API: pinned host inputs -> device, step, result -> host
+    e2e = run_e2e(pkv, copies, host0, dev, stream, ws, args)
+
+    hbm, peak_kind = _peaks()
+    bytes_dec = decode_bytes(lens, B, hq, hkv, d)
+    achieved = bytes_dec / (dec_ms * 1e-3) / 1e9
+    tokens_per_s = world * B / (ms * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": round(tokens_per_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/q; shuffled block tables)",
+        "config": {
+            "workload": "llama8b decode layer: B=32, Hq=32, Hkv=8, d=128, block 16, "
+                        "L=U[3500,4500]+1, kv_append + paged decode",
+            "batch": B, "context_tokens": int(lens.sum()), "num_q_heads": hq, "num_kv_heads": hkv,
+            "head_dim": d, "block_size": 16,
+            "l2": f"inputs larger than L2: {ROTATE} rotating pool copies "
+                  f"({ROTATE * 2 * nb * hkv * 16 * d * 2 / 1e9:.2f} GB)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "kv_read_gbs": round(kv_bytes(lens, hkv, d) / (dec_ms * 1e-3) / 1e9, 1),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "paged_decode_attention (split + merge launches)",
+            "achieved": round(achieved, 1),
+            "peak": hbm,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm, 4),
+            "traffic": None,
+            "algorithmic_bytes_per_launch": bytes_dec,
+            "launch_ms": round(dec_ms, 5),
+        },
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(host0, wl, lens)
+    if rank == 0 and args.secondary and world == 1:
+        line["secondary"] = run_secondary(pkv, W, dev, stream, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(pkv, copies, host0, dev, stream, ws, args):
+    """Same step through the public API with the step's inputs copied from pinned host
+    memory and the result read back, inside the timed region."""
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    hosts = [{n: host0[n].pin_memory() for n in names}]
+    for c in copies[1:]:
+        hosts.append({n: c[n].cpu().pin_memory() for n in names})
+    dev_in = [{n: torch.empty_like(copies[0][n]) for n in names} for _ in range(2)]
+    out_h = torch.empty((copies[0]["q"].shape), dtype=torch.bfloat16).pin_memory()
+    out = torch.empty_like(copies[0]["q"])
+    h2d = sum(host0[n].numel() * host0[n].element_size() for n in names)
+    d2h = out.numel() * out.element_size()
+
+    def one(i):
+        h, c, di = hosts[i % ROTATE], copies[i % ROTATE], dev_in[i % 2]
+        for n in names:
+            di[n].copy_(h[n], non_blocking=True)
+        pkv.kv_append(c["k_cache"], c["v_cache"], di["k_new"], di["v_new"], di["slot_mapping"],
+                      stream=stream)
+        pkv.paged_decode_attention(di["q"], c["k_cache"], c["v_cache"], di["block_tables"],
+                                   di["context_lens"], c["scale"], out=out, workspace=ws,
+                                   stream=stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        one(i)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        one(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    B = copies[0]["q"].shape[0]
+    return {"value": round(B / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def cpu_baseline(host0, wl, lens, budget_s: float = 10.0):
+    """The fp64 oracle, as it stands, on the host cores: whole decode steps of the same
+    workload (every row of the batch) until ~budget_s of CPU time."""
+    import oracle
+    q = host0["q"].view(torch.int16).numpy().view(np.uint16)
+    kc = host0["k_cache"].view(torch.int16).numpy().view(np.uint16)
+    vc = host0["v_cache"].view(torch.int16).numpy().view(np.uint16)
+    bt = host0["block_tables"].numpy()
+    ln = host0["context_lens"].numpy()
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.paged_decode(q, kc, vc, bt, ln, wl.scale)
+        steps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(steps * wl.batch / dt, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{steps} full decode steps of the llama8b workload (all {wl.batch}x{wl.num_q_heads} "
+                      f"rows, {int(lens.sum())} context tokens each step; the append's pool copy excluded)"}
+
+
+def run_secondary(pkv, W, dev, stream, args):
+    """Short device-timed measurements of the other workloads' paths (not the headline)."""
+    res = {}
+    hbm, _ = _peaks()
+    # long-context split-K decode: B=4 x 131072 tokens
+    wl = W.WORKLOADS["long128k"]
+    c = W.make_layer(wl, device=dev, device_rng=True)
+    ws = torch.empty(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                c["num_blocks"], c["max_blocks_per_seq"]),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(c["q"])
+
+    def f():
+        pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                   c["context_lens"], c["scale"], out=out, workspace=ws, stream=stream)
+    ms = _time(f, args.warmup, max(5, args.steps // 4), dev, stream)
+    nbytes = decode_bytes(c["context_lens"].cpu(), wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
+    res["long128k_decode"] = {"ms": round(ms, 4), "tokens_per_s": round(wl.batch / (ms * 1e-3), 1),
+                              "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                              "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                              "l2": "2.1 GB of K/V per launch (> L2)"}
+    del c, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def _time(fn, warmup, steps, dev, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps
+
+
+# ------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The fp64 CPU oracle timed on the host cores as the reference arm: each step runs the
+    oracle over a bounded sample of the same workload (4 of the 32 sequences, all heads)."""
+    dist, rank, world = _dist()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    import oracle
+    from paged_kv_cache_mapped_gb300 import inputs as W
+    wl = W.WORKLOADS[WORKLOAD]
+    host0 = W.make_layer(wl, layer=0, device="cpu")
+    n_seq = 4
+    q = host0["q"][:n_seq].contiguous().view(torch.int16).numpy().view(np.uint16)
+    kc = host0["k_cache"].view(torch.int16).numpy().view(np.uint16)
+    vc = host0["v_cache"].view(torch.int16).numpy().view(np.uint16)
+    bt = host0["block_tables"][:n_seq].contiguous().numpy()
+    ln = host0["context_lens"][:n_seq].contiguous().numpy()
+    for _ in range(args.warmup):
+        oracle.paged_decode(q, kc, vc, bt, ln, wl.scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_decode(q, kc, vc, bt, ln, wl.scale)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = round(n_seq / dt, 2)
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "llama8b decode layer (oracle sample: 4 sequences x 32 heads)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": f"{n_seq} of 32 sequences per step, all heads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,224 @@
-"""Paged KV-cache decode attention for GB300 (placeholder until the CUDA binding lands)."""
+"""Paged KV-cache decode attention for GB300 (sm_103a).
+
+Python binding of libpkv (declared in include/pkv.h).  Each function checks the torch
+tensors it is given, builds the C shape record and calls the C-ABI entry point of the same
+name (``pkv_<name>``) on the current CUDA stream.  All computation happens in the library's
+CUDA kernels; CPU tensors are rejected, there is no fallback path.  PyTorch only provides
+device memory (outputs and workspaces are ``torch.empty`` on the inputs' device) and the
+stream handle.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import PkvDims, PkvError, check, header_constants, header_functions, load
+
+__all__ = [
+    "BLOCK_SIZE", "PkvError", "kv_append", "decode_workspace_bytes", "paged_decode_attention",
+    "sparse_decode_workspace_bytes", "sparse_decode_attention", "kv_select_topk", "kv_compact",
+    "read_error", "new_error_word", "header_constants", "header_functions",
+]
+
+BLOCK_SIZE = 16
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, ndim, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _pool_dims(k_cache, v_cache):
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, k_cache.device)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    nb, hkv, bs, d = k_cache.shape
+    if bs != BLOCK_SIZE:
+        raise ValueError(f"pool block size must be {BLOCK_SIZE}")
+    return nb, hkv, d
+
+
+def _dims(batch, hq, hkv, d, nb, mb):
+    return PkvDims(batch, hq, hkv, d, BLOCK_SIZE, nb, mb)
+
+
+def new_error_word(device) -> torch.Tensor:
+    """A zeroed device int32 the kernels report device-side errors into."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def read_error(error_word: torch.Tensor, clear: bool = False, stream=None) -> int:
+    """Synchronise the stream and return the device error code (0 = none)."""
+    _need(error_word, "error_word", torch.int32, 1)
+    return int(load().pkv_read_error(_ptr(error_word), int(bool(clear)),
+                                     _stream(stream, error_word.device)))
+
+
+def kv_append(k_cache, v_cache, k, v, slot_mapping, *, error_word=None, stream=None):
+    """Write k, v [T, Hkv, d] into the pools [NB, Hkv, 16, d] at slot_mapping [T] (int64)."""
+    nb, hkv, d = _pool_dims(k_cache, v_cache)
+    dev = k_cache.device
+    _need(k, "k", torch.bfloat16, 3, dev)
+    _need(v, "v", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    T = slot_mapping.shape[0]
+    if k.shape != (T, hkv, d) or v.shape != k.shape:
+        raise ValueError("k/v must be [num_tokens, num_kv_heads, head_dim]")
+    dims = _dims(0, 0, hkv, d, nb, 0)
+    check("pkv_kv_append", load().pkv_kv_append(
+        _ptr(k_cache), _ptr(v_cache), _ptr(k), _ptr(v), _ptr(slot_mapping), T, ctypes.byref(dims),
+        _ptr(error_word), _stream(stream, dev)))
+
+
+def decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                           max_blocks_per_seq) -> int:
+    dims = _dims(batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq)
+    n = load().pkv_decode_workspace_bytes(ctypes.byref(dims))
+    if n == 0:
+        raise ValueError("invalid dims for paged decode")
+    return int(n)
+
+
+def sparse_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                                  max_blocks_per_seq, max_kept) -> int:
+    dims = _dims(batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq)
+    n = load().pkv_sparse_decode_workspace_bytes(ctypes.byref(dims), int(max_kept))
+    if n == 0:
+        raise ValueError("invalid dims for sparse decode")
+    return int(n)
+
+
+def _decode_inputs(q, k_cache, v_cache, block_tables, context_lens):
+    nb, hkv, d = _pool_dims(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    B, hq, dq = q.shape
+    if dq != d:
+        raise ValueError("q head_dim differs from the pools'")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens batch differs from q's")
+    return _dims(B, hq, hkv, d, nb, block_tables.shape[1]), dev
+
+
+def _out_ws(q, out, workspace, nbytes):
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3, q.device)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    else:
+        _need(workspace, "workspace", torch.uint8, 1, q.device)
+    return out, workspace
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, window=0, *,
+                           out=None, workspace=None, error_word=None, stream=None):
+    """softmax(scale * q K^T) V over the paged cache; returns out [B, Hq, d] bf16."""
+    dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
+    out, workspace = _out_ws(q, out, workspace, nbytes)
+    check("pkv_paged_decode_attention", load().pkv_paged_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
+        _ptr(error_word), _stream(stream, dev)))
+    return out
+
+
+def sparse_decode_attention(q, k_cache, v_cache, block_tables, context_lens, kept_index_lists,
+                            kept_lens, scale, *, out=None, workspace=None, error_word=None,
+                            stream=None):
+    """Decode attention over kept_index_lists [B, Hkv, max_kept][:kept_lens[b]]."""
+    dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    _need(kept_index_lists, "kept_index_lists", torch.int32, 3, dev)
+    _need(kept_lens, "kept_lens", torch.int32, 1, dev)
+    if kept_index_lists.shape[:2] != (dims.batch, dims.num_kv_heads):
+        raise ValueError("kept_index_lists must be [B, Hkv, max_kept]")
+    max_kept = kept_index_lists.shape[2]
+    nbytes = int(load().pkv_sparse_decode_workspace_bytes(ctypes.byref(dims), max_kept))
+    out, workspace = _out_ws(q, out, workspace, nbytes)
+    check("pkv_sparse_decode_attention", load().pkv_sparse_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(kept_index_lists), _ptr(kept_lens), max_kept, float(scale), _ptr(workspace),
+        workspace.numel(), ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+    return out
+
+
+def kv_select_topk(score_accum, context_lens, n_sink, n_recent, k_top, *, kept_out=None,
+                   kept_lens_out=None, error_word=None, stream=None):
+    """Kept positions per (sequence, kv head): sinks, top-k by score, recent window.
+
+    score_accum [B, Hkv, S] fp32 -> (kept [B, Hkv, n_sink+k_top+n_recent] int32 ascending,
+    kept_lens [B] int32); entries past kept_lens[b] are left as they were (-1 when allocated here).
+    """
+    _need(score_accum, "score_accum", torch.float32, 3)
+    dev = score_accum.device
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    B, hkv, stride = score_accum.shape
+    kmax = int(n_sink) + int(k_top) + int(n_recent)
+    if kept_out is None:
+        kept_out = torch.full((B, hkv, kmax), -1, dtype=torch.int32, device=dev)
+    else:
+        _need(kept_out, "kept_out", torch.int32, 3, dev)
+        if kept_out.shape != (B, hkv, kmax):
+            raise ValueError("kept_out must be [B, Hkv, n_sink + k_top + n_recent]")
+    if kept_lens_out is None:
+        kept_lens_out = torch.empty(B, dtype=torch.int32, device=dev)
+    else:
+        _need(kept_lens_out, "kept_lens_out", torch.int32, 1, dev)
+    dims = _dims(B, hkv, hkv, 128, 0, 0)
+    check("pkv_kv_select_topk", load().pkv_kv_select_topk(
+        _ptr(kept_out), _ptr(kept_lens_out), _ptr(score_accum), stride, _ptr(context_lens),
+        int(n_sink), int(n_recent), int(k_top), ctypes.byref(dims), _ptr(error_word),
+        _stream(stream, dev)))
+    return kept_out, kept_lens_out
+
+
+def kv_compact(dst_k_cache, dst_v_cache, dst_block_tables, src_k_cache, src_v_cache,
+               src_block_tables, context_lens, kept_index_lists, kept_lens, *, error_word=None,
+               stream=None):
+    """Copy each (sequence, kv head)'s kept tokens into consecutive slots of the dst pool."""
+    snb, hkv, d = _pool_dims(src_k_cache, src_v_cache)
+    dnb, dhkv, dd = _pool_dims(dst_k_cache, dst_v_cache)
+    if (dhkv, dd) != (hkv, d):
+        raise ValueError("source and destination pools differ in heads or head_dim")
+    dev = src_k_cache.device
+    _need(dst_block_tables, "dst_block_tables", torch.int32, 2, dev)
+    _need(src_block_tables, "src_block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(kept_index_lists, "kept_index_lists", torch.int32, 3, dev)
+    _need(kept_lens, "kept_lens", torch.int32, 1, dev)
+    B = kept_index_lists.shape[0]
+    if kept_index_lists.shape[1] != hkv:
+        raise ValueError("kept_index_lists must be [B, Hkv, max_kept]")
+    dims = _dims(B, hkv, hkv, d, snb, src_block_tables.shape[1])
+    check("pkv_kv_compact", load().pkv_kv_compact(
+        _ptr(dst_k_cache), _ptr(dst_v_cache), _ptr(dst_block_tables), dnb, dst_block_tables.shape[1],
+        _ptr(src_k_cache), _ptr(src_v_cache), _ptr(src_block_tables), _ptr(context_lens),
+        _ptr(kept_index_lists), _ptr(kept_lens), kept_index_lists.shape[2], ctypes.byref(dims),
+        _ptr(error_word), _stream(stream, dev)))

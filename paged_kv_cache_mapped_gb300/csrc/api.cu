@@ -1,0 +1,316 @@
+// api.cu -- the extern "C" boundary declared in include/pkv.h: argument validation on the
+// host, per-device one-time set-up, workspace sizing and kernel launches on the caller's
+// stream.  Allocates nothing and never synchronises (except pkv_read_error).
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "pkv.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxBatch = 4096;
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per mbarrier wait
+constexpr int kNumHeadDims = 2;
+constexpr int kGroups[] = {1, 2, 4, 6, 8};
+constexpr int kNumGroups = 5;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  size_t max_smem_optin = 0;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+
+int head_dim_index(int d) { return d == 128 ? 0 : (d == 64 ? 1 : -1); }
+
+// One-time per-device set-up: SM count and the dynamic shared-memory opt-in of every decode
+// instantiation.  Not a stream operation, so it is legal while a stream is being captured,
+// but the first call should still precede capture.
+const DeviceInfo* device_info(int* status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *status = PKV_ERR_NO_DEVICE;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& info = g_devices[dev];
+  if (!info.ready) {
+    int sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      *status = PKV_ERR_NO_DEVICE;
+      return nullptr;
+    }
+    for (int hd = 0; hd < kNumHeadDims; ++hd) {
+      for (int gi = 0; gi < kNumGroups; ++gi) {
+        for (int sp = 0; sp < 2; ++sp) {
+          const DecodeKernel k = decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp != 0);
+          if (k.split == nullptr) continue;
+          cudaError_t e = cudaFuncSetAttribute(k.split, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+          if (e != cudaSuccess) {
+            cudaGetLastError();
+            *status = PKV_ERR_CUDA_BASE + (int)e;
+            return nullptr;
+          }
+        }
+      }
+    }
+    info.sm_count = sms;
+    info.max_smem_optin = (size_t)optin;
+    info.ready = true;
+  }
+  *status = PKV_OK;
+  return &info;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const pkv_dims* d, bool need_q_heads) {
+  if (d == nullptr) return PKV_ERR_NULL_POINTER;
+  if (d->block_size != PKV_BLOCK_SIZE) return PKV_ERR_BLOCK_SIZE;
+  if (head_dim_index(d->head_dim) < 0) return PKV_ERR_HEAD_DIM;
+  if (d->batch < 0 || d->num_kv_heads <= 0 || d->num_blocks < 0 || d->max_blocks_per_seq < 0)
+    return PKV_ERR_DIMS;
+  if (need_q_heads) {
+    if (d->num_q_heads <= 0) return PKV_ERR_DIMS;
+    if (d->num_q_heads % d->num_kv_heads != 0) return PKV_ERR_GQA;
+  }
+  return PKV_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA_BASE + (int)e; }
+
+// Workspace layout of the decode calls (all offsets 256-byte aligned):
+//   int32 layout[2 + (B+1) + B] | float2 part_ml[B*Hq*max_parts] | float part_o[B*Hq*max_parts*D]
+struct WorkspacePlan {
+  size_t layout_off, ml_off, o_off, total;
+  int max_parts;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WorkspacePlan plan_workspace(const pkv_dims* d, int max_units_per_seq) {
+  WorkspacePlan p{};
+  p.max_parts = (max_units_per_seq + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp + 1;
+  const size_t rows = (size_t)d->batch * d->num_q_heads;
+  p.layout_off = 0;
+  p.ml_off = align256(sizeof(int32_t) * (2 + 2 * (size_t)d->batch + 1));
+  p.o_off = align256(p.ml_off + sizeof(float) * 2 * rows * p.max_parts);
+  p.total = align256(p.o_off + sizeof(float) * rows * p.max_parts * d->head_dim);
+  return p;
+}
+
+int decode_common(void* out, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, const int32_t* kept,
+                  const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
+                  void* workspace, size_t workspace_bytes, const pkv_dims* dims, int32_t* err,
+                  void* stream, bool sparse) {
+  int st = check_dims(dims, true);
+  if (st != PKV_OK) return st;
+  if (dims->batch > kMaxBatch) return PKV_ERR_DIMS;
+  if (dims->batch == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+    return (!workspace) ? PKV_ERR_WORKSPACE : PKV_ERR_NULL_POINTER;
+  if (sparse && (!kept || !kept_lens)) return PKV_ERR_NULL_POINTER;
+  if (sparse && max_kept <= 0) return PKV_ERR_ARGUMENT;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(workspace))
+    return PKV_ERR_ALIGNMENT;
+  const int group = dims->num_q_heads / dims->num_kv_heads;
+  const DecodeKernel k = decode_kernel(dims->head_dim, group, sparse);
+  if (k.split == nullptr) return PKV_ERR_GQA;
+  const int max_units = sparse ? (max_kept + 15) / 16 : dims->max_blocks_per_seq;
+  // the flattened unit count must fit int32
+  if ((long long)dims->batch * dims->num_kv_heads * (long long)(max_units + 1) >= (1ll << 31))
+    return PKV_ERR_DIMS;
+  const WorkspacePlan plan = plan_workspace(dims, max_units);
+  if (workspace_bytes < plan.total) return PKV_ERR_WORKSPACE;
+  const DeviceInfo* info = device_info(&st);
+  if (!info) return st;
+  const size_t smem = decode_smem_bytes(dims->head_dim, group, dims->batch);
+  if (smem > info->max_smem_optin) return PKV_ERR_DIMS;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.split, kDecodeWarps * 32, smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (per_sm < 1) return PKV_ERR_DIMS;
+
+  DecodeArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.kept = kept;
+  a.kept_lens = kept_lens;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.layout = reinterpret_cast<int32_t*>(ws + plan.layout_off);
+  a.part_ml = reinterpret_cast<float2*>(ws + plan.ml_off);
+  a.part_o = reinterpret_cast<float*>(ws + plan.o_off);
+  a.err = err;
+  a.B = dims->batch;
+  a.Hq = dims->num_q_heads;
+  a.Hkv = dims->num_kv_heads;
+  a.NB = dims->num_blocks;
+  a.MB = dims->max_blocks_per_seq;
+  a.max_kept = sparse ? max_kept : 0;
+  a.window = sparse ? 0 : window;
+  a.max_parts = plan.max_parts;
+  a.min_units = kMinUnitsPerWarp;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.timeout_ns = kWaitTimeoutNs;
+  const int grid = info->sm_count * per_sm;
+  return cuda_status(launch_decode(k, a, grid, smem, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
+                  const int64_t* slot_mapping, int64_t num_tokens, const pkv_dims* dims,
+                  int32_t* error_word, void* stream) {
+  int st = check_dims(dims, false);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_DIMS;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !k || !v || !slot_mapping) return PKV_ERR_NULL_POINTER;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k) || !aligned16(v))
+    return PKV_ERR_ALIGNMENT;
+  if (!device_info(&st)) return st;
+  return cuda_status(launch_kv_append(k_cache, v_cache, k, v, slot_mapping, num_tokens,
+                                      dims->num_kv_heads, dims->head_dim, dims->num_blocks,
+                                      error_word, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_dims* dims) {
+  if (check_dims(dims, true) != PKV_OK || dims->batch > kMaxBatch) return 0;
+  return plan_workspace(dims, dims->max_blocks_per_seq).total;
+}
+
+int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               float scale, int32_t window, void* workspace,
+                               size_t workspace_bytes, const pkv_dims* dims, int32_t* error_word,
+                               void* stream) {
+  return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, nullptr, nullptr, 0,
+                       scale, window, workspace, workspace_bytes, dims, error_word, stream, false);
+}
+
+size_t pkv_sparse_decode_workspace_bytes(const pkv_dims* dims, int32_t max_kept) {
+  if (check_dims(dims, true) != PKV_OK || dims->batch > kMaxBatch || max_kept <= 0) return 0;
+  return plan_workspace(dims, (max_kept + 15) / 16).total;
+}
+
+int pkv_sparse_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                const int32_t* kept_index_lists, const int32_t* kept_lens,
+                                int32_t max_kept, float scale, void* workspace,
+                                size_t workspace_bytes, const pkv_dims* dims, int32_t* error_word,
+                                void* stream) {
+  return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, kept_index_lists,
+                       kept_lens, max_kept, scale, 0, workspace, workspace_bytes, dims, error_word,
+                       stream, true);
+}
+
+int pkv_kv_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* score_accum,
+                       int32_t score_stride, const int32_t* context_lens, int32_t n_sink,
+                       int32_t n_recent, int32_t k_top, const pkv_dims* dims, int32_t* error_word,
+                       void* stream) {
+  if (dims == nullptr) return PKV_ERR_NULL_POINTER;
+  if (dims->batch < 0 || dims->num_kv_heads <= 0) return PKV_ERR_DIMS;
+  if (n_sink < 0 || n_recent < 0 || k_top < 0 || score_stride < 0 || score_stride > 262144)
+    return PKV_ERR_ARGUMENT;
+  if ((long long)n_sink + n_recent + k_top > (1ll << 30)) return PKV_ERR_ARGUMENT;
+  if (dims->batch == 0) return PKV_OK;
+  if (!kept_out || !kept_lens_out || !score_accum || !context_lens) return PKV_ERR_NULL_POINTER;
+  int st;
+  if (!device_info(&st)) return st;
+  return cuda_status(launch_select_topk(kept_out, kept_lens_out, score_accum, score_stride,
+                                        context_lens, dims->batch, dims->num_kv_heads, n_sink,
+                                        n_recent, k_top, error_word,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_block_tables,
+                   int32_t dst_num_blocks, int32_t dst_max_blocks_per_seq, const void* src_k_cache,
+                   const void* src_v_cache, const int32_t* src_block_tables,
+                   const int32_t* context_lens, const int32_t* kept_index_lists,
+                   const int32_t* kept_lens, int32_t max_kept, const pkv_dims* src_dims,
+                   int32_t* error_word, void* stream) {
+  int st = check_dims(src_dims, false);
+  if (st != PKV_OK) return st;
+  if (dst_num_blocks < 0 || dst_max_blocks_per_seq < 0 || max_kept < 0) return PKV_ERR_DIMS;
+  if (src_dims->batch == 0 || max_kept == 0) return PKV_OK;
+  if (!dst_k_cache || !dst_v_cache || !dst_block_tables || !src_k_cache || !src_v_cache ||
+      !src_block_tables || !context_lens || !kept_index_lists || !kept_lens)
+    return PKV_ERR_NULL_POINTER;
+  if (!aligned16(dst_k_cache) || !aligned16(dst_v_cache) || !aligned16(src_k_cache) ||
+      !aligned16(src_v_cache))
+    return PKV_ERR_ALIGNMENT;
+  if (!device_info(&st)) return st;
+  return cuda_status(launch_kv_compact(dst_k_cache, dst_v_cache, dst_block_tables, dst_num_blocks,
+                                       dst_max_blocks_per_seq, src_k_cache, src_v_cache,
+                                       src_block_tables, context_lens, kept_index_lists, kept_lens,
+                                       max_kept, src_dims->batch, src_dims->num_kv_heads,
+                                       src_dims->head_dim, src_dims->num_blocks,
+                                       src_dims->max_blocks_per_seq, error_word,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int pkv_read_error(int32_t* error_word, int32_t clear, void* stream) {
+  if (error_word == nullptr) return PKV_ERR_NULL_POINTER;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t value = 0;
+  cudaError_t e = cudaMemcpyAsync(&value, error_word, sizeof(value), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear) {
+    e = cudaMemsetAsync(error_word, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e != cudaSuccess) return -(PKV_ERR_CUDA_BASE + (int)e);
+  return value;
+}
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case PKV_ERR_DIMS: return "invalid or unsupported size";
+    case PKV_ERR_BLOCK_SIZE: return "block_size must be 16";
+    case PKV_ERR_HEAD_DIM: return "head_dim must be 64 or 128";
+    case PKV_ERR_GQA: return "num_q_heads must be a multiple of num_kv_heads with G in {1,2,4,6,8}";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_ALIGNMENT: return "a tensor pointer is not 16-byte aligned";
+    case PKV_ERR_ARGUMENT: return "invalid scalar argument";
+    case PKV_ERR_NO_DEVICE: return "no CUDA device";
+    default: break;
+  }
+  if (status >= PKV_ERR_CUDA_BASE) return cudaGetErrorString(static_cast<cudaError_t>(status - PKV_ERR_CUDA_BASE));
+  return "unknown status";
+}
+
+const char* pkv_device_error_string(int code) {
+  switch (code) {
+    case PKV_DEV_OK: return "no device error";
+    case PKV_DEV_BAD_BLOCK_ID: return "block table entry outside the pool";
+    case PKV_DEV_BAD_SLOT: return "slot outside the pool";
+    case PKV_DEV_BAD_KEPT_INDEX: return "kept index outside the context";
+    case PKV_DEV_BAD_CONTEXT_LEN: return "context length outside [0, max_blocks_per_seq*16]";
+    case PKV_DEV_WAIT_TIMEOUT: return "a bounded wait timed out";
+    case PKV_DEV_BAD_SCORE: return "NaN score";
+    default: return "unknown device error";
+  }
+}
+
+}  // extern "C"

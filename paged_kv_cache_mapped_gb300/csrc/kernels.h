@@ -1,0 +1,63 @@
+// kernels.h -- argument records and launchers shared between the C-ABI layer (api.cu) and
+// the kernel translation units.  Internal to the library; the public boundary is pkv.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+// Split-K decode: every consumer warp of the grid is an independent worker that owns a
+// contiguous range of the flattened (sequence, kv head, 16-token unit) list.
+struct DecodeArgs {
+  const __nv_bfloat16* q;        // [B, Hq, D]
+  const __nv_bfloat16* k_cache;  // [NB, Hkv, 16, D]
+  const __nv_bfloat16* v_cache;
+  const int32_t* block_tables;   // [B, MB]
+  const int32_t* context_lens;   // [B]
+  const int32_t* kept;           // [B, Hkv, max_kept] (sparse mode)
+  const int32_t* kept_lens;      // [B]               (sparse mode)
+  __nv_bfloat16* out;            // [B, Hq, D]
+  int32_t* layout;               // [2 + (B+1) + B]: total units, units per warp, unit start, units per kv head
+  float2* part_ml;               // [B*Hq, max_parts] (running max in log2 units, running sum)
+  float* part_o;                 // [B*Hq, max_parts, D] unnormalised partial outputs
+  int32_t* err;                  // device error word or nullptr
+  int B, Hq, Hkv, NB, MB, max_kept, window, max_parts, min_units;
+  float scale_log2;              // scale * log2(e): logits are kept in base-2 units
+  unsigned long long timeout_ns; // bound of every mbarrier wait
+};
+
+constexpr int kDecodeWarps = 4;      // worker warps per CTA
+constexpr int kMinUnitsPerWarp = 16; // lower bound of a worker's range (bounds partial count)
+constexpr int kMergeWarps = 8;
+
+// Dynamic shared memory and kernel handles of one (head_dim, group, sparse) instantiation.
+struct DecodeKernel {
+  const void* split;
+  const void* merge;
+  int head_dim, group;
+  bool sparse;
+};
+
+// Returns nullptr-filled struct (split == nullptr) when the combination is unsupported.
+DecodeKernel decode_kernel(int head_dim, int group, bool sparse);
+size_t decode_smem_bytes(int head_dim, int group, int batch);
+cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, size_t smem,
+                          cudaStream_t stream);
+
+// kv append / compaction / top-k selection.
+cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
+                             const int64_t* slots, int64_t T, int Hkv, int D, int NB,
+                             int32_t* err, cudaStream_t stream);
+cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, int dMB,
+                              const void* sk, const void* sv, const int32_t* sbt,
+                              const int32_t* lens, const int32_t* kept, const int32_t* kept_lens,
+                              int max_kept, int B, int Hkv, int D, int sNB, int sMB,
+                              int32_t* err, cudaStream_t stream);
+cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* scores,
+                               int stride, const int32_t* lens, int B, int Hkv, int n_sink,
+                               int n_recent, int k_top, int32_t* err, cudaStream_t stream);
+
+}  // namespace pkv

@@ -55,3 +55,25 @@ def paged_from_contiguous(k, v, lens, num_blocks, gen, max_blocks=None, fill=Non
 
 def rand_bf16(shape, gen):
     return torch.randn(shape, generator=gen).to(torch.bfloat16)
+
+
+# Tolerance of the floating-point parity gate: bf16 inputs, fp32 accumulation, bf16 output,
+# compared with the fp64 oracle.
+MAX_ABS = 1e-2
+REL_L2 = 2e-3
+
+
+def attn_errors(got: torch.Tensor, ref: np.ndarray):
+    """(max-abs, relative L2) of a bf16 GPU result against the fp64 oracle."""
+    g = got.detach().float().cpu().double().numpy().reshape(ref.shape)
+    diff = g - ref
+    denom = np.linalg.norm(ref)
+    rel = float(np.linalg.norm(diff) / denom) if denom > 0 else float(np.linalg.norm(diff))
+    return float(np.abs(diff).max()) if diff.size else 0.0, rel
+
+
+def assert_attn_close(got: torch.Tensor, ref: np.ndarray, what: str = ""):
+    mx, rel = attn_errors(got, ref)
+    assert np.all(np.isfinite(got.detach().float().cpu().numpy())), f"{what}: non-finite output"
+    assert mx <= MAX_ABS and rel <= REL_L2, f"{what}: max-abs {mx:.3e} rel-L2 {rel:.3e}"
+    return mx, rel

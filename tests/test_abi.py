@@ -1,0 +1,103 @@
+"""The C-ABI library builds, loads and exports every entry point include/pkv.h declares; host
+validation rejects bad arguments before anything touches a device.  No compute calls: these
+run on a machine without a GPU."""
+import ctypes
+import subprocess
+
+import pytest
+
+from paged_kv_cache_mapped_gb300 import _build, _lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return _lib.load()
+
+
+def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
+    return _lib.PkvDims(B, hq, hkv, d, bs, nb, mb)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _lib.header_functions()
+    assert len(declared) == 10
+    nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
+    exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
+    for name in declared:
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    c = _lib.header_constants()
+    assert lib.pkv_status_string(c["PKV_OK"]) == b"ok"
+    for name, val in c.items():
+        if name.startswith("PKV_ERR_") and name != "PKV_ERR_CUDA_BASE":
+            assert lib.pkv_status_string(val) not in (b"ok", b"unknown status"), name
+        if name.startswith("PKV_DEV_") and val != 0:
+            assert lib.pkv_device_error_string(val) != b"unknown device error", name
+
+
+def test_workspace_queries(lib):
+    d = _dims()
+    n = lib.pkv_decode_workspace_bytes(ctypes.byref(d))
+    rows = 4 * 32
+    max_parts = (64 + 15) // 16 + 1
+    assert n >= rows * max_parts * (128 + 2) * 4 and n % 256 == 0
+    s = lib.pkv_sparse_decode_workspace_bytes(ctypes.byref(d), 1540)
+    assert s >= rows * ((97 + 15) // 16 + 1) * 130 * 4
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(bs=32))) == 0
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(d=96))) == 0
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(hq=30))) == 0
+    assert lib.pkv_sparse_decode_workspace_bytes(ctypes.byref(d), 0) == 0
+
+
+def _decode(lib, dims, ptr=0x10000, ws_bytes=1 << 30, ws=0x20000):
+    P = ctypes.c_void_p
+    return lib.pkv_paged_decode_attention(P(ptr), P(ptr), P(ptr), P(ptr), P(ptr), P(ptr),
+                                          ctypes.c_float(0.1), 0, P(ws), ws_bytes,
+                                          ctypes.byref(dims), None, None)
+
+
+def test_host_validation_codes(lib):
+    c = _lib.header_constants()
+    P = ctypes.c_void_p
+    assert lib.pkv_paged_decode_attention(None, None, None, None, None, None, ctypes.c_float(1.0), 0,
+                                          None, 0, None, None, None) == c["PKV_ERR_NULL_POINTER"]
+    assert _decode(lib, _dims(bs=8)) == c["PKV_ERR_BLOCK_SIZE"]
+    assert _decode(lib, _dims(d=80)) == c["PKV_ERR_HEAD_DIM"]
+    assert _decode(lib, _dims(hq=12, hkv=8)) == c["PKV_ERR_GQA"]
+    assert _decode(lib, _dims(hq=24, hkv=8)) == c["PKV_ERR_GQA"]      # G = 3 is not built
+    assert _decode(lib, _dims(B=-1)) == c["PKV_ERR_DIMS"]
+    assert _decode(lib, _dims(), ptr=0x10004) == c["PKV_ERR_ALIGNMENT"]
+    assert _decode(lib, _dims(), ws_bytes=16) == c["PKV_ERR_WORKSPACE"]
+    assert _decode(lib, _dims(), ws=0) == c["PKV_ERR_WORKSPACE"]
+    assert _decode(lib, _dims(B=0)) == c["PKV_OK"]                    # empty batch: nothing to do
+    # append
+    assert lib.pkv_kv_append(P(0x1000), P(0x1000), P(0x1000), P(0x1000), P(0x1000), -1,
+                             ctypes.byref(_dims()), None, None) == c["PKV_ERR_DIMS"]
+    assert lib.pkv_kv_append(P(0x1000), P(0x1000), P(0x1000), P(0x1000), P(0x1000), 0,
+                             ctypes.byref(_dims()), None, None) == c["PKV_OK"]
+    assert lib.pkv_kv_append(None, P(0x1000), P(0x1000), P(0x1000), P(0x1000), 4,
+                             ctypes.byref(_dims()), None, None) == c["PKV_ERR_NULL_POINTER"]
+    # selection
+    assert lib.pkv_kv_select_topk(P(0x1000), P(0x1000), P(0x1000), 100, P(0x1000), -1, 4, 4,
+                                  ctypes.byref(_dims()), None, None) == c["PKV_ERR_ARGUMENT"]
+    # sparse decode with no kept lists
+    assert lib.pkv_sparse_decode_attention(P(0x10000), P(0x10000), P(0x10000), P(0x10000),
+                                           P(0x10000), P(0x10000), None, None, 16,
+                                           ctypes.c_float(0.1), P(0x20000), 1 << 30,
+                                           ctypes.byref(_dims()), None, None) == c["PKV_ERR_NULL_POINTER"]
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+
+    import paged_kv_cache_mapped_gb300 as pkv
+    q = torch.zeros(2, 8, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(4, 8, 16, 64, dtype=torch.bfloat16)
+    bt = torch.zeros(2, 2, dtype=torch.int32)
+    lens = torch.ones(2, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkv.paged_decode_attention(q, kc, kc, bt, lens, 0.125)

@@ -1,0 +1,193 @@
+"""GPU parity of kv_append and paged_decode_attention (through the C ABI) against the fp64
+oracle.  Small cases compare every output element; the full-size workloads run in the launch
+configuration the bench times and compare a deterministic sample of rows the oracle computes
+one by one.  Tolerance: max-abs 1e-2 and relative L2 2e-3 (bf16 in, fp32 accumulate, bf16 out);
+append is bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_mapped_gb300 as pkv
+from paged_kv_cache_mapped_gb300 import inputs as W
+from helpers import assert_attn_close, bits, paged_from_contiguous, rand_bf16
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _oracle_rows(case, rows, kc_bits=None, vc_bits=None, window=0):
+    return oracle.paged_decode(bits(case["q"]), bits(case["k_cache"]) if kc_bits is None else kc_bits,
+                               bits(case["v_cache"]) if vc_bits is None else vc_bits,
+                               case["block_tables"].cpu().numpy(), case["context_lens"].cpu().numpy(),
+                               case["scale"], window, rows=rows)
+
+
+def _run(case, window=0, err=None):
+    out = pkv.paged_decode_attention(case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
+                                     case["context_lens"], case["scale"], window, error_word=err)
+    torch.cuda.synchronize()
+    return out
+
+
+def _small_case(lens, hq, hkv, d, seed, fill=None, nb_extra=5):
+    g = torch.Generator().manual_seed(seed)
+    B = len(lens)
+    lmax = max(max(lens), 1)
+    k = rand_bf16((B, lmax, hkv, d), g)
+    v = rand_bf16((B, lmax, hkv, d), g)
+    q = rand_bf16((B, hq, d), g)
+    nb = sum((L + 15) // 16 for L in lens) + nb_extra
+    kc, vc, bt = paged_from_contiguous(k, v, lens, nb, g, fill=fill)
+    return {"q": q.to(DEV), "k_cache": kc.to(DEV), "v_cache": vc.to(DEV), "block_tables": bt.to(DEV),
+            "context_lens": torch.tensor(lens, dtype=torch.int32, device=DEV), "scale": d ** -0.5}
+
+
+@pytest.mark.parametrize("window", [0, 1, 16, 50, 100, 300])
+def test_tiny_workload_every_element(window):
+    wl = W.WORKLOADS["tiny"]
+    case = W.make_layer(wl, device=DEV)
+    err = pkv.new_error_word(DEV)
+    out = _run(case, window, err)
+    assert pkv.read_error(err) == 0
+    ref = _oracle_rows(case, None, window=window)
+    assert_attn_close(out, ref, f"tiny window={window}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 6, 8])
+def test_ragged_lengths_all_groups(d, group):
+    hkv = 2
+    lens = [1, 15, 16, 17, 33, 100, 257, 1000, 2049]
+    case = _small_case(lens, hq=hkv * group, hkv=hkv, d=d, seed=d + group)
+    for window in (0, 7, 40):
+        out = _run(case, window)
+        assert_attn_close(out, _oracle_rows(case, None, window=window), f"d={d} G={group} w={window}")
+
+
+def test_unused_slots_hold_nan():
+    case = _small_case([5, 17, 31, 64, 200], hq=8, hkv=2, d=128, seed=3, fill=float("nan"))
+    for window in (0, 9):
+        out = _run(case, window)
+        assert_attn_close(out, _oracle_rows(case, None, window=window), f"nan poison w={window}")
+
+
+def test_empty_sequences_give_zero_rows():
+    case = _small_case([0, 40, 0, 3], hq=4, hkv=2, d=64, seed=4)
+    out = _run(case)
+    assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
+    ref = _oracle_rows(case, None)
+    assert_attn_close(out, ref, "empty rows")
+
+
+def test_single_token_exact_and_equal_rows():
+    # one attended token: the output is that token's V row exactly (bf16 -> fp32 -> bf16)
+    case = _small_case([1, 1, 1], hq=8, hkv=2, d=128, seed=5)
+    out = _run(case)
+    bt = case["block_tables"].cpu()
+    for b in range(3):
+        blk = int(bt[b, 0])
+        for h in range(8):
+            assert torch.equal(out[b, h].cpu(), case["v_cache"][blk, h // 4, 0].cpu())
+    # window 1 over long contexts: the last token's V exactly
+    case = _small_case([300, 513], hq=4, hkv=4, d=64, seed=6)
+    out = _run(case, window=1)
+    bt = case["block_tables"].cpu()
+    for b, L in enumerate([300, 513]):
+        blk = int(bt[b, (L - 1) // 16])
+        for h in range(4):
+            assert torch.equal(out[b, h].cpu(), case["v_cache"][blk, h, (L - 1) % 16].cpu())
+
+
+def test_deterministic_and_workspace_reuse():
+    case = _small_case([700, 33, 1500], hq=8, hkv=2, d=128, seed=7)
+    ws = torch.empty(pkv.decode_workspace_bytes(3, 8, 2, 128, case["k_cache"].shape[0],
+                                                case["block_tables"].shape[1]),
+                     dtype=torch.uint8, device=DEV)
+    a = pkv.paged_decode_attention(case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
+                                   case["context_lens"], case["scale"], workspace=ws)
+    b = pkv.paged_decode_attention(case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
+                                   case["context_lens"], case["scale"], workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_bad_block_id_sets_error_word():
+    case = _small_case([100, 60], hq=4, hkv=2, d=128, seed=8)
+    case["block_tables"][1, 2] = case["k_cache"].shape[0] + 5
+    err = pkv.new_error_word(DEV)
+    out = _run(case, err=err)
+    assert pkv.read_error(err, clear=True) == pkv.header_constants()["PKV_DEV_BAD_BLOCK_ID"]
+    assert torch.isfinite(out.float()).all()
+    # the untouched sequence is still right
+    ref = _oracle_rows(case, list(range(0, 4)))
+    assert_attn_close(out[0], ref, "valid sequence next to a bad one")
+    assert pkv.read_error(err) == 0
+
+
+def test_bad_context_len_sets_error_word():
+    case = _small_case([100, 60], hq=4, hkv=2, d=64, seed=9)
+    case["context_lens"][1] = case["block_tables"].shape[1] * 16 + 1
+    err = pkv.new_error_word(DEV)
+    out = _run(case, err=err)
+    assert pkv.read_error(err) == pkv.header_constants()["PKV_DEV_BAD_CONTEXT_LEN"]
+    assert torch.count_nonzero(out[1]) == 0
+
+
+def _sample_rows(B, hq, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = {0, B * hq - 1}
+    rows |= {b * hq for b in range(B)}
+    rows |= set(rng.choice(B * hq, size=min(n, B * hq), replace=False).tolist())
+    return sorted(rows)
+
+
+def test_llama8b_full_size_append_then_decode():
+    wl = W.WORKLOADS["llama8b"]
+    case = W.make_layer(wl, device=DEV)
+    kc0, vc0 = bits(case["k_cache"]), bits(case["v_cache"])
+    err = pkv.new_error_word(DEV)
+    pkv.kv_append(case["k_cache"], case["v_cache"], case["k_new"], case["v_new"], case["slot_mapping"],
+                  error_word=err)
+    out = _run(case, err=err)
+    assert pkv.read_error(err) == 0
+    okc, ovc = oracle.kv_append(kc0, vc0, bits(case["k_new"]), bits(case["v_new"]),
+                                case["slot_mapping"].cpu().numpy())
+    assert np.array_equal(bits(case["k_cache"]), okc)
+    assert np.array_equal(bits(case["v_cache"]), ovc)
+    rows = _sample_rows(wl.batch, wl.num_q_heads, 64, 2)
+    ref = _oracle_rows(case, rows, okc, ovc)
+    got = out.view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)]
+    assert_attn_close(got, ref, "llama8b sampled rows")
+
+
+@pytest.mark.parametrize("layer", [0, 27])
+def test_qwen_layers_full_size(layer):
+    wl = W.WORKLOADS["qwen1p5b"]
+    case = W.make_layer(wl, layer=layer, device=DEV)
+    kc0, vc0 = bits(case["k_cache"]), bits(case["v_cache"])
+    pkv.kv_append(case["k_cache"], case["v_cache"], case["k_new"], case["v_new"], case["slot_mapping"])
+    out = _run(case)
+    okc, ovc = oracle.kv_append(kc0, vc0, bits(case["k_new"]), bits(case["v_new"]),
+                                case["slot_mapping"].cpu().numpy())
+    assert np.array_equal(bits(case["k_cache"]), okc)
+    rows = _sample_rows(wl.batch, wl.num_q_heads, 96, 3 + layer)
+    ref = _oracle_rows(case, rows, okc, ovc)
+    got = out.view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)]
+    assert_attn_close(got, ref, f"qwen layer {layer}")
+
+
+def test_long128k_full_size_sampled():
+    wl = W.WORKLOADS["long128k"]
+    case = W.make_layer(wl, device=DEV, device_rng=True)
+    err = pkv.new_error_word(DEV)
+    out = _run(case, err=err)
+    assert pkv.read_error(err) == 0
+    rows = _sample_rows(wl.batch, wl.num_q_heads, 12, 4)
+    ref = _oracle_rows(case, rows)
+    got = out.view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)]
+    assert_attn_close(got, ref, "long128k sampled rows")
+    # a sliding window over the same long context
+    out_w = _run(case, window=4096)
+    ref_w = _oracle_rows(case, rows, window=4096)
+    assert_attn_close(out_w.view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)], ref_w, "long128k w=4096")

@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn tokens/s and KV-read HBM GB/s (% of GB300 peak), 1 GPU"
 WORKLOAD = "llama8b"
-ROTATE = 4
+ROTATE = 4  # pool copies the timed steps rotate over (overridden by --rotate)
 
 
 def _peaks():
@@ -145,6 +145,8 @@ def run_ours(args):
     B, hq, hkv, d = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
 
     # pool copy 0 from the CPU generator (also feeds the CPU baseline), 1..3 drawn on device
+    global ROTATE
+    ROTATE = args.rotate
     host0 = W.make_layer(wl, layer=0, device="cpu")
     copies = [{k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in host0.items()}]
     for r in range(1, ROTATE):
@@ -175,9 +177,19 @@ def run_ours(args):
     ev1 = torch.cuda.Event(enable_timing=True)
     dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    _barrier(dist)
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        # same load for ~0.8 s before the timed region, so nvidia-smi (200 ms period) has
+        # started sampling when the timed steps run
+        t_end = time.perf_counter() + args.preload_s
+        i = 0
+        while time.perf_counter() < t_end:
+            step(copies[i % ROTATE])
+            i += 1
+            if i % 256 == 0:
+                torch.cuda.synchronize(dev)
+        _barrier(dist)
+        torch.cuda.synchronize(dev)
+        host_t0 = time.perf_counter()
         ev0.record(stream)
         for i in range(args.steps):
             c = copies[i % ROTATE]
@@ -189,6 +201,7 @@ def run_ours(args):
                                        error_word=err, stream=stream)
             dec[i][1].record(stream)
         ev1.record(stream)
+        host_ms = (time.perf_counter() - host_t0) * 1e3 / args.steps
         torch.cuda.synchronize(dev)
     _barrier(dist)
     ms = ev0.elapsed_time(ev1) / args.steps
@@ -198,7 +211,7 @@ def run_ours(args):
         raise RuntimeError("device error during the timed region")
 
     # end to end through the public API: pinned host inputs -> device, step, result -> host
-    e2e = run_e2e(pkv, copies, host0, dev, stream, ws, args)
+    e2e = run_e2e(pkv, copies, host0, dev, stream, ws, args) if args.e2e else None
 
     hbm, peak_kind = _peaks()
     bytes_dec = decode_bytes(lens, B, hq, hkv, d)
@@ -240,10 +253,11 @@ def run_ours(args):
             "launch_ms": round(dec_ms, 5),
         },
         "gpu_launches": 3 * args.steps,
-        "clocks": clk.summary(),
+        "host_launch_ms_per_step": round(host_ms, 5),
+        "clocks": dict(clk.summary(), window=f"last {args.preload_s} s of identical warm-up load + the timed region"),
         "e2e": e2e,
     }
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.baseline:
         line["cpu_baseline"] = cpu_baseline(host0, wl, lens)
     if rank == 0 and args.secondary and world == 1:
         line["secondary"] = run_secondary(pkv, W, dev, stream, args)
@@ -401,10 +415,19 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false",
+                    help="skip the other workloads' measurements")
+    ap.add_argument("--no-baseline", dest="baseline", action="store_false",
+                    help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false",
+                    help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--preload-s", type=float, default=0.8,
+                    help="seconds of untimed identical load before the timed region (clock sampling)")
+    ap.add_argument("--rotate", type=int, default=ROTATE,
+                    help="independent pool copies the timed steps rotate over")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

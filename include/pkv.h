@@ -208,6 +208,35 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
                    void* stream);
 
 /*
+ * pkv_paged_decode_attention_fixed_scratch -- pkv_paged_decode_attention for callers that
+ * cannot allocate device memory.  It has no counterpart on the pages: it exists only for
+ * callers with no device allocator at hand (for example a plain C program or plugin that
+ * links just this library) or whose host runtime owns the device heap and forbids
+ * cudaMalloc (which can also synchronise the device at a moment the caller cannot afford).
+ * It takes the same inputs and output as pkv_paged_decode_attention minus the workspace:
+ * the split-K scratch is a static device array of PKV_FIXED_SCRATCH_BYTES (16 MiB) inside
+ * the library, which every GPU that loads the library keeps until the process exits.  The
+ * call itself allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *   - Shapes whose scratch need, pkv_decode_workspace_bytes(dims), exceeds
+ *     PKV_FIXED_SCRATCH_BYTES return PKV_ERR_WORKSPACE and enqueue nothing.  At d=128 the
+ *     need is about 520 bytes x B*Hq x (ceil(MB/16) + 1); batch 32 with 32 query heads fits
+ *     up to MB = 480 blocks (7,680 tokens per sequence).
+ *   - The first call on a device looks up the array's device address on that device (with
+ *     it current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, whose contents persist between calls
+ *     (nothing in it needs to start at zero).  Calls whose kernels overlap on the GPU --
+ *     different streams without ordering, or several host threads -- race on it and give
+ *     wrong results: serialise them.
+ *   - Results are identical to pkv_paged_decode_attention with the same arguments.
+ */
+#define PKV_FIXED_SCRATCH_BYTES (16 * 1024 * 1024)
+int pkv_paged_decode_attention_fixed_scratch(void* out, const void* q, const void* k_cache,
+                                             const void* v_cache, const int32_t* block_tables,
+                                             const int32_t* context_lens, float scale,
+                                             int32_t window, const pkv_dims* dims,
+                                             int32_t* error_word, void* stream);
+
+/*
  * pkv_read_error -- synchronise `stream`, then return the device error word's value
  * (PKV_DEV_*), or a negative host status if it cannot be read.  If `clear` is non-zero
  * the word is reset to 0 afterwards.  Diagnostic; not for the hot loop.

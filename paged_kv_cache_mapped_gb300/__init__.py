@@ -19,6 +19,7 @@ __all__ = [
     "BLOCK_SIZE", "PkvError", "kv_append", "decode_workspace_bytes", "paged_decode_attention",
     "sparse_decode_workspace_bytes", "sparse_decode_attention", "kv_select_topk", "kv_compact",
     "read_error", "new_error_word", "header_constants", "header_functions",
+    "paged_decode_attention_fixed_scratch",
 ]
 
 BLOCK_SIZE = 16
@@ -147,6 +148,28 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
         _ptr(error_word), _stream(stream, dev)))
+    return out
+
+
+def paged_decode_attention_fixed_scratch(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                         window=0, *, out=None, error_word=None, stream=None):
+    """paged_decode_attention without a workspace, for callers that cannot allocate device
+    memory: the library's fixed static scratch (PKV_FIXED_SCRATCH_BYTES) holds the split-K
+    partials.  Shapes that need more scratch are refused.  Calls that overlap on the GPU
+    share that scratch and race; issue them one after another.  (Only `out`, when not
+    given, is allocated here by torch; pass it to allocate nothing.)"""
+    dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    check("pkv_paged_decode_attention_fixed_scratch",
+          load().pkv_paged_decode_attention_fixed_scratch(
+              _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+              _ptr(context_lens), float(scale), int(window), ctypes.byref(dims), _ptr(error_word),
+              _stream(stream, dev)))
     return out
 
 

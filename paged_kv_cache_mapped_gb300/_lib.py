@@ -39,8 +39,8 @@ def header_constants() -> dict:
     """#define NAME value pairs of include/pkv.h (status and device-error codes)."""
     out = {}
     with open(HEADER) as f:
-        for m in re.finditer(r"^#define\s+(PKV_\w+)\s+\(?(-?\d+)\)?", f.read(), re.M):
-            out[m.group(1)] = int(m.group(2))
+        for m in re.finditer(r"^#define\s+(PKV_\w+)\s+([-+*() 0-9]+?)\s*(?:/\*.*)?$", f.read(), re.M):
+            out[m.group(1)] = int(eval(m.group(2), {"__builtins__": {}}, {}))  # integer literal arithmetic only
     return out
 
 
@@ -72,6 +72,7 @@ def load():
             "pkv_sparse_decode_attention": (I32, [P, P, P, P, P, P, P, P, I32, F32, P, SZ, D, P, P]),
             "pkv_kv_select_topk": (I32, [P, P, P, I32, P, I32, I32, I32, D, P, P]),
             "pkv_kv_compact": (I32, [P, P, P, I32, I32, P, P, P, P, P, P, I32, D, P, P]),
+            "pkv_paged_decode_attention_fixed_scratch": (I32, [P, P, P, P, P, P, F32, I32, D, P, P]),
             "pkv_read_error": (I32, [P, I32, P]),
             "pkv_status_string": (ctypes.c_char_p, [I32]),
             "pkv_device_error_string": (ctypes.c_char_p, [I32]),

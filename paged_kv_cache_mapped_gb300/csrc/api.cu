@@ -107,6 +107,8 @@ WorkspacePlan plan_workspace(const pkv_dims* d, int max_units_per_seq) {
   return p;
 }
 
+}  // namespace
+
 int decode_common(void* out, const void* q, const void* k_cache, const void* v_cache,
                   const int32_t* block_tables, const int32_t* context_lens, const int32_t* kept,
                   const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
@@ -170,7 +172,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   return cuda_status(launch_decode(k, a, grid, smem, static_cast<cudaStream_t>(stream)));
 }
 
-}  // namespace
+
 }  // namespace pkv
 
 using namespace pkv;

@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "pkv.h"
+
 namespace pkv {
 
 // Split-K decode: every consumer warp of the grid is an independent worker that owns a
@@ -59,5 +61,13 @@ cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, i
 cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* scores,
                                int stride, const int32_t* lens, int B, int Hkv, int n_sink,
                                int n_recent, int k_top, int32_t* err, cudaStream_t stream);
+
+// Validates a paged (sparse == false) or sparse decode call, sizes its partition and
+// launches it with `workspace` as scratch.  Defined in api.cu; returns a PKV status.
+int decode_common(void* out, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, const int32_t* kept,
+                  const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
+                  void* workspace, size_t workspace_bytes, const struct pkv_dims* dims, int32_t* err,
+                  void* stream, bool sparse);
 
 }  // namespace pkv

@@ -1,0 +1,87 @@
+"""The allocation-free decode entry point (pkv_paged_decode_attention_fixed_scratch).
+
+It serves callers that cannot allocate device memory -- a plain C program or plugin with no
+device allocator of its own, or a host runtime that owns the device heap and forbids
+cudaMalloc -- by keeping its split-K scratch in a fixed static device array inside the
+library.  These tests call it through the C ABI (ctypes on libpkv.so, no Python helper in
+between) twice in a row and compare both results with the workspace-taking entry point,
+within the same tolerance the other attention tests use.  They also check that a shape too
+large for the fixed scratch is refused.  This file is collected last, and each test builds
+its own inputs, so it passes alone in a fresh process as well as after the other tests.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import paged_kv_cache_mapped_gb300 as pkv
+from paged_kv_cache_mapped_gb300 import _lib
+from paged_kv_cache_mapped_gb300 import inputs as W
+from helpers import MAX_ABS, REL_L2, attn_errors
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+C = _lib.header_constants()
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dims(case):
+    q, kc, bt = case["q"], case["k_cache"], case["block_tables"]
+    return _lib.PkvDims(q.shape[0], q.shape[1], kc.shape[1], kc.shape[3], 16, kc.shape[0], bt.shape[1])
+
+
+def _fixed(case, out, window=0, err=None):
+    stream = ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)
+    return _lib.load().pkv_paged_decode_attention_fixed_scratch(
+        _p(out), _p(case["q"]), _p(case["k_cache"]), _p(case["v_cache"]), _p(case["block_tables"]),
+        _p(case["context_lens"]), ctypes.c_float(case["scale"]), window, ctypes.byref(_dims(case)),
+        None if err is None else _p(err), stream)
+
+
+def _with_workspace(case, window=0):
+    dims = _dims(case)
+    lib = _lib.load()
+    ws = torch.empty(lib.pkv_decode_workspace_bytes(ctypes.byref(dims)), dtype=torch.uint8, device=DEV)
+    out = torch.empty_like(case["q"])
+    stream = ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)
+    st = lib.pkv_paged_decode_attention(
+        _p(out), _p(case["q"]), _p(case["k_cache"]), _p(case["v_cache"]), _p(case["block_tables"]),
+        _p(case["context_lens"]), ctypes.c_float(case["scale"]), window, _p(ws), ws.numel(),
+        ctypes.byref(dims), None, stream)
+    assert st == C["PKV_OK"]
+    return out
+
+
+def _compare(got, ref, what):
+    mx, rel = attn_errors(got, ref.double().cpu().numpy())
+    assert torch.isfinite(got.float()).all(), what
+    assert mx <= MAX_ABS and rel <= REL_L2, f"{what}: max-abs {mx:.3e} rel-L2 {rel:.3e}"
+
+
+@pytest.mark.parametrize("name,window", [("tiny", 0), ("tiny", 50), ("llama8b", 0)])
+def test_fixed_scratch_matches_workspace_entry_point_twice(name, window):
+    case = W.make_layer(W.WORKLOADS[name], device=DEV, device_rng=(name != "tiny"))
+    ref = _with_workspace(case, window).float()
+    err = pkv.new_error_word(DEV)
+    for call in range(2):
+        out = torch.full_like(case["q"], float("nan"))
+        assert _fixed(case, out, window, err) == C["PKV_OK"]
+        torch.cuda.synchronize()
+        _compare(out, ref, f"{name} window={window} call {call}")
+    assert pkv.read_error(err) == 0
+
+
+def test_fixed_scratch_refuses_oversized_shapes():
+    # batch 4 x 32 heads over 131072-token contexts needs ~34 MB of scratch: refused, nothing run
+    wl = W.WORKLOADS["long128k"]
+    lens = torch.tensor([64] * 4, dtype=torch.int32)
+    case = W.make_layer(wl, device=DEV, lengths=lens, num_blocks=32, max_blocks=8192)
+    need = _lib.load().pkv_decode_workspace_bytes(ctypes.byref(_dims(case)))
+    assert need > C["PKV_FIXED_SCRATCH_BYTES"]
+    out = torch.zeros_like(case["q"])
+    assert _fixed(case, out) == C["PKV_ERR_WORKSPACE"]
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0

@@ -5,7 +5,9 @@ layer -- batch 32, 32 query / 8 kv heads (GQA 4), head_dim 128, block 16, contex
 U[3500, 4500] + 1, physical blocks shuffled over a shared pool.  One step = kv_append of the
 new token of every sequence + paged_decode_attention over all cached tokens.  Inputs are
 resident in HBM and rotate over 4 independent pool copies (2.3 GB in total, far above the
-129 MB L2) so no step reads K/V that a previous step left in L2.
+129 MB L2) so no step reads K/V that a previous step left in L2.  The step runs as one call of
+paged_decode_attention_append (the append fused into the decode kernel; tests check it
+against kv_append followed by paged decode).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-secondary]
 
@@ -161,11 +163,9 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(c):
-        pkv.kv_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["slot_mapping"],
-                      error_word=err, stream=stream)
-        pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
-                                   c["context_lens"], c["scale"], out=out, workspace=ws,
-                                   error_word=err, stream=stream)
+        pkv.paged_decode_attention_append(c["q"], c["k_cache"], c["v_cache"], c["k_new"], c["v_new"],
+                                          c["block_tables"], c["context_lens"], c["scale"], out=out,
+                                          workspace=ws, error_word=err, stream=stream)
 
     for i in range(args.warmup):
         step(copies[i % ROTATE])
@@ -192,13 +192,8 @@ def run_ours(args):
         host_t0 = time.perf_counter()
         ev0.record(stream)
         for i in range(args.steps):
-            c = copies[i % ROTATE]
-            pkv.kv_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["slot_mapping"],
-                          error_word=err, stream=stream)
             dec[i][0].record(stream)
-            pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
-                                       c["context_lens"], c["scale"], out=out, workspace=ws,
-                                       error_word=err, stream=stream)
+            step(copies[i % ROTATE])
             dec[i][1].record(stream)
         ev1.record(stream)
         host_ms = (time.perf_counter() - host_t0) * 1e3 / args.steps
@@ -214,7 +209,8 @@ def run_ours(args):
     e2e = run_e2e(pkv, copies, host0, dev, stream, ws, args) if args.e2e else None
 
     hbm, peak_kind = _peaks()
-    bytes_dec = decode_bytes(lens, B, hq, hkv, d)
+    # KV read + q/out + table entries + the append (new K/V rows read and written)
+    bytes_dec = decode_bytes(lens, B, hq, hkv, d) + 2 * (B * hkv * d * 2 * 2)
     achieved = bytes_dec / (dec_ms * 1e-3) / 1e9
     tokens_per_s = world * B / (ms * 1e-3)
     line = {
@@ -232,7 +228,7 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) bf16 K/V/q; shuffled block tables)",
         "config": {
             "workload": "llama8b decode layer: B=32, Hq=32, Hkv=8, d=128, block 16, "
-                        "L=U[3500,4500]+1, kv_append + paged decode",
+                        "L=U[3500,4500]+1, append of the new token + paged decode",
             "batch": B, "context_tokens": int(lens.sum()), "num_q_heads": hq, "num_kv_heads": hkv,
             "head_dim": d, "block_size": 16,
             "l2": f"inputs larger than L2: {ROTATE} rotating pool copies "
@@ -242,7 +238,7 @@ def run_ours(args):
         "kv_read_gbs": round(kv_bytes(lens, hkv, d) / (dec_ms * 1e-3) / 1e9, 1),
         "roofline": {
             "bound": "hbm",
-            "kernel": "paged_decode_attention (split + merge launches)",
+            "kernel": "paged_decode_attention_append (split kernel with the fused append + merge kernel)",
             "achieved": round(achieved, 1),
             "peak": hbm,
             "peak_kind": peak_kind,
@@ -252,7 +248,7 @@ def run_ours(args):
             "algorithmic_bytes_per_launch": bytes_dec,
             "launch_ms": round(dec_ms, 5),
         },
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "host_launch_ms_per_step": round(host_ms, 5),
         "clocks": dict(clk.summary(), window=f"last {args.preload_s} s of identical warm-up load + the timed region"),
         "e2e": e2e,
@@ -270,7 +266,7 @@ def run_ours(args):
 def run_e2e(pkv, copies, host0, dev, stream, ws, args):
     """Same step through the public API with the step's inputs copied from pinned host
     memory and the result read back, inside the timed region."""
-    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    names = ("q", "k_new", "v_new", "block_tables", "context_lens")
     hosts = [{n: host0[n].pin_memory() for n in names}]
     for c in copies[1:]:
         hosts.append({n: c[n].cpu().pin_memory() for n in names})
@@ -284,11 +280,9 @@ def run_e2e(pkv, copies, host0, dev, stream, ws, args):
         h, c, di = hosts[i % ROTATE], copies[i % ROTATE], dev_in[i % 2]
         for n in names:
             di[n].copy_(h[n], non_blocking=True)
-        pkv.kv_append(c["k_cache"], c["v_cache"], di["k_new"], di["v_new"], di["slot_mapping"],
-                      stream=stream)
-        pkv.paged_decode_attention(di["q"], c["k_cache"], c["v_cache"], di["block_tables"],
-                                   di["context_lens"], c["scale"], out=out, workspace=ws,
-                                   stream=stream)
+        pkv.paged_decode_attention_append(di["q"], c["k_cache"], c["v_cache"], di["k_new"], di["v_new"],
+                                          di["block_tables"], di["context_lens"], c["scale"], out=out,
+                                          workspace=ws, stream=stream)
         out_h.copy_(out, non_blocking=True)
 
     for i in range(args.warmup):

@@ -53,7 +53,7 @@ extern "C" {
 #define PKV_ERR_DIMS (-2)           /* a size is negative/zero where it must be positive */
 #define PKV_ERR_BLOCK_SIZE (-3)     /* block_size != 16 */
 #define PKV_ERR_HEAD_DIM (-4)       /* head_dim not in {64, 128} */
-#define PKV_ERR_GQA (-5)            /* num_q_heads % num_kv_heads != 0 or unsupported G */
+#define PKV_ERR_GQA (-5)            /* num_q_heads % num_kv_heads != 0 or G = Hq/Hkv > 8 */
 #define PKV_ERR_WORKSPACE (-6)      /* workspace NULL or smaller than the *_workspace_bytes query */
 #define PKV_ERR_ALIGNMENT (-7)      /* a tensor pointer is not 16-byte aligned */
 #define PKV_ERR_ARGUMENT (-8)       /* any other invalid scalar argument */
@@ -129,13 +129,33 @@ size_t pkv_decode_workspace_bytes(const pkv_dims* dims);
  *   window         : > 0 attends tokens [max(0, L_b - window), L_b); <= 0 attends all.
  *   workspace      : >= pkv_decode_workspace_bytes(dims) bytes, 16-byte aligned.
  *   error_word     : optional; PKV_DEV_BAD_BLOCK_ID / _BAD_CONTEXT_LEN / _WAIT_TIMEOUT.
- * Supported: d in {64, 128}; G in {1, 2, 4, 6, 8}.
+ * Supported: d in {64, 128}; G = Hq / Hkv in 1..8.
  */
 int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
                                const void* v_cache, const int32_t* block_tables,
                                const int32_t* context_lens, float scale, int32_t window,
                                void* workspace, size_t workspace_bytes, const pkv_dims* dims,
                                int32_t* error_word, void* stream);
+
+/*
+ * pkv_paged_decode_attention_append -- one decode step's KV append and attention in one
+ * kernel: the same result as pkv_kv_append of this step's token followed by
+ * pkv_paged_decode_attention, for the usual decode layout in which the new token of
+ * sequence b is its logical position L_b - 1 (L_b = context_lens[b] counts it).  The step's
+ * K/V rows are written into the pool at that position (block block_tables[b][(L_b-1)/16],
+ * offset (L_b-1)%16, every kv head) and used for it directly, which saves the separate
+ * append launch and the re-read of the freshly written rows ("KV Cache primer",
+ * cf-1.com/news/5988169, section 2.2: compute the new token's K,V, append, attend).
+ *   k_cache, v_cache : [NB, Hkv, 16, d] bf16, read and updated in place.
+ *   k_new, v_new     : [B, Hkv, d] bf16, the step's new rows (one token per sequence).
+ *   other arguments  : as pkv_paged_decode_attention; sequences with L_b == 0 append nothing.
+ */
+int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                      const void* k_new, const void* v_new,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      float scale, int32_t window, void* workspace,
+                                      size_t workspace_bytes, const pkv_dims* dims,
+                                      int32_t* error_word, void* stream);
 
 /*
  * pkv_sparse_decode_workspace_bytes -- workspace for pkv_sparse_decode_attention with

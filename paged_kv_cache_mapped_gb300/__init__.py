@@ -19,7 +19,7 @@ __all__ = [
     "BLOCK_SIZE", "PkvError", "kv_append", "decode_workspace_bytes", "paged_decode_attention",
     "sparse_decode_workspace_bytes", "sparse_decode_attention", "kv_select_topk", "kv_compact",
     "read_error", "new_error_word", "header_constants", "header_functions",
-    "paged_decode_attention_fixed_scratch",
+    "paged_decode_attention_fixed_scratch", "paged_decode_attention_append",
 ]
 
 BLOCK_SIZE = 16
@@ -148,6 +148,26 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
         _ptr(error_word), _stream(stream, dev)))
+    return out
+
+
+def paged_decode_attention_append(q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                                  scale, window=0, *, out=None, workspace=None, error_word=None,
+                                  stream=None):
+    """One decode step: write k_new/v_new [B, Hkv, d] at each sequence's last position
+    (context_lens[b] - 1, through the block table) and attend, in one kernel.  Same result as
+    kv_append followed by paged_decode_attention for that slot layout."""
+    dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    _need(k_new, "k_new", torch.bfloat16, 3, dev)
+    _need(v_new, "v_new", torch.bfloat16, 3, dev)
+    if k_new.shape != (dims.batch, dims.num_kv_heads, dims.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
+    nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
+    out, workspace = _out_ws(q, out, workspace, nbytes)
+    check("pkv_paged_decode_attention_append", load().pkv_paged_decode_attention_append(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+        _ptr(block_tables), _ptr(context_lens), float(scale), int(window), _ptr(workspace),
+        workspace.numel(), ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
     return out
 
 

@@ -1,6 +1,8 @@
 // api.cu -- the extern "C" boundary declared in include/pkv.h: argument validation on the
 // host, per-device one-time set-up, workspace sizing and kernel launches on the caller's
 // stream.  Allocates nothing and never synchronises (except pkv_read_error).
+#include <cudaTypedefs.h>
+
 #include <cstring>
 #include <mutex>
 
@@ -14,8 +16,8 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxBatch = 4096;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per mbarrier wait
 constexpr int kNumHeadDims = 2;
-constexpr int kGroups[] = {1, 2, 4, 6, 8};
-constexpr int kNumGroups = 5;
+constexpr int kGroups[] = {1};  // every group size shares one kernel per (head_dim, mode)
+constexpr int kNumGroups = 1;
 
 struct DeviceInfo {
   bool ready = false;
@@ -70,6 +72,37 @@ const DeviceInfo* device_info(int* status) {
   return &info;
 }
 
+// cuTensorMapEncodeTiled, resolved once through the runtime (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// A pool [NB, Hkv, 16, D] viewed as a 2-D bf16 tensor of NB*Hkv*16 rows of D elements, read
+// in boxes of 64 columns (128 bytes) x 16 rows with the 128-byte swizzle.
+int encode_pool_map(CUtensorMap* map, const void* base, long long rows, int head_dim) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return PKV_ERR_NO_DEVICE;
+  const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_ARGUMENT;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_dims(const pkv_dims* d, bool need_q_heads) {
@@ -113,7 +146,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
                   const int32_t* block_tables, const int32_t* context_lens, const int32_t* kept,
                   const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
                   void* workspace, size_t workspace_bytes, const pkv_dims* dims, int32_t* err,
-                  void* stream, bool sparse) {
+                  void* stream, bool sparse, const void* k_new, const void* v_new) {
   int st = check_dims(dims, true);
   if (st != PKV_OK) return st;
   if (dims->batch > kMaxBatch) return PKV_ERR_DIMS;
@@ -129,14 +162,16 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   const DecodeKernel k = decode_kernel(dims->head_dim, group, sparse);
   if (k.split == nullptr) return PKV_ERR_GQA;
   const int max_units = sparse ? (max_kept + 15) / 16 : dims->max_blocks_per_seq;
-  // the flattened unit count must fit int32
+  // the flattened unit count and the pool's row count (a TMA coordinate) must fit int32
   if ((long long)dims->batch * dims->num_kv_heads * (long long)(max_units + 1) >= (1ll << 31))
     return PKV_ERR_DIMS;
+  const long long pool_rows = (long long)dims->num_blocks * dims->num_kv_heads * PKV_BLOCK_SIZE;
+  if (pool_rows >= (1ll << 31)) return PKV_ERR_DIMS;
   const WorkspacePlan plan = plan_workspace(dims, max_units);
   if (workspace_bytes < plan.total) return PKV_ERR_WORKSPACE;
   const DeviceInfo* info = device_info(&st);
   if (!info) return st;
-  const size_t smem = decode_smem_bytes(dims->head_dim, group, dims->batch);
+  const size_t smem = decode_smem_bytes(dims->head_dim, sparse, dims->batch);
   if (smem > info->max_smem_optin) return PKV_ERR_DIMS;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.split, kDecodeWarps * 32, smem);
@@ -144,6 +179,11 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   if (per_sm < 1) return PKV_ERR_DIMS;
 
   DecodeArgs a{};
+  if (!sparse) {
+    st = encode_pool_map(&a.tmap_k, k_cache, pool_rows, dims->head_dim);
+    if (st == PKV_OK) st = encode_pool_map(&a.tmap_v, v_cache, pool_rows, dims->head_dim);
+    if (st != PKV_OK) return st;
+  }
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
   a.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
@@ -151,6 +191,12 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.context_lens = context_lens;
   a.kept = kept;
   a.kept_lens = kept_lens;
+  if (k_new != nullptr) {
+    a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    a.k_pool_out = static_cast<__nv_bfloat16*>(const_cast<void*>(k_cache));
+    a.v_pool_out = static_cast<__nv_bfloat16*>(const_cast<void*>(v_cache));
+  }
   a.out = static_cast<__nv_bfloat16*>(out);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   a.layout = reinterpret_cast<int32_t*>(ws + plan.layout_off);
@@ -207,6 +253,19 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
                                void* stream) {
   return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, nullptr, nullptr, 0,
                        scale, window, workspace, workspace_bytes, dims, error_word, stream, false);
+}
+
+int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                      const void* k_new, const void* v_new,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      float scale, int32_t window, void* workspace,
+                                      size_t workspace_bytes, const pkv_dims* dims,
+                                      int32_t* error_word, void* stream) {
+  if (k_new == nullptr || v_new == nullptr) return PKV_ERR_NULL_POINTER;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_ALIGNMENT;
+  return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, nullptr, nullptr, 0,
+                       scale, window, workspace, workspace_bytes, dims, error_word, stream, false,
+                       k_new, v_new);
 }
 
 size_t pkv_sparse_decode_workspace_bytes(const pkv_dims* dims, int32_t max_kept) {
@@ -291,7 +350,7 @@ const char* pkv_status_string(int status) {
     case PKV_ERR_DIMS: return "invalid or unsupported size";
     case PKV_ERR_BLOCK_SIZE: return "block_size must be 16";
     case PKV_ERR_HEAD_DIM: return "head_dim must be 64 or 128";
-    case PKV_ERR_GQA: return "num_q_heads must be a multiple of num_kv_heads with G in {1,2,4,6,8}";
+    case PKV_ERR_GQA: return "num_q_heads must be a multiple of num_kv_heads with G = Hq/Hkv <= 8";
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
     case PKV_ERR_ALIGNMENT: return "a tensor pointer is not 16-byte aligned";
     case PKV_ERR_ARGUMENT: return "invalid scalar argument";

@@ -7,27 +7,33 @@
 // section 4.1).  Dense mode attends [max(0, L-window), L); sparse mode attends a kept list
 // (the layer-wise sparse variant of "How KV Sparsity Achieves 1.5x Acceleration for vLLM").
 //
-// Design (GB300-first; HBM-bound, 4-6 flop per KV byte):
-//  * Work partition ("stream-K" split): the (sequence, kv head, 16-token unit) list is
-//    flattened and cut into equal contiguous ranges, one per worker warp of a persistent
-//    grid sized to the SMs, so every SM streams the same number of bytes whatever the
-//    length mix.  A range may end inside a (sequence, head) segment: each worker emits a
-//    partial (running max m, running sum l, unnormalised o) per segment it touches; a
-//    segment covered by one worker writes its output directly.
-//  * Each worker warp owns a ring of K/V tile pairs in shared memory.  One lane issues TMA
-//    bulk copies (cp.async.bulk, 4 KiB per tile at d=128, L2 evict-first) completing on a
-//    per-slot mbarrier; the warp consumes slots in order and refills a slot once every lane
-//    has finished reading it.  Sparse mode gathers rows instead: 32 lanes each issue one
-//    row copy (16 K rows + 16 V rows) into the same tile layout.
-//  * GQA: the G query heads sharing a kv head are processed together, so each K/V byte is
-//    read from HBM once per kv head.
-//  * Math in fp32 on CUDA cores with Blackwell packed fp32x2 FMA: lane (half, es) holds 8
-//    (d=128) or 4 (d=64) elements of q for the G heads and the same slice of the output.
-//    Tokens alternate between the two half-warps.  Partial dot products are finished by a
-//    butterfly reduce-scatter over the 16 lanes of a half-warp (each lane ends with whole
-//    logits of one head), then the online-softmax update ("How KV Sparsity...", section
-//    "2. Attention modification", Fig. 7: running max, running sum, rescale, divide at the
-//    end) happens in base 2 with log2(e) folded into q.
+// Design (GB300-first; the step is HBM-bound at 4-6 flop per KV byte):
+//  * Work partition (a "stream-K" split): the (sequence, kv head, 16-token unit) list is
+//    flattened and cut into equal contiguous ranges, one per worker warp of a grid sized to
+//    the SMs, so every worker streams the same number of bytes whatever the length mix.  A
+//    range may end inside a (sequence, kv head) segment: each worker emits a partial
+//    (running max m, running sum l, unnormalised o) per segment it touches, and a segment
+//    covered by one worker writes its output directly.  A merge kernel combines the rest.
+//  * Each worker warp owns a ring of K/V tile pairs in shared memory that complete on
+//    per-slot mbarriers.  Dense mode fills them with TMA tiled copies of a 2-D tensor map
+//    over the pool (one 64-column x 16-row box per 128 bytes of row, 128-byte swizzle, L2
+//    evict-first): 4 copy operations per unit, and the swizzle puts the 8 rows an ldmatrix
+//    reads in 8 different bank groups.  Sparse mode gathers rows: each lane issues one
+//    256-byte cp.async.bulk row copy chosen through its kept index into rows stored at a
+//    272-byte pitch (again conflict-free for ldmatrix).
+//  * GQA: the G <= 8 query heads sharing a kv head are processed together, so each K/V byte
+//    is read from HBM once per kv head.
+//  * Both contractions run on the tensor cores as warp-level mma.m16n8k16 (bf16 inputs,
+//    exact products, fp32 accumulation), with tokens as the 16-row dimension and heads as
+//    the 8-column one: S^T = K q^T (16 tokens x 8 heads) and O^T += V^T P^T (d x 8 heads).
+//    P^T leaves the first product as an accumulator fragment and becomes the second one's
+//    operand by an in-register 8x8 transpose (movmatrix); it is carried as bf16 hi + lo
+//    parts so P keeps ~16 significant bits.  This replaces ~870 CUDA-core instructions per
+//    unit with ~100, leaving the warps waiting on memory rather than on issue slots.
+//  * Online softmax ("How KV Sparsity...", section "2. Attention modification", Fig. 7:
+//    running max, running sum, rescale, divide at the end) in base 2 with log2(e) folded
+//    into the scale; the running max only moves when a unit's max exceeds it by 2^8, so the
+//    output rescale is rare.
 //  * Every wait is bounded (globaltimer); a timeout records PKV_DEV_WAIT_TIMEOUT, waits for
 //    the copies in flight and returns.  Bad block ids / kept indices are skipped and
 //    recorded, never dereferenced.
@@ -40,31 +46,43 @@
 namespace pkv {
 namespace {
 
-template <int D>
+template <int D, bool SPARSE>
 struct Geo {
-  static constexpr int kEPL = D / 16;       // bf16 elements of a row held by one lane
-  static constexpr int kPairs = kEPL / 2;   // fp32 pairs per lane per row
-  static constexpr int kRow = D * 2;        // bytes per K/V row
-  static constexpr int kTile = 16 * kRow;   // bytes per 16-token tile
-  static constexpr int kRing = (D == 128) ? 3 : 5;
+  static constexpr int kRow = D * 2;                       // bytes per K/V row in HBM
+  static constexpr int kBoxes = D / 64;                    // dense: 128-byte column boxes per row
+  static constexpr int kPitch = D * 2 + 16;                // sparse: padded row pitch in smem
+  static constexpr int kTile = SPARSE ? 16 * kPitch : 16 * D * 2;  // bytes per 16-row tile
+  static constexpr int kKSteps = D / 16;                   // k-steps of q.K, m-tiles of P.V
+  static constexpr int kRing = (D == 128) ? PKV_RING_D128 : PKV_RING_D64;
+  static_assert(kBoxes * 128 == kRow && kRing >= 2, "head_dim must be a multiple of 64");
 };
 
-template <int G>
-struct Grp {
-  static constexpr int kGP = G == 1 ? 1 : (G == 2 ? 2 : (G <= 4 ? 4 : 8));  // padded group
-  static constexpr int kN = kGP * 8;                     // partial logits per lane per tile
-  static constexpr int kVPL = kN >= 16 ? kN / 16 : 1;    // whole logits per lane after reduction
-  static constexpr int kLPG = kN >= 16 ? 8 / kVPL : 16;  // lanes of a half-warp sharing one head
-};
+// Byte offset inside a tile of the 16-byte chunk holding row r, columns [8c, 8c + 8).
+// Dense tiles are kBoxes boxes of 16 rows x 128 bytes written by TMA with the 128-byte
+// swizzle (chunk index XOR row % 8 inside each 1024-byte box); sparse tiles are plain rows
+// at the padded pitch.
+template <int D, bool SPARSE>
+__device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
+  if constexpr (SPARSE) {
+    return (uint32_t)(r * Geo<D, SPARSE>::kPitch + c * 16);
+  } else {
+    return (uint32_t)((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  }
+}
 
-template <int D, int G>
+// A running max is only moved (and the output rescaled) when a unit's max exceeds it by more
+// than this many base-2 units, so unnormalised weights stay below 2^8 and most units skip
+// the rescale.  Any reference value gives the same normalised result.
+constexpr float kRescaleSlack = 8.0f;
+
+template <int D, bool SPARSE>
 struct WarpSmem {
-  alignas(128) unsigned char tiles[Geo<D>::kRing][2][Geo<D>::kTile];
-  uint64_t p2[2 * 8 * Grp<G>::kGP];  // (p, p) pairs, [half][token index][head]
-  uint64_t a2[Grp<G>::kGP];          // (alpha, alpha) per head
-  float2 ml[Grp<G>::kGP];            // (m, l) per head, at flush
-  uint64_t bar[Geo<D>::kRing];
-  uint32_t meta[Geo<D>::kRing];      // valid-token mask of the unit held by a slot
+  alignas(1024) unsigned char k[Geo<D, SPARSE>::kRing][Geo<D, SPARSE>::kTile];
+  alignas(1024) unsigned char v[Geo<D, SPARSE>::kRing][Geo<D, SPARSE>::kTile];
+  uint64_t bar_k[Geo<D, SPARSE>::kRing];  // K rows of the slot landed
+  uint64_t bar_v[Geo<D, SPARSE>::kRing];  // V rows of the slot landed
+  uint32_t meta[Geo<D, SPARSE>::kRing];   // rows of the unit that were copied (bit t = token t)
+  int32_t phys[Geo<D, SPARSE>::kRing];    // dense: physical block of the unit in the slot
 };
 
 struct Cursor {
@@ -96,57 +114,19 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* s_nb, int B, i
   }
 }
 
-template <int EPL>
-__device__ __forceinline__ void load_row(const unsigned char* p, uint32_t (&w)[EPL / 2]) {
-  if constexpr (EPL == 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-  } else {
-    const uint2 v = *reinterpret_cast<const uint2*>(p);
-    w[0] = v.x; w[1] = v.y;
-  }
-}
-
-// One level of the butterfly reduce-scatter across lanes differing in bit `M` of `es`:
-// of the `n` live values, the lane keeps the upper half when its bit is set (else the
-// lower half), adds the partner lane's copy of that half, and ends with n/2 live values.
-// With a single live value the level is a plain all-reduce.
-template <int n, int M, int CAP>
-__device__ __forceinline__ void rs_level(float (&v)[CAP], int es) {
-  if constexpr (n >= 2) {
-    const bool upper = (es & M) != 0;
-#pragma unroll
-    for (int j = 0; j < n / 2; ++j) {
-      const float send = upper ? v[j] : v[j + n / 2];
-      const float keep = upper ? v[j + n / 2] : v[j];
-      v[j] = keep + __shfl_xor_sync(kFullMask, send, M);
-    }
-  } else {
-    v[0] += __shfl_xor_sync(kFullMask, v[0], M);
-  }
-}
-
-__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
-  const float2 f = unpack2(v);
-  return pack2(__shfl_xor_sync(kFullMask, f.x, m), __shfl_xor_sync(kFullMask, f.y, m));
-}
-
-template <int D, int G, bool SPARSE>
+template <int D, bool SPARSE>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
-decode_split_kernel(const DecodeArgs a) {
-  using GE = Geo<D>;
-  using GR = Grp<G>;
+decode_split_kernel(const __grid_constant__ DecodeArgs a) {
+  using GE = Geo<D, SPARSE>;
+  using WS = WarpSmem<D, SPARSE>;
   constexpr int R = GE::kRing;
-  constexpr int EPL = GE::kEPL;
-  constexpr int NP = GE::kPairs;
-  constexpr int GP = GR::kGP;
-  constexpr int N = GR::kN;
-  constexpr int VPL = GR::kVPL;
-  constexpr int LPG = GR::kLPG;
+  constexpr int KS = GE::kKSteps;
 
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  auto* warps_smem = reinterpret_cast<WarpSmem<D, G>*>(smem_raw);
-  int32_t* s_start = reinterpret_cast<int32_t*>(smem_raw + sizeof(WarpSmem<D, G>) * kDecodeWarps);
+  extern __shared__ __align__(1024) unsigned char smem_dyn[];
+  // the swizzle pattern is a function of address bits 4-9: start the tiles on 1 KiB
+  unsigned char* smem_raw = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+  auto* warps_smem = reinterpret_cast<WS*>(smem_raw);
+  int32_t* s_start = reinterpret_cast<int32_t*>(smem_raw + sizeof(WS) * kDecodeWarps);
   int32_t* s_nb = s_start + (a.B + 1);
   int32_t* s_first = s_nb + a.B;
   int32_t* s_lo = s_first + a.B;   // dense: first attended token; sparse: context length
@@ -154,9 +134,22 @@ decode_split_kernel(const DecodeArgs a) {
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;
-  const int es = lane & 15;
-  WarpSmem<D, G>& W = warps_smem[warp];
+  const int gq = lane >> 2;  // fragment row group
+  const int tq = lane & 3;   // fragment column pair
+  const int G = a.G;
+  WS& W = warps_smem[warp];
+
+  if (lane == 0) {
+    for (int s = 0; s < R; ++s) {
+      mbar_init(&W.bar_k[s], 1);
+      mbar_init(&W.bar_v[s], 1);
+    }
+    fence_mbar_init();
+  }
+  // Launched with programmatic stream serialisation: wait for the previous kernel on the
+  // stream before reading anything in global memory, then let the merge kernel launch.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   // ---- per-sequence unit counts and partition (identical in every CTA) -------------------
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
@@ -186,10 +179,6 @@ decode_split_kernel(const DecodeArgs a) {
     s_first[b] = first;
     s_lo[b] = lo;
     s_len[b] = len;
-  }
-  if (lane == 0) {
-    for (int s = 0; s < R; ++s) mbar_init(&W.bar[s], 1);
-    fence_mbar_init();
   }
   __syncthreads();
   if (warp == 0) {
@@ -228,40 +217,83 @@ decode_split_kernel(const DecodeArgs a) {
   const int nunits = min(total - u0, per);
 
   const uint64_t pol = l2_policy_evict_first();
+  Cursor ic = locate(u0, s_start, s_nb, a.B);  // next unit to issue
+  Cursor cc = ic;                               // next unit to consume
 
-  // ---- producer side (issue a unit into a slot) -----------------------------------------
-  Cursor ic = locate(u0, s_start, s_nb, a.B);
-  Cursor cc = ic;
-  int pend_phys = -1;  // dense: block id of the unit `ic` names, loaded one issue ahead
+  // q of the next segment as raw bf16x2 words in B-fragment order: word 2ks+i holds head gq's
+  // elements 16ks + 8i + 2tq, +1 (zero for heads >= G).  The first segment's right away.
+  uint32_t qraw[2 * KS];
+  auto load_q = [&](int b, int g) {
+    if (gq < G) {
+      const uint32_t* qw = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * a.Hq + (size_t)g * G + gq) * D);
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qraw[2 * ks] = __ldg(qw + ks * 8 + tq);
+        qraw[2 * ks + 1] = __ldg(qw + ks * 8 + 4 + tq);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2 * KS; ++i) qraw[i] = 0u;
+    }
+  };
+  load_q(cc.b, cc.g);
+
+  // Dense: the block-table entries of this worker's units, 32 per coalesced load (lane l
+  // holds the entry of unit chunk_base + l), fetched one chunk ahead of use.
+  int bt_cur = -1, bt_next = -1, chunk_base = 0;
+  auto load_chunk = [&](int first) -> int {
+    int phys = -1;
+    if (first + lane < nunits) {
+      const Cursor c = locate(u0 + first + lane, s_start, s_nb, a.B);
+      phys = __ldg(a.block_tables + (size_t)c.b * a.MB + s_first[c.b] + c.j);
+    }
+    return phys;
+  };
   if constexpr (!SPARSE) {
-    if (lane == 0) pend_phys = __ldg(a.block_tables + (size_t)ic.b * a.MB + s_first[ic.b] + ic.j);
+    bt_cur = load_chunk(0);
+    if (nunits > 32) bt_next = load_chunk(32);
   }
 
+  // Issue unit k (the one `ic` names) into slot k % R.  Dense: lane 0 copies the K and V
+  // tiles as TMA boxes.  Sparse: lane r < 16 copies K row r, lane 16 + r V row r.
   auto issue = [&](int k) {
     const int slot = k % R;
     fence_proxy_async_smem();
     if constexpr (!SPARSE) {
+      if (k - chunk_base == 32) {
+        chunk_base += 32;
+        bt_cur = bt_next;
+        if (chunk_base + 32 < nunits) bt_next = load_chunk(chunk_base + 32);
+      }
+      const int phys = __shfl_sync(kFullMask, bt_cur, k - chunk_base);
       if (lane == 0) {
-        const int phys = pend_phys;
-        if (phys < 0 || phys >= a.NB) {
+        if (phys >= 0 && phys < a.NB) {
+          const int y = (phys * a.Hkv + ic.g) * 16;  // host checks NB*Hkv*16 < 2^31
+          W.meta[slot] = 0xffffu;
+          W.phys[slot] = phys;
+          mbar_arrive_expect_tx(&W.bar_k[slot], GE::kTile);
+#pragma unroll
+          for (int bx = 0; bx < GE::kBoxes; ++bx)
+            tma_load_2d(W.k[slot] + bx * 2048, &a.tmap_k, bx * 64, y, &W.bar_k[slot], pol);
+          mbar_arrive_expect_tx(&W.bar_v[slot], GE::kTile);
+#pragma unroll
+          for (int bx = 0; bx < GE::kBoxes; ++bx)
+            tma_load_2d(W.v[slot] + bx * 2048, &a.tmap_v, bx * 64, y, &W.bar_v[slot], pol);
+        } else {
           record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
           W.meta[slot] = 0u;
-          mbar_arrive_expect_tx(&W.bar[slot], 0);
-        } else {
-          W.meta[slot] = 1u;
-          mbar_arrive_expect_tx(&W.bar[slot], 2 * GE::kTile);
-          const size_t off = ((size_t)phys * a.Hkv + ic.g) * 16 * D;
-          bulk_g2s(W.tiles[slot][0], a.k_cache + off, GE::kTile, &W.bar[slot], pol);
-          bulk_g2s(W.tiles[slot][1], a.v_cache + off, GE::kTile, &W.bar[slot], pol);
+          mbar_arrive_expect_tx(&W.bar_k[slot], 0);
+          mbar_arrive_expect_tx(&W.bar_v[slot], 0);
         }
       }
       advance(ic, s_nb, a.B, a.Hkv);
-      if (lane == 0 && k + 1 < nunits)
-        pend_phys = __ldg(a.block_tables + (size_t)ic.b * a.MB + s_first[ic.b] + ic.j);
     } else {
       const int r = lane & 15;
+      const bool is_v = lane >= 16;
+      bool ok;
+      size_t src = 0;
       const int pos = ic.j * 16 + r;
-      bool ok = pos < s_len[ic.b];
+      ok = pos < s_len[ic.b];
       int t = 0, phys = 0;
       if (ok) {
         t = __ldg(a.kept + ((size_t)ic.b * a.Hkv + ic.g) * a.max_kept + pos);
@@ -277,16 +309,17 @@ decode_split_kernel(const DecodeArgs a) {
           ok = false;
         }
       }
-      const uint32_t vmask = __ballot_sync(kFullMask, ok) & 0xffffu;
+      src = (((size_t)phys * a.Hkv + ic.g) * 16 + (t & 15)) * D;
+      const uint32_t vmask = __ballot_sync(kFullMask, ok) & 0xffffu;  // K and V lanes agree
       if (lane == 0) {
         W.meta[slot] = vmask;
-        mbar_arrive_expect_tx(&W.bar[slot], 2u * __popc(vmask) * GE::kRow);
+        mbar_arrive_expect_tx(&W.bar_k[slot], __popc(vmask) * GE::kRow);
+        mbar_arrive_expect_tx(&W.bar_v[slot], __popc(vmask) * GE::kRow);
       }
       __syncwarp();
       if (ok) {
-        const size_t off = (((size_t)phys * a.Hkv + ic.g) * 16 + (t & 15)) * D;
-        const __nv_bfloat16* src = (lane >= 16 ? a.v_cache : a.k_cache) + off;
-        bulk_g2s(W.tiles[slot][lane >> 4] + r * GE::kRow, src, GE::kRow, &W.bar[slot], pol);
+        unsigned char* dst = (is_v ? W.v[slot] : W.k[slot]) + r * GE::kPitch;
+        bulk_g2s(dst, (is_v ? a.v_cache : a.k_cache) + src, GE::kRow, is_v ? &W.bar_v[slot] : &W.bar_k[slot], pol);
       }
       advance(ic, s_nb, a.B, a.Hkv);
     }
@@ -295,52 +328,51 @@ decode_split_kernel(const DecodeArgs a) {
   int issued = 0;
   for (; issued < nunits && issued < R; ++issued) issue(issued);
 
-  // ---- consumer state --------------------------------------------------------------------
-  uint64_t q2[G][NP];
-  uint64_t o2[G][NP];
-  float m_run = -INFINITY, l_run = 0.f;
-  const int my_head = es / LPG;  // head (within the group) whose logits this lane finishes
+  // ---- consumer state: this lane's heads are h0 = 2tq and h1 = 2tq + 1 ------------------
+  uint32_t qb[2 * KS];   // q^T B fragments of the current segment
+  float o[KS][4];        // O^T accumulator fragments: [m-tile][d row gq / gq+8, head h0 / h1]
+  float mr0 = -INFINITY, mr1 = -INFINITY;  // running max (reference) of heads h0, h1
+  float l0 = 0.f, l1 = 0.f;                // this lane's share of the running sums
   int seg_b = -1, seg_g = -1, part = 0, nparts = 0;
+  const float sl2 = a.scale_log2;
+  // Dense append mode: this step's K (lanes 0-15) or V (lanes 16-31) row chunk of the current
+  // segment, to be written at token L_b - 1 (pool and tile) when its unit is consumed.
+  const bool appending = !SPARSE && a.k_new != nullptr;
+  uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
+  const int new_chunk = lane & 15;
+  const bool new_lane = new_chunk < D / 8;
 
   auto flush = [&]() {
-    float l = l_run;
 #pragma unroll
-    for (int m = 1; m < LPG; m <<= 1) l += __shfl_xor_sync(kFullMask, l, m);
-    l += __shfl_xor_sync(kFullMask, l, 16);
+    for (int m = 4; m <= 16; m <<= 1) {
+      l0 += __shfl_xor_sync(kFullMask, l0, m);
+      l1 += __shfl_xor_sync(kFullMask, l1, m);
+    }
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg)
+    for (int hh = 0; hh < 2; ++hh) {
+      const int head = 2 * tq + hh;
+      if (head >= G) continue;
+      const float l = hh ? l1 : l0;
+      const float m = hh ? mr1 : mr0;
+      const size_t row = (size_t)seg_b * a.Hq + (size_t)seg_g * G + head;
+      if (nparts == 1) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* dst = a.out + row * D + gq;
 #pragma unroll
-      for (int k = 0; k < NP; ++k) o2[gg][k] = fadd2(o2[gg][k], shfl_xor64(o2[gg][k], 16));
-    if (half == 0 && (es % LPG) == 0 && my_head < G) W.ml[my_head] = make_float2(m_run, l);
-    __syncwarp();
-    if (half == 0) {
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        const float2 ml = W.ml[gg];
-        const size_t row = (size_t)seg_b * a.Hq + (size_t)seg_g * G + gg;
-        if (nparts == 1) {
-          const float inv = ml.y > 0.f ? 1.f / ml.y : 0.f;
-          uint32_t packed[NP];
-#pragma unroll
-          for (int k = 0; k < NP; ++k) {
-            const float2 f = unpack2(o2[gg][k]);
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(f.x * inv, f.y * inv);
-            packed[k] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          __nv_bfloat16* dst = a.out + row * D + es * EPL;
-          if constexpr (EPL == 8)
-            *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          else
-            *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-        } else {
-          float* dst = a.part_o + (row * a.max_parts + part) * D + es * EPL;
-#pragma unroll
-          for (int k = 0; k < NP; ++k) reinterpret_cast<float2*>(dst)[k] = unpack2(o2[gg][k]);
-          if (es == 0) a.part_ml[row * a.max_parts + part] = ml;
+        for (int mt = 0; mt < KS; ++mt) {
+          dst[mt * 16] = __float2bfloat16_rn(o[mt][hh] * inv);
+          dst[mt * 16 + 8] = __float2bfloat16_rn(o[mt][2 + hh] * inv);
         }
+      } else {
+        float* dst = a.part_o + (row * a.max_parts + part) * D + gq;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          dst[mt * 16] = o[mt][hh];
+          dst[mt * 16 + 8] = o[mt][2 + hh];
+        }
+        if (gq == 0) a.part_ml[row * a.max_parts + part] = make_float2(m, l);
       }
     }
-    __syncwarp();
   };
 
   auto begin_segment = [&](const Cursor& c) {
@@ -351,22 +383,34 @@ decode_split_kernel(const DecodeArgs a) {
     const int w0 = seg_begin / per;
     nparts = (seg_begin + nb - 1) / per - w0 + 1;
     part = (int)gw - w0;
-    const uint64_t sc = pack2(a.scale_log2, a.scale_log2);
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      const unsigned char* qp = reinterpret_cast<const unsigned char*>(
-          a.q + ((size_t)c.b * a.Hq + (size_t)c.g * G + gg) * D + es * EPL);
-      uint32_t w[NP];
-      load_row<EPL>(qp, w);
-#pragma unroll
-      for (int k = 0; k < NP; ++k) {
-        q2[gg][k] = fmul2(bf16x2_to_f32x2(w[k]), sc);
-        o2[gg][k] = 0ull;
-      }
+    for (int i = 0; i < 2 * KS; ++i) qb[i] = qraw[i];
+    if (appending && new_lane) {
+      const __nv_bfloat16* src = (lane >= 16 ? a.v_new : a.k_new) + ((size_t)c.b * a.Hkv + c.g) * D + new_chunk * 8;
+      new_row = __ldg(reinterpret_cast<const uint4*>(src));
     }
-    m_run = -INFINITY;
-    l_run = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
+    mr0 = mr1 = -INFINITY;
+    l0 = l1 = 0.f;
+    // prefetch q of the segment that follows, if this worker reaches it
+    if (seg_begin + nb < u0 + nunits) {
+      int nb2 = c.b, ng2 = c.g + 1;
+      if (ng2 == a.Hkv) {
+        ng2 = 0;
+        do { ++nb2; } while (nb2 < a.B && s_nb[nb2] == 0);
+      }
+      if (nb2 < a.B) load_q(nb2, ng2);
+    }
   };
+
+  // ldmatrix rows of this lane: K (non-transposed A of S^T = K q^T) reads row lane & 15, chunk
+  // 2 ks + lane / 16; V (transposed A of O^T = V^T P^T) reads token (lane & 7) + 8 (lane / 16),
+  // chunk 2 mt + (lane / 8) % 2.
+  const int k_row = lane & 15, k_half = lane >> 4;
+  const int v_row = (lane & 7) + ((lane >> 4) << 3), v_half = (lane >> 3) & 1;
 
   bool aborted = false;
   int k = 0;
@@ -376,112 +420,128 @@ decode_split_kernel(const DecodeArgs a) {
       begin_segment(cc);
     }
     const int slot = k % R;
+    const uint32_t parity = (uint32_t)(k / R) & 1u;
     // every lane waits (acquiring the TMA writes); the give-up decision is warp-uniform
-    const bool landed = mbar_wait_bounded(&W.bar[slot], (uint32_t)(k / R) & 1u, a.timeout_ns);
-    if (!__all_sync(kFullMask, landed)) {
+    if (!__all_sync(kFullMask, mbar_wait_bounded(&W.bar_k[slot], parity, a.timeout_ns))) {
       if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
       aborted = true;
       break;
     }
-    uint32_t mask;
-    if constexpr (SPARSE) {
-      mask = W.meta[slot];
-    } else {
+    uint32_t mask = W.meta[slot];
+    int t_new = -1;  // tile row of this step's token when the unit holds it (append mode)
+    if constexpr (!SPARSE) {
       const int tok0 = (s_first[cc.b] + cc.j) * 16;
       const int lo = max(s_lo[cc.b] - tok0, 0);
       const int hi = min(s_len[cc.b] - tok0, 16);
-      mask = W.meta[slot] ? (((1u << hi) - 1u) & ~((1u << lo) - 1u)) : 0u;
+      mask &= ((1u << hi) - 1u) & ~((1u << lo) - 1u);
+      if (appending && mask != 0u && s_len[cc.b] - 1 - tok0 < 16) {
+        t_new = s_len[cc.b] - 1 - tok0;
+        // the tile was read before the append: put the new K row in it and in the pool
+        if (lane < 16 && new_lane) {
+          *reinterpret_cast<uint4*>(W.k[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
+          *reinterpret_cast<uint4*>(a.k_pool_out + (((size_t)W.phys[slot] * a.Hkv + cc.g) * 16 + t_new) * D +
+                                    new_chunk * 8) = new_row;
+        }
+        __syncwarp();
+      }
     }
     if (mask != 0u) {
-      const unsigned char* kt = W.tiles[slot][0] + es * EPL * 2;
-      const unsigned char* vt = W.tiles[slot][1] + es * EPL * 2;
-      // -- logits: partial dot products of this lane's slice for its 8 tokens -------------
-      float v[N];
+      // -- S^T = K q^T: 16 tokens x 8 heads --------------------------------------------------
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t kbase = smem_u32(W.k[slot]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int t = 2 * i + half;
-        uint32_t w[NP];
-        load_row<EPL>(kt + t * GE::kRow, w);
-        uint64_t kf[NP];
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t af[4];
+        ldsm_x4(kbase + chunk_offset<D, SPARSE>(k_row, 2 * ks + k_half), af);
+        mma_bf16_m16n8k16(c, af, qb[2 * ks], qb[2 * ks + 1]);
+      }
+      // c[0] = (token gq, head h0), c[1] = (gq, h1), c[2] = (gq + 8, h0), c[3] = (gq + 8, h1)
+      const bool t0 = (mask >> gq) & 1u;
+      const bool t1 = (mask >> (gq + 8)) & 1u;
+      const bool v0 = 2 * tq < G, v1 = 2 * tq + 1 < G;
+      const float s00 = (t0 && v0) ? c[0] * sl2 : -INFINITY;
+      const float s01 = (t0 && v1) ? c[1] * sl2 : -INFINITY;
+      const float s10 = (t1 && v0) ? c[2] * sl2 : -INFINITY;
+      const float s11 = (t1 && v1) ? c[3] * sl2 : -INFINITY;
+      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
-        for (int kk = 0; kk < NP; ++kk) kf[kk] = bf16x2_to_f32x2(w[kk]);
+      for (int m = 4; m <= 16; m <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, m));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, m));
+      }
+      // lazy running max: move it only when this unit's max is well above it
+      const bool g0 = mx0 > mr0 + kRescaleSlack, g1 = mx1 > mr1 + kRescaleSlack;
+      if (__any_sync(kFullMask, g0 || g1)) {
+        float al0 = 1.f, al1 = 1.f;
+        if (g0) {
+          al0 = exp2f(mr0 - mx0);
+          mr0 = mx0;
+        }
+        if (g1) {
+          al1 = exp2f(mr1 - mx1);
+          mr1 = mx1;
+        }
+        l0 *= al0;
+        l1 *= al1;
 #pragma unroll
-        for (int gg = 0; gg < GP; ++gg) {
-          if (gg < G) {
-            uint64_t acc = ffma2(q2[gg][0], kf[0], 0ull);
-#pragma unroll
-            for (int kk = 1; kk < NP; ++kk) acc = ffma2(q2[gg][kk], kf[kk], acc);
-            const float2 f = unpack2(acc);
-            v[gg * 8 + i] = f.x + f.y;
-          } else {
-            v[gg * 8 + i] = 0.f;
-          }
+        for (int mt = 0; mt < KS; ++mt) {
+          o[mt][0] *= al0;
+          o[mt][1] *= al1;
+          o[mt][2] *= al0;
+          o[mt][3] *= al1;
         }
       }
-      // -- butterfly reduce-scatter over the 16 lanes of the half-warp -------------------
-      rs_level<N, 8>(v, es);
-      rs_level<(N >= 2 ? N / 2 : 1), 4>(v, es);
-      rs_level<(N >= 4 ? N / 4 : 1), 2>(v, es);
-      rs_level<(N >= 8 ? N / 8 : 1), 1>(v, es);
-      // -- mask, block max, online-softmax update ----------------------------------------
-      float bmax = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int f = (N >= 16) ? es * VPL + j : (es >> 1);
-        const int t = 2 * (f & 7) + half;
-        const bool ok = ((mask >> t) & 1u) && (f >> 3) < G;
-        v[j] = ok ? v[j] : -INFINITY;
-        bmax = fmaxf(bmax, v[j]);
+      const float ref0 = (mr0 == -INFINITY) ? 0.f : mr0;
+      const float ref1 = (mr1 == -INFINITY) ? 0.f : mr1;
+      const float p00 = exp2f(s00 - ref0), p01 = exp2f(s01 - ref1);
+      const float p10 = exp2f(s10 - ref0), p11 = exp2f(s11 - ref1);
+      l0 += p00 + p10;
+      l1 += p01 + p11;
+      // -- P^T as bf16 hi + lo B fragments (tokens x heads -> heads x tokens) -------------
+      const uint32_t hA = pack_bf16x2(p00, p01);  // token gq
+      const uint32_t hB = pack_bf16x2(p10, p11);  // token gq + 8
+      const uint32_t lA = pack_bf16x2(p00 - bf16_lo_to_f32(hA), p01 - bf16_hi_to_f32(hA));
+      const uint32_t lB = pack_bf16x2(p10 - bf16_lo_to_f32(hB), p11 - bf16_hi_to_f32(hB));
+      const uint32_t bh0 = movmatrix_trans(hA), bh1 = movmatrix_trans(hB);
+      const uint32_t bl0 = movmatrix_trans(lA), bl1 = movmatrix_trans(lB);
+      if (!__all_sync(kFullMask, mbar_wait_bounded(&W.bar_v[slot], parity, a.timeout_ns))) {
+        if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+        aborted = true;
+        break;
       }
-#pragma unroll
-      for (int m = 1; m < LPG; m <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(kFullMask, bmax, m));
-      bmax = fmaxf(bmax, __shfl_xor_sync(kFullMask, bmax, 16));
-      const float m_new = fmaxf(m_run, bmax);
-      const float mref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = exp2f(m_run - mref);
-      const bool dup = (N < 16) && (es & 1);  // G == 1: lanes es, es^1 hold the same logit
-      float psum = 0.f;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const float p = exp2f(v[j] - mref);
-        const int f = (N >= 16) ? es * VPL + j : (es >> 1);
-        if (!dup && (f >> 3) < G) {
-          W.p2[(half * 8 + (f & 7)) * GP + (f >> 3)] = pack2(p, p);
-          psum += p;
+      if (t_new >= 0) {  // append mode: the new V row, into the tile and the pool
+        if (lane >= 16 && new_lane) {
+          *reinterpret_cast<uint4*>(W.v[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
+          *reinterpret_cast<uint4*>(a.v_pool_out + (((size_t)W.phys[slot] * a.Hkv + cc.g) * 16 + t_new) * D +
+                                    new_chunk * 8) = new_row;
         }
+        __syncwarp();
       }
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-      if (half == 0 && (es % LPG) == 0 && my_head < G) W.a2[my_head] = pack2(alpha, alpha);
-      __syncwarp();
-      // -- rescale and accumulate P.V for this lane's 8 tokens -------------------------------
+      if (mask != 0xffffu) {
+        // rows of tokens outside the attended set may hold anything (even NaN): zero them,
+        // since the tensor core would turn 0 * NaN into NaN
 #pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        const uint64_t a2 = W.a2[gg];
-#pragma unroll
-        for (int kk = 0; kk < NP; ++kk) o2[gg][kk] = fmul2(o2[gg][kk], a2);
-      }
-      const bool partial = mask != 0xffffu;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int t = 2 * i + half;
-        uint32_t w[NP];
-        load_row<EPL>(vt + t * GE::kRow, w);
-        if (partial && !((mask >> t) & 1u)) {
-#pragma unroll
-          for (int kk = 0; kk < NP; ++kk) w[kk] = 0u;
+        for (int i = 0; i < 8; ++i) {
+          const int t = 2 * i + (lane >> 4);
+          const int c = lane & 15;  // chunk (16 bytes) of the row
+          if (!((mask >> t) & 1u) && c < D / 8)
+            *reinterpret_cast<uint4*>(W.v[slot] + chunk_offset<D, SPARSE>(t, c)) = make_uint4(0u, 0u, 0u, 0u);
         }
-        uint64_t vf[NP];
-#pragma unroll
-        for (int kk = 0; kk < NP; ++kk) vf[kk] = bf16x2_to_f32x2(w[kk]);
-        const uint64_t* prow = W.p2 + (half * 8 + i) * GP;
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          const uint64_t pp = prow[gg];
-#pragma unroll
-          for (int kk = 0; kk < NP; ++kk) o2[gg][kk] = ffma2(pp, vf[kk], o2[gg][kk]);
-        }
+        __syncwarp();
       }
+      // -- O^T += V^T P^T -------------------------------------------------------------------
+      const uint32_t vbase = smem_u32(W.v[slot]);
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t av[4];
+        ldsm_x4_trans(vbase + chunk_offset<D, SPARSE>(v_row, 2 * mt + v_half), av);
+        mma_bf16_m16n8k16(o[mt], av, bh0, bh1);
+        mma_bf16_m16n8k16(o[mt], av, bl0, bl1);
+      }
+    } else if (!__all_sync(kFullMask, mbar_wait_bounded(&W.bar_v[slot], parity, a.timeout_ns))) {
+      if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+      aborted = true;
+      break;
     }
     __syncwarp();
     if (issued < nunits) {
@@ -491,8 +551,11 @@ decode_split_kernel(const DecodeArgs a) {
     advance(cc, s_nb, a.B, a.Hkv);
   }
 
-  if (aborted) {
-    for (int kk = k; kk < issued; ++kk) (void)mbar_wait_bounded(&W.bar[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
+  if (aborted) {  // let the copies in flight land before the CTA's shared memory goes away
+    for (int kk = k; kk < issued; ++kk) {
+      (void)mbar_wait_bounded(&W.bar_k[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
+      (void)mbar_wait_bounded(&W.bar_v[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
+    }
     return;
   }
   flush();
@@ -507,6 +570,8 @@ decode_merge_kernel(const DecodeArgs a, int group) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kMergeWarps + warp;
+  grid_dependency_wait();  // the split kernel's partials and partition record
+  grid_launch_dependents();
   if (row >= a.B * a.Hq) return;
   const int b = row / a.Hq;
   const int g = (row % a.Hq) / group;
@@ -524,28 +589,41 @@ decode_merge_kernel(const DecodeArgs a, int group) {
   if (np == 1) return;
   const float2* ml = a.part_ml + (size_t)row * a.max_parts;
   const float* po = a.part_o + (size_t)row * a.max_parts * D + lane * EPW;
-  float M = -INFINITY;
-  for (int p = lane; p < np; p += 32) M = fmaxf(M, ml[p].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
-  const float mref = (M == -INFINITY) ? 0.f : M;
-  float L = 0.f;
-  for (int p = lane; p < np; p += 32) L += ml[p].y * exp2f(ml[p].x - mref);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFullMask, L, o);
+  // Partials in groups of 32: lane p holds (m, l) of partial p; the o loads of a group are
+  // independent of the weights, so one memory round trip covers a group.
+  float M = -INFINITY, L = 0.f;
   float acc[EPW];
 #pragma unroll
   for (int e = 0; e < EPW; ++e) acc[e] = 0.f;
-#pragma unroll 4
-  for (int p = 0; p < np; ++p) {
-    const float w = exp2f(ml[p].x - mref);
-    const float* src = po + (size_t)p * D;
-    if constexpr (EPW == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(src);
-      acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(src);
-      acc[0] += w * x.x; acc[1] += w * x.y;
+  for (int p0 = 0; p0 < np; p0 += 32) {
+    const int n = min(32, np - p0);
+    const float2 mlp = lane < n ? ml[p0 + lane] : make_float2(-INFINITY, 0.f);
+    float gmax = mlp.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(kFullMask, gmax, o));
+    const float M_new = fmaxf(M, gmax);
+    const float mref = (M_new == -INFINITY) ? 0.f : M_new;
+    const float carry = exp2f(M - mref);  // rescale what earlier groups accumulated
+    L *= carry;
+#pragma unroll
+    for (int e = 0; e < EPW; ++e) acc[e] *= carry;
+    M = M_new;
+    const float w_lane = exp2f(mlp.x - mref);
+    float lsum = w_lane * mlp.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFullMask, lsum, o);
+    L += lsum;
+#pragma unroll 8
+    for (int p = 0; p < n; ++p) {
+      const float w = __shfl_sync(kFullMask, w_lane, p);
+      const float* src = po + (size_t)(p0 + p) * D;
+      if constexpr (EPW == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * x.x; acc[1] += w * x.y;
+      }
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -555,50 +633,43 @@ decode_merge_kernel(const DecodeArgs a, int group) {
   }
 }
 
-template <int D, int G>
-constexpr size_t warp_smem_bytes() { return sizeof(WarpSmem<D, G>); }
-
 }  // namespace
 
-#define PKV_DECODE_CASE(D, G)                                                              \
-  if (head_dim == D && group == G)                                                         \
-    return sparse ? DecodeKernel{(const void*)decode_split_kernel<D, G, true>,             \
-                                 (const void*)decode_merge_kernel<D>, D, G, true}          \
-                  : DecodeKernel{(const void*)decode_split_kernel<D, G, false>,            \
-                                 (const void*)decode_merge_kernel<D>, D, G, false};
-
 DecodeKernel decode_kernel(int head_dim, int group, bool sparse) {
-  PKV_DECODE_CASE(128, 1) PKV_DECODE_CASE(128, 2) PKV_DECODE_CASE(128, 4)
-  PKV_DECODE_CASE(128, 6) PKV_DECODE_CASE(128, 8)
-  PKV_DECODE_CASE(64, 1) PKV_DECODE_CASE(64, 2) PKV_DECODE_CASE(64, 4)
-  PKV_DECODE_CASE(64, 6) PKV_DECODE_CASE(64, 8)
+  if (group < 1 || group > kMaxGroup) return DecodeKernel{nullptr, nullptr, head_dim, group, sparse};
+  if (head_dim == 128)
+    return DecodeKernel{sparse ? (const void*)decode_split_kernel<128, true>
+                               : (const void*)decode_split_kernel<128, false>,
+                        (const void*)decode_merge_kernel<128>, 128, group, sparse};
+  if (head_dim == 64)
+    return DecodeKernel{sparse ? (const void*)decode_split_kernel<64, true>
+                               : (const void*)decode_split_kernel<64, false>,
+                        (const void*)decode_merge_kernel<64>, 64, group, sparse};
   return DecodeKernel{nullptr, nullptr, head_dim, group, sparse};
 }
 
-#define PKV_SMEM_CASE(D, G) \
-  if (head_dim == D && group == G) per_warp = warp_smem_bytes<D, G>();
-
-size_t decode_smem_bytes(int head_dim, int group, int batch) {
+size_t decode_smem_bytes(int head_dim, bool sparse, int batch) {
   size_t per_warp = 0;
-  PKV_SMEM_CASE(128, 1) PKV_SMEM_CASE(128, 2) PKV_SMEM_CASE(128, 4) PKV_SMEM_CASE(128, 6)
-  PKV_SMEM_CASE(128, 8) PKV_SMEM_CASE(64, 1) PKV_SMEM_CASE(64, 2) PKV_SMEM_CASE(64, 4)
-  PKV_SMEM_CASE(64, 6) PKV_SMEM_CASE(64, 8)
+  if (head_dim == 128) per_warp = sparse ? sizeof(WarpSmem<128, true>) : sizeof(WarpSmem<128, false>);
+  if (head_dim == 64) per_warp = sparse ? sizeof(WarpSmem<64, true>) : sizeof(WarpSmem<64, false>);
   if (per_warp == 0) return 0;
-  return per_warp * kDecodeWarps + sizeof(int32_t) * (5 * (size_t)batch + 1);
+  // + 1 KiB so the tiles can start on a 1 KiB boundary
+  return 1024 + per_warp * kDecodeWarps + sizeof(int32_t) * (5 * (size_t)batch + 1);
 }
 
 cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, size_t smem,
                           cudaStream_t stream) {
   DecodeArgs args = a;
+  args.G = k.group;
   void* split_params[] = {&args};
-  cudaError_t e = cudaLaunchKernel(k.split, dim3(grid), dim3(kDecodeWarps * 32), split_params, smem, stream);
+  cudaError_t e = launch_pdl(k.split, dim3(grid), dim3(kDecodeWarps * 32), smem, stream, split_params);
   if (e != cudaSuccess) return e;
   int group = k.group;
   void* merge_params[] = {&args, &group};
   const int rows = a.B * a.Hq;
   const int mgrid = (rows + kMergeWarps - 1) / kMergeWarps;
   if (mgrid == 0) return cudaSuccess;
-  return cudaLaunchKernel(k.merge, dim3(mgrid), dim3(kMergeWarps * 32), merge_params, 0, stream);
+  return launch_pdl(k.merge, dim3(mgrid), dim3(kMergeWarps * 32), 0, stream, merge_params);
 }
 
 }  // namespace pkv

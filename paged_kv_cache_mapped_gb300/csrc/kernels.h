@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -14,6 +15,8 @@ namespace pkv {
 // Split-K decode: every consumer warp of the grid is an independent worker that owns a
 // contiguous range of the flattened (sequence, kv head, 16-token unit) list.
 struct DecodeArgs {
+  CUtensorMap tmap_k;            // dense mode: the K pool as a 2-D [NB*Hkv*16, D] bf16 tensor,
+  CUtensorMap tmap_v;            //   box 64 x 16, 128-byte swizzle (likewise V)
   const __nv_bfloat16* q;        // [B, Hq, D]
   const __nv_bfloat16* k_cache;  // [NB, Hkv, 16, D]
   const __nv_bfloat16* v_cache;
@@ -21,19 +24,36 @@ struct DecodeArgs {
   const int32_t* context_lens;   // [B]
   const int32_t* kept;           // [B, Hkv, max_kept] (sparse mode)
   const int32_t* kept_lens;      // [B]               (sparse mode)
+  const __nv_bfloat16* k_new;    // [B, Hkv, D] this step's token (dense append mode) or nullptr
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_pool_out;     // the pools again, writable (append mode)
+  __nv_bfloat16* v_pool_out;
   __nv_bfloat16* out;            // [B, Hq, D]
   int32_t* layout;               // [2 + (B+1) + B]: total units, units per warp, unit start, units per kv head
   float2* part_ml;               // [B*Hq, max_parts] (running max in log2 units, running sum)
   float* part_o;                 // [B*Hq, max_parts, D] unnormalised partial outputs
   int32_t* err;                  // device error word or nullptr
   int B, Hq, Hkv, NB, MB, max_kept, window, max_parts, min_units;
+  int G;                         // query heads per kv head (1..kMaxGroup)
   float scale_log2;              // scale * log2(e): logits are kept in base-2 units
   unsigned long long timeout_ns; // bound of every mbarrier wait
 };
 
-constexpr int kDecodeWarps = 4;      // worker warps per CTA
+// Tuning knobs (compile-time; every setting computes the same result).
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 2
+#endif
+#ifndef PKV_RING_D128
+#define PKV_RING_D128 2  // K/V tile pairs in flight per worker warp at head_dim 128
+#endif
+#ifndef PKV_RING_D64
+#define PKV_RING_D64 4
+#endif
+
+constexpr int kDecodeWarps = PKV_DECODE_WARPS;  // worker warps per CTA
 constexpr int kMinUnitsPerWarp = 16; // lower bound of a worker's range (bounds partial count)
 constexpr int kMergeWarps = 8;
+constexpr int kMaxGroup = 8;         // query heads per kv head handled by one fragment
 
 // Dynamic shared memory and kernel handles of one (head_dim, group, sparse) instantiation.
 struct DecodeKernel {
@@ -45,7 +65,7 @@ struct DecodeKernel {
 
 // Returns nullptr-filled struct (split == nullptr) when the combination is unsupported.
 DecodeKernel decode_kernel(int head_dim, int group, bool sparse);
-size_t decode_smem_bytes(int head_dim, int group, int batch);
+size_t decode_smem_bytes(int head_dim, bool sparse, int batch);
 cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, size_t smem,
                           cudaStream_t stream);
 
@@ -62,12 +82,30 @@ cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const 
                                int stride, const int32_t* lens, int B, int Hkv, int n_sink,
                                int n_recent, int k_top, int32_t* err, cudaStream_t stream);
 
+// Launches `kernel` with programmatic stream serialisation (it may start before the previous
+// kernel on the stream ends; every kernel of this library waits for it before touching
+// global memory).
+inline cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kernel, args);
+}
+
 // Validates a paged (sparse == false) or sparse decode call, sizes its partition and
 // launches it with `workspace` as scratch.  Defined in api.cu; returns a PKV status.
 int decode_common(void* out, const void* q, const void* k_cache, const void* v_cache,
                   const int32_t* block_tables, const int32_t* context_lens, const int32_t* kept,
                   const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
                   void* workspace, size_t workspace_bytes, const struct pkv_dims* dims, int32_t* err,
-                  void* stream, bool sparse);
+                  void* stream, bool sparse, const void* k_new = nullptr, const void* v_new = nullptr);
 
 }  // namespace pkv

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(__nv_bfloat16* __restric
                                                         int32_t* err) {
   const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  grid_dependency_wait();  // programmatic launch: the previous kernel may still read the pool
+  grid_launch_dependents();
   if (item >= T * Hkv) return;
   const int64_t tok = item / Hkv;
   const int g = (int)(item - tok * Hkv);
@@ -58,6 +60,8 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
     int Hkv, int sNB, int sMB, int32_t* err) {
   const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  grid_dependency_wait();
+  grid_launch_dependents();
   if (item >= (int64_t)B * Hkv * max_kept) return;
   const int j = (int)(item % max_kept);
   const int64_t bg = item / max_kept;
@@ -136,6 +140,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   __shared__ int warp_sums[kSelWarps];
   __shared__ int s_digit, s_need;
 
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int pair = blockIdx.x;
   const int b = pair / Hkv;
   const int g = pair - b * Hkv;
@@ -227,9 +233,9 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const 
   auto* vc = static_cast<__nv_bfloat16*>(v_cache);
   auto* kk = static_cast<const __nv_bfloat16*>(k);
   auto* vv = static_cast<const __nv_bfloat16*>(v);
-  if (D == 128) kv_append_kernel<128><<<grid, 256, 0, stream>>>(kc, vc, kk, vv, slots, T, Hkv, NB, err);
-  else kv_append_kernel<64><<<grid, 256, 0, stream>>>(kc, vc, kk, vv, slots, T, Hkv, NB, err);
-  return cudaGetLastError();
+  void* args[] = {&kc, &vc, &kk, &vv, &slots, &T, &Hkv, &NB, &err};
+  const void* fn = D == 128 ? (const void*)kv_append_kernel<128> : (const void*)kv_append_kernel<64>;
+  return launch_pdl(fn, dim3(grid), dim3(256), 0, stream, args);
 }
 
 cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, int dMB,
@@ -244,13 +250,10 @@ cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, i
   auto* c = static_cast<__nv_bfloat16*>(dv);
   auto* s1 = static_cast<const __nv_bfloat16*>(sk);
   auto* s2 = static_cast<const __nv_bfloat16*>(sv);
-  if (D == 128)
-    kv_compact_kernel<128><<<grid, 256, 0, stream>>>(a, c, dbt, dNB, dMB, s1, s2, sbt, lens, kept,
-                                                     kept_lens, max_kept, B, Hkv, sNB, sMB, err);
-  else
-    kv_compact_kernel<64><<<grid, 256, 0, stream>>>(a, c, dbt, dNB, dMB, s1, s2, sbt, lens, kept,
-                                                    kept_lens, max_kept, B, Hkv, sNB, sMB, err);
-  return cudaGetLastError();
+  void* args[] = {&a, &c, &dbt, &dNB, &dMB, &s1, &s2, &sbt, &lens, &kept, &kept_lens,
+                  &max_kept, &B, &Hkv, &sNB, &sMB, &err};
+  const void* fn = D == 128 ? (const void*)kv_compact_kernel<128> : (const void*)kv_compact_kernel<64>;
+  return launch_pdl(fn, dim3(grid), dim3(256), 0, stream, args);
 }
 
 cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* scores,
@@ -258,9 +261,9 @@ cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const 
                                int n_recent, int k_top, int32_t* err, cudaStream_t stream) {
   const int pairs = B * Hkv;
   if (pairs == 0) return cudaSuccess;
-  select_topk_kernel<<<pairs, kSelThreads, 0, stream>>>(kept_out, kept_lens_out, scores, stride,
-                                                         lens, Hkv, n_sink, n_recent, k_top, err);
-  return cudaGetLastError();
+  void* args[] = {&kept_out, &kept_lens_out, &scores, &stride, &lens, &Hkv, &n_sink, &n_recent,
+                  &k_top, &err};
+  return launch_pdl((const void*)select_topk_kernel, dim3(pairs), dim3(kSelThreads), 0, stream, args);
 }
 
 }  // namespace pkv

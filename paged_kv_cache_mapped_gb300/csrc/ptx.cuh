@@ -81,6 +81,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       : "memory");
 }
 
+// TMA tiled copy of one box of a 2-D tensor map (coordinates in elements: x innermost, a
+// multiple of 16 bytes; y rows) into shared memory; completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst_smem, const void* tmap, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // Orders this thread's earlier generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses to shared memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -124,6 +135,64 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
 // upper half of a binary32, so widening is a shift / mask (exact).
 __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
   return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// ------------------------------------------------------------- warp-level tensor-core ops
+
+// Four 8x8 b16 matrices from shared memory; lanes 8i..8i+7 give the row addresses of matrix
+// i.  Lane l receives row l/4, elements 2(l%4) and 2(l%4)+1 of each matrix (or, with .trans,
+// of each matrix's transpose).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// d += a * b for a 16x16 bf16 A (row-major fragment), a 16x8 bf16 B (column fragment) and
+// a 16x8 fp32 accumulator; products are exact and sums are fp32.
+__device__ __forceinline__ void mma_bf16_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                  uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 b16 matrix held one row pair per lane (the ldmatrix fragment layout).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Two fp32 -> packed bf16x2, round-to-nearest-even; `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialisation
+// may start while the previous kernel on its stream is still running; it must call
+// grid_dependency_wait() before touching global memory that kernel may produce or read.
+// grid_launch_dependents() lets the next such kernel start early (it will wait in turn).
+// Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void record_error(int32_t* err, int32_t code) {

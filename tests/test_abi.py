@@ -21,7 +21,7 @@ def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _lib.header_functions()
-    assert len(declared) == 11
+    assert len(declared) == 12
     nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     for name in declared:
@@ -68,7 +68,7 @@ def test_host_validation_codes(lib):
     assert _decode(lib, _dims(bs=8)) == c["PKV_ERR_BLOCK_SIZE"]
     assert _decode(lib, _dims(d=80)) == c["PKV_ERR_HEAD_DIM"]
     assert _decode(lib, _dims(hq=12, hkv=8)) == c["PKV_ERR_GQA"]
-    assert _decode(lib, _dims(hq=24, hkv=8)) == c["PKV_ERR_GQA"]      # G = 3 is not built
+    assert _decode(lib, _dims(hq=32, hkv=2)) == c["PKV_ERR_GQA"]      # G = 16 exceeds one fragment
     assert _decode(lib, _dims(B=-1)) == c["PKV_ERR_DIMS"]
     assert _decode(lib, _dims(), ptr=0x10004) == c["PKV_ERR_ALIGNMENT"]
     assert _decode(lib, _dims(), ws_bytes=16) == c["PKV_ERR_WORKSPACE"]

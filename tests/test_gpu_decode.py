@@ -191,3 +191,47 @@ def test_long128k_full_size_sampled():
     out_w = _run(case, window=4096)
     ref_w = _oracle_rows(case, rows, window=4096)
     assert_attn_close(out_w.view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)], ref_w, "long128k w=4096")
+
+
+@pytest.mark.parametrize("window", [0, 5])
+def test_fused_append_decode_small_ragged(window):
+    """paged_decode_attention_append == kv_append at position L-1 then paged decode (oracle)."""
+    lens = [1, 15, 16, 17, 33, 100, 257]
+    for d, hq, hkv in ((128, 8, 2), (64, 6, 3)):
+        case = _small_case(lens, hq=hq, hkv=hkv, d=d, seed=31 + d, fill=float("nan"))
+        g = torch.Generator().manual_seed(32)
+        k_new = rand_bf16((len(lens), hkv, d), g)
+        v_new = rand_bf16((len(lens), hkv, d), g)
+        bt = case["block_tables"].cpu()
+        slots = np.array([int(bt[b, (L - 1) // 16]) * 16 + (L - 1) % 16 for b, L in enumerate(lens)],
+                         dtype=np.int64)
+        okc, ovc = oracle.kv_append(bits(case["k_cache"]), bits(case["v_cache"]), bits(k_new), bits(v_new),
+                                    slots)
+        err = pkv.new_error_word(DEV)
+        out = pkv.paged_decode_attention_append(case["q"], case["k_cache"], case["v_cache"], k_new.to(DEV),
+                                                v_new.to(DEV), case["block_tables"], case["context_lens"],
+                                                case["scale"], window, error_word=err)
+        torch.cuda.synchronize()
+        assert pkv.read_error(err) == 0
+        assert np.array_equal(bits(case["k_cache"]), okc) and np.array_equal(bits(case["v_cache"]), ovc)
+        ref = _oracle_rows(case, None, okc, ovc, window=window)
+        assert_attn_close(out, ref, f"fused append d={d} w={window}")
+
+
+def test_fused_append_decode_llama8b_full_size():
+    wl = W.WORKLOADS["llama8b"]
+    case = W.make_layer(wl, device=DEV, device_rng=True)
+    kc0, vc0 = bits(case["k_cache"]), bits(case["v_cache"])
+    err = pkv.new_error_word(DEV)
+    out = pkv.paged_decode_attention_append(case["q"], case["k_cache"], case["v_cache"], case["k_new"],
+                                            case["v_new"], case["block_tables"], case["context_lens"],
+                                            case["scale"], error_word=err)
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    okc, ovc = oracle.kv_append(kc0, vc0, bits(case["k_new"]), bits(case["v_new"]),
+                                case["slot_mapping"].cpu().numpy())
+    assert np.array_equal(bits(case["k_cache"]), okc) and np.array_equal(bits(case["v_cache"]), ovc)
+    rows = _sample_rows(wl.batch, wl.num_q_heads, 64, 12)
+    ref = _oracle_rows(case, rows, okc, ovc)
+    got = out.view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)]
+    assert_attn_close(got, ref, "llama8b fused append sampled rows")

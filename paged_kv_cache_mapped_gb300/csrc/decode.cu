@@ -597,7 +597,7 @@ decode_merge_kernel(const DecodeArgs a, int group) {
   for (int e = 0; e < EPW; ++e) acc[e] = 0.f;
   for (int p0 = 0; p0 < np; p0 += 32) {
     const int n = min(32, np - p0);
-    const float2 mlp = lane < n ? ml[p0 + lane] : make_float2(-INFINITY, 0.f);
+    const float2 mlp = lane < n ? __ldcg(ml + p0 + lane) : make_float2(-INFINITY, 0.f);
     float gmax = mlp.x;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(kFullMask, gmax, o));
@@ -613,16 +613,29 @@ decode_merge_kernel(const DecodeArgs a, int group) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFullMask, lsum, o);
     L += lsum;
-#pragma unroll 8
-    for (int p = 0; p < n; ++p) {
-      const float w = __shfl_sync(kFullMask, w_lane, p);
-      const float* src = po + (size_t)(p0 + p) * D;
-      if constexpr (EPW == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * x.x; acc[1] += w * x.y;
+    // batches of 8 partials: all loads of a batch are issued before any is used
+    for (int pb = 0; pb < n; pb += 8) {
+      float x[8][EPW];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (pb + j < n) {
+          const float* src = po + (size_t)(p0 + pb + j) * D;
+          if constexpr (EPW == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+            x[j][0] = v.x; x[j][1] = v.y; x[j][2] = v.z; x[j][3] = v.w;
+          } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+            x[j][0] = v.x; x[j][1] = v.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = __shfl_sync(kFullMask, w_lane, (pb + j) & 31);
+        if (pb + j < n) {
+#pragma unroll
+          for (int e = 0; e < EPW; ++e) acc[e] += w * x[j][e];
+        }
       }
     }
   }

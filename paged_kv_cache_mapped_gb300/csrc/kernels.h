@@ -41,7 +41,7 @@ struct DecodeArgs {
 
 // Tuning knobs (compile-time; every setting computes the same result).
 #ifndef PKV_DECODE_WARPS
-#define PKV_DECODE_WARPS 2
+#define PKV_DECODE_WARPS 1
 #endif
 #ifndef PKV_RING_D128
 #define PKV_RING_D128 2  // K/V tile pairs in flight per worker warp at head_dim 128

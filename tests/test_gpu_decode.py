@@ -101,7 +101,7 @@ def test_single_token_exact_and_equal_rows():
 
 def test_deterministic_and_workspace_reuse():
     case = _small_case([700, 33, 1500], hq=8, hkv=2, d=128, seed=7)
-    ws = torch.empty(pkv.decode_workspace_bytes(3, 8, 2, 128, case["k_cache"].shape[0],
+    ws = torch.zeros(pkv.decode_workspace_bytes(3, 8, 2, 128, case["k_cache"].shape[0],
                                                 case["block_tables"].shape[1]),
                      dtype=torch.uint8, device=DEV)
     a = pkv.paged_decode_attention(case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
@@ -235,3 +235,21 @@ def test_fused_append_decode_llama8b_full_size():
     ref = _oracle_rows(case, rows, okc, ovc)
     got = out.view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)]
     assert_attn_close(got, ref, "llama8b fused append sampled rows")
+
+
+def test_workspace_reused_across_shapes():
+    """One zero-filled workspace serves calls of different batch sizes and head counts in turn
+    (the per-segment arrival counters live in a fixed region partials never overwrite)."""
+    cases = [_small_case([700, 33, 1500], hq=8, hkv=2, d=128, seed=41),
+             _small_case([90] * 16, hq=16, hkv=4, d=128, seed=42),
+             _small_case([5000, 1, 2500, 17], hq=32, hkv=8, d=128, seed=43),
+             _small_case([700, 33, 1500], hq=8, hkv=2, d=128, seed=41)]
+    need = max(pkv.decode_workspace_bytes(c["q"].shape[0], c["q"].shape[1], c["k_cache"].shape[1], 128,
+                                          c["k_cache"].shape[0], c["block_tables"].shape[1]) for c in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for i, c in enumerate(cases):
+        for _ in range(2):
+            out = pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                             c["context_lens"], c["scale"], workspace=ws)
+            torch.cuda.synchronize()
+            assert_attn_close(out, _oracle_rows(c, None), f"shape {i}")

@@ -52,7 +52,7 @@ def _dist():
     if ws > 1:
         import torch.distributed as dist
         if not dist.is_initialized():
-            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            backend = os.environ.get("PKV_DIST_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
             dist.init_process_group(backend=backend)
         return dist, dist.get_rank(), ws
     return None, 0, 1
@@ -117,6 +117,33 @@ class ClockSampler:
         reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(self.samples)}
+
+
+KERNEL_SOURCES = ("paged_kv_cache_mapped_gb300/csrc/decode.cu", "paged_kv_cache_mapped_gb300/csrc/kernels.h",
+                  "paged_kv_cache_mapped_gb300/csrc/ptx.cuh")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if it is missing or the
+    decode kernel's sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{name}_counters.txt")  # JSON text
+    try:
+        with open(path) as f:
+            p = json.load(f)
+    except Exception:
+        return None
+    if p.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return p.get("dram_bytes_per_launch")
 
 
 def kv_bytes(lens: torch.Tensor, hkv: int, d: int, window: int = 0) -> int:
@@ -244,7 +271,9 @@ def run_ours(args):
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / hbm, 4),
-            "traffic": None,
+            "traffic": profiled_traffic("decode_split_llama8b"),
+            "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the split kernel "
+                            "(profiles/decode_split_llama8b.md); the merge kernel adds the partials",
             "algorithmic_bytes_per_launch": bytes_dec,
             "launch_ms": round(dec_ms, 5),
         },
@@ -347,6 +376,119 @@ def run_secondary(pkv, W, dev, stream, args):
                               "l2": "2.1 GB of K/V per launch (> L2)"}
     del c, ws, out
     torch.cuda.empty_cache()
+    res["qwen1p5b_step"] = _qwen_step(pkv, W, dev, stream, args, hbm)
+    torch.cuda.empty_cache()
+    res.update(_sparse_step(pkv, W, dev, stream, args, hbm))
+    torch.cuda.empty_cache()
+    return res
+
+
+def _graph_time(calls, warmup, steps, dev, stream):
+    """Capture `calls` (a list of no-arg launchers) into one CUDA graph; time its replays."""
+    for f in calls:
+        f()
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for f in calls:
+            f()
+    return _time(g.replay, warmup, steps, dev, stream)
+
+
+def _qwen_step(pkv, W, dev, stream, args, hbm):
+    """Qwen2.5-1.5B-shaped decode step: 28 layers, each with its own pool, append + decode per
+    layer, the 28 calls replayed as one CUDA graph."""
+    wl = W.WORKLOADS["qwen1p5b"]
+    lens = W.context_lengths(wl)
+    layers = [W.make_layer(wl, layer=l, device=dev, device_rng=True) for l in range(wl.layers)]
+    need = max(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                          c["num_blocks"], c["max_blocks_per_seq"]) for c in layers)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(layers[0]["q"])
+    gstream = torch.cuda.Stream(dev)
+
+    def call(c):
+        return lambda: pkv.paged_decode_attention_append(
+            c["q"], c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["block_tables"],
+            c["context_lens"], c["scale"], out=out, workspace=ws, stream=torch.cuda.current_stream(dev))
+    with torch.cuda.stream(gstream):
+        ms = _graph_time([call(c) for c in layers], args.warmup, max(5, args.steps // 20), dev, gstream)
+    nbytes = wl.layers * (decode_bytes(lens, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
+                          + 2 * wl.batch * wl.num_kv_heads * wl.head_dim * 2 * 2)
+    del layers
+    return {"ms": round(ms, 4), "tokens_per_s": round(wl.batch / (ms * 1e-3), 1),
+            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+            "layers": wl.layers, "launch": "28 fused append+decode calls in one CUDA graph",
+            "l2": f"{wl.layers} separate pools, {nbytes / 1e9:.2f} GB per step (> L2)"}
+
+
+def _sparse_step(pkv, W, dev, stream, args, hbm):
+    """Layer-wise sparse decode step (B16 x 16384, 32 layers): layers 0-3 paged decode over the
+    full cache, layers 4-31 paged decode over compacted pools of 1540 kept tokens, replayed as
+    one CUDA graph; plus one sparse layer's selection, compaction and gather-decode."""
+    wl = W.WORKLOADS["sparse"]
+    lens = W.context_lengths(wl)
+    B, hq, hkv, d, K = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.keep_max
+    full = [W.make_layer(wl, layer=l, device=dev, device_rng=True) for l in range(wl.full_layers)]
+    dbt_cpu, dnb = W.compact_tables(K, B, seed=5)
+    dbt = dbt_cpu.to(dev)
+    klens = torch.full((B,), K, dtype=torch.int32, device=dev)
+    comp = []
+    for l in range(wl.full_layers, wl.layers):
+        g = torch.Generator(device=dev).manual_seed(W.layer_seed(wl, l))
+        pool = lambda: torch.randn((dnb, hkv, 16, d), generator=g, device=dev).to(torch.bfloat16)
+        comp.append({"q": torch.randn((B, hq, d), generator=g, device=dev).to(torch.bfloat16),
+                     "k_cache": pool(), "v_cache": pool()})
+    need = max(pkv.decode_workspace_bytes(B, hq, hkv, d, c["num_blocks"], c["max_blocks_per_seq"]) for c in full)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=dev)
+    gstream = torch.cuda.Stream(dev)
+
+    def full_call(c):
+        return lambda: pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                                  c["context_lens"], c["scale"], out=out, workspace=ws,
+                                                  stream=torch.cuda.current_stream(dev))
+
+    def comp_call(c):
+        return lambda: pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], dbt, klens, wl.scale,
+                                                  out=out, workspace=ws, stream=torch.cuda.current_stream(dev))
+    with torch.cuda.stream(gstream):
+        ms = _graph_time([full_call(c) for c in full] + [comp_call(c) for c in comp], args.warmup,
+                         max(5, args.steps // 20), dev, gstream)
+    full_bytes = decode_bytes(lens, B, hq, hkv, d)
+    sparse_bytes = decode_bytes(torch.full((B,), K, dtype=torch.int32), B, hq, hkv, d)
+    nbytes = wl.full_layers * full_bytes + (wl.layers - wl.full_layers) * sparse_bytes
+    res = {"sparse_step": {"ms": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+                           "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                           "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                           "launch": "32 decode calls in one CUDA graph (4 full, 28 over compacted pools)",
+                           "dense_equivalent_gb": round(wl.layers * full_bytes / 1e9, 2)}}
+    # one sparse layer: select -> compact, and gather decode over the full pool
+    src = full[0]
+    scores = W.make_scores(wl, wl.full_layers, lens, device=dev, device_rng=True)
+    kept = torch.empty((B, hkv, K), dtype=torch.int32, device=dev)
+    kl = torch.empty((B,), dtype=torch.int32, device=dev)
+    sel = lambda: pkv.kv_select_topk(scores, src["context_lens"], wl.n_sink, wl.n_recent, wl.k_top,
+                                     kept_out=kept, kept_lens_out=kl, stream=stream)
+    ms_sel = _time(sel, args.warmup, 20, dev, stream)
+    dk, dv = comp[0]["k_cache"], comp[0]["v_cache"]
+    cmp = lambda: pkv.kv_compact(dk, dv, dbt, src["k_cache"], src["v_cache"], src["block_tables"],
+                                 src["context_lens"], kept, kl, stream=stream)
+    ms_cmp = _time(cmp, args.warmup, 20, dev, stream)
+    ws_s = torch.zeros(pkv.sparse_decode_workspace_bytes(B, hq, hkv, d, src["num_blocks"],
+                                                         src["max_blocks_per_seq"], K),
+                       dtype=torch.uint8, device=dev)
+    gat = lambda: pkv.sparse_decode_attention(src["q"], src["k_cache"], src["v_cache"], src["block_tables"],
+                                              src["context_lens"], kept, kl, wl.scale, out=out,
+                                              workspace=ws_s, stream=stream)
+    ms_gat = _time(gat, args.warmup, 20, dev, stream)
+    sel_bytes = int(scores.numel()) * 4 + B * hkv * K * 4
+    cmp_bytes = B * hkv * K * d * 2 * 2 * 2
+    res["sparse_layer_select_topk"] = {"ms": round(ms_sel, 4), "gbs": round(sel_bytes / (ms_sel * 1e-3) / 1e9, 1)}
+    res["sparse_layer_compact"] = {"ms": round(ms_cmp, 4), "gbs": round(cmp_bytes / (ms_cmp * 1e-3) / 1e9, 1)}
+    res["sparse_layer_gather_decode"] = {"ms": round(ms_gat, 4),
+                                         "gbs": round(sparse_bytes / (ms_gat * 1e-3) / 1e9, 1)}
+    del full, comp, scores
     return res
 
 

@@ -64,6 +64,14 @@ const DeviceInfo* device_info(int* status) {
         }
       }
     }
+    {
+      const cudaError_t e = kvops_device_setup();
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        *status = PKV_ERR_CUDA_BASE + (int)e;
+        return nullptr;
+      }
+    }
     info.sm_count = sms;
     info.max_smem_optin = (size_t)optin;
     info.ready = true;

@@ -69,7 +69,9 @@ size_t decode_smem_bytes(int head_dim, bool sparse, int batch);
 cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, size_t smem,
                           cudaStream_t stream);
 
-// kv append / compaction / top-k selection.
+// kv append / compaction / top-k selection.  kvops_device_setup() sets the kernels'
+// attributes on the current device (called once per device by the C ABI).
+cudaError_t kvops_device_setup();
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
                              const int64_t* slots, int64_t T, int Hkv, int D, int NB,
                              int32_t* err, cudaStream_t stream);

@@ -93,51 +93,67 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
 
 // ---------------------------------------------------------------------------- top-k select
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelSmemKeys = 40960;  // candidates cached in shared memory (160 KiB)
 
 // Order-preserving map of an fp32 score to uint32: a larger key is a larger score.  -0.0
-// is folded onto +0.0 first so the two compare equal, as the selection rule requires.
+// is folded onto +0.0 first so the two compare equal, as the selection rule requires; NaN
+// (invalid input, reported) maps to the smallest key.
 __device__ __forceinline__ uint32_t score_key(float s) {
+  if (s != s) return 0u;
   uint32_t u = __float_as_uint(s);
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive scan of one flag per thread; returns the exclusive prefix and sets
-// *total.  Uses `warp_sums` (kSelWarps ints) in shared memory.
-__device__ __forceinline__ int block_exclusive_scan(int flag, int* warp_sums, int* total) {
+// Block-wide exclusive scan of one int per thread; returns the prefix, sets *total.
+// `warp_sums` holds kSelWarps ints of shared memory.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const unsigned ballot = __ballot_sync(kFullMask, flag);
-  const int in_warp = __popc(ballot & ((1u << lane) - 1u));
-  if (lane == 0) warp_sums[warp] = __popc(ballot);
-  __syncthreads();
-  int before = 0, sum = 0;
+  int incl = v;
 #pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) {
-    const int c = warp_sums[w];
-    before += (w < warp) ? c : 0;
-    sum += c;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < kSelWarps ? warp_sums[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFullMask, wi, o);
+      if (lane >= o) wi += t;
+    }
+    if (lane < kSelWarps) warp_sums[lane] = wi - w;  // exclusive prefix of the warp totals
+    if (lane == 31) warp_sums[kSelWarps] = wi;
   }
   __syncthreads();
-  *total = sum;
-  return before + in_warp;
+  const int result = warp_sums[warp] + incl - v;
+  *total = warp_sums[kSelWarps];
+  __syncthreads();
+  return result;
 }
 
 // Kept-token selection for one (sequence, kv head) per CTA ("How KV Sparsity...": sections
 // "System model" -- drop low-score KV, retain high-score and recent KV -- and "2. Attention
 // modification" -- per layer and head, the top-k tokens by accumulated score; sink tokens
 // from its introduction).  The k_top-th largest key among the candidates is found by an
-// MSD radix select (4 passes of 8 bits over a 256-bin histogram); candidates above it are
-// kept, and of those equal to it the lowest positions fill the remainder.  The kept list
-// is emitted in ascending position order by block-wide scans, so the result is exact.
+// MSD radix select (4 passes of 8 bits over a 256-bin histogram, the keys cached in shared
+// memory when they fit); candidates above it are kept, and of those equal to it the lowest
+// positions fill the remainder.  One ordered pass (each thread a contiguous run of
+// candidates, two block scans) writes the kept list in ascending position, so the result is
+// exact and unique.
 __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     int32_t* __restrict__ kept_out, int32_t* __restrict__ kept_lens_out,
     const float* __restrict__ scores, int stride, const int32_t* __restrict__ lens, int Hkv,
     int n_sink, int n_recent, int k_top, int32_t* err) {
+  extern __shared__ uint32_t s_keys[];  // kSelSmemKeys when the candidates fit
   __shared__ int hist[256];
-  __shared__ int warp_sums[kSelWarps];
+  __shared__ int warp_sums[kSelWarps + 1];
   __shared__ int s_digit, s_need;
 
   grid_dependency_wait();
@@ -159,7 +175,28 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   }
   const float* row = scores + (size_t)pair * stride;
   const int first = n_sink;
-  const int last = L - n_recent;  // candidates [first, last)
+  const int n = L - n_recent - n_sink;  // candidates: positions first .. first + n - 1
+  if (k_top == 0) {  // no candidate is kept: sinks and the recent window only
+    for (int t = threadIdx.x; t < n_sink; t += blockDim.x) out[t] = t;
+    for (int t = threadIdx.x; t < n_recent; t += blockDim.x) out[n_sink + t] = first + n + t;
+    return;
+  }
+  const bool cached = n <= kSelSmemKeys;
+  const int lane = threadIdx.x & 31;
+
+  bool nan_seen = false;
+  if (cached) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const float v = __ldg(row + first + i);
+      nan_seen |= (v != v);
+      s_keys[i] = score_key(v);
+    }
+  } else {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) nan_seen |= (__ldg(row + first + i) != __ldg(row + first + i));
+  }
+  if (nan_seen) record_error(err, PKV_DEV_BAD_SCORE);
+  __syncthreads();
+  auto key_at = [&](int i) -> uint32_t { return cached ? s_keys[i] : score_key(__ldg(row + first + i)); };
 
   uint32_t prefix = 0u;
   int need = k_top;
@@ -168,60 +205,82 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     const uint32_t hi_mask = pass == 0 ? 0u : (0xffffffffu << (shift + 8));
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int c = first + threadIdx.x; c < last; c += blockDim.x) {
-      const float s = __ldg(row + c);
-      if (pass == 0 && s != s) record_error(err, PKV_DEV_BAD_SCORE);
-      const uint32_t key = (s != s) ? 0u : score_key(s);
-      if ((key & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(key >> shift) & 0xffu], 1);
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int i = base + threadIdx.x;
+      const uint32_t key = i < n ? key_at(i) : 0u;
+      const bool hit = i < n && (key & hi_mask) == (prefix & hi_mask);
+      const int digit = hit ? (int)((key >> shift) & 0xffu) : -1;
+      // warp-aggregated increment: one atomic per distinct digit in the warp
+      const unsigned peers = __match_any_sync(kFullMask, digit);
+      if (hit && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      // The digit d holding the need-th largest key: count(> d) < need <= count(>= d).
-      int cum = 0;
-      int digit = 0;
-      for (int d = 255; d >= 0; --d) {
-        const int c = hist[d];
-        if (cum + c >= need) {
-          digit = d;
-          break;
-        }
-        cum += c;
+    if (threadIdx.x < 32) {
+      // the digit d holding the need-th largest key: count(> d) < need <= count(>= d).
+      // Lane l owns bins [8l, 8l + 8); suffix sums over lanes from the top.
+      int c[8], own = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[8 * lane + j];
+        own += c[j];
       }
-      s_digit = digit;
-      s_need = need - cum;
+      int suffix = own;  // sum over lanes >= lane
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(kFullMask, suffix, o);
+        if (lane + o < 32) suffix += t;
+      }
+      const int above = suffix - own;  // keys in bins owned by higher lanes
+      if (above < need && need <= suffix) {
+        int cum = above;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+          if (cum + c[j] >= need) {
+            s_digit = 8 * lane + j;
+            s_need = need - cum;
+            break;
+          }
+          cum += c[j];
+        }
+      }
     }
     __syncthreads();
     prefix |= (uint32_t)s_digit << shift;
     need = s_need;
-    __syncthreads();
   }
-  // prefix is the key of the k_top-th best candidate; `need` of the candidates equal to it
-  // are kept, the lowest positions first.
-  const uint32_t thr = prefix;
+  const uint32_t thr = prefix;  // key of the k_top-th best candidate
+
+  // Ordered pass: thread t owns candidates [t*C, t*C + C) (C odd: conflict-free smem reads).
+  int C = (n + blockDim.x - 1) / blockDim.x;
+  C |= 1;
+  const int c0 = min(n, (int)threadIdx.x * C);
+  const int c1 = min(n, c0 + C);
+  int gt = 0, eq = 0;
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t key = key_at(i);
+    gt += key > thr;
+    eq += key == thr;
+  }
+  int total;
+  const int eq_before = block_exclusive_scan(eq, warp_sums, &total);
+  const int eq_take = max(0, min(eq, need - eq_before));  // lowest positions among equal keys
+  const int pos = block_exclusive_scan(gt + eq_take, warp_sums, &total);
+  int w = n_sink + pos, eq_left = eq_take;
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t key = key_at(i);
+    if (key > thr || (key == thr && eq_left-- > 0)) out[w++] = first + i;
+  }
   for (int t = threadIdx.x; t < n_sink; t += blockDim.x) out[t] = t;
-  int eq_base = 0, sel_base = 0;
-  for (int base = first; base < last; base += blockDim.x) {
-    const int c = base + threadIdx.x;
-    uint32_t key = 0u;
-    if (c < last) {
-      const float s = __ldg(row + c);
-      key = (s != s) ? 0u : score_key(s);
-    }
-    const bool in = c < last;
-    const int eq = in && key == thr;
-    int eq_total;
-    const int eq_rank = eq_base + block_exclusive_scan(eq, warp_sums, &eq_total);
-    eq_base += eq_total;
-    const int sel = in && (key > thr || (eq && eq_rank < need));
-    int sel_total;
-    const int pos = sel_base + block_exclusive_scan(sel, warp_sums, &sel_total);
-    sel_base += sel_total;
-    if (sel) out[n_sink + pos] = c;
-  }
-  for (int t = threadIdx.x; t < n_recent; t += blockDim.x) out[n_sink + k_top + t] = last + t;
+  for (int t = threadIdx.x; t < n_recent; t += blockDim.x) out[n_sink + k_top + t] = first + n + t;
 }
 
 }  // namespace
+
+cudaError_t kvops_device_setup() {
+  // the selection's key cache needs more than the default 48 KiB of dynamic shared memory
+  return cudaFuncSetAttribute((const void*)select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSelSmemKeys * (int)sizeof(uint32_t));
+}
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
                              const int64_t* slots, int64_t T, int Hkv, int D, int NB,
@@ -263,7 +322,8 @@ cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const 
   if (pairs == 0) return cudaSuccess;
   void* args[] = {&kept_out, &kept_lens_out, &scores, &stride, &lens, &Hkv, &n_sink, &n_recent,
                   &k_top, &err};
-  return launch_pdl((const void*)select_topk_kernel, dim3(pairs), dim3(kSelThreads), 0, stream, args);
+  return launch_pdl((const void*)select_topk_kernel, dim3(pairs), dim3(kSelThreads),
+                    kSelSmemKeys * sizeof(uint32_t), stream, args);
 }
 
 }  // namespace pkv

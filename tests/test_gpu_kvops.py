@@ -186,3 +186,13 @@ def test_sparse_workload_layer_pipeline():
     idx = torch.tensor(rows, device=DEV)
     assert_attn_close(comp.view(-1, 128)[idx], ref, "sparse layer: compact pool")
     assert_attn_close(gath.view(-1, 128)[idx], ref, "sparse layer: gather")
+
+
+@pytest.mark.parametrize("k_top", [0, 7, 300])
+def test_topk_uncached_long_lists_and_zero_k(k_top):
+    """Candidates beyond the shared-memory key cache (n > 40960) and k_top = 0."""
+    g = torch.Generator().manual_seed(100 + k_top)
+    lens = torch.tensor([60000, 45000, 30000], dtype=torch.int32)
+    scores = torch.empty((3, 2, 60000)).exponential_(generator=g)
+    scores[0, 1, 1000:9000] = 4.0          # ties across the cut
+    _assert_same_selection(*_topk_both(scores, lens, 3, 64, k_top))

@@ -22,7 +22,7 @@ constexpr int kNumGroups = 1;
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
-  size_t max_smem_optin = 0;
+  size_t max_dyn_smem[2][2] = {};  // [head_dim index][sparse]: opt-in minus the kernel's static
 };
 
 std::mutex g_mutex;
@@ -55,12 +55,17 @@ const DeviceInfo* device_info(int* status) {
         for (int sp = 0; sp < 2; ++sp) {
           const DecodeKernel k = decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp != 0);
           if (k.split == nullptr) continue;
-          cudaError_t e = cudaFuncSetAttribute(k.split, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+          cudaFuncAttributes fa{};
+          cudaError_t e = cudaFuncGetAttributes(&fa, k.split);
+          const int dyn = optin - (int)fa.sharedSizeBytes;
+          if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k.split, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
           if (e != cudaSuccess) {
             cudaGetLastError();
             *status = PKV_ERR_CUDA_BASE + (int)e;
             return nullptr;
           }
+          info.max_dyn_smem[hd][sp] = (size_t)dyn;
         }
       }
     }
@@ -73,7 +78,6 @@ const DeviceInfo* device_info(int* status) {
       }
     }
     info.sm_count = sms;
-    info.max_smem_optin = (size_t)optin;
     info.ready = true;
   }
   *status = PKV_OK;
@@ -180,7 +184,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   const DeviceInfo* info = device_info(&st);
   if (!info) return st;
   const size_t smem = decode_smem_bytes(dims->head_dim, sparse, dims->batch);
-  if (smem > info->max_smem_optin) return PKV_ERR_DIMS;
+  if (smem > info->max_dyn_smem[head_dim_index(dims->head_dim)][sparse ? 1 : 0]) return PKV_ERR_DIMS;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.split, kDecodeWarps * 32, smem);
   if (e != cudaSuccess) return cuda_status(e);

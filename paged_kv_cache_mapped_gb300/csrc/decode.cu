@@ -76,9 +76,13 @@ __device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
 constexpr float kRescaleSlack = 8.0f;
 
 template <int D, bool SPARSE>
-struct WarpSmem {
+struct WarpTiles {
   alignas(1024) unsigned char k[Geo<D, SPARSE>::kRing][Geo<D, SPARSE>::kTile];
   alignas(1024) unsigned char v[Geo<D, SPARSE>::kRing][Geo<D, SPARSE>::kTile];
+};
+
+template <int D, bool SPARSE>
+struct WarpSlots {
   uint64_t bar_k[Geo<D, SPARSE>::kRing];  // K rows of the slot landed
   uint64_t bar_v[Geo<D, SPARSE>::kRing];  // V rows of the slot landed
   uint32_t meta[Geo<D, SPARSE>::kRing];   // rows of the unit that were copied (bit t = token t)
@@ -118,15 +122,20 @@ template <int D, bool SPARSE>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   using GE = Geo<D, SPARSE>;
-  using WS = WarpSmem<D, SPARSE>;
+  using WT = WarpTiles<D, SPARSE>;
+  using WB = WarpSlots<D, SPARSE>;
   constexpr int R = GE::kRing;
   constexpr int KS = GE::kKSteps;
 
-  extern __shared__ __align__(1024) unsigned char smem_dyn[];
-  // the swizzle pattern is a function of address bits 4-9: start the tiles on 1 KiB
-  unsigned char* smem_raw = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
-  auto* warps_smem = reinterpret_cast<WS*>(smem_raw);
-  int32_t* s_start = reinterpret_cast<int32_t*>(smem_raw + sizeof(WS) * kDecodeWarps);
+  // Tile rings in static shared memory: the toolchain honours the 1 KiB alignment the
+  // 128-byte swizzle pattern needs (it is a function of address bits 4-9).  The per-sequence
+  // arrays, sized by the batch, are dynamic.
+  static_assert((sizeof(WT) + sizeof(WB)) * kDecodeWarps <= 48 * 1024,
+                "tile rings exceed static shared memory");
+  __shared__ WT warps_tiles[kDecodeWarps];
+  __shared__ WB warps_slots[kDecodeWarps];
+  extern __shared__ __align__(16) int32_t smem_dyn[];
+  int32_t* s_start = smem_dyn;
   int32_t* s_nb = s_start + (a.B + 1);
   int32_t* s_first = s_nb + a.B;
   int32_t* s_lo = s_first + a.B;   // dense: first attended token; sparse: context length
@@ -137,12 +146,13 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   const int gq = lane >> 2;  // fragment row group
   const int tq = lane & 3;   // fragment column pair
   const int G = a.G;
-  WS& W = warps_smem[warp];
+  WT& Wt = warps_tiles[warp];  // this warp's K/V tile ring
+  WB& Wb = warps_slots[warp];  // its barriers and per-slot records
 
   if (lane == 0) {
     for (int s = 0; s < R; ++s) {
-      mbar_init(&W.bar_k[s], 1);
-      mbar_init(&W.bar_v[s], 1);
+      mbar_init(&Wb.bar_k[s], 1);
+      mbar_init(&Wb.bar_v[s], 1);
     }
     fence_mbar_init();
   }
@@ -269,21 +279,21 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       if (lane == 0) {
         if (phys >= 0 && phys < a.NB) {
           const int y = (phys * a.Hkv + ic.g) * 16;  // host checks NB*Hkv*16 < 2^31
-          W.meta[slot] = 0xffffu;
-          W.phys[slot] = phys;
-          mbar_arrive_expect_tx(&W.bar_k[slot], GE::kTile);
+          Wb.meta[slot] = 0xffffu;
+          Wb.phys[slot] = phys;
+          mbar_arrive_expect_tx(&Wb.bar_k[slot], GE::kTile);
 #pragma unroll
           for (int bx = 0; bx < GE::kBoxes; ++bx)
-            tma_load_2d(W.k[slot] + bx * 2048, &a.tmap_k, bx * 64, y, &W.bar_k[slot], pol);
-          mbar_arrive_expect_tx(&W.bar_v[slot], GE::kTile);
+            tma_load_2d(Wt.k[slot] + bx * 2048, &a.tmap_k, bx * 64, y, &Wb.bar_k[slot], pol);
+          mbar_arrive_expect_tx(&Wb.bar_v[slot], GE::kTile);
 #pragma unroll
           for (int bx = 0; bx < GE::kBoxes; ++bx)
-            tma_load_2d(W.v[slot] + bx * 2048, &a.tmap_v, bx * 64, y, &W.bar_v[slot], pol);
+            tma_load_2d(Wt.v[slot] + bx * 2048, &a.tmap_v, bx * 64, y, &Wb.bar_v[slot], pol);
         } else {
           record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
-          W.meta[slot] = 0u;
-          mbar_arrive_expect_tx(&W.bar_k[slot], 0);
-          mbar_arrive_expect_tx(&W.bar_v[slot], 0);
+          Wb.meta[slot] = 0u;
+          mbar_arrive_expect_tx(&Wb.bar_k[slot], 0);
+          mbar_arrive_expect_tx(&Wb.bar_v[slot], 0);
         }
       }
       advance(ic, s_nb, a.B, a.Hkv);
@@ -312,14 +322,14 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       src = (((size_t)phys * a.Hkv + ic.g) * 16 + (t & 15)) * D;
       const uint32_t vmask = __ballot_sync(kFullMask, ok) & 0xffffu;  // K and V lanes agree
       if (lane == 0) {
-        W.meta[slot] = vmask;
-        mbar_arrive_expect_tx(&W.bar_k[slot], __popc(vmask) * GE::kRow);
-        mbar_arrive_expect_tx(&W.bar_v[slot], __popc(vmask) * GE::kRow);
+        Wb.meta[slot] = vmask;
+        mbar_arrive_expect_tx(&Wb.bar_k[slot], __popc(vmask) * GE::kRow);
+        mbar_arrive_expect_tx(&Wb.bar_v[slot], __popc(vmask) * GE::kRow);
       }
       __syncwarp();
       if (ok) {
-        unsigned char* dst = (is_v ? W.v[slot] : W.k[slot]) + r * GE::kPitch;
-        bulk_g2s(dst, (is_v ? a.v_cache : a.k_cache) + src, GE::kRow, is_v ? &W.bar_v[slot] : &W.bar_k[slot], pol);
+        unsigned char* dst = (is_v ? Wt.v[slot] : Wt.k[slot]) + r * GE::kPitch;
+        bulk_g2s(dst, (is_v ? a.v_cache : a.k_cache) + src, GE::kRow, is_v ? &Wb.bar_v[slot] : &Wb.bar_k[slot], pol);
       }
       advance(ic, s_nb, a.B, a.Hkv);
     }
@@ -422,12 +432,12 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     const int slot = k % R;
     const uint32_t parity = (uint32_t)(k / R) & 1u;
     // every lane waits (acquiring the TMA writes); the give-up decision is warp-uniform
-    if (!__all_sync(kFullMask, mbar_wait_bounded(&W.bar_k[slot], parity, a.timeout_ns))) {
+    if (!__all_sync(kFullMask, mbar_wait_bounded(&Wb.bar_k[slot], parity, a.timeout_ns))) {
       if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
       aborted = true;
       break;
     }
-    uint32_t mask = W.meta[slot];
+    uint32_t mask = Wb.meta[slot];
     int t_new = -1;  // tile row of this step's token when the unit holds it (append mode)
     if constexpr (!SPARSE) {
       const int tok0 = (s_first[cc.b] + cc.j) * 16;
@@ -438,8 +448,8 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         t_new = s_len[cc.b] - 1 - tok0;
         // the tile was read before the append: put the new K row in it and in the pool
         if (lane < 16 && new_lane) {
-          *reinterpret_cast<uint4*>(W.k[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
-          *reinterpret_cast<uint4*>(a.k_pool_out + (((size_t)W.phys[slot] * a.Hkv + cc.g) * 16 + t_new) * D +
+          *reinterpret_cast<uint4*>(Wt.k[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
+          *reinterpret_cast<uint4*>(a.k_pool_out + (((size_t)Wb.phys[slot] * a.Hkv + cc.g) * 16 + t_new) * D +
                                     new_chunk * 8) = new_row;
         }
         __syncwarp();
@@ -448,7 +458,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     if (mask != 0u) {
       // -- S^T = K q^T: 16 tokens x 8 heads --------------------------------------------------
       float c[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t kbase = smem_u32(W.k[slot]);
+      const uint32_t kbase = smem_u32(Wt.k[slot]);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         uint32_t af[4];
@@ -504,15 +514,15 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       const uint32_t lB = pack_bf16x2(p10 - bf16_lo_to_f32(hB), p11 - bf16_hi_to_f32(hB));
       const uint32_t bh0 = movmatrix_trans(hA), bh1 = movmatrix_trans(hB);
       const uint32_t bl0 = movmatrix_trans(lA), bl1 = movmatrix_trans(lB);
-      if (!__all_sync(kFullMask, mbar_wait_bounded(&W.bar_v[slot], parity, a.timeout_ns))) {
+      if (!__all_sync(kFullMask, mbar_wait_bounded(&Wb.bar_v[slot], parity, a.timeout_ns))) {
         if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
         aborted = true;
         break;
       }
       if (t_new >= 0) {  // append mode: the new V row, into the tile and the pool
         if (lane >= 16 && new_lane) {
-          *reinterpret_cast<uint4*>(W.v[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
-          *reinterpret_cast<uint4*>(a.v_pool_out + (((size_t)W.phys[slot] * a.Hkv + cc.g) * 16 + t_new) * D +
+          *reinterpret_cast<uint4*>(Wt.v[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
+          *reinterpret_cast<uint4*>(a.v_pool_out + (((size_t)Wb.phys[slot] * a.Hkv + cc.g) * 16 + t_new) * D +
                                     new_chunk * 8) = new_row;
         }
         __syncwarp();
@@ -525,12 +535,12 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
           const int t = 2 * i + (lane >> 4);
           const int c = lane & 15;  // chunk (16 bytes) of the row
           if (!((mask >> t) & 1u) && c < D / 8)
-            *reinterpret_cast<uint4*>(W.v[slot] + chunk_offset<D, SPARSE>(t, c)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(Wt.v[slot] + chunk_offset<D, SPARSE>(t, c)) = make_uint4(0u, 0u, 0u, 0u);
         }
         __syncwarp();
       }
       // -- O^T += V^T P^T -------------------------------------------------------------------
-      const uint32_t vbase = smem_u32(W.v[slot]);
+      const uint32_t vbase = smem_u32(Wt.v[slot]);
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         uint32_t av[4];
@@ -538,7 +548,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         mma_bf16_m16n8k16(o[mt], av, bh0, bh1);
         mma_bf16_m16n8k16(o[mt], av, bl0, bl1);
       }
-    } else if (!__all_sync(kFullMask, mbar_wait_bounded(&W.bar_v[slot], parity, a.timeout_ns))) {
+    } else if (!__all_sync(kFullMask, mbar_wait_bounded(&Wb.bar_v[slot], parity, a.timeout_ns))) {
       if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
       aborted = true;
       break;
@@ -553,8 +563,8 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
 
   if (aborted) {  // let the copies in flight land before the CTA's shared memory goes away
     for (int kk = k; kk < issued; ++kk) {
-      (void)mbar_wait_bounded(&W.bar_k[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
-      (void)mbar_wait_bounded(&W.bar_v[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
+      (void)mbar_wait_bounded(&Wb.bar_k[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
+      (void)mbar_wait_bounded(&Wb.bar_v[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
     }
     return;
   }
@@ -662,12 +672,10 @@ DecodeKernel decode_kernel(int head_dim, int group, bool sparse) {
 }
 
 size_t decode_smem_bytes(int head_dim, bool sparse, int batch) {
-  size_t per_warp = 0;
-  if (head_dim == 128) per_warp = sparse ? sizeof(WarpSmem<128, true>) : sizeof(WarpSmem<128, false>);
-  if (head_dim == 64) per_warp = sparse ? sizeof(WarpSmem<64, true>) : sizeof(WarpSmem<64, false>);
-  if (per_warp == 0) return 0;
-  // + 1 KiB so the tiles can start on a 1 KiB boundary
-  return 1024 + per_warp * kDecodeWarps + sizeof(int32_t) * (5 * (size_t)batch + 1);
+  (void)sparse;
+  if (head_dim != 128 && head_dim != 64) return 0;
+  // dynamic part only: the per-sequence arrays (the tile rings are static)
+  return sizeof(int32_t) * (5 * (size_t)batch + 1);
 }
 
 cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, size_t smem,

@@ -253,3 +253,79 @@ def test_workspace_reused_across_shapes():
                                              c["context_lens"], c["scale"], workspace=ws)
             torch.cuda.synchronize()
             assert_attn_close(out, _oracle_rows(c, None), f"shape {i}")
+
+
+def test_result_independent_of_batch_partition():
+    """A sequence's rows do not depend on which other sequences share the launch (each batch
+    composition cuts the flattened work differently, so this checks split-count invariance)."""
+    lens = [4000, 37, 2500, 900, 16, 3100]
+    case = _small_case(lens, hq=16, hkv=4, d=128, seed=51)
+    full = _run(case).float().cpu()
+    for subset in ([0], [0, 2], [5, 3, 1], [1, 4]):
+        idx = torch.tensor(subset)
+        sub = {k: (v[idx.to(v.device)] if k in ("q", "block_tables", "context_lens") else v)
+               for k, v in case.items()}
+        out = _run(sub).float().cpu()
+        ref = _oracle_rows(sub, None)
+        assert_attn_close(out, ref, f"subset {subset}")
+        mx = float((out - full[idx]).abs().max())
+        assert mx <= 1e-2, (subset, mx)
+
+
+def test_cuda_graph_capture_and_replay():
+    """The decode calls enqueue no host synchronisation or allocation: captured in a CUDA
+    graph and replayed, they give the eager result bit for bit."""
+    case = _small_case([700, 33, 1500, 129], hq=8, hkv=2, d=128, seed=52)
+    g = torch.Generator().manual_seed(53)
+    k_new = rand_bf16((4, 2, 128), g).to(DEV)
+    v_new = rand_bf16((4, 2, 128), g).to(DEV)
+    ws = torch.zeros(pkv.decode_workspace_bytes(4, 8, 2, 128, case["k_cache"].shape[0],
+                                                case["block_tables"].shape[1]), dtype=torch.uint8, device=DEV)
+    out = torch.empty_like(case["q"])
+    kc0, vc0 = case["k_cache"].clone(), case["v_cache"].clone()
+    eager = pkv.paged_decode_attention_append(case["q"], case["k_cache"], case["v_cache"], k_new, v_new,
+                                              case["block_tables"], case["context_lens"], case["scale"],
+                                              workspace=ws).clone()
+    case["k_cache"].copy_(kc0)
+    case["v_cache"].copy_(vc0)
+    s = torch.cuda.Stream(DEV)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            pkv.paged_decode_attention_append(case["q"], case["k_cache"], case["v_cache"], k_new, v_new,
+                                              case["block_tables"], case["context_lens"], case["scale"],
+                                              out=out, workspace=ws)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_shapes_fuzz(seed):
+    """Seeded random shapes: batch, lengths (incl. 0 and block edges), d, G in 1..8, window, and
+    the fused append, all against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    d = int(rng.choice([64, 128]))
+    hkv = int(rng.integers(1, 5))
+    G = int(rng.integers(1, 9))
+    B = int(rng.integers(1, 9))
+    lens = [int(x) for x in rng.choice([0, 1, 15, 16, 17, 31, 32, 33, 200, 777, 2048, 3000], size=B)]
+    window = int(rng.choice([0, 0, 1, 16, 100, 5000]))
+    case = _small_case(lens, hq=hkv * G, hkv=hkv, d=d, seed=2000 + seed, fill=float("nan"))
+    out = _run(case, window)
+    assert_attn_close(out, _oracle_rows(case, None, window=window), f"fuzz {seed}: d={d} G={G} lens={lens}")
+    if min(lens) > 0:
+        gen = torch.Generator().manual_seed(3000 + seed)
+        k_new = rand_bf16((B, hkv, d), gen)
+        v_new = rand_bf16((B, hkv, d), gen)
+        bt = case["block_tables"].cpu()
+        slots = np.array([int(bt[b, (L - 1) // 16]) * 16 + (L - 1) % 16 for b, L in enumerate(lens)],
+                         dtype=np.int64)
+        okc, ovc = oracle.kv_append(bits(case["k_cache"]), bits(case["v_cache"]), bits(k_new), bits(v_new), slots)
+        out2 = pkv.paged_decode_attention_append(case["q"], case["k_cache"], case["v_cache"], k_new.to(DEV),
+                                                 v_new.to(DEV), case["block_tables"], case["context_lens"],
+                                                 case["scale"], window)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(case["k_cache"]), okc) and np.array_equal(bits(case["v_cache"]), ovc)
+        assert_attn_close(out2, _oracle_rows(case, None, okc, ovc, window=window), f"fuzz append {seed}")

@@ -184,7 +184,7 @@ def run_ours(args):
     for c in copies:
         assert c["num_blocks"] == nb and c["max_blocks_per_seq"] == mb
     ws_bytes = pkv.decode_workspace_bytes(B, hq, hkv, d, nb, mb)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=dev)
     err = pkv.new_error_word(dev)
     stream = torch.cuda.current_stream(dev)
@@ -200,10 +200,11 @@ def run_ours(args):
     if pkv.read_error(err) != 0:
         raise RuntimeError("device error during warm-up")
 
+    # Steps run back to back between two events on the launching stream: an event recorded
+    # between two calls would end the programmatic (PDL) overlap of one call's launch with the
+    # previous call's tail, which back-to-back decode layers get.
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         # same load for ~0.8 s before the timed region, so nvidia-smi (200 ms period) has
         # started sampling when the timed steps run
@@ -219,16 +220,14 @@ def run_ours(args):
         host_t0 = time.perf_counter()
         ev0.record(stream)
         for i in range(args.steps):
-            dec[i][0].record(stream)
             step(copies[i % ROTATE])
-            dec[i][1].record(stream)
         ev1.record(stream)
         host_ms = (time.perf_counter() - host_t0) * 1e3 / args.steps
         torch.cuda.synchronize(dev)
     _barrier(dist)
     ms = ev0.elapsed_time(ev1) / args.steps
     ms = _max_over_ranks(dist, ms, dev)
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec)
+    dec_ms = ev0.elapsed_time(ev1) / args.steps  # this rank's own average step (one decode call)
     if pkv.read_error(err) != 0:
         raise RuntimeError("device error during the timed region")
 
@@ -265,7 +264,8 @@ def run_ours(args):
         "kv_read_gbs": round(kv_bytes(lens, hkv, d) / (dec_ms * 1e-3) / 1e9, 1),
         "roofline": {
             "bound": "hbm",
-            "kernel": "paged_decode_attention_append (split kernel with the fused append + merge kernel)",
+            "kernel": "paged_decode_attention_append: split kernel (fused append) + merge kernel, "
+                      "timed together as the step; the split kernel alone is faster",
             "achieved": round(achieved, 1),
             "peak": hbm,
             "peak_kind": peak_kind,
@@ -360,7 +360,7 @@ def run_secondary(pkv, W, dev, stream, args):
     # long-context split-K decode: B=4 x 131072 tokens
     wl = W.WORKLOADS["long128k"]
     c = W.make_layer(wl, device=dev, device_rng=True)
-    ws = torch.empty(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+    ws = torch.zeros(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
                                                 c["num_blocks"], c["max_blocks_per_seq"]),
                      dtype=torch.uint8, device=dev)
     out = torch.empty_like(c["q"])

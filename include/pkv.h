@@ -54,7 +54,7 @@ extern "C" {
 #define PKV_ERR_BLOCK_SIZE (-3)     /* block_size != 16 */
 #define PKV_ERR_HEAD_DIM (-4)       /* head_dim not in {64, 128} */
 #define PKV_ERR_GQA (-5)            /* num_q_heads % num_kv_heads != 0 or G = Hq/Hkv > 8 */
-#define PKV_ERR_WORKSPACE (-6)      /* workspace NULL or smaller than the *_workspace_bytes query */
+#define PKV_ERR_WORKSPACE (-6)      /* workspace NULL or too small (see pkv_decode_workspace_bytes) */
 #define PKV_ERR_ALIGNMENT (-7)      /* a tensor pointer is not 16-byte aligned */
 #define PKV_ERR_ARGUMENT (-8)       /* any other invalid scalar argument */
 #define PKV_ERR_NO_DEVICE (-9)      /* no current CUDA device could be queried */
@@ -68,6 +68,7 @@ extern "C" {
 #define PKV_DEV_BAD_CONTEXT_LEN 4   /* context_len < 0 or > max_blocks_per_seq*16 */
 #define PKV_DEV_WAIT_TIMEOUT 5      /* an mbarrier wait exceeded its bound (kernel gave up) */
 #define PKV_DEV_BAD_SCORE 6         /* NaN score given to top-k selection */
+#define PKV_DEV_DIRTY_WORKSPACE 7   /* decode workspace counters were not zero at the call */
 
 /* Shape record shared by the calls. */
 typedef struct pkv_dims {
@@ -101,9 +102,17 @@ int pkv_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
                   int32_t* error_word, void* stream);
 
 /*
- * pkv_decode_workspace_bytes -- bytes of device workspace pkv_paged_decode_attention
- * needs for these dims on the current device (split-K partial results).  The workspace
- * needs no initialisation and may be reused by consecutive calls on one stream.
+ * pkv_decode_workspace_bytes -- bytes of device workspace for pkv_paged_decode_attention and
+ * pkv_paged_decode_attention_append with these dims.  The split-K decode cuts the work into
+ * one slice per worker warp (at most 2048 warps): a static head per warp plus up to four
+ * tail chunks per slice that warps take from a ticket counter as they finish, and keeps two
+ * partial results per such range: about 2 * 10240 * G * (d + 2) * 4 bytes, whatever the
+ * context lengths (G = Hq / Hkv).  A smaller workspace is accepted as long as it holds the
+ * partials of 2048 ranges; it then gets fewer tail chunks.
+ * The workspace's first 8 bytes are the ticket counters: they must be zero before the
+ * first call (e.g. allocate it zero-filled) and every call leaves them zero, so one
+ * workspace serves consecutive calls on one stream, of any shape, without re-clearing.
+ * Counters found non-zero make the call record PKV_DEV_DIRTY_WORKSPACE.
  * Returns 0 if dims are invalid.
  */
 size_t pkv_decode_workspace_bytes(const pkv_dims* dims);
@@ -127,8 +136,10 @@ size_t pkv_decode_workspace_bytes(const pkv_dims* dims);
  *                    0 <= L_b <= MB*16.  L_b == 0 gives a zero output row.
  *   scale          : logit scale (normally 1/sqrt(d)).
  *   window         : > 0 attends tokens [max(0, L_b - window), L_b); <= 0 attends all.
- *   workspace      : >= pkv_decode_workspace_bytes(dims) bytes, 16-byte aligned.
- *   error_word     : optional; PKV_DEV_BAD_BLOCK_ID / _BAD_CONTEXT_LEN / _WAIT_TIMEOUT.
+ *   workspace      : pkv_decode_workspace_bytes(dims) bytes, 16-byte aligned, its first 8
+ *                    bytes zero before the first use (every call leaves them zero).
+ *   error_word     : optional; PKV_DEV_BAD_BLOCK_ID / _BAD_CONTEXT_LEN / _WAIT_TIMEOUT /
+ *                    _DIRTY_WORKSPACE.
  * Supported: d in {64, 128}; G = Hq / Hkv in 1..8.
  */
 int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
@@ -159,7 +170,8 @@ int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, v
 
 /*
  * pkv_sparse_decode_workspace_bytes -- workspace for pkv_sparse_decode_attention with
- * kept lists of row length max_kept.  Returns 0 if the arguments are invalid.
+ * kept lists of row length max_kept: the same size and rules as pkv_decode_workspace_bytes
+ * (it does not depend on max_kept).  Returns 0 if the arguments are invalid.
  */
 size_t pkv_sparse_decode_workspace_bytes(const pkv_dims* dims, int32_t max_kept);
 
@@ -237,17 +249,18 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
  * the split-K scratch is a static device array of PKV_FIXED_SCRATCH_BYTES (16 MiB) inside
  * the library, which every GPU that loads the library keeps until the process exits.  The
  * call itself allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
- *   - Shapes whose scratch need, pkv_decode_workspace_bytes(dims), exceeds
- *     PKV_FIXED_SCRATCH_BYTES return PKV_ERR_WORKSPACE and enqueue nothing.  At d=128 the
- *     need is about 520 bytes x B*Hq x (ceil(MB/16) + 1); batch 32 with 32 query heads fits
- *     up to MB = 480 blocks (7,680 tokens per sequence).
+ *   - It holds the partial results of 2048 worker ranges plus load-balancing chunks as
+ *     far as it has room (see pkv_decode_workspace_bytes).  Shapes for which 2048 ranges
+ *     do not fit -- G * d above 512, that is G = 8 at d = 128 -- return PKV_ERR_WORKSPACE
+ *     and enqueue nothing.
  *   - The first call on a device looks up the array's device address on that device (with
  *     it current); make that first call before any stream capture.
- *   - Every call on a device shares the one array, whose contents persist between calls
- *     (nothing in it needs to start at zero).  Calls whose kernels overlap on the GPU --
- *     different streams without ordering, or several host threads -- race on it and give
- *     wrong results: serialise them.
- *   - Results are identical to pkv_paged_decode_attention with the same arguments.
+ *   - Every call on a device shares the one array.  Its two control words start at zero
+ *     (static storage) and every call leaves them zero.  Calls whose kernels overlap on
+ *     the GPU -- different streams without ordering, or several host threads -- race on
+ *     it and give wrong results: serialise them.
+ *   - Results equal those of pkv_paged_decode_attention up to fp32 summation order (with
+ *     fewer load-balancing chunks the split-K partition may differ).
  */
 #define PKV_FIXED_SCRATCH_BYTES (16 * 1024 * 1024)
 int pkv_paged_decode_attention_fixed_scratch(void* out, const void* q, const void* k_cache,

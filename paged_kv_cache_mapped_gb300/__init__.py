@@ -4,7 +4,7 @@ Python binding of libpkv (declared in include/pkv.h).  Each function checks the 
 tensors it is given, builds the C shape record and calls the C-ABI entry point of the same
 name (``pkv_<name>``) on the current CUDA stream.  All computation happens in the library's
 CUDA kernels; CPU tensors are rejected, there is no fallback path.  PyTorch only provides
-device memory (outputs and workspaces are ``torch.empty`` on the inputs' device) and the
+device memory (outputs ``torch.empty``, workspaces ``torch.zeros``, on the inputs' device) and the
 stream handle.
 """
 from __future__ import annotations
@@ -132,7 +132,7 @@ def _out_ws(q, out, workspace, nbytes):
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
     if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
     else:
         _need(workspace, "workspace", torch.uint8, 1, q.device)
     return out, workspace

@@ -3,6 +3,7 @@
 // stream.  Allocates nothing and never synchronises (except pkv_read_error).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -23,6 +24,7 @@ struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
   size_t max_dyn_smem[2][2] = {};  // [head_dim index][sparse]: opt-in minus the kernel's static
+  int merge_ctas_per_sm[2] = {};   // [head_dim index]: resident merge CTAs per SM
 };
 
 std::mutex g_mutex;
@@ -66,6 +68,14 @@ const DeviceInfo* device_info(int* status) {
             return nullptr;
           }
           info.max_dyn_smem[hd][sp] = (size_t)dyn;
+          int per_sm = 0;
+          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.merge, kMergeWarps * 32, 0);
+          if (e != cudaSuccess) {
+            cudaGetLastError();
+            *status = PKV_ERR_CUDA_BASE + (int)e;
+            return nullptr;
+          }
+          info.merge_ctas_per_sm[hd] = per_sm > 0 ? per_sm : 1;
         }
       }
     }
@@ -132,25 +142,60 @@ int check_dims(const pkv_dims* d, bool need_q_heads) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA_BASE + (int)e; }
 
-// Workspace layout of the decode calls (all offsets 256-byte aligned):
-//   int32 layout[2 + (B+1) + B] | float2 part_ml[B*Hq*max_parts] | float part_o[B*Hq*max_parts*D]
-struct WorkspacePlan {
-  size_t layout_off, ml_off, o_off, total;
-  int max_parts;
-};
+// Merge warps per output row (log2), from an upper estimate of the partials a row has: one
+// more warp per PKV_MERGE_PARTIALS_PER_WARP partials, at most 8, and no more than the GPU holds
+// in one wave of merge CTAs.
+// The estimate mirrors the split kernel's partition with every sequence at its maximum length.
+int merge_warps_log2(const pkv_dims* d, int max_units, long long workers, int min_units, int tail_pct,
+                     int chunk_min, int cpw_cap, long long resident_warps) {
+  const long long total = (long long)d->batch * d->num_kv_heads * max_units;
+  long long P = (total + workers - 1) / workers;
+  if (P < min_units) P = min_units;
+  const long long tail = P * tail_pct / 100;
+  int cpw = 0;
+  while (cpw < cpw_cap && tail >= chunk_min * ((2ll << cpw) - 1)) ++cpw;
+  const long long np = ((long long)max_units + P - 1) / P * (1 + cpw) + 1;
+  int lg = 0;
+  while (lg < 3 && np >= (long long)PKV_MERGE_PARTIALS_PER_WARP << (lg + 1)) ++lg;
+  const long long rows = (long long)d->batch * d->num_q_heads;
+  while (lg > 0 && (rows << lg) > resident_warps) --lg;
+  return lg;
+}
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WorkspacePlan plan_workspace(const pkv_dims* d, int max_units_per_seq) {
+}  // namespace
+
+// Workspace layout of the decode calls (offsets 256-byte aligned):
+//   uint32 ctrl[2] | int32 layout[2B] | float2 part_ml[2 * ranges][G] | float part_o[2 * ranges][G][D]
+// for a workspace with partial slots for `ranges` ranges (two per range: its first and its
+// last segment).  ctrl must be zero before the first call; every call leaves it zero.
+WorkspacePlan plan_workspace(const pkv_dims* d, long long ranges) {
   WorkspacePlan p{};
-  p.max_parts = (max_units_per_seq + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp + 1;
-  const size_t rows = (size_t)d->batch * d->num_q_heads;
-  p.layout_off = 0;
-  p.ml_off = align256(sizeof(int32_t) * (2 + 2 * (size_t)d->batch + 1));
-  p.o_off = align256(p.ml_off + sizeof(float) * 2 * rows * p.max_parts);
-  p.total = align256(p.o_off + sizeof(float) * rows * p.max_parts * d->head_dim);
+  const size_t G = (size_t)(d->num_q_heads / d->num_kv_heads);
+  const size_t slots = 2 * (size_t)ranges * G;
+  p.ranges = ranges;
+  p.ctrl_off = 0;
+  p.layout_off = 256;
+  p.ml_off = align256(p.layout_off + sizeof(int32_t) * 2 * (size_t)d->batch);
+  p.o_off = align256(p.ml_off + sizeof(float2) * slots);
+  p.total = align256(p.o_off + sizeof(float) * slots * d->head_dim);
   return p;
 }
+
+// The plan with the most ranges that fits in `bytes` (0 ranges if not even one fits).
+WorkspacePlan fit_workspace(const pkv_dims* d, size_t bytes) {
+  const WorkspacePlan base = plan_workspace(d, 0);
+  const size_t G = (size_t)(d->num_q_heads / d->num_kv_heads);
+  const size_t per_range = 2 * G * (sizeof(float2) + sizeof(float) * d->head_dim);
+  // an upper estimate (alignment padding ignored), then down to the largest plan that fits
+  long long r = bytes > base.total ? (long long)((bytes - base.total) / per_range) : 0;
+  WorkspacePlan p = plan_workspace(d, r);
+  while (r > 0 && p.total > bytes) p = plan_workspace(d, --r);
+  return p;
+}
+
+namespace {
 
 }  // namespace
 
@@ -175,12 +220,13 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   if (k.split == nullptr) return PKV_ERR_GQA;
   const int max_units = sparse ? (max_kept + 15) / 16 : dims->max_blocks_per_seq;
   // the flattened unit count and the pool's row count (a TMA coordinate) must fit int32
-  if ((long long)dims->batch * dims->num_kv_heads * (long long)(max_units + 1) >= (1ll << 31))
+  if ((long long)dims->batch * dims->num_kv_heads * (long long)(max_units + 1) >= (1ll << 30))
     return PKV_ERR_DIMS;
   const long long pool_rows = (long long)dims->num_blocks * dims->num_kv_heads * PKV_BLOCK_SIZE;
   if (pool_rows >= (1ll << 31)) return PKV_ERR_DIMS;
-  const WorkspacePlan plan = plan_workspace(dims, max_units);
-  if (workspace_bytes < plan.total) return PKV_ERR_WORKSPACE;
+  // partial slots for at least the static ranges of the largest grid
+  const WorkspacePlan plan = fit_workspace(dims, workspace_bytes);
+  if (plan.ranges < kMaxWorkers) return PKV_ERR_WORKSPACE;
   const DeviceInfo* info = device_info(&st);
   if (!info) return st;
   const size_t smem = decode_smem_bytes(dims->head_dim, sparse, dims->batch);
@@ -211,6 +257,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   }
   a.out = static_cast<__nv_bfloat16*>(out);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.ctrl = reinterpret_cast<uint32_t*>(ws + plan.ctrl_off);
   a.layout = reinterpret_cast<int32_t*>(ws + plan.layout_off);
   a.part_ml = reinterpret_cast<float2*>(ws + plan.ml_off);
   a.part_o = reinterpret_cast<float*>(ws + plan.o_off);
@@ -222,12 +269,21 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.MB = dims->max_blocks_per_seq;
   a.max_kept = sparse ? max_kept : 0;
   a.window = sparse ? 0 : window;
-  a.max_parts = plan.max_parts;
-  a.min_units = kMinUnitsPerWarp;
+  const int grid = std::min(info->sm_count * per_sm, kMaxWorkers / kDecodeWarps);
+  const long long workers = (long long)grid * kDecodeWarps;
+  a.workers = (int)workers;
+  const int ring = dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64;
+  a.min_units = std::max(PKV_MIN_UNITS, 1);
+  a.tail_pct = std::min(std::max(PKV_TAIL_PCT, 0), 50);
+  a.chunk_min = std::max(PKV_CHUNK_MIN, ring);  // a chunk never ends inside the tile ring
+  a.cpw_cap = (int)std::min<long long>(std::min(PKV_MAX_TAIL_CHUNKS, kMaxTailChunksLimit),
+                                       plan.ranges / workers - 1);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.timeout_ns = kWaitTimeoutNs;
-  const int grid = info->sm_count * per_sm;
-  return cuda_status(launch_decode(k, a, grid, smem, static_cast<cudaStream_t>(stream)));
+  const int wpr_log2 = merge_warps_log2(
+      dims, max_units, workers, a.min_units, a.tail_pct, a.chunk_min, a.cpw_cap,
+      (long long)info->sm_count * info->merge_ctas_per_sm[head_dim_index(dims->head_dim)] * kMergeWarps);
+  return cuda_status(launch_decode(k, a, grid, smem, wpr_log2, static_cast<cudaStream_t>(stream)));
 }
 
 
@@ -255,7 +311,8 @@ int pkv_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
 
 size_t pkv_decode_workspace_bytes(const pkv_dims* dims) {
   if (check_dims(dims, true) != PKV_OK || dims->batch > kMaxBatch) return 0;
-  return plan_workspace(dims, dims->max_blocks_per_seq).total;
+  if (dims->num_q_heads / dims->num_kv_heads > kMaxGroup) return 0;
+  return plan_workspace(dims, (long long)kMaxWorkers * (1 + std::min(PKV_MAX_TAIL_CHUNKS, kMaxTailChunksLimit))).total;
 }
 
 int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -281,8 +338,8 @@ int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, v
 }
 
 size_t pkv_sparse_decode_workspace_bytes(const pkv_dims* dims, int32_t max_kept) {
-  if (check_dims(dims, true) != PKV_OK || dims->batch > kMaxBatch || max_kept <= 0) return 0;
-  return plan_workspace(dims, (max_kept + 15) / 16).total;
+  if (max_kept <= 0) return 0;
+  return pkv_decode_workspace_bytes(dims);
 }
 
 int pkv_sparse_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -382,6 +439,7 @@ const char* pkv_device_error_string(int code) {
     case PKV_DEV_BAD_CONTEXT_LEN: return "context length outside [0, max_blocks_per_seq*16]";
     case PKV_DEV_WAIT_TIMEOUT: return "a bounded wait timed out";
     case PKV_DEV_BAD_SCORE: return "NaN score";
+    case PKV_DEV_DIRTY_WORKSPACE: return "decode workspace counters were not zero (zero-fill it before first use)";
     default: return "unknown device error";
   }
 }

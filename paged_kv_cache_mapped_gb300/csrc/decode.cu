@@ -8,12 +8,17 @@
 // (the layer-wise sparse variant of "How KV Sparsity Achieves 1.5x Acceleration for vLLM").
 //
 // Design (GB300-first; the step is HBM-bound at 4-6 flop per KV byte):
-//  * Work partition (a "stream-K" split): the (sequence, kv head, 16-token unit) list is
-//    flattened and cut into equal contiguous ranges, one per worker warp of a grid sized to
-//    the SMs, so every worker streams the same number of bytes whatever the length mix.  A
-//    range may end inside a (sequence, kv head) segment: each worker emits a partial
-//    (running max m, running sum l, unnormalised o) per segment it touches, and a segment
-//    covered by one worker writes its output directly.  A merge kernel combines the rest.
+//  * Work partition (a "stream-K" split with a dynamic tail): the (sequence, kv head,
+//    16-token unit) list is flattened and cut into one equal slice per worker warp of a grid
+//    sized to the SMs, so every worker streams about the same number of bytes whatever the
+//    length mix.  A slice is a static head, run by the warp of the same index, and a few tail
+//    chunks of halving length that warps take from a ticket counter once their own work is
+//    done: warps on SMs that stream faster (SMs differ by up to ~20% in sustained bandwidth)
+//    absorb the work of slower ones, which shortens the end of the launch.  A range (a head
+//    or a chunk) may start or end inside a (sequence, kv head) segment: it then emits a
+//    partial (running max m, running sum l, unnormalised o) into slots fixed by the range,
+//    so the result does not depend on which warp ran it; a segment inside one range is
+//    written out directly.  A merge kernel combines the partials.
 //  * Each worker warp owns a ring of K/V tile pairs in shared memory that complete on
 //    per-slot mbarriers.  Dense mode fills them with TMA tiled copies of a 2-D tensor map
 //    over the pool (one 64-column x 16-row box per 128 bytes of row, 128-byte swizzle, L2
@@ -118,6 +123,118 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* s_nb, int B, i
   }
 }
 
+// ---- the partition of the unit list into ranges ------------------------------------------
+// p is the partition record (PartField).  Slice w covers units [wP, (w+1)P).  A full slice is
+// its static head [wP, wP+S) followed by cpw tail chunks: chunk c covers
+// [wP+S+O_c, wP+S+O_{c+1}) of a tail of T = P - S units, with O_c = T - floor(T (2^(cpw-c) - 1)
+// / (2^cpw - 1)), so chunk lengths halve from one to the next.  Tickets hand out every slice's
+// chunk c before any chunk c+1: the long chunks go first and the short ones even out the end
+// (guided self-scheduling).  A partial last slice is one static range ending at the total.
+// Every chunk is at least as long as a worker's tile ring.
+//
+// A range is named by rid = (w << kRangeShift) | j, j = 0 for the head and c + 1 for chunk c,
+// so no division recovers its slice; range_index(rid) = w (1 + cpw) + j numbers the ranges in
+// unit order (it indexes the partial slots).
+constexpr int kRangeShift = 3;
+
+__device__ __forceinline__ int range_of(const int32_t* p, int u) {
+  const int P = p[kPartP], S = p[kPartS];
+  const int w = u / P, o = u - w * P;
+  if (o < S || w >= p[kPartNfull]) return w << kRangeShift;
+  const int cpw = p[kPartCpw], ot = o - S;
+  int c = 0;
+  while (c + 1 < cpw && p[kPartOff + c + 1] <= ot) ++c;
+  return (w << kRangeShift) | (c + 1);
+}
+
+__device__ __forceinline__ int range_start(const int32_t* p, int rid) {
+  const int w = rid >> kRangeShift, j = rid & ((1 << kRangeShift) - 1);
+  return w * p[kPartP] + (j == 0 ? 0 : p[kPartS] + p[kPartOff + j - 1]);
+}
+
+__device__ __forceinline__ int range_end(const int32_t* p, int rid) {
+  const int w = rid >> kRangeShift, j = rid & ((1 << kRangeShift) - 1);
+  if (w >= p[kPartNfull]) return p[kPartTotal];
+  return w * p[kPartP] + p[kPartS] + (j == 0 ? 0 : p[kPartOff + j]);
+}
+
+__device__ __forceinline__ int range_index(const int32_t* p, int rid) {
+  return (rid >> kRangeShift) * (1 + p[kPartCpw]) + (rid & ((1 << kRangeShift) - 1));
+}
+
+// The range of tail ticket t < p[kPartTickets]: chunk t / nfull of slice t % nfull.
+__device__ __forceinline__ int ticket_range(const int32_t* p, int t) {
+  const int nfull = p[kPartNfull];
+  const int c = t / nfull;
+  return ((t - c * nfull) << kRangeShift) | (c + 1);
+}
+
+constexpr uint32_t kNoTicket = 0xffffffffu;
+
+
+
+// Batches up to this size let the merge kernel derive its rows' partitions from the lengths
+// before the split kernel ends; larger ones read the split kernel's record after it.
+constexpr int kMergeScanMaxBatch = 256;
+
+// Units (16-token blocks of one kv head) that sequence b attends, with the bounds the split
+// kernel needs; invalid lengths count as empty and return the device error to report.
+struct SeqUnits {
+  int nb;     // units
+  int first;  // dense: first attended block; sparse: 0
+  int lo;     // dense: first attended token; sparse: context length
+  int len;    // dense: context length; sparse: kept count
+  int err;    // PKV_DEV_* code or 0
+};
+
+template <bool SPARSE>
+__device__ __forceinline__ SeqUnits seq_units(const DecodeArgs& a, int b) {
+  SeqUnits s{0, 0, 0, 0, 0};
+  int L = a.context_lens[b];
+  if (L < 0 || L > a.MB * 16) {
+    s.err = PKV_DEV_BAD_CONTEXT_LEN;
+    L = 0;
+  }
+  if constexpr (SPARSE) {
+    int n = a.kept_lens[b];
+    if (n < 0 || n > a.max_kept) {
+      if (s.err == 0) s.err = PKV_DEV_BAD_KEPT_INDEX;
+      n = 0;
+    }
+    s.nb = (n + 15) >> 4;
+    s.lo = L;
+    s.len = n;
+  } else {
+    s.lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
+    s.first = s.lo >> 4;
+    s.nb = L > 0 ? ((L - 1) >> 4) - s.first + 1 : 0;
+    s.len = L;
+  }
+  return s;
+}
+
+// Partition of `total` units over `nw` worker warps (total < 2^30).
+__device__ void make_partition(int32_t* p, int total, int nw, const DecodeArgs& a) {
+  int P = (total + nw - 1) / nw;
+  if (P < a.min_units) P = a.min_units;
+  // as many halving chunks as keep the last one, floor(T / (2^cpw - 1)), >= chunk_min
+  const int tail = (int)((long long)P * a.tail_pct / 100);
+  int cpw = 0;
+  while (cpw < a.cpw_cap && tail >= a.chunk_min * ((2 << cpw) - 1)) ++cpw;
+  const int T = cpw > 0 ? tail : 0;
+  const int nfull = total / P;
+  p[kPartTotal] = total;
+  p[kPartP] = P;
+  p[kPartS] = P - T;
+  p[kPartTail] = T;
+  p[kPartCpw] = cpw;
+  p[kPartNfull] = nfull;
+  p[kPartTickets] = nfull * cpw;
+  p[kPartWorkers] = nfull + (nfull * P < total ? 1 : 0);
+  for (int c = 0; c <= cpw; ++c)
+    p[kPartOff + c] = cpw > 0 ? T - (int)((long long)T * ((1 << (cpw - c)) - 1) / ((1 << cpw) - 1)) : 0;
+}
+
 template <int D, bool SPARSE>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_split_kernel(const __grid_constant__ DecodeArgs a) {
@@ -134,6 +251,8 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
                 "tile rings exceed static shared memory");
   __shared__ WT warps_tiles[kDecodeWarps];
   __shared__ WB warps_slots[kDecodeWarps];
+  __shared__ int32_t s_part[kPartFields];
+  __shared__ uint32_t s_ticket[kDecodeWarps];
   extern __shared__ __align__(16) int32_t smem_dyn[];
   int32_t* s_start = smem_dyn;
   int32_t* s_nb = s_start + (a.B + 1);
@@ -163,32 +282,12 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
 
   // ---- per-sequence unit counts and partition (identical in every CTA) -------------------
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
-    int L = a.context_lens[b];
-    if (L < 0 || L > a.MB * 16) {
-      if (blockIdx.x == 0) record_error(a.err, PKV_DEV_BAD_CONTEXT_LEN);
-      L = 0;
-    }
-    int nb, first, lo, len;
-    if constexpr (SPARSE) {
-      int n = a.kept_lens[b];
-      if (n < 0 || n > a.max_kept) {
-        if (blockIdx.x == 0) record_error(a.err, PKV_DEV_BAD_KEPT_INDEX);
-        n = 0;
-      }
-      nb = (n + 15) >> 4;
-      first = 0;
-      lo = L;
-      len = n;
-    } else {
-      lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
-      first = lo >> 4;
-      nb = L > 0 ? ((L - 1) >> 4) - first + 1 : 0;
-      len = L;
-    }
-    s_nb[b] = nb;
-    s_first[b] = first;
-    s_lo[b] = lo;
-    s_len[b] = len;
+    const SeqUnits su = seq_units<SPARSE>(a, b);
+    if (su.err != 0 && blockIdx.x == 0) record_error(a.err, su.err);
+    s_nb[b] = su.nb;
+    s_first[b] = su.first;
+    s_lo[b] = su.lo;
+    s_len[b] = su.len;
   }
   __syncthreads();
   if (warp == 0) {
@@ -205,26 +304,63 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       if (b < a.B) s_start[b] = carry + incl - v;
       carry += __shfl_sync(kFullMask, incl, 31);
     }
-    if (lane == 0) s_start[a.B] = carry;
+    if (lane == 0) {
+      s_start[a.B] = carry;
+      make_partition(s_part, carry, a.workers, a);
+    }
   }
   __syncthreads();
 
-  const int total = s_start[a.B];
-  const long long nworkers = (long long)gridDim.x * kDecodeWarps;
-  int per = (int)((total + nworkers - 1) / nworkers);
-  if (per < a.min_units) per = a.min_units;
-  if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i <= a.B; i += blockDim.x) a.layout[2 + i] = s_start[i];
-    for (int i = threadIdx.x; i < a.B; i += blockDim.x) a.layout[3 + a.B + i] = s_nb[i];
-    if (threadIdx.x == 0) {
-      a.layout[0] = total;
-      a.layout[1] = per;
-    }
+  // Large batches: the merge kernel reads the unit starts from here rather than recomputing
+  // them (smaller ones it derives from the lengths while this kernel still runs).
+  if (blockIdx.x == 0 && a.B > kMergeScanMaxBatch) {
+    for (int i = threadIdx.x; i < a.B; i += blockDim.x) a.layout[i] = s_start[i];
+    for (int i = threadIdx.x; i < a.B; i += blockDim.x) a.layout[a.B + i] = s_nb[i];
   }
-  const long long gw = (long long)blockIdx.x * kDecodeWarps + warp;
-  if (gw * per >= total) return;  // no __syncthreads after this point
-  const int u0 = (int)(gw * per);
-  const int nunits = min(total - u0, per);
+  const int gw = (int)blockIdx.x * kDecodeWarps + warp;
+  const int tickets = s_part[kPartTickets];
+  uint32_t n_taken = 0;        // tail tickets this warp took
+  uint32_t t_req = kNoTicket;  // lane 0: a ticket requested before the current range ends
+  // The next range from the ticket counter, or -1 (lane 0 hands the ticket over through
+  // shared memory, so every lane sees the same value).
+  auto take_ticket = [&]() -> int {
+    int r = -1;
+    if (tickets > 0) {
+      if (lane == 0) s_ticket[warp] = (t_req == kNoTicket) ? atomicAdd(a.ctrl, 1u) : t_req;
+      t_req = kNoTicket;
+      __syncwarp();
+      const uint32_t t = s_ticket[warp];
+      __syncwarp();
+      if (t < (uint32_t)tickets) {
+        ++n_taken;
+        r = ticket_range(s_part, (int)t);
+      }
+    }
+    return r;
+  };
+  // this warp's first range: its slice's static head, or a tail chunk
+  int rid = gw < s_part[kPartWorkers] ? (gw << kRangeShift) : take_ticket();
+  bool aborted = false;
+  bool first_range = true;
+  while (rid >= 0 && !aborted) {
+  const int u0 = range_start(s_part, rid);
+  const int nunits = range_end(s_part, rid) - u0;
+  const int ridx = range_index(s_part, rid);
+  if (!first_range) {
+    // a new range restarts the tile ring from phase 0 (every copy of the last one has landed)
+    __syncwarp();
+    if (lane == 0) {
+      for (int s = 0; s < R; ++s) {
+        mbar_inval(&Wb.bar_k[s]);
+        mbar_inval(&Wb.bar_v[s]);
+        mbar_init(&Wb.bar_k[s], 1);
+        mbar_init(&Wb.bar_v[s], 1);
+      }
+      fence_mbar_init();
+    }
+    __syncwarp();
+  }
+  first_range = false;
 
   const uint64_t pol = l2_policy_evict_first();
   Cursor ic = locate(u0, s_start, s_nb, a.B);  // next unit to issue
@@ -248,7 +384,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   };
   load_q(cc.b, cc.g);
 
-  // Dense: the block-table entries of this worker's units, 32 per coalesced load (lane l
+  // Dense: the block-table entries of this range's units, 32 per coalesced load (lane l
   // holds the entry of unit chunk_base + l), fetched one chunk ahead of use.
   int bt_cur = -1, bt_next = -1, chunk_base = 0;
   auto load_chunk = [&](int first) -> int {
@@ -337,13 +473,20 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
 
   int issued = 0;
   for (; issued < nunits && issued < R; ++issued) issue(issued);
+  // ask for the next range while this one's last units are still in flight
+  bool requested = false;
+  if (issued == nunits) {
+    if (lane == 0 && tickets > 0) t_req = atomicAdd(a.ctrl, 1u);
+    requested = true;
+  }
 
   // ---- consumer state: this lane's heads are h0 = 2tq and h1 = 2tq + 1 ------------------
   uint32_t qb[2 * KS];   // q^T B fragments of the current segment
   float o[KS][4];        // O^T accumulator fragments: [m-tile][d row gq / gq+8, head h0 / h1]
   float mr0 = -INFINITY, mr1 = -INFINITY;  // running max (reference) of heads h0, h1
   float l0 = 0.f, l1 = 0.f;                // this lane's share of the running sums
-  int seg_b = -1, seg_g = -1, part = 0, nparts = 0;
+  int seg_b = -1, seg_g = -1;
+  int seg_slot = -1;  // partial slot of the current segment, -1: written out directly
   const float sl2 = a.scale_log2;
   // Dense append mode: this step's K (lanes 0-15) or V (lanes 16-31) row chunk of the current
   // segment, to be written at token L_b - 1 (pool and tile) when its unit is consumed.
@@ -365,7 +508,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       const float l = hh ? l1 : l0;
       const float m = hh ? mr1 : mr0;
       const size_t row = (size_t)seg_b * a.Hq + (size_t)seg_g * G + head;
-      if (nparts == 1) {
+      if (seg_slot < 0) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16* dst = a.out + row * D + gq;
 #pragma unroll
@@ -374,13 +517,14 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
           dst[mt * 16 + 8] = __float2bfloat16_rn(o[mt][2 + hh] * inv);
         }
       } else {
-        float* dst = a.part_o + (row * a.max_parts + part) * D + gq;
+        const size_t e = (size_t)seg_slot * G + head;  // a flush writes G adjacent entries
+        float* dst = a.part_o + e * D + gq;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           dst[mt * 16] = o[mt][hh];
           dst[mt * 16 + 8] = o[mt][2 + hh];
         }
-        if (gq == 0) a.part_ml[row * a.max_parts + part] = make_float2(m, l);
+        if (gq == 0) a.part_ml[e] = make_float2(m, l);
       }
     }
   };
@@ -390,9 +534,9 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     seg_g = c.g;
     const int nb = s_nb[c.b];
     const int seg_begin = s_start[c.b] + c.g * nb;
-    const int w0 = seg_begin / per;
-    nparts = (seg_begin + nb - 1) / per - w0 + 1;
-    part = (int)gw - w0;
+    // a segment inside this range is written out directly; otherwise the range's share is a
+    // partial in slot 2 ridx (the segment holds the range's start) or 2 ridx + 1 (its end)
+    seg_slot = (seg_begin >= u0 && seg_begin + nb <= u0 + nunits) ? -1 : 2 * ridx + (u0 >= seg_begin ? 0 : 1);
 #pragma unroll
     for (int i = 0; i < 2 * KS; ++i) qb[i] = qraw[i];
     if (appending && new_lane) {
@@ -422,7 +566,6 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   const int k_row = lane & 15, k_half = lane >> 4;
   const int v_row = (lane & 7) + ((lane >> 4) << 3), v_half = (lane >> 3) & 1;
 
-  bool aborted = false;
   int k = 0;
   for (; k < nunits; ++k) {
     if (cc.b != seg_b || cc.g != seg_g) {
@@ -557,6 +700,9 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     if (issued < nunits) {
       issue(issued);
       ++issued;
+    } else if (!requested) {
+      if (lane == 0 && tickets > 0) t_req = atomicAdd(a.ctrl, 1u);
+      requested = true;
     }
     advance(cc, s_nb, a.B, a.Hkv);
   }
@@ -566,90 +712,176 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       (void)mbar_wait_bounded(&Wb.bar_k[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
       (void)mbar_wait_bounded(&Wb.bar_v[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
     }
-    return;
+  } else {
+    flush();
+    rid = take_ticket();
   }
-  flush();
+  }  // ranges
+  if (lane == 0 && n_taken != 0u) atomicAdd(a.ctrl + 1, n_taken);
 }
 
 // Log-sum-exp merge of the partials of every (sequence, query head) row that more than one
-// worker touched; also writes the zero row of empty sequences.
+// range touched.  A CTA of W warps serves W / wpr rows with wpr = 2^wpr_log2 warps each:
+// warp `sub` of a row combines its partials sub, sub + wpr, sub + 2 wpr, ... and the row's
+// first warp combines the wpr results through shared memory.  Also writes the zero row of
+// empty sequences, checks that every tail chunk was taken exactly once and re-arms the
+// ticket counters for the next call.
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32)
-decode_merge_kernel(const DecodeArgs a, int group) {
+decode_merge_kernel(const DecodeArgs a, int group, int wpr_log2) {
   constexpr int EPW = D / 32;
+  constexpr int W = kMergeWarps;
+  __shared__ float s_acc[W][D];
+  __shared__ float2 s_ml[W];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kMergeWarps + warp;
-  grid_dependency_wait();  // the split kernel's partials and partition record
-  grid_launch_dependents();
-  if (row >= a.B * a.Hq) return;
-  const int b = row / a.Hq;
-  const int g = (row % a.Hq) / group;
-  const int per = a.layout[1];
-  const int nb = a.layout[3 + a.B + b];
-  __nv_bfloat16* dst = a.out + (size_t)row * D + lane * EPW;
-  if (nb == 0) {
+  const int wpr = 1 << wpr_log2;
+  const int sub = warp & (wpr - 1);
+  const int row = blockIdx.x * (W >> wpr_log2) + (warp >> wpr_log2);
+  // What this row needs (uniform over its warps; no early exit before the block barrier):
+  // nothing (written by the split kernel, or past the last row), a zero row, or a merge of
+  // np partials.  The partition follows from the lengths (inputs the split kernel does not
+  // write, final before it started), so small batches work it out, and prefetch their first
+  // partials into L2, before the split kernel ends.
+  const bool sparse = a.max_kept > 0;
+  const int rrow = min(row, a.B * a.Hq - 1);
+  const int b = rrow / a.Hq;
+  const int g = (rrow - b * a.Hq) / group;
+  const int head = row - (row / group) * group;
+  int32_t part[kPartFields];
+  int np = 0, r0 = 0, slot0 = 0;
+  bool zero_row = false;
+  auto describe = [&](int before, int total, int nb) {
+    make_partition(part, total * a.Hkv, a.workers, a);
+    if (row >= a.B * a.Hq) return;
+    if (nb == 0) {
+      zero_row = true;
+      return;
+    }
+    const int seg = before * a.Hkv + g * nb;
+    const int rid0 = range_of(part, seg);
+    r0 = range_index(part, rid0);
+    np = range_index(part, range_of(part, seg + nb - 1)) - r0 + 1;
+    if (np == 1) np = 0;
+    // partial i of the row: range r0 + i (in unit order), slot 2 (r0 + i), except that the
+    // segment is the second one range r0 touches (slot 2 r0 + 1) when it starts inside it
+    slot0 = 2 * r0 + (range_start(part, rid0) < seg ? 1 : 0);
+  };
+  auto entry = [&](int i) -> size_t {
+    return (size_t)(i == 0 ? slot0 : 2 * (r0 + i)) * group + head;
+  };
+  if (a.B <= kMergeScanMaxBatch) {
+    int before = 0, total = 0, nb = 0;  // units of the sequences before b, of all, of b
+    for (int base = 0; base < a.B; base += 32) {
+      const int bb = base + lane;
+      int v = 0;
+      if (bb < a.B) v = sparse ? seq_units<true>(a, bb).nb : seq_units<false>(a, bb).nb;
+      const int own = __shfl_sync(kFullMask, v, (b - base) & 31);
+      if (b >= base && b < base + 32) nb = own;
+      int sa = v, sb = bb < b ? v : 0;
 #pragma unroll
-    for (int e = 0; e < EPW; ++e) dst[e] = __float2bfloat16_rn(0.f);
-    return;
+      for (int o = 16; o > 0; o >>= 1) {
+        sa += __shfl_xor_sync(kFullMask, sa, o);
+        sb += __shfl_xor_sync(kFullMask, sb, o);
+      }
+      total += sa;
+      before += sb;
+    }
+    describe(before, total, nb);
+    // this warp's first batch of partials (see below): lane 8j + i, i < 4, prefetches a
+    // quarter of partial j's o row (512 bytes at d = 128), lane 8j + 4 its (m, l)
+    const int j = lane >> 3, q = lane & 7;
+    for (int jj = j; jj < 8; jj += 4) {
+      const int i = sub + wpr * jj;
+      if (i < np) {
+        const size_t en = entry(i);
+        if (q < 4) prefetch_l2(a.part_o + en * D + q * (D / 4));
+        else if (q == 4) prefetch_l2(a.part_ml + en);
+      }
+    }
   }
-  const int seg = a.layout[2 + b] + g * nb;
-  const int w0 = seg / per;
-  const int np = (seg + nb - 1) / per - w0 + 1;
-  if (np == 1) return;
-  const float2* ml = a.part_ml + (size_t)row * a.max_parts;
-  const float* po = a.part_o + (size_t)row * a.max_parts * D + lane * EPW;
-  // Partials in groups of 32: lane p holds (m, l) of partial p; the o loads of a group are
-  // independent of the weights, so one memory round trip covers a group.
+  grid_dependency_wait();  // the split kernel's partials (and, for large batches, its record)
+  grid_launch_dependents();
+  if (a.B > kMergeScanMaxBatch) {
+    // the record holds unit starts (already times Hkv) and unit counts per sequence
+    const int last = a.B - 1;
+    describe(__ldcg(a.layout + b) / a.Hkv,
+             (__ldcg(a.layout + last) + a.Hkv * __ldcg(a.layout + a.B + last)) / a.Hkv,
+             __ldcg(a.layout + a.B + b));
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (a.ctrl[1] != (uint32_t)part[kPartTickets]) record_error(a.err, PKV_DEV_DIRTY_WORKSPACE);
+    a.ctrl[0] = 0u;
+    a.ctrl[1] = 0u;
+  }
+  // this warp's partials i = sub + wpr p, p < npw, in batches of 8.  Every lane loads the
+  // batch's (m, l) pairs (one broadcast transaction each) together with its slice of the
+  // batch's o rows, so a batch costs one memory round trip.
+  const int npw = np > sub ? (np - sub + wpr - 1) / wpr : 0;
   float M = -INFINITY, L = 0.f;
   float acc[EPW];
 #pragma unroll
   for (int e = 0; e < EPW; ++e) acc[e] = 0.f;
-  for (int p0 = 0; p0 < np; p0 += 32) {
-    const int n = min(32, np - p0);
-    const float2 mlp = lane < n ? __ldcg(ml + p0 + lane) : make_float2(-INFINITY, 0.f);
-    float gmax = mlp.x;
+  for (int pb = 0; pb < npw; pb += 8) {
+    float2 ml[8];
+    float x[8][EPW];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(kFullMask, gmax, o));
-    const float M_new = fmaxf(M, gmax);
-    const float mref = (M_new == -INFINITY) ? 0.f : M_new;
-    const float carry = exp2f(M - mref);  // rescale what earlier groups accumulated
-    L *= carry;
+    for (int j = 0; j < 8; ++j) {
+      ml[j] = make_float2(-INFINITY, 0.f);
 #pragma unroll
-    for (int e = 0; e < EPW; ++e) acc[e] *= carry;
-    M = M_new;
-    const float w_lane = exp2f(mlp.x - mref);
-    float lsum = w_lane * mlp.y;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFullMask, lsum, o);
-    L += lsum;
-    // batches of 8 partials: all loads of a batch are issued before any is used
-    for (int pb = 0; pb < n; pb += 8) {
-      float x[8][EPW];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (pb + j < n) {
-          const float* src = po + (size_t)(p0 + pb + j) * D;
-          if constexpr (EPW == 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-            x[j][0] = v.x; x[j][1] = v.y; x[j][2] = v.z; x[j][3] = v.w;
-          } else {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-            x[j][0] = v.x; x[j][1] = v.y;
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float w = __shfl_sync(kFullMask, w_lane, (pb + j) & 31);
-        if (pb + j < n) {
-#pragma unroll
-          for (int e = 0; e < EPW; ++e) acc[e] += w * x[j][e];
+      for (int e = 0; e < EPW; ++e) x[j][e] = 0.f;
+      if (pb + j < npw) {
+        const size_t en = entry(sub + wpr * (pb + j));
+        ml[j] = __ldcg(a.part_ml + en);
+        const float* src = a.part_o + en * D + lane * EPW;
+        if constexpr (EPW == 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+          x[j][0] = v.x; x[j][1] = v.y; x[j][2] = v.z; x[j][3] = v.w;
+        } else {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+          x[j][0] = v.x; x[j][1] = v.y;
         }
       }
     }
+    float gmax = M;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) gmax = fmaxf(gmax, ml[j].x);
+    const float mref = (gmax == -INFINITY) ? 0.f : gmax;
+    const float carry = exp2f(M - mref);  // rescale what earlier batches accumulated
+    L *= carry;
+#pragma unroll
+    for (int e = 0; e < EPW; ++e) acc[e] *= carry;
+    M = gmax;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float w = exp2f(ml[j].x - mref);  // 0 for the padding entries
+      L += w * ml[j].y;
+#pragma unroll
+      for (int e = 0; e < EPW; ++e) acc[e] += w * x[j][e];
+    }
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  if (wpr > 1) {  // (uniform over the CTA) combine the row's wpr results
+    if (lane == 0) s_ml[warp] = make_float2(M, L);
+#pragma unroll
+    for (int e = 0; e < EPW; ++e) s_acc[warp][lane * EPW + e] = acc[e];
+    __syncthreads();
+    if (sub != 0) return;
+    float Mg = -INFINITY;
+    for (int w = 0; w < wpr; ++w) Mg = fmaxf(Mg, s_ml[warp + w].x);
+    const float mref = (Mg == -INFINITY) ? 0.f : Mg;
+    L = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPW; ++e) acc[e] = 0.f;
+    for (int w = 0; w < wpr; ++w) {
+      const float f = exp2f(s_ml[warp + w].x - mref);  // 0 for a warp without partials
+      L += f * s_ml[warp + w].y;
+#pragma unroll
+      for (int e = 0; e < EPW; ++e) acc[e] += f * s_acc[warp + w][lane * EPW + e];
+    }
+  }
+  if (np == 0 && !zero_row) return;
+  __nv_bfloat16* dst = a.out + (size_t)row * D + lane * EPW;
+  const float inv = L > 0.f ? 1.f / L : 0.f;  // a zero row has L = 0 and acc = 0
 #pragma unroll
   for (int e = 0; e < EPW; e += 2) {
     *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
@@ -679,18 +911,20 @@ size_t decode_smem_bytes(int head_dim, bool sparse, int batch) {
 }
 
 cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, size_t smem,
-                          cudaStream_t stream) {
+                          int merge_wpr_log2, cudaStream_t stream) {
   DecodeArgs args = a;
   args.G = k.group;
   void* split_params[] = {&args};
   cudaError_t e = launch_pdl(k.split, dim3(grid), dim3(kDecodeWarps * 32), smem, stream, split_params);
   if (e != cudaSuccess) return e;
   int group = k.group;
-  void* merge_params[] = {&args, &group};
-  const int rows = a.B * a.Hq;
-  const int mgrid = (rows + kMergeWarps - 1) / kMergeWarps;
+  int wpr_log2 = merge_wpr_log2;
+  void* merge_params[] = {&args, &group, &wpr_log2};
+  const long long rows = (long long)a.B * a.Hq;
+  const int rows_per_cta = kMergeWarps >> merge_wpr_log2;
+  const long long mgrid = (rows + rows_per_cta - 1) / rows_per_cta;
   if (mgrid == 0) return cudaSuccess;
-  return launch_pdl(k.merge, dim3(mgrid), dim3(kMergeWarps * 32), 0, stream, merge_params);
+  return launch_pdl(k.merge, dim3((unsigned)mgrid), dim3(kMergeWarps * 32), 0, stream, merge_params);
 }
 
 }  // namespace pkv

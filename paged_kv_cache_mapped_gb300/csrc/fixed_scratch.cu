@@ -55,21 +55,14 @@ extern "C" int pkv_paged_decode_attention_fixed_scratch(
     void* out, const void* q, const void* k_cache, const void* v_cache,
     const int32_t* block_tables, const int32_t* context_lens, float scale, int32_t window,
     const pkv_dims* dims, int32_t* error_word, void* stream) {
-  if (dims == nullptr) return PKV_ERR_NULL_POINTER;
-  // Refuse shapes whose partial results would not fit the fixed scratch (clear error,
-  // nothing enqueued).  Nothing in the scratch has to start at zero: every call rewrites
-  // the partition record and the partials it later reads.
-  const size_t need = pkv_decode_workspace_bytes(dims);
-  if (need == 0) {
-    // invalid dims: let the shared validation report the precise status
-    return pkv::decode_common(out, q, k_cache, v_cache, block_tables, context_lens, nullptr,
-                              nullptr, 0, scale, window, nullptr, 0, dims, error_word, stream,
-                              false);
-  }
-  if (need > (size_t)PKV_FIXED_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
+  // Invalid dims, and shapes whose partial results do not fit the fixed scratch, are
+  // refused by the shared validation before anything is enqueued (clear status).  The
+  // scratch's ticket counters start at zero (static storage) and every call leaves them so.
   void* scratch = nullptr;
-  const int st = pkv::fixed_scratch_address(&scratch);
-  if (st != PKV_OK) return st;
+  if (pkv_decode_workspace_bytes(dims) != 0) {
+    const int st = pkv::fixed_scratch_address(&scratch);
+    if (st != PKV_OK) return st;
+  }
   return pkv::decode_common(out, q, k_cache, v_cache, block_tables, context_lens, nullptr, nullptr,
                             0, scale, window, scratch, (size_t)PKV_FIXED_SCRATCH_BYTES, dims,
                             error_word, stream, false);

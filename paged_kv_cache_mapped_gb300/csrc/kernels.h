@@ -12,8 +12,12 @@
 
 namespace pkv {
 
-// Split-K decode: every consumer warp of the grid is an independent worker that owns a
-// contiguous range of the flattened (sequence, kv head, 16-token unit) list.
+// Split-K decode.  The flattened (sequence, kv head, 16-token unit) list is cut into one
+// slice of P units per worker warp.  A slice is a static head of S units, processed by the
+// warp of the same index, and cpw tail chunks of halving length that warps take from a
+// shared ticket counter once their head is done, so warps on faster SMs absorb the work of
+// slower ones.  Heads and chunks are the "ranges" of the partition; which warp runs a range never
+// changes what it computes, and its partial results go to fixed slots of the range.
 struct DecodeArgs {
   CUtensorMap tmap_k;            // dense mode: the K pool as a 2-D [NB*Hkv*16, D] bf16 tensor,
   CUtensorMap tmap_v;            //   box 64 x 16, 128-byte swizzle (likewise V)
@@ -29,15 +33,28 @@ struct DecodeArgs {
   __nv_bfloat16* k_pool_out;     // the pools again, writable (append mode)
   __nv_bfloat16* v_pool_out;
   __nv_bfloat16* out;            // [B, Hq, D]
-  int32_t* layout;               // [2 + (B+1) + B]: total units, units per warp, unit start, units per kv head
-  float2* part_ml;               // [B*Hq, max_parts] (running max in log2 units, running sum)
-  float* part_o;                 // [B*Hq, max_parts, D] unnormalised partial outputs
+  uint32_t* ctrl;                // [2]: tail-chunk ticket counter, chunks taken; zero between calls
+  int32_t* layout;               // [2B]: unit start (times Hkv) and units of each sequence, for large B
+  float2* part_ml;               // [2 ranges, G] (running max in log2 units, running sum)
+  float* part_o;                 // [2 ranges, G, D] unnormalised partial outputs
   int32_t* err;                  // device error word or nullptr
-  int B, Hq, Hkv, NB, MB, max_kept, window, max_parts, min_units;
+  int B, Hq, Hkv, NB, MB, max_kept, window;
+  int workers;                   // worker warps of the split grid
+  int min_units;                 // lower bound of the slice length P
+  int tail_pct;                  // share of a slice given out as tail chunks, in percent
+  int chunk_min;                 // lower bound of a chunk length (>= the tile ring depth)
+  int cpw_cap;                   // upper bound of the chunks per slice (workspace slots)
   int G;                         // query heads per kv head (1..kMaxGroup)
   float scale_log2;              // scale * log2(e): logits are kept in base-2 units
   unsigned long long timeout_ns; // bound of every mbarrier wait
 };
+
+// Partition record: computed from the total unit count and the worker count alone, so every
+// split CTA and every merge warp derives the same one.
+// kPartOff + c holds O_c, the start of tail chunk c within the tail (c = 0..cpw).
+enum PartField { kPartTotal = 0, kPartP, kPartS, kPartTail, kPartCpw, kPartNfull, kPartTickets, kPartWorkers, kPartOff };
+constexpr int kMaxTailChunksLimit = 7;  // cpw bound of the record (and of the range-id packing)
+constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 
 // Tuning knobs (compile-time; every setting computes the same result).
 #ifndef PKV_DECODE_WARPS
@@ -50,8 +67,24 @@ struct DecodeArgs {
 #define PKV_RING_D64 4
 #endif
 
+#ifndef PKV_MIN_UNITS
+#define PKV_MIN_UNITS 16  // lower bound of a worker slice, in 16-token units
+#endif
+#ifndef PKV_TAIL_PCT
+#define PKV_TAIL_PCT 20   // share of a slice handed out dynamically
+#endif
+#ifndef PKV_CHUNK_MIN
+#define PKV_CHUNK_MIN 6   // shortest tail chunk, in units (at least the tile ring depth)
+#endif
+#ifndef PKV_MAX_TAIL_CHUNKS
+#define PKV_MAX_TAIL_CHUNKS 4
+#endif
+#ifndef PKV_MERGE_PARTIALS_PER_WARP
+#define PKV_MERGE_PARTIALS_PER_WARP 16 // merge warps per row grow while a warp would take more
+#endif
+
 constexpr int kDecodeWarps = PKV_DECODE_WARPS;  // worker warps per CTA
-constexpr int kMinUnitsPerWarp = 16; // lower bound of a worker's range (bounds partial count)
+constexpr int kMaxWorkers = 2048;    // worker warps of a decode grid at most (sizes the workspace)
 constexpr int kMergeWarps = 8;
 constexpr int kMaxGroup = 8;         // query heads per kv head handled by one fragment
 
@@ -66,8 +99,9 @@ struct DecodeKernel {
 // Returns nullptr-filled struct (split == nullptr) when the combination is unsupported.
 DecodeKernel decode_kernel(int head_dim, int group, bool sparse);
 size_t decode_smem_bytes(int head_dim, bool sparse, int batch);
+// merge_wpr_log2: log2 of the merge warps per output row (0..3).
 cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, size_t smem,
-                          cudaStream_t stream);
+                          int merge_wpr_log2, cudaStream_t stream);
 
 // kv append / compaction / top-k selection.  kvops_device_setup() sets the kernels'
 // attributes on the current device (called once per device by the C ABI).
@@ -101,6 +135,14 @@ inline cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t 
   cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, kernel, args);
 }
+
+// Workspace of a decode call with partial slots for `ranges` ranges (api.cu).
+struct WorkspacePlan {
+  size_t ctrl_off, layout_off, ml_off, o_off, total;
+  long long ranges;
+};
+WorkspacePlan plan_workspace(const struct pkv_dims* d, long long ranges);
+WorkspacePlan fit_workspace(const struct pkv_dims* d, size_t bytes);
 
 // Validates a paged (sparse == false) or sparse decode call, sizes its partition and
 // launches it with `workspace` as scratch.  Defined in api.cu; returns a PKV status.

@@ -21,6 +21,12 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 
 // Makes initialised barriers visible to the async (TMA) proxy.
+// Retire an mbarrier (no thread waiting on it, no copy pending) so that it can be initialised
+// again from phase 0.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -187,6 +193,12 @@ __device__ __forceinline__ float bf16_hi_to_f32(uint32_t w) { return __uint_as_f
 // grid_dependency_wait() before touching global memory that kernel may produce or read.
 // grid_launch_dependents() lets the next such kernel start early (it will wait in turn).
 // Both are no-ops for kernels launched without the attribute.
+// Hint: bring the line holding p into L2 (no data returned; L2 is the coherence point, so a
+// line written afterwards is simply updated there).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }

@@ -42,14 +42,17 @@ def test_status_strings(lib):
 def test_workspace_queries(lib):
     d = _dims()
     n = lib.pkv_decode_workspace_bytes(ctypes.byref(d))
-    rows = 4 * 32
-    max_parts = (64 + 15) // 16 + 1
-    assert n >= rows * max_parts * (128 + 2) * 4 and n % 256 == 0
-    s = lib.pkv_sparse_decode_workspace_bytes(ctypes.byref(d), 1540)
-    assert s >= rows * ((97 + 15) // 16 + 1) * 130 * 4
+    # two partial slots of G heads x (d + 2) floats for each of 2048 static ranges and up to
+    # three tail chunks per slice, whatever the context length
+    assert n >= 2 * 2048 * 4 * 4 * (128 + 2) * 4 and n % 256 == 0
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(mb=8192))) == n
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(B=64))) >= n
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(hq=64))) > n      # G = 8
+    assert lib.pkv_sparse_decode_workspace_bytes(ctypes.byref(d), 1540) == n
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(bs=32))) == 0
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(d=96))) == 0
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(hq=30))) == 0
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(_dims(hq=32, hkv=2))) == 0  # G = 16
     assert lib.pkv_sparse_decode_workspace_bytes(ctypes.byref(d), 0) == 0
 
 

@@ -239,7 +239,7 @@ def test_fused_append_decode_llama8b_full_size():
 
 def test_workspace_reused_across_shapes():
     """One zero-filled workspace serves calls of different batch sizes and head counts in turn
-    (the per-segment arrival counters live in a fixed region partials never overwrite)."""
+    (every call leaves the ticket counters at its start zero)."""
     cases = [_small_case([700, 33, 1500], hq=8, hkv=2, d=128, seed=41),
              _small_case([90] * 16, hq=16, hkv=4, d=128, seed=42),
              _small_case([5000, 1, 2500, 17], hq=32, hkv=8, d=128, seed=43),
@@ -329,3 +329,87 @@ def test_random_shapes_fuzz(seed):
         torch.cuda.synchronize()
         assert np.array_equal(bits(case["k_cache"]), okc) and np.array_equal(bits(case["v_cache"]), ovc)
         assert_attn_close(out2, _oracle_rows(case, None, okc, ovc, window=window), f"fuzz append {seed}")
+
+
+def _llama8b_ws_case():
+    wl = W.WORKLOADS["llama8b"]
+    case = W.make_layer(wl, device=DEV, device_rng=True)
+    need = pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                      case["num_blocks"], case["max_blocks_per_seq"])
+    return wl, case, need
+
+
+def _decode_ws(case, ws, err=None):
+    out = pkv.paged_decode_attention(case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
+                                     case["context_lens"], case["scale"], workspace=ws, error_word=err)
+    torch.cuda.synchronize()
+    return out
+
+
+def test_dynamic_tail_chunks_deterministic_rearmed_and_checked():
+    """At the llama8b size every worker slice has tail chunks that warps take from a ticket
+    counter.  Which warp runs a chunk never changes what it computes, so repeated calls agree
+    bit for bit; every call leaves the counters zero; counters that were not zero at the call
+    (a workspace not zero-filled) are reported, and the call after that is clean again."""
+    wl, case, need = _llama8b_ws_case()
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    err = pkv.new_error_word(DEV)
+    outs = [_decode_ws(case, ws, err).clone() for _ in range(3)]
+    assert pkv.read_error(err) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert int(torch.count_nonzero(ws[:8])) == 0
+    rows = _sample_rows(wl.batch, wl.num_q_heads, 48, 21)
+    ref = _oracle_rows(case, rows)
+    assert_attn_close(outs[0].view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)], ref, "llama8b tail chunks")
+    dirty = pkv.header_constants()["PKV_DEV_DIRTY_WORKSPACE"]
+    for word, value in ((0, 3), (1, 7)):          # a stale ticket count, a stale taken count
+        ws[4 * word] = value
+        _decode_ws(case, ws, err)
+        assert pkv.read_error(err, clear=True) == dirty
+        assert int(torch.count_nonzero(ws[:8])) == 0
+        again = _decode_ws(case, ws, err)
+        assert pkv.read_error(err) == 0
+        assert torch.equal(again, outs[0])
+
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_smallest_accepted_workspace():
+    """A workspace holding the partials of 2048 ranges (static heads only) is accepted and
+    gives the same result up to summation order; 256 bytes less is refused."""
+    wl, case, need = _llama8b_ws_case()
+    B, G, d = wl.batch, wl.num_q_heads // wl.num_kv_heads, wl.head_dim
+    slots = 2 * 2048 * G
+    ml_off = _align256(256 + 4 * 2 * B)
+    smallest = _align256(_align256(ml_off + 8 * slots) + 4 * slots * d)
+    assert smallest < need
+    full = _decode_ws(case, torch.zeros(need, dtype=torch.uint8, device=DEV)).float()
+    err = pkv.new_error_word(DEV)
+    out = _decode_ws(case, torch.zeros(smallest, dtype=torch.uint8, device=DEV), err).float()
+    assert pkv.read_error(err) == 0
+    assert float((out - full).abs().max()) <= 1e-2
+    rows = _sample_rows(wl.batch, wl.num_q_heads, 24, 22)
+    assert_attn_close(out.view(-1, d)[torch.tensor(rows, device=DEV)], _oracle_rows(case, rows), "smallest ws")
+    with pytest.raises(pkv.PkvError) as e:
+        _decode_ws(case, torch.zeros(smallest - 256, dtype=torch.uint8, device=DEV))
+    assert e.value.status == pkv.header_constants()["PKV_ERR_WORKSPACE"]
+
+
+def test_large_batch_reads_split_record():
+    """Batches above 256 sequences take the merge path that reads the split kernel's record of
+    unit starts (smaller ones derive it from the lengths): 320 ragged sequences, some empty,
+    enough work for tail chunks."""
+    wl = W.Workload("batch320", 91, batch=320, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                    len_uniform=(0, 3000))
+    lens = W.context_lengths(wl)
+    lens[::37] = 0
+    case = W.make_layer(wl, device=DEV, lengths=lens, device_rng=True)
+    err = pkv.new_error_word(DEV)
+    out = _run(case, err=err)
+    assert pkv.read_error(err) == 0
+    rows = sorted(set(_sample_rows(wl.batch, wl.num_q_heads, 160, 23)) | {37 * 8, 37 * 8 + 7})
+    ref = _oracle_rows(case, rows)
+    assert_attn_close(out.view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)], ref, "batch 320")
+    assert torch.count_nonzero(out[::37]) == 0

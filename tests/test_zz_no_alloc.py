@@ -5,8 +5,8 @@ device allocator of its own, or a host runtime that owns the device heap and for
 cudaMalloc -- by keeping its split-K scratch in a fixed static device array inside the
 library.  These tests call it through the C ABI (ctypes on libpkv.so, no Python helper in
 between) twice in a row and compare both results with the workspace-taking entry point,
-within the same tolerance the other attention tests use.  They also check that a shape too
-large for the fixed scratch is refused.  This file is collected last, and each test builds
+within the same tolerance the other attention tests use.  They also check that a shape whose
+partial results do not fit the fixed scratch (G = 8 at head_dim 128) is refused.  This file is collected last, and each test builds
 its own inputs, so it passes alone in a fresh process as well as after the other tests.
 """
 import ctypes
@@ -44,7 +44,7 @@ def _fixed(case, out, window=0, err=None):
 def _with_workspace(case, window=0):
     dims = _dims(case)
     lib = _lib.load()
-    ws = torch.empty(lib.pkv_decode_workspace_bytes(ctypes.byref(dims)), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(lib.pkv_decode_workspace_bytes(ctypes.byref(dims)), dtype=torch.uint8, device=DEV)
     out = torch.empty_like(case["q"])
     stream = ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)
     st = lib.pkv_paged_decode_attention(
@@ -75,10 +75,12 @@ def test_fixed_scratch_matches_workspace_entry_point_twice(name, window):
 
 
 def test_fixed_scratch_refuses_oversized_shapes():
-    # batch 4 x 32 heads over 131072-token contexts needs ~34 MB of scratch: refused, nothing run
-    wl = W.WORKLOADS["long128k"]
-    lens = torch.tensor([64] * 4, dtype=torch.int32)
-    case = W.make_layer(wl, device=DEV, lengths=lens, num_blocks=32, max_blocks=8192)
+    # G = 8 query heads per kv head at d = 128: the partials of 2048 worker ranges take
+    # ~17 MB, more than the fixed scratch holds: refused, nothing run
+    B, hq, hkv, d = 2, 64, 8, 128
+    lens = torch.tensor([40, 17], dtype=torch.int32)
+    wl = W.Workload("g8", 90, batch=B, num_q_heads=hq, num_kv_heads=hkv, head_dim=d)
+    case = W.make_layer(wl, device=DEV, lengths=lens, num_blocks=8, max_blocks=4)
     need = _lib.load().pkv_decode_workspace_bytes(ctypes.byref(_dims(case)))
     assert need > C["PKV_FIXED_SCRATCH_BYTES"]
     out = torch.zeros_like(case["q"])

@@ -80,10 +80,12 @@ def _load():
             lib.oracle_sparse_decode.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                                  i64, i32, f64, P, i64]
             lib.oracle_select_topk.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, i32]
+            lib.oracle_decode_scores.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, i32,
+                                                 f64, i32, i64, P, i64]
             lib.oracle_compact.argtypes = [P, P, P, i64, i32, P, P, P, P, P, P, i32, i32, i32,
                                            i32, i64, i32]
             for name in ("oracle_kv_append", "oracle_paged_decode", "oracle_sparse_decode",
-                         "oracle_select_topk", "oracle_compact"):
+                         "oracle_select_topk", "oracle_compact", "oracle_decode_scores"):
                 getattr(lib, name).restype = i32
             _lib = lib
     return _lib
@@ -171,6 +173,37 @@ def sparse_decode(q, k_cache, v_cache, block_tables, context_lens, kept, kept_le
                                         bt.shape[1], float(scale), None if r is None else _ptr(r), n),
            "sparse_decode")
     return out.reshape(b, hq, d) if rows is None else out
+
+
+def decode_scores(q, k_cache, block_tables, context_lens, scale, window=0, stride=None, segs=None):
+    """fp64 sparsification score of one decode step and the rows' log-sum-exp.
+
+    segs=None -> (score_add [B, Hkv, stride], lse [B, Hq]); else a list of b*Hkv+g ->
+    (score_add [len(segs), stride], lse [len(segs), G]).  stride defaults to max L_b."""
+    q = _arr(q, np.uint16)
+    kc = _arr(k_cache, np.uint16)
+    bt = _arr(block_tables, np.int32)
+    lens = _arr(context_lens, np.int32)
+    b, hq, d = q.shape
+    nb, hkv, bs, d2 = kc.shape
+    assert bs == 16 and d2 == d and bt.shape[0] == b
+    g = hq // hkv
+    if stride is None:
+        stride = max(int(lens.max()) if lens.size else 0, 1)
+    if segs is None:
+        s_arr, n = None, b * hkv
+    else:
+        s_arr = _arr(np.asarray(segs, dtype=np.int64), np.int64)
+        n = s_arr.shape[0]
+    score = np.zeros((n, stride), dtype=np.float64)
+    lse = np.zeros((n, g), dtype=np.float64)
+    _check(_load().oracle_decode_scores(_ptr(score), _ptr(lse), _ptr(q), _ptr(kc), _ptr(bt), _ptr(lens),
+                                        b, hq, hkv, d, nb, bt.shape[1], float(scale), int(window),
+                                        int(stride), None if s_arr is None else _ptr(s_arr), n),
+           "decode_scores")
+    if segs is None:
+        return score.reshape(b, hkv, stride), lse.reshape(b, hq)
+    return score, lse
 
 
 def select_topk(scores, context_lens, n_sink, n_recent, k_top):

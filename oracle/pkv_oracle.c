@@ -261,6 +261,111 @@ int oracle_sparse_decode(double* out, const uint16_t* q, const uint16_t* k_cache
   return status;
 }
 
+/*
+ * Logits of one query row over an explicit list of logical positions:
+ * logits[j] = scale * sum_e q[e] * K_{tokens[j]}[e]  (as in attend_one_row).
+ */
+static int row_logits(double* logits, const uint16_t* q_row, const uint16_t* k_cache,
+                      const int32_t* block_row, int max_blocks_per_seq, int64_t num_blocks,
+                      int num_kv_heads, int head_dim, int kv_head, double scale,
+                      const int64_t* tokens, int64_t n_tokens) {
+  for (int64_t j = 0; j < n_tokens; ++j) {
+    int64_t t = tokens[j];
+    int64_t logical_block = t / ORC_BLOCK;
+    if (t < 0 || logical_block >= max_blocks_per_seq) return ORC_ERR_INDEX;
+    int64_t physical = block_row[logical_block];
+    if (physical < 0 || physical >= num_blocks) return ORC_ERR_BLOCK;
+    int64_t row = ((physical * num_kv_heads + kv_head) * ORC_BLOCK + t % ORC_BLOCK) * head_dim;
+    double dot = 0.0;
+    for (int e = 0; e < head_dim; ++e)
+      dot += bf16_to_double(q_row[e]) * bf16_to_double(k_cache[row + e]);
+    logits[j] = scale * dot;
+  }
+  return ORC_OK;
+}
+
+/*
+ * Sparsification score of one decode step ([novita] section "2. Attention modification",
+ * the scoring step built on FlashAttention): the attention pass yields each query row's
+ * maximum logit m (rowmax) and normaliser l = sum_t exp(s_t - m); a second step turns every
+ * attended key's logit into its softmax probability p_t = exp(s_t - m) / l and sums those
+ * probabilities into the key's score.  One KV row serves the G query heads of its kv head,
+ * so the score of (b, kv head g, position t) adds the probabilities of those G heads.
+ * For each listed segment seg = b * Hkv + g (all B*Hkv when seg_ids is NULL):
+ *   score_add[seg][t] = sum over the group's heads h of p_{h,t}   (t attended; 0 elsewhere),
+ *   lse[seg][i]      = m + log(l) of head h = g*G + i              (the row's log-sum-exp).
+ * The attended set is that of oracle_paged_decode (window as there); stride >= every L_b.
+ * An empty set gives a zero score row and lse = -infinity.
+ */
+int oracle_decode_scores(double* score_add, double* lse, const uint16_t* q,
+                         const uint16_t* k_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, int batch, int num_q_heads,
+                         int num_kv_heads, int head_dim, int64_t num_blocks,
+                         int max_blocks_per_seq, double scale, int window, int64_t stride,
+                         const int64_t* seg_ids, int64_t n_segs) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return ORC_ERR_ARG;
+  if (num_q_heads % num_kv_heads != 0 || stride < 0) return ORC_ERR_ARG;
+  int group = num_q_heads / num_kv_heads;
+  int64_t total = seg_ids ? n_segs : (int64_t)batch * num_kv_heads;
+  int status = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < total; ++r) {
+    int64_t seg = seg_ids ? seg_ids[r] : r;
+    int b = (int)(seg / num_kv_heads);
+    int g = (int)(seg % num_kv_heads);
+    double* score = score_add + r * stride;
+    for (int64_t t = 0; t < stride; ++t) score[t] = 0.0;
+    int st = ORC_OK;
+    if (b < 0 || b >= batch) {
+      st = ORC_ERR_ARG;
+    } else {
+      int64_t len = context_lens[b];
+      int64_t start = 0;
+      if (len < 0 || len > (int64_t)max_blocks_per_seq * ORC_BLOCK || len > stride) {
+        st = ORC_ERR_LEN;
+      } else {
+        if (window > 0 && len > window) start = len - window;
+        int64_t n = len - start;
+        int64_t* tokens = (int64_t*)malloc((size_t)(n > 0 ? n : 1) * sizeof(int64_t));
+        double* logits = (double*)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+        if (!tokens || !logits) {
+          st = ORC_ERR_MEM;
+        } else {
+          for (int64_t j = 0; j < n; ++j) tokens[j] = start + j;
+          for (int i = 0; i < group && st == ORC_OK; ++i) {
+            int h = g * group + i;
+            double* lse_out = lse + r * group + i;
+            if (n == 0) {
+              *lse_out = -INFINITY;
+              continue;
+            }
+            st = row_logits(logits, q + ((int64_t)b * num_q_heads + h) * head_dim, k_cache,
+                            block_tables + (int64_t)b * max_blocks_per_seq, max_blocks_per_seq,
+                            num_blocks, num_kv_heads, head_dim, g, scale, tokens, n);
+            if (st != ORC_OK) break;
+            /* first pass: rowmax and l */
+            double m = logits[0];
+            for (int64_t j = 1; j < n; ++j)
+              if (logits[j] > m) m = logits[j];
+            double l = 0.0;
+            for (int64_t j = 0; j < n; ++j) l += exp(logits[j] - m);
+            /* second pass: probabilities, summed into the keys' scores */
+            for (int64_t j = 0; j < n; ++j) score[tokens[j]] += exp(logits[j] - m) / l;
+            *lse_out = m + log(l);
+          }
+        }
+        free(tokens);
+        free(logits);
+      }
+    }
+    if (st != ORC_OK) {
+#pragma omp critical
+      status = st;
+    }
+  }
+  return status;
+}
+
 /* Candidate ordering for the top-k: higher score first; equal scores, lower position first. */
 typedef struct {
   double score;

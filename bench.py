@@ -376,11 +376,50 @@ def run_secondary(pkv, W, dev, stream, args):
                               "l2": "2.1 GB of K/V per launch (> L2)"}
     del c, ws, out
     torch.cuda.empty_cache()
+    res["llama8b_decode_with_scores"] = _scores_row(pkv, W, dev, stream, args, hbm)
+    torch.cuda.empty_cache()
     res["qwen1p5b_step"] = _qwen_step(pkv, W, dev, stream, args, hbm)
     torch.cuda.empty_cache()
     res.update(_sparse_step(pkv, W, dev, stream, args, hbm))
     torch.cuda.empty_cache()
     return res
+
+
+def _scores_row(pkv, W, dev, stream, args, hbm):
+    """llama8b decode layer with the sparsification score emitted (logits kept, then turned
+    into probabilities added to the scores), against the same decode without it."""
+    wl = W.WORKLOADS["llama8b"]
+    c = W.make_layer(wl, device=dev, device_rng=True)
+    stride = c["max_blocks_per_seq"] * 16
+    ws = torch.zeros(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                c["num_blocks"], c["max_blocks_per_seq"]),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(c["q"])
+    acc = torch.zeros((wl.batch, wl.num_kv_heads, stride), dtype=torch.float32, device=dev)
+    lse = torch.empty((wl.batch, wl.num_q_heads), dtype=torch.float32, device=dev)
+    logits = torch.empty((wl.batch, wl.num_q_heads, stride), dtype=torch.float32, device=dev)
+
+    def plain():
+        pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
+                                   c["scale"], out=out, workspace=ws, stream=stream)
+
+    def scored():
+        pkv.paged_decode_attention_scores(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                          c["context_lens"], c["scale"], acc, out=out, lse=lse, logits=logits,
+                                          workspace=ws, stream=stream)
+    steps = max(5, args.steps // 4)
+    ms_plain = _time(plain, args.warmup, steps, dev, stream)
+    ms_scored = _time(scored, args.warmup, steps, dev, stream)
+    lens = c["context_lens"].cpu()
+    kv = decode_bytes(lens, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
+    keys = int(lens.to(torch.int64).sum()) * wl.num_kv_heads
+    extra = keys * (wl.group * 4 * 2 + 4 * 2)  # logits written and read back, scores read and written
+    del c, ws, out, acc, logits
+    return {"ms": round(ms_scored, 4), "ms_without_scores": round(ms_plain, 4),
+            "overhead": round(ms_scored / ms_plain - 1.0, 4),
+            "gbs": round((kv + extra) / (ms_scored * 1e-3) / 1e9, 1),
+            "frac": round((kv + extra) / (ms_scored * 1e-3) / 1e9 / hbm, 4),
+            "score_bytes": extra, "l2": "one 0.58 GB pool (> L2)"}
 
 
 def _graph_time(calls, warmup, steps, dev, stream):

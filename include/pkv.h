@@ -169,6 +169,41 @@ int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, v
                                       int32_t* error_word, void* stream);
 
 /*
+ * pkv_paged_decode_attention_scores -- pkv_paged_decode_attention (with this step's append
+ * when k_new and v_new are given, as pkv_paged_decode_attention_append) that also produces
+ * the step's sparsification score: the scoring of "How KV Sparsity Achieves 1.5x
+ * Acceleration for vLLM", section "2. Attention modification" -- the attention pass already
+ * has each row's maximum and normaliser (rowmax / l), so every attended key's softmax
+ * probability is exp(s - rowmax) / l, and a key's score is the sum of such probabilities.
+ * A kv head's key serves the G query heads of its group, so its score adds their G
+ * probabilities.  The pages' kernel recomputes q . k in a second pass; here the decode keeps
+ * every attended key's logit (4 bytes per query head and key) and a light second kernel
+ * turns them into probabilities, which reads far fewer bytes than reading K again.
+ *   lse_out        : [B, Hq] fp32: natural log-sum-exp of each row's attended logits
+ *                    (-infinity when nothing is attended).
+ *   score_accum    : [B, Hkv, score_stride] fp32, updated in place: for every attended
+ *                    position t < score_stride of (b, kv head g),
+ *                    score_accum[b][g][t] += sum over h in g's group of p_{b,h,t}.
+ *                    Other positions are left unchanged.
+ *   logits         : [B, Hq, score_stride] fp32 scratch, caller-owned; contents on return
+ *                    unspecified.
+ *   score_stride   : > 0; should be >= every L_b (max_blocks_per_seq * 16 always is): keys
+ *                    at positions >= score_stride get no score and the call records
+ *                    PKV_DEV_BAD_CONTEXT_LEN.
+ *   k_new, v_new   : both NULL (no append) or both set, as pkv_paged_decode_attention_append.
+ *   other arguments: as pkv_paged_decode_attention.  out is bit-identical to what that call
+ *                    (or the append variant) writes for the same inputs and workspace size.
+ * Same device error codes as pkv_paged_decode_attention.
+ */
+int pkv_paged_decode_attention_scores(void* out, float* lse_out, float* score_accum, float* logits,
+                                      int32_t score_stride, const void* q, void* k_cache,
+                                      void* v_cache, const void* k_new, const void* v_new,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      float scale, int32_t window, void* workspace,
+                                      size_t workspace_bytes, const pkv_dims* dims,
+                                      int32_t* error_word, void* stream);
+
+/*
  * pkv_sparse_decode_workspace_bytes -- workspace for pkv_sparse_decode_attention with
  * kept lists of row length max_kept: the same size and rules as pkv_decode_workspace_bytes
  * (it does not depend on max_kept).  Returns 0 if the arguments are invalid.

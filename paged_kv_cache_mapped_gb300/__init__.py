@@ -20,6 +20,7 @@ __all__ = [
     "sparse_decode_workspace_bytes", "sparse_decode_attention", "kv_select_topk", "kv_compact",
     "read_error", "new_error_word", "header_constants", "header_functions",
     "paged_decode_attention_fixed_scratch", "paged_decode_attention_append",
+    "paged_decode_attention_scores",
 ]
 
 BLOCK_SIZE = 16
@@ -169,6 +170,48 @@ def paged_decode_attention_append(q, k_cache, v_cache, k_new, v_new, block_table
         _ptr(block_tables), _ptr(context_lens), float(scale), int(window), _ptr(workspace),
         workspace.numel(), ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
     return out
+
+
+def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_lens, scale, score_accum,
+                                  window=0, *, k_new=None, v_new=None, out=None, lse=None, logits=None,
+                                  workspace=None, error_word=None, stream=None):
+    """paged_decode_attention (with the step's append when k_new/v_new are given) that also
+    adds the step's sparsification score into score_accum [B, Hkv, S] fp32: for every attended
+    key t < S of (b, kv head g), the sum over g's query heads of their softmax probability of
+    t.  Returns (out [B, Hq, d] bf16, lse [B, Hq] fp32: each row's natural log-sum-exp).
+    logits [B, Hq, S] fp32 is scratch (allocated when not given)."""
+    dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    _need(score_accum, "score_accum", torch.float32, 3, dev)
+    if score_accum.shape[:2] != (dims.batch, dims.num_kv_heads):
+        raise ValueError("score_accum must be [B, Hkv, S]")
+    stride = score_accum.shape[2]
+    if (k_new is None) != (v_new is None):
+        raise ValueError("give both k_new and v_new, or neither")
+    if k_new is not None:
+        _need(k_new, "k_new", torch.bfloat16, 3, dev)
+        _need(v_new, "v_new", torch.bfloat16, 3, dev)
+        if k_new.shape != (dims.batch, dims.num_kv_heads, dims.head_dim) or v_new.shape != k_new.shape:
+            raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
+    if lse is None:
+        lse = torch.empty((dims.batch, dims.num_q_heads), dtype=torch.float32, device=dev)
+    else:
+        _need(lse, "lse", torch.float32, 2, dev)
+        if lse.shape != (dims.batch, dims.num_q_heads):
+            raise ValueError("lse must be [B, Hq]")
+    if logits is None:
+        logits = torch.empty((dims.batch, dims.num_q_heads, stride), dtype=torch.float32, device=dev)
+    else:
+        _need(logits, "logits", torch.float32, 3, dev)
+        if logits.shape != (dims.batch, dims.num_q_heads, stride):
+            raise ValueError("logits must be [B, Hq, S]")
+    nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
+    out, workspace = _out_ws(q, out, workspace, nbytes)
+    check("pkv_paged_decode_attention_scores", load().pkv_paged_decode_attention_scores(
+        _ptr(out), _ptr(lse), _ptr(score_accum), _ptr(logits), int(stride), _ptr(q), _ptr(k_cache),
+        _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(context_lens), float(scale),
+        int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims), _ptr(error_word),
+        _stream(stream, dev)))
+    return out, lse
 
 
 def paged_decode_attention_fixed_scratch(q, k_cache, v_cache, block_tables, context_lens, scale,

@@ -23,7 +23,8 @@ constexpr int kNumGroups = 1;
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
-  size_t max_dyn_smem[2][2] = {};  // [head_dim index][sparse]: opt-in minus the kernel's static
+  size_t max_dyn_smem[2][3] = {};  // [head_dim index][mode: dense, sparse, dense + scores]:
+                                   //   opt-in minus the kernel's static shared memory
   int merge_ctas_per_sm[2] = {};   // [head_dim index]: resident merge CTAs per SM
 };
 
@@ -54,8 +55,8 @@ const DeviceInfo* device_info(int* status) {
     }
     for (int hd = 0; hd < kNumHeadDims; ++hd) {
       for (int gi = 0; gi < kNumGroups; ++gi) {
-        for (int sp = 0; sp < 2; ++sp) {
-          const DecodeKernel k = decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp != 0);
+        for (int sp = 0; sp < 3; ++sp) {
+          const DecodeKernel k = decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp == 1, sp == 2);
           if (k.split == nullptr) continue;
           cudaFuncAttributes fa{};
           cudaError_t e = cudaFuncGetAttributes(&fa, k.split);
@@ -203,7 +204,8 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
                   const int32_t* block_tables, const int32_t* context_lens, const int32_t* kept,
                   const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
                   void* workspace, size_t workspace_bytes, const pkv_dims* dims, int32_t* err,
-                  void* stream, bool sparse, const void* k_new, const void* v_new) {
+                  void* stream, bool sparse, const void* k_new, const void* v_new,
+                  const ScoreOutputs* score_out) {
   int st = check_dims(dims, true);
   if (st != PKV_OK) return st;
   if (dims->batch > kMaxBatch) return PKV_ERR_DIMS;
@@ -216,7 +218,15 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
       !aligned16(workspace))
     return PKV_ERR_ALIGNMENT;
   const int group = dims->num_q_heads / dims->num_kv_heads;
-  const DecodeKernel k = decode_kernel(dims->head_dim, group, sparse);
+  if (score_out != nullptr) {
+    if (sparse) return PKV_ERR_ARGUMENT;
+    if (!score_out->lse || !score_out->scores || !score_out->logits) return PKV_ERR_NULL_POINTER;
+    if (score_out->stride <= 0) return PKV_ERR_DIMS;
+    if ((reinterpret_cast<uintptr_t>(score_out->lse) | reinterpret_cast<uintptr_t>(score_out->scores) |
+         reinterpret_cast<uintptr_t>(score_out->logits)) & 3u)
+      return PKV_ERR_ALIGNMENT;
+  }
+  const DecodeKernel k = decode_kernel(dims->head_dim, group, sparse, score_out != nullptr);
   if (k.split == nullptr) return PKV_ERR_GQA;
   const int max_units = sparse ? (max_kept + 15) / 16 : dims->max_blocks_per_seq;
   // the flattened unit count and the pool's row count (a TMA coordinate) must fit int32
@@ -230,7 +240,8 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   const DeviceInfo* info = device_info(&st);
   if (!info) return st;
   const size_t smem = decode_smem_bytes(dims->head_dim, sparse, dims->batch);
-  if (smem > info->max_dyn_smem[head_dim_index(dims->head_dim)][sparse ? 1 : 0]) return PKV_ERR_DIMS;
+  if (smem > info->max_dyn_smem[head_dim_index(dims->head_dim)][sparse ? 1 : (score_out ? 2 : 0)])
+    return PKV_ERR_DIMS;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.split, kDecodeWarps * 32, smem);
   if (e != cudaSuccess) return cuda_status(e);
@@ -261,6 +272,12 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.layout = reinterpret_cast<int32_t*>(ws + plan.layout_off);
   a.part_ml = reinterpret_cast<float2*>(ws + plan.ml_off);
   a.part_o = reinterpret_cast<float*>(ws + plan.o_off);
+  if (score_out != nullptr) {
+    a.logits = score_out->logits;
+    a.lse = score_out->lse;
+    a.scores = score_out->scores;
+    a.score_stride = score_out->stride;
+  }
   a.err = err;
   a.B = dims->batch;
   a.Hq = dims->num_q_heads;
@@ -335,6 +352,21 @@ int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, v
   return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, nullptr, nullptr, 0,
                        scale, window, workspace, workspace_bytes, dims, error_word, stream, false,
                        k_new, v_new);
+}
+
+int pkv_paged_decode_attention_scores(void* out, float* lse_out, float* score_accum, float* logits,
+                                      int32_t score_stride, const void* q, void* k_cache,
+                                      void* v_cache, const void* k_new, const void* v_new,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      float scale, int32_t window, void* workspace,
+                                      size_t workspace_bytes, const pkv_dims* dims,
+                                      int32_t* error_word, void* stream) {
+  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_NULL_POINTER;
+  if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_ALIGNMENT;
+  const ScoreOutputs so{lse_out, score_accum, logits, score_stride};
+  return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, nullptr, nullptr, 0,
+                       scale, window, workspace, workspace_bytes, dims, error_word, stream, false,
+                       k_new, v_new, &so);
 }
 
 size_t pkv_sparse_decode_workspace_bytes(const pkv_dims* dims, int32_t max_kept) {

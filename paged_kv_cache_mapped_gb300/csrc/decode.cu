@@ -235,9 +235,15 @@ __device__ void make_partition(int32_t* p, int total, int nw, const DecodeArgs& 
     p[kPartOff + c] = cpw > 0 ? T - (int)((long long)T * ((1 << (cpw - c)) - 1) / ((1 << cpw) - 1)) : 0;
 }
 
-template <int D, bool SPARSE>
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// SCORES (dense only): also keep every attended key's base-2 logit and write the log-sum-exp of
+// rows written out directly, for the score step (decode_score_kernel).
+template <int D, bool SPARSE, bool SCORES>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_split_kernel(const __grid_constant__ DecodeArgs a) {
+  static_assert(!(SPARSE && SCORES), "scores are emitted by the dense decode only");
   using GE = Geo<D, SPARSE>;
   using WT = WarpTiles<D, SPARSE>;
   using WB = WarpSlots<D, SPARSE>;
@@ -284,6 +290,9 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
     const SeqUnits su = seq_units<SPARSE>(a, b);
     if (su.err != 0 && blockIdx.x == 0) record_error(a.err, su.err);
+    if constexpr (SCORES) {  // a context longer than the score rows: its keys beyond them get no score
+      if (su.len > a.score_stride && blockIdx.x == 0) record_error(a.err, PKV_DEV_BAD_CONTEXT_LEN);
+    }
     s_nb[b] = su.nb;
     s_first[b] = su.first;
     s_lo[b] = su.lo;
@@ -509,6 +518,9 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       const float m = hh ? mr1 : mr0;
       const size_t row = (size_t)seg_b * a.Hq + (size_t)seg_g * G + head;
       if (seg_slot < 0) {
+        if constexpr (SCORES) {  // the row's log-sum-exp: m is the reference l is relative to
+          if (gq == 0) a.lse[row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        }
         const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16* dst = a.out + row * D + gq;
 #pragma unroll
@@ -616,6 +628,18 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       const float s01 = (t0 && v1) ? c[1] * sl2 : -INFINITY;
       const float s10 = (t1 && v0) ? c[2] * sl2 : -INFINITY;
       const float s11 = (t1 && v1) ? c[3] * sl2 : -INFINITY;
+      if constexpr (SCORES) {  // keep the attended keys' logits for the score step
+        const int tok = (s_first[cc.b] + cc.j) * 16 + gq;
+        float* lg = a.logits + ((size_t)cc.b * a.Hq + (size_t)cc.g * G + 2 * tq) * a.score_stride + tok;
+        if (tok < a.score_stride) {
+          if (t0 && v0) lg[0] = s00;
+          if (t0 && v1) lg[a.score_stride] = s01;
+        }
+        if (tok + 8 < a.score_stride) {
+          if (t1 && v0) lg[8] = s10;
+          if (t1 && v1) lg[a.score_stride + 8] = s11;
+        }
+      }
       float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
       for (int m = 4; m <= 16; m <<= 1) {
@@ -860,6 +884,7 @@ decode_merge_kernel(const DecodeArgs a, int group, int wpr_log2) {
       for (int e = 0; e < EPW; ++e) acc[e] += w * x[j][e];
     }
   }
+  float m_ref = (M == -INFINITY) ? 0.f : M;  // the reference L is relative to
   if (wpr > 1) {  // (uniform over the CTA) combine the row's wpr results
     if (lane == 0) s_ml[warp] = make_float2(M, L);
 #pragma unroll
@@ -869,6 +894,7 @@ decode_merge_kernel(const DecodeArgs a, int group, int wpr_log2) {
     float Mg = -INFINITY;
     for (int w = 0; w < wpr; ++w) Mg = fmaxf(Mg, s_ml[warp + w].x);
     const float mref = (Mg == -INFINITY) ? 0.f : Mg;
+    m_ref = mref;
     L = 0.f;
 #pragma unroll
     for (int e = 0; e < EPW; ++e) acc[e] = 0.f;
@@ -880,6 +906,8 @@ decode_merge_kernel(const DecodeArgs a, int group, int wpr_log2) {
     }
   }
   if (np == 0 && !zero_row) return;
+  if (a.lse != nullptr && lane == 0)  // scores mode: the row's natural log-sum-exp
+    a.lse[row] = L > 0.f ? (m_ref + log2f(L)) * kLn2 : -INFINITY;
   __nv_bfloat16* dst = a.out + (size_t)row * D + lane * EPW;
   const float inv = L > 0.f ? 1.f / L : 0.f;  // a zero row has L = 0 and acc = 0
 #pragma unroll
@@ -888,19 +916,51 @@ decode_merge_kernel(const DecodeArgs a, int group, int wpr_log2) {
   }
 }
 
+// The score step ([novita] "2. Attention modification": with each row's max and sum from the
+// attention pass, every attended key's probability is exp(s - m) / l = exp(s - lse); a key's
+// score adds the probabilities of the G query heads sharing its kv head):
+//   scores[b, g, t] += sum_i 2^(logit[b, gG + i, t] - lse[b, gG + i] log2 e)
+// over the attended t < score_stride.  One thread per key, tiles of 256 keys per (b, g); reads
+// G logits and writes one score per key, all coalesced.
+__global__ void __launch_bounds__(256) decode_score_kernel(const DecodeArgs a, int group, int tiles) {
+  const int seg = blockIdx.x / tiles;  // b * Hkv + g
+  const int tile = blockIdx.x - seg * tiles;
+  grid_dependency_wait();  // the logits and log-sum-exps of the decode
+  grid_launch_dependents();
+  const int b = seg / a.Hkv;
+  const int g = seg - b * a.Hkv;
+  int L = a.context_lens[b];
+  if (L < 0 || L > a.MB * 16) L = 0;  // reported by the split kernel
+  const int start = (a.window > 0 && L > a.window) ? L - a.window : 0;
+  const int end = min(L, a.score_stride);
+  const int t = start + tile * 256 + (int)threadIdx.x;
+  if (t >= end) return;
+  const size_t row0 = (size_t)b * a.Hq + (size_t)g * group;
+  float sum = 0.f;
+  for (int i = 0; i < group; ++i) {
+    const float lse2 = a.lse[row0 + i] * kLog2e;
+    sum += exp2f(a.logits[(row0 + i) * a.score_stride + t] - lse2);
+  }
+  a.scores[(size_t)seg * a.score_stride + t] += sum;
+}
+
 }  // namespace
 
-DecodeKernel decode_kernel(int head_dim, int group, bool sparse) {
-  if (group < 1 || group > kMaxGroup) return DecodeKernel{nullptr, nullptr, head_dim, group, sparse};
+DecodeKernel decode_kernel(int head_dim, int group, bool sparse, bool scores) {
+  const DecodeKernel none{nullptr, nullptr, nullptr, head_dim, group, sparse, scores};
+  if (group < 1 || group > kMaxGroup || (sparse && scores)) return none;
+  const void* score = scores ? (const void*)decode_score_kernel : nullptr;
   if (head_dim == 128)
-    return DecodeKernel{sparse ? (const void*)decode_split_kernel<128, true>
-                               : (const void*)decode_split_kernel<128, false>,
-                        (const void*)decode_merge_kernel<128>, 128, group, sparse};
+    return DecodeKernel{sparse   ? (const void*)decode_split_kernel<128, true, false>
+                        : scores ? (const void*)decode_split_kernel<128, false, true>
+                                 : (const void*)decode_split_kernel<128, false, false>,
+                        (const void*)decode_merge_kernel<128>, score, 128, group, sparse, scores};
   if (head_dim == 64)
-    return DecodeKernel{sparse ? (const void*)decode_split_kernel<64, true>
-                               : (const void*)decode_split_kernel<64, false>,
-                        (const void*)decode_merge_kernel<64>, 64, group, sparse};
-  return DecodeKernel{nullptr, nullptr, head_dim, group, sparse};
+    return DecodeKernel{sparse   ? (const void*)decode_split_kernel<64, true, false>
+                        : scores ? (const void*)decode_split_kernel<64, false, true>
+                                 : (const void*)decode_split_kernel<64, false, false>,
+                        (const void*)decode_merge_kernel<64>, score, 64, group, sparse, scores};
+  return none;
 }
 
 size_t decode_smem_bytes(int head_dim, bool sparse, int batch) {
@@ -924,7 +984,17 @@ cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, 
   const int rows_per_cta = kMergeWarps >> merge_wpr_log2;
   const long long mgrid = (rows + rows_per_cta - 1) / rows_per_cta;
   if (mgrid == 0) return cudaSuccess;
-  return launch_pdl(k.merge, dim3((unsigned)mgrid), dim3(kMergeWarps * 32), 0, stream, merge_params);
+  e = launch_pdl(k.merge, dim3((unsigned)mgrid), dim3(kMergeWarps * 32), 0, stream, merge_params);
+  if (e != cudaSuccess || !k.scores) return e;
+  // score step: tiles of 256 keys over the longest attended range any sequence can have
+  long long span = (long long)a.MB * 16;
+  if (a.window > 0 && a.window < span) span = a.window;
+  if (a.score_stride < span) span = a.score_stride;
+  int tiles = (int)((span + 255) / 256);
+  if (tiles < 1) tiles = 1;
+  void* score_params[] = {&args, &group, &tiles};
+  const long long sgrid = (long long)a.B * a.Hkv * tiles;
+  return launch_pdl(k.score, dim3((unsigned)sgrid), dim3(256), 0, stream, score_params);
 }
 
 }  // namespace pkv

@@ -37,6 +37,10 @@ struct DecodeArgs {
   int32_t* layout;               // [2B]: unit start (times Hkv) and units of each sequence, for large B
   float2* part_ml;               // [2 ranges, G] (running max in log2 units, running sum)
   float* part_o;                 // [2 ranges, G, D] unnormalised partial outputs
+  float* logits;                 // scores mode: [B, Hq, score_stride] base-2 logits of attended keys
+  float* lse;                    // scores mode: [B, Hq] natural log-sum-exp of each row
+  float* scores;                 // scores mode: [B, Hkv, score_stride] accumulated scores
+  int score_stride;              // scores mode: row length of logits and scores
   int32_t* err;                  // device error word or nullptr
   int B, Hq, Hkv, NB, MB, max_kept, window;
   int workers;                   // worker warps of the split grid
@@ -88,16 +92,18 @@ constexpr int kMaxWorkers = 2048;    // worker warps of a decode grid at most (s
 constexpr int kMergeWarps = 8;
 constexpr int kMaxGroup = 8;         // query heads per kv head handled by one fragment
 
-// Dynamic shared memory and kernel handles of one (head_dim, group, sparse) instantiation.
+// Kernel handles of one (head_dim, group, sparse, scores) instantiation.
 struct DecodeKernel {
   const void* split;
   const void* merge;
+  const void* score;  // scores mode: adds the step's probabilities into the scores
   int head_dim, group;
-  bool sparse;
+  bool sparse, scores;
 };
 
-// Returns nullptr-filled struct (split == nullptr) when the combination is unsupported.
-DecodeKernel decode_kernel(int head_dim, int group, bool sparse);
+// Returns a struct with split == nullptr when the combination is unsupported (scores mode
+// exists for dense decode only).
+DecodeKernel decode_kernel(int head_dim, int group, bool sparse, bool scores = false);
 size_t decode_smem_bytes(int head_dim, bool sparse, int batch);
 // merge_wpr_log2: log2 of the merge warps per output row (0..3).
 cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, size_t smem,
@@ -146,10 +152,19 @@ WorkspacePlan fit_workspace(const struct pkv_dims* d, size_t bytes);
 
 // Validates a paged (sparse == false) or sparse decode call, sizes its partition and
 // launches it with `workspace` as scratch.  Defined in api.cu; returns a PKV status.
+// Score emission of a dense decode (pkv_paged_decode_attention_scores); nullptr: none.
+struct ScoreOutputs {
+  float* lse;
+  float* scores;
+  float* logits;
+  int stride;
+};
+
 int decode_common(void* out, const void* q, const void* k_cache, const void* v_cache,
                   const int32_t* block_tables, const int32_t* context_lens, const int32_t* kept,
                   const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
                   void* workspace, size_t workspace_bytes, const struct pkv_dims* dims, int32_t* err,
-                  void* stream, bool sparse, const void* k_new = nullptr, const void* v_new = nullptr);
+                  void* stream, bool sparse, const void* k_new = nullptr, const void* v_new = nullptr,
+                  const ScoreOutputs* score_out = nullptr);
 
 }  // namespace pkv

@@ -21,7 +21,7 @@ def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _lib.header_functions()
-    assert len(declared) == 12
+    assert len(declared) == 13
     nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     for name in declared:
@@ -87,6 +87,17 @@ def test_host_validation_codes(lib):
     # selection
     assert lib.pkv_kv_select_topk(P(0x1000), P(0x1000), P(0x1000), 100, P(0x1000), -1, 4, 4,
                                   ctypes.byref(_dims()), None, None) == c["PKV_ERR_ARGUMENT"]
+    # score-emitting decode
+    def scores(lse=0x30000, acc=0x40000, logits=0x50000, stride=64, k_new=None, v_new=None):
+        return lib.pkv_paged_decode_attention_scores(
+            P(0x10000), P(lse), P(acc), P(logits), stride, P(0x10000), P(0x10000), P(0x10000),
+            P(k_new), P(v_new), P(0x10000), P(0x10000), ctypes.c_float(0.1), 0, P(0x20000), 16,
+            ctypes.byref(_dims()), None, None)
+    assert scores(lse=0) == c["PKV_ERR_NULL_POINTER"]
+    assert scores(stride=0) == c["PKV_ERR_DIMS"]
+    assert scores(acc=0x40002) == c["PKV_ERR_ALIGNMENT"]
+    assert scores(k_new=0x60000) == c["PKV_ERR_NULL_POINTER"]        # k_new without v_new
+    assert scores() == c["PKV_ERR_WORKSPACE"]                         # 16-byte workspace
     # sparse decode with no kept lists
     assert lib.pkv_sparse_decode_attention(P(0x10000), P(0x10000), P(0x10000), P(0x10000),
                                            P(0x10000), P(0x10000), None, None, 16,

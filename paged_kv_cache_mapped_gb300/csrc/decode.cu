@@ -496,6 +496,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   float l0 = 0.f, l1 = 0.f;                // this lane's share of the running sums
   int seg_b = -1, seg_g = -1;
   int seg_slot = -1;  // partial slot of the current segment, -1: written out directly
+  float* seg_logits = nullptr;  // scores mode: logit row of this lane's head h0 in the segment
   const float sl2 = a.scale_log2;
   // Dense append mode: this step's K (lanes 0-15) or V (lanes 16-31) row chunk of the current
   // segment, to be written at token L_b - 1 (pool and tile) when its unit is consumed.
@@ -549,6 +550,8 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     // a segment inside this range is written out directly; otherwise the range's share is a
     // partial in slot 2 ridx (the segment holds the range's start) or 2 ridx + 1 (its end)
     seg_slot = (seg_begin >= u0 && seg_begin + nb <= u0 + nunits) ? -1 : 2 * ridx + (u0 >= seg_begin ? 0 : 1);
+    if constexpr (SCORES)
+      seg_logits = a.logits + ((size_t)c.b * a.Hq + (size_t)c.g * G + 2 * tq) * a.score_stride;
 #pragma unroll
     for (int i = 0; i < 2 * KS; ++i) qb[i] = qraw[i];
     if (appending && new_lane) {
@@ -630,7 +633,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       const float s11 = (t1 && v1) ? c[3] * sl2 : -INFINITY;
       if constexpr (SCORES) {  // keep the attended keys' logits for the score step
         const int tok = (s_first[cc.b] + cc.j) * 16 + gq;
-        float* lg = a.logits + ((size_t)cc.b * a.Hq + (size_t)cc.g * G + 2 * tq) * a.score_stride + tok;
+        float* lg = seg_logits + tok;
         if (tok < a.score_stride) {
           if (t0 && v0) lg[0] = s00;
           if (t0 && v1) lg[a.score_stride] = s01;
@@ -920,9 +923,13 @@ decode_merge_kernel(const DecodeArgs a, int group, int wpr_log2) {
 // attention pass, every attended key's probability is exp(s - m) / l = exp(s - lse); a key's
 // score adds the probabilities of the G query heads sharing its kv head):
 //   scores[b, g, t] += sum_i 2^(logit[b, gG + i, t] - lse[b, gG + i] log2 e)
-// over the attended t < score_stride.  One thread per key, tiles of 256 keys per (b, g); reads
-// G logits and writes one score per key, all coalesced.
-__global__ void __launch_bounds__(256) decode_score_kernel(const DecodeArgs a, int group, int tiles) {
+// over the attended t < score_stride.  A CTA covers 1024 keys of one (b, g); a thread four
+// consecutive keys, as 16-byte loads and stores when the rows allow it (16-byte aligned
+// buffers, score_stride % 4 == 0).
+constexpr int kScoreThreads = 256;
+constexpr int kScoreKeys = 4 * kScoreThreads;
+
+__global__ void __launch_bounds__(kScoreThreads) decode_score_kernel(const DecodeArgs a, int group, int tiles) {
   const int seg = blockIdx.x / tiles;  // b * Hkv + g
   const int tile = blockIdx.x - seg * tiles;
   grid_dependency_wait();  // the logits and log-sum-exps of the decode
@@ -933,15 +940,40 @@ __global__ void __launch_bounds__(256) decode_score_kernel(const DecodeArgs a, i
   if (L < 0 || L > a.MB * 16) L = 0;  // reported by the split kernel
   const int start = (a.window > 0 && L > a.window) ? L - a.window : 0;
   const int end = min(L, a.score_stride);
-  const int t = start + tile * 256 + (int)threadIdx.x;
-  if (t >= end) return;
+  const int t0 = (start & ~3) + tile * kScoreKeys + 4 * (int)threadIdx.x;  // keys t0 .. t0 + 3
+  if (t0 >= end || t0 + 4 <= start) return;
   const size_t row0 = (size_t)b * a.Hq + (size_t)g * group;
-  float sum = 0.f;
+  float* dst = a.scores + (size_t)seg * a.score_stride + t0;
+  const bool vec = (a.score_stride & 3) == 0 && t0 >= start && t0 + 4 <= end &&
+                   ((reinterpret_cast<uintptr_t>(a.scores) | reinterpret_cast<uintptr_t>(a.logits)) & 15u) == 0;
+  float sum[4] = {0.f, 0.f, 0.f, 0.f};
   for (int i = 0; i < group; ++i) {
     const float lse2 = a.lse[row0 + i] * kLog2e;
-    sum += exp2f(a.logits[(row0 + i) * a.score_stride + t] - lse2);
+    const float* src = a.logits + (row0 + i) * a.score_stride + t0;
+    if (vec) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      sum[0] += exp2f(v.x - lse2);
+      sum[1] += exp2f(v.y - lse2);
+      sum[2] += exp2f(v.z - lse2);
+      sum[3] += exp2f(v.w - lse2);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (t0 + e >= start && t0 + e < end) sum[e] += exp2f(src[e] - lse2);
+    }
   }
-  a.scores[(size_t)seg * a.score_stride + t] += sum;
+  if (vec) {
+    float4 o = *reinterpret_cast<float4*>(dst);
+    o.x += sum[0];
+    o.y += sum[1];
+    o.z += sum[2];
+    o.w += sum[3];
+    *reinterpret_cast<float4*>(dst) = o;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (t0 + e >= start && t0 + e < end) dst[e] += sum[e];
+  }
 }
 
 }  // namespace
@@ -990,11 +1022,11 @@ cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, 
   long long span = (long long)a.MB * 16;
   if (a.window > 0 && a.window < span) span = a.window;
   if (a.score_stride < span) span = a.score_stride;
-  int tiles = (int)((span + 255) / 256);
+  int tiles = (int)((span + 3 + kScoreKeys - 1) / kScoreKeys);  // +3: the start rounds down to 4
   if (tiles < 1) tiles = 1;
   void* score_params[] = {&args, &group, &tiles};
   const long long sgrid = (long long)a.B * a.Hkv * tiles;
-  return launch_pdl(k.score, dim3((unsigned)sgrid), dim3(256), 0, stream, score_params);
+  return launch_pdl(k.score, dim3((unsigned)sgrid), dim3(kScoreThreads), 0, stream, score_params);
 }
 
 }  // namespace pkv

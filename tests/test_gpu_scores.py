@@ -196,3 +196,18 @@ def test_emitted_scores_feed_the_selection():
     for b in range(3):
         n = int(ref_lens[b])
         assert np.array_equal(kept[b, :, :n].cpu().numpy(), ref_kept[b, :, :n])
+
+
+def test_unaligned_score_rows_take_the_scalar_path():
+    """score_stride not a multiple of 4 and buffers only 4-byte aligned: same scores."""
+    case = _small_case([301, 77, 5], hq=8, hkv=2, d=64, seed=16)
+    stride = 303
+    big = torch.zeros((3 * 2 * stride + 1,), dtype=torch.float32, device=DEV)
+    acc = big[1:].view(3, 2, stride)                       # offset by 4 bytes
+    lg_big = torch.empty((3 * 8 * stride + 1,), dtype=torch.float32, device=DEV)
+    logits = lg_big[1:].view(3, 8, stride)
+    pkv.paged_decode_attention_scores(case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
+                                      case["context_lens"], case["scale"], acc, 40, logits=logits)
+    torch.cuda.synchronize()
+    ref, _ = _oracle(case, stride, window=40)
+    _check_scores(acc.double().cpu().numpy(), ref, "unaligned")

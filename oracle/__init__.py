@@ -82,10 +82,13 @@ def _load():
             lib.oracle_select_topk.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, i32]
             lib.oracle_decode_scores.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, i32,
                                                  f64, i32, i64, P, i64]
+            lib.oracle_rolling_admit.argtypes = [P, P, P, i64, i32, P, P, P, P, P, P, i32, i32, i32,
+                                                 i32, i32, i32]
             lib.oracle_compact.argtypes = [P, P, P, i64, i32, P, P, P, P, P, P, i32, i32, i32,
                                            i32, i64, i32]
             for name in ("oracle_kv_append", "oracle_paged_decode", "oracle_sparse_decode",
-                         "oracle_select_topk", "oracle_compact", "oracle_decode_scores"):
+                         "oracle_select_topk", "oracle_compact", "oracle_decode_scores",
+                         "oracle_rolling_admit"):
                 getattr(lib, name).restype = i32
             _lib = lib
     return _lib
@@ -237,3 +240,25 @@ def compact(dst_k, dst_v, dst_block_tables, src_k, src_v, src_block_tables, cont
                                   _ptr(sk), _ptr(sv), _ptr(sbt), _ptr(lens), _ptr(kept), _ptr(kl),
                                   max_kept, b, hkv, d, sk.shape[0], sbt.shape[1]), "compact")
     return dk, dv
+
+
+def rolling_admit(k_cache, v_cache, block_tables, slot_pos, slot_score, kept_lens, context_lens, k_new, v_new,
+                  n_sink, n_recent):
+    """One step's rolling admission; returns updated copies (k_cache, v_cache, slot_pos,
+    slot_score, kept_lens).  slot_pos/slot_score are [B, Hkv, capacity]."""
+    kc = np.array(_arr(k_cache, np.uint16), copy=True)
+    vc = np.array(_arr(v_cache, np.uint16), copy=True)
+    bt = _arr(block_tables, np.int32)
+    pos = np.array(_arr(slot_pos, np.int32), copy=True)
+    sc = np.array(_arr(slot_score, np.float32), copy=True)
+    kl = np.array(_arr(kept_lens, np.int32), copy=True)
+    lens = _arr(context_lens, np.int32)
+    kn = _arr(k_new, np.uint16)
+    vn = _arr(v_new, np.uint16)
+    nb, hkv, bs, d = kc.shape
+    b, hkv2, cap = pos.shape
+    assert bs == 16 and hkv2 == hkv and sc.shape == pos.shape and kn.shape == (b, hkv, d)
+    _check(_load().oracle_rolling_admit(_ptr(kc), _ptr(vc), _ptr(bt), nb, bt.shape[1], _ptr(pos), _ptr(sc),
+                                        _ptr(kl), _ptr(lens), _ptr(kn), _ptr(vn), b, hkv, d, cap,
+                                        int(n_sink), int(n_recent)), "rolling_admit")
+    return kc, vc, pos, sc, kl

@@ -481,3 +481,71 @@ int oracle_compact(uint16_t* dst_k, uint16_t* dst_v, const int32_t* dst_block_ta
   }
   return ORC_OK;
 }
+
+/*
+ * Rolling admission of one decode step's token into a sparse layer of fixed budget ([novita]
+ * section "System model": a sparse layer keeps the high-score and the recent KV and drops the
+ * rest; the token entering the cache takes the place of the lowest-score KV).  The layer's
+ * compact pool holds, per (b, kv head g), `capacity` slots (slot s lives at block
+ * block_tables[b][s / 16], offset s % 16); slot_pos[b][g][s] is the logical position a slot
+ * holds, slot_score[b][g][s] its accumulated score, kept_lens[b] the slots in use.  The new
+ * token has position L_b - 1 (context_lens counts it) and rows k_new[b][g], v_new[b][g].
+ *   - Budget not full (kept_lens[b] < capacity): the token takes slot kept_lens[b].
+ *   - Full: the token at position p = L_b - 1 - n_recent leaves the recent window.  It
+ *     competes with the top-k set -- the slots whose positions lie in [n_sink, p).  If its
+ *     score is strictly greater than the lowest score of that set (among equal lowest scores,
+ *     the highest position is the weakest), the weakest one is dropped; otherwise the leaving
+ *     token is dropped.  The new token takes the dropped token's slot.  Sinks and the recent
+ *     window are never dropped.
+ * The slot taken gets the new rows, position L_b - 1 and score 0; kept_lens[b] grows by one
+ * while below capacity.  NaN scores, a missing leaving token or a bad block are refused.
+ */
+int oracle_rolling_admit(uint16_t* k_cache, uint16_t* v_cache, const int32_t* block_tables,
+                         int64_t num_blocks, int max_blocks_per_seq, int32_t* slot_pos,
+                         float* slot_score, int32_t* kept_lens, const int32_t* context_lens,
+                         const uint16_t* k_new, const uint16_t* v_new, int batch,
+                         int num_kv_heads, int head_dim, int capacity, int n_sink, int n_recent) {
+  if (batch < 0 || num_kv_heads <= 0 || head_dim <= 0 || capacity <= 0 || n_sink < 0 ||
+      n_recent < 0 || n_sink + n_recent > capacity)
+    return ORC_ERR_ARG;
+  for (int b = 0; b < batch; ++b) {
+    int64_t len = context_lens[b];
+    int used = kept_lens[b];
+    if (len < 1 || used < 0 || used > capacity) return ORC_ERR_LEN;
+    int full = used == capacity;
+    for (int g = 0; g < num_kv_heads; ++g) {
+      int32_t* pos = slot_pos + ((int64_t)b * num_kv_heads + g) * capacity;
+      float* score = slot_score + ((int64_t)b * num_kv_heads + g) * capacity;
+      int target = used;
+      if (full) {
+        int64_t leaving = len - 1 - n_recent;
+        int s_out = -1, s_min = -1;
+        for (int s = 0; s < capacity; ++s) {
+          if (score[s] != score[s]) return ORC_ERR_ARG; /* NaN */
+          if (pos[s] == leaving) s_out = s;
+          if (pos[s] >= n_sink && pos[s] < leaving) {
+            if (s_min < 0 || score[s] < score[s_min] ||
+                (score[s] == score[s_min] && pos[s] > pos[s_min]))
+              s_min = s;
+          }
+        }
+        if (s_out < 0) return ORC_ERR_INDEX;
+        target = (s_min >= 0 && score[s_out] > score[s_min]) ? s_min : s_out;
+      }
+      int64_t logical_block = target / ORC_BLOCK;
+      if (logical_block >= max_blocks_per_seq) return ORC_ERR_INDEX;
+      int64_t physical = block_tables[(int64_t)b * max_blocks_per_seq + logical_block];
+      if (physical < 0 || physical >= num_blocks) return ORC_ERR_BLOCK;
+      int64_t dst = ((physical * num_kv_heads + g) * ORC_BLOCK + target % ORC_BLOCK) * head_dim;
+      int64_t src = ((int64_t)b * num_kv_heads + g) * head_dim;
+      for (int e = 0; e < head_dim; ++e) {
+        k_cache[dst + e] = k_new[src + e];
+        v_cache[dst + e] = v_new[src + e];
+      }
+      pos[target] = (int32_t)(len - 1);
+      score[target] = 0.0f;
+    }
+    if (!full) kept_lens[b] = used + 1;
+  }
+  return ORC_OK;
+}

@@ -275,6 +275,39 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
                    void* stream);
 
 /*
+ * pkv_kv_rolling_admit -- admit one decode step's token into each sequence's sparse-layer cache
+ * of fixed budget: capacity = n_sink + k_top + n_recent slots per (sequence, kv head) in a
+ * compact pool (slot s at block block_tables[b][s / 16], offset s % 16).  The rolling form of
+ * the layer-wise sparse cache of "How KV Sparsity Achieves 1.5x Acceleration for vLLM"
+ * (section "System model": a sparse layer keeps high-score and recent KV; the new KV replaces
+ * the lowest-score KV).  Per (b, kv head g):
+ *   - kept_lens[b] < capacity: the token takes slot kept_lens[b];
+ *   - full: the token at position L_b - 1 - n_recent leaves the recent window and meets the
+ *     top-k set (the slots holding positions in [n_sink, L_b - 1 - n_recent)): if its score is
+ *     strictly greater than the set's lowest score (among equal lowest scores the highest
+ *     position is the weakest), the weakest is dropped, otherwise the leaving token is; the
+ *     new token takes the dropped token's slot.  Sinks and the recent window are never dropped.
+ * The slot taken receives k_new[b][g] / v_new[b][g], position L_b - 1 and score 0;
+ * kept_lens[b] grows by one while below capacity.  Bit-exact.
+ *   k_cache, v_cache : compact pool [NB, Hkv, 16, d] bf16, updated in place.
+ *   block_tables     : [B, MB] int32 compact tables; capacity <= MB * 16.
+ *   slot_pos         : [B, Hkv, capacity] int32 logical positions held (updated).
+ *   slot_score       : [B, Hkv, capacity] fp32 accumulated scores (updated), e.g. from
+ *                      pkv_paged_decode_attention_scores over the compact pool.
+ *   kept_lens        : [B] int32 slots in use (updated).
+ *   context_lens     : [B] int32 L_b counting the new token (>= 1).
+ *   k_new, v_new     : [B, Hkv, d] bf16.
+ *   error_word       : optional; PKV_DEV_BAD_SCORE (a NaN score), PKV_DEV_BAD_KEPT_INDEX (the
+ *                      leaving token is in no slot), PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT_LEN;
+ *                      that (b, g) (or b) is then left unchanged.
+ */
+int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tables,
+                         int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
+                         const int32_t* context_lens, const void* k_new, const void* v_new,
+                         int32_t capacity, int32_t n_sink, int32_t n_recent, const pkv_dims* dims,
+                         int32_t* error_word, void* stream);
+
+/*
  * pkv_paged_decode_attention_fixed_scratch -- pkv_paged_decode_attention for callers that
  * cannot allocate device memory.  It has no counterpart on the pages: it exists only for
  * callers with no device allocator at hand (for example a plain C program or plugin that

@@ -20,7 +20,7 @@ __all__ = [
     "sparse_decode_workspace_bytes", "sparse_decode_attention", "kv_select_topk", "kv_compact",
     "read_error", "new_error_word", "header_constants", "header_functions",
     "paged_decode_attention_fixed_scratch", "paged_decode_attention_append",
-    "paged_decode_attention_scores",
+    "paged_decode_attention_scores", "kv_rolling_admit",
 ]
 
 BLOCK_SIZE = 16
@@ -212,6 +212,35 @@ def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_len
         int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims), _ptr(error_word),
         _stream(stream, dev)))
     return out, lse
+
+
+def kv_rolling_admit(k_cache, v_cache, block_tables, slot_pos, slot_score, kept_lens, context_lens, k_new,
+                     v_new, n_sink, n_recent, *, error_word=None, stream=None):
+    """Admit this step's token (k_new/v_new [B, Hkv, d], position context_lens[b] - 1) into each
+    sequence's fixed-budget sparse cache: the compact pool [NB, Hkv, 16, d] with its tables,
+    slot_pos [B, Hkv, C] int32 and slot_score [B, Hkv, C] fp32 (C = n_sink + k_top + n_recent
+    slots) and kept_lens [B] int32, all updated in place.  See pkv_kv_rolling_admit."""
+    nb, hkv, d = _pool_dims(k_cache, v_cache)
+    dev = k_cache.device
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(slot_pos, "slot_pos", torch.int32, 3, dev)
+    _need(slot_score, "slot_score", torch.float32, 3, dev)
+    _need(kept_lens, "kept_lens", torch.int32, 1, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(k_new, "k_new", torch.bfloat16, 3, dev)
+    _need(v_new, "v_new", torch.bfloat16, 3, dev)
+    B = slot_pos.shape[0]
+    if slot_pos.shape[1] != hkv or slot_score.shape != slot_pos.shape:
+        raise ValueError("slot_pos and slot_score must be [B, Hkv, capacity]")
+    if k_new.shape != (B, hkv, d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
+    if block_tables.shape[0] != B or kept_lens.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / kept_lens / context_lens batch differs")
+    dims = _dims(B, 1, hkv, d, nb, block_tables.shape[1])
+    check("pkv_kv_rolling_admit", load().pkv_kv_rolling_admit(
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(slot_pos), _ptr(slot_score), _ptr(kept_lens),
+        _ptr(context_lens), _ptr(k_new), _ptr(v_new), slot_pos.shape[2], int(n_sink), int(n_recent),
+        ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
 
 
 def paged_decode_attention_fixed_scratch(q, k_cache, v_cache, block_tables, context_lens, scale,

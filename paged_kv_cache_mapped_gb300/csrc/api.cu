@@ -430,6 +430,29 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
                                        static_cast<cudaStream_t>(stream)));
 }
 
+int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tables,
+                         int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
+                         const int32_t* context_lens, const void* k_new, const void* v_new,
+                         int32_t capacity, int32_t n_sink, int32_t n_recent, const pkv_dims* dims,
+                         int32_t* error_word, void* stream) {
+  int st = check_dims(dims, false);
+  if (st != PKV_OK) return st;
+  if (capacity <= 0 || n_sink < 0 || n_recent < 0 || (long long)n_sink + n_recent > capacity)
+    return PKV_ERR_ARGUMENT;
+  if ((long long)capacity > (long long)dims->max_blocks_per_seq * PKV_BLOCK_SIZE) return PKV_ERR_DIMS;
+  if (dims->batch == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !block_tables || !slot_pos || !slot_score || !kept_lens ||
+      !context_lens || !k_new || !v_new)
+    return PKV_ERR_NULL_POINTER;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+    return PKV_ERR_ALIGNMENT;
+  if (!device_info(&st)) return st;
+  return cuda_status(launch_kv_rolling_admit(
+      k_cache, v_cache, block_tables, dims->num_blocks, dims->max_blocks_per_seq, slot_pos, slot_score,
+      kept_lens, context_lens, k_new, v_new, dims->batch, dims->num_kv_heads, dims->head_dim, capacity,
+      n_sink, n_recent, error_word, static_cast<cudaStream_t>(stream)));
+}
+
 int pkv_read_error(int32_t* error_word, int32_t clear, void* stream) {
   if (error_word == nullptr) return PKV_ERR_NULL_POINTER;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

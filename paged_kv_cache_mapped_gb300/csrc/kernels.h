@@ -120,6 +120,11 @@ cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, i
                               const int32_t* lens, const int32_t* kept, const int32_t* kept_lens,
                               int max_kept, int B, int Hkv, int D, int sNB, int sMB,
                               int32_t* err, cudaStream_t stream);
+cudaError_t launch_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* bt, int NB, int MB,
+                                    int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
+                                    const int32_t* lens, const void* k_new, const void* v_new, int B,
+                                    int Hkv, int D, int capacity, int n_sink, int n_recent, int32_t* err,
+                                    cudaStream_t stream);
 cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* scores,
                                int stride, const int32_t* lens, int B, int Hkv, int n_sink,
                                int n_recent, int k_top, int32_t* err, cudaStream_t stream);

@@ -274,6 +274,96 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   for (int t = threadIdx.x; t < n_recent; t += blockDim.x) out[n_sink + k_top + t] = first + n + t;
 }
 
+// Rolling admission of a decode step's token into a sparse layer of fixed budget ("How KV
+// Sparsity Achieves 1.5x Acceleration for vLLM", section "System model": the layer keeps the
+// high-score and the recent KV; the token entering takes the place of the lowest-score one).
+// Per (b, kv head g): while the budget is not full the token takes the next slot; when it is,
+// the token leaving the recent window (position L - 1 - n_recent) meets the top-k set (slots
+// holding positions in [n_sink, that position)): if its score is strictly above the set's
+// lowest (ties: the highest position is the weakest), the weakest is dropped, else the leaving
+// token is; the new token takes the dropped slot with score 0.  One CTA per sequence, a warp
+// per kv head: the warp scans the slots (lane-strided), reduces the leaving slot and the
+// weakest (score, position) pair across its lanes, then copies the rows (lanes 0-15 K,
+// 16-31 V).  The slot count is updated after every head is done.
+constexpr int kAdmitWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
+    __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc, const int32_t* __restrict__ bt,
+    int NB, int MB, int32_t* __restrict__ slot_pos, float* __restrict__ slot_score,
+    int32_t* __restrict__ kept_lens, const int32_t* __restrict__ lens, const __nv_bfloat16* __restrict__ k_new,
+    const __nv_bfloat16* __restrict__ v_new, int Hkv, int capacity, int n_sink, int n_recent, int32_t* err) {
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int L = lens[b];
+  const int used = kept_lens[b];
+  const bool valid = L >= 1 && used >= 0 && used <= capacity;
+  if (!valid && threadIdx.x == 0) record_error(err, PKV_DEV_BAD_CONTEXT_LEN);
+  const bool full = used == capacity;
+  for (int g = warp; valid && g < Hkv; g += kAdmitWarps) {
+    int32_t* pos = slot_pos + ((size_t)b * Hkv + g) * capacity;
+    float* score = slot_score + ((size_t)b * Hkv + g) * capacity;
+    int target = used;
+    bool ok = true;
+    if (full) {
+      const int leaving = L - 1 - n_recent;
+      int s_out = -1, s_min = -1, p_min = -1;
+      float x_min = INFINITY;
+      bool nan = false;
+      for (int s = lane; s < capacity; s += 32) {
+        const int p = pos[s];
+        const float x = score[s];
+        nan |= (x != x);
+        if (p == leaving) s_out = s;
+        if (p >= n_sink && p < leaving && (s_min < 0 || x < x_min || (x == x_min && p > p_min))) {
+          s_min = s;
+          x_min = x;
+          p_min = p;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s_out = max(s_out, __shfl_xor_sync(kFullMask, s_out, o));
+        const int s2 = __shfl_xor_sync(kFullMask, s_min, o);
+        const int p2 = __shfl_xor_sync(kFullMask, p_min, o);
+        const float x2 = __shfl_xor_sync(kFullMask, x_min, o);
+        if (s2 >= 0 && (s_min < 0 || x2 < x_min || (x2 == x_min && p2 > p_min))) {
+          s_min = s2;
+          x_min = x2;
+          p_min = p2;
+        }
+      }
+      nan = __any_sync(kFullMask, nan);
+      if (nan || s_out < 0) {
+        if (lane == 0) record_error(err, nan ? PKV_DEV_BAD_SCORE : PKV_DEV_BAD_KEPT_INDEX);
+        ok = false;
+      } else {
+        target = (s_min >= 0 && score[s_out] > x_min) ? s_min : s_out;
+      }
+    }
+    if (ok) {
+      const int blk = target / 16 < MB ? bt[(size_t)b * MB + target / 16] : -1;
+      if (blk < 0 || blk >= NB) {
+        if (lane == 0) record_error(err, PKV_DEV_BAD_BLOCK_ID);
+      } else {
+        const size_t dst = (((size_t)blk * Hkv + g) * 16 + (target & 15)) * D;
+        const size_t src = ((size_t)b * Hkv + g) * D;
+        if (lane < 16) copy_row_half<D>(kc + dst, k_new + src, lane);
+        else copy_row_half<D>(vc + dst, v_new + src, lane - 16);
+        if (lane == 0) {
+          pos[target] = L - 1;
+          score[target] = 0.f;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && valid && !full) kept_lens[b] = used + 1;
+}
+
 }  // namespace
 
 cudaError_t kvops_device_setup() {
@@ -324,6 +414,22 @@ cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const 
                   &k_top, &err};
   return launch_pdl((const void*)select_topk_kernel, dim3(pairs), dim3(kSelThreads),
                     kSelSmemKeys * sizeof(uint32_t), stream, args);
+}
+
+cudaError_t launch_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* bt, int NB, int MB,
+                                    int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
+                                    const int32_t* lens, const void* k_new, const void* v_new, int B,
+                                    int Hkv, int D, int capacity, int n_sink, int n_recent, int32_t* err,
+                                    cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  auto* kc = static_cast<__nv_bfloat16*>(k_cache);
+  auto* vc = static_cast<__nv_bfloat16*>(v_cache);
+  auto* kn = static_cast<const __nv_bfloat16*>(k_new);
+  auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+  void* args[] = {&kc, &vc, &bt, &NB, &MB, &slot_pos, &slot_score, &kept_lens, &lens, &kn, &vn,
+                  &Hkv, &capacity, &n_sink, &n_recent, &err};
+  const void* fn = D == 128 ? (const void*)kv_rolling_admit_kernel<128> : (const void*)kv_rolling_admit_kernel<64>;
+  return launch_pdl(fn, dim3(B), dim3(kAdmitWarps * 32), 0, stream, args);
 }
 
 }  // namespace pkv

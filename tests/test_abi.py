@@ -21,7 +21,7 @@ def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _lib.header_functions()
-    assert len(declared) == 13
+    assert len(declared) == 14
     nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     for name in declared:
@@ -98,6 +98,16 @@ def test_host_validation_codes(lib):
     assert scores(acc=0x40002) == c["PKV_ERR_ALIGNMENT"]
     assert scores(k_new=0x60000) == c["PKV_ERR_NULL_POINTER"]        # k_new without v_new
     assert scores() == c["PKV_ERR_WORKSPACE"]                         # 16-byte workspace
+    # rolling admission
+    def admit(cap=60, n_sink=4, n_recent=32, slot_pos=0x30000, dims=None):
+        return lib.pkv_kv_rolling_admit(P(0x10000), P(0x10000), P(0x10000), P(slot_pos), P(0x40000),
+                                        P(0x50000), P(0x60000), P(0x70000), P(0x80000), cap, n_sink,
+                                        n_recent, ctypes.byref(dims or _dims()), None, None)
+    assert admit(cap=0) == c["PKV_ERR_ARGUMENT"]
+    assert admit(n_sink=40, n_recent=32) == c["PKV_ERR_ARGUMENT"]     # sinks + recent > capacity
+    assert admit(cap=64 * 16 + 1) == c["PKV_ERR_DIMS"]                # more slots than the tables
+    assert admit(slot_pos=0) == c["PKV_ERR_NULL_POINTER"]
+    assert admit(dims=_dims(B=0)) == c["PKV_OK"]
     # sparse decode with no kept lists
     assert lib.pkv_sparse_decode_attention(P(0x10000), P(0x10000), P(0x10000), P(0x10000),
                                            P(0x10000), P(0x10000), None, None, 16,

@@ -507,28 +507,112 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
     scores = W.make_scores(wl, wl.full_layers, lens, device=dev, device_rng=True)
     kept = torch.empty((B, hkv, K), dtype=torch.int32, device=dev)
     kl = torch.empty((B,), dtype=torch.int32, device=dev)
+    cur = lambda: torch.cuda.current_stream(dev)  # the capturing stream inside _graph_time
     sel = lambda: pkv.kv_select_topk(scores, src["context_lens"], wl.n_sink, wl.n_recent, wl.k_top,
-                                     kept_out=kept, kept_lens_out=kl, stream=stream)
-    ms_sel = _time(sel, args.warmup, 20, dev, stream)
+                                     kept_out=kept, kept_lens_out=kl, stream=cur())
     dk, dv = comp[0]["k_cache"], comp[0]["v_cache"]
     cmp = lambda: pkv.kv_compact(dk, dv, dbt, src["k_cache"], src["v_cache"], src["block_tables"],
-                                 src["context_lens"], kept, kl, stream=stream)
-    ms_cmp = _time(cmp, args.warmup, 20, dev, stream)
+                                 src["context_lens"], kept, kl, stream=cur())
     ws_s = torch.zeros(pkv.sparse_decode_workspace_bytes(B, hq, hkv, d, src["num_blocks"],
                                                          src["max_blocks_per_seq"], K),
                        dtype=torch.uint8, device=dev)
     gat = lambda: pkv.sparse_decode_attention(src["q"], src["k_cache"], src["v_cache"], src["block_tables"],
                                               src["context_lens"], kept, kl, wl.scale, out=out,
-                                              workspace=ws_s, stream=stream)
-    ms_gat = _time(gat, args.warmup, 20, dev, stream)
+                                              workspace=ws_s, stream=cur())
+    # each per-layer call is microseconds of device work: time it as 10 calls in one CUDA graph
+    # (as a decode step runs), not as Python launches that the host would bound
+    with torch.cuda.stream(gstream):
+        ms_sel = _graph_time([sel] * 10, args.warmup, 5, dev, gstream) / 10
+        ms_cmp = _graph_time([cmp] * 10, args.warmup, 5, dev, gstream) / 10
+        ms_gat = _graph_time([gat] * 10, args.warmup, 5, dev, gstream) / 10
     sel_bytes = int(scores.numel()) * 4 + B * hkv * K * 4
     cmp_bytes = B * hkv * K * d * 2 * 2 * 2
     res["sparse_layer_select_topk"] = {"ms": round(ms_sel, 4), "gbs": round(sel_bytes / (ms_sel * 1e-3) / 1e9, 1)}
     res["sparse_layer_compact"] = {"ms": round(ms_cmp, 4), "gbs": round(cmp_bytes / (ms_cmp * 1e-3) / 1e9, 1)}
     res["sparse_layer_gather_decode"] = {"ms": round(ms_gat, 4),
                                          "gbs": round(sparse_bytes / (ms_gat * 1e-3) / 1e9, 1)}
+    with torch.cuda.stream(gstream):
+        res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, comp[0], dbt, klens, ws, out))
     del full, comp, scores
     return res
+
+
+def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, calls=10, trials=5):
+    """One sparse layer kept at its fixed budget by rolling admission.  The state is a top-k
+    selection over the first L - 1 tokens; call i admits token L - 1 + i (its own row of context
+    lengths), then, in the layer step, attends over the compact pool with the scores added to
+    the slot scores.  Admission changes the state, so the `calls` calls are one CUDA graph
+    replayed once per trial from a restored state."""
+    B, hq, hkv, d, K = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.keep_max
+    prev = (lens - 1).to(dev)
+    kept = torch.empty((B, hkv, K), dtype=torch.int32, device=dev)
+    kl = torch.empty((B,), dtype=torch.int32, device=dev)
+    pkv.kv_select_topk(scores, prev, wl.n_sink, wl.n_recent, wl.k_top, kept_out=kept, kept_lens_out=kl,
+                       stream=gstream)
+    pos0 = kept.clone()
+    sc0 = torch.gather(scores, 2, kept.to(torch.int64))
+    kl0 = kl.clone()
+    g = torch.Generator(device=dev).manual_seed(11)
+    k_new = torch.randn((B, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    v_new = torch.randn((B, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    lens_rows = (lens.to(dev).view(1, B) + torch.arange(calls, dtype=torch.int32, device=dev).view(-1, 1)).contiguous()
+    pos, sc, kls = pos0.clone(), sc0.clone(), kl0.clone()
+    lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
+    logits = torch.empty((B, hq, K), dtype=torch.float32, device=dev)
+    err = pkv.new_error_word(dev)
+
+    def admit(i):
+        pkv.kv_rolling_admit(c["k_cache"], c["v_cache"], dbt, pos, sc, kls, lens_rows[i], k_new, v_new,
+                             wl.n_sink, wl.n_recent, error_word=err, stream=torch.cuda.current_stream(dev))
+
+    def decode_scores():
+        pkv.paged_decode_attention_scores(c["q"], c["k_cache"], c["v_cache"], dbt, klens, wl.scale, sc,
+                                          out=out, lse=lse, logits=logits, workspace=ws, error_word=err,
+                                          stream=torch.cuda.current_stream(dev))
+
+    def plain():
+        pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], dbt, klens, wl.scale, out=out,
+                                   workspace=ws, stream=torch.cuda.current_stream(dev))
+
+    def restore():
+        pos.copy_(pos0)
+        sc.copy_(sc0)
+        kls.copy_(kl0)
+        torch.cuda.synchronize(dev)
+
+    def series(body):
+        restore()
+        body(0)                              # one eager call: any lazy setup happens outside the capture
+        restore()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=gstream):
+            for i in range(calls):
+                body(i)
+        times = []
+        for _ in range(trials + 1):          # the first replay is a warm-up
+            restore()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(gstream)
+            gr.replay()
+            e1.record(gstream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1) / calls)
+        return sorted(times[1:])[trials // 2]
+    ms_adm = series(admit)
+    ms_layer = series(lambda i: (admit(i), decode_scores()))
+    ms_plain = series(lambda i: plain())
+    if pkv.read_error(err) != 0:
+        raise RuntimeError(f"rolling admission reported device error {pkv.read_error(err)}")
+    segs = B * hkv
+    adm_bytes = segs * (K * 8 + 2 * 2 * d * 2 + 8)  # slot positions+scores read, K/V rows in and out
+    kv = decode_bytes(klens.cpu(), B, hq, hkv, d)
+    return {"sparse_layer_rolling_admit": {"ms": round(ms_adm, 4), "bytes": adm_bytes,
+                                           "gbs": round(adm_bytes / (ms_adm * 1e-3) / 1e9, 1)},
+            "sparse_layer_rolling_step": {"ms": round(ms_layer, 4), "ms_plain_compact_decode": round(ms_plain, 4),
+                                          "gbs": round((kv + adm_bytes) / (ms_layer * 1e-3) / 1e9, 1),
+                                          "what": "admit + score-emitting decode over 1540 slots per (b, kv head)",
+                                          "launch": f"{calls} layer steps in one CUDA graph, median of {trials}"}}
 
 
 def _time(fn, warmup, steps, dev, stream):

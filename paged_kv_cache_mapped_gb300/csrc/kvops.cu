@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
 // weakest (score, position) pair across its lanes, then copies the rows (lanes 0-15 K,
 // 16-31 V).  The slot count is updated after every head is done.
 constexpr int kAdmitWarps = 8;
+constexpr int kAdmitUnroll = 4;  // 16-byte slot loads in flight per lane and per array
 
 template <int D>
 __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
@@ -313,9 +314,9 @@ __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
       int s_out = -1, s_min = -1, p_min = -1;
       float x_min = INFINITY;
       bool nan = false;
-      for (int s = lane; s < capacity; s += 32) {
-        const int p = pos[s];
-        const float x = score[s];
+      // the weakest top-k token is unique under (score ascending, position descending), so
+      // the order in which the lanes visit the slots does not matter
+      auto visit = [&](int s, int p, float x) {
         nan |= (x != x);
         if (p == leaving) s_out = s;
         if (p >= n_sink && p < leaving && (s_min < 0 || x < x_min || (x == x_min && p > p_min))) {
@@ -323,6 +324,33 @@ __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
           x_min = x;
           p_min = p;
         }
+      };
+      if ((capacity & 3) == 0 && ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(score)) & 15) == 0) {
+        // 16-byte loads, kAdmitUnroll of each issued before any is used
+        for (int base = lane * 4; base < capacity; base += 32 * 4 * kAdmitUnroll) {
+          int4 pv[kAdmitUnroll];
+          float4 xv[kAdmitUnroll];
+#pragma unroll
+          for (int u = 0; u < kAdmitUnroll; ++u) {
+            const int s = base + u * 128;
+            if (s < capacity) {
+              pv[u] = *reinterpret_cast<const int4*>(pos + s);
+              xv[u] = *reinterpret_cast<const float4*>(score + s);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kAdmitUnroll; ++u) {
+            const int s = base + u * 128;
+            if (s < capacity) {
+              visit(s, pv[u].x, xv[u].x);
+              visit(s + 1, pv[u].y, xv[u].y);
+              visit(s + 2, pv[u].z, xv[u].z);
+              visit(s + 3, pv[u].w, xv[u].w);
+            }
+          }
+        }
+      } else {
+        for (int s = lane; s < capacity; s += 32) visit(s, pos[s], score[s]);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {

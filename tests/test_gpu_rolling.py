@@ -44,13 +44,13 @@ def _admit_both(st, lens, k_new, v_new, n_sink, n_recent, err=None):
         assert np.array_equal(a, b), name
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_steps_from_empty_to_full_bit_exact(d):
-    B, hkv, n_sink, k_top, n_recent = 3, 4, 4, 24, 32
+@pytest.mark.parametrize("d,k_top", [(64, 24), (128, 24), (64, 23)])  # 60 slots: 16-byte scan; 59: scalar
+def test_steps_from_empty_to_full_bit_exact(d, k_top):
+    B, hkv, n_sink, n_recent = 3, 4, 4, 32
     cap = n_sink + k_top + n_recent
-    st = _state(B, hkv, d, cap, seed=d)
+    st = _state(B, hkv, d, cap, seed=d + k_top)
     g = torch.Generator().manual_seed(d + 1)
-    rng = np.random.default_rng(d)
+    rng = np.random.default_rng(d + k_top)
     err = pkv.new_error_word(DEV)
     for L in range(1, 160):
         lens = torch.full((B,), L, dtype=torch.int32, device=DEV)

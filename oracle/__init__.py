@@ -18,6 +18,11 @@ Parity status of each function (what pins it; see ``tests/test_oracle_*.py``):
   select_topk      -- pinned by a hand-worked golden case, exhaustive subset search on tiny
                       inputs and the selection invariants
   compact          -- pinned by a brute-force dict-of-slots model
+  quantize_rows    -- pinned by exact round trips of codes times power-of-two scales, hand-worked
+                      half-way ties, the rounding bound and the absmax element's code
+  kv_append_q8     -- pinned by a dict-of-slots model over quantize_rows
+  paged_decode_q8  -- pinned by equality with paged_decode where code * scale is a bf16 value,
+                      and by torch SDPA (fp64) on the dequantized contiguous K/V
 """
 from __future__ import annotations
 
@@ -47,6 +52,7 @@ _CODES = {
     -5: "invalid length",
     -6: "NaN score",
     -7: "out of memory",
+    -8: "non-finite value",
 }
 
 
@@ -86,9 +92,14 @@ def _load():
                                                  i32, i32, i32]
             lib.oracle_compact.argtypes = [P, P, P, i64, i32, P, P, P, P, P, P, i32, i32, i32,
                                            i32, i64, i32]
+            lib.oracle_quantize_rows.argtypes = [P, P, P, i64, i32]
+            lib.oracle_kv_append_q8.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i64]
+            lib.oracle_paged_decode_q8.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i64,
+                                                   i32, f64, i32, P, i64]
             for name in ("oracle_kv_append", "oracle_paged_decode", "oracle_sparse_decode",
                          "oracle_select_topk", "oracle_compact", "oracle_decode_scores",
-                         "oracle_rolling_admit"):
+                         "oracle_rolling_admit", "oracle_quantize_rows", "oracle_kv_append_q8",
+                         "oracle_paged_decode_q8"):
                 getattr(lib, name).restype = i32
             _lib = lib
     return _lib
@@ -262,3 +273,54 @@ def rolling_admit(k_cache, v_cache, block_tables, slot_pos, slot_score, kept_len
                                         _ptr(kl), _ptr(lens), _ptr(kn), _ptr(vn), b, hkv, d, cap,
                                         int(n_sink), int(n_recent)), "rolling_admit")
     return kc, vc, pos, sc, kl
+
+
+def quantize_rows(x):
+    """INT8 quantization of the last axis of x (bf16 bits): (codes int8 x.shape, scales fp32 x.shape[:-1])."""
+    x = _arr(x, np.uint16)
+    d = x.shape[-1]
+    n = x.size // d if d else 0
+    codes = np.zeros(x.shape, dtype=np.int8)
+    scales = np.zeros(x.shape[:-1], dtype=np.float32)
+    _check(_load().oracle_quantize_rows(_ptr(codes), _ptr(scales), _ptr(x), n, d), "quantize_rows")
+    return codes, scales
+
+
+def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k, v, slot_mapping):
+    """Return copies of the INT8 pools ([NB,Hkv,16,d] int8 codes, [NB,Hkv,16] fp32 scales)
+    after quantizing k, v [T,Hkv,d] (bf16 bits) into the slots."""
+    kc = np.array(_arr(k_codes, np.int8), copy=True)
+    vc = np.array(_arr(v_codes, np.int8), copy=True)
+    ks = np.array(_arr(k_scales, np.float32), copy=True)
+    vs = np.array(_arr(v_scales, np.float32), copy=True)
+    k = _arr(k, np.uint16)
+    v = _arr(v, np.uint16)
+    slots = _arr(slot_mapping, np.int64)
+    nb, hkv, bs, d = kc.shape
+    assert bs == 16 and vc.shape == kc.shape and ks.shape == (nb, hkv, 16) and vs.shape == ks.shape
+    assert k.shape == (slots.shape[0], hkv, d) and v.shape == k.shape
+    _check(_load().oracle_kv_append_q8(_ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(k), _ptr(v), _ptr(slots),
+                                       slots.shape[0], hkv, d, nb), "kv_append_q8")
+    return kc, vc, ks, vs
+
+
+def paged_decode_q8(q, k_codes, k_scales, v_codes, v_scales, block_tables, context_lens, scale, window=0,
+                    rows=None):
+    """fp64 attention over INT8 pools (values code * scale).  Shapes as paged_decode."""
+    q = _arr(q, np.uint16)
+    kc = _arr(k_codes, np.int8)
+    vc = _arr(v_codes, np.int8)
+    ks = _arr(k_scales, np.float32)
+    vs = _arr(v_scales, np.float32)
+    bt = _arr(block_tables, np.int32)
+    lens = _arr(context_lens, np.int32)
+    b, hq, d = q.shape
+    nb, hkv, bs, d2 = kc.shape
+    assert bs == 16 and d2 == d and vc.shape == kc.shape and ks.shape == (nb, hkv, 16) and vs.shape == ks.shape
+    assert bt.shape[0] == b
+    r, n = _rows(rows, b, hq)
+    out = np.zeros((n, d), dtype=np.float64)
+    _check(_load().oracle_paged_decode_q8(_ptr(out), _ptr(q), _ptr(kc), _ptr(ks), _ptr(vc), _ptr(vs), _ptr(bt),
+                                          _ptr(lens), b, hq, hkv, d, nb, bt.shape[1], float(scale), int(window),
+                                          None if r is None else _ptr(r), n), "paged_decode_q8")
+    return out.reshape(b, hq, d) if rows is None else out

@@ -5,6 +5,8 @@
  * or constant with the CUDA library: every operation is written here straight from its
  * definition, in the order the definition states it, with no blocking, fusion or
  * reordering.  bf16 values are widened exactly to double; sums and exponentials are fp64.
+ * The one exception is INT8 quantization, whose integer codes are decided in fp32 (see
+ * quantize_row); dequantized values are exact in fp64.
  *
  * Page names used in the citations below:
  *   [primer]  KV-cache primer article, cf-1.com/news/5988169 (sections numbered as on the page)
@@ -33,6 +35,7 @@
 #define ORC_ERR_LEN (-5)
 #define ORC_ERR_NAN (-6)
 #define ORC_ERR_MEM (-7)
+#define ORC_ERR_VALUE (-8)
 
 /* bfloat16 is the upper half of an IEEE binary32: widening is exact. */
 static double bf16_to_double(uint16_t bits) {
@@ -40,6 +43,29 @@ static double bf16_to_double(uint16_t bits) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+static float bf16_to_float(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/*
+ * A K or V pool as the decode reads it: bf16 elements, or INT8 codes with one fp32 scale per
+ * (block, kv head, token) row, whose values are code * scale (exact in fp64).
+ * Row r = (physical block * Hkv + kv head) * 16 + offset; element e of row r is at r * d + e.
+ */
+typedef struct {
+  const uint16_t* bf16;
+  const int8_t* codes;
+  const float* scales;
+} pool_t;
+
+static double pool_value(const pool_t* p, int64_t row, int head_dim, int e) {
+  if (p->bf16) return bf16_to_double(p->bf16[row * head_dim + e]);
+  return (double)p->codes[row * head_dim + e] * (double)p->scales[row];
 }
 
 int oracle_num_threads(void) {
@@ -98,8 +124,8 @@ int oracle_kv_append(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k, co
  * ([primer] section 4.1).  Subtracting the max is the textbook stable softmax; it does not
  * change the value.  An empty list gives a zero row.
  */
-static int attend_one_row(double* out, const uint16_t* q_row, const uint16_t* k_cache,
-                          const uint16_t* v_cache, const int32_t* block_row,
+static int attend_one_row(double* out, const uint16_t* q_row, const pool_t* k_pool,
+                          const pool_t* v_pool, const int32_t* block_row,
                           int max_blocks_per_seq, int64_t num_blocks, int num_kv_heads,
                           int head_dim, int kv_head, double scale, const int64_t* tokens,
                           int64_t n_tokens) {
@@ -127,10 +153,10 @@ static int attend_one_row(double* out, const uint16_t* q_row, const uint16_t* k_
       free(rows);
       return ORC_ERR_BLOCK;
     }
-    rows[j] = ((physical * num_kv_heads + kv_head) * ORC_BLOCK + offset) * head_dim;
+    rows[j] = (physical * num_kv_heads + kv_head) * ORC_BLOCK + offset;
     double dot = 0.0;
     for (int e = 0; e < head_dim; ++e)
-      dot += bf16_to_double(q_row[e]) * bf16_to_double(k_cache[rows[j] + e]);
+      dot += bf16_to_double(q_row[e]) * pool_value(k_pool, rows[j], head_dim, e);
     logits[j] = scale * dot;
   }
   double m = logits[0];
@@ -143,7 +169,7 @@ static int attend_one_row(double* out, const uint16_t* q_row, const uint16_t* k_
   }
   for (int64_t j = 0; j < n_tokens; ++j)
     for (int e = 0; e < head_dim; ++e)
-      out[e] += logits[j] * bf16_to_double(v_cache[rows[j] + e]);
+      out[e] += logits[j] * pool_value(v_pool, rows[j], head_dim, e);
   for (int e = 0; e < head_dim; ++e) out[e] /= denom;
   free(logits);
   free(rows);
@@ -159,12 +185,12 @@ static int attend_one_row(double* out, const uint16_t* q_row, const uint16_t* k_
  * keeps only the most recent `window` tokens ([primer] section 4.3).  L_b counts the token
  * appended this step.
  */
-int oracle_paged_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
-                        const uint16_t* v_cache, const int32_t* block_tables,
-                        const int32_t* context_lens, int batch, int num_q_heads,
-                        int num_kv_heads, int head_dim, int64_t num_blocks,
-                        int max_blocks_per_seq, double scale, int window,
-                        const int64_t* row_ids, int64_t n_rows) {
+static int paged_decode_pools(double* out, const uint16_t* q, const pool_t* k_pool,
+                              const pool_t* v_pool, const int32_t* block_tables,
+                              const int32_t* context_lens, int batch, int num_q_heads,
+                              int num_kv_heads, int head_dim, int64_t num_blocks,
+                              int max_blocks_per_seq, double scale, int window,
+                              const int64_t* row_ids, int64_t n_rows) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return ORC_ERR_ARG;
   if (num_q_heads % num_kv_heads != 0) return ORC_ERR_ARG;
   int group = num_q_heads / num_kv_heads;
@@ -191,7 +217,7 @@ int oracle_paged_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
           st = ORC_ERR_MEM;
         } else {
           for (int64_t j = 0; j < n; ++j) tokens[j] = start + j;
-          st = attend_one_row(out + r * head_dim, q + row * head_dim, k_cache, v_cache,
+          st = attend_one_row(out + r * head_dim, q + row * head_dim, k_pool, v_pool,
                               block_tables + (int64_t)b * max_blocks_per_seq,
                               max_blocks_per_seq, num_blocks, num_kv_heads, head_dim,
                               h / group, scale, tokens, n);
@@ -205,6 +231,102 @@ int oracle_paged_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
     }
   }
   return status;
+}
+
+int oracle_paged_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
+                        const uint16_t* v_cache, const int32_t* block_tables,
+                        const int32_t* context_lens, int batch, int num_q_heads,
+                        int num_kv_heads, int head_dim, int64_t num_blocks,
+                        int max_blocks_per_seq, double scale, int window,
+                        const int64_t* row_ids, int64_t n_rows) {
+  pool_t k_pool = {k_cache, NULL, NULL}, v_pool = {v_cache, NULL, NULL};
+  return paged_decode_pools(out, q, &k_pool, &v_pool, block_tables, context_lens, batch,
+                            num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq,
+                            scale, window, row_ids, n_rows);
+}
+
+/*
+ * INT8 KV cache.  [primer] section 4.2 stores K and V as 8-bit integers to halve the cache,
+ * and section 5.2 turns it on with vLLM's --kv-cache-dtype int8; neither gives the scheme.
+ * Read as symmetric absmax quantization of each (token, kv head) row of d values:
+ *   s = max_e |x_e| / 127            (one fp32 scale per row)
+ *   c_e = round_half_even(x_e / s), clamped to [-127, 127]
+ * and the row's values are c_e * s.  The division and the rounding are single-precision
+ * IEEE operations: they decide an integer, so they are taken in the precision the kernel
+ * takes them in.  A row of zeros gets s = 0 and codes 0; a non-finite element is refused.
+ */
+static int quantize_row(int8_t* codes, float* scale, const uint16_t* x, int head_dim) {
+  float amax = 0.0f;
+  for (int e = 0; e < head_dim; ++e) {
+    float v = bf16_to_float(x[e]);
+    if (!isfinite(v)) return ORC_ERR_VALUE;
+    if (fabsf(v) > amax) amax = fabsf(v);
+  }
+  float s = amax / 127.0f;
+  *scale = s;
+  for (int e = 0; e < head_dim; ++e) {
+    if (s == 0.0f) {
+      codes[e] = 0;
+      continue;
+    }
+    float c = rintf(bf16_to_float(x[e]) / s);
+    if (c > 127.0f) c = 127.0f;
+    if (c < -127.0f) c = -127.0f;
+    codes[e] = (int8_t)c;
+  }
+  return ORC_OK;
+}
+
+/* Quantize n_rows rows of d bf16 values: codes [n_rows][d], scales [n_rows]. */
+int oracle_quantize_rows(int8_t* codes, float* scales, const uint16_t* x, int64_t n_rows,
+                         int head_dim) {
+  if (n_rows < 0 || head_dim <= 0) return ORC_ERR_ARG;
+  for (int64_t r = 0; r < n_rows; ++r) {
+    int st = quantize_row(codes + r * head_dim, scales + r, x + r * head_dim, head_dim);
+    if (st != ORC_OK) return st;
+  }
+  return ORC_OK;
+}
+
+/*
+ * Append into INT8 pools: as oracle_kv_append, with each (token, kv head) row of K and of V
+ * quantized on the way in.  Code pools are [NB][Hkv][16][d] int8, scale pools [NB][Hkv][16].
+ */
+int oracle_kv_append_q8(int8_t* k_codes, int8_t* v_codes, float* k_scales, float* v_scales,
+                        const uint16_t* k, const uint16_t* v, const int64_t* slot_mapping,
+                        int64_t num_tokens, int num_kv_heads, int head_dim, int64_t num_blocks) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return ORC_ERR_ARG;
+  for (int64_t i = 0; i < num_tokens; ++i) {
+    int64_t slot = slot_mapping[i];
+    if (slot < 0) continue;
+    if (slot >= num_blocks * ORC_BLOCK) return ORC_ERR_SLOT;
+    int64_t block = slot / ORC_BLOCK;
+    int64_t offset = slot % ORC_BLOCK;
+    for (int g = 0; g < num_kv_heads; ++g) {
+      int64_t row = (block * num_kv_heads + g) * ORC_BLOCK + offset;
+      int64_t src = (i * num_kv_heads + g) * head_dim;
+      int st = quantize_row(k_codes + row * head_dim, k_scales + row, k + src, head_dim);
+      if (st == ORC_OK) st = quantize_row(v_codes + row * head_dim, v_scales + row, v + src, head_dim);
+      if (st != ORC_OK) return st;
+    }
+  }
+  return ORC_OK;
+}
+
+/*
+ * Paged decode attention over INT8 pools: oracle_paged_decode with every K and V element
+ * dequantized (code * scale, exact in fp64) where it is used.
+ */
+int oracle_paged_decode_q8(double* out, const uint16_t* q, const int8_t* k_codes,
+                           const float* k_scales, const int8_t* v_codes, const float* v_scales,
+                           const int32_t* block_tables, const int32_t* context_lens, int batch,
+                           int num_q_heads, int num_kv_heads, int head_dim, int64_t num_blocks,
+                           int max_blocks_per_seq, double scale, int window,
+                           const int64_t* row_ids, int64_t n_rows) {
+  pool_t k_pool = {NULL, k_codes, k_scales}, v_pool = {NULL, v_codes, v_scales};
+  return paged_decode_pools(out, q, &k_pool, &v_pool, block_tables, context_lens, batch,
+                            num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq,
+                            scale, window, row_ids, n_rows);
 }
 
 /*
@@ -245,8 +367,9 @@ int oracle_sparse_decode(double* out, const uint16_t* q, const uint16_t* k_cache
           if (list[j] < 0 || list[j] >= context_lens[b]) st = ORC_ERR_INDEX;
           if (j > 0 && list[j] <= list[j - 1]) st = ORC_ERR_INDEX;
         }
+        pool_t k_pool = {k_cache, NULL, NULL}, v_pool = {v_cache, NULL, NULL};
         if (st == ORC_OK)
-          st = attend_one_row(out + r * head_dim, q + row * head_dim, k_cache, v_cache,
+          st = attend_one_row(out + r * head_dim, q + row * head_dim, &k_pool, &v_pool,
                               block_tables + (int64_t)b * max_blocks_per_seq,
                               max_blocks_per_seq, num_blocks, num_kv_heads, head_dim, g,
                               scale, tokens, n);

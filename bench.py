@@ -378,6 +378,8 @@ def run_secondary(pkv, W, dev, stream, args):
     torch.cuda.empty_cache()
     res["llama8b_decode_with_scores"] = _scores_row(pkv, W, dev, stream, args, hbm)
     torch.cuda.empty_cache()
+    res["llama8b_decode_int8"] = _q8_row(pkv, W, dev, stream, args, hbm)
+    torch.cuda.empty_cache()
     res["qwen1p5b_step"] = _qwen_step(pkv, W, dev, stream, args, hbm)
     torch.cuda.empty_cache()
     res.update(_sparse_step(pkv, W, dev, stream, args, hbm))
@@ -420,6 +422,44 @@ def _scores_row(pkv, W, dev, stream, args, hbm):
             "gbs": round((kv + extra) / (ms_scored * 1e-3) / 1e9, 1),
             "frac": round((kv + extra) / (ms_scored * 1e-3) / 1e9 / hbm, 4),
             "score_bytes": extra, "l2": "one 0.58 GB pool (> L2)"}
+
+
+def _q8_row(pkv, W, dev, stream, args, hbm):
+    """llama8b decode layer over INT8 pools (random codes, per-row scales ~ Exp, the same
+    context lengths), against the bf16 decode of the same shape."""
+    wl = W.WORKLOADS["llama8b"]
+    c = W.make_layer(wl, device=dev, device_rng=True)
+    nb, hkv, _, d = c["k_cache"].shape
+    g = torch.Generator(device=dev).manual_seed(41)
+    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
+    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
+    ks = torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g) * 0.02
+    vs = torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g) * 0.02
+    ws = torch.zeros(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                c["num_blocks"], c["max_blocks_per_seq"]),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(c["q"])
+
+    def plain():
+        pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
+                                   c["scale"], out=out, workspace=ws, stream=stream)
+
+    def q8():
+        pkv.paged_decode_attention_q8(c["q"], kq, vq, ks, vs, c["block_tables"], c["context_lens"], c["scale"],
+                                      out=out, workspace=ws, stream=stream)
+    steps = max(5, args.steps // 4)
+    ms_plain = _time(plain, args.warmup, steps, dev, stream)
+    ms_q8 = _time(q8, args.warmup, steps, dev, stream)
+    lens = c["context_lens"].cpu()
+    tokens = int(lens.to(torch.int64).sum())
+    blocks = int(((lens.to(torch.int64) + 15) // 16).sum())
+    nbytes = (tokens * wl.num_kv_heads * (wl.head_dim + 4) * 2 + 2 * wl.batch * wl.num_q_heads * wl.head_dim * 2
+              + blocks * 4 + wl.batch * 4)  # codes + row scales of K and V, q, out, tables, lengths
+    del c, kq, vq, ks, vs, ws, out
+    return {"ms": round(ms_q8, 4), "ms_bf16": round(ms_plain, 4), "speedup": round(ms_plain / ms_q8, 3),
+            "tokens_per_s": round(wl.batch / (ms_q8 * 1e-3), 1), "bytes": nbytes,
+            "gbs": round(nbytes / (ms_q8 * 1e-3) / 1e9, 1), "frac": round(nbytes / (ms_q8 * 1e-3) / 1e9 / hbm, 4),
+            "l2": "0.29 GB of INT8 K/V + scales per call (> L2)"}
 
 
 def _graph_time(calls, warmup, steps, dev, stream):

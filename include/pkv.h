@@ -69,6 +69,7 @@ extern "C" {
 #define PKV_DEV_WAIT_TIMEOUT 5      /* an mbarrier wait exceeded its bound (kernel gave up) */
 #define PKV_DEV_BAD_SCORE 6         /* NaN score given to top-k selection */
 #define PKV_DEV_DIRTY_WORKSPACE 7   /* decode workspace counters were not zero at the call */
+#define PKV_DEV_BAD_VALUE 8         /* non-finite K/V element given to the INT8 append */
 
 /* Shape record shared by the calls. */
 typedef struct pkv_dims {
@@ -167,6 +168,46 @@ int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, v
                                       float scale, int32_t window, void* workspace,
                                       size_t workspace_bytes, const pkv_dims* dims,
                                       int32_t* error_word, void* stream);
+
+/*
+ * INT8 KV cache: K and V stored as 8-bit integers, which halves the cache ("KV Cache
+ * primer", cf-1.com/news/5988169, section 4.2; section 5.2 enables it in vLLM with
+ * --kv-cache-dtype int8).  The pages give no scheme; the one used here is symmetric absmax
+ * quantization per (token, kv head) row: scale s = max|x| / 127 (fp32), codes
+ * c = round_half_even(x / s) clamped to [-127, 127] (single-precision IEEE division and
+ * rounding), value c * s.  A zero row has s = 0 and codes 0.
+ * Code pools are [NB, Hkv, 16, d] int8 (the bf16 layout, one byte per element); scale pools
+ * are [NB, Hkv, 16] fp32 (one scale per row: 4/d bytes per element more, 3.1 % at d = 128).
+ *
+ * pkv_kv_append_q8 -- pkv_kv_append into INT8 pools: each new K and V row is quantized into
+ * its slot.
+ *   k_codes, v_codes   : [NB, Hkv, 16, d] int8, updated in place.
+ *   k_scales, v_scales : [NB, Hkv, 16] fp32, updated in place.
+ *   k, v, slot_mapping, num_tokens, dims : as pkv_kv_append.
+ *   error_word         : optional; PKV_DEV_BAD_SLOT, or PKV_DEV_BAD_VALUE for a token whose K or
+ *                        V row holds a non-finite value (its rows are then left unwritten).
+ * All pointers 16-byte aligned.  Bit-exact: the codes and scales of the rule above.
+ */
+int pkv_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k,
+                     const void* v, const int64_t* slot_mapping, int64_t num_tokens, const pkv_dims* dims,
+                     int32_t* error_word, void* stream);
+
+/*
+ * pkv_paged_decode_attention_q8 -- pkv_paged_decode_attention over INT8 pools: every K and V
+ * element is read as code * scale of its row.  Reads half the K/V bytes (plus the scales).
+ *   k_codes, v_codes   : [NB, Hkv, 16, d] int8.
+ *   k_scales, v_scales : [NB, Hkv, 16] fp32, 16-byte aligned; rows of tokens outside the
+ *                        attended set are never used.
+ *   other arguments    : as pkv_paged_decode_attention; the same workspace
+ *                        (pkv_decode_workspace_bytes) serves both.
+ * Computed with fp16 tensor-core products of the exact codes and of q scaled by a power of
+ * two into fp16 range (exact for bf16 q), fp32 sums; the row scales are applied in fp32.
+ */
+int pkv_paged_decode_attention_q8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                                  const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                                  const int32_t* context_lens, float scale, int32_t window, void* workspace,
+                                  size_t workspace_bytes, const pkv_dims* dims, int32_t* error_word,
+                                  void* stream);
 
 /*
  * pkv_paged_decode_attention_scores -- pkv_paged_decode_attention (with this step's append

@@ -21,6 +21,8 @@ __all__ = [
     "read_error", "new_error_word", "header_constants", "header_functions",
     "paged_decode_attention_fixed_scratch", "paged_decode_attention_append",
     "paged_decode_attention_scores", "kv_rolling_admit",
+    "kv_append_q8",
+    "paged_decode_attention_q8",
 ]
 
 BLOCK_SIZE = 16
@@ -93,6 +95,39 @@ def kv_append(k_cache, v_cache, k, v, slot_mapping, *, error_word=None, stream=N
         _ptr(error_word), _stream(stream, dev)))
 
 
+def _q8_pool_dims(k_codes, v_codes, k_scales, v_scales):
+    _need(k_codes, "k_codes", torch.int8, 4)
+    dev = k_codes.device
+    _need(v_codes, "v_codes", torch.int8, 4, dev)
+    _need(k_scales, "k_scales", torch.float32, 3, dev)
+    _need(v_scales, "v_scales", torch.float32, 3, dev)
+    if v_codes.shape != k_codes.shape:
+        raise ValueError("k_codes and v_codes shapes differ")
+    nb, hkv, bs, d = k_codes.shape
+    if bs != BLOCK_SIZE:
+        raise ValueError(f"pool block size must be {BLOCK_SIZE}")
+    if k_scales.shape != (nb, hkv, BLOCK_SIZE) or v_scales.shape != k_scales.shape:
+        raise ValueError("scale pools must be [num_blocks, num_kv_heads, 16]")
+    return nb, hkv, d
+
+
+def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k, v, slot_mapping, *, error_word=None, stream=None):
+    """Quantize k, v [T, Hkv, d] (bf16) into the INT8 pools at slot_mapping [T] (int64):
+    codes [NB, Hkv, 16, d] int8 and one fp32 scale per row, [NB, Hkv, 16]."""
+    nb, hkv, d = _q8_pool_dims(k_codes, v_codes, k_scales, v_scales)
+    dev = k_codes.device
+    _need(k, "k", torch.bfloat16, 3, dev)
+    _need(v, "v", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    T = slot_mapping.shape[0]
+    if k.shape != (T, hkv, d) or v.shape != k.shape:
+        raise ValueError("k/v must be [num_tokens, num_kv_heads, head_dim]")
+    dims = _dims(0, 0, hkv, d, nb, 0)
+    check("pkv_kv_append_q8", load().pkv_kv_append_q8(
+        _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(k), _ptr(v), _ptr(slot_mapping), T,
+        ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+
+
 def decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
                            max_blocks_per_seq) -> int:
     dims = _dims(batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq)
@@ -148,6 +183,29 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     check("pkv_paged_decode_attention", load().pkv_paged_decode_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
+        _ptr(error_word), _stream(stream, dev)))
+    return out
+
+
+def paged_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale,
+                              window=0, *, out=None, workspace=None, error_word=None, stream=None):
+    """paged_decode_attention over INT8 pools (each element code * its row's scale)."""
+    nb, hkv, d = _q8_pool_dims(k_codes, v_codes, k_scales, v_scales)
+    dev = k_codes.device
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    B, hq, dq = q.shape
+    if dq != d:
+        raise ValueError("q head_dim differs from the pools'")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens batch differs from q's")
+    dims = _dims(B, hq, hkv, d, nb, block_tables.shape[1])
+    nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
+    out, workspace = _out_ws(q, out, workspace, nbytes)
+    check("pkv_paged_decode_attention_q8", load().pkv_paged_decode_attention_q8(
+        _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_tables),
+        _ptr(context_lens), float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
         _ptr(error_word), _stream(stream, dev)))
     return out
 

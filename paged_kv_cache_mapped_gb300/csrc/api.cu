@@ -23,8 +23,8 @@ constexpr int kNumGroups = 1;
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
-  size_t max_dyn_smem[2][3] = {};  // [head_dim index][mode: dense, sparse, dense + scores]:
-                                   //   opt-in minus the kernel's static shared memory
+  size_t max_dyn_smem[2][4] = {};  // [head_dim index][mode: dense, sparse, dense + scores,
+                                   //   dense INT8]: opt-in minus the kernel's static shared memory
   int merge_ctas_per_sm[2] = {};   // [head_dim index]: resident merge CTAs per SM
 };
 
@@ -55,8 +55,8 @@ const DeviceInfo* device_info(int* status) {
     }
     for (int hd = 0; hd < kNumHeadDims; ++hd) {
       for (int gi = 0; gi < kNumGroups; ++gi) {
-        for (int sp = 0; sp < 3; ++sp) {
-          const DecodeKernel k = decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp == 1, sp == 2);
+        for (int sp = 0; sp < 4; ++sp) {
+          const DecodeKernel k = decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp == 1, sp == 2, sp == 3);
           if (k.split == nullptr) continue;
           cudaFuncAttributes fa{};
           cudaError_t e = cudaFuncGetAttributes(&fa, k.split);
@@ -122,6 +122,22 @@ int encode_pool_map(CUtensorMap* map, const void* base, long long rows, int head
   const cuuint32_t elem_strides[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_ARGUMENT;
+}
+
+// An INT8 pool [NB, Hkv, 16, D] as a 2-D byte tensor of NB*Hkv*16 rows of D bytes, read in
+// one box of D bytes x 16 rows with the swizzle of the row size (128 or 64 bytes).
+int encode_pool_map_q8(CUtensorMap* map, const void* base, long long rows, int head_dim) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return PKV_ERR_NO_DEVICE;
+  const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[1] = {(cuuint64_t)head_dim};
+  const cuuint32_t box[2] = {(cuuint32_t)head_dim, 16};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_ARGUMENT;
 }
@@ -205,7 +221,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
                   const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
                   void* workspace, size_t workspace_bytes, const pkv_dims* dims, int32_t* err,
                   void* stream, bool sparse, const void* k_new, const void* v_new,
-                  const ScoreOutputs* score_out) {
+                  const ScoreOutputs* score_out, const Q8Scales* q8) {
   int st = check_dims(dims, true);
   if (st != PKV_OK) return st;
   if (dims->batch > kMaxBatch) return PKV_ERR_DIMS;
@@ -218,6 +234,11 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
       !aligned16(workspace))
     return PKV_ERR_ALIGNMENT;
   const int group = dims->num_q_heads / dims->num_kv_heads;
+  if (q8 != nullptr) {
+    if (sparse || score_out != nullptr || k_new != nullptr) return PKV_ERR_ARGUMENT;
+    if (!q8->k_scale || !q8->v_scale) return PKV_ERR_NULL_POINTER;
+    if (!aligned16(q8->k_scale) || !aligned16(q8->v_scale)) return PKV_ERR_ALIGNMENT;
+  }
   if (score_out != nullptr) {
     if (sparse) return PKV_ERR_ARGUMENT;
     if (!score_out->lse || !score_out->scores || !score_out->logits) return PKV_ERR_NULL_POINTER;
@@ -226,7 +247,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
          reinterpret_cast<uintptr_t>(score_out->logits)) & 3u)
       return PKV_ERR_ALIGNMENT;
   }
-  const DecodeKernel k = decode_kernel(dims->head_dim, group, sparse, score_out != nullptr);
+  const DecodeKernel k = decode_kernel(dims->head_dim, group, sparse, score_out != nullptr, q8 != nullptr);
   if (k.split == nullptr) return PKV_ERR_GQA;
   const int max_units = sparse ? (max_kept + 15) / 16 : dims->max_blocks_per_seq;
   // the flattened unit count and the pool's row count (a TMA coordinate) must fit int32
@@ -240,7 +261,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   const DeviceInfo* info = device_info(&st);
   if (!info) return st;
   const size_t smem = decode_smem_bytes(dims->head_dim, sparse, dims->batch);
-  if (smem > info->max_dyn_smem[head_dim_index(dims->head_dim)][sparse ? 1 : (score_out ? 2 : 0)])
+  if (smem > info->max_dyn_smem[head_dim_index(dims->head_dim)][sparse ? 1 : (score_out ? 2 : (q8 ? 3 : 0))])
     return PKV_ERR_DIMS;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.split, kDecodeWarps * 32, smem);
@@ -248,7 +269,13 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   if (per_sm < 1) return PKV_ERR_DIMS;
 
   DecodeArgs a{};
-  if (!sparse) {
+  if (q8 != nullptr) {
+    st = encode_pool_map_q8(&a.tmap_k, k_cache, pool_rows, dims->head_dim);
+    if (st == PKV_OK) st = encode_pool_map_q8(&a.tmap_v, v_cache, pool_rows, dims->head_dim);
+    if (st != PKV_OK) return st;
+    a.k_scale = q8->k_scale;
+    a.v_scale = q8->v_scale;
+  } else if (!sparse) {
     st = encode_pool_map(&a.tmap_k, k_cache, pool_rows, dims->head_dim);
     if (st == PKV_OK) st = encode_pool_map(&a.tmap_v, v_cache, pool_rows, dims->head_dim);
     if (st != PKV_OK) return st;
@@ -289,7 +316,8 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   const int grid = std::min(info->sm_count * per_sm, kMaxWorkers / kDecodeWarps);
   const long long workers = (long long)grid * kDecodeWarps;
   a.workers = (int)workers;
-  const int ring = dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64;
+  const int ring = q8 != nullptr ? (dims->head_dim == 128 ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
+                                 : (dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64);
   a.min_units = std::max(PKV_MIN_UNITS, 1);
   a.tail_pct = std::min(std::max(PKV_TAIL_PCT, 0), 50);
   a.chunk_min = std::max(PKV_CHUNK_MIN, ring);  // a chunk never ends inside the tile ring
@@ -339,6 +367,34 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
                                void* stream) {
   return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, nullptr, nullptr, 0,
                        scale, window, workspace, workspace_bytes, dims, error_word, stream, false);
+}
+
+int pkv_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k,
+                     const void* v, const int64_t* slot_mapping, int64_t num_tokens, const pkv_dims* dims,
+                     int32_t* error_word, void* stream) {
+  int st = check_dims(dims, false);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_DIMS;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_codes || !v_codes || !k_scales || !v_scales || !k || !v || !slot_mapping) return PKV_ERR_NULL_POINTER;
+  if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales) ||
+      !aligned16(k) || !aligned16(v))
+    return PKV_ERR_ALIGNMENT;
+  if (!device_info(&st)) return st;
+  return cuda_status(launch_kv_append_q8(k_codes, v_codes, k_scales, v_scales, k, v, slot_mapping, num_tokens,
+                                         dims->num_kv_heads, dims->head_dim, dims->num_blocks, error_word,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int pkv_paged_decode_attention_q8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                                  const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                                  const int32_t* context_lens, float scale, int32_t window, void* workspace,
+                                  size_t workspace_bytes, const pkv_dims* dims, int32_t* error_word,
+                                  void* stream) {
+  const Q8Scales q8{k_scales, v_scales};
+  return decode_common(out, q, k_codes, v_codes, block_tables, context_lens, nullptr, nullptr, 0, scale,
+                       window, workspace, workspace_bytes, dims, error_word, stream, false, nullptr, nullptr,
+                       nullptr, &q8);
 }
 
 int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, void* v_cache,
@@ -495,6 +551,7 @@ const char* pkv_device_error_string(int code) {
     case PKV_DEV_WAIT_TIMEOUT: return "a bounded wait timed out";
     case PKV_DEV_BAD_SCORE: return "NaN score";
     case PKV_DEV_DIRTY_WORKSPACE: return "decode workspace counters were not zero (zero-fill it before first use)";
+    case PKV_DEV_BAD_VALUE: return "non-finite K/V element given to the INT8 append (token skipped)";
     default: return "unknown device error";
   }
 }

@@ -51,24 +51,34 @@
 namespace pkv {
 namespace {
 
-template <int D, bool SPARSE>
+// Q8: INT8 pools, one byte per element; a tile is a single TMA box of 16 rows x D bytes.
+template <int D, bool SPARSE, bool Q8 = false>
 struct Geo {
-  static constexpr int kRow = D * 2;                       // bytes per K/V row in HBM
-  static constexpr int kBoxes = D / 64;                    // dense: 128-byte column boxes per row
+  static constexpr int kRow = Q8 ? D : D * 2;              // bytes per K/V row in HBM
+  static constexpr int kBoxes = Q8 ? 1 : D / 64;           // dense: 128-byte column boxes per row
   static constexpr int kPitch = D * 2 + 16;                // sparse: padded row pitch in smem
-  static constexpr int kTile = SPARSE ? 16 * kPitch : 16 * D * 2;  // bytes per 16-row tile
+  static constexpr int kTile = Q8 ? 16 * D : (SPARSE ? 16 * kPitch : 16 * D * 2);  // bytes per tile
   static constexpr int kKSteps = D / 16;                   // k-steps of q.K, m-tiles of P.V
-  static constexpr int kRing = (D == 128) ? PKV_RING_D128 : PKV_RING_D64;
-  static_assert(kBoxes * 128 == kRow && kRing >= 2, "head_dim must be a multiple of 64");
+  static constexpr int kRing = Q8 ? ((D == 128) ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
+                                  : ((D == 128) ? PKV_RING_D128 : PKV_RING_D64);
+  static_assert((Q8 || kBoxes * 128 == kRow) && kRing >= 2, "head_dim must be a multiple of 64");
 };
 
 // Byte offset inside a tile of the 16-byte chunk holding row r, columns [8c, 8c + 8).
 // Dense tiles are kBoxes boxes of 16 rows x 128 bytes written by TMA with the 128-byte
 // swizzle (chunk index XOR row % 8 inside each 1024-byte box); sparse tiles are plain rows
 // at the padded pitch.
-template <int D, bool SPARSE>
+// INT8 tiles are one box of 16 rows x D bytes, written with the swizzle of the row size:
+// 128 bytes (chunk XOR row % 8) at D = 128, 64 bytes (chunk XOR (row / 2) % 4) at D = 64.
+// Either way the 8 rows an ldmatrix reads land in 8 different bank groups.
+template <int D, bool SPARSE, bool Q8 = false>
 __device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
-  if constexpr (SPARSE) {
+  if constexpr (Q8) {
+    if constexpr (D == 128)
+      return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+    else
+      return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+  } else if constexpr (SPARSE) {
     return (uint32_t)(r * Geo<D, SPARSE>::kPitch + c * 16);
   } else {
     return (uint32_t)((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
@@ -79,19 +89,29 @@ __device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
 // than this many base-2 units, so unnormalised weights stay below 2^8 and most units skip
 // the rescale.  Any reference value gives the same normalised result.
 constexpr float kRescaleSlack = 8.0f;
+// INT8 pools: the V-scale reference moves when a unit's largest V scale exceeds it by this
+// factor, so P times scale / reference stays below 2^8 * 64 (inside fp16).
+constexpr float kVrefSlack = 64.0f;
 
-template <int D, bool SPARSE>
+template <int D, bool SPARSE, bool Q8 = false>
 struct WarpTiles {
-  alignas(1024) unsigned char k[Geo<D, SPARSE>::kRing][Geo<D, SPARSE>::kTile];
-  alignas(1024) unsigned char v[Geo<D, SPARSE>::kRing][Geo<D, SPARSE>::kTile];
+  alignas(1024) unsigned char k[Geo<D, SPARSE, Q8>::kRing][Geo<D, SPARSE, Q8>::kTile];
+  alignas(1024) unsigned char v[Geo<D, SPARSE, Q8>::kRing][Geo<D, SPARSE, Q8>::kTile];
 };
 
-template <int D, bool SPARSE>
+template <int D, bool SPARSE, bool Q8 = false>
 struct WarpSlots {
-  uint64_t bar_k[Geo<D, SPARSE>::kRing];  // K rows of the slot landed
-  uint64_t bar_v[Geo<D, SPARSE>::kRing];  // V rows of the slot landed
-  uint32_t meta[Geo<D, SPARSE>::kRing];   // rows of the unit that were copied (bit t = token t)
-  int32_t phys[Geo<D, SPARSE>::kRing];    // dense: physical block of the unit in the slot
+  uint64_t bar_k[Geo<D, SPARSE, Q8>::kRing];  // K rows of the slot landed
+  uint64_t bar_v[Geo<D, SPARSE, Q8>::kRing];  // V rows of the slot landed
+  uint32_t meta[Geo<D, SPARSE, Q8>::kRing];   // rows of the unit that were copied (bit t = token t)
+  int32_t phys[Geo<D, SPARSE, Q8>::kRing];    // dense: physical block of the unit in the slot
+};
+
+// INT8 pools: the row scales of the K and V tiles of each slot, copied with the K tile.
+template <int R>
+struct WarpScales {
+  alignas(16) float k[R][16];
+  alignas(16) float v[R][16];
 };
 
 struct Cursor {
@@ -240,13 +260,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // SCORES (dense only): also keep every attended key's base-2 logit and write the log-sum-exp of
 // rows written out directly, for the score step (decode_score_kernel).
-template <int D, bool SPARSE, bool SCORES>
+template <int D, bool SPARSE, bool SCORES, bool Q8>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   static_assert(!(SPARSE && SCORES), "scores are emitted by the dense decode only");
-  using GE = Geo<D, SPARSE>;
-  using WT = WarpTiles<D, SPARSE>;
-  using WB = WarpSlots<D, SPARSE>;
+  static_assert(!(Q8 && (SPARSE || SCORES)), "INT8 pools are read by the plain dense decode only");
+  using GE = Geo<D, SPARSE, Q8>;
+  using WT = WarpTiles<D, SPARSE, Q8>;
+  using WB = WarpSlots<D, SPARSE, Q8>;
   constexpr int R = GE::kRing;
   constexpr int KS = GE::kKSteps;
 
@@ -257,6 +278,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
                 "tile rings exceed static shared memory");
   __shared__ WT warps_tiles[kDecodeWarps];
   __shared__ WB warps_slots[kDecodeWarps];
+  __shared__ WarpScales<Q8 ? GE::kRing : 1> warps_scales[Q8 ? kDecodeWarps : 1];  // INT8 pools only
   __shared__ int32_t s_part[kPartFields];
   __shared__ uint32_t s_ticket[kDecodeWarps];
   extern __shared__ __align__(16) int32_t smem_dyn[];
@@ -377,14 +399,26 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
 
   // q of the next segment as raw bf16x2 words in B-fragment order: word 2ks+i holds head gq's
   // elements 16ks + 8i + 2tq, +1 (zero for heads >= G).  The first segment's right away.
+  // INT8 pools: word 2ks+i holds elements 16ks + 4tq + 2i, +1 (the order in which an ldmatrix
+  // of int8 rows hands each lane its K bytes: four consecutive columns).
   uint32_t qraw[2 * KS];
   auto load_q = [&](int b, int g) {
     if (gq < G) {
-      const uint32_t* qw = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * a.Hq + (size_t)g * G + gq) * D);
+      if constexpr (Q8) {
+        const uint2* qw = reinterpret_cast<const uint2*>(a.q + ((size_t)b * a.Hq + (size_t)g * G + gq) * D);
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qraw[2 * ks] = __ldg(qw + ks * 8 + tq);
-        qraw[2 * ks + 1] = __ldg(qw + ks * 8 + 4 + tq);
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint2 w = __ldg(qw + ks * 4 + tq);
+          qraw[2 * ks] = w.x;
+          qraw[2 * ks + 1] = w.y;
+        }
+      } else {
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * a.Hq + (size_t)g * G + gq) * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          qraw[2 * ks] = __ldg(qw + ks * 8 + tq);
+          qraw[2 * ks + 1] = __ldg(qw + ks * 8 + 4 + tq);
+        }
       }
     } else {
 #pragma unroll
@@ -426,14 +460,26 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
           const int y = (phys * a.Hkv + ic.g) * 16;  // host checks NB*Hkv*16 < 2^31
           Wb.meta[slot] = 0xffffu;
           Wb.phys[slot] = phys;
-          mbar_arrive_expect_tx(&Wb.bar_k[slot], GE::kTile);
+          if constexpr (Q8) {
+            // the K tile and both tiles' 16 row scales (64 bytes each, 64-byte aligned rows of
+            // the scale pools) complete on the K barrier: the softmax needs the V scales too
+            auto& Ws = warps_scales[warp];
+            mbar_arrive_expect_tx(&Wb.bar_k[slot], GE::kTile + 2 * 64);
+            tma_load_2d(Wt.k[slot], &a.tmap_k, 0, y, &Wb.bar_k[slot], pol);
+            bulk_g2s(Ws.k[slot], a.k_scale + y, 64, &Wb.bar_k[slot], pol);
+            bulk_g2s(Ws.v[slot], a.v_scale + y, 64, &Wb.bar_k[slot], pol);
+            mbar_arrive_expect_tx(&Wb.bar_v[slot], GE::kTile);
+            tma_load_2d(Wt.v[slot], &a.tmap_v, 0, y, &Wb.bar_v[slot], pol);
+          } else {
+            mbar_arrive_expect_tx(&Wb.bar_k[slot], GE::kTile);
 #pragma unroll
-          for (int bx = 0; bx < GE::kBoxes; ++bx)
-            tma_load_2d(Wt.k[slot] + bx * 2048, &a.tmap_k, bx * 64, y, &Wb.bar_k[slot], pol);
-          mbar_arrive_expect_tx(&Wb.bar_v[slot], GE::kTile);
+            for (int bx = 0; bx < GE::kBoxes; ++bx)
+              tma_load_2d(Wt.k[slot] + bx * 2048, &a.tmap_k, bx * 64, y, &Wb.bar_k[slot], pol);
+            mbar_arrive_expect_tx(&Wb.bar_v[slot], GE::kTile);
 #pragma unroll
-          for (int bx = 0; bx < GE::kBoxes; ++bx)
-            tma_load_2d(Wt.v[slot] + bx * 2048, &a.tmap_v, bx * 64, y, &Wb.bar_v[slot], pol);
+            for (int bx = 0; bx < GE::kBoxes; ++bx)
+              tma_load_2d(Wt.v[slot] + bx * 2048, &a.tmap_v, bx * 64, y, &Wb.bar_v[slot], pol);
+          }
         } else {
           record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
           Wb.meta[slot] = 0u;
@@ -498,9 +544,13 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   int seg_slot = -1;  // partial slot of the current segment, -1: written out directly
   float* seg_logits = nullptr;  // scores mode: logit row of this lane's head h0 in the segment
   const float sl2 = a.scale_log2;
+  // INT8 pools: q of the segment is prescaled by a power of two into fp16 range, so logits
+  // use sl2q = sl2 over that power; o is kept in units of a V-scale reference vref that moves
+  // (and rescales o) only when a unit's largest V scale exceeds it by kVrefSlack.
+  float sl2q = sl2, vref = 0.f, inv_vref = 0.f;
   // Dense append mode: this step's K (lanes 0-15) or V (lanes 16-31) row chunk of the current
   // segment, to be written at token L_b - 1 (pool and tile) when its unit is consumed.
-  const bool appending = !SPARSE && a.k_new != nullptr;
+  const bool appending = !SPARSE && !Q8 && a.k_new != nullptr;
   uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
   const int new_chunk = lane & 15;
   const bool new_lane = new_chunk < D / 8;
@@ -523,19 +573,34 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
           if (gq == 0) a.lse[row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* dst = a.out + row * D + gq;
+        if constexpr (Q8) {  // accumulator rows gq, gq + 8 are columns 2gq, 2gq + 1 of each 16
+          const float f = inv * vref;
+          __nv_bfloat16* dst = a.out + row * D + 2 * gq;
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          dst[mt * 16] = __float2bfloat16_rn(o[mt][hh] * inv);
-          dst[mt * 16 + 8] = __float2bfloat16_rn(o[mt][2 + hh] * inv);
+          for (int mt = 0; mt < KS; ++mt)
+            *reinterpret_cast<uint32_t*>(dst + mt * 16) = pack_bf16x2(o[mt][hh] * f, o[mt][2 + hh] * f);
+        } else {
+          __nv_bfloat16* dst = a.out + row * D + gq;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            dst[mt * 16] = __float2bfloat16_rn(o[mt][hh] * inv);
+            dst[mt * 16 + 8] = __float2bfloat16_rn(o[mt][2 + hh] * inv);
+          }
         }
       } else {
         const size_t e = (size_t)seg_slot * G + head;  // a flush writes G adjacent entries
-        float* dst = a.part_o + e * D + gq;
+        if constexpr (Q8) {
+          float* dst = a.part_o + e * D + 2 * gq;
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          dst[mt * 16] = o[mt][hh];
-          dst[mt * 16 + 8] = o[mt][2 + hh];
+          for (int mt = 0; mt < KS; ++mt)
+            *reinterpret_cast<float2*>(dst + mt * 16) = make_float2(o[mt][hh] * vref, o[mt][2 + hh] * vref);
+        } else {
+          float* dst = a.part_o + e * D + gq;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            dst[mt * 16] = o[mt][hh];
+            dst[mt * 16 + 8] = o[mt][2 + hh];
+          }
         }
         if (gq == 0) a.part_ml[e] = make_float2(m, l);
       }
@@ -552,8 +617,24 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     seg_slot = (seg_begin >= u0 && seg_begin + nb <= u0 + nunits) ? -1 : 2 * ridx + (u0 >= seg_begin ? 0 : 1);
     if constexpr (SCORES)
       seg_logits = a.logits + ((size_t)c.b * a.Hq + (size_t)c.g * G + 2 * tq) * a.score_stride;
+    if constexpr (Q8) {
+      // q times 2^kq, with the segment's largest |q| brought into [2^14, 2^15): exact for
+      // bf16 inputs, inside fp16 range (sign-cleared fp32 bit patterns order like the values)
+      uint32_t mx = 0u;
 #pragma unroll
-    for (int i = 0; i < 2 * KS; ++i) qb[i] = qraw[i];
+      for (int i = 0; i < 2 * KS; ++i) mx = max(mx, max(qraw[i] & 0x7fff0000u, (qraw[i] << 16) & 0x7fff0000u));
+      mx = __reduce_max_sync(kFullMask, mx);
+      const int kq = mx == 0u ? 0 : max(-100, min(100, 141 - (int)(mx >> 23)));
+      const float up = __int_as_float((127 + kq) << 23);
+      sl2q = sl2 * __int_as_float((127 - kq) << 23);
+#pragma unroll
+      for (int i = 0; i < 2 * KS; ++i) qb[i] = pack_f16x2(bf16_lo_to_f32(qraw[i]) * up, bf16_hi_to_f32(qraw[i]) * up);
+      vref = 0.f;
+      inv_vref = 0.f;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2 * KS; ++i) qb[i] = qraw[i];
+    }
     if (appending && new_lane) {
       const __nv_bfloat16* src = (lane >= 16 ? a.v_new : a.k_new) + ((size_t)c.b * a.Hkv + c.g) * D + new_chunk * 8;
       new_row = __ldg(reinterpret_cast<const uint4*>(src));
@@ -617,20 +698,41 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       // -- S^T = K q^T: 16 tokens x 8 heads --------------------------------------------------
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t kbase = smem_u32(Wt.k[slot]);
+      float fk0 = sl2, fk1 = sl2;  // logit factor of tokens gq and gq + 8
+      if constexpr (Q8) {
+        // int8 rows: one ldmatrix yields two k-steps; each lane holds 4 consecutive columns
+        // of a row per matrix, the order q was loaded in
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t af[4];
-        ldsm_x4(kbase + chunk_offset<D, SPARSE>(k_row, 2 * ks + k_half), af);
-        mma_bf16_m16n8k16(c, af, qb[2 * ks], qb[2 * ks + 1]);
+        for (int pp = 0; pp < KS / 2; ++pp) {
+          uint32_t r[4];
+          ldsm_x4(kbase + chunk_offset<D, SPARSE, Q8>(k_row, 2 * pp + k_half), r);
+          const uint32_t f0 = r[0] ^ 0x80808080u, f1 = r[1] ^ 0x80808080u;
+          const uint32_t f2 = r[2] ^ 0x80808080u, f3 = r[3] ^ 0x80808080u;
+          const uint32_t a0[4] = {i8x2_to_f16x2<0x4140>(f0), i8x2_to_f16x2<0x4140>(f1),
+                                  i8x2_to_f16x2<0x4342>(f0), i8x2_to_f16x2<0x4342>(f1)};
+          mma_f16_m16n8k16(c, a0, qb[4 * pp], qb[4 * pp + 1]);
+          const uint32_t a1[4] = {i8x2_to_f16x2<0x4140>(f2), i8x2_to_f16x2<0x4140>(f3),
+                                  i8x2_to_f16x2<0x4342>(f2), i8x2_to_f16x2<0x4342>(f3)};
+          mma_f16_m16n8k16(c, a1, qb[4 * pp + 2], qb[4 * pp + 3]);
+        }
+        fk0 = warps_scales[warp].k[slot][gq] * sl2q;
+        fk1 = warps_scales[warp].k[slot][gq + 8] * sl2q;
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t af[4];
+          ldsm_x4(kbase + chunk_offset<D, SPARSE>(k_row, 2 * ks + k_half), af);
+          mma_bf16_m16n8k16(c, af, qb[2 * ks], qb[2 * ks + 1]);
+        }
       }
       // c[0] = (token gq, head h0), c[1] = (gq, h1), c[2] = (gq + 8, h0), c[3] = (gq + 8, h1)
       const bool t0 = (mask >> gq) & 1u;
       const bool t1 = (mask >> (gq + 8)) & 1u;
       const bool v0 = 2 * tq < G, v1 = 2 * tq + 1 < G;
-      const float s00 = (t0 && v0) ? c[0] * sl2 : -INFINITY;
-      const float s01 = (t0 && v1) ? c[1] * sl2 : -INFINITY;
-      const float s10 = (t1 && v0) ? c[2] * sl2 : -INFINITY;
-      const float s11 = (t1 && v1) ? c[3] * sl2 : -INFINITY;
+      const float s00 = (t0 && v0) ? c[0] * fk0 : -INFINITY;
+      const float s01 = (t0 && v1) ? c[1] * fk0 : -INFINITY;
+      const float s10 = (t1 && v0) ? c[2] * fk1 : -INFINITY;
+      const float s11 = (t1 && v1) ? c[3] * fk1 : -INFINITY;
       if constexpr (SCORES) {  // keep the attended keys' logits for the score step
         const int tok = (s_first[cc.b] + cc.j) * 16 + gq;
         float* lg = seg_logits + tok;
@@ -649,9 +751,21 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, m));
         mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, m));
       }
+      // INT8 pools: the V scales of the attended tokens, and their largest (warp-uniform)
+      float vs0 = 0.f, vs1 = 0.f;
+      bool gv = false;
+      float vm = 0.f;
+      if constexpr (Q8) {
+        vs0 = t0 ? warps_scales[warp].v[slot][gq] : 0.f;
+        vs1 = t1 ? warps_scales[warp].v[slot][gq + 8] : 0.f;
+        vm = fmaxf(vs0, vs1);
+#pragma unroll
+        for (int m = 4; m <= 16; m <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullMask, vm, m));
+        gv = vm > vref * kVrefSlack;
+      }
       // lazy running max: move it only when this unit's max is well above it
       const bool g0 = mx0 > mr0 + kRescaleSlack, g1 = mx1 > mr1 + kRescaleSlack;
-      if (__any_sync(kFullMask, g0 || g1)) {
+      if (__any_sync(kFullMask, g0 || g1) || gv) {
         float al0 = 1.f, al1 = 1.f;
         if (g0) {
           al0 = exp2f(mr0 - mx0);
@@ -663,6 +777,15 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         }
         l0 *= al0;
         l1 *= al1;
+        if constexpr (Q8) {
+          if (gv) {  // o moves to the new V reference (o is zero while vref is)
+            const float fv = vref > 0.f ? vref / vm : 0.f;
+            al0 *= fv;
+            al1 *= fv;
+            vref = vm;
+            inv_vref = 1.f / vm;
+          }
+        }
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           o[mt][0] *= al0;
@@ -678,10 +801,21 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       l0 += p00 + p10;
       l1 += p01 + p11;
       // -- P^T as bf16 hi + lo B fragments (tokens x heads -> heads x tokens) -------------
-      const uint32_t hA = pack_bf16x2(p00, p01);  // token gq
-      const uint32_t hB = pack_bf16x2(p10, p11);  // token gq + 8
-      const uint32_t lA = pack_bf16x2(p00 - bf16_lo_to_f32(hA), p01 - bf16_hi_to_f32(hA));
-      const uint32_t lB = pack_bf16x2(p10 - bf16_lo_to_f32(hB), p11 - bf16_hi_to_f32(hB));
+      // INT8 pools: fp16 parts of P times each token's V scale over vref (at most 2^8 * slack)
+      uint32_t hA, hB, lA, lB;
+      if constexpr (Q8) {
+        const float r0 = vs0 * inv_vref, r1 = vs1 * inv_vref;
+        const float w00 = p00 * r0, w01 = p01 * r0, w10 = p10 * r1, w11 = p11 * r1;
+        hA = pack_f16x2(w00, w01);
+        hB = pack_f16x2(w10, w11);
+        lA = pack_f16x2(w00 - f16_lo_to_f32(hA), w01 - f16_hi_to_f32(hA));
+        lB = pack_f16x2(w10 - f16_lo_to_f32(hB), w11 - f16_hi_to_f32(hB));
+      } else {
+        hA = pack_bf16x2(p00, p01);  // token gq
+        hB = pack_bf16x2(p10, p11);  // token gq + 8
+        lA = pack_bf16x2(p00 - bf16_lo_to_f32(hA), p01 - bf16_hi_to_f32(hA));
+        lB = pack_bf16x2(p10 - bf16_lo_to_f32(hB), p11 - bf16_hi_to_f32(hB));
+      }
       const uint32_t bh0 = movmatrix_trans(hA), bh1 = movmatrix_trans(hB);
       const uint32_t bl0 = movmatrix_trans(lA), bl1 = movmatrix_trans(lB);
       if (!__all_sync(kFullMask, mbar_wait_bounded(&Wb.bar_v[slot], parity, a.timeout_ns))) {
@@ -697,9 +831,9 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         }
         __syncwarp();
       }
-      if (mask != 0xffffu) {
+      if (!Q8 && mask != 0xffffu) {
         // rows of tokens outside the attended set may hold anything (even NaN): zero them,
-        // since the tensor core would turn 0 * NaN into NaN
+        // since the tensor core would turn 0 * NaN into NaN (int8 codes are always finite)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int t = 2 * i + (lane >> 4);
@@ -711,12 +845,32 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       }
       // -- O^T += V^T P^T -------------------------------------------------------------------
       const uint32_t vbase = smem_u32(Wt.v[slot]);
+      if constexpr (Q8) {
+        // transposed int8 ldmatrix: each lane gets columns 2gq, 2gq + 1 of tokens 2tq, 2tq + 1;
+        // columns 2gq and 2gq + 1 become accumulator rows gq and gq + 8 of the 16-column tile
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        uint32_t av[4];
-        ldsm_x4_trans(vbase + chunk_offset<D, SPARSE>(v_row, 2 * mt + v_half), av);
-        mma_bf16_m16n8k16(o[mt], av, bh0, bh1);
-        mma_bf16_m16n8k16(o[mt], av, bl0, bl1);
+        for (int pp = 0; pp < KS / 2; ++pp) {
+          uint32_t r[4];
+          ldsm_x4_trans(vbase + chunk_offset<D, SPARSE, Q8>(k_row, 2 * pp + k_half), r);
+          const uint32_t f0 = r[0] ^ 0x80808080u, f1 = r[1] ^ 0x80808080u;
+          const uint32_t f2 = r[2] ^ 0x80808080u, f3 = r[3] ^ 0x80808080u;
+          const uint32_t a0[4] = {i8x2_to_f16x2<0x4240>(f0), i8x2_to_f16x2<0x4341>(f0),
+                                  i8x2_to_f16x2<0x4240>(f1), i8x2_to_f16x2<0x4341>(f1)};
+          mma_f16_m16n8k16(o[2 * pp], a0, bh0, bh1);
+          mma_f16_m16n8k16(o[2 * pp], a0, bl0, bl1);
+          const uint32_t a1[4] = {i8x2_to_f16x2<0x4240>(f2), i8x2_to_f16x2<0x4341>(f2),
+                                  i8x2_to_f16x2<0x4240>(f3), i8x2_to_f16x2<0x4341>(f3)};
+          mma_f16_m16n8k16(o[2 * pp + 1], a1, bh0, bh1);
+          mma_f16_m16n8k16(o[2 * pp + 1], a1, bl0, bl1);
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          uint32_t av[4];
+          ldsm_x4_trans(vbase + chunk_offset<D, SPARSE>(v_row, 2 * mt + v_half), av);
+          mma_bf16_m16n8k16(o[mt], av, bh0, bh1);
+          mma_bf16_m16n8k16(o[mt], av, bl0, bl1);
+        }
       }
     } else if (!__all_sync(kFullMask, mbar_wait_bounded(&Wb.bar_v[slot], parity, a.timeout_ns))) {
       if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
@@ -978,20 +1132,22 @@ __global__ void __launch_bounds__(kScoreThreads) decode_score_kernel(const Decod
 
 }  // namespace
 
-DecodeKernel decode_kernel(int head_dim, int group, bool sparse, bool scores) {
-  const DecodeKernel none{nullptr, nullptr, nullptr, head_dim, group, sparse, scores};
-  if (group < 1 || group > kMaxGroup || (sparse && scores)) return none;
+DecodeKernel decode_kernel(int head_dim, int group, bool sparse, bool scores, bool q8) {
+  const DecodeKernel none{nullptr, nullptr, nullptr, head_dim, group, sparse, scores, q8};
+  if (group < 1 || group > kMaxGroup || (sparse && scores) || (q8 && (sparse || scores))) return none;
   const void* score = scores ? (const void*)decode_score_kernel : nullptr;
   if (head_dim == 128)
-    return DecodeKernel{sparse   ? (const void*)decode_split_kernel<128, true, false>
-                        : scores ? (const void*)decode_split_kernel<128, false, true>
-                                 : (const void*)decode_split_kernel<128, false, false>,
-                        (const void*)decode_merge_kernel<128>, score, 128, group, sparse, scores};
+    return DecodeKernel{q8       ? (const void*)decode_split_kernel<128, false, false, true>
+                        : sparse ? (const void*)decode_split_kernel<128, true, false, false>
+                        : scores ? (const void*)decode_split_kernel<128, false, true, false>
+                                 : (const void*)decode_split_kernel<128, false, false, false>,
+                        (const void*)decode_merge_kernel<128>, score, 128, group, sparse, scores, q8};
   if (head_dim == 64)
-    return DecodeKernel{sparse   ? (const void*)decode_split_kernel<64, true, false>
-                        : scores ? (const void*)decode_split_kernel<64, false, true>
-                                 : (const void*)decode_split_kernel<64, false, false>,
-                        (const void*)decode_merge_kernel<64>, score, 64, group, sparse, scores};
+    return DecodeKernel{q8       ? (const void*)decode_split_kernel<64, false, false, true>
+                        : sparse ? (const void*)decode_split_kernel<64, true, false, false>
+                        : scores ? (const void*)decode_split_kernel<64, false, true, false>
+                                 : (const void*)decode_split_kernel<64, false, false, false>,
+                        (const void*)decode_merge_kernel<64>, score, 64, group, sparse, scores, q8};
   return none;
 }
 

@@ -20,7 +20,8 @@ namespace pkv {
 // changes what it computes, and its partial results go to fixed slots of the range.
 struct DecodeArgs {
   CUtensorMap tmap_k;            // dense mode: the K pool as a 2-D [NB*Hkv*16, D] bf16 tensor,
-  CUtensorMap tmap_v;            //   box 64 x 16, 128-byte swizzle (likewise V)
+  CUtensorMap tmap_v;            //   box 64 x 16, 128-byte swizzle (likewise V); INT8 pools:
+                                 //   [NB*Hkv*16, D] bytes, box D x 16, swizzle of D bytes
   const __nv_bfloat16* q;        // [B, Hq, D]
   const __nv_bfloat16* k_cache;  // [NB, Hkv, 16, D]
   const __nv_bfloat16* v_cache;
@@ -37,6 +38,8 @@ struct DecodeArgs {
   int32_t* layout;               // [2B]: unit start (times Hkv) and units of each sequence, for large B
   float2* part_ml;               // [2 ranges, G] (running max in log2 units, running sum)
   float* part_o;                 // [2 ranges, G, D] unnormalised partial outputs
+  const float* k_scale;          // INT8 pools: [NB, Hkv, 16] fp32 scale of each K row
+  const float* v_scale;          //   (likewise V); the pools then hold int8 codes
   float* logits;                 // scores mode: [B, Hq, score_stride] base-2 logits of attended keys
   float* lse;                    // scores mode: [B, Hq] natural log-sum-exp of each row
   float* scores;                 // scores mode: [B, Hkv, score_stride] accumulated scores
@@ -71,6 +74,13 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #define PKV_RING_D64 4
 #endif
 
+#ifndef PKV_RING_Q8_D128
+#define PKV_RING_Q8_D128 4  // INT8 K/V tile pairs in flight per worker warp at head_dim 128
+#endif
+#ifndef PKV_RING_Q8_D64
+#define PKV_RING_Q8_D64 4
+#endif
+
 #ifndef PKV_MIN_UNITS
 #define PKV_MIN_UNITS 16  // lower bound of a worker slice, in 16-token units
 #endif
@@ -92,18 +102,18 @@ constexpr int kMaxWorkers = 2048;    // worker warps of a decode grid at most (s
 constexpr int kMergeWarps = 8;
 constexpr int kMaxGroup = 8;         // query heads per kv head handled by one fragment
 
-// Kernel handles of one (head_dim, group, sparse, scores) instantiation.
+// Kernel handles of one (head_dim, group, sparse, scores, INT8) instantiation.
 struct DecodeKernel {
   const void* split;
   const void* merge;
   const void* score;  // scores mode: adds the step's probabilities into the scores
   int head_dim, group;
-  bool sparse, scores;
+  bool sparse, scores, q8;
 };
 
 // Returns a struct with split == nullptr when the combination is unsupported (scores mode
-// exists for dense decode only).
-DecodeKernel decode_kernel(int head_dim, int group, bool sparse, bool scores = false);
+// and INT8 pools exist for dense decode only, and not together).
+DecodeKernel decode_kernel(int head_dim, int group, bool sparse, bool scores = false, bool q8 = false);
 size_t decode_smem_bytes(int head_dim, bool sparse, int batch);
 // merge_wpr_log2: log2 of the merge warps per output row (0..3).
 cudaError_t launch_decode(const DecodeKernel& k, const DecodeArgs& a, int grid, size_t smem,
@@ -115,6 +125,9 @@ cudaError_t kvops_device_setup();
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
                              const int64_t* slots, int64_t T, int Hkv, int D, int NB,
                              int32_t* err, cudaStream_t stream);
+cudaError_t launch_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                                const void* k, const void* v, const int64_t* slots, int64_t T, int Hkv,
+                                int D, int NB, int32_t* err, cudaStream_t stream);
 cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, int dMB,
                               const void* sk, const void* sv, const int32_t* sbt,
                               const int32_t* lens, const int32_t* kept, const int32_t* kept_lens,
@@ -165,11 +178,17 @@ struct ScoreOutputs {
   int stride;
 };
 
+// INT8 pools of a dense decode (pkv_paged_decode_attention_q8); nullptr: bf16 pools.
+struct Q8Scales {
+  const float* k_scale;
+  const float* v_scale;
+};
+
 int decode_common(void* out, const void* q, const void* k_cache, const void* v_cache,
                   const int32_t* block_tables, const int32_t* context_lens, const int32_t* kept,
                   const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
                   void* workspace, size_t workspace_bytes, const struct pkv_dims* dims, int32_t* err,
                   void* stream, bool sparse, const void* k_new = nullptr, const void* v_new = nullptr,
-                  const ScoreOutputs* score_out = nullptr);
+                  const ScoreOutputs* score_out = nullptr, const Q8Scales* q8 = nullptr);
 
 }  // namespace pkv

@@ -48,6 +48,85 @@ __global__ void __launch_bounds__(256) kv_append_kernel(__nv_bfloat16* __restric
   else copy_row_half<D>(vc + dst, v + src, lane - 16);
 }
 
+// INT8 append: the new token's K and V rows quantized into INT8 pools (the KV-cache primer's
+// INT8 cache, section 4.2).  Each (token, kv head) row of d values gets one fp32 scale
+// s = max|x| / 127 and codes round_half_even(x / s), clamped to [-127, 127]; a zero row gets
+// s = 0 and codes 0.  The division and rounding are IEEE single precision (they decide the
+// codes).  One warp per (token, kv head): lanes 0-15 quantize the K row, lanes 16-31 the V
+// row, D/16 elements each.  A non-finite element skips the token's rows and is reported.
+template <int D>
+__global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ kq, int8_t* __restrict__ vq,
+                                                           float* __restrict__ ks, float* __restrict__ vs,
+                                                           const __nv_bfloat16* __restrict__ k,
+                                                           const __nv_bfloat16* __restrict__ v,
+                                                           const int64_t* __restrict__ slots, int64_t T,
+                                                           int Hkv, int NB, int32_t* err) {
+  constexpr int E = D / 16;  // elements per lane
+  const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (item >= T * Hkv) return;
+  const int64_t tok = item / Hkv;
+  const int g = (int)(item - tok * Hkv);
+  const int64_t slot = __ldg(slots + tok);
+  if (slot < 0) return;
+  if (slot >= (int64_t)NB * 16) {
+    if (lane == 0) record_error(err, PKV_DEV_BAD_SLOT);
+    return;
+  }
+  const int h = lane & 15;
+  const __nv_bfloat16* src = (lane < 16 ? k : v) + ((size_t)tok * Hkv + g) * D + h * E;
+  float x[E];
+  if constexpr (E == 8) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(ws[i] << 16);
+      x[2 * i + 1] = __uint_as_float(ws[i] & 0xffff0000u);
+    }
+  } else {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+    const uint32_t ws[2] = {w.x, w.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      x[2 * i] = __uint_as_float(ws[i] << 16);
+      x[2 * i + 1] = __uint_as_float(ws[i] & 0xffff0000u);
+    }
+  }
+  float amax = 0.f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    finite &= isfinite(x[i]);
+    amax = fmaxf(amax, fabsf(x[i]));
+  }
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));  // within the half
+  if (!__all_sync(kFullMask, finite)) {
+    if (lane == 0) record_error(err, PKV_DEV_BAD_VALUE);
+    return;
+  }
+  const float sc = __fdiv_rn(amax, 127.0f);
+  uint32_t packed[E / 4];
+#pragma unroll
+  for (int i = 0; i < E / 4; ++i) packed[i] = 0u;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    int c = 0;
+    if (sc != 0.f) c = max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], sc))));
+    packed[i / 4] |= (uint32_t)(c & 0xff) << (8 * (i % 4));
+  }
+  const size_t row = ((size_t)(slot >> 4) * Hkv + g) * 16 + (size_t)(slot & 15);
+  int8_t* dst = (lane < 16 ? kq : vq) + row * D + h * E;
+  if constexpr (E == 8)
+    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+  else
+    *reinterpret_cast<uint32_t*>(dst) = packed[0];
+  if (h == 0) (lane < 16 ? ks : vs)[row] = sc;
+}
+
 // Compaction: compact position j of (b, g) <- source token kept[b][g][j] (the per-layer
 // block-table policy of "How KV Sparsity Achieves 1.5x Acceleration for vLLM", section "Key
 // technique 1").  One warp per (b, g, j).
@@ -412,6 +491,21 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const 
   auto* vv = static_cast<const __nv_bfloat16*>(v);
   void* args[] = {&kc, &vc, &kk, &vv, &slots, &T, &Hkv, &NB, &err};
   const void* fn = D == 128 ? (const void*)kv_append_kernel<128> : (const void*)kv_append_kernel<64>;
+  return launch_pdl(fn, dim3(grid), dim3(256), 0, stream, args);
+}
+
+cudaError_t launch_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                                const void* k, const void* v, const int64_t* slots, int64_t T, int Hkv,
+                                int D, int NB, int32_t* err, cudaStream_t stream) {
+  const int64_t warps = T * Hkv;
+  if (warps == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
+  auto* kq = static_cast<int8_t*>(k_codes);
+  auto* vq = static_cast<int8_t*>(v_codes);
+  auto* kk = static_cast<const __nv_bfloat16*>(k);
+  auto* vv = static_cast<const __nv_bfloat16*>(v);
+  void* args[] = {&kq, &vq, &k_scales, &v_scales, &kk, &vv, &slots, &T, &Hkv, &NB, &err};
+  const void* fn = D == 128 ? (const void*)kv_append_q8_kernel<128> : (const void*)kv_append_q8_kernel<64>;
   return launch_pdl(fn, dim3(grid), dim3(256), 0, stream, args);
 }
 

@@ -171,6 +171,16 @@ __device__ __forceinline__ void mma_bf16_m16n8k16(float (&d)[4], const uint32_t 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// d += a * b as mma_bf16_m16n8k16, with fp16 operands: products exact, fp32 sums.
+__device__ __forceinline__ void mma_f16_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                 uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Transpose an 8x8 b16 matrix held one row pair per lane (the ldmatrix fragment layout).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
@@ -182,6 +192,36 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 -> packed f16x2, round-to-nearest-even; `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t w) {
+  float f;
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, l; }" : "=f"(f) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t w) {
+  float f;
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, h; }" : "=f"(f) : "r"(w));
+  return f;
+}
+
+// Two int8 codes of a word as an exact f16x2.  `flipped` is the word with every byte's sign
+// bit inverted (byte = code + 128); SEL names the two bytes (low result half first) in the
+// form 0x4j4i.  Byte u under the exponent byte 0x64 is the fp16 number 1024 + u (fp16 holds
+// every integer below 2048), so subtracting 1152 leaves the code itself.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t flipped) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(flipped), "r"(0x64646464u), "n"(SEL));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r) : "r"(0x64806480u));
   return r;
 }
 

@@ -21,7 +21,7 @@ def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _lib.header_functions()
-    assert len(declared) == 14
+    assert len(declared) == 16
     nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     for name in declared:
@@ -108,6 +108,24 @@ def test_host_validation_codes(lib):
     assert admit(cap=64 * 16 + 1) == c["PKV_ERR_DIMS"]                # more slots than the tables
     assert admit(slot_pos=0) == c["PKV_ERR_NULL_POINTER"]
     assert admit(dims=_dims(B=0)) == c["PKV_OK"]
+    # INT8 pools
+    def q8_append(ks=0x30000, n=4):
+        return lib.pkv_kv_append_q8(P(0x10000), P(0x10000), P(ks), P(0x40000), P(0x10000), P(0x10000),
+                                    P(0x50000), n, ctypes.byref(_dims()), None, None)
+    assert q8_append(n=0) == c["PKV_OK"]
+    assert q8_append(n=-1) == c["PKV_ERR_DIMS"]
+    assert q8_append(ks=0) == c["PKV_ERR_NULL_POINTER"]
+    assert q8_append(ks=0x30004) == c["PKV_ERR_ALIGNMENT"]
+
+    def q8_decode(vs=0x40000, ws_bytes=16, dims=None):
+        return lib.pkv_paged_decode_attention_q8(P(0x10000), P(0x10000), P(0x10000), P(0x10000), P(0x30000),
+                                                 P(vs), P(0x10000), P(0x10000), ctypes.c_float(0.1), 0,
+                                                 P(0x20000), ws_bytes, ctypes.byref(dims or _dims()), None, None)
+    assert q8_decode(vs=0) == c["PKV_ERR_NULL_POINTER"]
+    assert q8_decode(vs=0x40008) == c["PKV_ERR_ALIGNMENT"]
+    assert q8_decode() == c["PKV_ERR_WORKSPACE"]                      # 16-byte workspace
+    assert q8_decode(dims=_dims(d=80)) == c["PKV_ERR_HEAD_DIM"]
+    assert q8_decode(dims=_dims(B=0)) == c["PKV_OK"]
     # sparse decode with no kept lists
     assert lib.pkv_sparse_decode_attention(P(0x10000), P(0x10000), P(0x10000), P(0x10000),
                                            P(0x10000), P(0x10000), None, None, 16,

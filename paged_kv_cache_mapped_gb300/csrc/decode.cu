@@ -261,7 +261,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // SCORES (dense only): also keep every attended key's base-2 logit and write the log-sum-exp of
 // rows written out directly, for the score step (decode_score_kernel).
 template <int D, bool SPARSE, bool SCORES, bool Q8>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+__global__ void __launch_bounds__(kDecodeWarps * 32, Q8 ? PKV_Q8_MIN_CTAS : 0)
 decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   static_assert(!(SPARSE && SCORES), "scores are emitted by the dense decode only");
   static_assert(!(Q8 && (SPARSE || SCORES)), "INT8 pools are read by the plain dense decode only");

@@ -75,10 +75,14 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #endif
 
 #ifndef PKV_RING_Q8_D128
-#define PKV_RING_Q8_D128 4  // INT8 K/V tile pairs in flight per worker warp at head_dim 128
+#define PKV_RING_Q8_D128 3  // INT8 K/V tile pairs in flight per worker warp at head_dim 128
 #endif
 #ifndef PKV_RING_Q8_D64
 #define PKV_RING_Q8_D64 4
+#endif
+
+#ifndef PKV_Q8_MIN_CTAS
+#define PKV_Q8_MIN_CTAS 0   // INT8 decode: resident CTAs per SM the register budget must allow (0: no bound)
 #endif
 
 #ifndef PKV_MIN_UNITS

@@ -23,6 +23,9 @@ Parity status of each function (what pins it; see ``tests/test_oracle_*.py``):
   kv_append_q8     -- pinned by a dict-of-slots model over quantize_rows
   paged_decode_q8  -- pinned by equality with paged_decode where code * scale is a bf16 value,
                       and by torch SDPA (fp64) on the dequantized contiguous K/V
+  prefill_scores   -- pinned by torch causal softmax (fp64), a segment's scores summing to G per
+                      window row, the q = 0 closed form, alpha = 1 against decode_scores, the
+                      given-lse property and block-permutation invariance
 """
 from __future__ import annotations
 
@@ -92,6 +95,8 @@ def _load():
                                                  i32, i32, i32]
             lib.oracle_compact.argtypes = [P, P, P, i64, i32, P, P, P, P, P, P, i32, i32, i32,
                                            i32, i64, i32]
+            lib.oracle_prefill_scores.argtypes = [P, P, i32, P, P, P, P, i32, i32, i32, i32, i64, i32,
+                                                  i32, f64, i64, P, i64]
             lib.oracle_quantize_rows.argtypes = [P, P, P, i64, i32]
             lib.oracle_kv_append_q8.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i64]
             lib.oracle_paged_decode_q8.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i64,
@@ -99,7 +104,7 @@ def _load():
             for name in ("oracle_kv_append", "oracle_paged_decode", "oracle_sparse_decode",
                          "oracle_select_topk", "oracle_compact", "oracle_decode_scores",
                          "oracle_rolling_admit", "oracle_quantize_rows", "oracle_kv_append_q8",
-                         "oracle_paged_decode_q8"):
+                         "oracle_paged_decode_q8", "oracle_prefill_scores"):
                 getattr(lib, name).restype = i32
             _lib = lib
     return _lib
@@ -324,3 +329,33 @@ def paged_decode_q8(q, k_codes, k_scales, v_codes, v_scales, block_tables, conte
                                           _ptr(lens), b, hq, hkv, d, nb, bt.shape[1], float(scale), int(window),
                                           None if r is None else _ptr(r), n), "paged_decode_q8")
     return out.reshape(b, hq, d) if rows is None else out
+
+
+def prefill_scores(q_win, k_cache, block_tables, context_lens, alpha, scale, lse=None, stride=None, segs=None):
+    """fp64 prefill-window score.  q_win [B, alpha, Hq, d] (bf16 bits): row r is position
+    L_b - alpha + r.  lse [B, Hq, alpha] given, or None to compute it.  Returns
+    (score_add [B, Hkv, stride] or [len(segs), stride], lse [B, Hq, alpha])."""
+    q = _arr(q_win, np.uint16)
+    kc = _arr(k_cache, np.uint16)
+    bt = _arr(block_tables, np.int32)
+    lens = _arr(context_lens, np.int32)
+    b, a, hq, d = q.shape
+    nb, hkv, bs, d2 = kc.shape
+    assert a == alpha and bs == 16 and d2 == d and bt.shape[0] == b
+    if stride is None:
+        stride = max(int(lens.max()) if lens.size else 0, 1)
+    given = lse is not None
+    lse_arr = np.array(lse, dtype=np.float64, copy=True) if given else np.zeros((b, hq, alpha), dtype=np.float64)
+    assert lse_arr.shape == (b, hq, alpha)
+    if segs is None:
+        s_arr, n = None, b * hkv
+    else:
+        s_arr = _arr(np.asarray(segs, dtype=np.int64), np.int64)
+        n = s_arr.shape[0]
+    score = np.zeros((n, stride), dtype=np.float64)
+    _check(_load().oracle_prefill_scores(_ptr(score), _ptr(lse_arr), int(given), _ptr(q), _ptr(kc), _ptr(bt),
+                                         _ptr(lens), b, hq, hkv, d, nb, bt.shape[1], int(alpha), float(scale),
+                                         int(stride), None if s_arr is None else _ptr(s_arr), n), "prefill_scores")
+    if segs is None:
+        score = score.reshape(b, hkv, stride)
+    return score, lse_arr

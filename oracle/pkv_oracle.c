@@ -489,6 +489,83 @@ int oracle_decode_scores(double* score_add, double* lse, const uint16_t* q,
   return status;
 }
 
+/*
+ * Prefill-side sparsification score ([novita] section "2. Attention modification": the
+ * PyramidKV-style score).  After a prompt of L_b tokens, the score of key i in kv head g is
+ * the sum of its softmax probabilities A[j][i] over the instruction window, the last alpha
+ * query positions j in [L_b - alpha, L_b), and over the G query heads sharing kv head g.
+ * Attention is causal: row j attends keys [0, j].  The page computes it from the forward
+ * pass's rowmax and l (their log-sum-exp lse_j): A[j][i] = exp(s_ji - lse_j).  With
+ * lse_given == 0 the oracle first computes lse_j itself (max + log of the sum of
+ * exponentials, the textbook stable form) and writes it out; otherwise it takes lse as given.
+ *   q_win [B][alpha][Hq][d]: the query of position L_b - alpha + r is row r (rows whose
+ *                           position is negative, L_b < alpha, are not used)
+ *   lse   [B][Hq][alpha]:   in (lse_given) or out; unused rows get -infinity
+ *   score_add [segments][stride]: each key's score (this call's addition), stride >= L_b.
+ */
+int oracle_prefill_scores(double* score_add, double* lse, int lse_given, const uint16_t* q_win,
+                          const uint16_t* k_cache, const int32_t* block_tables,
+                          const int32_t* context_lens, int batch, int num_q_heads, int num_kv_heads,
+                          int head_dim, int64_t num_blocks, int max_blocks_per_seq, int alpha,
+                          double scale, int64_t stride, const int64_t* seg_ids, int64_t n_segs) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || alpha <= 0) return ORC_ERR_ARG;
+  if (num_q_heads % num_kv_heads != 0 || stride < 0) return ORC_ERR_ARG;
+  int group = num_q_heads / num_kv_heads;
+  int64_t total = seg_ids ? n_segs : (int64_t)batch * num_kv_heads;
+  int status = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < total; ++r) {
+    int64_t seg = seg_ids ? seg_ids[r] : r;
+    int b = (int)(seg / num_kv_heads);
+    int g = (int)(seg % num_kv_heads);
+    double* score = score_add + r * stride;
+    for (int64_t t = 0; t < stride; ++t) score[t] = 0.0;
+    int st = ORC_OK;
+    int64_t len = (b >= 0 && b < batch) ? context_lens[b] : -1;
+    if (len < 0 || len > (int64_t)max_blocks_per_seq * ORC_BLOCK || len > stride) st = ORC_ERR_LEN;
+    int64_t* tokens = (int64_t*)malloc((size_t)(len > 0 ? len : 1) * sizeof(int64_t));
+    double* logits = (double*)malloc((size_t)(len > 0 ? len : 1) * sizeof(double));
+    if (st == ORC_OK && (!tokens || !logits)) st = ORC_ERR_MEM;
+    for (int64_t t = 0; st == ORC_OK && t < len; ++t) tokens[t] = t;
+    for (int hi = 0; st == ORC_OK && hi < group; ++hi) {
+      int h = g * group + hi;
+      for (int rw = 0; rw < alpha && st == ORC_OK; ++rw) {
+        int64_t j = len - alpha + rw; /* this window row's position */
+        double* lse_jh = lse + ((int64_t)b * num_q_heads + h) * alpha + rw;
+        if (j < 0) {
+          if (!lse_given) *lse_jh = -INFINITY;
+          continue;
+        }
+        /* causal: row j attends keys [0, j] */
+        st = row_logits(logits, q_win + (((int64_t)b * alpha + rw) * num_q_heads + h) * head_dim,
+                        k_cache, block_tables + (int64_t)b * max_blocks_per_seq, max_blocks_per_seq,
+                        num_blocks, num_kv_heads, head_dim, g, scale, tokens, j + 1);
+        if (st != ORC_OK) break;
+        double row_lse;
+        if (lse_given) {
+          row_lse = *lse_jh;
+        } else {
+          double m = logits[0];
+          for (int64_t i = 1; i <= j; ++i)
+            if (logits[i] > m) m = logits[i];
+          double l = 0.0;
+          for (int64_t i = 0; i <= j; ++i) l += exp(logits[i] - m);
+          row_lse = m + log(l);
+          *lse_jh = row_lse;
+        }
+        for (int64_t i = 0; i <= j; ++i) score[i] += exp(logits[i] - row_lse);
+      }
+    }
+    free(tokens);
+    free(logits);
+    if (st != ORC_OK) {
+#pragma omp critical
+      status = st;
+    }
+  }
+  return status;
+}
+
 /* Candidate ordering for the top-k: higher score first; equal scores, lower position first. */
 typedef struct {
   double score;

@@ -210,6 +210,32 @@ int pkv_paged_decode_attention_q8(void* out, const void* q, const void* k_codes,
                                   void* stream);
 
 /*
+ * pkv_prefill_window_scores -- the prefill-side sparsification score: after a prompt of L_b
+ * tokens, key i of kv head g scores the sum, over the last alpha prompt positions j (the
+ * instruction window, j >= i) and the G query heads of the group, of its causal softmax
+ * probability exp(scale * q_j . k_i - lse_j) ("How KV Sparsity Achieves 1.5x Acceleration for
+ * vLLM", section "2. Attention modification": the PyramidKV score computed from the forward
+ * pass's rowmax and l, with the loop over keys outermost).  The sums are ADDED into
+ * score_accum, which then feeds pkv_kv_select_topk.
+ *   score_accum  : [B, Hkv, score_stride] fp32, 4-byte aligned; keys >= score_stride get no score
+ *                  (PKV_DEV_BAD_CONTEXT_LEN is recorded).
+ *   lse          : [B, Hq, alpha] fp32 natural-log row log-sum-exps of the window rows.  With
+ *                  lse_given != 0 they are read (the prefill attention's rowmax + log l); with
+ *                  lse_given == 0 they are computed first (a pass over each row's causal keys)
+ *                  and written; rows of negative position (L_b < alpha) get -infinity.
+ *   q_win        : [B, alpha, Hq, d] bf16, 16-byte aligned; row r is the query of position
+ *                  L_b - alpha + r (rows of negative position are not read).
+ *   k_cache      : [NB, Hkv, 16, d] bf16 pool; block_tables [B, MB]; context_lens [B] = L_b.
+ *   alpha        : >= 1, alpha * G <= 16384.     scale : logit scale.
+ *   error_word   : optional; PKV_DEV_BAD_BLOCK_ID, _BAD_CONTEXT_LEN, _WAIT_TIMEOUT.
+ * Supported: d in {64, 128}; G = Hq / Hkv in 1..8.
+ */
+int pkv_prefill_window_scores(float* score_accum, int32_t score_stride, float* lse, int32_t lse_given,
+                              const void* q_win, const void* k_cache, const int32_t* block_tables,
+                              const int32_t* context_lens, int32_t alpha, float scale, const pkv_dims* dims,
+                              int32_t* error_word, void* stream);
+
+/*
  * pkv_paged_decode_attention_scores -- pkv_paged_decode_attention (with this step's append
  * when k_new and v_new are given, as pkv_paged_decode_attention_append) that also produces
  * the step's sparsification score: the scoring of "How KV Sparsity Achieves 1.5x

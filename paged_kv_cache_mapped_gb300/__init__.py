@@ -23,6 +23,7 @@ __all__ = [
     "paged_decode_attention_scores", "kv_rolling_admit",
     "kv_append_q8",
     "paged_decode_attention_q8",
+    "prefill_window_scores",
 ]
 
 BLOCK_SIZE = 16
@@ -208,6 +209,39 @@ def paged_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tab
         _ptr(context_lens), float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
         _ptr(error_word), _stream(stream, dev)))
     return out
+
+
+def prefill_window_scores(q_win, k_cache, block_tables, context_lens, scale, score_accum, *, lse=None,
+                          lse_given=False, error_word=None, stream=None):
+    """Add the prefill-window score of every prompt key into score_accum [B, Hkv, S] (fp32).
+    q_win [B, alpha, Hq, d] bf16 holds the queries of the last alpha prompt positions.  lse
+    [B, Hq, alpha] fp32: read when lse_given (the prefill attention's log-sum-exps), else
+    computed into it (allocated when None).  Returns lse."""
+    nb, hkv, d = _pool_dims(k_cache, k_cache)
+    dev = k_cache.device
+    _need(q_win, "q_win", torch.bfloat16, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(score_accum, "score_accum", torch.float32, 3, dev)
+    B, alpha, hq, dq = q_win.shape
+    if dq != d:
+        raise ValueError("q_win head_dim differs from the pool's")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B or score_accum.shape[:2] != (B, hkv):
+        raise ValueError("batch / kv heads of block_tables, context_lens or score_accum differ from q_win's")
+    if lse is None:
+        if lse_given:
+            raise ValueError("lse_given needs lse")
+        lse = torch.empty((B, hq, alpha), dtype=torch.float32, device=dev)
+    else:
+        _need(lse, "lse", torch.float32, 3, dev)
+        if lse.shape != (B, hq, alpha):
+            raise ValueError("lse must be [B, Hq, alpha]")
+    dims = _dims(B, hq, hkv, d, nb, block_tables.shape[1])
+    check("pkv_prefill_window_scores", load().pkv_prefill_window_scores(
+        _ptr(score_accum), score_accum.shape[2], _ptr(lse), int(bool(lse_given)), _ptr(q_win), _ptr(k_cache),
+        _ptr(block_tables), _ptr(context_lens), int(alpha), float(scale), ctypes.byref(dims), _ptr(error_word),
+        _stream(stream, dev)))
+    return lse
 
 
 def paged_decode_attention_append(q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,

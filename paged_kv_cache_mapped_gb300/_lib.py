@@ -67,6 +67,7 @@ def load():
         sig = {
             "pkv_kv_append": (I32, [P, P, P, P, P, I64, D, P, P]),
             "pkv_kv_append_q8": (I32, [P, P, P, P, P, P, P, I64, D, P, P]),
+            "pkv_prefill_window_scores": (I32, [P, I32, P, I32, P, P, P, P, I32, F32, D, P, P]),
             "pkv_decode_workspace_bytes": (SZ, [D]),
             "pkv_paged_decode_attention_q8": (I32, [P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, P, P]),
             "pkv_paged_decode_attention": (I32, [P, P, P, P, P, P, F32, I32, P, SZ, D, P, P]),

@@ -81,7 +81,8 @@ const DeviceInfo* device_info(int* status) {
       }
     }
     {
-      const cudaError_t e = kvops_device_setup();
+      cudaError_t e = kvops_device_setup();
+      if (e == cudaSuccess) e = prefill_device_setup();
       if (e != cudaSuccess) {
         cudaGetLastError();
         *status = PKV_ERR_CUDA_BASE + (int)e;
@@ -138,6 +139,22 @@ int encode_pool_map_q8(CUtensorMap* map, const void* base, long long rows, int h
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_ARGUMENT;
+}
+
+// The prefill window's queries [B*alpha, Hq, D] bf16 as a 3-D tensor read in boxes of 64
+// columns x G heads x R window rows (one query chunk: G*R columns of 128 bytes each).
+int encode_window_map(CUtensorMap* map, const void* base, long long rows, int num_q_heads, int head_dim, int group,
+                      int chunk_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return PKV_ERR_NO_DEVICE;
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_q_heads * head_dim * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)chunk_rows};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_ARGUMENT;
 }
@@ -395,6 +412,54 @@ int pkv_paged_decode_attention_q8(void* out, const void* q, const void* k_codes,
   return decode_common(out, q, k_codes, v_codes, block_tables, context_lens, nullptr, nullptr, 0, scale,
                        window, workspace, workspace_bytes, dims, error_word, stream, false, nullptr, nullptr,
                        nullptr, &q8);
+}
+
+int pkv_prefill_window_scores(float* score_accum, int32_t score_stride, float* lse, int32_t lse_given,
+                              const void* q_win, const void* k_cache, const int32_t* block_tables,
+                              const int32_t* context_lens, int32_t alpha, float scale, const pkv_dims* dims,
+                              int32_t* error_word, void* stream) {
+  int st = check_dims(dims, true);
+  if (st != PKV_OK) return st;
+  if (dims->batch > kMaxBatch) return PKV_ERR_DIMS;
+  const int group = dims->num_q_heads / dims->num_kv_heads;
+  if (group > kMaxGroup) return PKV_ERR_GQA;
+  if (alpha <= 0 || score_stride <= 0) return PKV_ERR_ARGUMENT;
+  if ((long long)alpha * group > kPrefillMaxColumns) return PKV_ERR_DIMS;
+  if (dims->batch == 0) return PKV_OK;
+  if (!score_accum || !lse || !q_win || !k_cache || !block_tables || !context_lens) return PKV_ERR_NULL_POINTER;
+  if (!aligned16(q_win) || !aligned16(k_cache) ||
+      ((reinterpret_cast<uintptr_t>(score_accum) | reinterpret_cast<uintptr_t>(lse)) & 3u))
+    return PKV_ERR_ALIGNMENT;
+  const long long pool_rows = (long long)dims->num_blocks * dims->num_kv_heads * PKV_BLOCK_SIZE;
+  if (pool_rows >= (1ll << 31) || (long long)dims->batch * alpha >= (1ll << 31) ||
+      (long long)dims->max_blocks_per_seq * PKV_BLOCK_SIZE >= (1ll << 30))
+    return PKV_ERR_DIMS;
+  if (!device_info(&st)) return st;
+  PrefillArgs a{};
+  const int chunk_rows = 64 / group;
+  st = encode_pool_map(&a.tmap_k, k_cache, pool_rows, dims->head_dim);
+  if (st == PKV_OK)
+    st = encode_window_map(&a.tmap_q, q_win, (long long)dims->batch * alpha, dims->num_q_heads, dims->head_dim,
+                           group, chunk_rows);
+  if (st != PKV_OK) return st;
+  a.q_win = static_cast<const __nv_bfloat16*>(q_win);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.lse = lse;
+  a.scores = score_accum;
+  a.err = error_word;
+  a.score_stride = score_stride;
+  a.B = dims->batch;
+  a.Hq = dims->num_q_heads;
+  a.Hkv = dims->num_kv_heads;
+  a.NB = dims->num_blocks;
+  a.MB = dims->max_blocks_per_seq;
+  a.alpha = alpha;
+  a.G = group;
+  a.R = chunk_rows;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.timeout_ns = kWaitTimeoutNs;
+  return cuda_status(launch_prefill(a, dims->head_dim, lse_given != 0, static_cast<cudaStream_t>(stream)));
 }
 
 int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, void* v_cache,

@@ -146,6 +146,29 @@ cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const 
                                int stride, const int32_t* lens, int B, int Hkv, int n_sink,
                                int n_recent, int k_top, int32_t* err, cudaStream_t stream);
 
+// Prefill-window score (prefill.cu).  The window's queries and the pool are read through
+// tensor maps; lse is [B, Hq, alpha] natural-log, scores [B, Hkv, score_stride].
+struct PrefillArgs {
+  CUtensorMap tmap_k;            // the K pool as [NB*Hkv*16, D] bf16, box 64 x 16, 128-byte swizzle
+  CUtensorMap tmap_q;            // q_win as [B*alpha, Hq, D] bf16, box 64 x G x R, 128-byte swizzle
+  const __nv_bfloat16* q_win;    // [B, alpha, Hq, D]: row r is the query of position L_b - alpha + r
+  const int32_t* block_tables;   // [B, MB]
+  const int32_t* context_lens;   // [B] prompt lengths
+  float* lse;                    // [B, Hq, alpha]
+  float* scores;                 // [B, Hkv, score_stride], added into
+  int32_t* err;
+  int score_stride;
+  int B, Hq, Hkv, NB, MB, alpha, G;
+  int R;                         // window rows per query chunk (G * R <= 64 columns)
+  float scale_log2;              // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+constexpr int kPrefillMaxColumns = 16384;  // alpha * G bound (the score kernel stages every lse)
+size_t prefill_score_smem_bytes(int head_dim, int alpha, int group);
+size_t prefill_lse_smem_bytes(int head_dim);
+cudaError_t prefill_device_setup();
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool lse_given, cudaStream_t stream);
+
 // Launches `kernel` with programmatic stream serialisation (it may start before the previous
 // kernel on the stream ends; every kernel of this library waits for it before touching
 // global memory).

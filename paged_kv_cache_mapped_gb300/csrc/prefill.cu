@@ -1,0 +1,466 @@
+// prefill.cu -- prefill-side sparsification score over the instruction window, for sm_103a.
+//
+// After a prompt of L tokens, the score of key i in kv head g is the sum, over the window rows
+// j in [L - alpha, L) (the instruction tokens) and the G query heads of the group, of the causal
+// softmax probability A[j][i] = exp(scale * q_j . k_i - lse_j), i <= j ("How KV Sparsity Achieves
+// 1.5x Acceleration for vLLM", section "2. Attention modification": the PyramidKV-style score,
+// computed from the forward pass's rowmax and l, whose log-sum-exp is lse_j).
+//
+// Two kernels, both on warp-level mma.m16n8k16 (bf16 inputs, exact products, fp32 sums):
+//  * prefill_score_kernel -- the page's k-outer loop order.  A CTA owns 128 keys of one
+//    (sequence, kv head) with their K fragments in registers and streams the window's query
+//    columns (column = window row x query head of the group) through a ring of TMA boxes; a key's
+//    sum stays in the registers of the lane that holds it, so no sum crosses warps or CTAs.
+//    Window rows that lie before the CTA's first key attend none of its keys and are not read
+//    (causality), and CTAs past the prompt exit at once.
+//  * prefill_lse_kernel -- only when the caller has no lse: the q-outer order.  A CTA owns 128
+//    query columns as register fragments and streams the sequence's K blocks up to its last
+//    attended key through a TMA ring, keeping a running max (moved lazily) and sum per column.
+// Every wait is bounded; bad block ids are skipped and recorded, never dereferenced.
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "pkv.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kScoreWarps = 4;
+constexpr int kScoreKeys = 32 * kScoreWarps;  // keys per score CTA: two 16-row m-tiles per warp
+constexpr int kScoreTiles = kScoreKeys / 16;  // pool blocks per score CTA
+constexpr int kQSlots = 2;                    // query chunks in flight per score CTA
+constexpr int kQBox = 64 * 128;               // a chunk's d-half box: up to 64 columns x 128 bytes
+constexpr int kQSlotBytes = 2 * kQBox;
+constexpr int kLseWarps = 8;
+constexpr int kLseCols = 16 * kLseWarps;      // query columns per lse CTA
+constexpr int kKSlots = 4;                    // K blocks in flight per lse CTA
+constexpr float kLseSlack = 8.0f;             // running max moves only when exceeded by this (base 2)
+constexpr float kLog2eF = 1.4426950408889634f;
+constexpr float kLn2F = 0.6931471805599453f;
+
+template <int D>
+__host__ __device__ constexpr int tile_bytes() {
+  return 16 * D * 2;
+}
+
+// Byte offset of row r, 16-byte chunk c of a bf16 tile written by TMA as boxes of 64 columns
+// (128 bytes) with the 128-byte swizzle (chunk XOR row % 8), box b at b * box_stride.
+__device__ __forceinline__ uint32_t swz(int r, int c, int box_stride) {
+  return (uint32_t)((c >> 3) * box_stride + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
+  return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
+
+// -------------------------------------------------------------------------- score kernel
+
+template <int D>
+__global__ void __launch_bounds__(kScoreWarps * 32) prefill_score_kernel(const __grid_constant__ PrefillArgs a) {
+  constexpr int KS = D / 16;
+  constexpr int TB = tile_bytes<D>();
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* ktiles = align1024(smem_raw);
+  unsigned char* qslots = ktiles + kScoreTiles * TB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qslots + kQSlots * kQSlotBytes);
+  uint64_t* bar_k = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = bars + 1 + kQSlots;
+  uint32_t* s_tile_ok = reinterpret_cast<uint32_t*>(bars + 1 + 2 * kQSlots);
+  float* lse2 = reinterpret_cast<float*>(s_tile_ok + 4);  // every window column's lse, base 2
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int key0 = blockIdx.x * kScoreKeys;
+  const int G = a.G, alpha = a.alpha;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_k, 1);
+    for (int s = 0; s < kQSlots; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], kScoreWarps);
+    }
+    fence_mbar_init();
+  }
+  grid_dependency_wait();  // the lse kernel (or the caller's producer) may still be running
+  grid_launch_dependents();
+
+  const int L = a.context_lens[b];
+  if (L < 0 || L > a.MB * 16) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) record_error(a.err, PKV_DEV_BAD_CONTEXT_LEN);
+    return;
+  }
+  if (key0 >= L) return;  // past the prompt
+  if (L > a.score_stride && threadIdx.x == 0 && blockIdx.x == 0 && g == 0) record_error(a.err, PKV_DEV_BAD_CONTEXT_LEN);
+  // window rows whose position L - alpha + r reaches this CTA's first key
+  const int first_row = max(max(0, alpha - L), key0 - (L - alpha));
+  const int n_chunks = (alpha - first_row + a.R - 1) / a.R;  // >= 1: position L - 1 >= key0
+  const int chunk_bytes = (D / 64) * G * a.R * 128;
+  const uint64_t pol_q = l2_policy_evict_last();  // every key block of the sequence reads the window
+
+  int q_issued = 0;  // thread 0: chunks issued so far
+  auto issue_q = [&](int i) {
+    const int slot = i % kQSlots;
+    ++q_issued;
+    mbar_arrive_expect_tx(&q_full[slot], (uint32_t)chunk_bytes);
+#pragma unroll
+    for (int bx = 0; bx < D / 64; ++bx)
+      tma_load_3d(qslots + slot * kQSlotBytes + bx * kQBox, &a.tmap_q, bx * 64, g * G, b * alpha + first_row + i * a.R,
+                  &q_full[slot], pol_q);
+  };
+
+  __syncthreads();  // barriers initialised
+  if (threadIdx.x == 0) {
+    const uint64_t pol_k = l2_policy_evict_first();
+    uint32_t ok = 0, bytes = 0;
+    int phys[kScoreTiles];
+#pragma unroll
+    for (int p = 0; p < kScoreTiles; ++p) {
+      const int u = key0 / 16 + p;
+      phys[p] = -1;
+      if (u * 16 < L) {
+        const int pb = a.block_tables[(size_t)b * a.MB + u];
+        if (pb >= 0 && pb < a.NB) {
+          phys[p] = pb;
+          ok |= 1u << p;
+          bytes += TB;
+        } else {
+          record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
+        }
+      }
+    }
+    *s_tile_ok = ok;
+    mbar_arrive_expect_tx(bar_k, bytes);
+#pragma unroll
+    for (int p = 0; p < kScoreTiles; ++p) {
+      if (!((ok >> p) & 1u)) continue;
+      const int y = (phys[p] * a.Hkv + g) * 16;  // host checks NB*Hkv*16 < 2^31
+#pragma unroll
+      for (int bx = 0; bx < D / 64; ++bx) tma_load_2d(ktiles + p * TB + bx * 2048, &a.tmap_k, bx * 64, y, bar_k, pol_k);
+    }
+    for (int i = 0; i < kQSlots && i < n_chunks; ++i) issue_q(i);
+  }
+  // stage every window column's lse in base 2 (column c = window row c / G, head g G + c % G)
+  for (int c = threadIdx.x; c < alpha * G; c += blockDim.x) {
+    const int r = c / G, hi = c - r * G;
+    lse2[c] = a.lse[((size_t)b * a.Hq + (size_t)g * G + hi) * alpha + r] * kLog2eF;
+  }
+  __syncthreads();
+
+  bool aborted = false;
+  if (!__all_sync(kFullMask, mbar_wait_bounded(bar_k, 0, a.timeout_ns))) {
+    if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+    aborted = true;
+  }
+  // this warp's keys: two m-tiles (pool blocks 2 warp, 2 warp + 1), rows gq and gq + 8 of each
+  const uint32_t tiles_ok = *s_tile_ok;
+  uint32_t af[2][KS][4];
+  int key[2][2];
+  bool kval[2][2];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const int p = 2 * warp + mt;
+    const uint32_t tb = smem_u32(ktiles + p * TB);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) ldsm_x4(tb + swz(lane & 15, 2 * ks + (lane >> 4), 2048), af[mt][ks]);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      key[mt][rr] = key0 + p * 16 + gq + 8 * rr;
+      kval[mt][rr] = !aborted && ((tiles_ok >> p) & 1u) && key[mt][rr] < L;
+    }
+  }
+  const int key_last = min(key0 + kScoreKeys, L) - 1;
+  const float sl2 = a.scale_log2;
+  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+
+  int i = 0;
+  for (; i < n_chunks && !aborted; ++i) {
+    const int slot = i % kQSlots;
+    const uint32_t parity = (uint32_t)(i / kQSlots) & 1u;
+    if (!__all_sync(kFullMask, mbar_wait_bounded(&q_full[slot], parity, a.timeout_ns))) {
+      if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+      aborted = true;
+      break;
+    }
+    const int rs = first_row + i * a.R;
+    const int ncols = min(a.R, alpha - rs) * G;
+    const int jbase = L - alpha + rs;           // position of the chunk's first row
+    const bool all_attended = key_last <= jbase;  // every key here precedes every row
+    const uint32_t qbase = smem_u32(qslots + slot * kQSlotBytes);
+    for (int n8 = 0; n8 < ncols; n8 += 8) {
+      float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kp = 0; kp < KS / 2; ++kp) {
+        uint32_t bq[4];
+        ldsm_x4(qbase + swz(n8 + (lane & 7), 4 * kp + (lane >> 3), kQBox), bq);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          mma_bf16_m16n8k16(c[mt], af[mt][2 * kp], bq[0], bq[1]);
+          mma_bf16_m16n8k16(c[mt], af[mt][2 * kp + 1], bq[2], bq[3]);
+        }
+      }
+      // this lane's columns: n8 + 2tq and n8 + 2tq + 1 of the chunk
+      const int cc0 = n8 + 2 * tq, cc1 = cc0 + 1;
+      const bool cv0 = cc0 < ncols, cv1 = cc1 < ncols;
+      const float l0 = cv0 ? lse2[rs * G + cc0] : 0.f;
+      const float l1 = cv1 ? lse2[rs * G + cc1] : 0.f;
+      const int j0 = jbase + cc0 / G, j1 = jbase + cc1 / G;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int k = key[mt][rr];
+          const bool a0 = kval[mt][rr] && cv0 && (all_attended || k <= j0);
+          const bool a1 = kval[mt][rr] && cv1 && (all_attended || k <= j1);
+          const float e0 = exp2f(c[mt][2 * rr] * sl2 - l0);
+          const float e1 = exp2f(c[mt][2 * rr + 1] * sl2 - l1);
+          acc[mt][rr] += (a0 ? e0 : 0.f) + (a1 ? e1 : 0.f);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q_empty[slot]);
+    if (threadIdx.x == 0 && i + kQSlots < n_chunks) {
+      if (!mbar_wait_bounded(&q_empty[slot], parity, a.timeout_ns)) {
+        record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+        aborted = true;
+      } else {
+        fence_proxy_async_smem();
+        issue_q(i + kQSlots);
+      }
+    }
+  }
+  if (threadIdx.x == 0) {  // let every copy this thread issued land before the CTA exits
+    for (int k = i; k < q_issued; ++k)
+      (void)mbar_wait_bounded(&q_full[k % kQSlots], (uint32_t)(k / kQSlots) & 1u, a.timeout_ns);
+    (void)mbar_wait_bounded(bar_k, 0, a.timeout_ns);
+  }
+  if (aborted) return;
+  // a key's sum is spread over the 4 lanes of its row group
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      float v = acc[mt][rr];
+      v += __shfl_xor_sync(kFullMask, v, 1);
+      v += __shfl_xor_sync(kFullMask, v, 2);
+      const int k = key[mt][rr];
+      if (tq == 0 && kval[mt][rr] && k < a.score_stride) {
+        float* dst = a.scores + ((size_t)b * a.Hkv + g) * a.score_stride + k;
+        *dst += v;
+      }
+    }
+}
+
+// ---------------------------------------------------------------------------- lse kernel
+
+template <int D>
+__global__ void __launch_bounds__(kLseWarps * 32) prefill_lse_kernel(const __grid_constant__ PrefillArgs a) {
+  constexpr int KS = D / 16;
+  constexpr int TB = tile_bytes<D>();
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* ktiles = align1024(smem_raw);
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(ktiles + kKSlots * TB);
+  uint64_t* k_empty = k_full + kKSlots;
+  uint32_t* s_ok = reinterpret_cast<uint32_t*>(k_empty + kKSlots);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int cbase = blockIdx.x * kLseCols;
+  const int G = a.G, alpha = a.alpha;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kKSlots; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], kLseWarps);
+    }
+    fence_mbar_init();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  const int L = a.context_lens[b];
+  if (L < 0 || L > a.MB * 16) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) record_error(a.err, PKV_DEV_BAD_CONTEXT_LEN);
+    return;
+  }
+  const int ncol = alpha * G;
+  const int c_lo = max(0, alpha - L) * G;  // columns of rows before position 0 have no keys
+  if (cbase >= ncol) return;
+  auto lse_at = [&](int c) -> float* {
+    return a.lse + ((size_t)b * a.Hq + (size_t)g * G + c % G) * alpha + c / G;
+  };
+  for (int c = cbase + (int)threadIdx.x; c < min(cbase + kLseCols, c_lo); c += blockDim.x) *lse_at(c) = -INFINITY;
+  if (cbase + kLseCols <= c_lo) return;
+  const int c_last = min(cbase + kLseCols, ncol) - 1;
+  const int nblk = (L - alpha + c_last / G) / 16 + 1;  // blocks up to the CTA's last attended key
+
+  int k_issued = 0;  // thread 0: blocks issued so far
+  auto issue_k = [&](int u) {
+    const int slot = u % kKSlots;
+    ++k_issued;
+    const int phys = a.block_tables[(size_t)b * a.MB + u];
+    if (phys >= 0 && phys < a.NB) {
+      s_ok[slot] = 1u;
+      mbar_arrive_expect_tx(&k_full[slot], TB);
+      const int y = (phys * a.Hkv + g) * 16;
+#pragma unroll
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_load_2d(ktiles + slot * TB + bx * 2048, &a.tmap_k, bx * 64, y, &k_full[slot], l2_policy_evict_last());
+    } else {
+      record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
+      s_ok[slot] = 0u;
+      mbar_arrive_expect_tx(&k_full[slot], 0);
+    }
+  };
+  __syncthreads();  // barriers initialised
+  if (threadIdx.x == 0)
+    for (int u = 0; u < kKSlots && u < nblk; ++u) issue_k(u);
+
+  // this warp's 16 columns as the A operand (rows gq and gq + 8), zero where invalid
+  const int col_a = cbase + warp * 16 + gq, col_b = col_a + 8;
+  const bool va = col_a >= c_lo && col_a < ncol, vb = col_b >= c_lo && col_b < ncol;
+  const __nv_bfloat16* qa = a.q_win + (((size_t)b * alpha + col_a / G) * a.Hq + (size_t)g * G + col_a % G) * D;
+  const __nv_bfloat16* qb = a.q_win + (((size_t)b * alpha + col_b / G) * a.Hq + (size_t)g * G + col_b % G) * D;
+  uint32_t aq[KS][4];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    aq[ks][0] = va ? ld_u32(qa + 16 * ks + 2 * tq) : 0u;
+    aq[ks][1] = vb ? ld_u32(qb + 16 * ks + 2 * tq) : 0u;
+    aq[ks][2] = va ? ld_u32(qa + 16 * ks + 8 + 2 * tq) : 0u;
+    aq[ks][3] = vb ? ld_u32(qb + 16 * ks + 8 + 2 * tq) : 0u;
+  }
+  const int ja = L - alpha + col_a / G, jb = L - alpha + col_b / G;  // the rows' positions
+  const float sl2 = a.scale_log2;
+  float ma = -INFINITY, la = 0.f, mb = -INFINITY, lb = 0.f;  // this lane's share of each row
+
+  bool aborted = false;
+  int u = 0;
+  for (; u < nblk; ++u) {
+    const int slot = u % kKSlots;
+    const uint32_t parity = (uint32_t)(u / kKSlots) & 1u;
+    if (!__all_sync(kFullMask, mbar_wait_bounded(&k_full[slot], parity, a.timeout_ns))) {
+      if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+      aborted = true;
+      break;
+    }
+    if (s_ok[slot]) {
+      const uint32_t tb = smem_u32(ktiles + slot * TB);
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kp = 0; kp < KS / 2; ++kp) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          uint32_t bk[4];
+          ldsm_x4(tb + swz(8 * n + (lane & 7), 4 * kp + (lane >> 3), 2048), bk);
+          mma_bf16_m16n8k16(s[n], aq[2 * kp], bk[0], bk[1]);
+          mma_bf16_m16n8k16(s[n], aq[2 * kp + 1], bk[2], bk[3]);
+        }
+      }
+      // s[n] = (row gq, key 8n + 2tq), (gq, +1), (gq + 8, 8n + 2tq), (gq + 8, +1) of this block
+      float xa[4], xb[4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = u * 16 + 8 * n + 2 * tq + e;  // causal: k <= j (also < L, as j < L)
+          xa[2 * n + e] = k <= ja ? s[n][e] * sl2 : -INFINITY;
+          xb[2 * n + e] = k <= jb ? s[n][2 + e] * sl2 : -INFINITY;
+        }
+      const float mxa = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
+      const float mxb = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
+      if (mxa > ma + kLseSlack) {
+        la *= exp2f(ma - mxa);
+        ma = mxa;
+      }
+      if (mxb > mb + kLseSlack) {
+        lb *= exp2f(mb - mxb);
+        mb = mxb;
+      }
+      if (ma != -INFINITY) la += exp2f(xa[0] - ma) + exp2f(xa[1] - ma) + exp2f(xa[2] - ma) + exp2f(xa[3] - ma);
+      if (mb != -INFINITY) lb += exp2f(xb[0] - mb) + exp2f(xb[1] - mb) + exp2f(xb[2] - mb) + exp2f(xb[3] - mb);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&k_empty[slot]);
+    if (threadIdx.x == 0 && u + kKSlots < nblk) {
+      if (!mbar_wait_bounded(&k_empty[slot], parity, a.timeout_ns)) {
+        record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+        aborted = true;
+      } else {
+        fence_proxy_async_smem();
+        issue_k(u + kKSlots);
+      }
+    }
+  }
+  if (threadIdx.x == 0) {  // let every copy this thread issued land before the CTA exits
+    for (int k = u; k < k_issued; ++k)
+      (void)mbar_wait_bounded(&k_full[k % kKSlots], (uint32_t)(k / kKSlots) & 1u, a.timeout_ns);
+  }
+  if (aborted) return;
+  // combine the 4 lanes of each row: (m, l) pairs under a common max
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    const float ma2 = __shfl_xor_sync(kFullMask, ma, o), la2 = __shfl_xor_sync(kFullMask, la, o);
+    const float mb2 = __shfl_xor_sync(kFullMask, mb, o), lb2 = __shfl_xor_sync(kFullMask, lb, o);
+    const float Ma = fmaxf(ma, ma2), Mb = fmaxf(mb, mb2);
+    la = (ma == -INFINITY ? 0.f : la * exp2f(ma - Ma)) + (ma2 == -INFINITY ? 0.f : la2 * exp2f(ma2 - Ma));
+    lb = (mb == -INFINITY ? 0.f : lb * exp2f(mb - Mb)) + (mb2 == -INFINITY ? 0.f : lb2 * exp2f(mb2 - Mb));
+    ma = Ma;
+    mb = Mb;
+  }
+  if (tq == 0) {
+    if (va) *lse_at(col_a) = la > 0.f ? (ma + log2f(la)) * kLn2F : -INFINITY;
+    if (vb) *lse_at(col_b) = lb > 0.f ? (mb + log2f(lb)) * kLn2F : -INFINITY;
+  }
+}
+
+}  // namespace
+
+size_t prefill_score_smem_bytes(int head_dim, int alpha, int group) {
+  const size_t tb = 16 * (size_t)head_dim * 2;
+  return 1024 + kScoreTiles * tb + kQSlots * (size_t)kQSlotBytes + sizeof(uint64_t) * (1 + 2 * kQSlots) + 16 +
+         sizeof(float) * (size_t)alpha * group;
+}
+
+size_t prefill_lse_smem_bytes(int head_dim) {
+  const size_t tb = 16 * (size_t)head_dim * 2;
+  return 1024 + kKSlots * tb + sizeof(uint64_t) * 2 * kKSlots + sizeof(uint32_t) * kKSlots;
+}
+
+cudaError_t prefill_device_setup() {
+  const int score_max = (int)prefill_score_smem_bytes(128, kPrefillMaxColumns, 1);
+  const void* score[] = {(const void*)prefill_score_kernel<128>, (const void*)prefill_score_kernel<64>};
+  for (const void* f : score) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, score_max);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool lse_given, cudaStream_t stream) {
+  PrefillArgs args = a;
+  void* params[] = {&args};
+  if (!lse_given) {
+    const dim3 grid((unsigned)((a.alpha * a.G + kLseCols - 1) / kLseCols), (unsigned)a.Hkv, (unsigned)a.B);
+    const void* f = head_dim == 128 ? (const void*)prefill_lse_kernel<128> : (const void*)prefill_lse_kernel<64>;
+    const cudaError_t e = launch_pdl(f, grid, dim3(kLseWarps * 32), prefill_lse_smem_bytes(head_dim), stream, params);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid((unsigned)((a.MB * 16 + kScoreKeys - 1) / kScoreKeys), (unsigned)a.Hkv, (unsigned)a.B);
+  const void* f = head_dim == 128 ? (const void*)prefill_score_kernel<128> : (const void*)prefill_score_kernel<64>;
+  return launch_pdl(f, grid, dim3(kScoreWarps * 32), prefill_score_smem_bytes(head_dim, a.alpha, a.G), stream,
+                    params);
+}
+
+}  // namespace pkv

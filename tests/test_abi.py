@@ -21,7 +21,7 @@ def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _lib.header_functions()
-    assert len(declared) == 16
+    assert len(declared) == 17
     nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     for name in declared:
@@ -126,6 +126,18 @@ def test_host_validation_codes(lib):
     assert q8_decode() == c["PKV_ERR_WORKSPACE"]                      # 16-byte workspace
     assert q8_decode(dims=_dims(d=80)) == c["PKV_ERR_HEAD_DIM"]
     assert q8_decode(dims=_dims(B=0)) == c["PKV_OK"]
+    # prefill-window score
+    def prefill(alpha=16, stride=64, lse=0x30000, qw=0x10000, dims=None):
+        return lib.pkv_prefill_window_scores(P(0x40000), stride, P(lse), 0, P(qw), P(0x10000), P(0x10000),
+                                             P(0x10000), alpha, ctypes.c_float(0.1), ctypes.byref(dims or _dims()),
+                                             None, None)
+    assert prefill(alpha=0) == c["PKV_ERR_ARGUMENT"]
+    assert prefill(stride=0) == c["PKV_ERR_ARGUMENT"]
+    assert prefill(alpha=4097) == c["PKV_ERR_DIMS"]                   # alpha * G above 16384
+    assert prefill(lse=0) == c["PKV_ERR_NULL_POINTER"]
+    assert prefill(qw=0x10008) == c["PKV_ERR_ALIGNMENT"]
+    assert prefill(dims=_dims(hq=32, hkv=2)) == c["PKV_ERR_GQA"]
+    assert prefill(dims=_dims(B=0)) == c["PKV_OK"]
     # sparse decode with no kept lists
     assert lib.pkv_sparse_decode_attention(P(0x10000), P(0x10000), P(0x10000), P(0x10000),
                                            P(0x10000), P(0x10000), None, None, 16,

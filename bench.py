@@ -47,6 +47,15 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    """Measured dense bf16 TFLOP/s (burst), for kernels timed alone."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
@@ -380,6 +389,8 @@ def run_secondary(pkv, W, dev, stream, args):
     torch.cuda.empty_cache()
     res["llama8b_decode_int8"] = _q8_row(pkv, W, dev, stream, args, hbm)
     torch.cuda.empty_cache()
+    res["sparse_layer_prefill_scores"] = _prefill_row(pkv, W, dev, stream, args)
+    torch.cuda.empty_cache()
     res["qwen1p5b_step"] = _qwen_step(pkv, W, dev, stream, args, hbm)
     torch.cuda.empty_cache()
     res.update(_sparse_step(pkv, W, dev, stream, args, hbm))
@@ -460,6 +471,42 @@ def _q8_row(pkv, W, dev, stream, args, hbm):
             "tokens_per_s": round(wl.batch / (ms_q8 * 1e-3), 1), "bytes": nbytes,
             "gbs": round(nbytes / (ms_q8 * 1e-3) / 1e9, 1), "frac": round(nbytes / (ms_q8 * 1e-3) / 1e9 / hbm, 4),
             "l2": "0.29 GB of INT8 K/V + scales per call (> L2)"}
+
+
+def _prefill_row(pkv, W, dev, stream, args, alpha=256):
+    """One sparse layer's prefill-window score: 16 prompts of 16384 tokens, 32/8 heads, d = 128,
+    a 256-token instruction window; with the forward pass's lse given (the score pass alone) and
+    with the lse computed first (two passes over the keys)."""
+    wl = W.WORKLOADS["sparse"]
+    c = W.make_layer(wl, device=dev, device_rng=True)
+    B, hq, hkv, d = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    g = torch.Generator(device=dev).manual_seed(51)
+    q_win = torch.randn((B, alpha, hq, d), generator=g, device=dev).to(torch.bfloat16)
+    acc = torch.zeros((B, hkv, c["max_blocks_per_seq"] * 16), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, hq, alpha), dtype=torch.float32, device=dev)
+    pkv.prefill_window_scores(q_win, c["k_cache"], c["block_tables"], c["context_lens"], wl.scale, acc, lse=lse,
+                              stream=stream)
+
+    def given():
+        pkv.prefill_window_scores(q_win, c["k_cache"], c["block_tables"], c["context_lens"], wl.scale, acc, lse=lse,
+                                  lse_given=True, stream=stream)
+
+    def computed():
+        pkv.prefill_window_scores(q_win, c["k_cache"], c["block_tables"], c["context_lens"], wl.scale, acc, lse=lse,
+                                  stream=stream)
+    ms_given = _time(given, args.warmup, 10, dev, stream)
+    ms_both = _time(computed, args.warmup, 10, dev, stream)
+    lens = c["context_lens"].cpu().to(torch.int64)
+    # attended (row, key) pairs: window row j sees keys [0, j]
+    pairs = sum(int(sum(int(L) - alpha + r + 1 for r in range(alpha) if int(L) - alpha + r >= 0)) for L in lens)
+    flop = 2 * d * pairs * hq  # q.k per attended (row, head, key); the score pass alone
+    peak, kind = _tensor_peak()
+    tf = flop / (ms_given * 1e-3) / 1e12
+    del c, q_win, acc, lse
+    return {"ms_lse_given": round(ms_given, 4), "ms_lse_computed": round(ms_both, 4), "tflops": round(tf, 1),
+            "frac": round(tf / peak, 4), "peak": peak, "peak_kind": kind, "bound": "tensor",
+            "exps_per_s": round(pairs * hq / (ms_given * 1e-3), 1),
+            "what": "16 prompts x 16384 tokens, 32/8 heads, d 128, window 256 (warp mma.sync bf16 + exp2)"}
 
 
 def _graph_time(calls, warmup, steps, dev, stream):

@@ -228,7 +228,7 @@ int pkv_paged_decode_attention_q8(void* out, const void* q, const void* k_codes,
  *   k_cache      : [NB, Hkv, 16, d] bf16 pool; block_tables [B, MB]; context_lens [B] = L_b.
  *   alpha        : >= 1, alpha * G <= 16384.     scale : logit scale.
  *   error_word   : optional; PKV_DEV_BAD_BLOCK_ID, _BAD_CONTEXT_LEN, _WAIT_TIMEOUT.
- * Supported: d in {64, 128}; G = Hq / Hkv in 1..8.
+ * Supported: d in {64, 128}; G = Hq / Hkv in 1..8; MB <= 32768 blocks.
  */
 int pkv_prefill_window_scores(float* score_accum, int32_t score_stride, float* lse, int32_t lse_given,
                               const void* q_win, const void* k_cache, const int32_t* block_tables,

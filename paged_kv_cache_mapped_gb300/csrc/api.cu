@@ -424,7 +424,8 @@ int pkv_prefill_window_scores(float* score_accum, int32_t score_stride, float* l
   const int group = dims->num_q_heads / dims->num_kv_heads;
   if (group > kMaxGroup) return PKV_ERR_GQA;
   if (alpha <= 0 || score_stride <= 0) return PKV_ERR_ARGUMENT;
-  if ((long long)alpha * group > kPrefillMaxColumns) return PKV_ERR_DIMS;
+  if ((long long)alpha * group > kPrefillMaxColumns || dims->max_blocks_per_seq > kPrefillMaxBlocks)
+    return PKV_ERR_DIMS;
   if (dims->batch == 0) return PKV_OK;
   if (!score_accum || !lse || !q_win || !k_cache || !block_tables || !context_lens) return PKV_ERR_NULL_POINTER;
   if (!aligned16(q_win) || !aligned16(k_cache) ||

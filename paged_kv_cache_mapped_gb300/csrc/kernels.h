@@ -164,8 +164,9 @@ struct PrefillArgs {
   unsigned long long timeout_ns;
 };
 constexpr int kPrefillMaxColumns = 16384;  // alpha * G bound (the score kernel stages every lse)
+constexpr int kPrefillMaxBlocks = 32768;   // block-table width bound (the lse kernel stages a row)
 size_t prefill_score_smem_bytes(int head_dim, int alpha, int group);
-size_t prefill_lse_smem_bytes(int head_dim);
+size_t prefill_lse_smem_bytes(int head_dim, int max_blocks);
 cudaError_t prefill_device_setup();
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool lse_given, cudaStream_t stream);
 

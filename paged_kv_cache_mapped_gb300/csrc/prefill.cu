@@ -26,15 +26,17 @@
 namespace pkv {
 namespace {
 
-constexpr int kScoreWarps = 4;
+constexpr int kScoreWarps = 8;
 constexpr int kScoreKeys = 32 * kScoreWarps;  // keys per score CTA: two 16-row m-tiles per warp
 constexpr int kScoreTiles = kScoreKeys / 16;  // pool blocks per score CTA
-constexpr int kQSlots = 2;                    // query chunks in flight per score CTA
 constexpr int kQBox = 64 * 128;               // a chunk's d-half box: up to 64 columns x 128 bytes
 constexpr int kQSlotBytes = 2 * kQBox;
+constexpr int kQOwnSlots = 2;                 // query slots of their own; once the K fragments are in
+constexpr int kQSlots = kQOwnSlots + kScoreTiles * 4096 / kQSlotBytes;  // registers, the K tiles' area holds more
 constexpr int kLseWarps = 8;
-constexpr int kLseCols = 16 * kLseWarps;      // query columns per lse CTA
-constexpr int kKSlots = 4;                    // K blocks in flight per lse CTA
+constexpr int kLseMT = 1;                     // 16-column m-tiles per lse warp (two: fewer CTAs and a spill, slower)
+constexpr int kLseCols = 16 * kLseMT * kLseWarps;  // query columns per lse CTA
+constexpr int kKSlots = 16;                   // K blocks in flight per lse CTA
 constexpr float kLseSlack = 8.0f;             // running max moves only when exceeded by this (base 2)
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
@@ -62,6 +64,14 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 
 __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
 
+// 2^x by the hardware approximation (the PTX ex2 instruction; relative error ~2^-22, results
+// below 2^-126 flushed to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // -------------------------------------------------------------------------- score kernel
 
 template <int D>
@@ -70,8 +80,12 @@ __global__ void __launch_bounds__(kScoreWarps * 32) prefill_score_kernel(const _
   constexpr int TB = tile_bytes<D>();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* ktiles = align1024(smem_raw);
-  unsigned char* qslots = ktiles + kScoreTiles * TB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qslots + kQSlots * kQSlotBytes);
+  unsigned char* qown = ktiles + kScoreTiles * 4096;  // the K area is sized for d = 128 (as 4 slots)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qown + kQOwnSlots * kQSlotBytes);
+  // query slot s: the own slots first, then the K tiles' area once the fragments are loaded
+  auto qslot = [&](int slot) -> unsigned char* {
+    return slot < kQOwnSlots ? qown + slot * kQSlotBytes : ktiles + (slot - kQOwnSlots) * kQSlotBytes;
+  };
   uint64_t* bar_k = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = bars + 1 + kQSlots;
@@ -115,7 +129,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) prefill_score_kernel(const _
     mbar_arrive_expect_tx(&q_full[slot], (uint32_t)chunk_bytes);
 #pragma unroll
     for (int bx = 0; bx < D / 64; ++bx)
-      tma_load_3d(qslots + slot * kQSlotBytes + bx * kQBox, &a.tmap_q, bx * 64, g * G, b * alpha + first_row + i * a.R,
+      tma_load_3d(qslot(slot) + bx * kQBox, &a.tmap_q, bx * 64, g * G, b * alpha + first_row + i * a.R,
                   &q_full[slot], pol_q);
   };
 
@@ -148,7 +162,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) prefill_score_kernel(const _
 #pragma unroll
       for (int bx = 0; bx < D / 64; ++bx) tma_load_2d(ktiles + p * TB + bx * 2048, &a.tmap_k, bx * 64, y, bar_k, pol_k);
     }
-    for (int i = 0; i < kQSlots && i < n_chunks; ++i) issue_q(i);
+    for (int i = 0; i < kQOwnSlots && i < n_chunks; ++i) issue_q(i);
   }
   // stage every window column's lse in base 2 (column c = window row c / G, head g G + c % G)
   for (int c = threadIdx.x; c < alpha * G; c += blockDim.x) {
@@ -178,7 +192,24 @@ __global__ void __launch_bounds__(kScoreWarps * 32) prefill_score_kernel(const _
       key[mt][rr] = key0 + p * 16 + gq + 8 * rr;
       kval[mt][rr] = !aborted && ((tiles_ok >> p) & 1u) && key[mt][rr] < L;
     }
+    // rows of invalid keys (past the prompt, a skipped block) become zeros, so their logits are
+    // finite and a 0 factor removes them: af[.][.][0], [2] hold row gq, [1], [3] row gq + 8
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (!kval[mt][0]) af[mt][ks][0] = af[mt][ks][2] = 0u;
+      if (!kval[mt][1]) af[mt][ks][1] = af[mt][ks][3] = 0u;
+    }
   }
+  float kf[2][2];  // 1 for a valid key, 0 otherwise
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) kf[mt][rr] = kval[mt][rr] ? 1.f : 0.f;
+  // every warp has its fragments: the K tiles' area now takes query chunks
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0 && !aborted)
+    for (int i = kQOwnSlots; i < kQSlots && i < n_chunks; ++i) issue_q(i);
   const int key_last = min(key0 + kScoreKeys, L) - 1;
   const float sl2 = a.scale_log2;
   float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
@@ -196,7 +227,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) prefill_score_kernel(const _
     const int ncols = min(a.R, alpha - rs) * G;
     const int jbase = L - alpha + rs;           // position of the chunk's first row
     const bool all_attended = key_last <= jbase;  // every key here precedes every row
-    const uint32_t qbase = smem_u32(qslots + slot * kQSlotBytes);
+    const uint32_t qbase = smem_u32(qslot(slot));
     for (int n8 = 0; n8 < ncols; n8 += 8) {
       float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -211,21 +242,32 @@ __global__ void __launch_bounds__(kScoreWarps * 32) prefill_score_kernel(const _
       }
       // this lane's columns: n8 + 2tq and n8 + 2tq + 1 of the chunk
       const int cc0 = n8 + 2 * tq, cc1 = cc0 + 1;
-      const bool cv0 = cc0 < ncols, cv1 = cc1 < ncols;
-      const float l0 = cv0 ? lse2[rs * G + cc0] : 0.f;
-      const float l1 = cv1 ? lse2[rs * G + cc1] : 0.f;
-      const int j0 = jbase + cc0 / G, j1 = jbase + cc1 / G;
+      if (all_attended && n8 + 8 <= ncols) {
+        // every key of the CTA precedes every row of the chunk: no causal or column masks
+        const float l0 = lse2[rs * G + cc0], l1 = lse2[rs * G + cc1];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int k = key[mt][rr];
-          const bool a0 = kval[mt][rr] && cv0 && (all_attended || k <= j0);
-          const bool a1 = kval[mt][rr] && cv1 && (all_attended || k <= j1);
-          const float e0 = exp2f(c[mt][2 * rr] * sl2 - l0);
-          const float e1 = exp2f(c[mt][2 * rr + 1] * sl2 - l1);
-          acc[mt][rr] += (a0 ? e0 : 0.f) + (a1 ? e1 : 0.f);
-        }
+          for (int rr = 0; rr < 2; ++rr) {
+            const float e = ex2(fmaf(c[mt][2 * rr], sl2, -l0)) + ex2(fmaf(c[mt][2 * rr + 1], sl2, -l1));
+            acc[mt][rr] = fmaf(kf[mt][rr], e, acc[mt][rr]);
+          }
+      } else {
+        const bool cv0 = cc0 < ncols, cv1 = cc1 < ncols;
+        const float l0 = cv0 ? lse2[rs * G + cc0] : 0.f;
+        const float l1 = cv1 ? lse2[rs * G + cc1] : 0.f;
+        const int j0 = jbase + cc0 / G, j1 = jbase + cc1 / G;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int k = key[mt][rr];
+            const bool a0 = kval[mt][rr] && cv0 && k <= j0;
+            const bool a1 = kval[mt][rr] && cv1 && k <= j1;
+            const float e0 = ex2(fmaf(c[mt][2 * rr], sl2, -l0));
+            const float e1 = ex2(fmaf(c[mt][2 * rr + 1], sl2, -l1));
+            acc[mt][rr] += (a0 ? e0 : 0.f) + (a1 ? e1 : 0.f);
+          }
       }
     }
     __syncwarp();
@@ -273,6 +315,7 @@ __global__ void __launch_bounds__(kLseWarps * 32) prefill_lse_kernel(const __gri
   uint64_t* k_full = reinterpret_cast<uint64_t*>(ktiles + kKSlots * TB);
   uint64_t* k_empty = k_full + kKSlots;
   uint32_t* s_ok = reinterpret_cast<uint32_t*>(k_empty + kKSlots);
+  int32_t* s_bt = reinterpret_cast<int32_t*>(s_ok + kKSlots);  // the sequence's block ids, staged once
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
@@ -310,7 +353,7 @@ __global__ void __launch_bounds__(kLseWarps * 32) prefill_lse_kernel(const __gri
   auto issue_k = [&](int u) {
     const int slot = u % kKSlots;
     ++k_issued;
-    const int phys = a.block_tables[(size_t)b * a.MB + u];
+    const int phys = s_bt[u];
     if (phys >= 0 && phys < a.NB) {
       s_ok[slot] = 1u;
       mbar_arrive_expect_tx(&k_full[slot], TB);
@@ -324,26 +367,42 @@ __global__ void __launch_bounds__(kLseWarps * 32) prefill_lse_kernel(const __gri
       mbar_arrive_expect_tx(&k_full[slot], 0);
     }
   };
-  __syncthreads();  // barriers initialised
+  for (int u = threadIdx.x; u < nblk; u += blockDim.x) s_bt[u] = a.block_tables[(size_t)b * a.MB + u];
+  __syncthreads();  // barriers initialised, block ids staged
   if (threadIdx.x == 0)
     for (int u = 0; u < kKSlots && u < nblk; ++u) issue_k(u);
 
-  // this warp's 16 columns as the A operand (rows gq and gq + 8), zero where invalid
-  const int col_a = cbase + warp * 16 + gq, col_b = col_a + 8;
-  const bool va = col_a >= c_lo && col_a < ncol, vb = col_b >= c_lo && col_b < ncol;
-  const __nv_bfloat16* qa = a.q_win + (((size_t)b * alpha + col_a / G) * a.Hq + (size_t)g * G + col_a % G) * D;
-  const __nv_bfloat16* qb = a.q_win + (((size_t)b * alpha + col_b / G) * a.Hq + (size_t)g * G + col_b % G) * D;
-  uint32_t aq[KS][4];
+  // this warp's 16 * kLseMT columns as A operands: m-tile mt, fragment row gq + 8 rr is column
+  // cbase + warp * 16 kLseMT + 16 mt + gq + 8 rr; invalid columns are zeros
+  int col[kLseMT][2], jpos[kLseMT][2];
+  bool cval[kLseMT][2];
+  uint32_t aq[kLseMT][KS][4];
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    aq[ks][0] = va ? ld_u32(qa + 16 * ks + 2 * tq) : 0u;
-    aq[ks][1] = vb ? ld_u32(qb + 16 * ks + 2 * tq) : 0u;
-    aq[ks][2] = va ? ld_u32(qa + 16 * ks + 8 + 2 * tq) : 0u;
-    aq[ks][3] = vb ? ld_u32(qb + 16 * ks + 8 + 2 * tq) : 0u;
-  }
-  const int ja = L - alpha + col_a / G, jb = L - alpha + col_b / G;  // the rows' positions
+  for (int mt = 0; mt < kLseMT; ++mt)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int c = cbase + warp * 16 * kLseMT + 16 * mt + gq + 8 * rr;
+      col[mt][rr] = c;
+      cval[mt][rr] = c >= c_lo && c < ncol;
+      jpos[mt][rr] = L - alpha + c / G;  // the row's position
+      const __nv_bfloat16* qr = a.q_win + (((size_t)b * alpha + c / G) * a.Hq + (size_t)g * G + c % G) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        aq[mt][ks][rr] = cval[mt][rr] ? ld_u32(qr + 16 * ks + 2 * tq) : 0u;
+        aq[mt][ks][2 + rr] = cval[mt][rr] ? ld_u32(qr + 16 * ks + 8 + 2 * tq) : 0u;
+      }
+    }
+  // the smallest position among the warp's columns (invalid columns count as the window start)
+  const int j_warp = L - alpha + max(cbase + warp * 16 * kLseMT, c_lo) / G;
   const float sl2 = a.scale_log2;
-  float ma = -INFINITY, la = 0.f, mb = -INFINITY, lb = 0.f;  // this lane's share of each row
+  float m[kLseMT][2], l[kLseMT][2];  // this lane's share of each row: running max (base 2), sum
+#pragma unroll
+  for (int mt = 0; mt < kLseMT; ++mt)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      m[mt][rr] = -INFINITY;
+      l[mt][rr] = 0.f;
+    }
 
   bool aborted = false;
   int u = 0;
@@ -357,39 +416,46 @@ __global__ void __launch_bounds__(kLseWarps * 32) prefill_lse_kernel(const __gri
     }
     if (s_ok[slot]) {
       const uint32_t tb = smem_u32(ktiles + slot * TB);
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float sc[kLseMT][2][4] = {};
 #pragma unroll
       for (int kp = 0; kp < KS / 2; ++kp) {
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
           uint32_t bk[4];
           ldsm_x4(tb + swz(8 * n + (lane & 7), 4 * kp + (lane >> 3), 2048), bk);
-          mma_bf16_m16n8k16(s[n], aq[2 * kp], bk[0], bk[1]);
-          mma_bf16_m16n8k16(s[n], aq[2 * kp + 1], bk[2], bk[3]);
+#pragma unroll
+          for (int mt = 0; mt < kLseMT; ++mt) {
+            mma_bf16_m16n8k16(sc[mt][n], aq[mt][2 * kp], bk[0], bk[1]);
+            mma_bf16_m16n8k16(sc[mt][n], aq[mt][2 * kp + 1], bk[2], bk[3]);
+          }
         }
       }
-      // s[n] = (row gq, key 8n + 2tq), (gq, +1), (gq + 8, 8n + 2tq), (gq + 8, +1) of this block
-      float xa[4], xb[4];
+      // sc[mt][n] = (row gq, key 8n + 2tq), (gq, +1), (gq + 8, 8n + 2tq), (gq + 8, +1) of this block
+      const bool unmasked = u * 16 + 15 <= j_warp;  // the block precedes every row of this warp
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+      for (int mt = 0; mt < kLseMT; ++mt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int k = u * 16 + 8 * n + 2 * tq + e;  // causal: k <= j (also < L, as j < L)
-          xa[2 * n + e] = k <= ja ? s[n][e] * sl2 : -INFINITY;
-          xb[2 * n + e] = k <= jb ? s[n][2 + e] * sl2 : -INFINITY;
+        for (int rr = 0; rr < 2; ++rr) {
+          float x[4];
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int k = u * 16 + 8 * n + 2 * tq + e;  // causal: k <= j (also < L, as j < L)
+              x[2 * n + e] = (unmasked || k <= jpos[mt][rr]) ? sc[mt][n][2 * rr + e] : -INFINITY;
+            }
+          // unscaled logits: sl2 > 0 keeps the order, so the max scales after
+          const float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])) * sl2;
+          float& mr = m[mt][rr];
+          float& lr = l[mt][rr];
+          if (mx > mr + kLseSlack) {
+            lr *= ex2(mr - mx);
+            mr = mx;
+          }
+          if (mr != -INFINITY)
+            lr += ex2(fmaf(x[0], sl2, -mr)) + ex2(fmaf(x[1], sl2, -mr)) + ex2(fmaf(x[2], sl2, -mr)) +
+                  ex2(fmaf(x[3], sl2, -mr));
         }
-      const float mxa = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
-      const float mxb = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
-      if (mxa > ma + kLseSlack) {
-        la *= exp2f(ma - mxa);
-        ma = mxa;
-      }
-      if (mxb > mb + kLseSlack) {
-        lb *= exp2f(mb - mxb);
-        mb = mxb;
-      }
-      if (ma != -INFINITY) la += exp2f(xa[0] - ma) + exp2f(xa[1] - ma) + exp2f(xa[2] - ma) + exp2f(xa[3] - ma);
-      if (mb != -INFINITY) lb += exp2f(xb[0] - mb) + exp2f(xb[1] - mb) + exp2f(xb[2] - mb) + exp2f(xb[3] - mb);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&k_empty[slot]);
@@ -410,32 +476,33 @@ __global__ void __launch_bounds__(kLseWarps * 32) prefill_lse_kernel(const __gri
   if (aborted) return;
   // combine the 4 lanes of each row: (m, l) pairs under a common max
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    const float ma2 = __shfl_xor_sync(kFullMask, ma, o), la2 = __shfl_xor_sync(kFullMask, la, o);
-    const float mb2 = __shfl_xor_sync(kFullMask, mb, o), lb2 = __shfl_xor_sync(kFullMask, lb, o);
-    const float Ma = fmaxf(ma, ma2), Mb = fmaxf(mb, mb2);
-    la = (ma == -INFINITY ? 0.f : la * exp2f(ma - Ma)) + (ma2 == -INFINITY ? 0.f : la2 * exp2f(ma2 - Ma));
-    lb = (mb == -INFINITY ? 0.f : lb * exp2f(mb - Mb)) + (mb2 == -INFINITY ? 0.f : lb2 * exp2f(mb2 - Mb));
-    ma = Ma;
-    mb = Mb;
-  }
-  if (tq == 0) {
-    if (va) *lse_at(col_a) = la > 0.f ? (ma + log2f(la)) * kLn2F : -INFINITY;
-    if (vb) *lse_at(col_b) = lb > 0.f ? (mb + log2f(lb)) * kLn2F : -INFINITY;
-  }
+  for (int mt = 0; mt < kLseMT; ++mt)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      float mr = m[mt][rr], lr = l[mt][rr];
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        const float m2 = __shfl_xor_sync(kFullMask, mr, o), l2 = __shfl_xor_sync(kFullMask, lr, o);
+        const float M = fmaxf(mr, m2);
+        lr = (mr == -INFINITY ? 0.f : lr * exp2f(mr - M)) + (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - M));
+        mr = M;
+      }
+      if (tq == 0 && cval[mt][rr]) *lse_at(col[mt][rr]) = lr > 0.f ? (mr + log2f(lr)) * kLn2F : -INFINITY;
+    }
 }
 
 }  // namespace
 
 size_t prefill_score_smem_bytes(int head_dim, int alpha, int group) {
-  const size_t tb = 16 * (size_t)head_dim * 2;
-  return 1024 + kScoreTiles * tb + kQSlots * (size_t)kQSlotBytes + sizeof(uint64_t) * (1 + 2 * kQSlots) + 16 +
+  (void)head_dim;  // the K tiles' area is sized for d = 128 either way (it doubles as query slots)
+  return 1024 + kScoreTiles * 4096 + kQOwnSlots * (size_t)kQSlotBytes + sizeof(uint64_t) * (1 + 2 * kQSlots) + 16 +
          sizeof(float) * (size_t)alpha * group;
 }
 
-size_t prefill_lse_smem_bytes(int head_dim) {
+size_t prefill_lse_smem_bytes(int head_dim, int max_blocks) {
   const size_t tb = 16 * (size_t)head_dim * 2;
-  return 1024 + kKSlots * tb + sizeof(uint64_t) * 2 * kKSlots + sizeof(uint32_t) * kKSlots;
+  return 1024 + kKSlots * tb + sizeof(uint64_t) * 2 * kKSlots + sizeof(uint32_t) * kKSlots +
+         sizeof(int32_t) * (size_t)max_blocks;
 }
 
 cudaError_t prefill_device_setup() {
@@ -443,6 +510,13 @@ cudaError_t prefill_device_setup() {
   const void* score[] = {(const void*)prefill_score_kernel<128>, (const void*)prefill_score_kernel<64>};
   for (const void* f : score) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, score_max);
+    if (e != cudaSuccess) return e;
+  }
+  const void* lse[] = {(const void*)prefill_lse_kernel<128>, (const void*)prefill_lse_kernel<64>};
+  for (const void* f : lse) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)prefill_lse_smem_bytes(128, kPrefillMaxBlocks));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -454,7 +528,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool lse_given, c
   if (!lse_given) {
     const dim3 grid((unsigned)((a.alpha * a.G + kLseCols - 1) / kLseCols), (unsigned)a.Hkv, (unsigned)a.B);
     const void* f = head_dim == 128 ? (const void*)prefill_lse_kernel<128> : (const void*)prefill_lse_kernel<64>;
-    const cudaError_t e = launch_pdl(f, grid, dim3(kLseWarps * 32), prefill_lse_smem_bytes(head_dim), stream, params);
+    const cudaError_t e =
+        launch_pdl(f, grid, dim3(kLseWarps * 32), prefill_lse_smem_bytes(head_dim, a.MB), stream, params);
     if (e != cudaSuccess) return e;
   }
   const dim3 grid((unsigned)((a.MB * 16 + kScoreKeys - 1) / kScoreKeys), (unsigned)a.Hkv, (unsigned)a.B);

@@ -506,7 +506,7 @@ def _prefill_row(pkv, W, dev, stream, args, alpha=256):
     return {"ms_lse_given": round(ms_given, 4), "ms_lse_computed": round(ms_both, 4), "tflops": round(tf, 1),
             "frac": round(tf / peak, 4), "peak": peak, "peak_kind": kind, "bound": "tensor",
             "exps_per_s": round(pairs * hq / (ms_given * 1e-3), 1),
-            "what": "16 prompts x 16384 tokens, 32/8 heads, d 128, window 256 (warp mma.sync bf16 + exp2)"}
+            "what": "16 prompts x 16384 tokens, 32/8 heads, d 128, window 256 (tcgen05 UMMA bf16 into TMEM + ex2)"}
 
 
 def _graph_time(calls, warmup, steps, dev, stream):

@@ -163,6 +163,9 @@ struct PrefillArgs {
   float scale_log2;              // scale * log2(e)
   unsigned long long timeout_ns;
 };
+#ifndef PKV_PREFILL_TCGEN05
+#define PKV_PREFILL_TCGEN05 1  // prefill score on tcgen05 where supported (d = 128, G a power of two)
+#endif
 constexpr int kPrefillMaxColumns = 16384;  // alpha * G bound (the score kernel stages every lse)
 constexpr int kPrefillMaxBlocks = 32768;   // block-table width bound (the lse kernel stages a row)
 size_t prefill_score_smem_bytes(int head_dim, int alpha, int group);

@@ -304,6 +304,229 @@ __global__ void __launch_bounds__(kScoreWarps * 32) prefill_score_kernel(const _
     }
 }
 
+// ------------------------------------------------------------ score kernel on tcgen05 (UMMA)
+//
+// The same k-outer score, with the contraction on the 5th-generation tensor cores: a CTA owns
+// 128 keys of one (sequence, kv head); their K tile is the A operand (128 keys x 128 d, K-major,
+// 128-byte swizzle, as TMA writes it), each chunk of 128 window columns the B operand, and
+// S^T = K Q^T (128 x 128 fp32) accumulates in tensor memory over 8 k-steps of 16.  Roles: warp 4
+// issues the TMA copies, one thread of warp 5 issues the MMAs, warps 0-3 read the accumulator
+// (warp w owns TMEM lanes 32w..32w+31, one key per thread) and add each probability to the
+// thread's key sum.  Two accumulators (256 TMEM columns) let the MMAs of chunk i + 1 run while
+// chunk i is read.  d = 128 and G a power of two (so a chunk is whole window rows).
+constexpr int kTcKeys = 128;
+constexpr int kTcCols = 128;                   // window columns per chunk (the MMA's N)
+constexpr int kTcHalf = 128 * 128;             // one d-half of a 128-row operand: 128 rows x 128 B
+constexpr int kTcQSlots = 2;
+constexpr int kTcThreads = 192;
+constexpr uint32_t kTcTmemCols = 2 * kTcCols;
+
+__global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __grid_constant__ PrefillArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sa = align1024(smem_raw);              // A: 2 d-halves x 16 KiB
+  unsigned char* sq = sa + 2 * kTcHalf;                 // B slots: kTcQSlots x 2 d-halves x 16 KiB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sq + kTcQSlots * 2 * kTcHalf);
+  uint64_t* k_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + kTcQSlots;
+  uint64_t* acc_full = q_empty + kTcQSlots;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint32_t* s_tiles_ok = s_tmem + 1;
+  // window columns from the CTA's first row, base 2; 16-byte aligned for the vector reads
+  float* lse2 = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s_tmem + 4) + 15) & ~uintptr_t(15));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int key0 = blockIdx.x * kTcKeys;
+  const int G = a.G, alpha = a.alpha;
+  const int rows_per_chunk = kTcCols / G;
+
+  if (threadIdx.x == 0) {
+    mbar_init(k_full, 1);
+    for (int s = 0; s < kTcQSlots; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 4);
+    }
+    fence_mbar_init();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  const int L = a.context_lens[b];
+  if (L < 0 || L > a.MB * 16) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) record_error(a.err, PKV_DEV_BAD_CONTEXT_LEN);
+    return;
+  }
+  if (key0 >= L) return;
+  if (L > a.score_stride && threadIdx.x == 0 && blockIdx.x == 0 && g == 0) record_error(a.err, PKV_DEV_BAD_CONTEXT_LEN);
+  const int first_row = max(max(0, alpha - L), key0 - (L - alpha));
+  const int n_chunks = (alpha - first_row + rows_per_chunk - 1) / rows_per_chunk;
+
+  if (warp == 0) {  // tensor memory for the two accumulators
+    tmem_alloc(s_tmem, kTcTmemCols);
+    tmem_relinquish();
+  }
+  // lse of the columns from the first row on, chunk-major (chunk i's column c at i * 128 + c)
+  for (int k = threadIdx.x; k < (alpha - first_row) * G; k += blockDim.x) {
+    const int c = first_row * G + k;
+    const int r = c / G, hi = c - r * G;
+    lse2[k] = a.lse[((size_t)b * a.Hq + (size_t)g * G + hi) * alpha + r] * kLog2eF;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  bool aborted = false;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_k = l2_policy_evict_first(), pol_q = l2_policy_evict_last();
+      uint32_t ok = 0, bytes = 0;
+      int phys[8];
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        const int u = key0 / 16 + p;
+        phys[p] = -1;
+        if (u * 16 < L) {
+          const int pb = a.block_tables[(size_t)b * a.MB + u];
+          if (pb >= 0 && pb < a.NB) {
+            phys[p] = pb;
+            ok |= 1u << p;
+            bytes += 2 * 2048;
+          } else {
+            record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
+          }
+        }
+      }
+      *s_tiles_ok = ok;
+      mbar_arrive_expect_tx(k_full, bytes);
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        if (!((ok >> p) & 1u)) continue;
+        const int y = (phys[p] * a.Hkv + g) * 16;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) tma_load_2d(sa + h * kTcHalf + p * 2048, &a.tmap_k, h * 64, y, k_full, pol_k);
+      }
+      int issued = 0;
+      for (int i = 0; i < n_chunks; ++i) {
+        const int s = i % kTcQSlots;
+        if (i >= kTcQSlots && !mbar_wait_bounded(&q_empty[s], (uint32_t)((i / kTcQSlots) - 1) & 1u, a.timeout_ns)) {
+          record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        const int rs = first_row + i * rows_per_chunk;
+        mbar_arrive_expect_tx(&q_full[s], 2 * kTcHalf);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_load_3d(sq + (s * 2 + h) * kTcHalf + j * 8192, &a.tmap_q, h * 64, g * G,
+                        b * alpha + rs + j * (64 / G), &q_full[s], pol_q);
+        ++issued;
+      }
+      // every copy lands before the CTA may exit
+      (void)mbar_wait_bounded(k_full, 0, a.timeout_ns);
+      for (int i = max(0, issued - kTcQSlots); i < issued; ++i)
+        (void)mbar_wait_bounded(&q_full[i % kTcQSlots], (uint32_t)(i / kTcQSlots) & 1u, a.timeout_ns);
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(128, kTcCols);
+      int done = 0;
+      if (mbar_wait_bounded(k_full, 0, a.timeout_ns)) {
+        const uint32_t a0 = smem_u32(sa);
+        for (int i = 0; i < n_chunks; ++i) {
+          const int s = i % kTcQSlots, acc = i & 1;
+          if (!mbar_wait_bounded(&q_full[s], (uint32_t)(i / kTcQSlots) & 1u, a.timeout_ns)) break;
+          if (i >= 2 && !mbar_wait_bounded(&acc_empty[acc], (uint32_t)((i >> 1) - 1) & 1u, a.timeout_ns)) break;
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(sq + s * 2 * kTcHalf);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (uint32_t)((k >> 2) * kTcHalf + (k & 3) * 32);
+            umma_bf16(tmem + acc * kTcCols, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, k > 0);
+          }
+          umma_commit(&q_empty[s]);
+          umma_commit(&acc_full[acc]);
+          ++done;
+        }
+      } else {
+        record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+      }
+      if (done > 0)  // the last MMAs complete before the CTA may release tensor memory
+        (void)mbar_wait_bounded(&acc_full[(done - 1) & 1], (uint32_t)((done - 1) >> 1) & 1u, a.timeout_ns);
+    }
+  } else {
+    // ---------------------------------------------------------------- accumulator readers
+    const int row = 32 * warp + lane;  // TMEM lane = key row
+    const int key = key0 + row;
+    bool kval = key < L;
+    const float sl2 = a.scale_log2;
+    const int key_last = min(key0 + kTcKeys, L) - 1;
+    const int log2g = 31 - __clz(G);
+    float sum = 0.f;
+    if (!__all_sync(kFullMask, mbar_wait_bounded(k_full, 0, a.timeout_ns))) {
+      if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+      aborted = true;
+    }
+    kval = kval && ((*s_tiles_ok >> (row >> 4)) & 1u);
+    for (int i = 0; i < n_chunks && !aborted; ++i) {
+      const int acc = i & 1;
+      if (!__all_sync(kFullMask, mbar_wait_bounded(&acc_full[acc], (uint32_t)(i >> 1) & 1u, a.timeout_ns))) {
+        if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t = tmem + ((uint32_t)(32 * warp) << 16) + acc * kTcCols;
+      const int rs = first_row + i * rows_per_chunk;
+      const int ncols = min(rows_per_chunk, alpha - rs) * G;
+      const int jbase = L - alpha + rs;
+      const bool fast = ncols == kTcCols && key_last <= jbase;  // whole chunk, every key before every row
+      const float* l2c = lse2 + i * kTcCols;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {  // 32 accumulator columns at a time
+        float v[32];
+        tmem_ld_x32(t + 32 * q, v);
+        tmem_wait_ld();
+        if (kval) {
+          if (fast) {
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 l = *reinterpret_cast<const float4*>(l2c + 32 * q + 4 * c4);
+              sum += ex2(fmaf(v[4 * c4], sl2, -l.x)) + ex2(fmaf(v[4 * c4 + 1], sl2, -l.y)) +
+                     ex2(fmaf(v[4 * c4 + 2], sl2, -l.z)) + ex2(fmaf(v[4 * c4 + 3], sl2, -l.w));
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int cc = 32 * q + c;
+              if (cc < ncols && key <= jbase + (cc >> log2g)) sum += ex2(fmaf(v[c], sl2, -l2c[cc]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+    if (!aborted && kval && key < a.score_stride) a.scores[((size_t)b * a.Hkv + g) * a.score_stride + key] += sum;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------------------- lse kernel
 
 template <int D>
@@ -499,6 +722,15 @@ size_t prefill_score_smem_bytes(int head_dim, int alpha, int group) {
          sizeof(float) * (size_t)alpha * group;
 }
 
+size_t prefill_score_tc_smem_bytes(int alpha, int group) {
+  return 1024 + 2 * kTcHalf + kTcQSlots * 2 * kTcHalf + sizeof(uint64_t) * (1 + 2 * kTcQSlots + 4) + 16 + 16 +
+         sizeof(float) * ((size_t)alpha * group + kTcCols);
+}
+
+bool prefill_tc_supported(int head_dim, int group) {
+  return head_dim == 128 && group >= 1 && group <= 8 && (group & (group - 1)) == 0;
+}
+
 size_t prefill_lse_smem_bytes(int head_dim, int max_blocks) {
   const size_t tb = 16 * (size_t)head_dim * 2;
   return 1024 + kKSlots * tb + sizeof(uint64_t) * 2 * kKSlots + sizeof(uint32_t) * kKSlots +
@@ -510,6 +742,12 @@ cudaError_t prefill_device_setup() {
   const void* score[] = {(const void*)prefill_score_kernel<128>, (const void*)prefill_score_kernel<64>};
   for (const void* f : score) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, score_max);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const cudaError_t e = cudaFuncSetAttribute((const void*)prefill_score_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)prefill_score_tc_smem_bytes(kPrefillMaxColumns, 1));
     if (e != cudaSuccess) return e;
   }
   const void* lse[] = {(const void*)prefill_lse_kernel<128>, (const void*)prefill_lse_kernel<64>};
@@ -531,6 +769,11 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool lse_given, c
     const cudaError_t e =
         launch_pdl(f, grid, dim3(kLseWarps * 32), prefill_lse_smem_bytes(head_dim, a.MB), stream, params);
     if (e != cudaSuccess) return e;
+  }
+  if (PKV_PREFILL_TCGEN05 && prefill_tc_supported(head_dim, a.G)) {
+    const dim3 grid((unsigned)((a.MB * 16 + kTcKeys - 1) / kTcKeys), (unsigned)a.Hkv, (unsigned)a.B);
+    return launch_pdl((const void*)prefill_score_tc_kernel, grid, dim3(kTcThreads),
+                      prefill_score_tc_smem_bytes(a.alpha, a.G), stream, params);
   }
   const dim3 grid((unsigned)((a.MB * 16 + kScoreKeys - 1) / kScoreKeys), (unsigned)a.Hkv, (unsigned)a.B);
   const void* f = head_dim == 128 ? (const void*)prefill_score_kernel<128> : (const void*)prefill_score_kernel<64>;

@@ -1,5 +1,6 @@
 """GPU parity of the prefill-window score (pkv_prefill_window_scores) against the fp64 oracle
-(oracle.prefill_scores).
+(oracle.prefill_scores).  d = 128 with G a power of two runs the tcgen05 kernel, d = 64 and
+G = 6 the warp-level one; both are covered.
 
 Tolerances: each probability is exp2 of an fp32 logit (exact bf16 products, fp32 sums) minus an
 fp32 log-sum-exp, so it carries a relative error of ~1e-6 (the logit's fp32 error times its
@@ -98,8 +99,9 @@ def test_given_lse_and_accumulation():
     assert torch.equal(lse_out, lse)          # read, not written
 
 
-def test_bad_block_is_reported_and_skipped():
-    c = _case([200, 90], 16, 8, 2, 64, seed=5)
+@pytest.mark.parametrize("d", [64, 128])  # the warp-level kernel and the tcgen05 one
+def test_bad_block_is_reported_and_skipped(d):
+    c = _case([200, 90], 16, 8, 2, d, seed=5)
     c["bt"][0, 3] = 10 ** 6
     err = pkv.new_error_word(DEV)
     got, _ = _gpu(c, 208, err=err)

@@ -163,6 +163,23 @@ struct PrefillArgs {
   float scale_log2;              // scale * log2(e)
   unsigned long long timeout_ns;
 };
+// tcgen05 prefill-score shape: 128-key halves per CTA, window columns per chunk (the MMA's N),
+// query chunks in flight, accumulators per key half, CTAs per SM the registers must allow
+#ifndef PKV_TC_KH
+#define PKV_TC_KH 1
+#endif
+#ifndef PKV_TC_COLS
+#define PKV_TC_COLS 128
+#endif
+#ifndef PKV_TC_QSLOTS
+#define PKV_TC_QSLOTS 2
+#endif
+#ifndef PKV_TC_ACC
+#define PKV_TC_ACC 2
+#endif
+#ifndef PKV_TC_MINB
+#define PKV_TC_MINB 2
+#endif
 #ifndef PKV_PREFILL_TCGEN05
 #define PKV_PREFILL_TCGEN05 1  // prefill score on tcgen05 where supported (d = 128, G a power of two)
 #endif

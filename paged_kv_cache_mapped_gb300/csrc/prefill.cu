@@ -306,35 +306,47 @@ __global__ void __launch_bounds__(kScoreWarps * 32) prefill_score_kernel(const _
 
 // ------------------------------------------------------------ score kernel on tcgen05 (UMMA)
 //
-// The same k-outer score, with the contraction on the 5th-generation tensor cores: a CTA owns
-// 128 keys of one (sequence, kv head); their K tile is the A operand (128 keys x 128 d, K-major,
-// 128-byte swizzle, as TMA writes it), each chunk of 128 window columns the B operand, and
-// S^T = K Q^T (128 x 128 fp32) accumulates in tensor memory over 8 k-steps of 16.  Roles: warp 4
-// issues the TMA copies, one thread of warp 5 issues the MMAs, warps 0-3 read the accumulator
-// (warp w owns TMEM lanes 32w..32w+31, one key per thread) and add each probability to the
-// thread's key sum.  Two accumulators (256 TMEM columns) let the MMAs of chunk i + 1 run while
-// chunk i is read.  d = 128 and G a power of two (so a chunk is whole window rows).
-constexpr int kTcKeys = 128;
-constexpr int kTcCols = 128;                   // window columns per chunk (the MMA's N)
-constexpr int kTcHalf = 128 * 128;             // one d-half of a 128-row operand: 128 rows x 128 B
-constexpr int kTcQSlots = 2;
-constexpr int kTcThreads = 192;
-constexpr uint32_t kTcTmemCols = 2 * kTcCols;
+// The same k-outer score, with the contraction on the 5th-generation tensor cores: a CTA (one
+// per SM) owns 256 keys of one (sequence, kv head) as two 128-key halves; each half's K tile is
+// an A operand (128 keys x 128 d, K-major, 128-byte swizzle, as TMA writes it), each chunk of 128
+// window columns the B operand both halves share (so each CTA reads the window once per 256 keys),
+// and S^T = K Q^T (128 x 128 fp32 per half) accumulates in tensor memory over 8 k-steps of 16.
+// Roles: warp 16 issues the TMA copies, one thread of warp 17 issues the MMAs, warps 0-15 read
+// the accumulators (warp w reads TMEM lanes 32 (w % 4) .. + 31 of key half (w / 4) % 2, one key per
+// thread, and column half w / 8) and add each probability to the thread's key sum; the column
+// halves' sums meet in shared memory.  Two accumulators per key half (all 512 TMEM columns) let
+// the MMAs of chunk i + 1 run while chunk i is read.  d = 128 and G a power of two (so a chunk is
+// whole window rows).
+constexpr int kTcKH = PKV_TC_KH;               // 128-key halves per CTA
+constexpr int kTcKeys = 128 * kTcKH;
+constexpr int kTcCols = PKV_TC_COLS;           // window columns per chunk (the MMA's N; 64 or 128)
+constexpr int kTcHalf = 128 * 128;             // one d-half of a 128-key A operand: 128 rows x 128 B
+constexpr int kTcQHalf = kTcCols * 128;        // one d-half of a query chunk
+constexpr int kTcQSlots = PKV_TC_QSLOTS;       // query chunks in flight
+constexpr int kTcAcc = PKV_TC_ACC;             // accumulators per key half in tensor memory
+constexpr int kTcReaders = 8 * kTcKH;          // accumulator-reading warps: lane group x key half x column half
+constexpr int kTcThreads = 32 * (kTcReaders + 2);
+constexpr uint32_t kTcTmemUsed = kTcAcc * kTcKH * kTcCols;
+constexpr uint32_t kTcTmemCols = kTcTmemUsed <= 32 ? 32 : kTcTmemUsed <= 64 ? 64 : kTcTmemUsed <= 128 ? 128
+                                 : kTcTmemUsed <= 256 ? 256 : 512;  // allocations are powers of two
+static_assert(kTcTmemUsed <= 512 && (kTcCols == 64 || kTcCols == 128), "tensor memory / chunk shape");
+constexpr int kTcMaxColumns = 8192;            // alpha * G bound of this kernel (its lse copy in shared memory)
 
-__global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __grid_constant__ PrefillArgs a) {
+__global__ void __launch_bounds__(kTcThreads, PKV_TC_MINB) prefill_score_tc_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* sa = align1024(smem_raw);              // A: 2 d-halves x 16 KiB
-  unsigned char* sq = sa + 2 * kTcHalf;                 // B slots: kTcQSlots x 2 d-halves x 16 KiB
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sq + kTcQSlots * 2 * kTcHalf);
+  unsigned char* sa = align1024(smem_raw);              // A: 2 d-halves x kTcKH x 16 KiB
+  unsigned char* sq = sa + 2 * kTcKH * kTcHalf;         // B slots: kTcQSlots x 2 d-halves x kTcQHalf
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sq + kTcQSlots * 2 * kTcQHalf);
   uint64_t* k_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + kTcQSlots;
   uint64_t* acc_full = q_empty + kTcQSlots;
-  uint64_t* acc_empty = acc_full + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* acc_empty = acc_full + kTcAcc;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_empty + kTcAcc);
   uint32_t* s_tiles_ok = s_tmem + 1;
+  float* s_half = reinterpret_cast<float*>(s_tmem + 4);  // the second column half's key sums
   // window columns from the CTA's first row, base 2; 16-byte aligned for the vector reads
-  float* lse2 = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s_tmem + 4) + 15) & ~uintptr_t(15));
+  float* lse2 = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s_half + kTcKeys) + 15) & ~uintptr_t(15));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, g = blockIdx.y;
@@ -348,9 +360,9 @@ __global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __gr
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kTcAcc; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);
+      mbar_init(&acc_empty[s], kTcReaders);
     }
     fence_mbar_init();
   }
@@ -382,15 +394,20 @@ __global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __gr
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   bool aborted = false;
+  const int lg = warp & 3, kh = (warp >> 2) & (kTcKH - 1), ch = warp / (4 * kTcKH);  // readers
+  const int row = 128 * kh + 32 * lg + lane;  // key row of the CTA (TMEM lane 32 lg + lane of half kh)
+  const int key = key0 + row;
+  bool kval = false;
+  float sum = 0.f;
 
-  if (warp == 4) {
+  if (warp == kTcReaders) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol_k = l2_policy_evict_first(), pol_q = l2_policy_evict_last();
       uint32_t ok = 0, bytes = 0;
-      int phys[8];
+      int phys[kTcKeys / 16];
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {
+      for (int p = 0; p < kTcKeys / 16; ++p) {
         const int u = key0 / 16 + p;
         phys[p] = -1;
         if (u * 16 < L) {
@@ -407,11 +424,12 @@ __global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __gr
       *s_tiles_ok = ok;
       mbar_arrive_expect_tx(k_full, bytes);
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {
+      for (int p = 0; p < kTcKeys / 16; ++p) {
         if (!((ok >> p) & 1u)) continue;
         const int y = (phys[p] * a.Hkv + g) * 16;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) tma_load_2d(sa + h * kTcHalf + p * 2048, &a.tmap_k, h * 64, y, k_full, pol_k);
+        for (int h = 0; h < 2; ++h)
+          tma_load_2d(sa + h * kTcKH * kTcHalf + p * 2048, &a.tmap_k, h * 64, y, k_full, pol_k);
       }
       int issued = 0;
       for (int i = 0; i < n_chunks; ++i) {
@@ -421,12 +439,12 @@ __global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __gr
           break;
         }
         const int rs = first_row + i * rows_per_chunk;
-        mbar_arrive_expect_tx(&q_full[s], 2 * kTcHalf);
+        mbar_arrive_expect_tx(&q_full[s], 2 * kTcQHalf);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tma_load_3d(sq + (s * 2 + h) * kTcHalf + j * 8192, &a.tmap_q, h * 64, g * G,
+          for (int j = 0; j < kTcCols / 64; ++j)
+            tma_load_3d(sq + (s * 2 + h) * kTcQHalf + j * 8192, &a.tmap_q, h * 64, g * G,
                         b * alpha + rs + j * (64 / G), &q_full[s], pol_q);
         ++issued;
       }
@@ -435,7 +453,7 @@ __global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __gr
       for (int i = max(0, issued - kTcQSlots); i < issued; ++i)
         (void)mbar_wait_bounded(&q_full[i % kTcQSlots], (uint32_t)(i / kTcQSlots) & 1u, a.timeout_ns);
     }
-  } else if (warp == 5) {
+  } else if (warp == kTcReaders + 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(128, kTcCols);
@@ -443,16 +461,21 @@ __global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __gr
       if (mbar_wait_bounded(k_full, 0, a.timeout_ns)) {
         const uint32_t a0 = smem_u32(sa);
         for (int i = 0; i < n_chunks; ++i) {
-          const int s = i % kTcQSlots, acc = i & 1;
+          const int s = i % kTcQSlots, acc = i % kTcAcc;
           if (!mbar_wait_bounded(&q_full[s], (uint32_t)(i / kTcQSlots) & 1u, a.timeout_ns)) break;
-          if (i >= 2 && !mbar_wait_bounded(&acc_empty[acc], (uint32_t)((i >> 1) - 1) & 1u, a.timeout_ns)) break;
+          if (i >= kTcAcc && !mbar_wait_bounded(&acc_empty[acc], (uint32_t)((i / kTcAcc) - 1) & 1u, a.timeout_ns))
+            break;
           tc_fence_after();
-          const uint32_t b0 = smem_u32(sq + s * 2 * kTcHalf);
+          const uint32_t b0 = smem_u32(sq + s * 2 * kTcQHalf);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (uint32_t)((k >> 2) * kTcHalf + (k & 3) * 32);
-            umma_bf16(tmem + acc * kTcCols, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, k > 0);
-          }
+          for (int kh = 0; kh < kTcKH; ++kh)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t aoff = (uint32_t)(((k >> 2) * kTcKH + kh) * kTcHalf + (k & 3) * 32);
+              const uint32_t boff = (uint32_t)((k >> 2) * kTcQHalf + (k & 3) * 32);
+              umma_bf16(tmem + (acc * kTcKH + kh) * kTcCols, umma_desc_sw128(a0 + aoff), umma_desc_sw128(b0 + boff),
+                        idesc, k > 0);
+            }
           umma_commit(&q_empty[s]);
           umma_commit(&acc_full[acc]);
           ++done;
@@ -461,38 +484,35 @@ __global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __gr
         record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
       }
       if (done > 0)  // the last MMAs complete before the CTA may release tensor memory
-        (void)mbar_wait_bounded(&acc_full[(done - 1) & 1], (uint32_t)((done - 1) >> 1) & 1u, a.timeout_ns);
+        (void)mbar_wait_bounded(&acc_full[(done - 1) % kTcAcc], (uint32_t)((done - 1) / kTcAcc) & 1u, a.timeout_ns);
     }
   } else {
     // ---------------------------------------------------------------- accumulator readers
-    const int row = 32 * warp + lane;  // TMEM lane = key row
-    const int key = key0 + row;
-    bool kval = key < L;
+    kval = key < L;
     const float sl2 = a.scale_log2;
     const int key_last = min(key0 + kTcKeys, L) - 1;
     const int log2g = 31 - __clz(G);
-    float sum = 0.f;
     if (!__all_sync(kFullMask, mbar_wait_bounded(k_full, 0, a.timeout_ns))) {
       if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
       aborted = true;
     }
     kval = kval && ((*s_tiles_ok >> (row >> 4)) & 1u);
     for (int i = 0; i < n_chunks && !aborted; ++i) {
-      const int acc = i & 1;
-      if (!__all_sync(kFullMask, mbar_wait_bounded(&acc_full[acc], (uint32_t)(i >> 1) & 1u, a.timeout_ns))) {
+      const int acc = i % kTcAcc;
+      if (!__all_sync(kFullMask, mbar_wait_bounded(&acc_full[acc], (uint32_t)(i / kTcAcc) & 1u, a.timeout_ns))) {
         if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
         aborted = true;
         break;
       }
       tc_fence_after();
-      const uint32_t t = tmem + ((uint32_t)(32 * warp) << 16) + acc * kTcCols;
+      const uint32_t t = tmem + ((uint32_t)(32 * lg) << 16) + (acc * kTcKH + kh) * kTcCols;
       const int rs = first_row + i * rows_per_chunk;
       const int ncols = min(rows_per_chunk, alpha - rs) * G;
       const int jbase = L - alpha + rs;
       const bool fast = ncols == kTcCols && key_last <= jbase;  // whole chunk, every key before every row
       const float* l2c = lse2 + i * kTcCols;
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {  // 32 accumulator columns at a time
+      for (int q = ch * (kTcCols / 64); q < (ch + 1) * (kTcCols / 64); ++q) {  // this warp's half, 32 at a time
         float v[32];
         tmem_ld_x32(t + 32 * q, v);
         tmem_wait_ld();
@@ -517,10 +537,13 @@ __global__ void __launch_bounds__(kTcThreads) prefill_score_tc_kernel(const __gr
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
     }
-    if (!aborted && kval && key < a.score_stride) a.scores[((size_t)b * a.Hkv + g) * a.score_stride + key] += sum;
+    if (aborted) kval = false;
+    if (ch == 1) s_half[row] = kval ? sum : 0.f;
   }
   tc_fence_before();
   __syncthreads();
+  if (ch == 0 && warp < kTcReaders && kval && key < a.score_stride)
+    a.scores[((size_t)b * a.Hkv + g) * a.score_stride + key] += sum + s_half[row];
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTcTmemCols);
@@ -723,12 +746,13 @@ size_t prefill_score_smem_bytes(int head_dim, int alpha, int group) {
 }
 
 size_t prefill_score_tc_smem_bytes(int alpha, int group) {
-  return 1024 + 2 * kTcHalf + kTcQSlots * 2 * kTcHalf + sizeof(uint64_t) * (1 + 2 * kTcQSlots + 4) + 16 + 16 +
-         sizeof(float) * ((size_t)alpha * group + kTcCols);
+  return 1024 + 2 * kTcKH * kTcHalf + kTcQSlots * 2 * kTcQHalf + sizeof(uint64_t) * (1 + 2 * kTcQSlots + 2 * kTcAcc) +
+         16 + sizeof(float) * kTcKeys + 16 + sizeof(float) * ((size_t)alpha * group + kTcCols);
 }
 
-bool prefill_tc_supported(int head_dim, int group) {
-  return head_dim == 128 && group >= 1 && group <= 8 && (group & (group - 1)) == 0;
+bool prefill_tc_supported(int head_dim, int group, int alpha) {
+  return head_dim == 128 && group >= 1 && group <= 8 && (group & (group - 1)) == 0 &&
+         (long long)alpha * group <= kTcMaxColumns;
 }
 
 size_t prefill_lse_smem_bytes(int head_dim, int max_blocks) {
@@ -747,7 +771,7 @@ cudaError_t prefill_device_setup() {
   {
     const cudaError_t e = cudaFuncSetAttribute((const void*)prefill_score_tc_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)prefill_score_tc_smem_bytes(kPrefillMaxColumns, 1));
+                                               (int)prefill_score_tc_smem_bytes(kTcMaxColumns, 1));
     if (e != cudaSuccess) return e;
   }
   const void* lse[] = {(const void*)prefill_lse_kernel<128>, (const void*)prefill_lse_kernel<64>};
@@ -770,7 +794,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool lse_given, c
         launch_pdl(f, grid, dim3(kLseWarps * 32), prefill_lse_smem_bytes(head_dim, a.MB), stream, params);
     if (e != cudaSuccess) return e;
   }
-  if (PKV_PREFILL_TCGEN05 && prefill_tc_supported(head_dim, a.G)) {
+  if (PKV_PREFILL_TCGEN05 && prefill_tc_supported(head_dim, a.G, a.alpha)) {
     const dim3 grid((unsigned)((a.MB * 16 + kTcKeys - 1) / kTcKeys), (unsigned)a.Hkv, (unsigned)a.B);
     return launch_pdl((const void*)prefill_score_tc_kernel, grid, dim3(kTcThreads),
                       prefill_score_tc_smem_bytes(a.alpha, a.G), stream, params);

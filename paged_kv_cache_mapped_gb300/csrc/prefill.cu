@@ -550,6 +550,227 @@ __global__ void __launch_bounds__(kTcThreads, PKV_TC_MINB) prefill_score_tc_kern
   }
 }
 
+// ---------------------------------------------------------------- lse kernel on tcgen05 (UMMA)
+//
+// The window rows' log-sum-exps when the caller has none: the q-outer order on tcgen05.  A CTA
+// owns 128 window columns of one (sequence, kv head) as the A operand (TMA boxes of the window's
+// queries, K-major, 128-byte swizzle); the sequence's K streams as B operands in chunks of 128
+// keys (8 pool blocks) through a ring, up to the CTA's last attended key; S = Q K^T (128 x 128
+// fp32) accumulates in tensor memory.  Warp 8 issues the TMA copies, one thread of warp 9 the
+// MMAs, warps 0-7 read the accumulators (warp w: TMEM lanes 32 (w % 4) .., one column per
+// thread, key half w / 4 of each chunk) and keep a running max (moved lazily) and sum; the two
+// halves merge in shared memory.  d = 128 and G a power of two.
+constexpr int kLtKSlots = 2;
+constexpr int kLtThreads = 32 * 10;
+
+__global__ void __launch_bounds__(kLtThreads, 2) prefill_lse_tc_kernel(const __grid_constant__ PrefillArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sa = align1024(smem_raw);                // A: 2 d-halves x 128 columns x 128 B
+  unsigned char* sk = sa + 2 * kTcHalf;                   // B slots: kLtKSlots x 2 d-halves x 128 keys x 128 B
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sk + kLtKSlots * 2 * kTcHalf);
+  uint64_t* a_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + kLtKSlots;
+  uint64_t* acc_full = k_empty + kLtKSlots;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  float2* s_half = reinterpret_cast<float2*>(s_tmem + 4); // the second key half's (m, l) per column
+  int32_t* s_bt = reinterpret_cast<int32_t*>(s_half + 128);  // the sequence's block ids
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int cbase = blockIdx.x * 128;
+  const int G = a.G, alpha = a.alpha;
+
+  if (threadIdx.x == 0) {
+    mbar_init(a_full, 1);
+    for (int s = 0; s < kLtKSlots; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 8);
+    }
+    fence_mbar_init();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  const int L = a.context_lens[b];
+  if (L < 0 || L > a.MB * 16) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) record_error(a.err, PKV_DEV_BAD_CONTEXT_LEN);
+    return;
+  }
+  const int ncol = alpha * G;
+  const int c_lo = max(0, alpha - L) * G;  // columns of rows before position 0 have no keys
+  if (cbase >= ncol) return;
+  auto lse_at = [&](int c) -> float* {
+    return a.lse + ((size_t)b * a.Hq + (size_t)g * G + (c & (G - 1))) * alpha + c / G;
+  };
+  for (int c = cbase + (int)threadIdx.x; c < min(cbase + 128, c_lo); c += blockDim.x) *lse_at(c) = -INFINITY;
+  if (cbase + 128 <= c_lo) return;
+  const int c_last = min(cbase + 128, ncol) - 1;
+  const int j_last = L - alpha + c_last / G;             // the CTA's last attended key
+  const int n_chunks = j_last / 128 + 1;
+  const int nblk = j_last / 16 + 1;
+  for (int u = threadIdx.x; u < nblk; u += blockDim.x) s_bt[u] = a.block_tables[(size_t)b * a.MB + u];
+  if (warp == 0) {
+    tmem_alloc(s_tmem, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  bool aborted = false;
+  const int lg = warp & 3, kh = warp >> 2;  // readers: TMEM lane group, key half of each chunk
+  const int row = 32 * lg + lane;           // this thread's column of the CTA
+  const int col = cbase + row;
+  float m = -INFINITY, l = 0.f;             // running max (base 2) and sum over this thread's keys
+
+  if (warp == 8) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_q = l2_policy_evict_first(), pol_k = l2_policy_evict_last();
+      mbar_arrive_expect_tx(a_full, 2 * kTcHalf);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          tma_load_3d(sa + h * kTcHalf + j * 8192, &a.tmap_q, h * 64, g * G, b * alpha + cbase / G + j * (64 / G),
+                      a_full, pol_q);
+      int issued = 0;
+      for (int i = 0; i < n_chunks; ++i) {
+        const int s = i % kLtKSlots;
+        if (i >= kLtKSlots && !mbar_wait_bounded(&k_empty[s], (uint32_t)((i / kLtKSlots) - 1) & 1u, a.timeout_ns)) {
+          record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        uint32_t ok = 0, bytes = 0;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const int u = 8 * i + p;
+          if (u >= nblk) continue;
+          const int phys = s_bt[u];
+          if (phys >= 0 && phys < a.NB) {
+            ok |= 1u << p;
+            bytes += 2 * 2048;
+          } else {
+            record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
+          }
+        }
+        mbar_arrive_expect_tx(&k_full[s], bytes);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          if (!((ok >> p) & 1u)) continue;
+          const int y = (s_bt[8 * i + p] * a.Hkv + g) * 16;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(sk + (s * 2 + h) * kTcHalf + p * 2048, &a.tmap_k, h * 64, y, &k_full[s], pol_k);
+        }
+        ++issued;
+      }
+      // every copy lands before the CTA may exit
+      (void)mbar_wait_bounded(a_full, 0, a.timeout_ns);
+      for (int i = max(0, issued - kLtKSlots); i < issued; ++i)
+        (void)mbar_wait_bounded(&k_full[i % kLtKSlots], (uint32_t)(i / kLtKSlots) & 1u, a.timeout_ns);
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(128, 128);
+      int done = 0;
+      if (mbar_wait_bounded(a_full, 0, a.timeout_ns)) {
+        const uint32_t a0 = smem_u32(sa);
+        for (int i = 0; i < n_chunks; ++i) {
+          const int s = i % kLtKSlots, acc = i & 1;
+          if (!mbar_wait_bounded(&k_full[s], (uint32_t)(i / kLtKSlots) & 1u, a.timeout_ns)) break;
+          if (i >= 2 && !mbar_wait_bounded(&acc_empty[acc], (uint32_t)((i >> 1) - 1) & 1u, a.timeout_ns)) break;
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(sk + s * 2 * kTcHalf);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (uint32_t)((k >> 2) * kTcHalf + (k & 3) * 32);
+            umma_bf16(tmem + acc * 128, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, k > 0);
+          }
+          umma_commit(&k_empty[s]);
+          umma_commit(&acc_full[acc]);
+          ++done;
+        }
+      } else {
+        record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+      }
+      if (done > 0)  // the last MMAs complete before the CTA may release tensor memory
+        (void)mbar_wait_bounded(&acc_full[(done - 1) & 1], (uint32_t)((done - 1) >> 1) & 1u, a.timeout_ns);
+    }
+  } else {
+    // ---------------------------------------------------------------- accumulator readers
+    const float sl2 = a.scale_log2;
+    const int j = L - alpha + col / G;                               // this column's position
+    const int j_min = L - alpha + max(cbase, c_lo) / G;              // the CTA's first valid position
+    for (int i = 0; i < n_chunks && !aborted; ++i) {
+      const int acc = i & 1;
+      if (!__all_sync(kFullMask, mbar_wait_bounded(&acc_full[acc], (uint32_t)(i >> 1) & 1u, a.timeout_ns))) {
+        if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t = tmem + ((uint32_t)(32 * lg) << 16) + acc * 128;
+#pragma unroll 1
+      for (int q = 2 * kh; q < 2 * kh + 2; ++q) {  // this warp's 64 keys, 32 at a time
+        const int k0 = 128 * i + 32 * q;
+        float v[32];
+        tmem_ld_x32(t + 32 * q, v);
+        tmem_wait_ld();
+        const int u0 = k0 >> 4;
+        const bool blocks_ok = u0 + 1 < nblk && s_bt[u0] >= 0 && s_bt[u0] < a.NB && s_bt[u0 + 1] >= 0 &&
+                               s_bt[u0 + 1] < a.NB;
+        if (!(blocks_ok && k0 + 31 <= j_min)) {  // near the diagonal or a skipped block: mask keys
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int k = k0 + c, u = k >> 4;
+            const bool kv = k <= j && u < nblk && s_bt[u] >= 0 && s_bt[u] < a.NB;
+            v[c] = kv ? v[c] : -INFINITY;
+          }
+        }
+        float mx = v[0];
+#pragma unroll
+        for (int c = 1; c < 32; ++c) mx = fmaxf(mx, v[c]);
+        mx *= sl2;  // sl2 > 0 keeps the order
+        if (mx > m + kLseSlack) {
+          l *= ex2(m - mx);
+          m = mx;
+        }
+        if (m != -INFINITY) {
+          float e = 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) e += ex2(fmaf(v[c], sl2, -m));
+          l += e;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+    if (kh == 1) s_half[row] = make_float2(m, l);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp < 4 && !aborted && col >= c_lo && col < ncol) {
+    const float2 o = s_half[row];
+    const float M = fmaxf(m, o.x);
+    const float lt = (m == -INFINITY ? 0.f : l * exp2f(m - M)) + (o.x == -INFINITY ? 0.f : o.y * exp2f(o.x - M));
+    *lse_at(col) = lt > 0.f ? (M + log2f(lt)) * kLn2F : -INFINITY;
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 // ---------------------------------------------------------------------------- lse kernel
 
 template <int D>
@@ -755,6 +976,11 @@ bool prefill_tc_supported(int head_dim, int group, int alpha) {
          (long long)alpha * group <= kTcMaxColumns;
 }
 
+size_t prefill_lse_tc_smem_bytes(int max_blocks) {
+  return 1024 + 2 * kTcHalf + kLtKSlots * 2 * kTcHalf + sizeof(uint64_t) * (1 + 2 * kLtKSlots + 4) + 16 +
+         sizeof(float2) * 128 + sizeof(int32_t) * (size_t)max_blocks;
+}
+
 size_t prefill_lse_smem_bytes(int head_dim, int max_blocks) {
   const size_t tb = 16 * (size_t)head_dim * 2;
   return 1024 + kKSlots * tb + sizeof(uint64_t) * 2 * kKSlots + sizeof(uint32_t) * kKSlots +
@@ -774,6 +1000,12 @@ cudaError_t prefill_device_setup() {
                                                (int)prefill_score_tc_smem_bytes(kTcMaxColumns, 1));
     if (e != cudaSuccess) return e;
   }
+  {
+    const cudaError_t e = cudaFuncSetAttribute((const void*)prefill_lse_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)prefill_lse_tc_smem_bytes(kPrefillMaxBlocks));
+    if (e != cudaSuccess) return e;
+  }
   const void* lse[] = {(const void*)prefill_lse_kernel<128>, (const void*)prefill_lse_kernel<64>};
   for (const void* f : lse) {
     const cudaError_t e =
@@ -787,7 +1019,12 @@ cudaError_t prefill_device_setup() {
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool lse_given, cudaStream_t stream) {
   PrefillArgs args = a;
   void* params[] = {&args};
-  if (!lse_given) {
+  if (!lse_given && PKV_PREFILL_TCGEN05 && prefill_tc_supported(head_dim, a.G, a.alpha)) {
+    const dim3 grid((unsigned)((a.alpha * a.G + 127) / 128), (unsigned)a.Hkv, (unsigned)a.B);
+    const cudaError_t e = launch_pdl((const void*)prefill_lse_tc_kernel, grid, dim3(kLtThreads),
+                                     prefill_lse_tc_smem_bytes(a.MB), stream, params);
+    if (e != cudaSuccess) return e;
+  } else if (!lse_given) {
     const dim3 grid((unsigned)((a.alpha * a.G + kLseCols - 1) / kLseCols), (unsigned)a.Hkv, (unsigned)a.B);
     const void* f = head_dim == 128 ? (const void*)prefill_lse_kernel<128> : (const void*)prefill_lse_kernel<64>;
     const cudaError_t e =

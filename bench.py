@@ -280,6 +280,7 @@ def run_ours(args):
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / hbm, 4),
+            "frac_of_nominal_8000": round(achieved / 8000.0, 4),  # the part's nominal HBM3e figure
             "traffic": profiled_traffic("decode_split_llama8b"),
             "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the split kernel "
                             "(profiles/decode_split_llama8b.md); the merge kernel adds the partials",

@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(kTcThreads, PKV_TC_MINB) prefill_score_tc_kern
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_empty + kTcAcc);
   uint32_t* s_tiles_ok = s_tmem + 1;
   float* s_half = reinterpret_cast<float*>(s_tmem + 4);  // the second column half's key sums
-  // window columns from the CTA's first row, base 2; 16-byte aligned for the vector reads
-  float* lse2 = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s_half + kTcKeys) + 15) & ~uintptr_t(15));
+  // minus the lse (base 2) of the window columns from the CTA's first row; 16-byte aligned
+  float* nlse2 = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s_half + kTcKeys) + 15) & ~uintptr_t(15));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, g = blockIdx.y;
@@ -383,11 +383,12 @@ __global__ void __launch_bounds__(kTcThreads, PKV_TC_MINB) prefill_score_tc_kern
     tmem_alloc(s_tmem, kTcTmemCols);
     tmem_relinquish();
   }
-  // lse of the columns from the first row on, chunk-major (chunk i's column c at i * 128 + c)
+  // minus the lse of the columns from the first row on, chunk-major (chunk i's column c at
+  // i * kTcCols + c), so the logit FMA adds it
   for (int k = threadIdx.x; k < (alpha - first_row) * G; k += blockDim.x) {
     const int c = first_row * G + k;
     const int r = c / G, hi = c - r * G;
-    lse2[k] = a.lse[((size_t)b * a.Hq + (size_t)g * G + hi) * alpha + r] * kLog2eF;
+    nlse2[k] = -a.lse[((size_t)b * a.Hq + (size_t)g * G + hi) * alpha + r] * kLog2eF;
   }
   tc_fence_before();
   __syncthreads();
@@ -510,25 +511,31 @@ __global__ void __launch_bounds__(kTcThreads, PKV_TC_MINB) prefill_score_tc_kern
       const int ncols = min(rows_per_chunk, alpha - rs) * G;
       const int jbase = L - alpha + rs;
       const bool fast = ncols == kTcCols && key_last <= jbase;  // whole chunk, every key before every row
-      const float* l2c = lse2 + i * kTcCols;
+      const float* l2c = nlse2 + i * kTcCols;
 #pragma unroll 1
       for (int q = ch * (kTcCols / 64); q < (ch + 1) * (kTcCols / 64); ++q) {  // this warp's half, 32 at a time
         float v[32];
         tmem_ld_x32(t + 32 * q, v);
         tmem_wait_ld();
         if (kval) {
-          if (fast) {
+          if (fast) {  // packed fp32 pairs: one FMA and one add per two probabilities
+            const uint64_t s2 = pack2(sl2, sl2);
+            uint64_t acc2 = pack2(0.f, 0.f);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
               const float4 l = *reinterpret_cast<const float4*>(l2c + 32 * q + 4 * c4);
-              sum += ex2(fmaf(v[4 * c4], sl2, -l.x)) + ex2(fmaf(v[4 * c4 + 1], sl2, -l.y)) +
-                     ex2(fmaf(v[4 * c4 + 2], sl2, -l.z)) + ex2(fmaf(v[4 * c4 + 3], sl2, -l.w));
+              const float2 x01 = unpack2(ffma2(pack2(v[4 * c4], v[4 * c4 + 1]), s2, pack2(l.x, l.y)));
+              const float2 x23 = unpack2(ffma2(pack2(v[4 * c4 + 2], v[4 * c4 + 3]), s2, pack2(l.z, l.w)));
+              acc2 = fadd2(acc2, pack2(ex2(x01.x), ex2(x01.y)));
+              acc2 = fadd2(acc2, pack2(ex2(x23.x), ex2(x23.y)));
             }
+            const float2 a2 = unpack2(acc2);
+            sum += a2.x + a2.y;
           } else {
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
               const int cc = 32 * q + c;
-              if (cc < ncols && key <= jbase + (cc >> log2g)) sum += ex2(fmaf(v[c], sl2, -l2c[cc]));
+              if (cc < ncols && key <= jbase + (cc >> log2g)) sum += ex2(fmaf(v[c], sl2, l2c[cc]));
             }
           }
         }
@@ -744,11 +751,16 @@ __global__ void __launch_bounds__(kLtThreads, 2) prefill_lse_tc_kernel(const __g
           l *= ex2(m - mx);
           m = mx;
         }
-        if (m != -INFINITY) {
-          float e = 0.f;
+        if (m != -INFINITY) {  // packed fp32 pairs: one FMA and one add per two terms
+          const uint64_t s2 = pack2(sl2, sl2), nm2 = pack2(-m, -m);
+          uint64_t e2 = pack2(0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) e += ex2(fmaf(v[c], sl2, -m));
-          l += e;
+          for (int c = 0; c < 32; c += 2) {
+            const float2 x = unpack2(ffma2(pack2(v[c], v[c + 1]), s2, nm2));
+            e2 = fadd2(e2, pack2(ex2(x.x), ex2(x.y)));
+          }
+          const float2 e = unpack2(e2);
+          l += e.x + e.y;
         }
       }
       tc_fence_before();

@@ -23,6 +23,12 @@ Parity status of each function (what pins it; see ``tests/test_oracle_*.py``):
   kv_append_q8     -- pinned by a dict-of-slots model over quantize_rows
   paged_decode_q8  -- pinned by equality with paged_decode where code * scale is a bf16 value,
                       and by torch SDPA (fp64) on the dequantized contiguous K/V
+  decode_scores_q8 -- pinned by equality with decode_scores where code * scale is a bf16 value,
+                      and by torch softmax (fp64) on the dequantized K
+  compact_q8       -- pinned by a dict-of-slots model (codes and row scales move together) and
+                      by dequantize-then-compact == compact-then-dequantize
+  rolling_admit_q8 -- pinned by the bf16 rolling admission's slot choice on the same scores and
+                      by quantize_rows of the admitted rows
   prefill_scores   -- pinned by torch causal softmax (fp64), a segment's scores summing to G per
                       window row, the q = 0 closed form, alpha = 1 against decode_scores, the
                       given-lse property and block-permutation invariance
@@ -101,10 +107,17 @@ def _load():
             lib.oracle_kv_append_q8.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i64]
             lib.oracle_paged_decode_q8.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i64,
                                                    i32, f64, i32, P, i64]
+            lib.oracle_decode_scores_q8.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i64, i32,
+                                                    f64, i32, i64, P, i64]
+            lib.oracle_compact_q8.argtypes = [P, P, P, P, P, i64, i32, P, P, P, P, P, P, P, P, i32, i32,
+                                              i32, i32, i64, i32]
+            lib.oracle_rolling_admit_q8.argtypes = [P, P, P, P, P, i64, i32, P, P, P, P, P, P, i32, i32,
+                                                    i32, i32, i32, i32]
             for name in ("oracle_kv_append", "oracle_paged_decode", "oracle_sparse_decode",
                          "oracle_select_topk", "oracle_compact", "oracle_decode_scores",
                          "oracle_rolling_admit", "oracle_quantize_rows", "oracle_kv_append_q8",
-                         "oracle_paged_decode_q8", "oracle_prefill_scores"):
+                         "oracle_paged_decode_q8", "oracle_prefill_scores", "oracle_decode_scores_q8",
+                         "oracle_compact_q8", "oracle_rolling_admit_q8"):
                 getattr(lib, name).restype = i32
             _lib = lib
     return _lib
@@ -359,3 +372,83 @@ def prefill_scores(q_win, k_cache, block_tables, context_lens, alpha, scale, lse
     if segs is None:
         score = score.reshape(b, hkv, stride)
     return score, lse_arr
+
+
+def decode_scores_q8(q, k_codes, k_scales, block_tables, context_lens, scale, window=0, stride=None, segs=None):
+    """decode_scores over an INT8 K pool (values code * scale); same returns."""
+    q = _arr(q, np.uint16)
+    kc = _arr(k_codes, np.int8)
+    ks = _arr(k_scales, np.float32)
+    bt = _arr(block_tables, np.int32)
+    lens = _arr(context_lens, np.int32)
+    b, hq, d = q.shape
+    nb, hkv, bs, d2 = kc.shape
+    assert bs == 16 and d2 == d and ks.shape == (nb, hkv, 16) and bt.shape[0] == b
+    g = hq // hkv
+    if stride is None:
+        stride = max(int(lens.max()) if lens.size else 0, 1)
+    if segs is None:
+        s_arr, n = None, b * hkv
+    else:
+        s_arr = _arr(np.asarray(segs, dtype=np.int64), np.int64)
+        n = s_arr.shape[0]
+    score = np.zeros((n, stride), dtype=np.float64)
+    lse = np.zeros((n, g), dtype=np.float64)
+    _check(_load().oracle_decode_scores_q8(_ptr(score), _ptr(lse), _ptr(q), _ptr(kc), _ptr(ks), _ptr(bt),
+                                           _ptr(lens), b, hq, hkv, d, nb, bt.shape[1], float(scale), int(window),
+                                           int(stride), None if s_arr is None else _ptr(s_arr), n),
+           "decode_scores_q8")
+    if segs is None:
+        return score.reshape(b, hkv, stride), lse.reshape(b, hq)
+    return score, lse
+
+
+def compact_q8(dst_k, dst_v, dst_ks, dst_vs, dst_block_tables, src_k, src_v, src_ks, src_vs, src_block_tables,
+               context_lens, kept, kept_lens):
+    """INT8 compaction; returns copies (dst_k, dst_v, dst_ks, dst_vs) of the destination pools."""
+    dk = np.array(_arr(dst_k, np.int8), copy=True)
+    dv = np.array(_arr(dst_v, np.int8), copy=True)
+    dks = np.array(_arr(dst_ks, np.float32), copy=True)
+    dvs = np.array(_arr(dst_vs, np.float32), copy=True)
+    dbt = _arr(dst_block_tables, np.int32)
+    sk = _arr(src_k, np.int8)
+    sv = _arr(src_v, np.int8)
+    sks = _arr(src_ks, np.float32)
+    svs = _arr(src_vs, np.float32)
+    sbt = _arr(src_block_tables, np.int32)
+    lens = _arr(context_lens, np.int32)
+    kept = _arr(kept, np.int32)
+    kl = _arr(kept_lens, np.int32)
+    b, hkv, max_kept = kept.shape
+    d = sk.shape[3]
+    assert dks.shape == dk.shape[:3] and sks.shape == sk.shape[:3]
+    _check(_load().oracle_compact_q8(_ptr(dk), _ptr(dv), _ptr(dks), _ptr(dvs), _ptr(dbt), dk.shape[0],
+                                     dbt.shape[1], _ptr(sk), _ptr(sv), _ptr(sks), _ptr(svs), _ptr(sbt),
+                                     _ptr(lens), _ptr(kept), _ptr(kl), max_kept, b, hkv, d, sk.shape[0],
+                                     sbt.shape[1]), "compact_q8")
+    return dk, dv, dks, dvs
+
+
+def rolling_admit_q8(k_codes, v_codes, k_scales, v_scales, block_tables, slot_pos, slot_score, kept_lens,
+                     context_lens, k_new, v_new, n_sink, n_recent):
+    """rolling_admit into INT8 pools; returns updated copies (k_codes, v_codes, k_scales,
+    v_scales, slot_pos, slot_score, kept_lens)."""
+    kc = np.array(_arr(k_codes, np.int8), copy=True)
+    vc = np.array(_arr(v_codes, np.int8), copy=True)
+    ks = np.array(_arr(k_scales, np.float32), copy=True)
+    vs = np.array(_arr(v_scales, np.float32), copy=True)
+    bt = _arr(block_tables, np.int32)
+    pos = np.array(_arr(slot_pos, np.int32), copy=True)
+    sc = np.array(_arr(slot_score, np.float32), copy=True)
+    kl = np.array(_arr(kept_lens, np.int32), copy=True)
+    lens = _arr(context_lens, np.int32)
+    kn = _arr(k_new, np.uint16)
+    vn = _arr(v_new, np.uint16)
+    nb, hkv, bs, d = kc.shape
+    b, hkv2, cap = pos.shape
+    assert bs == 16 and hkv2 == hkv and sc.shape == pos.shape and kn.shape == (b, hkv, d)
+    assert ks.shape == (nb, hkv, 16) and vs.shape == ks.shape
+    _check(_load().oracle_rolling_admit_q8(_ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), nb, bt.shape[1],
+                                           _ptr(pos), _ptr(sc), _ptr(kl), _ptr(lens), _ptr(kn), _ptr(vn), b, hkv,
+                                           d, cap, int(n_sink), int(n_recent)), "rolling_admit_q8")
+    return kc, vc, ks, vs, pos, sc, kl

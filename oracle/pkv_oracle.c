@@ -386,9 +386,10 @@ int oracle_sparse_decode(double* out, const uint16_t* q, const uint16_t* k_cache
 
 /*
  * Logits of one query row over an explicit list of logical positions:
- * logits[j] = scale * sum_e q[e] * K_{tokens[j]}[e]  (as in attend_one_row).
+ * logits[j] = scale * sum_e q[e] * K_{tokens[j]}[e]  (as in attend_one_row; K read through its
+ * pool, so INT8 rows are code * scale).
  */
-static int row_logits(double* logits, const uint16_t* q_row, const uint16_t* k_cache,
+static int row_logits(double* logits, const uint16_t* q_row, const pool_t* k_pool,
                       const int32_t* block_row, int max_blocks_per_seq, int64_t num_blocks,
                       int num_kv_heads, int head_dim, int kv_head, double scale,
                       const int64_t* tokens, int64_t n_tokens) {
@@ -398,10 +399,10 @@ static int row_logits(double* logits, const uint16_t* q_row, const uint16_t* k_c
     if (t < 0 || logical_block >= max_blocks_per_seq) return ORC_ERR_INDEX;
     int64_t physical = block_row[logical_block];
     if (physical < 0 || physical >= num_blocks) return ORC_ERR_BLOCK;
-    int64_t row = ((physical * num_kv_heads + kv_head) * ORC_BLOCK + t % ORC_BLOCK) * head_dim;
+    int64_t row = (physical * num_kv_heads + kv_head) * ORC_BLOCK + t % ORC_BLOCK;
     double dot = 0.0;
     for (int e = 0; e < head_dim; ++e)
-      dot += bf16_to_double(q_row[e]) * bf16_to_double(k_cache[row + e]);
+      dot += bf16_to_double(q_row[e]) * pool_value(k_pool, row, head_dim, e);
     logits[j] = scale * dot;
   }
   return ORC_OK;
@@ -420,12 +421,12 @@ static int row_logits(double* logits, const uint16_t* q_row, const uint16_t* k_c
  * The attended set is that of oracle_paged_decode (window as there); stride >= every L_b.
  * An empty set gives a zero score row and lse = -infinity.
  */
-int oracle_decode_scores(double* score_add, double* lse, const uint16_t* q,
-                         const uint16_t* k_cache, const int32_t* block_tables,
-                         const int32_t* context_lens, int batch, int num_q_heads,
-                         int num_kv_heads, int head_dim, int64_t num_blocks,
-                         int max_blocks_per_seq, double scale, int window, int64_t stride,
-                         const int64_t* seg_ids, int64_t n_segs) {
+static int decode_scores_pools(double* score_add, double* lse, const uint16_t* q,
+                               const pool_t* k_pool, const int32_t* block_tables,
+                               const int32_t* context_lens, int batch, int num_q_heads,
+                               int num_kv_heads, int head_dim, int64_t num_blocks,
+                               int max_blocks_per_seq, double scale, int window, int64_t stride,
+                               const int64_t* seg_ids, int64_t n_segs) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return ORC_ERR_ARG;
   if (num_q_heads % num_kv_heads != 0 || stride < 0) return ORC_ERR_ARG;
   int group = num_q_heads / num_kv_heads;
@@ -462,7 +463,7 @@ int oracle_decode_scores(double* score_add, double* lse, const uint16_t* q,
               *lse_out = -INFINITY;
               continue;
             }
-            st = row_logits(logits, q + ((int64_t)b * num_q_heads + h) * head_dim, k_cache,
+            st = row_logits(logits, q + ((int64_t)b * num_q_heads + h) * head_dim, k_pool,
                             block_tables + (int64_t)b * max_blocks_per_seq, max_blocks_per_seq,
                             num_blocks, num_kv_heads, head_dim, g, scale, tokens, n);
             if (st != ORC_OK) break;
@@ -489,6 +490,32 @@ int oracle_decode_scores(double* score_add, double* lse, const uint16_t* q,
   return status;
 }
 
+/* The decode score over a bf16 K pool (the attended set of oracle_paged_decode). */
+int oracle_decode_scores(double* score_add, double* lse, const uint16_t* q,
+                         const uint16_t* k_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, int batch, int num_q_heads,
+                         int num_kv_heads, int head_dim, int64_t num_blocks,
+                         int max_blocks_per_seq, double scale, int window, int64_t stride,
+                         const int64_t* seg_ids, int64_t n_segs) {
+  pool_t k_pool = {k_cache, NULL, NULL};
+  return decode_scores_pools(score_add, lse, q, &k_pool, block_tables, context_lens, batch,
+                             num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq,
+                             scale, window, stride, seg_ids, n_segs);
+}
+
+/* The decode score over an INT8 K pool: every K element read as code * scale of its row. */
+int oracle_decode_scores_q8(double* score_add, double* lse, const uint16_t* q,
+                            const int8_t* k_codes, const float* k_scales,
+                            const int32_t* block_tables, const int32_t* context_lens, int batch,
+                            int num_q_heads, int num_kv_heads, int head_dim, int64_t num_blocks,
+                            int max_blocks_per_seq, double scale, int window, int64_t stride,
+                            const int64_t* seg_ids, int64_t n_segs) {
+  pool_t k_pool = {NULL, k_codes, k_scales};
+  return decode_scores_pools(score_add, lse, q, &k_pool, block_tables, context_lens, batch,
+                             num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq,
+                             scale, window, stride, seg_ids, n_segs);
+}
+
 /*
  * Prefill-side sparsification score ([novita] section "2. Attention modification": the
  * PyramidKV-style score).  After a prompt of L_b tokens, the score of key i in kv head g is
@@ -510,6 +537,7 @@ int oracle_prefill_scores(double* score_add, double* lse, int lse_given, const u
                           double scale, int64_t stride, const int64_t* seg_ids, int64_t n_segs) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || alpha <= 0) return ORC_ERR_ARG;
   if (num_q_heads % num_kv_heads != 0 || stride < 0) return ORC_ERR_ARG;
+  pool_t k_pool = {k_cache, NULL, NULL};
   int group = num_q_heads / num_kv_heads;
   int64_t total = seg_ids ? n_segs : (int64_t)batch * num_kv_heads;
   int status = ORC_OK;
@@ -538,7 +566,7 @@ int oracle_prefill_scores(double* score_add, double* lse, int lse_given, const u
         }
         /* causal: row j attends keys [0, j] */
         st = row_logits(logits, q_win + (((int64_t)b * alpha + rw) * num_q_heads + h) * head_dim,
-                        k_cache, block_tables + (int64_t)b * max_blocks_per_seq, max_blocks_per_seq,
+                        &k_pool, block_tables + (int64_t)b * max_blocks_per_seq, max_blocks_per_seq,
                         num_blocks, num_kv_heads, head_dim, g, scale, tokens, j + 1);
         if (st != ORC_OK) break;
         double row_lse;
@@ -648,14 +676,19 @@ int oracle_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* s
  * of the destination pool -- receives source token kept[b][g][j] (found through the source
  * block table).  This realises the per-layer block-table policy of [novita] section "Key
  * technique 1" (Fig. 5): a sparse layer's retained KV lives in its own 16-token blocks.
+ * The copy behind both compactions moves rows of elem_bytes * head_dim bytes (bf16 elements,
+ * or INT8 codes whose row scales move with them when the scale arrays are given).
  */
-int oracle_compact(uint16_t* dst_k, uint16_t* dst_v, const int32_t* dst_block_tables,
-                   int64_t dst_num_blocks, int dst_max_blocks_per_seq, const uint16_t* src_k,
-                   const uint16_t* src_v, const int32_t* src_block_tables,
-                   const int32_t* context_lens, const int32_t* kept, const int32_t* kept_lens,
-                   int max_kept, int batch, int num_kv_heads, int head_dim,
-                   int64_t src_num_blocks, int src_max_blocks_per_seq) {
+static int compact_pools(unsigned char* dst_k, unsigned char* dst_v, float* dst_ks, float* dst_vs,
+                         const int32_t* dst_block_tables, int64_t dst_num_blocks,
+                         int dst_max_blocks_per_seq, const unsigned char* src_k,
+                         const unsigned char* src_v, const float* src_ks, const float* src_vs,
+                         const int32_t* src_block_tables, const int32_t* context_lens,
+                         const int32_t* kept, const int32_t* kept_lens, int max_kept, int batch,
+                         int num_kv_heads, int head_dim, int64_t src_num_blocks,
+                         int src_max_blocks_per_seq, size_t elem_bytes) {
   if (batch < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kept < 0) return ORC_ERR_ARG;
+  size_t row_bytes = elem_bytes * (size_t)head_dim;
   for (int b = 0; b < batch; ++b) {
     int64_t n = kept_lens[b];
     if (n < 0 || n > max_kept || n > (int64_t)dst_max_blocks_per_seq * ORC_BLOCK)
@@ -670,16 +703,88 @@ int oracle_compact(uint16_t* dst_k, uint16_t* dst_v, const int32_t* dst_block_ta
         int64_t dst_block = dst_block_tables[(int64_t)b * dst_max_blocks_per_seq + j / ORC_BLOCK];
         if (src_block < 0 || src_block >= src_num_blocks) return ORC_ERR_BLOCK;
         if (dst_block < 0 || dst_block >= dst_num_blocks) return ORC_ERR_BLOCK;
-        int64_t src = ((src_block * num_kv_heads + g) * ORC_BLOCK + t % ORC_BLOCK) * head_dim;
-        int64_t dst = ((dst_block * num_kv_heads + g) * ORC_BLOCK + j % ORC_BLOCK) * head_dim;
-        for (int e = 0; e < head_dim; ++e) {
-          dst_k[dst + e] = src_k[src + e];
-          dst_v[dst + e] = src_v[src + e];
+        int64_t src = (src_block * num_kv_heads + g) * ORC_BLOCK + t % ORC_BLOCK;
+        int64_t dst = (dst_block * num_kv_heads + g) * ORC_BLOCK + j % ORC_BLOCK;
+        memcpy(dst_k + dst * row_bytes, src_k + src * row_bytes, row_bytes);
+        memcpy(dst_v + dst * row_bytes, src_v + src * row_bytes, row_bytes);
+        if (dst_ks) {
+          dst_ks[dst] = src_ks[src];
+          dst_vs[dst] = src_vs[src];
         }
       }
     }
   }
   return ORC_OK;
+}
+
+int oracle_compact(uint16_t* dst_k, uint16_t* dst_v, const int32_t* dst_block_tables,
+                   int64_t dst_num_blocks, int dst_max_blocks_per_seq, const uint16_t* src_k,
+                   const uint16_t* src_v, const int32_t* src_block_tables,
+                   const int32_t* context_lens, const int32_t* kept, const int32_t* kept_lens,
+                   int max_kept, int batch, int num_kv_heads, int head_dim,
+                   int64_t src_num_blocks, int src_max_blocks_per_seq) {
+  return compact_pools((unsigned char*)dst_k, (unsigned char*)dst_v, NULL, NULL, dst_block_tables,
+                       dst_num_blocks, dst_max_blocks_per_seq, (const unsigned char*)src_k,
+                       (const unsigned char*)src_v, NULL, NULL, src_block_tables, context_lens,
+                       kept, kept_lens, max_kept, batch, num_kv_heads, head_dim, src_num_blocks,
+                       src_max_blocks_per_seq, sizeof(uint16_t));
+}
+
+/*
+ * Compaction of INT8 pools: the kept rows' codes and their row scales move together, so the
+ * compact pool holds the same values (code * scale) at the new positions.
+ */
+int oracle_compact_q8(int8_t* dst_k, int8_t* dst_v, float* dst_ks, float* dst_vs,
+                      const int32_t* dst_block_tables, int64_t dst_num_blocks,
+                      int dst_max_blocks_per_seq, const int8_t* src_k, const int8_t* src_v,
+                      const float* src_ks, const float* src_vs, const int32_t* src_block_tables,
+                      const int32_t* context_lens, const int32_t* kept, const int32_t* kept_lens,
+                      int max_kept, int batch, int num_kv_heads, int head_dim,
+                      int64_t src_num_blocks, int src_max_blocks_per_seq) {
+  if (!dst_ks || !dst_vs || !src_ks || !src_vs) return ORC_ERR_ARG;
+  return compact_pools((unsigned char*)dst_k, (unsigned char*)dst_v, dst_ks, dst_vs,
+                       dst_block_tables, dst_num_blocks, dst_max_blocks_per_seq,
+                       (const unsigned char*)src_k, (const unsigned char*)src_v, src_ks, src_vs,
+                       src_block_tables, context_lens, kept, kept_lens, max_kept, batch,
+                       num_kv_heads, head_dim, src_num_blocks, src_max_blocks_per_seq, 1);
+}
+
+/*
+ * A K/V pool pair being written: bf16 elements, or INT8 codes with one fp32 scale per row.
+ * write_row stores one bf16 row of K and of V at row r (rows as in pool_t), quantizing them
+ * (quantize_row) for INT8 pools; a non-finite value leaves both rows unwritten.
+ */
+typedef struct {
+  uint16_t* k_bf16;
+  uint16_t* v_bf16;
+  int8_t* k_codes;
+  int8_t* v_codes;
+  float* k_scales;
+  float* v_scales;
+} wpool_t;
+
+static int write_row(const wpool_t* p, int64_t r, const uint16_t* k, const uint16_t* v,
+                     int head_dim) {
+  if (p->k_bf16) {
+    memcpy(p->k_bf16 + r * head_dim, k, (size_t)head_dim * sizeof(uint16_t));
+    memcpy(p->v_bf16 + r * head_dim, v, (size_t)head_dim * sizeof(uint16_t));
+    return ORC_OK;
+  }
+  int8_t* kc = (int8_t*)malloc((size_t)head_dim);
+  int8_t* vc = (int8_t*)malloc((size_t)head_dim);
+  float ks = 0.0f, vs = 0.0f;
+  int st = (kc && vc) ? ORC_OK : ORC_ERR_MEM;
+  if (st == ORC_OK) st = quantize_row(kc, &ks, k, head_dim);
+  if (st == ORC_OK) st = quantize_row(vc, &vs, v, head_dim);
+  if (st == ORC_OK) {
+    memcpy(p->k_codes + r * head_dim, kc, (size_t)head_dim);
+    memcpy(p->v_codes + r * head_dim, vc, (size_t)head_dim);
+    p->k_scales[r] = ks;
+    p->v_scales[r] = vs;
+  }
+  free(kc);
+  free(vc);
+  return st;
 }
 
 /*
@@ -700,11 +805,12 @@ int oracle_compact(uint16_t* dst_k, uint16_t* dst_v, const int32_t* dst_block_ta
  * The slot taken gets the new rows, position L_b - 1 and score 0; kept_lens[b] grows by one
  * while below capacity.  NaN scores, a missing leaving token or a bad block are refused.
  */
-int oracle_rolling_admit(uint16_t* k_cache, uint16_t* v_cache, const int32_t* block_tables,
-                         int64_t num_blocks, int max_blocks_per_seq, int32_t* slot_pos,
-                         float* slot_score, int32_t* kept_lens, const int32_t* context_lens,
-                         const uint16_t* k_new, const uint16_t* v_new, int batch,
-                         int num_kv_heads, int head_dim, int capacity, int n_sink, int n_recent) {
+static int rolling_admit_pools(const wpool_t* pool, const int32_t* block_tables,
+                               int64_t num_blocks, int max_blocks_per_seq, int32_t* slot_pos,
+                               float* slot_score, int32_t* kept_lens, const int32_t* context_lens,
+                               const uint16_t* k_new, const uint16_t* v_new, int batch,
+                               int num_kv_heads, int head_dim, int capacity, int n_sink,
+                               int n_recent) {
   if (batch < 0 || num_kv_heads <= 0 || head_dim <= 0 || capacity <= 0 || n_sink < 0 ||
       n_recent < 0 || n_sink + n_recent > capacity)
     return ORC_ERR_ARG;
@@ -736,16 +842,42 @@ int oracle_rolling_admit(uint16_t* k_cache, uint16_t* v_cache, const int32_t* bl
       if (logical_block >= max_blocks_per_seq) return ORC_ERR_INDEX;
       int64_t physical = block_tables[(int64_t)b * max_blocks_per_seq + logical_block];
       if (physical < 0 || physical >= num_blocks) return ORC_ERR_BLOCK;
-      int64_t dst = ((physical * num_kv_heads + g) * ORC_BLOCK + target % ORC_BLOCK) * head_dim;
+      int64_t row = (physical * num_kv_heads + g) * ORC_BLOCK + target % ORC_BLOCK;
       int64_t src = ((int64_t)b * num_kv_heads + g) * head_dim;
-      for (int e = 0; e < head_dim; ++e) {
-        k_cache[dst + e] = k_new[src + e];
-        v_cache[dst + e] = v_new[src + e];
-      }
+      int st = write_row(pool, row, k_new + src, v_new + src, head_dim);
+      if (st != ORC_OK) return st;
       pos[target] = (int32_t)(len - 1);
       score[target] = 0.0f;
     }
     if (!full) kept_lens[b] = used + 1;
   }
   return ORC_OK;
+}
+
+int oracle_rolling_admit(uint16_t* k_cache, uint16_t* v_cache, const int32_t* block_tables,
+                         int64_t num_blocks, int max_blocks_per_seq, int32_t* slot_pos,
+                         float* slot_score, int32_t* kept_lens, const int32_t* context_lens,
+                         const uint16_t* k_new, const uint16_t* v_new, int batch,
+                         int num_kv_heads, int head_dim, int capacity, int n_sink, int n_recent) {
+  wpool_t pool = {k_cache, v_cache, NULL, NULL, NULL, NULL};
+  return rolling_admit_pools(&pool, block_tables, num_blocks, max_blocks_per_seq, slot_pos,
+                             slot_score, kept_lens, context_lens, k_new, v_new, batch,
+                             num_kv_heads, head_dim, capacity, n_sink, n_recent);
+}
+
+/*
+ * Rolling admission into INT8 pools: the same choice of slot; the new token's K and V rows
+ * are quantized into it (codes and row scale, as oracle_kv_append_q8 does).
+ */
+int oracle_rolling_admit_q8(int8_t* k_codes, int8_t* v_codes, float* k_scales, float* v_scales,
+                            const int32_t* block_tables, int64_t num_blocks,
+                            int max_blocks_per_seq, int32_t* slot_pos, float* slot_score,
+                            int32_t* kept_lens, const int32_t* context_lens,
+                            const uint16_t* k_new, const uint16_t* v_new, int batch,
+                            int num_kv_heads, int head_dim, int capacity, int n_sink,
+                            int n_recent) {
+  wpool_t pool = {NULL, NULL, k_codes, v_codes, k_scales, v_scales};
+  return rolling_admit_pools(&pool, block_tables, num_blocks, max_blocks_per_seq, slot_pos,
+                             slot_score, kept_lens, context_lens, k_new, v_new, batch,
+                             num_kv_heads, head_dim, capacity, n_sink, n_recent);
 }

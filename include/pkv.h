@@ -271,6 +271,23 @@ int pkv_paged_decode_attention_scores(void* out, float* lse_out, float* score_ac
                                       int32_t* error_word, void* stream);
 
 /*
+ * pkv_paged_decode_attention_scores_q8 -- pkv_paged_decode_attention_scores over INT8 pools
+ * (no append: INT8 pools take this step's token through pkv_kv_append_q8 first).  Every K
+ * element is read as code * scale of its row for the logits, every V element likewise for the
+ * output, as pkv_paged_decode_attention_q8; the score, lse and logits outputs are those of
+ * pkv_paged_decode_attention_scores for the dequantized K.
+ *   k_codes, v_codes, k_scales, v_scales : as pkv_paged_decode_attention_q8.
+ *   other arguments : as pkv_paged_decode_attention_scores.  out is bit-identical to what
+ *                     pkv_paged_decode_attention_q8 writes for the same inputs and workspace size.
+ */
+int pkv_paged_decode_attention_scores_q8(void* out, float* lse_out, float* score_accum, float* logits,
+                                         int32_t score_stride, const void* q, const void* k_codes,
+                                         const void* v_codes, const float* k_scales, const float* v_scales,
+                                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                                         int32_t window, void* workspace, size_t workspace_bytes,
+                                         const pkv_dims* dims, int32_t* error_word, void* stream);
+
+/*
  * pkv_sparse_decode_workspace_bytes -- workspace for pkv_sparse_decode_attention with
  * kept lists of row length max_kept: the same size and rules as pkv_decode_workspace_bytes
  * (it does not depend on max_kept).  Returns 0 if the arguments are invalid.
@@ -342,6 +359,20 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
                    void* stream);
 
 /*
+ * pkv_kv_compact_q8 -- pkv_kv_compact over INT8 pools: each kept row's codes and its fp32 row
+ * scale move together, so the compact pool holds the same values (code * scale).
+ *   dst_k_codes, dst_v_codes, src_k_codes, src_v_codes : [NB, Hkv, 16, d] int8 pools.
+ *   dst_k_scales, dst_v_scales, src_k_scales, src_v_scales : [NB, Hkv, 16] fp32 row scales.
+ *   other arguments : as pkv_kv_compact.  All pool pointers 16-byte aligned.  Bit-exact.
+ */
+int pkv_kv_compact_q8(void* dst_k_codes, void* dst_v_codes, float* dst_k_scales, float* dst_v_scales,
+                      const int32_t* dst_block_tables, int32_t dst_num_blocks, int32_t dst_max_blocks_per_seq,
+                      const void* src_k_codes, const void* src_v_codes, const float* src_k_scales,
+                      const float* src_v_scales, const int32_t* src_block_tables, const int32_t* context_lens,
+                      const int32_t* kept_index_lists, const int32_t* kept_lens, int32_t max_kept,
+                      const pkv_dims* src_dims, int32_t* error_word, void* stream);
+
+/*
  * pkv_kv_rolling_admit -- admit one decode step's token into each sequence's sparse-layer cache
  * of fixed budget: capacity = n_sink + k_top + n_recent slots per (sequence, kv head) in a
  * compact pool (slot s at block block_tables[b][s / 16], offset s % 16).  The rolling form of
@@ -373,6 +404,23 @@ int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tabl
                          const int32_t* context_lens, const void* k_new, const void* v_new,
                          int32_t capacity, int32_t n_sink, int32_t n_recent, const pkv_dims* dims,
                          int32_t* error_word, void* stream);
+
+/*
+ * pkv_kv_rolling_admit_q8 -- pkv_kv_rolling_admit into INT8 pools: the same choice of slot,
+ * and the new token's K and V rows quantized into it by the row rule of pkv_kv_append_q8.
+ *   k_codes, v_codes   : [NB, Hkv, 16, d] int8 compact pools, updated in place.
+ *   k_scales, v_scales : [NB, Hkv, 16] fp32 row scales, updated in place.
+ *   other arguments    : as pkv_kv_rolling_admit.
+ *   error_word         : as pkv_kv_rolling_admit, plus PKV_DEV_BAD_VALUE for a (b, g) whose new K
+ *                        or V row holds a non-finite value (its rows, position and score are
+ *                        then left unchanged).
+ * All pool pointers 16-byte aligned.  Bit-exact.
+ */
+int pkv_kv_rolling_admit_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                            const int32_t* block_tables, int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
+                            const int32_t* context_lens, const void* k_new, const void* v_new, int32_t capacity,
+                            int32_t n_sink, int32_t n_recent, const pkv_dims* dims, int32_t* error_word,
+                            void* stream);
 
 /*
  * pkv_paged_decode_attention_fixed_scratch -- pkv_paged_decode_attention for callers that

@@ -24,6 +24,7 @@ __all__ = [
     "kv_append_q8",
     "paged_decode_attention_q8",
     "prefill_window_scores",
+    "paged_decode_attention_scores_q8", "kv_compact_q8", "kv_rolling_admit_q8",
 ]
 
 BLOCK_SIZE = 16
@@ -188,9 +189,7 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     return out
 
 
-def paged_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale,
-                              window=0, *, out=None, workspace=None, error_word=None, stream=None):
-    """paged_decode_attention over INT8 pools (each element code * its row's scale)."""
+def _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens):
     nb, hkv, d = _q8_pool_dims(k_codes, v_codes, k_scales, v_scales)
     dev = k_codes.device
     _need(q, "q", torch.bfloat16, 3, dev)
@@ -201,7 +200,13 @@ def paged_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tab
         raise ValueError("q head_dim differs from the pools'")
     if block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("block_tables / context_lens batch differs from q's")
-    dims = _dims(B, hq, hkv, d, nb, block_tables.shape[1])
+    return _dims(B, hq, hkv, d, nb, block_tables.shape[1]), dev
+
+
+def paged_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale,
+                              window=0, *, out=None, workspace=None, error_word=None, stream=None):
+    """paged_decode_attention over INT8 pools (each element code * its row's scale)."""
+    dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
     out, workspace = _out_ws(q, out, workspace, nbytes)
     check("pkv_paged_decode_attention_q8", load().pkv_paged_decode_attention_q8(
@@ -264,26 +269,13 @@ def paged_decode_attention_append(q, k_cache, v_cache, k_new, v_new, block_table
     return out
 
 
-def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_lens, scale, score_accum,
-                                  window=0, *, k_new=None, v_new=None, out=None, lse=None, logits=None,
-                                  workspace=None, error_word=None, stream=None):
-    """paged_decode_attention (with the step's append when k_new/v_new are given) that also
-    adds the step's sparsification score into score_accum [B, Hkv, S] fp32: for every attended
-    key t < S of (b, kv head g), the sum over g's query heads of their softmax probability of
-    t.  Returns (out [B, Hq, d] bf16, lse [B, Hq] fp32: each row's natural log-sum-exp).
-    logits [B, Hq, S] fp32 is scratch (allocated when not given)."""
-    dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+def _score_buffers(dims, dev, score_accum, lse, logits):
+    """Checks score_accum [B, Hkv, S]; returns (S, lse [B, Hq], logits [B, Hq, S]), allocating
+    the last two when not given."""
     _need(score_accum, "score_accum", torch.float32, 3, dev)
     if score_accum.shape[:2] != (dims.batch, dims.num_kv_heads):
         raise ValueError("score_accum must be [B, Hkv, S]")
     stride = score_accum.shape[2]
-    if (k_new is None) != (v_new is None):
-        raise ValueError("give both k_new and v_new, or neither")
-    if k_new is not None:
-        _need(k_new, "k_new", torch.bfloat16, 3, dev)
-        _need(v_new, "v_new", torch.bfloat16, 3, dev)
-        if k_new.shape != (dims.batch, dims.num_kv_heads, dims.head_dim) or v_new.shape != k_new.shape:
-            raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
     if lse is None:
         lse = torch.empty((dims.batch, dims.num_q_heads), dtype=torch.float32, device=dev)
     else:
@@ -296,6 +288,26 @@ def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_len
         _need(logits, "logits", torch.float32, 3, dev)
         if logits.shape != (dims.batch, dims.num_q_heads, stride):
             raise ValueError("logits must be [B, Hq, S]")
+    return stride, lse, logits
+
+
+def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_lens, scale, score_accum,
+                                  window=0, *, k_new=None, v_new=None, out=None, lse=None, logits=None,
+                                  workspace=None, error_word=None, stream=None):
+    """paged_decode_attention (with the step's append when k_new/v_new are given) that also
+    adds the step's sparsification score into score_accum [B, Hkv, S] fp32: for every attended
+    key t < S of (b, kv head g), the sum over g's query heads of their softmax probability of
+    t.  Returns (out [B, Hq, d] bf16, lse [B, Hq] fp32: each row's natural log-sum-exp).
+    logits [B, Hq, S] fp32 is scratch (allocated when not given)."""
+    dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    stride, lse, logits = _score_buffers(dims, dev, score_accum, lse, logits)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("give both k_new and v_new, or neither")
+    if k_new is not None:
+        _need(k_new, "k_new", torch.bfloat16, 3, dev)
+        _need(v_new, "v_new", torch.bfloat16, 3, dev)
+        if k_new.shape != (dims.batch, dims.num_kv_heads, dims.head_dim) or v_new.shape != k_new.shape:
+            raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
     out, workspace = _out_ws(q, out, workspace, nbytes)
     check("pkv_paged_decode_attention_scores", load().pkv_paged_decode_attention_scores(
@@ -306,6 +318,22 @@ def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_len
     return out, lse
 
 
+def paged_decode_attention_scores_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale,
+                                     score_accum, window=0, *, out=None, lse=None, logits=None, workspace=None,
+                                     error_word=None, stream=None):
+    """paged_decode_attention_scores over INT8 pools (no append: INT8 pools take the step's
+    token through kv_append_q8).  Returns (out, lse) as paged_decode_attention_scores."""
+    dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
+    stride, lse, logits = _score_buffers(dims, dev, score_accum, lse, logits)
+    nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
+    out, workspace = _out_ws(q, out, workspace, nbytes)
+    check("pkv_paged_decode_attention_scores_q8", load().pkv_paged_decode_attention_scores_q8(
+        _ptr(out), _ptr(lse), _ptr(score_accum), _ptr(logits), int(stride), _ptr(q), _ptr(k_codes), _ptr(v_codes),
+        _ptr(k_scales), _ptr(v_scales), _ptr(block_tables), _ptr(context_lens), float(scale), int(window),
+        _ptr(workspace), workspace.numel(), ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+    return out, lse
+
+
 def kv_rolling_admit(k_cache, v_cache, block_tables, slot_pos, slot_score, kept_lens, context_lens, k_new,
                      v_new, n_sink, n_recent, *, error_word=None, stream=None):
     """Admit this step's token (k_new/v_new [B, Hkv, d], position context_lens[b] - 1) into each
@@ -313,7 +341,28 @@ def kv_rolling_admit(k_cache, v_cache, block_tables, slot_pos, slot_score, kept_
     slot_pos [B, Hkv, C] int32 and slot_score [B, Hkv, C] fp32 (C = n_sink + k_top + n_recent
     slots) and kept_lens [B] int32, all updated in place.  See pkv_kv_rolling_admit."""
     nb, hkv, d = _pool_dims(k_cache, v_cache)
-    dev = k_cache.device
+    dims = _rolling_dims(nb, hkv, d, k_cache.device, block_tables, slot_pos, slot_score, kept_lens, context_lens,
+                         k_new, v_new)
+    check("pkv_kv_rolling_admit", load().pkv_kv_rolling_admit(
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(slot_pos), _ptr(slot_score), _ptr(kept_lens),
+        _ptr(context_lens), _ptr(k_new), _ptr(v_new), slot_pos.shape[2], int(n_sink), int(n_recent),
+        ctypes.byref(dims), _ptr(error_word), _stream(stream, k_cache.device)))
+
+
+def kv_rolling_admit_q8(k_codes, v_codes, k_scales, v_scales, block_tables, slot_pos, slot_score, kept_lens,
+                        context_lens, k_new, v_new, n_sink, n_recent, *, error_word=None, stream=None):
+    """kv_rolling_admit into INT8 compact pools (codes [NB, Hkv, 16, d] int8, row scales
+    [NB, Hkv, 16] fp32): the same slot choice, the new rows quantized into the slot."""
+    nb, hkv, d = _q8_pool_dims(k_codes, v_codes, k_scales, v_scales)
+    dims = _rolling_dims(nb, hkv, d, k_codes.device, block_tables, slot_pos, slot_score, kept_lens, context_lens,
+                         k_new, v_new)
+    check("pkv_kv_rolling_admit_q8", load().pkv_kv_rolling_admit_q8(
+        _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_tables), _ptr(slot_pos),
+        _ptr(slot_score), _ptr(kept_lens), _ptr(context_lens), _ptr(k_new), _ptr(v_new), slot_pos.shape[2],
+        int(n_sink), int(n_recent), ctypes.byref(dims), _ptr(error_word), _stream(stream, k_codes.device)))
+
+
+def _rolling_dims(nb, hkv, d, dev, block_tables, slot_pos, slot_score, kept_lens, context_lens, k_new, v_new):
     _need(block_tables, "block_tables", torch.int32, 2, dev)
     _need(slot_pos, "slot_pos", torch.int32, 3, dev)
     _need(slot_score, "slot_score", torch.float32, 3, dev)
@@ -328,11 +377,7 @@ def kv_rolling_admit(k_cache, v_cache, block_tables, slot_pos, slot_score, kept_
         raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
     if block_tables.shape[0] != B or kept_lens.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("block_tables / kept_lens / context_lens batch differs")
-    dims = _dims(B, 1, hkv, d, nb, block_tables.shape[1])
-    check("pkv_kv_rolling_admit", load().pkv_kv_rolling_admit(
-        _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(slot_pos), _ptr(slot_score), _ptr(kept_lens),
-        _ptr(context_lens), _ptr(k_new), _ptr(v_new), slot_pos.shape[2], int(n_sink), int(n_recent),
-        ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+    return _dims(B, 1, hkv, d, nb, block_tables.shape[1])
 
 
 def paged_decode_attention_fixed_scratch(q, k_cache, v_cache, block_tables, context_lens, scale,
@@ -429,3 +474,30 @@ def kv_compact(dst_k_cache, dst_v_cache, dst_block_tables, src_k_cache, src_v_ca
         _ptr(src_k_cache), _ptr(src_v_cache), _ptr(src_block_tables), _ptr(context_lens),
         _ptr(kept_index_lists), _ptr(kept_lens), kept_index_lists.shape[2], ctypes.byref(dims),
         _ptr(error_word), _stream(stream, dev)))
+
+
+def kv_compact_q8(dst_k_codes, dst_v_codes, dst_k_scales, dst_v_scales, dst_block_tables, src_k_codes,
+                  src_v_codes, src_k_scales, src_v_scales, src_block_tables, context_lens, kept_index_lists,
+                  kept_lens, *, error_word=None, stream=None):
+    """kv_compact over INT8 pools: each kept row's codes and row scale move together."""
+    snb, hkv, d = _q8_pool_dims(src_k_codes, src_v_codes, src_k_scales, src_v_scales)
+    dnb, dhkv, dd = _q8_pool_dims(dst_k_codes, dst_v_codes, dst_k_scales, dst_v_scales)
+    if (dhkv, dd) != (hkv, d):
+        raise ValueError("source and destination pools differ in heads or head_dim")
+    dev = src_k_codes.device
+    if dst_k_codes.device != dev:
+        raise ValueError("source and destination pools are on different devices")
+    _need(dst_block_tables, "dst_block_tables", torch.int32, 2, dev)
+    _need(src_block_tables, "src_block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(kept_index_lists, "kept_index_lists", torch.int32, 3, dev)
+    _need(kept_lens, "kept_lens", torch.int32, 1, dev)
+    B = kept_index_lists.shape[0]
+    if kept_index_lists.shape[1] != hkv:
+        raise ValueError("kept_index_lists must be [B, Hkv, max_kept]")
+    dims = _dims(B, hkv, hkv, d, snb, src_block_tables.shape[1])
+    check("pkv_kv_compact_q8", load().pkv_kv_compact_q8(
+        _ptr(dst_k_codes), _ptr(dst_v_codes), _ptr(dst_k_scales), _ptr(dst_v_scales), _ptr(dst_block_tables), dnb,
+        dst_block_tables.shape[1], _ptr(src_k_codes), _ptr(src_v_codes), _ptr(src_k_scales), _ptr(src_v_scales),
+        _ptr(src_block_tables), _ptr(context_lens), _ptr(kept_index_lists), _ptr(kept_lens),
+        kept_index_lists.shape[2], ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))

@@ -23,8 +23,8 @@ constexpr int kNumGroups = 1;
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
-  size_t max_dyn_smem[2][4] = {};  // [head_dim index][mode: dense, sparse, dense + scores,
-                                   //   dense INT8]: opt-in minus the kernel's static shared memory
+  size_t max_dyn_smem[2][5] = {};  // [head_dim index][mode: dense, sparse, dense + scores,
+                                   //   dense INT8, INT8 + scores]: opt-in minus static shared memory
   int merge_ctas_per_sm[2] = {};   // [head_dim index]: resident merge CTAs per SM
 };
 
@@ -55,8 +55,9 @@ const DeviceInfo* device_info(int* status) {
     }
     for (int hd = 0; hd < kNumHeadDims; ++hd) {
       for (int gi = 0; gi < kNumGroups; ++gi) {
-        for (int sp = 0; sp < 4; ++sp) {
-          const DecodeKernel k = decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp == 1, sp == 2, sp == 3);
+        for (int sp = 0; sp < 5; ++sp) {
+          const DecodeKernel k =
+              decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp == 1, sp == 2 || sp == 4, sp >= 3);
           if (k.split == nullptr) continue;
           cudaFuncAttributes fa{};
           cudaError_t e = cudaFuncGetAttributes(&fa, k.split);
@@ -252,7 +253,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
     return PKV_ERR_ALIGNMENT;
   const int group = dims->num_q_heads / dims->num_kv_heads;
   if (q8 != nullptr) {
-    if (sparse || score_out != nullptr || k_new != nullptr) return PKV_ERR_ARGUMENT;
+    if (sparse || k_new != nullptr) return PKV_ERR_ARGUMENT;
     if (!q8->k_scale || !q8->v_scale) return PKV_ERR_NULL_POINTER;
     if (!aligned16(q8->k_scale) || !aligned16(q8->v_scale)) return PKV_ERR_ALIGNMENT;
   }
@@ -278,7 +279,8 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   const DeviceInfo* info = device_info(&st);
   if (!info) return st;
   const size_t smem = decode_smem_bytes(dims->head_dim, sparse, dims->batch);
-  if (smem > info->max_dyn_smem[head_dim_index(dims->head_dim)][sparse ? 1 : (score_out ? 2 : (q8 ? 3 : 0))])
+  const int mode = sparse ? 1 : (q8 ? (score_out ? 4 : 3) : (score_out ? 2 : 0));
+  if (smem > info->max_dyn_smem[head_dim_index(dims->head_dim)][mode])
     return PKV_ERR_DIMS;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.split, kDecodeWarps * 32, smem);
@@ -491,6 +493,19 @@ int pkv_paged_decode_attention_scores(void* out, float* lse_out, float* score_ac
                        k_new, v_new, &so);
 }
 
+int pkv_paged_decode_attention_scores_q8(void* out, float* lse_out, float* score_accum, float* logits,
+                                         int32_t score_stride, const void* q, const void* k_codes,
+                                         const void* v_codes, const float* k_scales, const float* v_scales,
+                                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                                         int32_t window, void* workspace, size_t workspace_bytes,
+                                         const pkv_dims* dims, int32_t* error_word, void* stream) {
+  const ScoreOutputs so{lse_out, score_accum, logits, score_stride};
+  const Q8Scales q8{k_scales, v_scales};
+  return decode_common(out, q, k_codes, v_codes, block_tables, context_lens, nullptr, nullptr, 0, scale,
+                       window, workspace, workspace_bytes, dims, error_word, stream, false, nullptr, nullptr,
+                       &so, &q8);
+}
+
 size_t pkv_sparse_decode_workspace_bytes(const pkv_dims* dims, int32_t max_kept) {
   if (max_kept <= 0) return 0;
   return pkv_decode_workspace_bytes(dims);
@@ -552,6 +567,31 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
                                        static_cast<cudaStream_t>(stream)));
 }
 
+int pkv_kv_compact_q8(void* dst_k_codes, void* dst_v_codes, float* dst_k_scales, float* dst_v_scales,
+                      const int32_t* dst_block_tables, int32_t dst_num_blocks, int32_t dst_max_blocks_per_seq,
+                      const void* src_k_codes, const void* src_v_codes, const float* src_k_scales,
+                      const float* src_v_scales, const int32_t* src_block_tables, const int32_t* context_lens,
+                      const int32_t* kept_index_lists, const int32_t* kept_lens, int32_t max_kept,
+                      const pkv_dims* src_dims, int32_t* error_word, void* stream) {
+  int st = check_dims(src_dims, false);
+  if (st != PKV_OK) return st;
+  if (dst_num_blocks < 0 || dst_max_blocks_per_seq < 0 || max_kept < 0) return PKV_ERR_DIMS;
+  if (src_dims->batch == 0 || max_kept == 0) return PKV_OK;
+  if (!dst_k_codes || !dst_v_codes || !dst_k_scales || !dst_v_scales || !dst_block_tables || !src_k_codes ||
+      !src_v_codes || !src_k_scales || !src_v_scales || !src_block_tables || !context_lens || !kept_index_lists ||
+      !kept_lens)
+    return PKV_ERR_NULL_POINTER;
+  if (!aligned16(dst_k_codes) || !aligned16(dst_v_codes) || !aligned16(src_k_codes) || !aligned16(src_v_codes) ||
+      !aligned16(dst_k_scales) || !aligned16(dst_v_scales) || !aligned16(src_k_scales) || !aligned16(src_v_scales))
+    return PKV_ERR_ALIGNMENT;
+  if (!device_info(&st)) return st;
+  return cuda_status(launch_kv_compact_q8(
+      dst_k_codes, dst_v_codes, dst_k_scales, dst_v_scales, dst_block_tables, dst_num_blocks, dst_max_blocks_per_seq,
+      src_k_codes, src_v_codes, src_k_scales, src_v_scales, src_block_tables, context_lens, kept_index_lists,
+      kept_lens, max_kept, src_dims->batch, src_dims->num_kv_heads, src_dims->head_dim, src_dims->num_blocks,
+      src_dims->max_blocks_per_seq, error_word, static_cast<cudaStream_t>(stream)));
+}
+
 int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tables,
                          int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
                          const int32_t* context_lens, const void* k_new, const void* v_new,
@@ -572,6 +612,30 @@ int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tabl
   return cuda_status(launch_kv_rolling_admit(
       k_cache, v_cache, block_tables, dims->num_blocks, dims->max_blocks_per_seq, slot_pos, slot_score,
       kept_lens, context_lens, k_new, v_new, dims->batch, dims->num_kv_heads, dims->head_dim, capacity,
+      n_sink, n_recent, error_word, static_cast<cudaStream_t>(stream)));
+}
+
+int pkv_kv_rolling_admit_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                            const int32_t* block_tables, int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
+                            const int32_t* context_lens, const void* k_new, const void* v_new, int32_t capacity,
+                            int32_t n_sink, int32_t n_recent, const pkv_dims* dims, int32_t* error_word,
+                            void* stream) {
+  int st = check_dims(dims, false);
+  if (st != PKV_OK) return st;
+  if (capacity <= 0 || n_sink < 0 || n_recent < 0 || (long long)n_sink + n_recent > capacity)
+    return PKV_ERR_ARGUMENT;
+  if ((long long)capacity > (long long)dims->max_blocks_per_seq * PKV_BLOCK_SIZE) return PKV_ERR_DIMS;
+  if (dims->batch == 0) return PKV_OK;
+  if (!k_codes || !v_codes || !k_scales || !v_scales || !block_tables || !slot_pos || !slot_score || !kept_lens ||
+      !context_lens || !k_new || !v_new)
+    return PKV_ERR_NULL_POINTER;
+  if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales) ||
+      !aligned16(k_new) || !aligned16(v_new))
+    return PKV_ERR_ALIGNMENT;
+  if (!device_info(&st)) return st;
+  return cuda_status(launch_kv_rolling_admit_q8(
+      k_codes, v_codes, k_scales, v_scales, block_tables, dims->num_blocks, dims->max_blocks_per_seq, slot_pos,
+      slot_score, kept_lens, context_lens, k_new, v_new, dims->batch, dims->num_kv_heads, dims->head_dim, capacity,
       n_sink, n_recent, error_word, static_cast<cudaStream_t>(stream)));
 }
 

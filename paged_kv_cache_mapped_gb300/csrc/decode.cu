@@ -264,7 +264,7 @@ template <int D, bool SPARSE, bool SCORES, bool Q8>
 __global__ void __launch_bounds__(kDecodeWarps * 32, Q8 ? PKV_Q8_MIN_CTAS : 0)
 decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   static_assert(!(SPARSE && SCORES), "scores are emitted by the dense decode only");
-  static_assert(!(Q8 && (SPARSE || SCORES)), "INT8 pools are read by the plain dense decode only");
+  static_assert(!(Q8 && SPARSE), "INT8 pools are read by the dense decode only");
   using GE = Geo<D, SPARSE, Q8>;
   using WT = WarpTiles<D, SPARSE, Q8>;
   using WB = WarpSlots<D, SPARSE, Q8>;
@@ -1134,16 +1134,18 @@ __global__ void __launch_bounds__(kScoreThreads) decode_score_kernel(const Decod
 
 DecodeKernel decode_kernel(int head_dim, int group, bool sparse, bool scores, bool q8) {
   const DecodeKernel none{nullptr, nullptr, nullptr, head_dim, group, sparse, scores, q8};
-  if (group < 1 || group > kMaxGroup || (sparse && scores) || (q8 && (sparse || scores))) return none;
+  if (group < 1 || group > kMaxGroup || (sparse && (scores || q8))) return none;
   const void* score = scores ? (const void*)decode_score_kernel : nullptr;
   if (head_dim == 128)
-    return DecodeKernel{q8       ? (const void*)decode_split_kernel<128, false, false, true>
+    return DecodeKernel{q8 ? (scores ? (const void*)decode_split_kernel<128, false, true, true>
+                                     : (const void*)decode_split_kernel<128, false, false, true>)
                         : sparse ? (const void*)decode_split_kernel<128, true, false, false>
                         : scores ? (const void*)decode_split_kernel<128, false, true, false>
                                  : (const void*)decode_split_kernel<128, false, false, false>,
                         (const void*)decode_merge_kernel<128>, score, 128, group, sparse, scores, q8};
   if (head_dim == 64)
-    return DecodeKernel{q8       ? (const void*)decode_split_kernel<64, false, false, true>
+    return DecodeKernel{q8 ? (scores ? (const void*)decode_split_kernel<64, false, true, true>
+                                     : (const void*)decode_split_kernel<64, false, false, true>)
                         : sparse ? (const void*)decode_split_kernel<64, true, false, false>
                         : scores ? (const void*)decode_split_kernel<64, false, true, false>
                                  : (const void*)decode_split_kernel<64, false, false, false>,

@@ -142,6 +142,17 @@ cudaError_t launch_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t*
                                     const int32_t* lens, const void* k_new, const void* v_new, int B,
                                     int Hkv, int D, int capacity, int n_sink, int n_recent, int32_t* err,
                                     cudaStream_t stream);
+// INT8 pools: codes [NB, Hkv, 16, D] int8 with row scales [NB, Hkv, 16] fp32 moving with them.
+cudaError_t launch_kv_compact_q8(void* dk, void* dv, float* dks, float* dvs, const int32_t* dbt, int dNB,
+                                 int dMB, const void* sk, const void* sv, const float* sks, const float* svs,
+                                 const int32_t* sbt, const int32_t* lens, const int32_t* kept,
+                                 const int32_t* kept_lens, int max_kept, int B, int Hkv, int D, int sNB,
+                                 int sMB, int32_t* err, cudaStream_t stream);
+cudaError_t launch_kv_rolling_admit_q8(void* k_cache, void* v_cache, float* k_scales, float* v_scales,
+                                       const int32_t* bt, int NB, int MB, int32_t* slot_pos, float* slot_score,
+                                       int32_t* kept_lens, const int32_t* lens, const void* k_new,
+                                       const void* v_new, int B, int Hkv, int D, int capacity, int n_sink,
+                                       int n_recent, int32_t* err, cudaStream_t stream);
 cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* scores,
                                int stride, const int32_t* lens, int B, int Hkv, int n_sink,
                                int n_recent, int k_top, int32_t* err, cudaStream_t stream);

@@ -48,35 +48,20 @@ __global__ void __launch_bounds__(256) kv_append_kernel(__nv_bfloat16* __restric
   else copy_row_half<D>(vc + dst, v + src, lane - 16);
 }
 
-// INT8 append: the new token's K and V rows quantized into INT8 pools (the KV-cache primer's
-// INT8 cache, section 4.2).  Each (token, kv head) row of d values gets one fp32 scale
-// s = max|x| / 127 and codes round_half_even(x / s), clamped to [-127, 127]; a zero row gets
-// s = 0 and codes 0.  The division and rounding are IEEE single precision (they decide the
-// codes).  One warp per (token, kv head): lanes 0-15 quantize the K row, lanes 16-31 the V
-// row, D/16 elements each.  A non-finite element skips the token's rows and is reported.
+// INT8 row rule (the KV-cache primer's INT8 cache, section 4.2): each (token, kv head) row of
+// d values gets one fp32 scale s = max|x| / 127 and codes round_half_even(x / s), clamped to
+// [-127, 127]; a zero row gets s = 0 and codes 0.  The division and rounding are IEEE single
+// precision (they decide the codes).  A warp quantizes one token's K row (lanes 0-15) and V
+// row (lanes 16-31), D/16 elements a lane, and stores codes and scales at the given rows; if
+// either row holds a non-finite value it stores nothing and returns false.  Every lane of the
+// warp calls it.
 template <int D>
-__global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ kq, int8_t* __restrict__ vq,
-                                                           float* __restrict__ ks, float* __restrict__ vs,
-                                                           const __nv_bfloat16* __restrict__ k,
-                                                           const __nv_bfloat16* __restrict__ v,
-                                                           const int64_t* __restrict__ slots, int64_t T,
-                                                           int Hkv, int NB, int32_t* err) {
+__device__ __forceinline__ bool quantize_kv_rows(int8_t* kq_row, int8_t* vq_row, float* ks_at, float* vs_at,
+                                                 const __nv_bfloat16* k_src, const __nv_bfloat16* v_src,
+                                                 int lane) {
   constexpr int E = D / 16;  // elements per lane
-  const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  grid_dependency_wait();
-  grid_launch_dependents();
-  if (item >= T * Hkv) return;
-  const int64_t tok = item / Hkv;
-  const int g = (int)(item - tok * Hkv);
-  const int64_t slot = __ldg(slots + tok);
-  if (slot < 0) return;
-  if (slot >= (int64_t)NB * 16) {
-    if (lane == 0) record_error(err, PKV_DEV_BAD_SLOT);
-    return;
-  }
   const int h = lane & 15;
-  const __nv_bfloat16* src = (lane < 16 ? k : v) + ((size_t)tok * Hkv + g) * D + h * E;
+  const __nv_bfloat16* src = (lane < 16 ? k_src : v_src) + h * E;
   float x[E];
   if constexpr (E == 8) {
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
@@ -104,10 +89,7 @@ __global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ 
   }
 #pragma unroll
   for (int m = 1; m < 16; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));  // within the half
-  if (!__all_sync(kFullMask, finite)) {
-    if (lane == 0) record_error(err, PKV_DEV_BAD_VALUE);
-    return;
-  }
+  if (!__all_sync(kFullMask, finite)) return false;
   const float sc = __fdiv_rn(amax, 127.0f);
   uint32_t packed[E / 4];
 #pragma unroll
@@ -118,23 +100,67 @@ __global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ 
     if (sc != 0.f) c = max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], sc))));
     packed[i / 4] |= (uint32_t)(c & 0xff) << (8 * (i % 4));
   }
-  const size_t row = ((size_t)(slot >> 4) * Hkv + g) * 16 + (size_t)(slot & 15);
-  int8_t* dst = (lane < 16 ? kq : vq) + row * D + h * E;
+  int8_t* dst = (lane < 16 ? kq_row : vq_row) + h * E;
   if constexpr (E == 8)
     *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
   else
     *reinterpret_cast<uint32_t*>(dst) = packed[0];
-  if (h == 0) (lane < 16 ? ks : vs)[row] = sc;
+  if (h == 0) *(lane < 16 ? ks_at : vs_at) = sc;
+  return true;
+}
+
+// INT8 append: the new token's K and V rows quantized into INT8 pools by the row rule above.
+// One warp per (token, kv head).  A non-finite element skips the token's rows and is reported.
+template <int D>
+__global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ kq, int8_t* __restrict__ vq,
+                                                           float* __restrict__ ks, float* __restrict__ vs,
+                                                           const __nv_bfloat16* __restrict__ k,
+                                                           const __nv_bfloat16* __restrict__ v,
+                                                           const int64_t* __restrict__ slots, int64_t T,
+                                                           int Hkv, int NB, int32_t* err) {
+  const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (item >= T * Hkv) return;
+  const int64_t tok = item / Hkv;
+  const int g = (int)(item - tok * Hkv);
+  const int64_t slot = __ldg(slots + tok);
+  if (slot < 0) return;
+  if (slot >= (int64_t)NB * 16) {
+    if (lane == 0) record_error(err, PKV_DEV_BAD_SLOT);
+    return;
+  }
+  const size_t row = ((size_t)(slot >> 4) * Hkv + g) * 16 + (size_t)(slot & 15);
+  const size_t src = ((size_t)tok * Hkv + g) * D;
+  if (!quantize_kv_rows<D>(kq + row * D, vq + row * D, ks + row, vs + row, k + src, v + src, lane) && lane == 0)
+    record_error(err, PKV_DEV_BAD_VALUE);
+}
+
+// Copies one row of RB bytes with a half-warp: lane r of the half moves RB/16 bytes.
+template <int RB>
+__device__ __forceinline__ void copy_bytes_half(unsigned char* dst, const unsigned char* src, int r) {
+  if constexpr (RB == 256) {
+    reinterpret_cast<uint4*>(dst)[r] = __ldg(reinterpret_cast<const uint4*>(src) + r);
+  } else if constexpr (RB == 128) {
+    reinterpret_cast<uint2*>(dst)[r] = __ldg(reinterpret_cast<const uint2*>(src) + r);
+  } else {
+    static_assert(RB == 64, "rows of 64, 128 or 256 bytes");
+    reinterpret_cast<uint32_t*>(dst)[r] = __ldg(reinterpret_cast<const uint32_t*>(src) + r);
+  }
 }
 
 // Compaction: compact position j of (b, g) <- source token kept[b][g][j] (the per-layer
 // block-table policy of "How KV Sparsity Achieves 1.5x Acceleration for vLLM", section "Key
-// technique 1").  One warp per (b, g, j).
-template <int D>
+// technique 1").  One warp per (b, g, j): lanes 0-15 move the K row, 16-31 the V row, RB
+// bytes each (bf16 rows of 2d bytes, or INT8 rows of d bytes whose fp32 row scales move with
+// them when SCALES).
+template <int RB, bool SCALES>
 __global__ void __launch_bounds__(256) kv_compact_kernel(
-    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, const int32_t* __restrict__ dbt,
-    int dNB, int dMB, const __nv_bfloat16* __restrict__ sk, const __nv_bfloat16* __restrict__ sv,
-    const int32_t* __restrict__ sbt, const int32_t* __restrict__ lens,
+    unsigned char* __restrict__ dk, unsigned char* __restrict__ dv, float* __restrict__ dks,
+    float* __restrict__ dvs, const int32_t* __restrict__ dbt, int dNB, int dMB,
+    const unsigned char* __restrict__ sk, const unsigned char* __restrict__ sv, const float* __restrict__ sks,
+    const float* __restrict__ svs, const int32_t* __restrict__ sbt, const int32_t* __restrict__ lens,
     const int32_t* __restrict__ kept, const int32_t* __restrict__ kept_lens, int max_kept, int B,
     int Hkv, int sNB, int sMB, int32_t* err) {
   const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -164,10 +190,14 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
     if (lane == 0) record_error(err, PKV_DEV_BAD_BLOCK_ID);
     return;
   }
-  const size_t src = (((size_t)src_blk * Hkv + g) * 16 + (t & 15)) * D;
-  const size_t dst = (((size_t)dst_blk * Hkv + g) * 16 + (j & 15)) * D;
-  if (lane < 16) copy_row_half<D>(dk + dst, sk + src, lane);
-  else copy_row_half<D>(dv + dst, sv + src, lane - 16);
+  const size_t src = ((size_t)src_blk * Hkv + g) * 16 + (t & 15);
+  const size_t dst = ((size_t)dst_blk * Hkv + g) * 16 + (j & 15);
+  if (lane < 16) copy_bytes_half<RB>(dk + dst * RB, sk + src * RB, lane);
+  else copy_bytes_half<RB>(dv + dst * RB, sv + src * RB, lane - 16);
+  if constexpr (SCALES) {
+    if (lane == 0) dks[dst] = __ldg(sks + src);
+    if (lane == 16) dvs[dst] = __ldg(svs + src);
+  }
 }
 
 // ---------------------------------------------------------------------------- top-k select
@@ -363,14 +393,16 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
 // token is; the new token takes the dropped slot with score 0.  One CTA per sequence, a warp
 // per kv head: the warp scans the slots (lane-strided), reduces the leaving slot and the
 // weakest (score, position) pair across its lanes, then copies the rows (lanes 0-15 K,
-// 16-31 V).  The slot count is updated after every head is done.
+// 16-31 V; with Q8 the rows are quantized into INT8 pools by the row rule of the INT8 append,
+// and a non-finite row leaves its (b, g) unchanged).  The slot count is updated after every
+// head is done.
 constexpr int kAdmitWarps = 8;
 constexpr int kAdmitUnroll = 4;  // 16-byte slot loads in flight per lane and per array
 
-template <int D>
+template <int D, bool Q8>
 __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
-    __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc, const int32_t* __restrict__ bt,
-    int NB, int MB, int32_t* __restrict__ slot_pos, float* __restrict__ slot_score,
+    void* __restrict__ kc, void* __restrict__ vc, float* __restrict__ ks, float* __restrict__ vs,
+    const int32_t* __restrict__ bt, int NB, int MB, int32_t* __restrict__ slot_pos, float* __restrict__ slot_score,
     int32_t* __restrict__ kept_lens, const int32_t* __restrict__ lens, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, int Hkv, int capacity, int n_sink, int n_recent, int32_t* err) {
   const int b = blockIdx.x;
@@ -450,17 +482,25 @@ __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
       } else {
         target = (s_min >= 0 && score[s_out] > x_min) ? s_min : s_out;
       }
+      __syncwarp();  // every lane has read the scores before lane 0 overwrites one
     }
     if (ok) {
       const int blk = target / 16 < MB ? bt[(size_t)b * MB + target / 16] : -1;
       if (blk < 0 || blk >= NB) {
         if (lane == 0) record_error(err, PKV_DEV_BAD_BLOCK_ID);
       } else {
-        const size_t dst = (((size_t)blk * Hkv + g) * 16 + (target & 15)) * D;
+        const size_t row = ((size_t)blk * Hkv + g) * 16 + (target & 15);
         const size_t src = ((size_t)b * Hkv + g) * D;
-        if (lane < 16) copy_row_half<D>(kc + dst, k_new + src, lane);
-        else copy_row_half<D>(vc + dst, v_new + src, lane - 16);
-        if (lane == 0) {
+        bool written = true;
+        if constexpr (Q8) {
+          written = quantize_kv_rows<D>(static_cast<int8_t*>(kc) + row * D, static_cast<int8_t*>(vc) + row * D,
+                                        ks + row, vs + row, k_new + src, v_new + src, lane);
+          if (!written && lane == 0) record_error(err, PKV_DEV_BAD_VALUE);
+        } else {
+          if (lane < 16) copy_row_half<D>(static_cast<__nv_bfloat16*>(kc) + row * D, k_new + src, lane);
+          else copy_row_half<D>(static_cast<__nv_bfloat16*>(vc) + row * D, v_new + src, lane - 16);
+        }
+        if (written && lane == 0) {
           pos[target] = L - 1;
           score[target] = 0.f;
         }
@@ -514,16 +554,28 @@ cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, i
                               const int32_t* lens, const int32_t* kept, const int32_t* kept_lens,
                               int max_kept, int B, int Hkv, int D, int sNB, int sMB,
                               int32_t* err, cudaStream_t stream) {
+  return launch_kv_compact_q8(dk, dv, nullptr, nullptr, dbt, dNB, dMB, sk, sv, nullptr, nullptr, sbt, lens,
+                              kept, kept_lens, max_kept, B, Hkv, D, sNB, sMB, err, stream);
+}
+
+cudaError_t launch_kv_compact_q8(void* dk, void* dv, float* dks, float* dvs, const int32_t* dbt, int dNB,
+                                 int dMB, const void* sk, const void* sv, const float* sks, const float* svs,
+                                 const int32_t* sbt, const int32_t* lens, const int32_t* kept,
+                                 const int32_t* kept_lens, int max_kept, int B, int Hkv, int D, int sNB,
+                                 int sMB, int32_t* err, cudaStream_t stream) {
   const int64_t warps = (int64_t)B * Hkv * max_kept;
   if (warps == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
-  auto* a = static_cast<__nv_bfloat16*>(dk);
-  auto* c = static_cast<__nv_bfloat16*>(dv);
-  auto* s1 = static_cast<const __nv_bfloat16*>(sk);
-  auto* s2 = static_cast<const __nv_bfloat16*>(sv);
-  void* args[] = {&a, &c, &dbt, &dNB, &dMB, &s1, &s2, &sbt, &lens, &kept, &kept_lens,
+  auto* a = static_cast<unsigned char*>(dk);
+  auto* c = static_cast<unsigned char*>(dv);
+  auto* s1 = static_cast<const unsigned char*>(sk);
+  auto* s2 = static_cast<const unsigned char*>(sv);
+  void* args[] = {&a, &c, &dks, &dvs, &dbt, &dNB, &dMB, &s1, &s2, &sks, &svs, &sbt, &lens, &kept, &kept_lens,
                   &max_kept, &B, &Hkv, &sNB, &sMB, &err};
-  const void* fn = D == 128 ? (const void*)kv_compact_kernel<128> : (const void*)kv_compact_kernel<64>;
+  const bool q8 = dks != nullptr;
+  const void* fn = q8 ? (D == 128 ? (const void*)kv_compact_kernel<128, true> : (const void*)kv_compact_kernel<64, true>)
+                      : (D == 128 ? (const void*)kv_compact_kernel<256, false>
+                                  : (const void*)kv_compact_kernel<128, false>);
   return launch_pdl(fn, dim3(grid), dim3(256), 0, stream, args);
 }
 
@@ -543,14 +595,26 @@ cudaError_t launch_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t*
                                     const int32_t* lens, const void* k_new, const void* v_new, int B,
                                     int Hkv, int D, int capacity, int n_sink, int n_recent, int32_t* err,
                                     cudaStream_t stream) {
+  return launch_kv_rolling_admit_q8(k_cache, v_cache, nullptr, nullptr, bt, NB, MB, slot_pos, slot_score,
+                                    kept_lens, lens, k_new, v_new, B, Hkv, D, capacity, n_sink, n_recent, err,
+                                    stream);
+}
+
+cudaError_t launch_kv_rolling_admit_q8(void* k_cache, void* v_cache, float* k_scales, float* v_scales,
+                                       const int32_t* bt, int NB, int MB, int32_t* slot_pos, float* slot_score,
+                                       int32_t* kept_lens, const int32_t* lens, const void* k_new,
+                                       const void* v_new, int B, int Hkv, int D, int capacity, int n_sink,
+                                       int n_recent, int32_t* err, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  auto* kc = static_cast<__nv_bfloat16*>(k_cache);
-  auto* vc = static_cast<__nv_bfloat16*>(v_cache);
   auto* kn = static_cast<const __nv_bfloat16*>(k_new);
   auto* vn = static_cast<const __nv_bfloat16*>(v_new);
-  void* args[] = {&kc, &vc, &bt, &NB, &MB, &slot_pos, &slot_score, &kept_lens, &lens, &kn, &vn,
-                  &Hkv, &capacity, &n_sink, &n_recent, &err};
-  const void* fn = D == 128 ? (const void*)kv_rolling_admit_kernel<128> : (const void*)kv_rolling_admit_kernel<64>;
+  void* args[] = {&k_cache, &v_cache, &k_scales, &v_scales, &bt, &NB, &MB, &slot_pos, &slot_score, &kept_lens,
+                  &lens, &kn, &vn, &Hkv, &capacity, &n_sink, &n_recent, &err};
+  const bool q8 = k_scales != nullptr;
+  const void* fn = q8 ? (D == 128 ? (const void*)kv_rolling_admit_kernel<128, true>
+                                  : (const void*)kv_rolling_admit_kernel<64, true>)
+                      : (D == 128 ? (const void*)kv_rolling_admit_kernel<128, false>
+                                  : (const void*)kv_rolling_admit_kernel<64, false>);
   return launch_pdl(fn, dim3(B), dim3(kAdmitWarps * 32), 0, stream, args);
 }
 

@@ -21,7 +21,7 @@ def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _lib.header_functions()
-    assert len(declared) == 17
+    assert len(declared) == 20
     nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     for name in declared:
@@ -126,6 +126,34 @@ def test_host_validation_codes(lib):
     assert q8_decode() == c["PKV_ERR_WORKSPACE"]                      # 16-byte workspace
     assert q8_decode(dims=_dims(d=80)) == c["PKV_ERR_HEAD_DIM"]
     assert q8_decode(dims=_dims(B=0)) == c["PKV_OK"]
+    def q8_scores(lse=0x50000, vs=0x40000, stride=64, dims=None):
+        return lib.pkv_paged_decode_attention_scores_q8(
+            P(0x10000), P(lse), P(0x60000), P(0x70000), stride, P(0x10000), P(0x10000), P(0x10000), P(0x30000),
+            P(vs), P(0x10000), P(0x10000), ctypes.c_float(0.1), 0, P(0x20000), 16, ctypes.byref(dims or _dims()),
+            None, None)
+    assert q8_scores(lse=0) == c["PKV_ERR_NULL_POINTER"]
+    assert q8_scores(vs=0x40008) == c["PKV_ERR_ALIGNMENT"]
+    assert q8_scores(stride=0) == c["PKV_ERR_DIMS"]
+    assert q8_scores() == c["PKV_ERR_WORKSPACE"]                     # 16-byte workspace
+    assert q8_scores(dims=_dims(B=0)) == c["PKV_OK"]
+
+    def q8_compact(dks=0x30000, max_kept=8):
+        return lib.pkv_kv_compact_q8(P(0x10000), P(0x10000), P(dks), P(0x40000), P(0x50000), 8, 4, P(0x10000),
+                                     P(0x10000), P(0x30000), P(0x40000), P(0x50000), P(0x60000), P(0x70000),
+                                     P(0x80000), max_kept, ctypes.byref(_dims()), None, None)
+    assert q8_compact(dks=0) == c["PKV_ERR_NULL_POINTER"]
+    assert q8_compact(dks=0x30004) == c["PKV_ERR_ALIGNMENT"]
+    assert q8_compact(max_kept=-1) == c["PKV_ERR_DIMS"]
+    assert q8_compact(max_kept=0) == c["PKV_OK"]
+
+    def q8_admit(cap=60, n_sink=4, n_recent=32, ks=0x30000):
+        return lib.pkv_kv_rolling_admit_q8(P(0x10000), P(0x10000), P(ks), P(0x40000), P(0x10000), P(0x30000),
+                                           P(0x40000), P(0x50000), P(0x60000), P(0x70000), P(0x80000), cap,
+                                           n_sink, n_recent, ctypes.byref(_dims()), None, None)
+    assert q8_admit(cap=0) == c["PKV_ERR_ARGUMENT"]
+    assert q8_admit(cap=64 * 16 + 1) == c["PKV_ERR_DIMS"]
+    assert q8_admit(ks=0) == c["PKV_ERR_NULL_POINTER"]
+    assert q8_admit(ks=0x30004) == c["PKV_ERR_ALIGNMENT"]
     # prefill-window score
     def prefill(alpha=16, stride=64, lse=0x30000, qw=0x10000, dims=None):
         return lib.pkv_prefill_window_scores(P(0x40000), stride, P(lse), 0, P(qw), P(0x10000), P(0x10000),

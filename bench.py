@@ -459,16 +459,27 @@ def _q8_row(pkv, W, dev, stream, args, hbm):
     def q8():
         pkv.paged_decode_attention_q8(c["q"], kq, vq, ks, vs, c["block_tables"], c["context_lens"], c["scale"],
                                       out=out, workspace=ws, stream=stream)
+    stride = c["max_blocks_per_seq"] * 16
+    acc = torch.zeros((wl.batch, wl.num_kv_heads, stride), dtype=torch.float32, device=dev)
+    lse = torch.empty((wl.batch, wl.num_q_heads), dtype=torch.float32, device=dev)
+    logits = torch.empty((wl.batch, wl.num_q_heads, stride), dtype=torch.float32, device=dev)
+
+    def q8_scored():
+        pkv.paged_decode_attention_scores_q8(c["q"], kq, vq, ks, vs, c["block_tables"], c["context_lens"],
+                                             c["scale"], acc, out=out, lse=lse, logits=logits, workspace=ws,
+                                             stream=stream)
     steps = max(5, args.steps // 4)
     ms_plain = _time(plain, args.warmup, steps, dev, stream)
     ms_q8 = _time(q8, args.warmup, steps, dev, stream)
+    ms_q8_scored = _time(q8_scored, args.warmup, steps, dev, stream)
     lens = c["context_lens"].cpu()
     tokens = int(lens.to(torch.int64).sum())
     blocks = int(((lens.to(torch.int64) + 15) // 16).sum())
     nbytes = (tokens * wl.num_kv_heads * (wl.head_dim + 4) * 2 + 2 * wl.batch * wl.num_q_heads * wl.head_dim * 2
               + blocks * 4 + wl.batch * 4)  # codes + row scales of K and V, q, out, tables, lengths
-    del c, kq, vq, ks, vs, ws, out
+    del c, kq, vq, ks, vs, ws, out, acc, logits
     return {"ms": round(ms_q8, 4), "ms_bf16": round(ms_plain, 4), "speedup": round(ms_plain / ms_q8, 3),
+            "ms_with_scores": round(ms_q8_scored, 4), "scores_overhead": round(ms_q8_scored / ms_q8 - 1.0, 4),
             "tokens_per_s": round(wl.batch / (ms_q8 * 1e-3), 1), "bytes": nbytes,
             "gbs": round(nbytes / (ms_q8 * 1e-3) / 1e9, 1), "frac": round(nbytes / (ms_q8 * 1e-3) / 1e9 / hbm, 4),
             "l2": "0.29 GB of INT8 K/V + scales per call (> L2)"}
@@ -621,16 +632,35 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
                                          "gbs": round(sparse_bytes / (ms_gat * 1e-3) / 1e9, 1)}
     with torch.cuda.stream(gstream):
         res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, comp[0], dbt, klens, ws, out))
-    del full, comp, scores
+    # the same layer over INT8 pools (random codes, row scales ~ Exp): compaction and rolling
+    gq = torch.Generator(device=dev).manual_seed(43)
+    codes = lambda n: torch.randint(-127, 128, (n, hkv, 16, d), generator=gq, device=dev, dtype=torch.int8)
+    rscales = lambda n: torch.empty((n, hkv, 16), device=dev).exponential_(generator=gq) * 0.02
+    snb = src["k_cache"].shape[0]
+    s8 = {"kq": codes(snb), "vq": codes(snb), "ks": rscales(snb), "vs": rscales(snb)}
+    d8 = {"q": comp[0]["q"], "kq": codes(dnb), "vq": codes(dnb), "ks": rscales(dnb), "vs": rscales(dnb)}
+    del full, comp
+    torch.cuda.empty_cache()
+    cmp8 = lambda: pkv.kv_compact_q8(d8["kq"], d8["vq"], d8["ks"], d8["vs"], dbt, s8["kq"], s8["vq"], s8["ks"],
+                                     s8["vs"], src["block_tables"], src["context_lens"], kept, kl, stream=cur())
+    with torch.cuda.stream(gstream):
+        ms_cmp8 = _graph_time([cmp8] * 10, args.warmup, 5, dev, gstream) / 10
+        res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, d8, dbt, klens, ws, out, q8=True))
+    cmp8_bytes = B * hkv * K * (d + 4) * 2 * 2
+    res["sparse_layer_compact_int8"] = {"ms": round(ms_cmp8, 4), "bytes": cmp8_bytes,
+                                        "gbs": round(cmp8_bytes / (ms_cmp8 * 1e-3) / 1e9, 1),
+                                        "ms_bf16": round(ms_cmp, 4)}
+    del s8, d8, scores
     return res
 
 
-def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, calls=10, trials=5):
+def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, calls=10, trials=5, q8=False):
     """One sparse layer kept at its fixed budget by rolling admission.  The state is a top-k
     selection over the first L - 1 tokens; call i admits token L - 1 + i (its own row of context
     lengths), then, in the layer step, attends over the compact pool with the scores added to
     the slot scores.  Admission changes the state, so the `calls` calls are one CUDA graph
-    replayed once per trial from a restored state."""
+    replayed once per trial from a restored state.  q8: the compact pool is INT8 (c holds
+    kq, vq, ks, vs) and the rows are named *_int8."""
     B, hq, hkv, d, K = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.keep_max
     prev = (lens - 1).to(dev)
     kept = torch.empty((B, hkv, K), dtype=torch.int32, device=dev)
@@ -649,18 +679,33 @@ def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, c
     logits = torch.empty((B, hq, K), dtype=torch.float32, device=dev)
     err = pkv.new_error_word(dev)
 
+    cur = lambda: torch.cuda.current_stream(dev)
+
     def admit(i):
-        pkv.kv_rolling_admit(c["k_cache"], c["v_cache"], dbt, pos, sc, kls, lens_rows[i], k_new, v_new,
-                             wl.n_sink, wl.n_recent, error_word=err, stream=torch.cuda.current_stream(dev))
+        if q8:
+            pkv.kv_rolling_admit_q8(c["kq"], c["vq"], c["ks"], c["vs"], dbt, pos, sc, kls, lens_rows[i], k_new,
+                                    v_new, wl.n_sink, wl.n_recent, error_word=err, stream=cur())
+        else:
+            pkv.kv_rolling_admit(c["k_cache"], c["v_cache"], dbt, pos, sc, kls, lens_rows[i], k_new, v_new,
+                                 wl.n_sink, wl.n_recent, error_word=err, stream=cur())
 
     def decode_scores():
-        pkv.paged_decode_attention_scores(c["q"], c["k_cache"], c["v_cache"], dbt, klens, wl.scale, sc,
-                                          out=out, lse=lse, logits=logits, workspace=ws, error_word=err,
-                                          stream=torch.cuda.current_stream(dev))
+        if q8:
+            pkv.paged_decode_attention_scores_q8(c["q"], c["kq"], c["vq"], c["ks"], c["vs"], dbt, klens, wl.scale,
+                                                 sc, out=out, lse=lse, logits=logits, workspace=ws, error_word=err,
+                                                 stream=cur())
+        else:
+            pkv.paged_decode_attention_scores(c["q"], c["k_cache"], c["v_cache"], dbt, klens, wl.scale, sc,
+                                              out=out, lse=lse, logits=logits, workspace=ws, error_word=err,
+                                              stream=cur())
 
     def plain():
-        pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], dbt, klens, wl.scale, out=out,
-                                   workspace=ws, stream=torch.cuda.current_stream(dev))
+        if q8:
+            pkv.paged_decode_attention_q8(c["q"], c["kq"], c["vq"], c["ks"], c["vs"], dbt, klens, wl.scale, out=out,
+                                          workspace=ws, stream=cur())
+        else:
+            pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], dbt, klens, wl.scale, out=out,
+                                       workspace=ws, stream=cur())
 
     def restore():
         pos.copy_(pos0)
@@ -693,14 +738,21 @@ def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, c
     if pkv.read_error(err) != 0:
         raise RuntimeError(f"rolling admission reported device error {pkv.read_error(err)}")
     segs = B * hkv
-    adm_bytes = segs * (K * 8 + 2 * 2 * d * 2 + 8)  # slot positions+scores read, K/V rows in and out
-    kv = decode_bytes(klens.cpu(), B, hq, hkv, d)
-    return {"sparse_layer_rolling_admit": {"ms": round(ms_adm, 4), "bytes": adm_bytes,
-                                           "gbs": round(adm_bytes / (ms_adm * 1e-3) / 1e9, 1)},
-            "sparse_layer_rolling_step": {"ms": round(ms_layer, 4), "ms_plain_compact_decode": round(ms_plain, 4),
-                                          "gbs": round((kv + adm_bytes) / (ms_layer * 1e-3) / 1e9, 1),
-                                          "what": "admit + score-emitting decode over 1540 slots per (b, kv head)",
-                                          "launch": f"{calls} layer steps in one CUDA graph, median of {trials}"}}
+    row_out = (d + 4) * 2 if q8 else d * 2 * 2     # one K and one V row written: codes + scale, or bf16
+    adm_bytes = segs * (K * 8 + 2 * d * 2 + row_out + 8)  # slot positions+scores read, new rows in, rows out
+    if q8:
+        tok = int(klens.to(torch.int64).sum().item())
+        kv = tok * hkv * (d + 4) * 2 + 2 * B * hq * d * 2
+    else:
+        kv = decode_bytes(klens.cpu(), B, hq, hkv, d)
+    sfx = "_int8" if q8 else ""
+    return {"sparse_layer_rolling_admit" + sfx: {"ms": round(ms_adm, 4), "bytes": adm_bytes,
+                                                 "gbs": round(adm_bytes / (ms_adm * 1e-3) / 1e9, 1)},
+            "sparse_layer_rolling_step" + sfx: {
+                "ms": round(ms_layer, 4), "ms_plain_compact_decode": round(ms_plain, 4),
+                "gbs": round((kv + adm_bytes) / (ms_layer * 1e-3) / 1e9, 1),
+                "what": "admit + score-emitting decode over 1540 slots per (b, kv head)",
+                "launch": f"{calls} layer steps in one CUDA graph, median of {trials}"}}
 
 
 def _time(fn, warmup, steps, dev, stream):

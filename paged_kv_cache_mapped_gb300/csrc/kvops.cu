@@ -137,24 +137,14 @@ __global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ 
     record_error(err, PKV_DEV_BAD_VALUE);
 }
 
-// Copies one row of RB bytes with a half-warp: lane r of the half moves RB/16 bytes.
-template <int RB>
-__device__ __forceinline__ void copy_bytes_half(unsigned char* dst, const unsigned char* src, int r) {
-  if constexpr (RB == 256) {
-    reinterpret_cast<uint4*>(dst)[r] = __ldg(reinterpret_cast<const uint4*>(src) + r);
-  } else if constexpr (RB == 128) {
-    reinterpret_cast<uint2*>(dst)[r] = __ldg(reinterpret_cast<const uint2*>(src) + r);
-  } else {
-    static_assert(RB == 64, "rows of 64, 128 or 256 bytes");
-    reinterpret_cast<uint32_t*>(dst)[r] = __ldg(reinterpret_cast<const uint32_t*>(src) + r);
-  }
-}
-
 // Compaction: compact position j of (b, g) <- source token kept[b][g][j] (the per-layer
 // block-table policy of "How KV Sparsity Achieves 1.5x Acceleration for vLLM", section "Key
-// technique 1").  One warp per (b, g, j): lanes 0-15 move the K row, 16-31 the V row, RB
-// bytes each (bf16 rows of 2d bytes, or INT8 rows of d bytes whose fp32 row scales move with
-// them when SCALES).
+// technique 1").  Rows are RB bytes: bf16 rows of 2d bytes, or INT8 rows of d bytes whose fp32
+// row scales move with them when SCALES.  One warp per (b, g, destination block): lanes r and
+// r + 16 resolve compact position 16 jb + r to its source row (kept index, then source block
+// id: one dependent chain for the 16 rows instead of one per row), then every lane loads its
+// 16-byte chunks of the 16 K and V rows before any is stored, and the stores fill the
+// destination block's 16 consecutive rows.
 template <int RB, bool SCALES>
 __global__ void __launch_bounds__(256) kv_compact_kernel(
     unsigned char* __restrict__ dk, unsigned char* __restrict__ dv, float* __restrict__ dks,
@@ -163,40 +153,73 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
     const float* __restrict__ svs, const int32_t* __restrict__ sbt, const int32_t* __restrict__ lens,
     const int32_t* __restrict__ kept, const int32_t* __restrict__ kept_lens, int max_kept, int B,
     int Hkv, int sNB, int sMB, int32_t* err) {
+  static_assert(RB == 64 || RB == 128 || RB == 256, "rows of 64, 128 or 256 bytes");
+  constexpr int CPR = RB / 16;  // 16-byte chunks per row
+  constexpr int PER = CPR / 2;  // chunks of each pool per lane: 16 rows x CPR chunks over 32 lanes
   const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   grid_dependency_wait();
   grid_launch_dependents();
-  if (item >= (int64_t)B * Hkv * max_kept) return;
-  const int j = (int)(item % max_kept);
-  const int64_t bg = item / max_kept;
+  const int groups = (max_kept + 15) >> 4;
+  if (item >= (int64_t)B * Hkv * groups) return;
+  const int jb = (int)(item % groups);
+  const int64_t bg = item / groups;
   const int b = (int)(bg / Hkv);
   const int g = (int)(bg - (int64_t)b * Hkv);
   const int n = __ldg(kept_lens + b);
-  if (j >= n) return;
+  const int j0 = jb * 16;
+  if (j0 >= n) return;
   if (n > max_kept || n > dMB * 16) {
     if (lane == 0) record_error(err, PKV_DEV_BAD_KEPT_INDEX);
     return;
   }
-  const int t = __ldg(kept + bg * max_kept + j);
-  const int L = __ldg(lens + b);
-  if (t < 0 || t >= L || (t >> 4) >= sMB) {
-    if (lane == 0) record_error(err, PKV_DEV_BAD_KEPT_INDEX);
-    return;
+  const int dst_blk = __ldg(dbt + (size_t)b * dMB + jb);
+  const int r = lane & 15;  // this lane's row of the group (lanes r and r + 16 share it)
+  long long src_row = -1;
+  if (j0 + r < n) {
+    const int t = __ldg(kept + bg * max_kept + j0 + r);
+    const int L = __ldg(lens + b);
+    if (t < 0 || t >= L || (t >> 4) >= sMB) {
+      if (lane < 16) record_error(err, PKV_DEV_BAD_KEPT_INDEX);
+    } else {
+      const int sb = __ldg(sbt + (size_t)b * sMB + (t >> 4));
+      if (sb < 0 || sb >= sNB) {
+        if (lane < 16) record_error(err, PKV_DEV_BAD_BLOCK_ID);
+      } else {
+        src_row = ((long long)sb * Hkv + g) * 16 + (t & 15);
+      }
+    }
   }
-  const int src_blk = __ldg(sbt + (size_t)b * sMB + (t >> 4));
-  const int dst_blk = __ldg(dbt + (size_t)b * dMB + (j >> 4));
-  if (src_blk < 0 || src_blk >= sNB || dst_blk < 0 || dst_blk >= dNB) {
+  if (dst_blk < 0 || dst_blk >= dNB) {
     if (lane == 0) record_error(err, PKV_DEV_BAD_BLOCK_ID);
     return;
   }
-  const size_t src = ((size_t)src_blk * Hkv + g) * 16 + (t & 15);
-  const size_t dst = ((size_t)dst_blk * Hkv + g) * 16 + (j & 15);
-  if (lane < 16) copy_bytes_half<RB>(dk + dst * RB, sk + src * RB, lane);
-  else copy_bytes_half<RB>(dv + dst * RB, sv + src * RB, lane - 16);
+  const size_t dst0 = ((size_t)dst_blk * Hkv + g) * 16;  // row of compact position j0
+  uint4 kbuf[PER], vbuf[PER];
+  uint32_t live = 0u;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int c = i * 32 + lane;
+    const long long sr = __shfl_sync(kFullMask, src_row, c / CPR);
+    if (sr >= 0) {
+      live |= 1u << i;
+      kbuf[i] = __ldg(reinterpret_cast<const uint4*>(sk + sr * RB) + c % CPR);
+      vbuf[i] = __ldg(reinterpret_cast<const uint4*>(sv + sr * RB) + c % CPR);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int c = i * 32 + lane;
+    if ((live >> i) & 1u) {
+      reinterpret_cast<uint4*>(dk + (dst0 + c / CPR) * RB)[c % CPR] = kbuf[i];
+      reinterpret_cast<uint4*>(dv + (dst0 + c / CPR) * RB)[c % CPR] = vbuf[i];
+    }
+  }
   if constexpr (SCALES) {
-    if (lane == 0) dks[dst] = __ldg(sks + src);
-    if (lane == 16) dvs[dst] = __ldg(svs + src);
+    if (src_row >= 0) {
+      if (lane < 16) dks[dst0 + r] = __ldg(sks + src_row);
+      else dvs[dst0 + r] = __ldg(svs + src_row);
+    }
   }
 }
 
@@ -563,7 +586,7 @@ cudaError_t launch_kv_compact_q8(void* dk, void* dv, float* dks, float* dvs, con
                                  const int32_t* sbt, const int32_t* lens, const int32_t* kept,
                                  const int32_t* kept_lens, int max_kept, int B, int Hkv, int D, int sNB,
                                  int sMB, int32_t* err, cudaStream_t stream) {
-  const int64_t warps = (int64_t)B * Hkv * max_kept;
+  const int64_t warps = (int64_t)B * Hkv * ((max_kept + 15) / 16);  // one per destination block
   if (warps == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
   auto* a = static_cast<unsigned char*>(dk);

@@ -240,6 +240,26 @@ def run_ours(args):
     if pkv.read_error(err) != 0:
         raise RuntimeError("device error during the timed region")
 
+    # the same step timed alone with L2 flushed before each: a buffer of twice the L2 size is
+    # written between steps, outside the events; median of 50 single steps (one call each, so
+    # no programmatic overlap with a previous call)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2 ** 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    pairs = []
+    for i in range(50):
+        flush.fill_(i & 0xff)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step(copies[0])
+        e1.record(stream)
+        pairs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    flushed_ms = float(np.median([a.elapsed_time(b) for a, b in pairs]))
+    del flush
+    if pkv.read_error(err) != 0:
+        raise RuntimeError("device error during the L2-flushed steps")
+
     # end to end through the public API: pinned host inputs -> device, step, result -> host
     e2e = run_e2e(pkv, copies, host0, dev, stream, ws, args) if args.e2e else None
 
@@ -291,6 +311,9 @@ def run_ours(args):
         "host_launch_ms_per_step": round(host_ms, 5),
         "clocks": dict(clk.summary(), window=f"last {args.preload_s} s of identical warm-up load + the timed region"),
         "e2e": e2e,
+        "l2_flushed": {"ms_median": round(flushed_ms, 5), "tokens_per_s": round(B / (flushed_ms * 1e-3), 1),
+                       "frac": round(bytes_dec / (flushed_ms * 1e-3) / 1e9 / hbm, 4),
+                       "what": f"median of 50 single steps, {2 * l2 / 1e6:.0f} MB written between steps"},
     }
     if rank == 0 and world == 1 and args.baseline:
         line["cpu_baseline"] = cpu_baseline(host0, wl, lens)
@@ -357,10 +380,25 @@ def cpu_baseline(host0, wl, lens, budget_s: float = 10.0):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(steps * wl.batch / dt, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
+    cores = oracle.num_threads()
+    # the same steps on one thread, for a per-core figure (a quarter of the budget)
+    oracle.set_num_threads(1)
+    steps1 = 0
+    t1 = time.perf_counter()
+    try:
+        while True:
+            oracle.paged_decode(q, kc, vc, bt, ln, wl.scale)
+            steps1 += 1
+            if time.perf_counter() - t1 >= budget_s / 4:
+                break
+    finally:
+        oracle.set_num_threads(cores)
+    dt1 = time.perf_counter() - t1
+    return {"value": round(steps * wl.batch / dt, 2), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle", "value_1_thread": round(steps1 * wl.batch / dt1, 2),
             "sample": f"{steps} full decode steps of the llama8b workload (all {wl.batch}x{wl.num_q_heads} "
-                      f"rows, {int(lens.sum())} context tokens each step; the append's pool copy excluded)"}
+                      f"rows, {int(lens.sum())} context tokens each step; the append's pool copy excluded); "
+                      f"{steps1} more on one thread for value_1_thread"}
 
 
 def run_secondary(pkv, W, dev, stream, args):

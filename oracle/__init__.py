@@ -143,6 +143,14 @@ def num_threads() -> int:
     return int(_load().oracle_num_threads())
 
 
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on (timing only; results do not depend on it)."""
+    lib = _load()
+    lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_num_threads.restype = None
+    lib.oracle_set_num_threads(int(n))
+
+
 def kv_cache_bytes(batch, layers, heads, head_dim, seq_len, dtype_bytes) -> int:
     return int(_load().oracle_kv_cache_bytes(batch, layers, heads, head_dim, seq_len, dtype_bytes))
 

@@ -76,6 +76,15 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads of the parallel loops from now on (n >= 1); a no-op without OpenMP. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /*
  * KV-cache size in bytes: 2 (K and V) x batch x layers x heads x head_dim x seq_len x
  * bytes per element.  [primer] section 3.1 (size formula).

@@ -228,6 +228,10 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelSmemKeys = 40960;  // candidates cached in shared memory (160 KiB)
+constexpr int kSelFilt = 4096;       // keys of the first pass's chosen bin kept for the others
+constexpr int kSelBatch = 16;        // score loads in flight per thread
+// dynamic shared memory: the per-warp first-pass histograms, then the cached keys
+constexpr int kSelDynSmem = (kSelWarps * 256 + kSelSmemKeys) * (int)sizeof(uint32_t);
 
 // Order-preserving map of an fp32 score to uint32: a larger key is a larger score.  -0.0
 // is folded onto +0.0 first so the two compare equal, as the selection rule requires; NaN
@@ -239,54 +243,73 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive scan of one int per thread; returns the prefix, sets *total.
-// `warp_sums` holds kSelWarps ints of shared memory.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+// Block-wide exclusive scan of two ints per thread at once (one set of barriers); returns
+// the prefixes in *pa, *pb.  `sums` holds 2 * (kSelWarps + 1) ints of shared memory.
+__device__ __forceinline__ void block_exclusive_scan2(int a, int b, int* sums, int* pa, int* pb) {
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  int incl = v;
+  int ia = a, ib = b;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(kFullMask, incl, o);
-    if (lane >= o) incl += t;
+    const int ta = __shfl_up_sync(kFullMask, ia, o);
+    const int tb = __shfl_up_sync(kFullMask, ib, o);
+    if (lane >= o) {
+      ia += ta;
+      ib += tb;
+    }
   }
-  if (lane == 31) warp_sums[warp] = incl;
+  if (lane == 31) {
+    sums[2 * warp] = ia;
+    sums[2 * warp + 1] = ib;
+  }
   __syncthreads();
   if (warp == 0) {
-    const int w = lane < kSelWarps ? warp_sums[lane] : 0;
-    int wi = w;
+    const int wa = lane < kSelWarps ? sums[2 * lane] : 0;
+    const int wb = lane < kSelWarps ? sums[2 * lane + 1] : 0;
+    int xa = wa, xb = wb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(kFullMask, wi, o);
-      if (lane >= o) wi += t;
+      const int ta = __shfl_up_sync(kFullMask, xa, o);
+      const int tb = __shfl_up_sync(kFullMask, xb, o);
+      if (lane >= o) {
+        xa += ta;
+        xb += tb;
+      }
     }
-    if (lane < kSelWarps) warp_sums[lane] = wi - w;  // exclusive prefix of the warp totals
-    if (lane == 31) warp_sums[kSelWarps] = wi;
+    __syncwarp();
+    if (lane < kSelWarps) {
+      sums[2 * lane] = xa - wa;
+      sums[2 * lane + 1] = xb - wb;
+    }
   }
   __syncthreads();
-  const int result = warp_sums[warp] + incl - v;
-  *total = warp_sums[kSelWarps];
+  *pa = sums[2 * warp] + ia - a;
+  *pb = sums[2 * warp + 1] + ib - b;
   __syncthreads();
-  return result;
 }
 
 // Kept-token selection for one (sequence, kv head) per CTA ("How KV Sparsity...": sections
 // "System model" -- drop low-score KV, retain high-score and recent KV -- and "2. Attention
 // modification" -- per layer and head, the top-k tokens by accumulated score; sink tokens
 // from its introduction).  The k_top-th largest key among the candidates is found by an
-// MSD radix select (4 passes of 8 bits over a 256-bin histogram, the keys cached in shared
-// memory when they fit); candidates above it are kept, and of those equal to it the lowest
-// positions fill the remainder.  One ordered pass (each thread a contiguous run of
-// candidates, two block scans) writes the kept list in ascending position, so the result is
-// exact and unique.
+// MSD radix select over 8-bit digits: the first pass counts every candidate (one shared
+// atomic per key into its warp's histogram, while the scores load); the candidates sharing
+// the chosen top byte go to a short list when it fits, and the three other passes count over
+// that list.  Candidates above the k_top-th key are kept, and of those equal to it the lowest
+// positions fill the remainder: each thread owns a run of consecutive candidates, marks its
+// kept ones in 64-bit masks, and two block scans place them, so the kept list is written in
+// ascending position and the result is exact and unique.
 __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     int32_t* __restrict__ kept_out, int32_t* __restrict__ kept_lens_out,
     const float* __restrict__ scores, int stride, const int32_t* __restrict__ lens, int Hkv,
     int n_sink, int n_recent, int k_top, int32_t* err) {
-  extern __shared__ uint32_t s_keys[];  // kSelSmemKeys when the candidates fit
-  __shared__ int hist[256];
-  __shared__ int warp_sums[kSelWarps + 1];
-  __shared__ int s_digit, s_need;
+  extern __shared__ uint32_t s_dyn[];
+  int* whist = reinterpret_cast<int*>(s_dyn);  // [kSelWarps][256] per-warp first-pass counts
+  uint32_t* s_keys = s_dyn + kSelWarps * 256;  // kSelSmemKeys keys when the candidates fit
+  __shared__ uint32_t s_filt[kSelFilt];        // keys sharing the top byte of the k_top-th best
+  __shared__ __align__(16) int hist2[2][256];  // pass p counts into hist2[p & 1]
+  __shared__ int warp_sums[2 * (kSelWarps + 1)];
+  __shared__ int s_digit, s_need, s_bin, s_fcount;
 
   grid_dependency_wait();
   grid_launch_dependents();
@@ -315,47 +338,58 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   }
   const bool cached = n <= kSelSmemKeys;
   const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  int* my_hist = whist + warp * 256;
 
+  for (int i = threadIdx.x; i < kSelWarps * 256; i += blockDim.x) whist[i] = 0;
+  if (threadIdx.x == 0) s_fcount = 0;
+  __syncthreads();
+  // Scores -> order-preserving keys in shared memory, kSelBatch independent loads in flight
+  // per thread, counted by top byte on the way.
   bool nan_seen = false;
-  if (cached) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const float v = __ldg(row + first + i);
-      nan_seen |= (v != v);
-      s_keys[i] = score_key(v);
+  for (int base = 0; base < n; base += kSelThreads * kSelBatch) {
+    float v[kSelBatch];
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const int i = base + u * kSelThreads + (int)threadIdx.x;
+      v[u] = i < n ? __ldg(row + first + i) : 0.f;
     }
-  } else {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) nan_seen |= (__ldg(row + first + i) != __ldg(row + first + i));
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const int i = base + u * kSelThreads + (int)threadIdx.x;
+      if (i < n) {
+        const uint32_t key = score_key(v[u]);
+        nan_seen |= v[u] != v[u];
+        if (cached) s_keys[i] = key;
+        atomicAdd(&my_hist[key >> 24], 1);
+      }
+    }
   }
   if (nan_seen) record_error(err, PKV_DEV_BAD_SCORE);
   __syncthreads();
+  if (threadIdx.x < 256) {
+    int c = 0;
+#pragma unroll 8
+    for (int w = 0; w < kSelWarps; ++w) c += whist[w * 256 + threadIdx.x];
+    hist2[0][threadIdx.x] = c;
+    hist2[1][threadIdx.x] = 0;
+  }
+  __syncthreads();
   auto key_at = [&](int i) -> uint32_t { return cached ? s_keys[i] : score_key(__ldg(row + first + i)); };
 
+  // The digit holding the need-th largest key among those matching the prefix so far:
+  // count(> d) < need <= count(>= d).  Lane l of warp 0 owns bins [8l, 8l + 8); suffix sums
+  // over lanes from the top.
   uint32_t prefix = 0u;
   int need = k_top;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    const uint32_t hi_mask = pass == 0 ? 0u : (0xffffffffu << (shift + 8));
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int base = 0; base < n; base += blockDim.x) {
-      const int i = base + threadIdx.x;
-      const uint32_t key = i < n ? key_at(i) : 0u;
-      const bool hit = i < n && (key & hi_mask) == (prefix & hi_mask);
-      const int digit = hit ? (int)((key >> shift) & 0xffu) : -1;
-      // warp-aggregated increment: one atomic per distinct digit in the warp
-      const unsigned peers = __match_any_sync(kFullMask, digit);
-      if (hit && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
-    }
-    __syncthreads();
+  auto pick_digit = [&](int shift, const int* hist) {
     if (threadIdx.x < 32) {
-      // the digit d holding the need-th largest key: count(> d) < need <= count(>= d).
-      // Lane l owns bins [8l, 8l + 8); suffix sums over lanes from the top.
-      int c[8], own = 0;
+      const int4 h0 = reinterpret_cast<const int4*>(hist)[2 * lane];
+      const int4 h1 = reinterpret_cast<const int4*>(hist)[2 * lane + 1];
+      const int c[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      int own = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = hist[8 * lane + j];
-        own += c[j];
-      }
+      for (int j = 0; j < 8; ++j) own += c[j];
       int suffix = own;  // sum over lanes >= lane
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -370,6 +404,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
           if (cum + c[j] >= need) {
             s_digit = 8 * lane + j;
             s_need = need - cum;
+            s_bin = c[j];
             break;
           }
           cum += c[j];
@@ -379,28 +414,111 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     __syncthreads();
     prefix |= (uint32_t)s_digit << shift;
     need = s_need;
+  };
+  pick_digit(24, hist2[0]);
+
+  // Keys sharing the chosen top byte go to a short list when they fit: each warp counts its
+  // hits, takes its share of the list with one atomic, then writes them.
+  const bool filtered = cached && s_bin <= kSelFilt;
+  if (filtered) {
+    int cnt = 0;
+    for (int base = 0; base < n; base += kSelThreads) {
+      const int i = base + (int)threadIdx.x;
+      cnt += __popc(__ballot_sync(kFullMask, i < n && (s_keys[i] >> 24) == (prefix >> 24)));
+    }
+    int at = 0;
+    if (lane == 0 && cnt > 0) at = atomicAdd(&s_fcount, cnt);
+    at = __shfl_sync(kFullMask, at, 0);
+    for (int base = 0; base < n; base += kSelThreads) {
+      const int i = base + (int)threadIdx.x;
+      const uint32_t key = i < n ? s_keys[i] : 0u;
+      const bool hit = i < n && (key >> 24) == (prefix >> 24);
+      const unsigned m = __ballot_sync(kFullMask, hit);
+      if (hit) s_filt[at + __popc(m & ((1u << lane) - 1u))] = key;
+      at += __popc(m);
+    }
+  }
+  // the three other passes: over the short list (its digits spread over the bins, so a plain
+  // shared atomic per key), else over every candidate matching the prefix
+  const int m_keys = filtered ? s_bin : n;
+  if (filtered) __syncthreads();  // the short list is written
+  for (int pass = 1; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    const uint32_t hi_mask = 0xffffffffu << (shift + 8);
+    int* hist = hist2[pass & 1];  // zero since the pass before the previous one (or the start)
+    if (threadIdx.x < 256) hist2[(pass + 1) & 1][threadIdx.x] = 0;  // read last by the previous pick
+    if (filtered) {
+      for (int i = threadIdx.x; i < m_keys; i += blockDim.x) {
+        const uint32_t key = s_filt[i];
+        if ((key & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(key >> shift) & 0xffu], 1);
+      }
+    } else {
+      for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const uint32_t key = i < n ? key_at(i) : 0u;
+        const bool hit = i < n && (key & hi_mask) == (prefix & hi_mask);
+        const int digit = (int)((key >> shift) & 0xffu);
+        // warp-aggregated increment: one atomic per distinct digit in the warp
+        const unsigned peers = __match_any_sync(kFullMask, hit ? digit : -1);
+        if (hit && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+      }
+    }
+    __syncthreads();
+    pick_digit(shift, hist);
   }
   const uint32_t thr = prefix;  // key of the k_top-th best candidate
 
-  // Ordered pass: thread t owns candidates [t*C, t*C + C) (C odd: conflict-free smem reads).
+  // Ordered pass: thread t owns candidates [t*C, t*C + C) (C odd: conflict-free smem reads),
+  // 64 at a time as bit masks (two 32-bit halves) of the keys above thr and equal to it.  A
+  // run of at most 64 (always, with the keys cached) keeps its masks for the write.
   int C = (n + blockDim.x - 1) / blockDim.x;
   C |= 1;
   const int c0 = min(n, (int)threadIdx.x * C);
   const int c1 = min(n, c0 + C);
+  auto masks = [&](int i0, uint32_t (&m)[4]) {  // gt lo, gt hi, eq lo, eq hi
+    m[0] = m[1] = m[2] = m[3] = 0u;
+    const int i1 = min(c1, i0 + 64), mid = min(i1, i0 + 32);
+    for (int i = i0; i < mid; ++i) {
+      const uint32_t key = key_at(i);
+      m[0] |= (uint32_t)(key > thr) << (i - i0);
+      m[2] |= (uint32_t)(key == thr) << (i - i0);
+    }
+    for (int i = mid; i < i1; ++i) {
+      const uint32_t key = key_at(i);
+      m[1] |= (uint32_t)(key > thr) << (i - i0 - 32);
+      m[3] |= (uint32_t)(key == thr) << (i - i0 - 32);
+    }
+  };
+  uint32_t mk[4];
   int gt = 0, eq = 0;
-  for (int i = c0; i < c1; ++i) {
-    const uint32_t key = key_at(i);
-    gt += key > thr;
-    eq += key == thr;
+  for (int i0 = c0; i0 < c1; i0 += 64) {
+    masks(i0, mk);
+    gt += __popc(mk[0]) + __popc(mk[1]);
+    eq += __popc(mk[2]) + __popc(mk[3]);
   }
-  int total;
-  const int eq_before = block_exclusive_scan(eq, warp_sums, &total);
-  const int eq_take = max(0, min(eq, need - eq_before));  // lowest positions among equal keys
-  const int pos = block_exclusive_scan(gt + eq_take, warp_sums, &total);
-  int w = n_sink + pos, eq_left = eq_take;
-  for (int i = c0; i < c1; ++i) {
-    const uint32_t key = key_at(i);
-    if (key > thr || (key == thr && eq_left-- > 0)) out[w++] = first + i;
+  // equal keys are taken lowest position first, so the threads before this one took
+  // min(need, eq_before) of them
+  int gt_before, eq_before;
+  block_exclusive_scan2(gt, eq, warp_sums, &gt_before, &eq_before);
+  int eq_left = max(0, min(eq, need - eq_before));
+  int w = n_sink + gt_before + min(need, eq_before);
+  if (gt + eq_left > 0) {
+    for (int i0 = c0; i0 < c1; i0 += 64) {
+      if (c1 - c0 > 64) masks(i0, mk);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t take = mk[h], eqm = mk[2 + h];
+        while (eq_left > 0 && eqm != 0u) {  // the lowest remaining equal keys
+          take |= eqm & (~eqm + 1u);
+          eqm &= eqm - 1u;
+          --eq_left;
+        }
+        while (take != 0u) {
+          out[w++] = first + i0 + 32 * h + (__ffs(take) - 1);
+          take &= take - 1u;
+        }
+      }
+    }
   }
   for (int t = threadIdx.x; t < n_sink; t += blockDim.x) out[t] = t;
   for (int t = threadIdx.x; t < n_recent; t += blockDim.x) out[n_sink + k_top + t] = first + n + t;
@@ -539,7 +657,7 @@ __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
 cudaError_t kvops_device_setup() {
   // the selection's key cache needs more than the default 48 KiB of dynamic shared memory
   return cudaFuncSetAttribute((const void*)select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSelSmemKeys * (int)sizeof(uint32_t));
+                              kSelDynSmem);
 }
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
@@ -610,7 +728,7 @@ cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const 
   void* args[] = {&kept_out, &kept_lens_out, &scores, &stride, &lens, &Hkv, &n_sink, &n_recent,
                   &k_top, &err};
   return launch_pdl((const void*)select_topk_kernel, dim3(pairs), dim3(kSelThreads),
-                    kSelSmemKeys * sizeof(uint32_t), stream, args);
+                    kSelDynSmem, stream, args);
 }
 
 cudaError_t launch_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* bt, int NB, int MB,

@@ -442,6 +442,50 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     bt_cur = load_chunk(0);
     if (nunits > 32) bt_next = load_chunk(32);
   }
+  // Sparse: the rows of this range's units are resolved in pairs of units (lane l: row l & 15
+  // of unit 2c + l / 16) through a pipeline -- the kept index two pairs ahead of issue, the
+  // block id one pair ahead -- so an issue waits on neither dependent load.
+  int sp_t = 0, sp_b = 0, sp_g = 0;   // stage 1: kept index of pair c + 2 (valid: sp_ok1)
+  int sp_phys = 0, sp_gt = -1;        // stage 2: block id of pair c + 1; g << 4 | offset, -1 none
+  int sp_row = -1;                    // pair c: this lane's pool row, -1 when not copied
+  bool sp_ok1 = false;
+  auto sp_stage1 = [&](int pair) {    // load the kept index of `pair`
+    sp_ok1 = false;
+    const int k = 2 * pair + (lane >> 4);
+    if (k < nunits) {
+      const Cursor c = locate(u0 + k, s_start, s_nb, a.B);
+      const int pos = c.j * 16 + (lane & 15);
+      if (pos < s_len[c.b]) {
+        sp_t = __ldg(a.kept + ((size_t)c.b * a.Hkv + c.g) * a.max_kept + pos);
+        sp_b = c.b;
+        sp_g = c.g;
+        sp_ok1 = true;
+      }
+    }
+  };
+  auto sp_stage2 = [&]() {            // stage 1 -> stage 2: check the index, load its block id
+    sp_gt = -1;
+    if (sp_ok1) {
+      if (sp_t < 0 || sp_t >= s_lo[sp_b]) {
+        record_error(a.err, PKV_DEV_BAD_KEPT_INDEX);
+      } else {
+        sp_phys = __ldg(a.block_tables + (size_t)sp_b * a.MB + (sp_t >> 4));
+        sp_gt = (sp_g << 4) | (sp_t & 15);
+      }
+    }
+  };
+  auto sp_stage3 = [&]() {            // stage 2 -> the pool row
+    sp_row = -1;
+    if (sp_gt >= 0) {
+      if (sp_phys < 0 || sp_phys >= a.NB) record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
+      else sp_row = (sp_phys * a.Hkv + (sp_gt >> 4)) * 16 + (sp_gt & 15);  // host checks < 2^31
+    }
+  };
+  if constexpr (SPARSE) {
+    sp_stage1(0);
+    sp_stage2();
+    sp_stage1(1);
+  }
 
   // Issue unit k (the one `ic` names) into slot k % R.  Dense: lane 0 copies the K and V
   // tiles as TMA boxes.  Sparse: lane r < 16 copies K row r, lane 16 + r V row r.
@@ -491,26 +535,14 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     } else {
       const int r = lane & 15;
       const bool is_v = lane >= 16;
-      bool ok;
-      size_t src = 0;
-      const int pos = ic.j * 16 + r;
-      ok = pos < s_len[ic.b];
-      int t = 0, phys = 0;
-      if (ok) {
-        t = __ldg(a.kept + ((size_t)ic.b * a.Hkv + ic.g) * a.max_kept + pos);
-        if (t < 0 || t >= s_lo[ic.b]) {
-          record_error(a.err, PKV_DEV_BAD_KEPT_INDEX);
-          ok = false;
-        }
+      if ((k & 1) == 0) {  // a new pair: advance the row pipeline
+        sp_stage3();
+        sp_stage2();
+        sp_stage1((k >> 1) + 2);
       }
-      if (ok) {
-        phys = __ldg(a.block_tables + (size_t)ic.b * a.MB + (t >> 4));
-        if (phys < 0 || phys >= a.NB) {
-          record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
-          ok = false;
-        }
-      }
-      src = (((size_t)phys * a.Hkv + ic.g) * 16 + (t & 15)) * D;
+      const int row = __shfl_sync(kFullMask, sp_row, ((k & 1) << 4) | r);
+      const bool ok = row >= 0;
+      const size_t src = (size_t)(ok ? row : 0) * D;
       const uint32_t vmask = __ballot_sync(kFullMask, ok) & 0xffffu;  // K and V lanes agree
       if (lane == 0) {
         Wb.meta[slot] = vmask;

@@ -140,11 +140,14 @@ __global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ 
 // Compaction: compact position j of (b, g) <- source token kept[b][g][j] (the per-layer
 // block-table policy of "How KV Sparsity Achieves 1.5x Acceleration for vLLM", section "Key
 // technique 1").  Rows are RB bytes: bf16 rows of 2d bytes, or INT8 rows of d bytes whose fp32
-// row scales move with them when SCALES.  One warp per (b, g, destination block): lanes r and
-// r + 16 resolve compact position 16 jb + r to its source row (kept index, then source block
-// id: one dependent chain for the 16 rows instead of one per row), then every lane loads its
-// 16-byte chunks of the 16 K and V rows before any is stored, and the stores fill the
-// destination block's 16 consecutive rows.
+// row scales move with them when SCALES.  One warp per (b, g, compact_rows(RB) consecutive
+// compact positions inside one destination block): the lanes resolve the group's positions to source
+// rows (kept index, then source block id: one chain of dependent loads for the group instead
+// of one per row), then every lane loads its 16-byte chunks of the group's K and V rows before
+// any is stored, and the stores fill consecutive rows of the destination block.
+// positions per warp (a divisor of 16): 4 for 256-byte rows, 8 for shorter ones (measured)
+__host__ __device__ constexpr int compact_rows(int rb) { return rb >= 256 ? 4 : 8; }
+
 template <int RB, bool SCALES>
 __global__ void __launch_bounds__(256) kv_compact_kernel(
     unsigned char* __restrict__ dk, unsigned char* __restrict__ dv, float* __restrict__ dks,
@@ -154,37 +157,39 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
     const int32_t* __restrict__ kept, const int32_t* __restrict__ kept_lens, int max_kept, int B,
     int Hkv, int sNB, int sMB, int32_t* err) {
   static_assert(RB == 64 || RB == 128 || RB == 256, "rows of 64, 128 or 256 bytes");
-  constexpr int CPR = RB / 16;  // 16-byte chunks per row
-  constexpr int PER = CPR / 2;  // chunks of each pool per lane: 16 rows x CPR chunks over 32 lanes
+  constexpr int NR = compact_rows(RB);
+  constexpr int CPR = RB / 16;             // 16-byte chunks per row
+  constexpr int PER = (NR * CPR + 31) / 32;  // chunks of each pool per lane
+  static_assert(16 % NR == 0 && NR * CPR >= 32, "a group fills the warp's lanes");
   const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   grid_dependency_wait();
   grid_launch_dependents();
-  const int groups = (max_kept + 15) >> 4;
+  const int groups = (max_kept + NR - 1) / NR;
   if (item >= (int64_t)B * Hkv * groups) return;
   const int jb = (int)(item % groups);
   const int64_t bg = item / groups;
   const int b = (int)(bg / Hkv);
   const int g = (int)(bg - (int64_t)b * Hkv);
   const int n = __ldg(kept_lens + b);
-  const int j0 = jb * 16;
+  const int j0 = jb * NR;
   if (j0 >= n) return;
   if (n > max_kept || n > dMB * 16) {
     if (lane == 0) record_error(err, PKV_DEV_BAD_KEPT_INDEX);
     return;
   }
-  const int dst_blk = __ldg(dbt + (size_t)b * dMB + jb);
-  const int r = lane & 15;  // this lane's row of the group (lanes r and r + 16 share it)
+  const int dst_blk = __ldg(dbt + (size_t)b * dMB + (j0 >> 4));
+  const int r = lane % NR;  // this lane's row of the group (lanes r, r + NR, ... share it)
   long long src_row = -1;
   if (j0 + r < n) {
     const int t = __ldg(kept + bg * max_kept + j0 + r);
     const int L = __ldg(lens + b);
     if (t < 0 || t >= L || (t >> 4) >= sMB) {
-      if (lane < 16) record_error(err, PKV_DEV_BAD_KEPT_INDEX);
+      if (lane < NR) record_error(err, PKV_DEV_BAD_KEPT_INDEX);
     } else {
       const int sb = __ldg(sbt + (size_t)b * sMB + (t >> 4));
       if (sb < 0 || sb >= sNB) {
-        if (lane < 16) record_error(err, PKV_DEV_BAD_BLOCK_ID);
+        if (lane < NR) record_error(err, PKV_DEV_BAD_BLOCK_ID);
       } else {
         src_row = ((long long)sb * Hkv + g) * 16 + (t & 15);
       }
@@ -194,14 +199,14 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
     if (lane == 0) record_error(err, PKV_DEV_BAD_BLOCK_ID);
     return;
   }
-  const size_t dst0 = ((size_t)dst_blk * Hkv + g) * 16;  // row of compact position j0
+  const size_t dst0 = ((size_t)dst_blk * Hkv + g) * 16 + (j0 & 15);  // row of compact position j0
   uint4 kbuf[PER], vbuf[PER];
   uint32_t live = 0u;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int c = i * 32 + lane;
-    const long long sr = __shfl_sync(kFullMask, src_row, c / CPR);
-    if (sr >= 0) {
+    const long long sr = __shfl_sync(kFullMask, src_row, (c / CPR) % NR);
+    if (c < NR * CPR && sr >= 0) {
       live |= 1u << i;
       kbuf[i] = __ldg(reinterpret_cast<const uint4*>(sk + sr * RB) + c % CPR);
       vbuf[i] = __ldg(reinterpret_cast<const uint4*>(sv + sr * RB) + c % CPR);
@@ -216,8 +221,8 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
     }
   }
   if constexpr (SCALES) {
-    if (src_row >= 0) {
-      if (lane < 16) dks[dst0 + r] = __ldg(sks + src_row);
+    if (lane < 2 * NR && src_row >= 0) {
+      if (lane < NR) dks[dst0 + r] = __ldg(sks + src_row);
       else dvs[dst0 + r] = __ldg(svs + src_row);
     }
   }
@@ -704,7 +709,8 @@ cudaError_t launch_kv_compact_q8(void* dk, void* dv, float* dks, float* dvs, con
                                  const int32_t* sbt, const int32_t* lens, const int32_t* kept,
                                  const int32_t* kept_lens, int max_kept, int B, int Hkv, int D, int sNB,
                                  int sMB, int32_t* err, cudaStream_t stream) {
-  const int64_t warps = (int64_t)B * Hkv * ((max_kept + 15) / 16);  // one per destination block
+  const int nr = compact_rows(dks != nullptr ? D : 2 * D);
+  const int64_t warps = (int64_t)B * Hkv * ((max_kept + nr - 1) / nr);
   if (warps == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
   auto* a = static_cast<unsigned char*>(dk);

@@ -834,14 +834,13 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       l1 += p01 + p11;
       // -- P^T as bf16 hi + lo B fragments (tokens x heads -> heads x tokens) -------------
       // INT8 pools: fp16 parts of P times each token's V scale over vref (at most 2^8 * slack)
-      uint32_t hA, hB, lA, lB;
+      // INT8 pools: one fp16 term (11 significant bits, below the bf16 output's rounding);
+      // bf16: a hi + lo pair of bf16 terms (8 bits alone would not be)
+      uint32_t hA, hB, lA = 0u, lB = 0u;
       if constexpr (Q8) {
         const float r0 = vs0 * inv_vref, r1 = vs1 * inv_vref;
-        const float w00 = p00 * r0, w01 = p01 * r0, w10 = p10 * r1, w11 = p11 * r1;
-        hA = pack_f16x2(w00, w01);
-        hB = pack_f16x2(w10, w11);
-        lA = pack_f16x2(w00 - f16_lo_to_f32(hA), w01 - f16_hi_to_f32(hA));
-        lB = pack_f16x2(w10 - f16_lo_to_f32(hB), w11 - f16_hi_to_f32(hB));
+        hA = pack_f16x2(p00 * r0, p01 * r0);
+        hB = pack_f16x2(p10 * r1, p11 * r1);
       } else {
         hA = pack_bf16x2(p00, p01);  // token gq
         hB = pack_bf16x2(p10, p11);  // token gq + 8
@@ -849,7 +848,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         lB = pack_bf16x2(p10 - bf16_lo_to_f32(hB), p11 - bf16_hi_to_f32(hB));
       }
       const uint32_t bh0 = movmatrix_trans(hA), bh1 = movmatrix_trans(hB);
-      const uint32_t bl0 = movmatrix_trans(lA), bl1 = movmatrix_trans(lB);
+      const uint32_t bl0 = Q8 ? 0u : movmatrix_trans(lA), bl1 = Q8 ? 0u : movmatrix_trans(lB);
       if (!__all_sync(kFullMask, mbar_wait_bounded(&Wb.bar_v[slot], parity, a.timeout_ns))) {
         if (lane == 0) record_error(a.err, PKV_DEV_WAIT_TIMEOUT);
         aborted = true;
@@ -889,11 +888,9 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
           const uint32_t a0[4] = {i8x2_to_f16x2<0x4240>(f0), i8x2_to_f16x2<0x4341>(f0),
                                   i8x2_to_f16x2<0x4240>(f1), i8x2_to_f16x2<0x4341>(f1)};
           mma_f16_m16n8k16(o[2 * pp], a0, bh0, bh1);
-          mma_f16_m16n8k16(o[2 * pp], a0, bl0, bl1);
           const uint32_t a1[4] = {i8x2_to_f16x2<0x4240>(f2), i8x2_to_f16x2<0x4341>(f2),
                                   i8x2_to_f16x2<0x4240>(f3), i8x2_to_f16x2<0x4341>(f3)};
           mma_f16_m16n8k16(o[2 * pp + 1], a1, bh0, bh1);
-          mma_f16_m16n8k16(o[2 * pp + 1], a1, bl0, bl1);
         }
       } else {
 #pragma unroll

@@ -82,7 +82,7 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #endif
 
 #ifndef PKV_Q8_MIN_CTAS
-#define PKV_Q8_MIN_CTAS 0   // INT8 decode: resident CTAs per SM the register budget must allow (0: no bound)
+#define PKV_Q8_MIN_CTAS 12  // INT8 decode: resident CTAs per SM the register budget must allow (0: no bound)
 #endif
 
 #ifndef PKV_MIN_UNITS

@@ -359,3 +359,56 @@ def test_int8_sparse_layer_chain_matches_the_oracle_chain():
     rk, rv, rks, rvs = ref_dst
     ref_out = oracle.paged_decode_q8(bits(c["q"]), rk, rks, rv, rvs, _n(dbt), ref_kl, c["scale"])
     _close(out, ref_out, "compact INT8 decode")
+
+
+def test_compact_q8_sparse_workload_full_size_bit_exact():
+    """One layer of the sparse workload (16 x 8 heads, 16384-token contexts, Exp(1) scores):
+    the GPU selection's kept lists (4 + 512 + 1024) compact INT8 pools into the compact tables,
+    bit for bit against the oracle over every row and scale."""
+    wl = W.WORKLOADS["sparse"]
+    lens = W.context_lengths(wl)
+    B, hkv, d, K = wl.batch, wl.num_kv_heads, wl.head_dim, wl.keep_max
+    mb = int((lens.max() + 15) // 16)
+    snb = B * mb + 16
+    g = torch.Generator(device=DEV).manual_seed(71)
+    codes = lambda n: torch.randint(-127, 128, (n, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    scales = lambda n: torch.empty((n, hkv, 16), device=DEV).exponential_(generator=g)
+    sk, sv, sks, svs = codes(snb), codes(snb), scales(snb), scales(snb)
+    sbt = torch.randperm(snb, device=DEV, generator=g)[: B * mb].view(B, mb).to(torch.int32)
+    scores = W.make_scores(wl, wl.full_layers, lens, device=DEV, device_rng=True)
+    L = lens.to(DEV)
+    kept = torch.empty((B, hkv, K), dtype=torch.int32, device=DEV)
+    kl = torch.empty((B,), dtype=torch.int32, device=DEV)
+    pkv.kv_select_topk(scores, L, wl.n_sink, wl.n_recent, wl.k_top, kept_out=kept, kept_lens_out=kl)
+    dbt_cpu, dnb = W.compact_tables(K, B, seed=5)
+    dbt = dbt_cpu.to(DEV)
+    dk, dv, dks, dvs = codes(dnb), codes(dnb), scales(dnb), scales(dnb)
+    ref = oracle.compact_q8(_n(dk), _n(dv), _n(dks), _n(dvs), dbt_cpu.numpy(), _n(sk), _n(sv), _n(sks), _n(svs),
+                            _n(sbt), _n(L), _n(kept), _n(kl))
+    err = pkv.new_error_word(DEV)
+    pkv.kv_compact_q8(dk, dv, dks, dvs, dbt, sk, sv, sks, svs, sbt, L, kept, kl, error_word=err)
+    assert pkv.read_error(err) == 0
+    for name, got, want in zip(("k_codes", "v_codes", "k_scales", "v_scales"), (dk, dv, dks, dvs), ref):
+        assert np.array_equal(_n(got), want), name
+
+
+def test_rolling_admit_q8_sparse_workload_shape_one_step():
+    """16 sequences x 8 kv heads at the full budget of 1540 slots (any slot order): one step's
+    admission into INT8 pools, bit for bit against the oracle."""
+    B, hkv, d, n_sink, k_top, n_recent = 16, 8, 128, 4, 512, 1024
+    cap = n_sink + k_top + n_recent
+    L = 16385
+    st = _rstate(B, hkv, d, cap, seed=72)
+    rng = np.random.default_rng(72)
+    scores = rng.exponential(size=(B, hkv, L - 1)).astype(np.float32)
+    kept, _ = oracle.select_topk(scores, np.full(B, L - 1, np.int32), n_sink, n_recent, k_top)
+    perm = np.stack([np.stack([rng.permutation(cap) for _ in range(hkv)]) for _ in range(B)])
+    pos = np.take_along_axis(kept, perm, axis=2).astype(np.int32)
+    st["slot_pos"].copy_(torch.from_numpy(pos))
+    st["slot_score"].copy_(torch.from_numpy(np.take_along_axis(scores, pos.astype(np.int64), axis=2)))
+    st["kept_lens"].fill_(cap)
+    g = torch.Generator().manual_seed(73)
+    err = pkv.new_error_word(DEV)
+    _admit_both(st, torch.full((B,), L, dtype=torch.int32, device=DEV), rand_bf16((B, hkv, d), g).to(DEV),
+                rand_bf16((B, hkv, d), g).to(DEV), n_sink, n_recent, err)
+    assert pkv.read_error(err) == 0

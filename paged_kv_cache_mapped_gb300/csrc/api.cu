@@ -337,8 +337,8 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.workers = (int)workers;
   const int ring = q8 != nullptr ? (dims->head_dim == 128 ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
                                  : (dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64);
-  a.min_units = std::max(PKV_MIN_UNITS, 1);
-  a.tail_pct = std::min(std::max(PKV_TAIL_PCT, 0), 50);
+  a.min_units = std::max(sparse ? PKV_MIN_UNITS_SPARSE : PKV_MIN_UNITS, 1);
+  a.tail_pct = std::min(std::max(sparse ? PKV_TAIL_PCT_SPARSE : PKV_TAIL_PCT, 0), 50);
   a.chunk_min = std::max(PKV_CHUNK_MIN, ring);  // a chunk never ends inside the tile ring
   a.cpw_cap = (int)std::min<long long>(std::min(PKV_MAX_TAIL_CHUNKS, kMaxTailChunksLimit),
                                        plan.ranges / workers - 1);

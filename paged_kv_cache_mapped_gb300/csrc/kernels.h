@@ -88,8 +88,14 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #ifndef PKV_MIN_UNITS
 #define PKV_MIN_UNITS 16  // lower bound of a worker slice, in 16-token units
 #endif
+#ifndef PKV_MIN_UNITS_SPARSE
+#define PKV_MIN_UNITS_SPARSE 8  // the same for the gather form of the sparse decode (measured)
+#endif
 #ifndef PKV_TAIL_PCT
 #define PKV_TAIL_PCT 20   // share of a slice handed out dynamically
+#endif
+#ifndef PKV_TAIL_PCT_SPARSE
+#define PKV_TAIL_PCT_SPARSE 30  // the same for the gather form of the sparse decode (measured)
 #endif
 #ifndef PKV_CHUNK_MIN
 #define PKV_CHUNK_MIN 6   // shortest tail chunk, in units (at least the tile ring depth)

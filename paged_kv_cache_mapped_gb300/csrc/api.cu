@@ -185,7 +185,9 @@ int merge_warps_log2(const pkv_dims* d, int max_units, long long workers, int mi
                      int chunk_min, int cpw_cap, long long resident_warps) {
   const long long total = (long long)d->batch * d->num_kv_heads * max_units;
   long long P = (total + workers - 1) / workers;
-  if (P < min_units) P = min_units;
+  const long long busy = std::max(1ll, workers * PKV_MIN_BUSY_PCT / 100);
+  const long long floor_units = std::min<long long>(min_units, (total + busy - 1) / busy);
+  if (P < floor_units) P = floor_units;
   const long long tail = P * tail_pct / 100;
   int cpw = 0;
   while (cpw < cpw_cap && tail >= chunk_min * ((2ll << cpw) - 1)) ++cpw;

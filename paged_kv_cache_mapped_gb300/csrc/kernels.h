@@ -88,6 +88,9 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #ifndef PKV_MIN_UNITS
 #define PKV_MIN_UNITS 16  // lower bound of a worker slice, in 16-token units
 #endif
+#ifndef PKV_MIN_BUSY_PCT
+#define PKV_MIN_BUSY_PCT 70  // the slice floor yields to keep this share of the workers busy (0: never)
+#endif
 #ifndef PKV_MIN_UNITS_SPARSE
 #define PKV_MIN_UNITS_SPARSE 8  // the same for the gather form of the sparse decode (measured)
 #endif

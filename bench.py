@@ -170,6 +170,19 @@ def decode_bytes(lens, B, hq, hkv, d, window=0) -> int:
 
 # ------------------------------------------------------------------------------- our arm
 
+def arm_config(wl, lens, nb, world):
+    """The workload's config record, the same for both arms."""
+    return {
+        "workload": "llama8b decode layer: B=32, Hq=32, Hkv=8, d=128, block 16, "
+                    "L=U[3500,4500]+1, append of the new token + paged decode",
+        "batch": wl.batch, "context_tokens": int(lens.sum()), "num_q_heads": wl.num_q_heads,
+        "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": 16,
+        "l2": f"inputs larger than L2: {ROTATE} rotating pool copies "
+              f"({ROTATE * 2 * nb * wl.num_kv_heads * 16 * wl.head_dim * 2 / 1e9:.2f} GB)",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
 def run_ours(args):
     import paged_kv_cache_mapped_gb300 as pkv
     from paged_kv_cache_mapped_gb300 import inputs as W
@@ -281,15 +294,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 K/V/q; shuffled block tables)",
-        "config": {
-            "workload": "llama8b decode layer: B=32, Hq=32, Hkv=8, d=128, block 16, "
-                        "L=U[3500,4500]+1, append of the new token + paged decode",
-            "batch": B, "context_tokens": int(lens.sum()), "num_q_heads": hq, "num_kv_heads": hkv,
-            "head_dim": d, "block_size": 16,
-            "l2": f"inputs larger than L2: {ROTATE} rotating pool copies "
-                  f"({ROTATE * 2 * nb * hkv * 16 * d * 2 / 1e9:.2f} GB)",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        },
+        "config": arm_config(wl, lens, nb, world),
         "kv_read_gbs": round(kv_bytes(lens, hkv, d) / (dec_ms * 1e-3) / 1e9, 1),
         "roofline": {
             "bound": "hbm",
@@ -861,9 +866,12 @@ def run_reference(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "llama8b decode layer (oracle sample: 4 sequences x 32 heads)"},
+        "config": arm_config(wl, W.context_lengths(wl), host0["num_blocks"], world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": f"{n_seq} of 32 sequences per step, all heads"},
+                         "kind": "oracle",
+                         "sample": f"each step: the oracle's decode of {n_seq} of the {wl.batch} sequences "
+                                   f"(all {wl.num_q_heads} heads, their full contexts); tokens/s counts "
+                                   f"those {n_seq} sequences"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -210,6 +210,28 @@ int pkv_paged_decode_attention_q8(void* out, const void* q, const void* k_codes,
                                   void* stream);
 
 /*
+ * pkv_paged_decode_attention_append_q8 -- pkv_kv_append_q8 fused into
+ * pkv_paged_decode_attention_q8 for the usual decode slot, as pkv_paged_decode_attention_append
+ * does for bf16 pools: each sequence's new token is at position L_b - 1 (its slot comes from
+ * the block table), its K and V rows are quantized by the row rule of pkv_kv_append_q8 into the
+ * code and scale pools, and the decode attends over them.
+ *   k_codes, v_codes, k_scales, v_scales : INT8 pools as pkv_paged_decode_attention_q8, updated
+ *                        in place at each sequence's position L_b - 1 (L_b >= 1).
+ *   k_new, v_new       : [B, Hkv, d] bf16, 16-byte aligned.
+ *   other arguments    : as pkv_paged_decode_attention_q8.
+ *   error_word         : as pkv_paged_decode_attention_q8, plus PKV_DEV_BAD_VALUE when a new row
+ *                        holds a non-finite value (that (b, kv head)'s rows are then not written
+ *                        and its attention reads the pool as it was).
+ * The pools end bit-identical to pkv_kv_append_q8 of the same rows, and out bit-identical to
+ * pkv_paged_decode_attention_q8 over the appended pools (same workspace size).
+ */
+int pkv_paged_decode_attention_append_q8(void* out, const void* q, void* k_codes, void* v_codes, float* k_scales,
+                                         float* v_scales, const void* k_new, const void* v_new,
+                                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                                         int32_t window, void* workspace, size_t workspace_bytes,
+                                         const pkv_dims* dims, int32_t* error_word, void* stream);
+
+/*
  * pkv_prefill_window_scores -- the prefill-side sparsification score: after a prompt of L_b
  * tokens, key i of kv head g scores the sum, over the last alpha prompt positions j (the
  * instruction window, j >= i) and the G query heads of the group, of its causal softmax

@@ -25,6 +25,7 @@ __all__ = [
     "paged_decode_attention_q8",
     "prefill_window_scores",
     "paged_decode_attention_scores_q8", "kv_compact_q8", "kv_rolling_admit_q8",
+    "paged_decode_attention_append_q8",
 ]
 
 BLOCK_SIZE = 16
@@ -316,6 +317,25 @@ def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_len
         int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims), _ptr(error_word),
         _stream(stream, dev)))
     return out, lse
+
+
+def paged_decode_attention_append_q8(q, k_codes, v_codes, k_scales, v_scales, k_new, v_new, block_tables,
+                                     context_lens, scale, window=0, *, out=None, workspace=None, error_word=None,
+                                     stream=None):
+    """kv_append_q8 of k_new/v_new [B, Hkv, d] (bf16) at each sequence's position L_b - 1, fused
+    into paged_decode_attention_q8 over the updated INT8 pools."""
+    dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
+    _need(k_new, "k_new", torch.bfloat16, 3, dev)
+    _need(v_new, "v_new", torch.bfloat16, 3, dev)
+    if k_new.shape != (dims.batch, dims.num_kv_heads, dims.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
+    nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
+    out, workspace = _out_ws(q, out, workspace, nbytes)
+    check("pkv_paged_decode_attention_append_q8", load().pkv_paged_decode_attention_append_q8(
+        _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(k_new), _ptr(v_new),
+        _ptr(block_tables), _ptr(context_lens), float(scale), int(window), _ptr(workspace), workspace.numel(),
+        ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+    return out
 
 
 def paged_decode_attention_scores_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale,

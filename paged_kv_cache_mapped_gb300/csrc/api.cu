@@ -255,7 +255,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
     return PKV_ERR_ALIGNMENT;
   const int group = dims->num_q_heads / dims->num_kv_heads;
   if (q8 != nullptr) {
-    if (sparse || k_new != nullptr) return PKV_ERR_ARGUMENT;
+    if (sparse) return PKV_ERR_ARGUMENT;
     if (!q8->k_scale || !q8->v_scale) return PKV_ERR_NULL_POINTER;
     if (!aligned16(q8->k_scale) || !aligned16(q8->v_scale)) return PKV_ERR_ALIGNMENT;
   }
@@ -311,8 +311,12 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   if (k_new != nullptr) {
     a.k_new = static_cast<const __nv_bfloat16*>(k_new);
     a.v_new = static_cast<const __nv_bfloat16*>(v_new);
-    a.k_pool_out = static_cast<__nv_bfloat16*>(const_cast<void*>(k_cache));
+    a.k_pool_out = static_cast<__nv_bfloat16*>(const_cast<void*>(k_cache));  // INT8: the code pools
     a.v_pool_out = static_cast<__nv_bfloat16*>(const_cast<void*>(v_cache));
+    if (q8 != nullptr) {
+      a.k_scale_out = const_cast<float*>(q8->k_scale);
+      a.v_scale_out = const_cast<float*>(q8->v_scale);
+    }
   }
   a.out = static_cast<__nv_bfloat16*>(out);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -416,6 +420,18 @@ int pkv_paged_decode_attention_q8(void* out, const void* q, const void* k_codes,
   return decode_common(out, q, k_codes, v_codes, block_tables, context_lens, nullptr, nullptr, 0, scale,
                        window, workspace, workspace_bytes, dims, error_word, stream, false, nullptr, nullptr,
                        nullptr, &q8);
+}
+
+int pkv_paged_decode_attention_append_q8(void* out, const void* q, void* k_codes, void* v_codes, float* k_scales,
+                                         float* v_scales, const void* k_new, const void* v_new,
+                                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                                         int32_t window, void* workspace, size_t workspace_bytes,
+                                         const pkv_dims* dims, int32_t* error_word, void* stream) {
+  if (k_new == nullptr || v_new == nullptr) return PKV_ERR_NULL_POINTER;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_ALIGNMENT;
+  const Q8Scales q8{k_scales, v_scales};
+  return decode_common(out, q, k_codes, v_codes, block_tables, context_lens, nullptr, nullptr, 0, scale, window,
+                       workspace, workspace_bytes, dims, error_word, stream, false, k_new, v_new, nullptr, &q8);
 }
 
 int pkv_prefill_window_scores(float* score_accum, int32_t score_stride, float* lse, int32_t lse_given,

@@ -586,10 +586,17 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   float sl2q = sl2, vref = 0.f, inv_vref = 0.f;
   // Dense append mode: this step's K (lanes 0-15) or V (lanes 16-31) row chunk of the current
   // segment, to be written at token L_b - 1 (pool and tile) when its unit is consumed.
-  const bool appending = !SPARSE && !Q8 && a.k_new != nullptr;
+  // INT8 pools: the half-warp quantizes its row when the segment begins (the INT8 append's row
+  // rule: scale max|x| / 127, codes round-half-even of x / scale, both in IEEE fp32) and the
+  // step writes codes and scale to the pool, the tile and the tile's scales; a row with a
+  // non-finite value is reported and neither row is written.
+  const bool appending = !SPARSE && a.k_new != nullptr;
   uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
   const int new_chunk = lane & 15;
   const bool new_lane = new_chunk < D / 8;
+  uint2 new_codes = make_uint2(0u, 0u);  // INT8: this lane's 8 codes of the row
+  float new_scale = 0.f;                 // INT8: the row's scale (K: lanes 0-15, V: 16-31)
+  bool new_ok = true;                    // INT8: both rows finite
 
   auto flush = [&]() {
 #pragma unroll
@@ -675,6 +682,36 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       const __nv_bfloat16* src = (lane >= 16 ? a.v_new : a.k_new) + ((size_t)c.b * a.Hkv + c.g) * D + new_chunk * 8;
       new_row = __ldg(reinterpret_cast<const uint4*>(src));
     }
+    if constexpr (Q8) {
+      if (appending) {
+        const uint32_t w[4] = {new_row.x, new_row.y, new_row.z, new_row.w};
+        float x[8], amax = 0.f;
+        bool finite = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[2 * i] = __uint_as_float(w[i] << 16);
+          x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          finite &= isfinite(x[i]);
+          amax = fmaxf(amax, fabsf(x[i]));
+        }
+#pragma unroll
+        for (int m = 1; m < 16; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));  // the half
+        new_ok = __all_sync(kFullMask, finite);
+        if (!new_ok && lane == 0) record_error(a.err, PKV_DEV_BAD_VALUE);
+        new_scale = __fdiv_rn(amax, 127.0f);
+        uint32_t pk[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          int cd = 0;
+          if (new_scale != 0.f) cd = max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], new_scale))));
+          pk[i / 4] |= (uint32_t)(cd & 0xff) << (8 * (i % 4));
+        }
+        new_codes = make_uint2(pk[0], pk[1]);
+      }
+    }
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
@@ -719,13 +756,31 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       const int lo = max(s_lo[cc.b] - tok0, 0);
       const int hi = min(s_len[cc.b] - tok0, 16);
       mask &= ((1u << hi) - 1u) & ~((1u << lo) - 1u);
-      if (appending && mask != 0u && s_len[cc.b] - 1 - tok0 < 16) {
+      if (appending && new_ok && mask != 0u && s_len[cc.b] - 1 - tok0 < 16) {
         t_new = s_len[cc.b] - 1 - tok0;
+        const size_t prow = ((size_t)Wb.phys[slot] * a.Hkv + cc.g) * 16 + t_new;  // pool row
         // the tile was read before the append: put the new K row in it and in the pool
-        if (lane < 16 && new_lane) {
-          *reinterpret_cast<uint4*>(Wt.k[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
-          *reinterpret_cast<uint4*>(a.k_pool_out + (((size_t)Wb.phys[slot] * a.Hkv + cc.g) * 16 + t_new) * D +
-                                    new_chunk * 8) = new_row;
+        if constexpr (Q8) {
+          // codes of elements [8c, 8c + 8) are the half (c & 1) of 16-byte chunk c / 2; both
+          // rows' scales go in now (the softmax reads the V scales before the V tile lands)
+          if (lane < 16 && new_lane) {
+            *reinterpret_cast<uint2*>(Wt.k[slot] + chunk_offset<D, SPARSE, Q8>(t_new, new_chunk >> 1) +
+                                      (new_chunk & 1) * 8) = new_codes;
+            *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(a.k_pool_out) + prow * D + new_chunk * 8) =
+                new_codes;
+          }
+          if (lane == 0) {
+            warps_scales[warp].k[slot][t_new] = new_scale;
+            a.k_scale_out[prow] = new_scale;
+          } else if (lane == 16) {
+            warps_scales[warp].v[slot][t_new] = new_scale;
+            a.v_scale_out[prow] = new_scale;
+          }
+        } else {
+          if (lane < 16 && new_lane) {
+            *reinterpret_cast<uint4*>(Wt.k[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
+            *reinterpret_cast<uint4*>(a.k_pool_out + prow * D + new_chunk * 8) = new_row;
+          }
         }
         __syncwarp();
       }
@@ -859,10 +914,17 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         break;
       }
       if (t_new >= 0) {  // append mode: the new V row, into the tile and the pool
+        const size_t prow = ((size_t)Wb.phys[slot] * a.Hkv + cc.g) * 16 + t_new;
         if (lane >= 16 && new_lane) {
-          *reinterpret_cast<uint4*>(Wt.v[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
-          *reinterpret_cast<uint4*>(a.v_pool_out + (((size_t)Wb.phys[slot] * a.Hkv + cc.g) * 16 + t_new) * D +
-                                    new_chunk * 8) = new_row;
+          if constexpr (Q8) {
+            *reinterpret_cast<uint2*>(Wt.v[slot] + chunk_offset<D, SPARSE, Q8>(t_new, new_chunk >> 1) +
+                                      (new_chunk & 1) * 8) = new_codes;
+            *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(a.v_pool_out) + prow * D + new_chunk * 8) =
+                new_codes;
+          } else {
+            *reinterpret_cast<uint4*>(Wt.v[slot] + chunk_offset<D, SPARSE>(t_new, new_chunk)) = new_row;
+            *reinterpret_cast<uint4*>(a.v_pool_out + prow * D + new_chunk * 8) = new_row;
+          }
         }
         __syncwarp();
       }

@@ -40,6 +40,8 @@ struct DecodeArgs {
   float* part_o;                 // [2 ranges, G, D] unnormalised partial outputs
   const float* k_scale;          // INT8 pools: [NB, Hkv, 16] fp32 scale of each K row
   const float* v_scale;          //   (likewise V); the pools then hold int8 codes
+  float* k_scale_out;            // INT8 append mode: the scale pools again, writable
+  float* v_scale_out;
   float* logits;                 // scores mode: [B, Hq, score_stride] base-2 logits of attended keys
   float* lse;                    // scores mode: [B, Hq] natural log-sum-exp of each row
   float* scores;                 // scores mode: [B, Hkv, score_stride] accumulated scores

@@ -21,7 +21,7 @@ def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _lib.header_functions()
-    assert len(declared) == 20
+    assert len(declared) == 21
     nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     for name in declared:
@@ -136,6 +136,14 @@ def test_host_validation_codes(lib):
     assert q8_scores(stride=0) == c["PKV_ERR_DIMS"]
     assert q8_scores() == c["PKV_ERR_WORKSPACE"]                     # 16-byte workspace
     assert q8_scores(dims=_dims(B=0)) == c["PKV_OK"]
+
+    def q8_append_decode(kn=0x50000, dims=None):
+        return lib.pkv_paged_decode_attention_append_q8(
+            P(0x10000), P(0x10000), P(0x10000), P(0x10000), P(0x30000), P(0x40000), P(kn), P(0x60000),
+            P(0x10000), P(0x10000), ctypes.c_float(0.1), 0, P(0x20000), 16, ctypes.byref(dims or _dims()), None, None)
+    assert q8_append_decode(kn=0) == c["PKV_ERR_NULL_POINTER"]
+    assert q8_append_decode(kn=0x50008) == c["PKV_ERR_ALIGNMENT"]
+    assert q8_append_decode() == c["PKV_ERR_WORKSPACE"]                # 16-byte workspace
 
     def q8_compact(dks=0x30000, max_kept=8):
         return lib.pkv_kv_compact_q8(P(0x10000), P(0x10000), P(dks), P(0x40000), P(0x50000), 8, 4, P(0x10000),

@@ -168,3 +168,91 @@ def test_llama8b_full_size_sampled_rows():
     rows = sorted({0, B * hq - 1} | set(rng.choice(B * hq, size=40, replace=False).tolist()))
     ref = _ref(c, rows=rows)
     _close(out.view(B * hq, d)[rows], ref, "llama8b INT8 sampled rows")
+
+
+def _slots_at_last(bt, lens):
+    return np.array([int(bt[b, (L - 1) // 16]) * 16 + (L - 1) % 16 for b, L in enumerate(lens)], dtype=np.int64)
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(128, 8, 2), (64, 6, 3), (128, 32, 8)])
+@pytest.mark.parametrize("window", [0, 16])
+def test_fused_append_q8_equals_append_then_decode(d, hq, hkv, window):
+    """paged_decode_attention_append_q8: the pools end as kv_append_q8 leaves them (bit for
+    bit, against the oracle), and the output matches the oracle decode over those pools and
+    the GPU's own append-then-decode bit for bit."""
+    lens = [1, 15, 16, 17, 33, 100, 257]
+    c = _case(lens, hq, hkv, d, seed=90 + d + window)
+    g = torch.Generator().manual_seed(91)
+    k_new = (rand_bf16((len(lens), hkv, d), g) * torch.logspace(-2, 2, len(lens)).view(-1, 1, 1)).to(torch.bfloat16)
+    v_new = rand_bf16((len(lens), hkv, d), g)
+    k_new[2, 0] = 0.0                                      # a zero row: scale 0, codes 0
+    n = lambda t: t.cpu().numpy()
+    slots = _slots_at_last(n(c["bt"]), lens)
+    ref_pools = oracle.kv_append_q8(n(c["kq"]), n(c["vq"]), n(c["ks"]), n(c["vs"]), bits(k_new), bits(v_new), slots)
+    # the same step as two calls, for the bit-identical comparison
+    two = {k: c[k].clone() for k in ("kq", "vq", "ks", "vs")}
+    pkv.kv_append_q8(two["kq"], two["vq"], two["ks"], two["vs"], k_new.to(DEV), v_new.to(DEV),
+                     torch.from_numpy(slots).to(DEV))
+    out_two = pkv.paged_decode_attention_q8(c["q"], two["kq"], two["vq"], two["ks"], two["vs"], c["bt"], c["lens"],
+                                            c["scale"], window).clone()
+    err = pkv.new_error_word(DEV)
+    out = pkv.paged_decode_attention_append_q8(c["q"], c["kq"], c["vq"], c["ks"], c["vs"], k_new.to(DEV),
+                                               v_new.to(DEV), c["bt"], c["lens"], c["scale"], window, error_word=err)
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    for name, want in zip(("kq", "vq", "ks", "vs"), ref_pools):
+        assert np.array_equal(n(c[name]), want), name
+    assert torch.equal(out, out_two)
+    _close(out, oracle.paged_decode_q8(bits(c["q"]), *[ref_pools[i] for i in (0, 2, 1, 3)], n(c["bt"]),
+                                       n(c["lens"]), c["scale"], window), f"fused INT8 append d={d} w={window}")
+
+
+def test_fused_append_q8_non_finite_row_is_reported_and_skipped():
+    lens = [40, 70]
+    c = _case(lens, 8, 2, 128, seed=92)
+    k_new = torch.ones((2, 2, 128), dtype=torch.bfloat16)
+    v_new = torch.ones((2, 2, 128), dtype=torch.bfloat16)
+    v_new[1, 1, 7] = float("inf")                          # sequence 1, kv head 1
+    before = {k: c[k].clone() for k in ("kq", "vq", "ks", "vs")}
+    err = pkv.new_error_word(DEV)
+    pkv.paged_decode_attention_append_q8(c["q"], c["kq"], c["vq"], c["ks"], c["vs"], k_new.to(DEV), v_new.to(DEV),
+                                         c["bt"], c["lens"], c["scale"], error_word=err)
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == pkv.header_constants()["PKV_DEV_BAD_VALUE"]
+    blk1, off1 = int(c["bt"][1, 69 // 16]), 69 % 16
+    for k in ("kq", "vq", "ks", "vs"):
+        assert torch.equal(c[k][blk1, 1, off1], before[k][blk1, 1, off1]), k   # (1, 1): not written
+    blk0, off0 = int(c["bt"][0, 39 // 16]), 39 % 16
+    assert torch.all(c["kq"][blk0, :, off0] == 127) and torch.all(c["kq"][blk1, 0, off1] == 127)
+
+
+def test_fused_append_q8_llama8b_full_size_sampled_rows():
+    wl = W.WORKLOADS["llama8b"]
+    lens = W.context_lengths(wl)
+    B, hq, hkv, d = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    mb = int((lens.max() + 15) // 16)
+    nb = B * mb + 64
+    g = torch.Generator(device=DEV).manual_seed(93)
+    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    ks = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
+    vs = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
+    bt = torch.randperm(nb, device=DEV, generator=g)[: B * mb].view(B, mb).to(torch.int32)
+    q = torch.randn((B, hq, d), generator=g, device=DEV).to(torch.bfloat16)
+    k_new = torch.randn((B, hkv, d), generator=g, device=DEV).to(torch.bfloat16)
+    v_new = torch.randn((B, hkv, d), generator=g, device=DEV).to(torch.bfloat16)
+    n = lambda t: t.cpu().numpy()
+    slots = _slots_at_last(n(bt), [int(x) for x in lens])
+    ref_pools = oracle.kv_append_q8(n(kq), n(vq), n(ks), n(vs), bits(k_new), bits(v_new), slots)
+    err = pkv.new_error_word(DEV)
+    out = pkv.paged_decode_attention_append_q8(q, kq, vq, ks, vs, k_new, v_new, bt, lens.to(DEV), d ** -0.5,
+                                               error_word=err)
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    for name, got, want in zip(("kq", "vq", "ks", "vs"), (kq, vq, ks, vs), ref_pools):
+        assert np.array_equal(n(got), want), name
+    rng = np.random.default_rng(94)
+    rows = sorted({0, B * hq - 1} | set(rng.choice(B * hq, size=40, replace=False).tolist()))
+    ref = oracle.paged_decode_q8(bits(q), ref_pools[0], ref_pools[2], ref_pools[1], ref_pools[3], n(bt), n(lens),
+                                 d ** -0.5, rows=rows)
+    _close(out.view(B * hq, d)[rows], ref, "llama8b fused INT8 append, sampled rows")

@@ -533,10 +533,19 @@ def _q8_row(pkv, W, dev, stream, args, hbm):
         pkv.paged_decode_attention_scores_q8(c["q"], kq, vq, ks, vs, c["block_tables"], c["context_lens"],
                                              c["scale"], acc, out=out, lse=lse, logits=logits, workspace=ws,
                                              stream=stream)
+    def q8_fused():  # this step's rows quantized into the pools inside the decode
+        pkv.paged_decode_attention_append_q8(c["q"], kq, vq, ks, vs, c["k_new"], c["v_new"], c["block_tables"],
+                                             c["context_lens"], c["scale"], out=out, workspace=ws, stream=stream)
+
+    def q8_two_calls():
+        pkv.kv_append_q8(kq, vq, ks, vs, c["k_new"], c["v_new"], c["slot_mapping"], stream=stream)
+        q8()
     steps = max(5, args.steps // 4)
     ms_plain = _time(plain, args.warmup, steps, dev, stream)
     ms_q8 = _time(q8, args.warmup, steps, dev, stream)
     ms_q8_scored = _time(q8_scored, args.warmup, steps, dev, stream)
+    ms_q8_fused = _time(q8_fused, args.warmup, steps, dev, stream)
+    ms_q8_two = _time(q8_two_calls, args.warmup, steps, dev, stream)
     lens = c["context_lens"].cpu()
     tokens = int(lens.to(torch.int64).sum())
     blocks = int(((lens.to(torch.int64) + 15) // 16).sum())
@@ -545,6 +554,7 @@ def _q8_row(pkv, W, dev, stream, args, hbm):
     del c, kq, vq, ks, vs, ws, out, acc, logits
     return {"ms": round(ms_q8, 4), "ms_bf16": round(ms_plain, 4), "speedup": round(ms_plain / ms_q8, 3),
             "ms_with_scores": round(ms_q8_scored, 4), "scores_overhead": round(ms_q8_scored / ms_q8 - 1.0, 4),
+            "ms_append_fused": round(ms_q8_fused, 4), "ms_append_then_decode": round(ms_q8_two, 4),
             "tokens_per_s": round(wl.batch / (ms_q8 * 1e-3), 1), "bytes": nbytes,
             "gbs": round(nbytes / (ms_q8 * 1e-3) / 1e9, 1), "frac": round(nbytes / (ms_q8 * 1e-3) / 1e9 / hbm, 4),
             "l2": "0.29 GB of INT8 K/V + scales per call (> L2)"}

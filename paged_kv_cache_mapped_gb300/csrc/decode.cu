@@ -678,12 +678,14 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
 #pragma unroll
       for (int i = 0; i < 2 * KS; ++i) qb[i] = qraw[i];
     }
-    if (appending && new_lane) {
+    // only the range holding the segment's last unit (position L - 1) appends
+    const bool seg_appends = appending && seg_begin + nb - 1 >= u0 && seg_begin + nb - 1 < u0 + nunits;
+    if (seg_appends && new_lane) {
       const __nv_bfloat16* src = (lane >= 16 ? a.v_new : a.k_new) + ((size_t)c.b * a.Hkv + c.g) * D + new_chunk * 8;
       new_row = __ldg(reinterpret_cast<const uint4*>(src));
     }
     if constexpr (Q8) {
-      if (appending) {
+      if (seg_appends) {
         const uint32_t w[4] = {new_row.x, new_row.y, new_row.z, new_row.w};
         float x[8], amax = 0.f;
         bool finite = true;

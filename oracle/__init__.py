@@ -23,6 +23,8 @@ Parity status of each function (what pins it; see ``tests/test_oracle_*.py``):
   kv_append_q8     -- pinned by a dict-of-slots model over quantize_rows
   paged_decode_q8  -- pinned by equality with paged_decode where code * scale is a bf16 value,
                       and by torch SDPA (fp64) on the dequantized contiguous K/V
+  sparse_decode_q8 -- pinned by equality with sparse_decode where code * scale is a bf16 value,
+                      and kept = all == paged_decode_q8
   decode_scores_q8 -- pinned by equality with decode_scores where code * scale is a bf16 value,
                       and by torch softmax (fp64) on the dequantized K
   compact_q8       -- pinned by a dict-of-slots model (codes and row scales move together) and
@@ -113,7 +115,9 @@ def _load():
                                               i32, i32, i64, i32]
             lib.oracle_rolling_admit_q8.argtypes = [P, P, P, P, P, i64, i32, P, P, P, P, P, P, i32, i32,
                                                     i32, i32, i32, i32]
-            for name in ("oracle_kv_append", "oracle_paged_decode", "oracle_sparse_decode",
+            lib.oracle_sparse_decode_q8.argtypes = [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                                    i64, i32, f64, P, i64]
+            for name in ("oracle_sparse_decode_q8", "oracle_kv_append", "oracle_paged_decode", "oracle_sparse_decode",
                          "oracle_select_topk", "oracle_compact", "oracle_decode_scores",
                          "oracle_rolling_admit", "oracle_quantize_rows", "oracle_kv_append_q8",
                          "oracle_paged_decode_q8", "oracle_prefill_scores", "oracle_decode_scores_q8",
@@ -460,3 +464,28 @@ def rolling_admit_q8(k_codes, v_codes, k_scales, v_scales, block_tables, slot_po
                                            _ptr(pos), _ptr(sc), _ptr(kl), _ptr(lens), _ptr(kn), _ptr(vn), b, hkv,
                                            d, cap, int(n_sink), int(n_recent)), "rolling_admit_q8")
     return kc, vc, ks, vs, pos, sc, kl
+
+
+def sparse_decode_q8(q, k_codes, k_scales, v_codes, v_scales, block_tables, context_lens, kept, kept_lens, scale,
+                     rows=None):
+    """sparse_decode over INT8 pools (values code * scale).  Shapes as sparse_decode."""
+    q = _arr(q, np.uint16)
+    kc = _arr(k_codes, np.int8)
+    vc = _arr(v_codes, np.int8)
+    ks = _arr(k_scales, np.float32)
+    vs = _arr(v_scales, np.float32)
+    bt = _arr(block_tables, np.int32)
+    lens = _arr(context_lens, np.int32)
+    kept = _arr(kept, np.int32)
+    kl = _arr(kept_lens, np.int32)
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = kc.shape
+    assert bs == 16 and vc.shape == kc.shape and ks.shape == (nb, hkv, 16) and vs.shape == ks.shape
+    assert kept.shape[:2] == (b, hkv)
+    r, n = _rows(rows, b, hq)
+    out = np.zeros((n, d), dtype=np.float64)
+    _check(_load().oracle_sparse_decode_q8(_ptr(out), _ptr(q), _ptr(kc), _ptr(ks), _ptr(vc), _ptr(vs), _ptr(bt),
+                                           _ptr(lens), _ptr(kept), _ptr(kl), kept.shape[2], b, hq, hkv, d, nb,
+                                           bt.shape[1], float(scale), None if r is None else _ptr(r), n),
+           "sparse_decode_q8")
+    return out.reshape(b, hq, d) if rows is None else out

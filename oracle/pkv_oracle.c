@@ -343,12 +343,13 @@ int oracle_paged_decode_q8(double* out, const uint16_t* q, const int8_t* k_codes
  * kept[b][g][0 : kept_lens[b]] ([novita] section "System model": the layer attends only the
  * KV pairs it retained).  The list must be strictly ascending and inside [0, L_b).
  */
-int oracle_sparse_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
-                         const uint16_t* v_cache, const int32_t* block_tables,
-                         const int32_t* context_lens, const int32_t* kept, const int32_t* kept_lens,
-                         int max_kept, int batch, int num_q_heads, int num_kv_heads,
-                         int head_dim, int64_t num_blocks, int max_blocks_per_seq, double scale,
-                         const int64_t* row_ids, int64_t n_rows) {
+static int sparse_decode_pools(double* out, const uint16_t* q, const pool_t* k_pool,
+                               const pool_t* v_pool, const int32_t* block_tables,
+                               const int32_t* context_lens, const int32_t* kept,
+                               const int32_t* kept_lens, int max_kept, int batch, int num_q_heads,
+                               int num_kv_heads, int head_dim, int64_t num_blocks,
+                               int max_blocks_per_seq, double scale, const int64_t* row_ids,
+                               int64_t n_rows) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kept < 0)
     return ORC_ERR_ARG;
   if (num_q_heads % num_kv_heads != 0) return ORC_ERR_ARG;
@@ -376,9 +377,8 @@ int oracle_sparse_decode(double* out, const uint16_t* q, const uint16_t* k_cache
           if (list[j] < 0 || list[j] >= context_lens[b]) st = ORC_ERR_INDEX;
           if (j > 0 && list[j] <= list[j - 1]) st = ORC_ERR_INDEX;
         }
-        pool_t k_pool = {k_cache, NULL, NULL}, v_pool = {v_cache, NULL, NULL};
         if (st == ORC_OK)
-          st = attend_one_row(out + r * head_dim, q + row * head_dim, &k_pool, &v_pool,
+          st = attend_one_row(out + r * head_dim, q + row * head_dim, k_pool, v_pool,
                               block_tables + (int64_t)b * max_blocks_per_seq,
                               max_blocks_per_seq, num_blocks, num_kv_heads, head_dim, g,
                               scale, tokens, n);
@@ -391,6 +391,32 @@ int oracle_sparse_decode(double* out, const uint16_t* q, const uint16_t* k_cache
     }
   }
   return status;
+}
+
+int oracle_sparse_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
+                         const uint16_t* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, const int32_t* kept, const int32_t* kept_lens,
+                         int max_kept, int batch, int num_q_heads, int num_kv_heads,
+                         int head_dim, int64_t num_blocks, int max_blocks_per_seq, double scale,
+                         const int64_t* row_ids, int64_t n_rows) {
+  pool_t k_pool = {k_cache, NULL, NULL}, v_pool = {v_cache, NULL, NULL};
+  return sparse_decode_pools(out, q, &k_pool, &v_pool, block_tables, context_lens, kept,
+                             kept_lens, max_kept, batch, num_q_heads, num_kv_heads, head_dim,
+                             num_blocks, max_blocks_per_seq, scale, row_ids, n_rows);
+}
+
+/* Sparse decode attention over INT8 pools: every K and V element read as code * row scale. */
+int oracle_sparse_decode_q8(double* out, const uint16_t* q, const int8_t* k_codes,
+                            const float* k_scales, const int8_t* v_codes, const float* v_scales,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            const int32_t* kept, const int32_t* kept_lens, int max_kept,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int64_t num_blocks, int max_blocks_per_seq, double scale,
+                            const int64_t* row_ids, int64_t n_rows) {
+  pool_t k_pool = {NULL, k_codes, k_scales}, v_pool = {NULL, v_codes, v_scales};
+  return sparse_decode_pools(out, q, &k_pool, &v_pool, block_tables, context_lens, kept,
+                             kept_lens, max_kept, batch, num_q_heads, num_kv_heads, head_dim,
+                             num_blocks, max_blocks_per_seq, scale, row_ids, n_rows);
 }
 
 /*

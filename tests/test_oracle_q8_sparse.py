@@ -8,7 +8,9 @@ rolling_admit_q8) to facts outside them.
     unchanged), and dequantize-then-compact == compact-then-dequantize;
   * rolling admission: the slot choice, positions, scores and counts of the bf16 admission on
     the same state, the admitted rows equal to quantize_rows of the new token, every other
-    row unchanged; a non-finite new row refused.
+    row unchanged; a non-finite new row refused;
+  * sparse decode over INT8 pools: equal bit for bit to the bf16 sparse decode where every
+    code * scale is a bf16 value, and to the INT8 paged decode when every token is kept.
 """
 import numpy as np
 import pytest
@@ -218,3 +220,51 @@ def test_rolling_admit_q8_refuses_a_non_finite_row():
         oracle.rolling_admit_q8(kc, kc, ks, ks, np.array([[1]], np.int32), np.zeros((B, hkv, cap), np.int32),
                                 np.zeros((B, hkv, cap), np.float32), np.zeros(B, np.int32), np.ones(B, np.int32),
                                 kn, vn, 0, 1)
+
+
+def _kept_lists(rng, lens, hkv, max_kept):
+    B = len(lens)
+    kept = np.full((B, hkv, max_kept), -1, dtype=np.int32)
+    kl = np.array([min(L, max_kept) for L in lens], dtype=np.int32)
+    for b in range(B):
+        for g in range(hkv):
+            kept[b, g, :kl[b]] = np.sort(rng.choice(lens[b], size=kl[b], replace=False)) if kl[b] else []
+    return kept, kl
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 2, 64), (32, 8, 128)])
+def test_sparse_q8_equals_bf16_sparse_on_representable_values(hq, hkv, d):
+    rng = np.random.default_rng(hq + d)
+    lens = [70, 1, 0, 150]
+    nb = 60
+    kc, ks, kb = _pow2_pool(nb, hkv, d, rng)
+    vc, vs, vb = _pow2_pool(nb, hkv, d, rng)
+    g = torch.Generator().manual_seed(hq * d + 1)
+    q = bits(rand_bf16((len(lens), hq, d), g))
+    bt = torch.randperm(nb, generator=g)[: len(lens) * 10].view(len(lens), 10).to(torch.int32).numpy()
+    kept, kl = _kept_lists(rng, lens, hkv, 40)
+    L = np.array(lens, np.int32)
+    got = oracle.sparse_decode_q8(q, kc, ks, vc, vs, bt, L, kept, kl, d ** -0.5)
+    ref = oracle.sparse_decode(q, kb, vb, bt, L, kept, kl, d ** -0.5)
+    assert np.array_equal(got, ref)
+
+
+def test_sparse_q8_with_every_token_kept_equals_paged_q8():
+    rng = np.random.default_rng(11)
+    lens = [37, 64, 1]
+    hq, hkv, d, nb = 8, 2, 64, 20
+    kc = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
+    vc = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
+    ks = rng.random((nb, hkv, 16)).astype(np.float32)
+    vs = rng.random((nb, hkv, 16)).astype(np.float32)
+    g = torch.Generator().manual_seed(12)
+    q = bits(rand_bf16((3, hq, d), g))
+    bt = rng.permutation(nb)[:12].reshape(3, 4).astype(np.int32)
+    max_kept = 64
+    kept = np.full((3, hkv, max_kept), -1, dtype=np.int32)
+    for b, L in enumerate(lens):
+        kept[b, :, :L] = np.arange(L)
+    L = np.array(lens, np.int32)
+    got = oracle.sparse_decode_q8(q, kc, ks, vc, vs, bt, L, kept, L.copy(), d ** -0.5)
+    ref = oracle.paged_decode_q8(q, kc, ks, vc, vs, bt, L, d ** -0.5)
+    assert np.array_equal(got, ref)

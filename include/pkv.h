@@ -381,6 +381,20 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
                    void* stream);
 
 /*
+ * pkv_sparse_decode_attention_q8 -- pkv_sparse_decode_attention over INT8 pools: the attended set
+ * of (b, kv head g) is its kept list, and every K and V element is read as code * scale of its
+ * row (the arithmetic of pkv_paged_decode_attention_q8).  Rows are gathered one by one (the
+ * codes by bulk copy, the two row scales by 4-byte asynchronous copies).
+ *   k_codes, v_codes, k_scales, v_scales : as pkv_paged_decode_attention_q8.
+ *   other arguments    : as pkv_sparse_decode_attention (same workspace, same errors).
+ */
+int pkv_sparse_decode_attention_q8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                                   const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                                   const int32_t* context_lens, const int32_t* kept_index_lists,
+                                   const int32_t* kept_lens, int32_t max_kept, float scale, void* workspace,
+                                   size_t workspace_bytes, const pkv_dims* dims, int32_t* error_word, void* stream);
+
+/*
  * pkv_kv_compact_q8 -- pkv_kv_compact over INT8 pools: each kept row's codes and its fp32 row
  * scale move together, so the compact pool holds the same values (code * scale).
  *   dst_k_codes, dst_v_codes, src_k_codes, src_v_codes : [NB, Hkv, 16, d] int8 pools.

@@ -25,7 +25,7 @@ __all__ = [
     "paged_decode_attention_q8",
     "prefill_window_scores",
     "paged_decode_attention_scores_q8", "kv_compact_q8", "kv_rolling_admit_q8",
-    "paged_decode_attention_append_q8",
+    "paged_decode_attention_append_q8", "sparse_decode_attention_q8",
 ]
 
 BLOCK_SIZE = 16
@@ -335,6 +335,25 @@ def paged_decode_attention_append_q8(q, k_codes, v_codes, k_scales, v_scales, k_
         _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(k_new), _ptr(v_new),
         _ptr(block_tables), _ptr(context_lens), float(scale), int(window), _ptr(workspace), workspace.numel(),
         ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+    return out
+
+
+def sparse_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens,
+                               kept_index_lists, kept_lens, scale, *, out=None, workspace=None, error_word=None,
+                               stream=None):
+    """sparse_decode_attention over INT8 pools (each element code * its row's scale)."""
+    dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
+    _need(kept_index_lists, "kept_index_lists", torch.int32, 3, dev)
+    _need(kept_lens, "kept_lens", torch.int32, 1, dev)
+    if kept_index_lists.shape[:2] != (dims.batch, dims.num_kv_heads) or kept_lens.shape[0] != dims.batch:
+        raise ValueError("kept_index_lists must be [B, Hkv, max_kept] and kept_lens [B]")
+    max_kept = kept_index_lists.shape[2]
+    nbytes = int(load().pkv_sparse_decode_workspace_bytes(ctypes.byref(dims), max_kept))
+    out, workspace = _out_ws(q, out, workspace, nbytes)
+    check("pkv_sparse_decode_attention_q8", load().pkv_sparse_decode_attention_q8(
+        _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_tables),
+        _ptr(context_lens), _ptr(kept_index_lists), _ptr(kept_lens), max_kept, float(scale), _ptr(workspace),
+        workspace.numel(), ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
     return out
 
 

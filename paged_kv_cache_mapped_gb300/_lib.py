@@ -79,6 +79,7 @@ def load():
                                                            SZ, D, P, P]),
             "pkv_paged_decode_attention_append_q8": (I32, [P, P, P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, P,
                                                            P]),
+            "pkv_sparse_decode_attention_q8": (I32, [P, P, P, P, P, P, P, P, P, P, I32, F32, P, SZ, D, P, P]),
             "pkv_kv_compact_q8": (I32, [P, P, P, P, P, I32, I32, P, P, P, P, P, P, P, P, I32, D, P, P]),
             "pkv_kv_rolling_admit_q8": (I32, [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, D, P, P]),
             "pkv_sparse_decode_workspace_bytes": (SZ, [D, I32]),

@@ -23,8 +23,9 @@ constexpr int kNumGroups = 1;
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
-  size_t max_dyn_smem[2][5] = {};  // [head_dim index][mode: dense, sparse, dense + scores,
-                                   //   dense INT8, INT8 + scores]: opt-in minus static shared memory
+  size_t max_dyn_smem[2][6] = {};  // [head_dim index][mode: dense, sparse, dense + scores,
+                                   //   dense INT8, INT8 + scores, sparse INT8]: opt-in minus static
+                                   //   shared memory
   int merge_ctas_per_sm[2] = {};   // [head_dim index]: resident merge CTAs per SM
 };
 
@@ -55,9 +56,9 @@ const DeviceInfo* device_info(int* status) {
     }
     for (int hd = 0; hd < kNumHeadDims; ++hd) {
       for (int gi = 0; gi < kNumGroups; ++gi) {
-        for (int sp = 0; sp < 5; ++sp) {
+        for (int sp = 0; sp < 6; ++sp) {
           const DecodeKernel k =
-              decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp == 1, sp == 2 || sp == 4, sp >= 3);
+              decode_kernel(hd == 0 ? 128 : 64, kGroups[gi], sp == 1 || sp == 5, sp == 2 || sp == 4, sp >= 3);
           if (k.split == nullptr) continue;
           cudaFuncAttributes fa{};
           cudaError_t e = cudaFuncGetAttributes(&fa, k.split);
@@ -255,7 +256,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
     return PKV_ERR_ALIGNMENT;
   const int group = dims->num_q_heads / dims->num_kv_heads;
   if (q8 != nullptr) {
-    if (sparse) return PKV_ERR_ARGUMENT;
+    if (sparse && k_new != nullptr) return PKV_ERR_ARGUMENT;
     if (!q8->k_scale || !q8->v_scale) return PKV_ERR_NULL_POINTER;
     if (!aligned16(q8->k_scale) || !aligned16(q8->v_scale)) return PKV_ERR_ALIGNMENT;
   }
@@ -281,7 +282,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   const DeviceInfo* info = device_info(&st);
   if (!info) return st;
   const size_t smem = decode_smem_bytes(dims->head_dim, sparse, dims->batch);
-  const int mode = sparse ? 1 : (q8 ? (score_out ? 4 : 3) : (score_out ? 2 : 0));
+  const int mode = sparse ? (q8 ? 5 : 1) : (q8 ? (score_out ? 4 : 3) : (score_out ? 2 : 0));
   if (smem > info->max_dyn_smem[head_dim_index(dims->head_dim)][mode])
     return PKV_ERR_DIMS;
   int per_sm = 0;
@@ -290,10 +291,12 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   if (per_sm < 1) return PKV_ERR_DIMS;
 
   DecodeArgs a{};
-  if (q8 != nullptr) {
-    st = encode_pool_map_q8(&a.tmap_k, k_cache, pool_rows, dims->head_dim);
-    if (st == PKV_OK) st = encode_pool_map_q8(&a.tmap_v, v_cache, pool_rows, dims->head_dim);
-    if (st != PKV_OK) return st;
+  if (q8 != nullptr) {  // the gather form copies rows one by one: no tensor maps
+    if (!sparse) {
+      st = encode_pool_map_q8(&a.tmap_k, k_cache, pool_rows, dims->head_dim);
+      if (st == PKV_OK) st = encode_pool_map_q8(&a.tmap_v, v_cache, pool_rows, dims->head_dim);
+      if (st != PKV_OK) return st;
+    }
     a.k_scale = q8->k_scale;
     a.v_scale = q8->v_scale;
   } else if (!sparse) {
@@ -538,6 +541,17 @@ int pkv_sparse_decode_attention(void* out, const void* q, const void* k_cache, c
   return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, kept_index_lists,
                        kept_lens, max_kept, scale, 0, workspace, workspace_bytes, dims, error_word,
                        stream, true);
+}
+
+int pkv_sparse_decode_attention_q8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                                   const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                                   const int32_t* context_lens, const int32_t* kept_index_lists,
+                                   const int32_t* kept_lens, int32_t max_kept, float scale, void* workspace,
+                                   size_t workspace_bytes, const pkv_dims* dims, int32_t* error_word, void* stream) {
+  const Q8Scales q8{k_scales, v_scales};
+  return decode_common(out, q, k_codes, v_codes, block_tables, context_lens, kept_index_lists, kept_lens, max_kept,
+                       scale, 0, workspace, workspace_bytes, dims, error_word, stream, true, nullptr, nullptr,
+                       nullptr, &q8);
 }
 
 int pkv_kv_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* score_accum,

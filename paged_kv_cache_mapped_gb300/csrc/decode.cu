@@ -56,8 +56,8 @@ template <int D, bool SPARSE, bool Q8 = false>
 struct Geo {
   static constexpr int kRow = Q8 ? D : D * 2;              // bytes per K/V row in HBM
   static constexpr int kBoxes = Q8 ? 1 : D / 64;           // dense: 128-byte column boxes per row
-  static constexpr int kPitch = D * 2 + 16;                // sparse: padded row pitch in smem
-  static constexpr int kTile = Q8 ? 16 * D : (SPARSE ? 16 * kPitch : 16 * D * 2);  // bytes per tile
+  static constexpr int kPitch = kRow + 16;                 // sparse: padded row pitch in smem
+  static constexpr int kTile = SPARSE ? 16 * kPitch : 16 * kRow;  // bytes per tile
   static constexpr int kKSteps = D / 16;                   // k-steps of q.K, m-tiles of P.V
   static constexpr int kRing = Q8 ? ((D == 128) ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
                                   : ((D == 128) ? PKV_RING_D128 : PKV_RING_D64);
@@ -73,13 +73,13 @@ struct Geo {
 // Either way the 8 rows an ldmatrix reads land in 8 different bank groups.
 template <int D, bool SPARSE, bool Q8 = false>
 __device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
-  if constexpr (Q8) {
+  if constexpr (SPARSE) {
+    return (uint32_t)(r * Geo<D, SPARSE, Q8>::kPitch + c * 16);
+  } else if constexpr (Q8) {
     if constexpr (D == 128)
       return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
     else
       return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
-  } else if constexpr (SPARSE) {
-    return (uint32_t)(r * Geo<D, SPARSE>::kPitch + c * 16);
   } else {
     return (uint32_t)((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
   }
@@ -268,7 +268,6 @@ template <int D, bool SPARSE, bool SCORES, bool Q8>
 __global__ void __launch_bounds__(kDecodeWarps * 32, Q8 ? PKV_Q8_MIN_CTAS : 0)
 decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   static_assert(!(SPARSE && SCORES), "scores are emitted by the dense decode only");
-  static_assert(!(Q8 && SPARSE), "INT8 pools are read by the dense decode only");
   using GE = Geo<D, SPARSE, Q8>;
   using WT = WarpTiles<D, SPARSE, Q8>;
   using WB = WarpSlots<D, SPARSE, Q8>;
@@ -546,8 +545,17 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       }
       const int row = __shfl_sync(kFullMask, sp_row, ((k & 1) << 4) | r);
       const bool ok = row >= 0;
-      const size_t src = (size_t)(ok ? row : 0) * D;
+      const size_t src = (size_t)(ok ? row : 0) * GE::kRow;  // bytes
       const uint32_t vmask = __ballot_sync(kFullMask, ok) & 0xffffu;  // K and V lanes agree
+      if constexpr (Q8) {
+        // the row's scale (K lanes: K, V lanes: V) by a 4-byte asynchronous copy that the K
+        // barrier tracks (the softmax reads the V scales before the V rows land); every lane
+        // registers with the barrier before lane 0's expect-tx arrival below
+        auto& Ws = warps_scales[warp];
+        if (ok) cp_async_4(is_v ? &Ws.v[slot][r] : &Ws.k[slot][r], (is_v ? a.v_scale : a.k_scale) + row);
+        cp_async_mbar_arrive(&Wb.bar_k[slot]);
+        __syncwarp();
+      }
       if (lane == 0) {
         Wb.meta[slot] = vmask;
         mbar_arrive_expect_tx(&Wb.bar_k[slot], __popc(vmask) * GE::kRow);
@@ -556,7 +564,8 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       __syncwarp();
       if (ok) {
         unsigned char* dst = (is_v ? Wt.v[slot] : Wt.k[slot]) + r * GE::kPitch;
-        bulk_g2s(dst, (is_v ? a.v_cache : a.k_cache) + src, GE::kRow, is_v ? &Wb.bar_v[slot] : &Wb.bar_k[slot], pol);
+        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(is_v ? a.v_cache : a.k_cache) + src, GE::kRow,
+                 is_v ? &Wb.bar_v[slot] : &Wb.bar_k[slot], pol);
       }
       advance(ic, s_nb, a.B, a.Hkv);
     }
@@ -930,17 +939,19 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         }
         __syncwarp();
       }
-      if (!Q8 && mask != 0xffffu) {
-        // rows of tokens outside the attended set may hold anything (even NaN): zero them,
-        // since the tensor core would turn 0 * NaN into NaN (int8 codes are always finite)
+      if constexpr (!Q8) {
+        if (mask != 0xffffu) {
+          // rows of tokens outside the attended set may hold anything (even NaN): zero them,
+          // since the tensor core would turn 0 * NaN into NaN (int8 codes are always finite)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int t = 2 * i + (lane >> 4);
-          const int c = lane & 15;  // chunk (16 bytes) of the row
-          if (!((mask >> t) & 1u) && c < D / 8)
-            *reinterpret_cast<uint4*>(Wt.v[slot] + chunk_offset<D, SPARSE>(t, c)) = make_uint4(0u, 0u, 0u, 0u);
+          for (int i = 0; i < 8; ++i) {
+            const int t = 2 * i + (lane >> 4);
+            const int c = lane & 15;  // chunk (16 bytes) of the row
+            if (!((mask >> t) & 1u) && c < D / 8)
+              *reinterpret_cast<uint4*>(Wt.v[slot] + chunk_offset<D, SPARSE>(t, c)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
       // -- O^T += V^T P^T -------------------------------------------------------------------
       const uint32_t vbase = smem_u32(Wt.v[slot]);
@@ -1231,18 +1242,20 @@ __global__ void __launch_bounds__(kScoreThreads) decode_score_kernel(const Decod
 
 DecodeKernel decode_kernel(int head_dim, int group, bool sparse, bool scores, bool q8) {
   const DecodeKernel none{nullptr, nullptr, nullptr, head_dim, group, sparse, scores, q8};
-  if (group < 1 || group > kMaxGroup || (sparse && (scores || q8))) return none;
+  if (group < 1 || group > kMaxGroup || (sparse && scores)) return none;
   const void* score = scores ? (const void*)decode_score_kernel : nullptr;
   if (head_dim == 128)
-    return DecodeKernel{q8 ? (scores ? (const void*)decode_split_kernel<128, false, true, true>
-                                     : (const void*)decode_split_kernel<128, false, false, true>)
+    return DecodeKernel{q8 ? (scores   ? (const void*)decode_split_kernel<128, false, true, true>
+                              : sparse ? (const void*)decode_split_kernel<128, true, false, true>
+                                       : (const void*)decode_split_kernel<128, false, false, true>)
                         : sparse ? (const void*)decode_split_kernel<128, true, false, false>
                         : scores ? (const void*)decode_split_kernel<128, false, true, false>
                                  : (const void*)decode_split_kernel<128, false, false, false>,
                         (const void*)decode_merge_kernel<128>, score, 128, group, sparse, scores, q8};
   if (head_dim == 64)
-    return DecodeKernel{q8 ? (scores ? (const void*)decode_split_kernel<64, false, true, true>
-                                     : (const void*)decode_split_kernel<64, false, false, true>)
+    return DecodeKernel{q8 ? (scores   ? (const void*)decode_split_kernel<64, false, true, true>
+                              : sparse ? (const void*)decode_split_kernel<64, true, false, true>
+                                       : (const void*)decode_split_kernel<64, false, false, true>)
                         : sparse ? (const void*)decode_split_kernel<64, true, false, false>
                         : scores ? (const void*)decode_split_kernel<64, false, true, false>
                                  : (const void*)decode_split_kernel<64, false, false, false>,

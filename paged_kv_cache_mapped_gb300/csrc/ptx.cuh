@@ -108,6 +108,19 @@ __device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, in
       : "memory");
 }
 
+// Asynchronous 4-byte copy global -> shared (cp.async); an mbarrier tracks it through
+// cp_async_mbar_arrive.
+__device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
+}
+
+// Makes `bar` track this thread's earlier cp.async copies: its pending arrival count grows by
+// one now and an arrival follows once they have landed, so the current phase cannot complete
+// before them (call it before the phase's last ordinary arrival).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // One plain arrival on an mbarrier (a consumer releasing a ring slot).
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.release.cta.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))

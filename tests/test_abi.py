@@ -21,7 +21,7 @@ def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _lib.header_functions()
-    assert len(declared) == 21
+    assert len(declared) == 22
     nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     for name in declared:
@@ -144,6 +144,14 @@ def test_host_validation_codes(lib):
     assert q8_append_decode(kn=0) == c["PKV_ERR_NULL_POINTER"]
     assert q8_append_decode(kn=0x50008) == c["PKV_ERR_ALIGNMENT"]
     assert q8_append_decode() == c["PKV_ERR_WORKSPACE"]                # 16-byte workspace
+
+    def q8_sparse(vs=0x40000, kept=0x50000, dims=None):
+        return lib.pkv_sparse_decode_attention_q8(
+            P(0x10000), P(0x10000), P(0x10000), P(0x10000), P(0x30000), P(vs), P(0x10000), P(0x10000), P(kept),
+            P(0x60000), 16, ctypes.c_float(0.1), P(0x20000), 16, ctypes.byref(dims or _dims()), None, None)
+    assert q8_sparse(kept=0) == c["PKV_ERR_NULL_POINTER"]
+    assert q8_sparse(vs=0x40008) == c["PKV_ERR_ALIGNMENT"]
+    assert q8_sparse() == c["PKV_ERR_WORKSPACE"]                      # 16-byte workspace
 
     def q8_compact(dks=0x30000, max_kept=8):
         return lib.pkv_kv_compact_q8(P(0x10000), P(0x10000), P(dks), P(0x40000), P(0x50000), 8, 4, P(0x10000),

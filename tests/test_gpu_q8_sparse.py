@@ -412,3 +412,89 @@ def test_rolling_admit_q8_sparse_workload_shape_one_step():
     _admit_both(st, torch.full((B,), L, dtype=torch.int32, device=DEV), rand_bf16((B, hkv, d), g).to(DEV),
                 rand_bf16((B, hkv, d), g).to(DEV), n_sink, n_recent, err)
     assert pkv.read_error(err) == 0
+
+
+def _kept_for(lens, hkv, max_kept, seed, kept_lens=None):
+    rng = np.random.default_rng(seed)
+    B = len(lens)
+    kept = np.full((B, hkv, max_kept), -1, dtype=np.int32)
+    kl = np.array([min(L, max_kept) for L in lens] if kept_lens is None else kept_lens, dtype=np.int32)
+    for b in range(B):
+        for g in range(hkv):
+            kept[b, g, :kl[b]] = np.sort(rng.choice(lens[b], size=kl[b], replace=False)) if kl[b] else []
+    return kept, kl
+
+
+def _sparse_q8_gpu(c, kept, kl, err=None):
+    out = pkv.sparse_decode_attention_q8(c["q"], c["kq"], c["vq"], c["ks"], c["vs"], c["bt"], c["lens"],
+                                         torch.from_numpy(kept).to(DEV), torch.from_numpy(kl).to(DEV), c["scale"],
+                                         error_word=err)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("group", [1, 4, 8])
+def test_sparse_q8_ragged_kept_lists(d, group):
+    hkv = 2
+    lens = [700, 1, 0, 33, 1500, 16, 257]
+    c = _case(lens, hkv * group, hkv, d, seed=100 + d + group, kmul=2.0)
+    kept, kl = _kept_for(lens, hkv, 300, seed=d + group, kept_lens=[300, 1, 0, 17, 300, 16, 129])
+    err = pkv.new_error_word(DEV)
+    out = _sparse_q8_gpu(c, kept, kl, err)
+    assert pkv.read_error(err) == 0
+    ref = oracle.sparse_decode_q8(bits(c["q"]), _n(c["kq"]), _n(c["ks"]), _n(c["vq"]), _n(c["vs"]), _n(c["bt"]),
+                                  _n(c["lens"]), kept, kl, c["scale"])
+    _close(out, ref, f"sparse INT8 d={d} G={group}")
+
+
+def test_sparse_q8_every_token_kept_matches_the_paged_q8_decode():
+    lens = [900, 70, 301]
+    c = _case(lens, 16, 4, 128, seed=110)
+    kept = np.full((3, 4, 900), -1, dtype=np.int32)
+    for b, L in enumerate(lens):
+        kept[b, :, :L] = np.arange(L)
+    out = _sparse_q8_gpu(c, kept, np.array(lens, np.int32))
+    ref = oracle.paged_decode_q8(bits(c["q"]), _n(c["kq"]), _n(c["ks"]), _n(c["vq"]), _n(c["vs"]), _n(c["bt"]),
+                                 _n(c["lens"]), c["scale"])
+    _close(out, ref, "sparse INT8, every token kept")
+    _close(_plain_q8(c), ref, "paged INT8")
+
+
+def test_sparse_q8_bad_kept_index_is_reported():
+    lens = [200, 90]
+    c = _case(lens, 8, 2, 64, seed=111)
+    kept, kl = _kept_for(lens, 2, 64, seed=112)
+    kept[1, 1, 5] = 95                                    # past L_1 = 90
+    err = pkv.new_error_word(DEV)
+    _sparse_q8_gpu(c, kept, kl, err)
+    assert pkv.read_error(err) == pkv.header_constants()["PKV_DEV_BAD_KEPT_INDEX"]
+
+
+def test_sparse_q8_sparse_workload_full_size_sampled_rows():
+    """One layer of the sparse workload over INT8 pools (random codes, Exp row scales): the
+    GPU selection's kept lists (4 + 512 + 1024 of 16384 tokens) attended by gather."""
+    wl = W.WORKLOADS["sparse"]
+    lens = W.context_lengths(wl)
+    B, hq, hkv, d, K = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.keep_max
+    mb = int((lens.max() + 15) // 16)
+    nb = B * mb + 16
+    g = torch.Generator(device=DEV).manual_seed(113)
+    codes = lambda: torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    scales = lambda: torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
+    c = {"q": torch.randn((B, hq, d), generator=g, device=DEV).to(torch.bfloat16), "kq": codes(), "vq": codes(),
+         "ks": scales(), "vs": scales(),
+         "bt": torch.randperm(nb, device=DEV, generator=g)[: B * mb].view(B, mb).to(torch.int32),
+         "lens": lens.to(DEV), "scale": wl.scale}
+    scores = W.make_scores(wl, wl.full_layers, lens, device=DEV, device_rng=True)
+    kept = torch.empty((B, hkv, K), dtype=torch.int32, device=DEV)
+    kl = torch.empty((B,), dtype=torch.int32, device=DEV)
+    pkv.kv_select_topk(scores, c["lens"], wl.n_sink, wl.n_recent, wl.k_top, kept_out=kept, kept_lens_out=kl)
+    err = pkv.new_error_word(DEV)
+    out = _sparse_q8_gpu(c, _n(kept), _n(kl), err)
+    assert pkv.read_error(err) == 0
+    rng = np.random.default_rng(114)
+    rows = sorted({0, B * hq - 1} | set(rng.choice(B * hq, size=40, replace=False).tolist()))
+    ref = oracle.sparse_decode_q8(bits(c["q"]), _n(c["kq"]), _n(c["ks"]), _n(c["vq"]), _n(c["vs"]), _n(c["bt"]),
+                                  _n(c["lens"]), _n(kept), _n(kl), c["scale"], rows=rows)
+    _close(out.view(B * hq, d)[rows], ref, "sparse workload, INT8 gather")

@@ -718,10 +718,18 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
     torch.cuda.empty_cache()
     cmp8 = lambda: pkv.kv_compact_q8(d8["kq"], d8["vq"], d8["ks"], d8["vs"], dbt, s8["kq"], s8["vq"], s8["ks"],
                                      s8["vs"], src["block_tables"], src["context_lens"], kept, kl, stream=cur())
+    gat8 = lambda: pkv.sparse_decode_attention_q8(src["q"], s8["kq"], s8["vq"], s8["ks"], s8["vs"],
+                                                  src["block_tables"], src["context_lens"], kept, kl, wl.scale,
+                                                  out=out, workspace=ws_s, stream=cur())
     with torch.cuda.stream(gstream):
+        ms_gat8 = _graph_time([gat8] * 10, args.warmup, 5, dev, gstream) / 10
         ms_cmp8 = _graph_time([cmp8] * 10, args.warmup, 5, dev, gstream) / 10
         res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, d8, dbt, klens, ws, out, q8=True))
     cmp8_bytes = B * hkv * K * (d + 4) * 2 * 2
+    gat8_bytes = B * hkv * K * (d + 4) * 2 + 2 * B * hq * d * 2
+    res["sparse_layer_gather_decode_int8"] = {"ms": round(ms_gat8, 4), "bytes": gat8_bytes,
+                                              "gbs": round(gat8_bytes / (ms_gat8 * 1e-3) / 1e9, 1),
+                                              "ms_bf16": round(ms_gat, 4)}
     res["sparse_layer_compact_int8"] = {"ms": round(ms_cmp8, 4), "bytes": cmp8_bytes,
                                         "gbs": round(cmp8_bytes / (ms_cmp8 * 1e-3) / 1e9, 1),
                                         "ms_bf16": round(ms_cmp, 4)}

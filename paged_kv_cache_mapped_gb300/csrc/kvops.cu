@@ -234,6 +234,7 @@ constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelSmemKeys = 40960;  // candidates cached in shared memory (160 KiB)
 constexpr int kSelFilt = 4096;       // keys of the first pass's chosen bin kept for the others
+constexpr int kSelTiny = 64;         // keys of the second pass's chosen bin ranked by one warp
 constexpr int kSelBatch = 16;        // score loads in flight per thread
 // dynamic shared memory: the per-warp first-pass histograms, then the cached keys
 constexpr int kSelDynSmem = (kSelWarps * 256 + kSelSmemKeys) * (int)sizeof(uint32_t);
@@ -314,7 +315,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   __shared__ uint32_t s_filt[kSelFilt];        // keys sharing the top byte of the k_top-th best
   __shared__ __align__(16) int hist2[2][256];  // pass p counts into hist2[p & 1]
   __shared__ int warp_sums[2 * (kSelWarps + 1)];
-  __shared__ int s_digit, s_need, s_bin, s_fcount;
+  __shared__ uint32_t s_tiny[kSelTiny];         // keys sharing the top 16 bits of the k_top-th best
+  __shared__ int s_digit, s_need, s_bin, s_fcount, s_tcount;
 
   grid_dependency_wait();
   grid_launch_dependents();
@@ -347,7 +349,10 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   int* my_hist = whist + warp * 256;
 
   for (int i = threadIdx.x; i < kSelWarps * 256; i += blockDim.x) whist[i] = 0;
-  if (threadIdx.x == 0) s_fcount = 0;
+  if (threadIdx.x == 0) {
+    s_fcount = 0;
+    s_tcount = 0;
+  }
   __syncthreads();
   // Scores -> order-preserving keys in shared memory, kSelBatch independent loads in flight
   // per thread, counted by top byte on the way.
@@ -470,6 +475,49 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     }
     __syncthreads();
     pick_digit(shift, hist);
+    if (pass == 1 && filtered && s_bin <= kSelTiny) {
+      // Few keys share the top 16 bits now: gather them (each warp takes its share with one
+      // atomic) and let warp 0 rank them exactly -- the need-th largest x has
+      // count(> x) < need <= count(>= x) -- instead of two more block-wide passes.
+      for (int base = 0; base < m_keys; base += blockDim.x) {
+        const int i = base + (int)threadIdx.x;
+        const uint32_t key = i < m_keys ? s_filt[i] : 0u;
+        const bool hit = i < m_keys && (key >> 16) == (prefix >> 16);
+        const unsigned m = __ballot_sync(kFullMask, hit);
+        int at = 0;
+        if (lane == 0 && m != 0u) at = atomicAdd(&s_tcount, __popc(m));
+        at = __shfl_sync(kFullMask, at, 0);
+        if (hit) s_tiny[at + __popc(m & ((1u << lane) - 1u))] = key;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int mt = s_bin;  // keys in the tiny list
+        const uint32_t k0 = lane < mt ? s_tiny[lane] : 0u, k1 = lane + 32 < mt ? s_tiny[lane + 32] : 0u;
+        int gt0 = 0, ge0 = 0, gt1 = 0, ge1 = 0;
+        for (int j = 0; j < mt; ++j) {
+          const uint32_t x = __shfl_sync(kFullMask, k0, j & 31), y = __shfl_sync(kFullMask, k1, j & 31);
+          const uint32_t kj = j < 32 ? x : y;
+          gt0 += kj > k0;
+          ge0 += kj >= k0;
+          gt1 += kj > k1;
+          ge1 += kj >= k1;
+        }
+        const bool f0 = lane < mt && gt0 < need && need <= ge0;
+        const bool f1 = lane + 32 < mt && gt1 < need && need <= ge1;
+        const unsigned fm = __ballot_sync(kFullMask, f0 || f1);  // lanes holding the key (all equal)
+        const int src = __ffs(fm) - 1;
+        const uint32_t key = __shfl_sync(kFullMask, f0 ? k0 : k1, src);
+        const int rem = __shfl_sync(kFullMask, need - (f0 ? gt0 : gt1), src);
+        if (lane == 0) {
+          s_digit = (int)key;
+          s_need = rem;
+        }
+      }
+      __syncthreads();
+      prefix = (uint32_t)s_digit;
+      need = s_need;
+      break;
+    }
   }
   const uint32_t thr = prefix;  // key of the k_top-th best candidate
 

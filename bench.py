@@ -676,6 +676,32 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
                            "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
                            "launch": "32 decode calls in one CUDA graph (4 full, 28 over compacted pools)",
                            "dense_equivalent_gb": round(wl.layers * full_bytes / 1e9, 2)}}
+    # the same step over INT8 pools (random codes, row scales ~ Exp, the same tables and q)
+    gq8 = torch.Generator(device=dev).manual_seed(47)
+
+    def q8_pools(nblocks):
+        codes = lambda: torch.randint(-127, 128, (nblocks, hkv, 16, d), generator=gq8, device=dev, dtype=torch.int8)
+        rs = lambda: torch.empty((nblocks, hkv, 16), device=dev).exponential_(generator=gq8) * 0.02
+        return codes(), codes(), rs(), rs()
+    full8 = [q8_pools(c["num_blocks"]) for c in full]
+    comp8 = [q8_pools(dnb) for _ in comp]
+
+    def q8_call(c, p, tables, clens, scale):
+        return lambda: pkv.paged_decode_attention_q8(c["q"], p[0], p[1], p[2], p[3], tables, clens, scale, out=out,
+                                                     workspace=ws, stream=torch.cuda.current_stream(dev))
+    calls8 = ([q8_call(c, p, c["block_tables"], c["context_lens"], c["scale"]) for c, p in zip(full, full8)]
+              + [q8_call(c, p, dbt, klens, wl.scale) for c, p in zip(comp, comp8)])
+    with torch.cuda.stream(gstream):
+        ms8 = _graph_time(calls8, args.warmup, max(5, args.steps // 20), dev, gstream)
+    qo = 2 * B * hq * d * 2
+    bytes8 = (wl.full_layers * (int(lens.to(torch.int64).sum()) * hkv * (d + 4) * 2 + qo)
+              + (wl.layers - wl.full_layers) * (B * K * hkv * (d + 4) * 2 + qo))
+    res["sparse_step_int8"] = {"ms": round(ms8, 4), "tokens_per_s": round(B / (ms8 * 1e-3), 1), "bytes": bytes8,
+                               "gbs": round(bytes8 / (ms8 * 1e-3) / 1e9, 1),
+                               "frac": round(bytes8 / (ms8 * 1e-3) / 1e9 / hbm, 4), "ms_bf16": round(ms, 4),
+                               "launch": "32 INT8 decode calls in one CUDA graph (4 full, 28 over compacted pools)"}
+    del full8, comp8, calls8
+    torch.cuda.empty_cache()
     # one sparse layer: select -> compact, and gather decode over the full pool
     src = full[0]
     scores = W.make_scores(wl, wl.full_layers, lens, device=dev, device_rng=True)

@@ -628,11 +628,35 @@ def _qwen_step(pkv, W, dev, stream, args, hbm):
         ms = _graph_time([call(c) for c in layers], args.warmup, max(5, args.steps // 20), dev, gstream)
     nbytes = wl.layers * (decode_bytes(lens, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
                           + 2 * wl.batch * wl.num_kv_heads * wl.head_dim * 2 * 2)
-    del layers
+    # the same step over INT8 pools (random codes, row scales ~ Exp): the fused INT8 append
+    g8 = torch.Generator(device=dev).manual_seed(53)
+    hkv, d = wl.num_kv_heads, wl.head_dim
+    pools8 = []
+    for c in layers:
+        nb = c["num_blocks"]
+        codes = lambda: torch.randint(-127, 128, (nb, hkv, 16, d), generator=g8, device=dev, dtype=torch.int8)
+        rs = lambda: torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g8) * 0.02
+        pools8.append((codes(), codes(), rs(), rs()))
+
+    def call8(c, p):
+        return lambda: pkv.paged_decode_attention_append_q8(
+            c["q"], p[0], p[1], p[2], p[3], c["k_new"], c["v_new"], c["block_tables"], c["context_lens"],
+            c["scale"], out=out, workspace=ws, stream=torch.cuda.current_stream(dev))
+    with torch.cuda.stream(gstream):
+        ms8 = _graph_time([call8(c, p) for c, p in zip(layers, pools8)], args.warmup, max(5, args.steps // 20),
+                          dev, gstream)
+    tokens = int(lens.to(torch.int64).sum())
+    bytes8 = wl.layers * (tokens * hkv * (d + 4) * 2 + 2 * wl.batch * wl.num_q_heads * d * 2
+                          + 2 * wl.batch * hkv * d * 2 + 2 * wl.batch * hkv * (d + 4))
+    del layers, pools8
     return {"ms": round(ms, 4), "tokens_per_s": round(wl.batch / (ms * 1e-3), 1),
             "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
             "layers": wl.layers, "launch": "28 fused append+decode calls in one CUDA graph",
-            "l2": f"{wl.layers} separate pools, {nbytes / 1e9:.2f} GB per step (> L2)"}
+            "l2": f"{wl.layers} separate pools, {nbytes / 1e9:.2f} GB per step (> L2)",
+            "int8": {"ms": round(ms8, 4), "tokens_per_s": round(wl.batch / (ms8 * 1e-3), 1), "bytes": bytes8,
+                     "gbs": round(bytes8 / (ms8 * 1e-3) / 1e9, 1),
+                     "frac": round(bytes8 / (ms8 * 1e-3) / 1e9 / hbm, 4),
+                     "launch": "28 fused INT8 append+decode calls in one CUDA graph"}}
 
 
 def _sparse_step(pkv, W, dev, stream, args, hbm):

@@ -35,6 +35,12 @@
 //    operand by an in-register 8x8 transpose (movmatrix); it is carried as bf16 hi + lo
 //    parts so P keeps ~16 significant bits.  This replaces ~870 CUDA-core instructions per
 //    unit with ~100, leaving the warps waiting on memory rather than on issue slots.
+//  * INT8 pools (one code byte per element plus one fp32 scale per row and kv head): the
+//    codes become fp16 in registers (a byte permute under the exponent of 1024 and one
+//    subtraction per pair), both products take fp16 operands, the K row scales multiply the
+//    logits and the V row scales enter P, relative to a per-segment reference scale, as one
+//    fp16 term.  Sparse rows are (d + 16)-byte pitched copies, their scales 4-byte copies
+//    completing on the same barrier.
 //  * Online softmax ("How KV Sparsity...", section "2. Attention modification", Fig. 7:
 //    running max, running sum, rescale, divide at the end) in base 2 with log2(e) folded
 //    into the scale; the running max only moves when a unit's max exceeds it by 2^8, so the
@@ -902,9 +908,9 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       const float p10 = exp2f(s10 - ref0), p11 = exp2f(s11 - ref1);
       l0 += p00 + p10;
       l1 += p01 + p11;
-      // -- P^T as bf16 hi + lo B fragments (tokens x heads -> heads x tokens) -------------
-      // INT8 pools: fp16 parts of P times each token's V scale over vref (at most 2^8 * slack)
-      // INT8 pools: one fp16 term (11 significant bits, below the bf16 output's rounding);
+      // -- P^T as B fragments (tokens x heads -> heads x tokens) ---------------------------
+      // INT8 pools: P times each token's V scale over vref (at most 2^8 * slack) as one fp16
+      // term (11 significant bits, below the bf16 output's rounding);
       // bf16: a hi + lo pair of bf16 terms (8 bits alone would not be)
       uint32_t hA, hB, lA = 0u, lB = 0u;
       if constexpr (Q8) {

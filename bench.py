@@ -451,6 +451,8 @@ def run_secondary(pkv, W, dev, stream, args):
                               "l2": "2.1 GB of K/V per launch (> L2)"}
     del c, ws, out
     torch.cuda.empty_cache()
+    res["llama8b_kv_append"] = _append_row(pkv, W, dev, stream, args)
+    torch.cuda.empty_cache()
     res["llama8b_decode_with_scores"] = _scores_row(pkv, W, dev, stream, args, hbm)
     torch.cuda.empty_cache()
     res["llama8b_decode_int8"] = _q8_row(pkv, W, dev, stream, args, hbm)
@@ -499,6 +501,52 @@ def _scores_row(pkv, W, dev, stream, args, hbm):
             "gbs": round((kv + extra) / (ms_scored * 1e-3) / 1e9, 1),
             "frac": round((kv + extra) / (ms_scored * 1e-3) / 1e9 / hbm, 4),
             "score_bytes": extra, "l2": "one 0.58 GB pool (> L2)"}
+
+
+def _append_row(pkv, W, dev, stream, args):
+    """The KV append on its own (llama8b layer: one new K and V row per sequence and kv head),
+    bf16 and INT8, and the bf16 append followed by the decode against the fused call."""
+    wl = W.WORKLOADS["llama8b"]
+    c = W.make_layer(wl, device=dev, device_rng=True)
+    nb, hkv, _, d = c["k_cache"].shape
+    g = torch.Generator(device=dev).manual_seed(43)
+    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
+    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
+    ks = torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g) * 0.02
+    vs = torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g) * 0.02
+    ws = torch.zeros(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                c["num_blocks"], c["max_blocks_per_seq"]),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(c["q"])
+
+    def append():
+        pkv.kv_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["slot_mapping"], stream=stream)
+
+    def append_q8():
+        pkv.kv_append_q8(kq, vq, ks, vs, c["k_new"], c["v_new"], c["slot_mapping"], stream=stream)
+
+    def two_calls():
+        append()
+        pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
+                                   c["scale"], out=out, workspace=ws, stream=stream)
+
+    def fused():
+        pkv.paged_decode_attention_append(c["q"], c["k_cache"], c["v_cache"], c["k_new"], c["v_new"],
+                                          c["block_tables"], c["context_lens"], c["scale"], out=out,
+                                          workspace=ws, stream=stream)
+    steps = max(20, args.steps // 2)
+    ms = _time(append, args.warmup, steps, dev, stream)
+    ms_q8 = _time(append_q8, args.warmup, steps, dev, stream)
+    ms_two = _time(two_calls, args.warmup, max(5, args.steps // 4), dev, stream)
+    ms_fused = _time(fused, args.warmup, max(5, args.steps // 4), dev, stream)
+    rows = wl.batch * hkv
+    nbytes = rows * d * 2 * 2 * 2 + wl.batch * 8  # K and V rows read and written, slots
+    nbytes_q8 = rows * d * 2 * 2 + rows * 2 * (d + 4) + wl.batch * 8  # bf16 in, codes + scales out
+    del c, kq, vq, ks, vs, ws, out
+    return {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "ms_int8": round(ms_q8, 4), "bytes_int8": nbytes_q8,
+            "ms_append_then_decode": round(ms_two, 4), "ms_fused_append_decode": round(ms_fused, 4),
+            "what": f"{rows} K and {rows} V rows of {d} bf16 per call, back to back; launch/latency-bound"}
 
 
 def _q8_row(pkv, W, dev, stream, args, hbm):
@@ -947,6 +995,128 @@ def run_reference(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------- small profiling cases
+
+CASES = ("q8", "gather", "prefill", "kvops", "layers", "append")
+
+
+def run_case(name: str, calls: int = 3):
+    """One small, self-contained case for an ncu capture: the named path called `calls` times
+    on one layer of its workload (a few GB on the device at most), then exit.  Nothing is
+    timed here; the profiles name these commands.
+
+      q8       llama8b-shaped layer over INT8 pools: paged_decode_attention_q8
+      gather   one sparse layer: kv_select_topk, then sparse_decode_attention (gather form)
+      prefill  one sparse layer: prefill_window_scores with the lse computed, then given
+      kvops    one sparse layer: kv_select_topk, kv_compact, kv_compact_q8 in turn
+      layers   a qwen1p5b layer (append + decode), a full sparse layer, a compacted sparse layer
+      append   llama8b layer: kv_append, kv_append_q8 in turn
+    """
+    import paged_kv_cache_mapped_gb300 as pkv
+    from paged_kv_cache_mapped_gb300 import inputs as W
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+
+    def q8_pools(nb, hkv, d, seed, scale_fn):
+        g = torch.Generator(device=dev).manual_seed(seed)
+        codes = [torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
+                 for _ in range(2)]
+        return codes + [scale_fn(g, (nb, hkv, 16)) for _ in range(2)]
+    exp_scales = lambda g, shape: torch.empty(shape, device=dev).exponential_(generator=g) * 0.02
+    uni_scales = lambda g, shape: torch.rand(shape, generator=g, device=dev)
+
+    def ws_for(wl, c):
+        return torch.zeros(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                      c["num_blocks"], c["max_blocks_per_seq"]),
+                           dtype=torch.uint8, device=dev)
+
+    if name in ("q8", "append"):
+        wl = W.WORKLOADS["llama8b"]
+        c = W.make_layer(wl, device=dev, device_rng=True)
+        nb, hkv, _, d = c["k_cache"].shape
+        kq, vq, ks, vs = q8_pools(nb, hkv, d, 41, exp_scales)
+        for _ in range(calls):
+            if name == "q8":
+                pkv.paged_decode_attention_q8(c["q"], kq, vq, ks, vs, c["block_tables"], c["context_lens"],
+                                              c["scale"])
+            else:
+                pkv.kv_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["slot_mapping"])
+                pkv.kv_append_q8(kq, vq, ks, vs, c["k_new"], c["v_new"], c["slot_mapping"])
+    elif name in ("gather", "kvops"):
+        wl = W.WORKLOADS["sparse"]
+        lens = W.context_lengths(wl)
+        B, hkv, d, K = wl.batch, wl.num_kv_heads, wl.head_dim, wl.keep_max
+        src = W.make_layer(wl, layer=0, device=dev, device_rng=True)
+        scores = W.make_scores(wl, wl.full_layers, lens, device=dev, device_rng=True)
+        kept = torch.empty((B, hkv, K), dtype=torch.int32, device=dev)
+        kl = torch.empty((B,), dtype=torch.int32, device=dev)
+        if name == "gather":
+            pkv.kv_select_topk(scores, src["context_lens"], wl.n_sink, wl.n_recent, wl.k_top,
+                               kept_out=kept, kept_lens_out=kl)
+            for _ in range(calls):
+                pkv.sparse_decode_attention(src["q"], src["k_cache"], src["v_cache"], src["block_tables"],
+                                            src["context_lens"], kept, kl, wl.scale)
+        else:
+            dbt_cpu, dnb = W.compact_tables(K, B, seed=5)
+            dbt = dbt_cpu.to(dev)
+            dk = torch.empty((dnb, hkv, 16, d), dtype=torch.bfloat16, device=dev)
+            dv = torch.empty_like(dk)
+            sq, svq, ss, svs = q8_pools(src["k_cache"].shape[0], hkv, d, 3, uni_scales)
+            dq, dvq, ds, dvs = q8_pools(dnb, hkv, d, 4, uni_scales)
+            for _ in range(calls):
+                pkv.kv_select_topk(scores, src["context_lens"], wl.n_sink, wl.n_recent, wl.k_top,
+                                   kept_out=kept, kept_lens_out=kl)
+                pkv.kv_compact(dk, dv, dbt, src["k_cache"], src["v_cache"], src["block_tables"],
+                               src["context_lens"], kept, kl)
+                pkv.kv_compact_q8(dq, dvq, ds, dvs, dbt, sq, svq, ss, svs, src["block_tables"],
+                                  src["context_lens"], kept, kl)
+    elif name == "prefill":
+        wl = W.WORKLOADS["sparse"]
+        c = W.make_layer(wl, device=dev, device_rng=True)
+        del c["v_cache"]
+        alpha = 256
+        g = torch.Generator(device=dev).manual_seed(51)
+        q_win = torch.randn((wl.batch, alpha, wl.num_q_heads, wl.head_dim), generator=g,
+                            device=dev).to(torch.bfloat16)
+        acc = torch.zeros((wl.batch, wl.num_kv_heads, c["max_blocks_per_seq"] * 16), dtype=torch.float32,
+                          device=dev)
+        lse = pkv.prefill_window_scores(q_win, c["k_cache"], c["block_tables"], c["context_lens"], wl.scale, acc)
+        pkv.prefill_window_scores(q_win, c["k_cache"], c["block_tables"], c["context_lens"], wl.scale, acc,
+                                  lse=lse, lse_given=True)
+    elif name == "layers":
+        wl = W.WORKLOADS["qwen1p5b"]
+        c = W.make_layer(wl, layer=0, device=dev, device_rng=True)
+        ws = ws_for(wl, c)
+        for _ in range(calls):
+            pkv.paged_decode_attention_append(c["q"], c["k_cache"], c["v_cache"], c["k_new"], c["v_new"],
+                                              c["block_tables"], c["context_lens"], c["scale"], workspace=ws)
+        torch.cuda.synchronize(dev)
+        del c, ws
+        torch.cuda.empty_cache()
+        wl = W.WORKLOADS["sparse"]
+        c = W.make_layer(wl, layer=0, device=dev, device_rng=True)
+        ws = ws_for(wl, c)
+        for _ in range(calls):
+            pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
+                                       c["scale"], workspace=ws)
+        torch.cuda.synchronize(dev)
+        del c
+        torch.cuda.empty_cache()
+        K = wl.keep_max
+        dbt, dnb = W.compact_tables(K, wl.batch, seed=5)
+        g = torch.Generator(device=dev).manual_seed(9)
+        kc = torch.randn((dnb, wl.num_kv_heads, 16, wl.head_dim), generator=g, device=dev).to(torch.bfloat16)
+        vc = torch.randn((dnb, wl.num_kv_heads, 16, wl.head_dim), generator=g, device=dev).to(torch.bfloat16)
+        q = torch.randn((wl.batch, wl.num_q_heads, wl.head_dim), generator=g, device=dev).to(torch.bfloat16)
+        kl = torch.full((wl.batch,), K, dtype=torch.int32, device=dev)
+        for _ in range(calls):
+            pkv.paged_decode_attention(q, kc, vc, dbt.to(dev), kl, wl.scale, workspace=ws)
+    else:
+        raise SystemExit(f"unknown case {name!r}; one of {', '.join(CASES)}")
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"case": name, "calls": calls, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -963,7 +1133,12 @@ def main():
                     help="seconds of untimed identical load before the timed region (clock sampling)")
     ap.add_argument("--rotate", type=int, default=ROTATE,
                     help="independent pool copies the timed steps rotate over")
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="run one small profiling case (no timing, no JSON metric line) and exit")
     args = ap.parse_args()
+    if args.case is not None:
+        run_case(args.case)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -519,14 +519,16 @@ def _append_row(pkv, W, dev, stream, args):
                      dtype=torch.uint8, device=dev)
     out = torch.empty_like(c["q"])
 
-    def append():
-        pkv.kv_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["slot_mapping"], stream=stream)
+    def append(st=None):
+        pkv.kv_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["slot_mapping"],
+                      stream=st or torch.cuda.current_stream(dev))
 
     def append_q8():
-        pkv.kv_append_q8(kq, vq, ks, vs, c["k_new"], c["v_new"], c["slot_mapping"], stream=stream)
+        pkv.kv_append_q8(kq, vq, ks, vs, c["k_new"], c["v_new"], c["slot_mapping"],
+                         stream=torch.cuda.current_stream(dev))
 
     def two_calls():
-        append()
+        append(stream)
         pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
                                    c["scale"], out=out, workspace=ws, stream=stream)
 
@@ -534,9 +536,12 @@ def _append_row(pkv, W, dev, stream, args):
         pkv.paged_decode_attention_append(c["q"], c["k_cache"], c["v_cache"], c["k_new"], c["v_new"],
                                           c["block_tables"], c["context_lens"], c["scale"], out=out,
                                           workspace=ws, stream=stream)
-    steps = max(20, args.steps // 2)
-    ms = _time(append, args.warmup, steps, dev, stream)
-    ms_q8 = _time(append_q8, args.warmup, steps, dev, stream)
+    # the appends as 20 calls in one CUDA graph (host launch cost would otherwise bound them)
+    n = 20
+    gstream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(gstream):
+        ms = _graph_time([append] * n, args.warmup, max(5, args.steps // 20), dev, gstream) / n
+        ms_q8 = _graph_time([append_q8] * n, args.warmup, max(5, args.steps // 20), dev, gstream) / n
     ms_two = _time(two_calls, args.warmup, max(5, args.steps // 4), dev, stream)
     ms_fused = _time(fused, args.warmup, max(5, args.steps // 4), dev, stream)
     rows = wl.batch * hkv
@@ -546,7 +551,7 @@ def _append_row(pkv, W, dev, stream, args):
     return {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
             "ms_int8": round(ms_q8, 4), "bytes_int8": nbytes_q8,
             "ms_append_then_decode": round(ms_two, 4), "ms_fused_append_decode": round(ms_fused, 4),
-            "what": f"{rows} K and {rows} V rows of {d} bf16 per call, back to back; launch/latency-bound"}
+            "what": f"{rows} K and {rows} V rows of {d} bf16 per call, {n} calls in one CUDA graph; latency-bound"}
 
 
 def _q8_row(pkv, W, dev, stream, args, hbm):

@@ -182,11 +182,11 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA
 // more warp per PKV_MERGE_PARTIALS_PER_WARP partials, at most 8, and no more than the GPU holds
 // in one wave of merge CTAs.
 // The estimate mirrors the split kernel's partition with every sequence at its maximum length.
-int merge_warps_log2(const pkv_dims* d, int max_units, long long workers, int min_units, int tail_pct,
-                     int chunk_min, int cpw_cap, long long resident_warps) {
+int merge_warps_log2(const pkv_dims* d, int max_units, long long workers, int min_units, int min_busy_pct,
+                     int tail_pct, int chunk_min, int cpw_cap, long long resident_warps) {
   const long long total = (long long)d->batch * d->num_kv_heads * max_units;
   long long P = (total + workers - 1) / workers;
-  const long long busy = std::max(1ll, workers * PKV_MIN_BUSY_PCT / 100);
+  const long long busy = std::max(1ll, workers * min_busy_pct / 100);
   const long long floor_units = std::min<long long>(min_units, (total + busy - 1) / busy);
   if (P < floor_units) P = floor_units;
   const long long tail = P * tail_pct / 100;
@@ -346,7 +346,11 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.workers = (int)workers;
   const int ring = q8 != nullptr ? (dims->head_dim == 128 ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
                                  : (dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64);
-  a.min_units = std::max(sparse ? PKV_MIN_UNITS_SPARSE : PKV_MIN_UNITS, 1);
+  a.min_units = std::max(sparse ? PKV_MIN_UNITS_SPARSE : q8 != nullptr ? PKV_MIN_UNITS_Q8 : PKV_MIN_UNITS, 1);
+  const int busy_pct = sparse ? PKV_MIN_BUSY_PCT
+                       : q8 != nullptr ? PKV_MIN_BUSY_PCT_Q8
+                       : score_out != nullptr ? PKV_MIN_BUSY_PCT_SCORES : PKV_MIN_BUSY_PCT;
+  a.min_busy_pct = std::min(std::max(busy_pct, 0), 100);
   a.tail_pct = std::min(std::max(sparse ? PKV_TAIL_PCT_SPARSE : PKV_TAIL_PCT, 0), 50);
   a.chunk_min = std::max(PKV_CHUNK_MIN, ring);  // a chunk never ends inside the tile ring
   a.cpw_cap = (int)std::min<long long>(std::min(PKV_MAX_TAIL_CHUNKS, kMaxTailChunksLimit),
@@ -354,7 +358,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.scale_log2 = scale * 1.4426950408889634f;
   a.timeout_ns = kWaitTimeoutNs;
   const int wpr_log2 = merge_warps_log2(
-      dims, max_units, workers, a.min_units, a.tail_pct, a.chunk_min, a.cpw_cap,
+      dims, max_units, workers, a.min_units, a.min_busy_pct, a.tail_pct, a.chunk_min, a.cpw_cap,
       (long long)info->sm_count * info->merge_ctas_per_sm[head_dim_index(dims->head_dim)] * kMergeWarps);
   return cuda_status(launch_decode(k, a, grid, smem, wpr_log2, static_cast<cudaStream_t>(stream)));
 }

@@ -242,9 +242,9 @@ __device__ __forceinline__ SeqUnits seq_units(const DecodeArgs& a, int b) {
 // Partition of `total` units over `nw` worker warps (total < 2^30).
 __device__ void make_partition(int32_t* p, int total, int nw, const DecodeArgs& a) {
   int P = (total + nw - 1) / nw;
-  // a slice of at least min_units, unless that would leave fewer than PKV_MIN_BUSY_PCT % of
-  // the workers with a slice
-  const int busy = max(1, (int)((long long)nw * PKV_MIN_BUSY_PCT / 100));
+  // a slice of at least min_units, unless that would leave fewer than min_busy_pct % of the
+  // workers with a slice
+  const int busy = max(1, (int)((long long)nw * a.min_busy_pct / 100));
   const int floor_units = min(a.min_units, (total + busy - 1) / busy);
   if (P < floor_units) P = floor_units;
   // as many halving chunks as keep the last one, floor(T / (2^cpw - 1)), >= chunk_min

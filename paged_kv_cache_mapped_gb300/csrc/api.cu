@@ -347,10 +347,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   const int ring = q8 != nullptr ? (dims->head_dim == 128 ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
                                  : (dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64);
   a.min_units = std::max(sparse ? PKV_MIN_UNITS_SPARSE : q8 != nullptr ? PKV_MIN_UNITS_Q8 : PKV_MIN_UNITS, 1);
-  const int busy_pct = sparse ? PKV_MIN_BUSY_PCT
-                       : q8 != nullptr ? PKV_MIN_BUSY_PCT_Q8
-                       : score_out != nullptr ? PKV_MIN_BUSY_PCT_SCORES : PKV_MIN_BUSY_PCT;
-  a.min_busy_pct = std::min(std::max(busy_pct, 0), 100);
+  a.min_busy_pct = std::min(std::max(!sparse && q8 != nullptr ? PKV_MIN_BUSY_PCT_Q8 : PKV_MIN_BUSY_PCT, 0), 100);
   a.tail_pct = std::min(std::max(sparse ? PKV_TAIL_PCT_SPARSE : PKV_TAIL_PCT, 0), 50);
   a.chunk_min = std::max(PKV_CHUNK_MIN, ring);  // a chunk never ends inside the tile ring
   a.cpw_cap = (int)std::min<long long>(std::min(PKV_MAX_TAIL_CHUNKS, kMaxTailChunksLimit),

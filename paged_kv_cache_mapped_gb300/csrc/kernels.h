@@ -94,18 +94,16 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #ifndef PKV_MIN_BUSY_PCT
 #define PKV_MIN_BUSY_PCT 70  // the slice floor yields to keep this share of the workers busy (0: never)
 #endif
-// The dense decode over INT8 pools and the score-emitting decode spend more instructions per
-// unit: there every worker takes a slice (measured: the 28-layer qwen step over INT8 pools
-// 0.913 -> 0.835 ms, the rolling sparse layer step 31.7 -> 30.8 us), while the plain bf16
-// decode keeps the floor (all workers busy made the qwen step 0.911 -> 0.973 ms).
+// The dense decode over INT8 pools spends more instructions per unit: there every worker takes
+// a slice (measured: the 28-layer qwen step over INT8 pools 0.913 -> 0.835 ms, the sparse step
+// over INT8 pools 1.098 -> 1.040 ms), while the bf16 decode keeps the floor (all workers busy
+// made the qwen step 0.911 -> 0.973 ms).  The score-emitting decode keeps the plain decode's
+// partition, so its output stays bit-identical to the plain call's.
 #ifndef PKV_MIN_UNITS_Q8
 #define PKV_MIN_UNITS_Q8 16
 #endif
 #ifndef PKV_MIN_BUSY_PCT_Q8
 #define PKV_MIN_BUSY_PCT_Q8 100
-#endif
-#ifndef PKV_MIN_BUSY_PCT_SCORES
-#define PKV_MIN_BUSY_PCT_SCORES 100
 #endif
 #ifndef PKV_MIN_UNITS_SPARSE
 #define PKV_MIN_UNITS_SPARSE 8  // the same for the gather form of the sparse decode (measured)

@@ -346,10 +346,11 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.workers = (int)workers;
   const int ring = q8 != nullptr ? (dims->head_dim == 128 ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
                                  : (dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64);
-  a.min_units = std::max(sparse ? PKV_MIN_UNITS_SPARSE : q8 != nullptr ? PKV_MIN_UNITS_Q8 : PKV_MIN_UNITS, 1);
-  a.min_busy_pct = std::min(std::max(!sparse && q8 != nullptr ? PKV_MIN_BUSY_PCT_Q8 : PKV_MIN_BUSY_PCT, 0), 100);
-  a.tail_pct = std::min(std::max(sparse ? PKV_TAIL_PCT_SPARSE : PKV_TAIL_PCT, 0), 50);
-  a.chunk_min = std::max(PKV_CHUNK_MIN, ring);  // a chunk never ends inside the tile ring
+  const bool dense_q8 = !sparse && q8 != nullptr;
+  a.min_units = std::max(sparse ? PKV_MIN_UNITS_SPARSE : dense_q8 ? PKV_MIN_UNITS_Q8 : PKV_MIN_UNITS, 1);
+  a.min_busy_pct = std::min(std::max(dense_q8 ? PKV_MIN_BUSY_PCT_Q8 : PKV_MIN_BUSY_PCT, 0), 100);
+  a.tail_pct = std::min(std::max(sparse ? PKV_TAIL_PCT_SPARSE : dense_q8 ? PKV_TAIL_PCT_Q8 : PKV_TAIL_PCT, 0), 50);
+  a.chunk_min = std::max(dense_q8 ? PKV_CHUNK_MIN_Q8 : PKV_CHUNK_MIN, ring);  // never ends inside the tile ring
   a.cpw_cap = (int)std::min<long long>(std::min(PKV_MAX_TAIL_CHUNKS, kMaxTailChunksLimit),
                                        plan.ranges / workers - 1);
   a.scale_log2 = scale * 1.4426950408889634f;

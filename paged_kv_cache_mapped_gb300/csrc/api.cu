@@ -183,7 +183,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA
 // in one wave of merge CTAs.
 // The estimate mirrors the split kernel's partition with every sequence at its maximum length.
 int merge_warps_log2(const pkv_dims* d, int max_units, long long workers, int min_units, int min_busy_pct,
-                     int tail_pct, int chunk_min, int cpw_cap, long long resident_warps) {
+                     int tail_pct, int chunk_min, int cpw_cap, long long resident_warps, int partials_per_warp) {
   const long long total = (long long)d->batch * d->num_kv_heads * max_units;
   long long P = (total + workers - 1) / workers;
   const long long busy = std::max(1ll, workers * min_busy_pct / 100);
@@ -194,7 +194,7 @@ int merge_warps_log2(const pkv_dims* d, int max_units, long long workers, int mi
   while (cpw < cpw_cap && tail >= chunk_min * ((2ll << cpw) - 1)) ++cpw;
   const long long np = ((long long)max_units + P - 1) / P * (1 + cpw) + 1;
   int lg = 0;
-  while (lg < 3 && np >= (long long)PKV_MERGE_PARTIALS_PER_WARP << (lg + 1)) ++lg;
+  while (lg < 3 && np >= (long long)partials_per_warp << (lg + 1)) ++lg;
   const long long rows = (long long)d->batch * d->num_q_heads;
   while (lg > 0 && (rows << lg) > resident_warps) --lg;
   return lg;
@@ -357,7 +357,8 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.timeout_ns = kWaitTimeoutNs;
   const int wpr_log2 = merge_warps_log2(
       dims, max_units, workers, a.min_units, a.min_busy_pct, a.tail_pct, a.chunk_min, a.cpw_cap,
-      (long long)info->sm_count * info->merge_ctas_per_sm[head_dim_index(dims->head_dim)] * kMergeWarps);
+      (long long)info->sm_count * info->merge_ctas_per_sm[head_dim_index(dims->head_dim)] * kMergeWarps,
+      dense_q8 ? PKV_MERGE_PARTIALS_PER_WARP_Q8 : PKV_MERGE_PARTIALS_PER_WARP);
   return cuda_status(launch_decode(k, a, grid, smem, wpr_log2, static_cast<cudaStream_t>(stream)));
 }
 

@@ -132,6 +132,12 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #ifndef PKV_MERGE_PARTIALS_PER_WARP
 #define PKV_MERGE_PARTIALS_PER_WARP 16 // merge warps per row grow while a warp would take more
 #endif
+// INT8 decodes, where every worker takes a slice and rows have more partials: more merge warps
+// per row (measured against 16: qwen INT8 step 0.833 -> 0.784 ms, sparse INT8 step 1.035 ->
+// 1.008 ms; for bf16 the qwen step lost 1 % at 4 and 6 % at 8, so it keeps 16).
+#ifndef PKV_MERGE_PARTIALS_PER_WARP_Q8
+#define PKV_MERGE_PARTIALS_PER_WARP_Q8 4
+#endif
 
 constexpr int kDecodeWarps = PKV_DECODE_WARPS;  // worker warps per CTA
 constexpr int kMaxWorkers = 2048;    // worker warps of a decode grid at most (sizes the workspace)

@@ -78,7 +78,7 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #endif
 
 #ifndef PKV_RING_Q8_D128
-#define PKV_RING_Q8_D128 3  // INT8 K/V tile pairs in flight per worker warp at head_dim 128
+#define PKV_RING_Q8_D128 2  // INT8 K/V tile pairs in flight per worker warp at head_dim 128
 #endif
 #ifndef PKV_RING_Q8_D64
 #define PKV_RING_Q8_D64 4

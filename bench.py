@@ -376,17 +376,27 @@ def run_e2e(pkv, copies, host0, dev, stream, ws, args):
     for i in range(args.warmup):
         one(i)
     torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        one(i)
-    e1.record(stream)
+    # the K steps in 5 consecutive blocks, each between two events; the median block is the
+    # figure (one stall of the shared host inside a block moves only that block)
+    nblk = 5 if args.steps >= 10 else 1
+    per = [args.steps // nblk + (1 if b < args.steps % nblk else 0) for b in range(nblk)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nblk + 1)]
+    ev[0].record(stream)
+    i = 0
+    for b in range(nblk):
+        for _ in range(per[b]):
+            one(i)
+            i += 1
+        ev[b + 1].record(stream)
     torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / args.steps
+    blocks = [ev[b].elapsed_time(ev[b + 1]) / per[b] for b in range(nblk)]
+    ms = statistics.median(blocks)
+    mean = ev[0].elapsed_time(ev[nblk]) / args.steps
     B = copies[0]["q"].shape[0]
     return {"value": round(B / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step_mean": round(mean, 5), "blocks_ms": [round(x, 5) for x in blocks],
+            "timing": f"median of {nblk} consecutive blocks of the {args.steps} steps",
             "copies_per_step": "one host-to-device copy of the packed inputs, one device-to-host copy of out"}
 
 

@@ -120,6 +120,9 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #ifndef PKV_TAIL_PCT
 #define PKV_TAIL_PCT 20   // share of a slice handed out dynamically
 #endif
+#ifndef PKV_MIN_BUSY_PCT_SPARSE
+#define PKV_MIN_BUSY_PCT_SPARSE 70  // the busy share of the gather form
+#endif
 #ifndef PKV_TAIL_PCT_SPARSE
 #define PKV_TAIL_PCT_SPARSE 30  // the same for the gather form of the sparse decode (measured)
 #endif

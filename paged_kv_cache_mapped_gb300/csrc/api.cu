@@ -348,7 +348,9 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
                                  : (dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64);
   const bool dense_q8 = !sparse && q8 != nullptr;
   a.min_units = std::max(sparse ? PKV_MIN_UNITS_SPARSE : dense_q8 ? PKV_MIN_UNITS_Q8 : PKV_MIN_UNITS, 1);
-  a.min_busy_pct = std::min(std::max(sparse ? PKV_MIN_BUSY_PCT_SPARSE : dense_q8 ? PKV_MIN_BUSY_PCT_Q8 : PKV_MIN_BUSY_PCT, 0), 100);
+  const int busy_pct = sparse ? (q8 != nullptr ? PKV_MIN_BUSY_PCT_SPARSE_Q8 : PKV_MIN_BUSY_PCT_SPARSE)
+                       : dense_q8 ? PKV_MIN_BUSY_PCT_Q8 : PKV_MIN_BUSY_PCT;
+  a.min_busy_pct = std::min(std::max(busy_pct, 0), 100);
   a.tail_pct = std::min(std::max(sparse ? PKV_TAIL_PCT_SPARSE : dense_q8 ? PKV_TAIL_PCT_Q8 : PKV_TAIL_PCT, 0), 50);
   a.chunk_min = std::max(dense_q8 ? PKV_CHUNK_MIN_Q8 : PKV_CHUNK_MIN, ring);  // never ends inside the tile ring
   a.cpw_cap = (int)std::min<long long>(std::min(PKV_MAX_TAIL_CHUNKS, kMaxTailChunksLimit),

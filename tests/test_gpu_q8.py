@@ -170,6 +170,34 @@ def test_llama8b_full_size_sampled_rows():
     _close(out.view(B * hq, d)[rows], ref, "llama8b INT8 sampled rows")
 
 
+def test_long_contexts_with_tail_chunks_sampled_rows():
+    """Slices long enough for the INT8 partition's tail chunks (about 71 units per worker, so
+    one ticket chunk each): sampled rows against the oracle, every ticket taken (the merge
+    reports a ticket left over), and the same bits on a second call although the tickets may
+    go to other warps."""
+    B, hq, hkv, d = 4, 32, 8, 128
+    lens = torch.tensor([65536, 65536, 60001, 65521], dtype=torch.int32)
+    mb = int((lens.max() + 15) // 16)
+    nb = B * mb + 64
+    g = torch.Generator(device=DEV).manual_seed(33)
+    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    ks = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
+    vs = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
+    bt = torch.randperm(nb, device=DEV, generator=g)[: B * mb].view(B, mb).to(torch.int32)
+    q = torch.randn((B, hq, d), generator=g, device=DEV).to(torch.bfloat16)
+    c = {"q": q, "kq": kq, "ks": ks, "vq": vq, "vs": vs, "bt": bt, "lens": lens.to(DEV), "scale": d ** -0.5}
+    err = pkv.new_error_word(DEV)
+    out = _gpu(c, err=err)
+    assert pkv.read_error(err) == 0
+    assert torch.equal(_gpu(c, err=err), out)
+    assert pkv.read_error(err) == 0
+    rng = np.random.default_rng(34)
+    rows = sorted({0, B * hq - 1} | set(rng.choice(B * hq, size=16, replace=False).tolist()))
+    ref = _ref(c, rows=rows)
+    _close(out.view(B * hq, d)[rows], ref, "long INT8 contexts, sampled rows")
+
+
 def _slots_at_last(bt, lens):
     return np.array([int(bt[b, (L - 1) // 16]) * 16 + (L - 1) % 16 for b, L in enumerate(lens)], dtype=np.int64)
 

@@ -346,6 +346,9 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.workers = (int)workers;
   const int ring = q8 != nullptr ? (dims->head_dim == 128 ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
                                  : (dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64);
+  // Partition settings by form (kernels.h has the measurements): the bf16 decode and its
+  // score-emitting variant share one set, so their outputs agree bit for bit; the dense INT8
+  // decode (issue-bound) and the gather form have their own.
   const bool dense_q8 = !sparse && q8 != nullptr;
   a.min_units = std::max(sparse ? PKV_MIN_UNITS_SPARSE : dense_q8 ? PKV_MIN_UNITS_Q8 : PKV_MIN_UNITS, 1);
   const int busy_pct = sparse ? (q8 != nullptr ? PKV_MIN_BUSY_PCT_SPARSE_Q8 : PKV_MIN_BUSY_PCT_SPARSE)

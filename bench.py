@@ -180,6 +180,8 @@ def arm_config(wl, lens, nb, world):
         "l2": f"inputs larger than L2: {ROTATE} rotating pool copies "
               f"({ROTATE * 2 * nb * wl.num_kv_heads * 16 * wl.head_dim * 2 / 1e9:.2f} GB)",
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "inputs_ready": "the calls declare pools, tables and lengths final before the previous "
+                        "call ends (PKV_DECODE_INPUTS_READY); figures without it are reported beside",
     }
 
 
@@ -211,10 +213,14 @@ def run_ours(args):
     err = pkv.new_error_word(dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(c):
+    # Consecutive steps rotate over independent pools, so a step's pools, tables and lengths are
+    # final before the previous step ends: the calls declare it (inputs_ready), which lets each
+    # call's partition and first tile copies overlap the previous call's last warps -- the case of
+    # consecutive decode layers.  q and the new rows are still read after the previous call ends.
+    def step(c, ready=True):
         pkv.paged_decode_attention_append(c["q"], c["k_cache"], c["v_cache"], c["k_new"], c["v_new"],
                                           c["block_tables"], c["context_lens"], c["scale"], out=out,
-                                          workspace=ws, error_word=err, stream=stream)
+                                          workspace=ws, error_word=err, stream=stream, inputs_ready=ready)
 
     for i in range(args.warmup):
         step(copies[i % ROTATE])
@@ -252,6 +258,18 @@ def run_ours(args):
     dec_ms = ev0.elapsed_time(ev1) / args.steps  # this rank's own average step (one decode call)
     if pkv.read_error(err) != 0:
         raise RuntimeError("device error during the timed region")
+    # the same K steps without the declaration (each call's start-up waits for the previous call)
+    for i in range(args.warmup):
+        step(copies[i % ROTATE], False)
+    torch.cuda.synchronize(dev)
+    ev2 = torch.cuda.Event(enable_timing=True)
+    ev3 = torch.cuda.Event(enable_timing=True)
+    ev2.record(stream)
+    for i in range(args.steps):
+        step(copies[i % ROTATE], False)
+    ev3.record(stream)
+    torch.cuda.synchronize(dev)
+    plain_ms = ev2.elapsed_time(ev3) / args.steps
 
     # the same step timed alone with L2 flushed before each: a buffer of twice the L2 size is
     # written between steps, outside the events; median of 50 single steps (one call each, so
@@ -264,7 +282,7 @@ def run_ours(args):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        step(copies[0])
+        step(copies[0], False)
         e1.record(stream)
         pairs.append((e0, e1))
     torch.cuda.synchronize(dev)
@@ -307,11 +325,18 @@ def run_ours(args):
             "frac": round(achieved / hbm, 4),
             "frac_of_nominal_8000": round(achieved / 8000.0, 4),  # the part's nominal HBM3e figure
             "traffic": profiled_traffic("decode_split_llama8b"),
-            "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the split kernel "
-                            "(profiles/decode_split_llama8b.md); the merge kernel adds the partials",
+            "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of decode_split_kernel"
+                            "<128,false,false,false> per launch on this workload, from the committed "
+                            "counters while the kernel sources are unchanged; the merge kernel adds the "
+                            "partials",
             "algorithmic_bytes_per_launch": bytes_dec,
             "launch_ms": round(dec_ms, 5),
         },
+        "without_inputs_ready": {
+            "ms_per_step": round(plain_ms, 5), "tokens_per_s": round(B / (plain_ms * 1e-3), 1),
+            "frac": round(bytes_dec / (plain_ms * 1e-3) / 1e9 / hbm, 4),
+            "what": "the same K steps, the calls not declaring their inputs final (each call's "
+                    "start-up waits for the previous call to end)"},
         "gpu_launches": 2 * args.steps,
         "host_launch_ms_per_step": round(host_ms, 5),
         "clocks": dict(clk.summary(), window=f"last {args.preload_s} s of identical warm-up load + the timed region"),
@@ -400,6 +425,31 @@ def run_e2e(pkv, copies, host0, dev, stream, ws, args):
             "copies_per_step": "one host-to-device copy of the packed inputs, one device-to-host copy of out"}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), with the machine type."""
+    import platform
+    name = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        fields = dict(line.split(":", 1) for line in out.splitlines() if ":" in line)
+        fields = {k.strip(): v.strip() for k, v in fields.items()}
+        name = fields.get("Model name", "")
+        if fields.get("Vendor ID") and fields["Vendor ID"] not in name:
+            name = f"{fields['Vendor ID']} {name}".strip()
+    except Exception:
+        pass
+    if not name:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu model", "hardware")):
+                        name = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return f"{name or 'unknown'} ({platform.machine()})"
+
+
 def cpu_baseline(host0, wl, lens, budget_s: float = 10.0):
     """The fp64 oracle, as it stands, on the host cores: whole decode steps of the same
     workload (every row of the batch) until ~budget_s of CPU time."""
@@ -432,6 +482,7 @@ def cpu_baseline(host0, wl, lens, budget_s: float = 10.0):
         oracle.set_num_threads(cores)
     dt1 = time.perf_counter() - t1
     return {"value": round(steps * wl.batch / dt, 2), "unit": "tokens/s", "cores": cores,
+            "cpu": cpu_model(), "os_cpu_count": os.cpu_count(),
             "kind": "oracle", "value_1_thread": round(steps1 * wl.batch / dt1, 2),
             "sample": f"{steps} full decode steps of the llama8b workload (all {wl.batch}x{wl.num_q_heads} "
                       f"rows, {int(lens.sum())} context tokens each step; the append's pool copy excluded); "
@@ -683,12 +734,17 @@ def _qwen_step(pkv, W, dev, stream, args, hbm):
     out = torch.empty_like(layers[0]["q"])
     gstream = torch.cuda.Stream(dev)
 
-    def call(c):
+    # each layer has its own pools, so every call declares its inputs final (inputs_ready): a
+    # layer's start-up overlaps the previous layer's last warps
+    def call(c, ready=True):
         return lambda: pkv.paged_decode_attention_append(
             c["q"], c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["block_tables"],
-            c["context_lens"], c["scale"], out=out, workspace=ws, stream=torch.cuda.current_stream(dev))
+            c["context_lens"], c["scale"], out=out, workspace=ws, stream=torch.cuda.current_stream(dev),
+            inputs_ready=ready)
     with torch.cuda.stream(gstream):
         ms = _graph_time([call(c) for c in layers], args.warmup, max(5, args.steps // 20), dev, gstream)
+        ms_plain = _graph_time([call(c, False) for c in layers], args.warmup, max(5, args.steps // 20), dev,
+                               gstream)
     nbytes = wl.layers * (decode_bytes(lens, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
                           + 2 * wl.batch * wl.num_kv_heads * wl.head_dim * 2 * 2)
     # the same step over INT8 pools (random codes, row scales ~ Exp): the fused INT8 append
@@ -704,7 +760,7 @@ def _qwen_step(pkv, W, dev, stream, args, hbm):
     def call8(c, p):
         return lambda: pkv.paged_decode_attention_append_q8(
             c["q"], p[0], p[1], p[2], p[3], c["k_new"], c["v_new"], c["block_tables"], c["context_lens"],
-            c["scale"], out=out, workspace=ws, stream=torch.cuda.current_stream(dev))
+            c["scale"], out=out, workspace=ws, stream=torch.cuda.current_stream(dev), inputs_ready=True)
     with torch.cuda.stream(gstream):
         ms8 = _graph_time([call8(c, p) for c, p in zip(layers, pools8)], args.warmup, max(5, args.steps // 20),
                           dev, gstream)
@@ -714,12 +770,14 @@ def _qwen_step(pkv, W, dev, stream, args, hbm):
     del layers, pools8
     return {"ms": round(ms, 4), "tokens_per_s": round(wl.batch / (ms * 1e-3), 1),
             "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
-            "layers": wl.layers, "launch": "28 fused append+decode calls in one CUDA graph",
+            "layers": wl.layers, "launch": "28 fused append+decode calls in one CUDA graph, inputs_ready",
+            "without_inputs_ready": {"ms": round(ms_plain, 4),
+                                     "frac": round(nbytes / (ms_plain * 1e-3) / 1e9 / hbm, 4)},
             "l2": f"{wl.layers} separate pools, {nbytes / 1e9:.2f} GB per step (> L2)",
             "int8": {"ms": round(ms8, 4), "tokens_per_s": round(wl.batch / (ms8 * 1e-3), 1), "bytes": bytes8,
                      "gbs": round(bytes8 / (ms8 * 1e-3) / 1e9, 1),
                      "frac": round(bytes8 / (ms8 * 1e-3) / 1e9 / hbm, 4),
-                     "launch": "28 fused INT8 append+decode calls in one CUDA graph"}}
+                     "launch": "28 fused INT8 append+decode calls in one CUDA graph, inputs_ready"}}
 
 
 def _sparse_step(pkv, W, dev, stream, args, hbm):
@@ -744,14 +802,16 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
     out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=dev)
     gstream = torch.cuda.Stream(dev)
 
+    # every layer reads its own pools: the calls declare their inputs final (inputs_ready)
     def full_call(c):
         return lambda: pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
                                                   c["context_lens"], c["scale"], out=out, workspace=ws,
-                                                  stream=torch.cuda.current_stream(dev))
+                                                  stream=torch.cuda.current_stream(dev), inputs_ready=True)
 
     def comp_call(c):
         return lambda: pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], dbt, klens, wl.scale,
-                                                  out=out, workspace=ws, stream=torch.cuda.current_stream(dev))
+                                                  out=out, workspace=ws, stream=torch.cuda.current_stream(dev),
+                                                  inputs_ready=True)
     with torch.cuda.stream(gstream):
         ms = _graph_time([full_call(c) for c in full] + [comp_call(c) for c in comp], args.warmup,
                          max(5, args.steps // 20), dev, gstream)
@@ -761,7 +821,8 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
     res = {"sparse_step": {"ms": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
                            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
                            "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
-                           "launch": "32 decode calls in one CUDA graph (4 full, 28 over compacted pools)",
+                           "launch": "32 decode calls in one CUDA graph (4 full, 28 over compacted pools), "
+                                     "inputs_ready",
                            "dense_equivalent_gb": round(wl.layers * full_bytes / 1e9, 2)}}
     # the same step over INT8 pools (random codes, row scales ~ Exp, the same tables and q)
     gq8 = torch.Generator(device=dev).manual_seed(47)
@@ -775,7 +836,8 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
 
     def q8_call(c, p, tables, clens, scale):
         return lambda: pkv.paged_decode_attention_q8(c["q"], p[0], p[1], p[2], p[3], tables, clens, scale, out=out,
-                                                     workspace=ws, stream=torch.cuda.current_stream(dev))
+                                                     workspace=ws, stream=torch.cuda.current_stream(dev),
+                                                     inputs_ready=True)
     calls8 = ([q8_call(c, p, c["block_tables"], c["context_lens"], c["scale"]) for c, p in zip(full, full8)]
               + [q8_call(c, p, dbt, klens, wl.scale) for c, p in zip(comp, comp8)])
     with torch.cuda.stream(gstream):
@@ -786,7 +848,8 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
     res["sparse_step_int8"] = {"ms": round(ms8, 4), "tokens_per_s": round(B / (ms8 * 1e-3), 1), "bytes": bytes8,
                                "gbs": round(bytes8 / (ms8 * 1e-3) / 1e9, 1),
                                "frac": round(bytes8 / (ms8 * 1e-3) / 1e9 / hbm, 4), "ms_bf16": round(ms, 4),
-                               "launch": "32 INT8 decode calls in one CUDA graph (4 full, 28 over compacted pools)"}
+                               "launch": "32 INT8 decode calls in one CUDA graph (4 full, 28 over compacted "
+                                         "pools), inputs_ready"}
     del full8, comp8, calls8
     torch.cuda.empty_cache()
     # one sparse layer: select -> compact, and gather decode over the full pool
@@ -999,7 +1062,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": arm_config(wl, W.context_lengths(wl), host0["num_blocks"], world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
-                         "kind": "oracle",
+                         "cpu": cpu_model(), "os_cpu_count": os.cpu_count(), "kind": "oracle",
                          "sample": f"each step: the oracle's decode of {n_seq} of the {wl.batch} sequences "
                                    f"(all {wl.num_q_heads} heads, their full contexts); tokens/s counts "
                                    f"those {n_seq} sequences"},
@@ -1132,6 +1195,43 @@ def run_case(name: str, calls: int = 3):
     print(json.dumps({"case": name, "calls": calls, "ok": True}))
 
 
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_replicas(n: int) -> int:
+    """`--gpus N` run directly (no WORLD_SIZE in the environment): start N ranks of this script,
+    one per GPU, through torch.distributed.run on 127.0.0.1, and return their exit status.  Each
+    rank runs an independent replica (the path shards by sequence with no exchange); rank 0
+    prints the JSON line."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.abspath(__file__),
+           *sys.argv[1:]]
+    return subprocess.run(cmd).returncode
+
+
+def dist_check():
+    """The multi-rank launch checked without a GPU (PKV_DIST_BACKEND=gloo): every rank joins,
+    the barrier passes, and rank 0 prints the ranks seen and the max over ranks of a value that
+    differs per rank (the reduction the timed region uses)."""
+    dist, rank, world = _dist()
+    dev = torch.device("cpu")
+    _barrier(dist)
+    ranks = [rank]
+    if dist is not None:
+        gathered = [None] * world
+        dist.all_gather_object(gathered, rank)
+        ranks = sorted(gathered)
+    mx = _max_over_ranks(dist, 1.0 + rank, dev)
+    if rank == 0:
+        print(json.dumps({"dist_check": {"world": world, "ranks": ranks, "max_over_ranks": mx}}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1150,9 +1250,21 @@ def main():
                     help="independent pool copies the timed steps rotate over")
     ap.add_argument("--case", choices=CASES, default=None,
                     help="run one small profiling case (no timing, no JSON metric line) and exit")
+    ap.add_argument("--dist-check", action="store_true",
+                    help="check the multi-rank launch (ranks, barrier, max over ranks) and exit")
     args = ap.parse_args()
     if args.case is not None:
         run_case(args.case)
+        return
+    if args.gpus < 1:
+        sys.exit("--gpus must be at least 1")
+    world = os.environ.get("WORLD_SIZE")
+    if world is None and args.gpus > 1:
+        sys.exit(launch_replicas(args.gpus))
+    if world is not None and int(world) != args.gpus:
+        sys.exit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per requested GPU")
+    if args.dist_check:
+        dist_check()
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -71,6 +71,28 @@ extern "C" {
 #define PKV_DEV_DIRTY_WORKSPACE 7   /* decode workspace counters were not zero at the call */
 #define PKV_DEV_BAD_VALUE 8         /* non-finite K/V element given to the INT8 append */
 
+/*
+ * Flags of the decode calls (their `flags` argument; 0 = none).
+ *
+ * PKV_DECODE_INPUTS_READY -- the caller declares that this call's K/V pools (for INT8 pools
+ *   also their scales), block_tables, context_lens and, in the sparse forms,
+ *   kept_index_lists and kept_lens are not written by the work that precedes the call on
+ *   its stream and may still be running when the call's first kernel starts.  With
+ *   programmatic dependent launch that is the kernel enqueued just before the call and
+ *   whatever that kernel lets run alongside it; when it is the previous decode call of
+ *   this library, it is that call's own kernels (so the flag is wrong when that call
+ *   appended into a pool this call reads).  The decode then works out its partition,
+ *   fetches its first block-table entries and starts its first K/V tile copies before
+ *   that work has ended, and waits for it only before it reads q, k_new/v_new, the
+ *   workspace or error_word -- which the preceding kernel may therefore still produce.
+ *   This is the case of a decode step's consecutive layers, each with its own pools
+ *   ("KV Cache primer", cf-1.com/news/5988169, section 2.2: the step appends the new
+ *   token's K/V and reads the whole cache, so every input but the new token's q, k and v
+ *   is ready before the step starts).  Results are identical with and without the flag.
+ * Unknown flag bits are refused with PKV_ERR_ARGUMENT.
+ */
+#define PKV_DECODE_INPUTS_READY 1
+
 /* Shape record shared by the calls. */
 typedef struct pkv_dims {
   int32_t batch;              /* B: sequences in this decode step */
@@ -139,6 +161,7 @@ size_t pkv_decode_workspace_bytes(const pkv_dims* dims);
  *   window         : > 0 attends tokens [max(0, L_b - window), L_b); <= 0 attends all.
  *   workspace      : pkv_decode_workspace_bytes(dims) bytes, 16-byte aligned, its first 8
  *                    bytes zero before the first use (every call leaves them zero).
+ *   flags          : 0 or PKV_DECODE_INPUTS_READY (see there); the same in every decode call.
  *   error_word     : optional; PKV_DEV_BAD_BLOCK_ID / _BAD_CONTEXT_LEN / _WAIT_TIMEOUT /
  *                    _DIRTY_WORKSPACE.
  * Supported: d in {64, 128}; G = Hq / Hkv in 1..8.
@@ -147,7 +170,7 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
                                const void* v_cache, const int32_t* block_tables,
                                const int32_t* context_lens, float scale, int32_t window,
                                void* workspace, size_t workspace_bytes, const pkv_dims* dims,
-                               int32_t* error_word, void* stream);
+                               uint32_t flags, int32_t* error_word, void* stream);
 
 /*
  * pkv_paged_decode_attention_append -- one decode step's KV append and attention in one
@@ -167,7 +190,7 @@ int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, v
                                       const int32_t* block_tables, const int32_t* context_lens,
                                       float scale, int32_t window, void* workspace,
                                       size_t workspace_bytes, const pkv_dims* dims,
-                                      int32_t* error_word, void* stream);
+                                      uint32_t flags, int32_t* error_word, void* stream);
 
 /*
  * INT8 KV cache: K and V stored as 8-bit integers, which halves the cache ("KV Cache
@@ -206,7 +229,8 @@ int pkv_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_sca
 int pkv_paged_decode_attention_q8(void* out, const void* q, const void* k_codes, const void* v_codes,
                                   const float* k_scales, const float* v_scales, const int32_t* block_tables,
                                   const int32_t* context_lens, float scale, int32_t window, void* workspace,
-                                  size_t workspace_bytes, const pkv_dims* dims, int32_t* error_word,
+                                  size_t workspace_bytes, const pkv_dims* dims, uint32_t flags,
+                                  int32_t* error_word,
                                   void* stream);
 
 /*
@@ -229,7 +253,8 @@ int pkv_paged_decode_attention_append_q8(void* out, const void* q, void* k_codes
                                          float* v_scales, const void* k_new, const void* v_new,
                                          const int32_t* block_tables, const int32_t* context_lens, float scale,
                                          int32_t window, void* workspace, size_t workspace_bytes,
-                                         const pkv_dims* dims, int32_t* error_word, void* stream);
+                                         const pkv_dims* dims, uint32_t flags, int32_t* error_word,
+                                         void* stream);
 
 /*
  * pkv_prefill_window_scores -- the prefill-side sparsification score: after a prompt of L_b
@@ -290,7 +315,7 @@ int pkv_paged_decode_attention_scores(void* out, float* lse_out, float* score_ac
                                       const int32_t* block_tables, const int32_t* context_lens,
                                       float scale, int32_t window, void* workspace,
                                       size_t workspace_bytes, const pkv_dims* dims,
-                                      int32_t* error_word, void* stream);
+                                      uint32_t flags, int32_t* error_word, void* stream);
 
 /*
  * pkv_paged_decode_attention_scores_q8 -- pkv_paged_decode_attention_scores over INT8 pools
@@ -307,7 +332,8 @@ int pkv_paged_decode_attention_scores_q8(void* out, float* lse_out, float* score
                                          const void* v_codes, const float* k_scales, const float* v_scales,
                                          const int32_t* block_tables, const int32_t* context_lens, float scale,
                                          int32_t window, void* workspace, size_t workspace_bytes,
-                                         const pkv_dims* dims, int32_t* error_word, void* stream);
+                                         const pkv_dims* dims, uint32_t flags, int32_t* error_word,
+                                         void* stream);
 
 /*
  * pkv_sparse_decode_workspace_bytes -- workspace for pkv_sparse_decode_attention with
@@ -334,7 +360,7 @@ int pkv_sparse_decode_attention(void* out, const void* q, const void* k_cache,
                                 const int32_t* kept_index_lists, const int32_t* kept_lens,
                                 int32_t max_kept, float scale, void* workspace,
                                 size_t workspace_bytes, const pkv_dims* dims,
-                                int32_t* error_word, void* stream);
+                                uint32_t flags, int32_t* error_word, void* stream);
 
 /*
  * pkv_kv_select_topk -- choose the tokens a sparse layer keeps, per (sequence, kv head):
@@ -392,7 +418,8 @@ int pkv_sparse_decode_attention_q8(void* out, const void* q, const void* k_codes
                                    const float* k_scales, const float* v_scales, const int32_t* block_tables,
                                    const int32_t* context_lens, const int32_t* kept_index_lists,
                                    const int32_t* kept_lens, int32_t max_kept, float scale, void* workspace,
-                                   size_t workspace_bytes, const pkv_dims* dims, int32_t* error_word, void* stream);
+                                   size_t workspace_bytes, const pkv_dims* dims, uint32_t flags,
+                                   int32_t* error_word, void* stream);
 
 /*
  * pkv_kv_compact_q8 -- pkv_kv_compact over INT8 pools: each kept row's codes and its fp32 row

@@ -29,6 +29,7 @@ __all__ = [
 ]
 
 BLOCK_SIZE = 16
+_INPUTS_READY = header_constants()["PKV_DECODE_INPUTS_READY"]
 
 
 def _ptr(t):
@@ -149,6 +150,12 @@ def sparse_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, nu
     return int(n)
 
 
+def _flags(inputs_ready: bool) -> int:
+    """The decode calls' flags word: PKV_DECODE_INPUTS_READY when the caller declares the pools,
+    block tables, lengths (and kept lists) final before the preceding work on the stream."""
+    return _INPUTS_READY if inputs_ready else 0
+
+
 def _decode_inputs(q, k_cache, v_cache, block_tables, context_lens):
     nb, hkv, d = _pool_dims(k_cache, v_cache)
     dev = k_cache.device
@@ -178,7 +185,7 @@ def _out_ws(q, out, workspace, nbytes):
 
 
 def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, window=0, *,
-                           out=None, workspace=None, error_word=None, stream=None):
+                           out=None, workspace=None, error_word=None, inputs_ready=False, stream=None):
     """softmax(scale * q K^T) V over the paged cache; returns out [B, Hq, d] bf16."""
     dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
@@ -186,7 +193,7 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     check("pkv_paged_decode_attention", load().pkv_paged_decode_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
-        _ptr(error_word), _stream(stream, dev)))
+        _flags(inputs_ready), _ptr(error_word), _stream(stream, dev)))
     return out
 
 
@@ -205,7 +212,7 @@ def _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, con
 
 
 def paged_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale,
-                              window=0, *, out=None, workspace=None, error_word=None, stream=None):
+                              window=0, *, out=None, workspace=None, error_word=None, inputs_ready=False, stream=None):
     """paged_decode_attention over INT8 pools (each element code * its row's scale)."""
     dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
@@ -213,7 +220,7 @@ def paged_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tab
     check("pkv_paged_decode_attention_q8", load().pkv_paged_decode_attention_q8(
         _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_tables),
         _ptr(context_lens), float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
-        _ptr(error_word), _stream(stream, dev)))
+        _flags(inputs_ready), _ptr(error_word), _stream(stream, dev)))
     return out
 
 
@@ -251,7 +258,7 @@ def prefill_window_scores(q_win, k_cache, block_tables, context_lens, scale, sco
 
 
 def paged_decode_attention_append(q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
-                                  scale, window=0, *, out=None, workspace=None, error_word=None,
+                                  scale, window=0, *, out=None, workspace=None, error_word=None, inputs_ready=False,
                                   stream=None):
     """One decode step: write k_new/v_new [B, Hkv, d] at each sequence's last position
     (context_lens[b] - 1, through the block table) and attend, in one kernel.  Same result as
@@ -266,7 +273,7 @@ def paged_decode_attention_append(q, k_cache, v_cache, k_new, v_new, block_table
     check("pkv_paged_decode_attention_append", load().pkv_paged_decode_attention_append(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
         _ptr(block_tables), _ptr(context_lens), float(scale), int(window), _ptr(workspace),
-        workspace.numel(), ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+        workspace.numel(), ctypes.byref(dims), _flags(inputs_ready), _ptr(error_word), _stream(stream, dev)))
     return out
 
 
@@ -294,7 +301,7 @@ def _score_buffers(dims, dev, score_accum, lse, logits):
 
 def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_lens, scale, score_accum,
                                   window=0, *, k_new=None, v_new=None, out=None, lse=None, logits=None,
-                                  workspace=None, error_word=None, stream=None):
+                                  workspace=None, error_word=None, inputs_ready=False, stream=None):
     """paged_decode_attention (with the step's append when k_new/v_new are given) that also
     adds the step's sparsification score into score_accum [B, Hkv, S] fp32: for every attended
     key t < S of (b, kv head g), the sum over g's query heads of their softmax probability of
@@ -314,13 +321,13 @@ def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_len
     check("pkv_paged_decode_attention_scores", load().pkv_paged_decode_attention_scores(
         _ptr(out), _ptr(lse), _ptr(score_accum), _ptr(logits), int(stride), _ptr(q), _ptr(k_cache),
         _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(context_lens), float(scale),
-        int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims), _ptr(error_word),
+        int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims), _flags(inputs_ready), _ptr(error_word),
         _stream(stream, dev)))
     return out, lse
 
 
 def paged_decode_attention_append_q8(q, k_codes, v_codes, k_scales, v_scales, k_new, v_new, block_tables,
-                                     context_lens, scale, window=0, *, out=None, workspace=None, error_word=None,
+                                     context_lens, scale, window=0, *, out=None, workspace=None, error_word=None, inputs_ready=False,
                                      stream=None):
     """kv_append_q8 of k_new/v_new [B, Hkv, d] (bf16) at each sequence's position L_b - 1, fused
     into paged_decode_attention_q8 over the updated INT8 pools."""
@@ -334,12 +341,12 @@ def paged_decode_attention_append_q8(q, k_codes, v_codes, k_scales, v_scales, k_
     check("pkv_paged_decode_attention_append_q8", load().pkv_paged_decode_attention_append_q8(
         _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(k_new), _ptr(v_new),
         _ptr(block_tables), _ptr(context_lens), float(scale), int(window), _ptr(workspace), workspace.numel(),
-        ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+        ctypes.byref(dims), _flags(inputs_ready), _ptr(error_word), _stream(stream, dev)))
     return out
 
 
 def sparse_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens,
-                               kept_index_lists, kept_lens, scale, *, out=None, workspace=None, error_word=None,
+                               kept_index_lists, kept_lens, scale, *, out=None, workspace=None, error_word=None, inputs_ready=False,
                                stream=None):
     """sparse_decode_attention over INT8 pools (each element code * its row's scale)."""
     dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
@@ -353,13 +360,13 @@ def sparse_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_ta
     check("pkv_sparse_decode_attention_q8", load().pkv_sparse_decode_attention_q8(
         _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_tables),
         _ptr(context_lens), _ptr(kept_index_lists), _ptr(kept_lens), max_kept, float(scale), _ptr(workspace),
-        workspace.numel(), ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+        workspace.numel(), ctypes.byref(dims), _flags(inputs_ready), _ptr(error_word), _stream(stream, dev)))
     return out
 
 
 def paged_decode_attention_scores_q8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale,
                                      score_accum, window=0, *, out=None, lse=None, logits=None, workspace=None,
-                                     error_word=None, stream=None):
+                                     error_word=None, inputs_ready=False, stream=None):
     """paged_decode_attention_scores over INT8 pools (no append: INT8 pools take the step's
     token through kv_append_q8).  Returns (out, lse) as paged_decode_attention_scores."""
     dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
@@ -369,7 +376,7 @@ def paged_decode_attention_scores_q8(q, k_codes, v_codes, k_scales, v_scales, bl
     check("pkv_paged_decode_attention_scores_q8", load().pkv_paged_decode_attention_scores_q8(
         _ptr(out), _ptr(lse), _ptr(score_accum), _ptr(logits), int(stride), _ptr(q), _ptr(k_codes), _ptr(v_codes),
         _ptr(k_scales), _ptr(v_scales), _ptr(block_tables), _ptr(context_lens), float(scale), int(window),
-        _ptr(workspace), workspace.numel(), ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+        _ptr(workspace), workspace.numel(), ctypes.byref(dims), _flags(inputs_ready), _ptr(error_word), _stream(stream, dev)))
     return out, lse
 
 
@@ -442,7 +449,7 @@ def paged_decode_attention_fixed_scratch(q, k_cache, v_cache, block_tables, cont
 
 
 def sparse_decode_attention(q, k_cache, v_cache, block_tables, context_lens, kept_index_lists,
-                            kept_lens, scale, *, out=None, workspace=None, error_word=None,
+                            kept_lens, scale, *, out=None, workspace=None, error_word=None, inputs_ready=False,
                             stream=None):
     """Decode attention over kept_index_lists [B, Hkv, max_kept][:kept_lens[b]]."""
     dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
@@ -456,7 +463,7 @@ def sparse_decode_attention(q, k_cache, v_cache, block_tables, context_lens, kep
     check("pkv_sparse_decode_attention", load().pkv_sparse_decode_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         _ptr(kept_index_lists), _ptr(kept_lens), max_kept, float(scale), _ptr(workspace),
-        workspace.numel(), ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+        workspace.numel(), ctypes.byref(dims), _flags(inputs_ready), _ptr(error_word), _stream(stream, dev)))
     return out
 
 

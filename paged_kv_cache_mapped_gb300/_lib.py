@@ -63,27 +63,28 @@ def load():
                 " (the CUDA library is required; there is no CPU fallback)")
         lib = ctypes.CDLL(LIB_PATH)
         P, I32, I64, SZ, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+        U32 = ctypes.c_uint32
         D = ctypes.POINTER(PkvDims)
         sig = {
             "pkv_kv_append": (I32, [P, P, P, P, P, I64, D, P, P]),
             "pkv_kv_append_q8": (I32, [P, P, P, P, P, P, P, I64, D, P, P]),
             "pkv_prefill_window_scores": (I32, [P, I32, P, I32, P, P, P, P, I32, F32, D, P, P]),
             "pkv_decode_workspace_bytes": (SZ, [D]),
-            "pkv_paged_decode_attention_q8": (I32, [P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, P, P]),
-            "pkv_paged_decode_attention": (I32, [P, P, P, P, P, P, F32, I32, P, SZ, D, P, P]),
-            "pkv_paged_decode_attention_append": (I32, [P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, P, P]),
+            "pkv_paged_decode_attention_q8": (I32, [P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, U32, P, P]),
+            "pkv_paged_decode_attention": (I32, [P, P, P, P, P, P, F32, I32, P, SZ, D, U32, P, P]),
+            "pkv_paged_decode_attention_append": (I32, [P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, U32, P, P]),
             "pkv_paged_decode_attention_scores": (I32, [P, P, P, P, I32, P, P, P, P, P, P, P, F32, I32, P, SZ,
-                                                        D, P, P]),
+                                                        D, U32, P, P]),
             "pkv_kv_rolling_admit": (I32, [P, P, P, P, P, P, P, P, P, I32, I32, I32, D, P, P]),
             "pkv_paged_decode_attention_scores_q8": (I32, [P, P, P, P, I32, P, P, P, P, P, P, P, F32, I32, P,
-                                                           SZ, D, P, P]),
-            "pkv_paged_decode_attention_append_q8": (I32, [P, P, P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, P,
-                                                           P]),
-            "pkv_sparse_decode_attention_q8": (I32, [P, P, P, P, P, P, P, P, P, P, I32, F32, P, SZ, D, P, P]),
+                                                           SZ, D, U32, P, P]),
+            "pkv_paged_decode_attention_append_q8": (I32, [P, P, P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, U32,
+                                                           P, P]),
+            "pkv_sparse_decode_attention_q8": (I32, [P, P, P, P, P, P, P, P, P, P, I32, F32, P, SZ, D, U32, P, P]),
             "pkv_kv_compact_q8": (I32, [P, P, P, P, P, I32, I32, P, P, P, P, P, P, P, P, I32, D, P, P]),
             "pkv_kv_rolling_admit_q8": (I32, [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, D, P, P]),
             "pkv_sparse_decode_workspace_bytes": (SZ, [D, I32]),
-            "pkv_sparse_decode_attention": (I32, [P, P, P, P, P, P, P, P, I32, F32, P, SZ, D, P, P]),
+            "pkv_sparse_decode_attention": (I32, [P, P, P, P, P, P, P, P, I32, F32, P, SZ, D, U32, P, P]),
             "pkv_kv_select_topk": (I32, [P, P, P, I32, P, I32, I32, I32, D, P, P]),
             "pkv_kv_compact": (I32, [P, P, P, I32, I32, P, P, P, P, P, P, I32, D, P, P]),
             "pkv_paged_decode_attention_fixed_scratch": (I32, [P, P, P, P, P, P, F32, I32, D, P, P]),

@@ -312,17 +312,31 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     }
     fence_mbar_init();
   }
-  // Launched with programmatic stream serialisation: wait for the previous kernel on the
-  // stream before reading anything in global memory, then let the merge kernel launch.
-  grid_dependency_wait();
-  grid_launch_dependents();
+  // Launched with programmatic stream serialisation: the previous kernel on the stream may
+  // still run.  Normally the kernel waits for it before reading anything in global memory.
+  // With a.early the caller has declared the pools, block tables, lengths and kept lists final
+  // before that kernel: the partition, the first range's table entries and its first ring of
+  // tile copies go ahead, and the wait comes before the first read of q, the new rows or the
+  // workspace (and before the first error-word write: errors found earlier are held in
+  // `pending_err`).  The merge kernel may launch once this kernel has waited, so at most the
+  // previous call's kernels run alongside an early prologue.
+  bool waited = a.early == 0;
+  int pending_err = 0;
+  if (waited) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
+  auto note_error = [&](int code) {
+    if (waited) record_error(a.err, code);
+    else if (pending_err == 0) pending_err = code;
+  };
 
   // ---- per-sequence unit counts and partition (identical in every CTA) -------------------
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
     const SeqUnits su = seq_units<SPARSE>(a, b);
-    if (su.err != 0 && blockIdx.x == 0) record_error(a.err, su.err);
+    if (su.err != 0 && blockIdx.x == 0) note_error(su.err);
     if constexpr (SCORES) {  // a context longer than the score rows: its keys beyond them get no score
-      if (su.len > a.score_stride && blockIdx.x == 0) record_error(a.err, PKV_DEV_BAD_CONTEXT_LEN);
+      if (su.len > a.score_stride && blockIdx.x == 0) note_error(PKV_DEV_BAD_CONTEXT_LEN);
     }
     s_nb[b] = su.nb;
     s_first[b] = su.first;
@@ -352,11 +366,25 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   __syncthreads();
 
   // Large batches: the merge kernel reads the unit starts from here rather than recomputing
-  // them (smaller ones it derives from the lengths while this kernel still runs).
-  if (blockIdx.x == 0 && a.B > kMergeScanMaxBatch) {
-    for (int i = threadIdx.x; i < a.B; i += blockDim.x) a.layout[i] = s_start[i];
-    for (int i = threadIdx.x; i < a.B; i += blockDim.x) a.layout[a.B + i] = s_nb[i];
-  }
+  // them (smaller ones it derives from the lengths while this kernel still runs).  The record
+  // is in the workspace, so it is written once the previous kernel has ended.
+  auto write_layout = [&]() {
+    if (blockIdx.x == 0 && a.B > kMergeScanMaxBatch) {
+      for (int i = threadIdx.x; i < a.B; i += blockDim.x) a.layout[i] = s_start[i];
+      for (int i = threadIdx.x; i < a.B; i += blockDim.x) a.layout[a.B + i] = s_nb[i];
+    }
+  };
+  // the early prologue's end: wait for the previous kernel, let the merge launch, then the
+  // writes held back
+  auto finish_wait = [&]() {
+    if (waited) return;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    waited = true;
+    if (pending_err != 0) record_error(a.err, pending_err);
+    write_layout();
+  };
+  if (waited) write_layout();
   const int gw = (int)blockIdx.x * kDecodeWarps + warp;
   const int tickets = s_part[kPartTickets];
   uint32_t n_taken = 0;        // tail tickets this warp took
@@ -379,7 +407,11 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     return r;
   };
   // this warp's first range: its slice's static head, or a tail chunk
-  int rid = gw < s_part[kPartWorkers] ? (gw << kRangeShift) : take_ticket();
+  int rid = gw << kRangeShift;
+  if (gw >= s_part[kPartWorkers]) {
+    finish_wait();  // the ticket counter is in the workspace
+    rid = take_ticket();
+  }
   bool aborted = false;
   bool first_range = true;
   while (rid >= 0 && !aborted) {
@@ -434,7 +466,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       for (int i = 0; i < 2 * KS; ++i) qraw[i] = 0u;
     }
   };
-  load_q(cc.b, cc.g);
+  if (waited) load_q(cc.b, cc.g);
 
   // Dense: the block-table entries of this range's units, 32 per coalesced load (lane l
   // holds the entry of unit chunk_base + l), fetched one chunk ahead of use.
@@ -476,7 +508,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     sp_gt = -1;
     if (sp_ok1) {
       if (sp_t < 0 || sp_t >= s_lo[sp_b]) {
-        record_error(a.err, PKV_DEV_BAD_KEPT_INDEX);
+        note_error(PKV_DEV_BAD_KEPT_INDEX);
       } else {
         sp_phys = __ldg(a.block_tables + (size_t)sp_b * a.MB + (sp_t >> 4));
         sp_gt = (sp_g << 4) | (sp_t & 15);
@@ -486,7 +518,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   auto sp_stage3 = [&]() {            // stage 2 -> the pool row
     sp_row = -1;
     if (sp_gt >= 0) {
-      if (sp_phys < 0 || sp_phys >= a.NB) record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
+      if (sp_phys < 0 || sp_phys >= a.NB) note_error(PKV_DEV_BAD_BLOCK_ID);
       else sp_row = (sp_phys * a.Hkv + (sp_gt >> 4)) * 16 + (sp_gt & 15);  // host checks < 2^31
     }
   };
@@ -534,7 +566,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
               tma_load_2d(Wt.v[slot] + bx * 2048, &a.tmap_v, bx * 64, y, &Wb.bar_v[slot], pol);
           }
         } else {
-          record_error(a.err, PKV_DEV_BAD_BLOCK_ID);
+          note_error(PKV_DEV_BAD_BLOCK_ID);
           Wb.meta[slot] = 0u;
           mbar_arrive_expect_tx(&Wb.bar_k[slot], 0);
           mbar_arrive_expect_tx(&Wb.bar_v[slot], 0);
@@ -579,6 +611,10 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
 
   int issued = 0;
   for (; issued < nunits && issued < R; ++issued) issue(issued);
+  if (!waited) {  // early prologue: the first tiles are on their way; q comes after the wait
+    finish_wait();
+    load_q(cc.b, cc.g);
+  }
   // ask for the next range while this one's last units are still in flight
   bool requested = false;
   if (issued == nunits) {
@@ -1012,6 +1048,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     rid = take_ticket();
   }
   }  // ranges
+  finish_wait();  // a warp with no range still ends after the previous kernel
   if (lane == 0 && n_taken != 0u) atomicAdd(a.ctrl + 1, n_taken);
 }
 
@@ -1028,6 +1065,12 @@ decode_merge_kernel(const DecodeArgs a, int group, int wpr_log2) {
   constexpr int W = kMergeWarps;
   __shared__ float s_acc[W][D];
   __shared__ float2 s_ml[W];
+  // With a.merge_trigger_early the next kernel on the stream may launch at once: every kernel
+  // of this library waits for this one (griddepcontrol.wait) before it reads what this one
+  // writes, and an early decode prologue reads only inputs its caller has declared final.  The
+  // next decode's CTAs then take the SM slots the split kernel's last warps free and start
+  // their tile copies there, instead of starting after this kernel's wait.
+  if (a.merge_trigger_early) grid_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int wpr = 1 << wpr_log2;
@@ -1096,7 +1139,7 @@ decode_merge_kernel(const DecodeArgs a, int group, int wpr_log2) {
     }
   }
   grid_dependency_wait();  // the split kernel's partials (and, for large batches, its record)
-  grid_launch_dependents();
+  if (!a.merge_trigger_early) grid_launch_dependents();
   if (a.B > kMergeScanMaxBatch) {
     // the record holds unit starts (already times Hkv) and unit counts per sequence
     const int last = a.B - 1;

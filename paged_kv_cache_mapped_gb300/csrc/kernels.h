@@ -55,6 +55,12 @@ struct DecodeArgs {
   int chunk_min;                 // lower bound of a chunk length (>= the tile ring depth)
   int cpw_cap;                   // upper bound of the chunks per slice (workspace slots)
   int G;                         // query heads per kv head (1..kMaxGroup)
+  int early;                     // 1: the pools, tables, lengths and kept lists are final before the
+                                 //   previous kernel on the stream ends (PKV_DECODE_INPUTS_READY): the
+                                 //   split kernel partitions and starts its first tile copies before
+                                 //   waiting for that kernel; q, new rows and the workspace after it
+  int merge_trigger_early;       // 1: the merge kernel lets the next kernel launch at its start, not
+                                 //   after its wait (set for early bf16 calls, see decode_common)
   float scale_log2;              // scale * log2(e): logits are kept in base-2 units
   unsigned long long timeout_ns; // bound of every mbarrier wait
 };
@@ -293,6 +299,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
                   const int32_t* kept_lens, int32_t max_kept, float scale, int32_t window,
                   void* workspace, size_t workspace_bytes, const struct pkv_dims* dims, int32_t* err,
                   void* stream, bool sparse, const void* k_new = nullptr, const void* v_new = nullptr,
-                  const ScoreOutputs* score_out = nullptr, const Q8Scales* q8 = nullptr);
+                  const ScoreOutputs* score_out = nullptr, const Q8Scales* q8 = nullptr,
+                  uint32_t flags = 0);
 
 }  // namespace pkv

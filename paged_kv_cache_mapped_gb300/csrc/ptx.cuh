@@ -1,6 +1,8 @@
-// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA bulk copies (the
-// non-tensor cp.async.bulk form: whole contiguous tiles, no tensor map), proxy fences,
-// L2 eviction policies, packed fp32x2 arithmetic and bf16 unpacking.
+// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers; TMA copies (contiguous
+// cp.async.bulk, tensor-map cp.async.bulk.tensor tiles, 4-byte cp.async); tcgen05 (tensor
+// memory allocation, UMMA descriptors, MMA issue and commit, tensor-memory loads); warp-level
+// mma.sync, ldmatrix and movmatrix; proxy fences, L2 policies and prefetches; programmatic
+// dependent launch; packed fp16/bf16 conversions.
 #pragma once
 
 #include <cstdint>
@@ -20,13 +22,13 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
-// Makes initialised barriers visible to the async (TMA) proxy.
 // Retire an mbarrier (no thread waiting on it, no copy pending) so that it can be initialised
 // again from phase 0.
 __device__ __forceinline__ void mbar_inval(uint64_t* bar) {
   asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Makes initialised barriers visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -56,18 +56,18 @@ def test_workspace_queries(lib):
     assert lib.pkv_sparse_decode_workspace_bytes(ctypes.byref(d), 0) == 0
 
 
-def _decode(lib, dims, ptr=0x10000, ws_bytes=1 << 30, ws=0x20000):
+def _decode(lib, dims, ptr=0x10000, ws_bytes=1 << 30, ws=0x20000, flags=0):
     P = ctypes.c_void_p
     return lib.pkv_paged_decode_attention(P(ptr), P(ptr), P(ptr), P(ptr), P(ptr), P(ptr),
                                           ctypes.c_float(0.1), 0, P(ws), ws_bytes,
-                                          ctypes.byref(dims), None, None)
+                                          ctypes.byref(dims), flags, None, None)
 
 
 def test_host_validation_codes(lib):
     c = _lib.header_constants()
     P = ctypes.c_void_p
     assert lib.pkv_paged_decode_attention(None, None, None, None, None, None, ctypes.c_float(1.0), 0,
-                                          None, 0, None, None, None) == c["PKV_ERR_NULL_POINTER"]
+                                          None, 0, None, 0, None, None) == c["PKV_ERR_NULL_POINTER"]
     assert _decode(lib, _dims(bs=8)) == c["PKV_ERR_BLOCK_SIZE"]
     assert _decode(lib, _dims(d=80)) == c["PKV_ERR_HEAD_DIM"]
     assert _decode(lib, _dims(hq=12, hkv=8)) == c["PKV_ERR_GQA"]
@@ -77,6 +77,8 @@ def test_host_validation_codes(lib):
     assert _decode(lib, _dims(), ws_bytes=16) == c["PKV_ERR_WORKSPACE"]
     assert _decode(lib, _dims(), ws=0) == c["PKV_ERR_WORKSPACE"]
     assert _decode(lib, _dims(B=0)) == c["PKV_OK"]                    # empty batch: nothing to do
+    assert _decode(lib, _dims(), flags=2) == c["PKV_ERR_ARGUMENT"]     # unknown flag bit
+    assert _decode(lib, _dims(B=0), flags=c["PKV_DECODE_INPUTS_READY"]) == c["PKV_OK"]
     # append
     assert lib.pkv_kv_append(P(0x1000), P(0x1000), P(0x1000), P(0x1000), P(0x1000), -1,
                              ctypes.byref(_dims()), None, None) == c["PKV_ERR_DIMS"]
@@ -92,7 +94,7 @@ def test_host_validation_codes(lib):
         return lib.pkv_paged_decode_attention_scores(
             P(0x10000), P(lse), P(acc), P(logits), stride, P(0x10000), P(0x10000), P(0x10000),
             P(k_new), P(v_new), P(0x10000), P(0x10000), ctypes.c_float(0.1), 0, P(0x20000), 16,
-            ctypes.byref(_dims()), None, None)
+            ctypes.byref(_dims()), 0, None, None)
     assert scores(lse=0) == c["PKV_ERR_NULL_POINTER"]
     assert scores(stride=0) == c["PKV_ERR_DIMS"]
     assert scores(acc=0x40002) == c["PKV_ERR_ALIGNMENT"]
@@ -120,7 +122,8 @@ def test_host_validation_codes(lib):
     def q8_decode(vs=0x40000, ws_bytes=16, dims=None):
         return lib.pkv_paged_decode_attention_q8(P(0x10000), P(0x10000), P(0x10000), P(0x10000), P(0x30000),
                                                  P(vs), P(0x10000), P(0x10000), ctypes.c_float(0.1), 0,
-                                                 P(0x20000), ws_bytes, ctypes.byref(dims or _dims()), None, None)
+                                                 P(0x20000), ws_bytes, ctypes.byref(dims or _dims()), 0, None,
+                                                 None)
     assert q8_decode(vs=0) == c["PKV_ERR_NULL_POINTER"]
     assert q8_decode(vs=0x40008) == c["PKV_ERR_ALIGNMENT"]
     assert q8_decode() == c["PKV_ERR_WORKSPACE"]                      # 16-byte workspace
@@ -130,7 +133,7 @@ def test_host_validation_codes(lib):
         return lib.pkv_paged_decode_attention_scores_q8(
             P(0x10000), P(lse), P(0x60000), P(0x70000), stride, P(0x10000), P(0x10000), P(0x10000), P(0x30000),
             P(vs), P(0x10000), P(0x10000), ctypes.c_float(0.1), 0, P(0x20000), 16, ctypes.byref(dims or _dims()),
-            None, None)
+            0, None, None)
     assert q8_scores(lse=0) == c["PKV_ERR_NULL_POINTER"]
     assert q8_scores(vs=0x40008) == c["PKV_ERR_ALIGNMENT"]
     assert q8_scores(stride=0) == c["PKV_ERR_DIMS"]
@@ -140,7 +143,8 @@ def test_host_validation_codes(lib):
     def q8_append_decode(kn=0x50000, dims=None):
         return lib.pkv_paged_decode_attention_append_q8(
             P(0x10000), P(0x10000), P(0x10000), P(0x10000), P(0x30000), P(0x40000), P(kn), P(0x60000),
-            P(0x10000), P(0x10000), ctypes.c_float(0.1), 0, P(0x20000), 16, ctypes.byref(dims or _dims()), None, None)
+            P(0x10000), P(0x10000), ctypes.c_float(0.1), 0, P(0x20000), 16, ctypes.byref(dims or _dims()), 0, None,
+            None)
     assert q8_append_decode(kn=0) == c["PKV_ERR_NULL_POINTER"]
     assert q8_append_decode(kn=0x50008) == c["PKV_ERR_ALIGNMENT"]
     assert q8_append_decode() == c["PKV_ERR_WORKSPACE"]                # 16-byte workspace
@@ -148,7 +152,7 @@ def test_host_validation_codes(lib):
     def q8_sparse(vs=0x40000, kept=0x50000, dims=None):
         return lib.pkv_sparse_decode_attention_q8(
             P(0x10000), P(0x10000), P(0x10000), P(0x10000), P(0x30000), P(vs), P(0x10000), P(0x10000), P(kept),
-            P(0x60000), 16, ctypes.c_float(0.1), P(0x20000), 16, ctypes.byref(dims or _dims()), None, None)
+            P(0x60000), 16, ctypes.c_float(0.1), P(0x20000), 16, ctypes.byref(dims or _dims()), 0, None, None)
     assert q8_sparse(kept=0) == c["PKV_ERR_NULL_POINTER"]
     assert q8_sparse(vs=0x40008) == c["PKV_ERR_ALIGNMENT"]
     assert q8_sparse() == c["PKV_ERR_WORKSPACE"]                      # 16-byte workspace
@@ -186,7 +190,7 @@ def test_host_validation_codes(lib):
     assert lib.pkv_sparse_decode_attention(P(0x10000), P(0x10000), P(0x10000), P(0x10000),
                                            P(0x10000), P(0x10000), None, None, 16,
                                            ctypes.c_float(0.1), P(0x20000), 1 << 30,
-                                           ctypes.byref(_dims()), None, None) == c["PKV_ERR_NULL_POINTER"]
+                                           ctypes.byref(_dims()), 0, None, None) == c["PKV_ERR_NULL_POINTER"]
 
 
 def test_binding_rejects_cpu_tensors():

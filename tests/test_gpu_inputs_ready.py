@@ -1,0 +1,331 @@
+"""Decode calls with PKV_DECODE_INPUTS_READY (the caller declares the pools, block tables and
+lengths final before the preceding work on the stream, so the split kernel partitions and starts
+its first tile copies before that work ends).
+
+The flag changes when inputs are read, never what is computed: every flagged result is checked
+against the fp64 oracle and, bit for bit, against the same call without the flag.  The calls run
+back to back on one stream with no synchronisation between them -- the case the flag exists for:
+consecutive layers of one decode step, each over its own pools, where a layer's split kernel starts
+while the previous layer's kernels finish -- eagerly and captured in a CUDA graph."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_mapped_gb300 as pkv
+from paged_kv_cache_mapped_gb300 import inputs as W
+from helpers import assert_attn_close, bits, paged_from_contiguous, rand_bf16
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _sample_rows(B, hq, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = {0, B * hq - 1} | {b * hq for b in range(B)}
+    rows |= set(rng.choice(B * hq, size=min(n, B * hq), replace=False).tolist())
+    return sorted(rows)
+
+
+def _oracle(case, rows=None, kc=None, vc=None, window=0):
+    return oracle.paged_decode(bits(case["q"]), bits(case["k_cache"]) if kc is None else kc,
+                               bits(case["v_cache"]) if vc is None else vc, case["block_tables"].cpu().numpy(),
+                               case["context_lens"].cpu().numpy(), case["scale"], window, rows=rows)
+
+
+def _append_call(c, out, ws, ready, err=None, window=0, stream=None):
+    return pkv.paged_decode_attention_append(c["q"], c["k_cache"], c["v_cache"], c["k_new"], c["v_new"],
+                                             c["block_tables"], c["context_lens"], c["scale"], window, out=out,
+                                             workspace=ws, error_word=err, inputs_ready=ready, stream=stream)
+
+
+def _qwen_layers(layers):
+    wl = W.WORKLOADS["qwen1p5b"]
+    cases = [W.make_layer(wl, layer=l, device=DEV) for l in layers]
+    need = max(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                          c["num_blocks"], c["max_blocks_per_seq"]) for c in cases)
+    return wl, cases, torch.zeros(need, dtype=torch.uint8, device=DEV)
+
+
+def test_qwen_layer_chain_full_size_against_oracle():
+    """Four full-size qwen-shaped layers (0, 1, 2 and 27), each appending this step's token into
+    its own pools and attending, issued back to back with the flag: pools bit-exact to the
+    oracle's append, sampled rows of every layer within the gate, and every output bit-identical
+    to the unflagged calls on the same inputs."""
+    wl, cases, ws = _qwen_layers([0, 1, 2, 27])
+    pools0 = [(c["k_cache"].clone(), c["v_cache"].clone()) for c in cases]
+    err = pkv.new_error_word(DEV)
+    outs = [torch.empty_like(c["q"]) for c in cases]
+    for c, o in zip(cases, outs):
+        _append_call(c, o, ws, True, err)
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    for i, (c, o, (k0, v0)) in enumerate(zip(cases, outs, pools0)):
+        okc, ovc = oracle.kv_append(bits(k0), bits(v0), bits(c["k_new"]), bits(c["v_new"]),
+                                    c["slot_mapping"].cpu().numpy())
+        assert np.array_equal(bits(c["k_cache"]), okc) and np.array_equal(bits(c["v_cache"]), ovc)
+        rows = _sample_rows(wl.batch, wl.num_q_heads, 96, 40 + i)
+        got = o.view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)]
+        assert_attn_close(got, _oracle(c, rows, okc, ovc), f"qwen layer {c['layer']} (flagged)")
+    # the same calls without the flag, from the original pools
+    for c, (k0, v0), o in zip(cases, pools0, outs):
+        c["k_cache"].copy_(k0)
+        c["v_cache"].copy_(v0)
+        plain = _append_call(c, torch.empty_like(c["q"]), ws, False)
+        torch.cuda.synchronize()
+        assert torch.equal(plain, o), f"layer {c['layer']}: flagged and plain results differ"
+
+
+def _small(lens, hq, hkv, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    B, lmax = len(lens), max(max(lens), 1)
+    k, v = rand_bf16((B, lmax, hkv, d), g), rand_bf16((B, lmax, hkv, d), g)
+    nb = sum((L + 15) // 16 for L in lens) + 3
+    kc, vc, bt = paged_from_contiguous(k, v, lens, nb, g, fill=float("nan"))
+    case = {"q": rand_bf16((B, hq, d), g).to(DEV), "k_cache": kc.to(DEV), "v_cache": vc.to(DEV),
+            "block_tables": bt.to(DEV), "context_lens": torch.tensor(lens, dtype=torch.int32, device=DEV),
+            "scale": d ** -0.5, "k_new": rand_bf16((B, hkv, d), g).to(DEV),
+            "v_new": rand_bf16((B, hkv, d), g).to(DEV)}
+    bt = case["block_tables"].cpu()
+    case["slot_mapping"] = torch.tensor([int(bt[b, (L - 1) // 16]) * 16 + (L - 1) % 16 if L > 0 else -1
+                                         for b, L in enumerate(lens)], dtype=torch.int64)
+    return case
+
+
+@pytest.mark.parametrize("window", [0, 1, 50])
+def test_ragged_shapes_back_to_back(window):
+    """Ragged batches of several shapes (d 64 and 128, G 1-8, empty and one-token sequences),
+    plain and fused-append calls alternating, all flagged and sharing one workspace, with no
+    synchronisation between them; every element against the oracle and bit-identical to the
+    unflagged calls."""
+    shapes = [([1, 15, 16, 17, 33, 100, 257], 8, 2, 128), ([0, 700, 33], 16, 2, 64),
+              ([4000, 1, 2500, 17], 32, 8, 128), ([90] * 12, 8, 8, 64), ([3, 1500], 48, 6, 128)]
+    cases = [_small(l, hq, hkv, d, 300 + i) for i, (l, hq, hkv, d) in enumerate(shapes)]
+    need = max(pkv.decode_workspace_bytes(c["q"].shape[0], c["q"].shape[1], c["k_cache"].shape[1],
+                                          c["k_cache"].shape[3], c["k_cache"].shape[0], c["block_tables"].shape[1])
+               for c in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    pools0 = [(c["k_cache"].clone(), c["v_cache"].clone()) for c in cases]
+
+    def run(ready):
+        outs = []
+        for i, c in enumerate(cases):
+            o = torch.empty_like(c["q"])
+            if i % 2 == 0 and int(c["context_lens"].min()) > 0:
+                _append_call(c, o, ws, ready, err, window)
+            else:
+                pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                           c["context_lens"], c["scale"], window, out=o, workspace=ws,
+                                           error_word=err, inputs_ready=ready)
+            outs.append(o)
+        return outs
+
+    err = pkv.new_error_word(DEV)
+    flagged = run(True)
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    for i, (c, o, (k0, v0)) in enumerate(zip(cases, flagged, pools0)):
+        appended = i % 2 == 0 and int(c["context_lens"].min()) > 0
+        if appended:
+            okc, ovc = oracle.kv_append(bits(k0), bits(v0), bits(c["k_new"]), bits(c["v_new"]),
+                                        c["slot_mapping"].numpy())
+            assert np.array_equal(bits(c["k_cache"]), okc) and np.array_equal(bits(c["v_cache"]), ovc)
+            ref = _oracle(c, None, okc, ovc, window)
+        else:
+            ref = _oracle(c, None, window=window)
+        assert_attn_close(o, ref, f"shape {i} window {window} (flagged)")
+    for c, (k0, v0) in zip(cases, pools0):
+        c["k_cache"].copy_(k0)
+        c["v_cache"].copy_(v0)
+    plain = run(False)
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(flagged, plain)):
+        assert torch.equal(a, b), f"shape {i}: flagged and plain results differ"
+
+
+def test_next_query_from_previous_output():
+    """The flag lets the split kernel start before the preceding kernel ends, but q is read only
+    after it: a call whose q is the previous flagged call's output (written by that call's merge
+    and split kernels) gives the result of the same call made after a synchronisation."""
+    c1 = _small([2000, 37, 900, 4000], 16, 4, 128, 401)
+    c2 = _small([1200, 3000, 16, 64], 16, 4, 128, 402)
+    ws = torch.zeros(pkv.decode_workspace_bytes(4, 16, 4, 128, max(c1["k_cache"].shape[0], c2["k_cache"].shape[0]),
+                                                max(c1["block_tables"].shape[1], c2["block_tables"].shape[1])),
+                     dtype=torch.uint8, device=DEV)
+    mid = torch.empty_like(c1["q"])
+    out = torch.empty_like(c2["q"])
+    for _ in range(3):
+        mid.fill_(float("nan"))
+        pkv.paged_decode_attention(c1["q"], c1["k_cache"], c1["v_cache"], c1["block_tables"], c1["context_lens"],
+                                   c1["scale"], out=mid, workspace=ws, inputs_ready=True)
+        pkv.paged_decode_attention(mid, c2["k_cache"], c2["v_cache"], c2["block_tables"], c2["context_lens"],
+                                   c2["scale"], out=out, workspace=ws, inputs_ready=True)
+        torch.cuda.synchronize()
+        assert_attn_close(mid, _oracle(c1), "first call")
+        ref = pkv.paged_decode_attention(mid.clone(), c2["k_cache"], c2["v_cache"], c2["block_tables"],
+                                         c2["context_lens"], c2["scale"], workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+
+
+def test_graph_of_flagged_layers_matches_eager_plain():
+    """Four qwen-shaped layers (fused append + decode, the flag set) captured in one CUDA graph and
+    replayed: every layer's output equals the eager unflagged call's bit for bit, and the pools
+    hold the appended rows."""
+    wl, cases, ws = _qwen_layers([3, 4, 5, 6])
+    pools0 = [(c["k_cache"].clone(), c["v_cache"].clone()) for c in cases]
+    eager = [_append_call(c, torch.empty_like(c["q"]), ws, False).clone() for c in cases]
+    torch.cuda.synchronize()
+    appended = [(c["k_cache"].clone(), c["v_cache"].clone()) for c in cases]
+    outs = [torch.empty_like(c["q"]) for c in cases]
+    s = torch.cuda.Stream(DEV)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        for c, o in zip(cases, outs):   # warm-up on the capture stream
+            _append_call(c, o, ws, True)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=s):
+            for c, o in zip(cases, outs):
+                _append_call(c, o, ws, True, stream=s)
+    for _ in range(2):
+        for c, (k0, v0) in zip(cases, pools0):
+            c["k_cache"].copy_(k0)
+            c["v_cache"].copy_(v0)
+        for o in outs:
+            o.fill_(float("nan"))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        for i, (c, o, e, (ka, va)) in enumerate(zip(cases, outs, eager, appended)):
+            assert torch.equal(o, e), f"layer {i}"
+            assert torch.equal(c["k_cache"], ka) and torch.equal(c["v_cache"], va)
+
+
+def test_large_batch_record_written_after_wait():
+    """Batches above 256 sequences hand the merge a record of unit starts in the workspace; with
+    the flag it is written after the preceding kernel ends.  Two different 320-sequence layers
+    back to back share the workspace."""
+    cases = []
+    for layer in range(2):
+        wl = W.Workload("batch320", 91, batch=320, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                        len_uniform=(0, 3000))
+        lens = W.context_lengths(wl)
+        lens[layer::37] = 0
+        cases.append(W.make_layer(wl, layer=layer, device=DEV, lengths=lens, device_rng=True))
+    need = max(pkv.decode_workspace_bytes(320, 8, 2, 128, c["num_blocks"], c["max_blocks_per_seq"]) for c in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    err = pkv.new_error_word(DEV)
+    outs = [pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
+                                       c["scale"], workspace=ws, error_word=err, inputs_ready=True) for c in cases]
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    for i, (c, o) in enumerate(zip(cases, outs)):
+        rows = _sample_rows(320, 8, 120, 60 + i)
+        assert_attn_close(o.view(-1, 128)[torch.tensor(rows, device=DEV)], _oracle(c, rows), f"batch 320 layer {i}")
+        plain = pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                           c["context_lens"], c["scale"], workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(plain, o)
+
+
+def test_errors_found_before_the_wait_are_recorded():
+    """A bad block id met while the first tiles are issued (before the wait) and a bad context
+    length met by the partition are still recorded, once the preceding kernel has ended."""
+    codes = pkv.header_constants()
+    c = _small([100, 40], 8, 2, 128, 501)
+    c["block_tables"][1, 0] = c["k_cache"].shape[0] + 5
+    err = pkv.new_error_word(DEV)
+    pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
+                               c["scale"], error_word=err, inputs_ready=True)
+    assert pkv.read_error(err) == codes["PKV_DEV_BAD_BLOCK_ID"]
+    c2 = _small([100, 40], 8, 2, 128, 502)
+    c2["context_lens"][0] = 16 * c2["block_tables"].shape[1] + 1
+    err2 = pkv.new_error_word(DEV)
+    out = pkv.paged_decode_attention(c2["q"], c2["k_cache"], c2["v_cache"], c2["block_tables"],
+                                     c2["context_lens"], c2["scale"], error_word=err2, inputs_ready=True)
+    assert pkv.read_error(err2) == codes["PKV_DEV_BAD_CONTEXT_LEN"]
+    ref = _oracle({**c2, "q": c2["q"][1:], "block_tables": c2["block_tables"][1:],
+                   "context_lens": c2["context_lens"][1:]})
+    assert_attn_close(out[1:], ref, "valid sequence beside a bad length")
+
+
+def _q8_pools(nb, hkv, d, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    codes = lambda: torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    scales = lambda: torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
+    return codes(), codes(), scales(), scales()
+
+
+def test_int8_scores_and_sparse_forms_flagged_equal_plain():
+    """The INT8 fused append, the score-emitting decode and the gather form of the sparse decode
+    take the flag too: back to back, their results equal the unflagged calls' bit for bit."""
+    wl, cases, ws = _qwen_layers([7, 8])
+    hkv, d = wl.num_kv_heads, wl.head_dim
+    p8 = [_q8_pools(c["num_blocks"], hkv, d, 70 + i) for i, c in enumerate(cases)]
+    p80 = [tuple(t.clone() for t in p) for p in p8]
+
+    def q8(ready):
+        outs = []
+        for c, p in zip(cases, p8):
+            outs.append(pkv.paged_decode_attention_append_q8(
+                c["q"], *p, c["k_new"], c["v_new"], c["block_tables"], c["context_lens"], c["scale"], workspace=ws,
+                inputs_ready=ready))
+        torch.cuda.synchronize()
+        return outs
+    a = q8(True)
+    after = [tuple(t.clone() for t in p) for p in p8]
+    for p, p0 in zip(p8, p80):
+        for t, t0 in zip(p, p0):
+            t.copy_(t0)
+    b = q8(False)
+    for i in range(2):
+        assert torch.equal(a[i], b[i]), f"INT8 layer {i}"
+        assert all(torch.equal(x, y) for x, y in zip(after[i], p8[i]))
+
+    S = cases[0]["block_tables"].shape[1] * 16
+
+    def scores(ready):
+        res = []
+        for c in cases:
+            acc = torch.zeros((wl.batch, hkv, S), dtype=torch.float32, device=DEV)
+            o, lse = pkv.paged_decode_attention_scores(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                                       c["context_lens"], c["scale"], acc, workspace=ws,
+                                                       inputs_ready=ready)
+            res.append((o, lse, acc))
+        torch.cuda.synchronize()
+        return res
+    for (o1, l1, s1), (o2, l2, s2) in zip(scores(True), scores(False)):
+        assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(s1, s2)
+
+    # gather form: kept lists of sinks, a strided middle and the recent window
+    def kept_for(c):
+        lens = c["context_lens"].cpu()
+        mk = 4 + 64 + 256
+        kept = torch.zeros((wl.batch, hkv, mk), dtype=torch.int32)
+        klen = torch.zeros(wl.batch, dtype=torch.int32)
+        for bb in range(wl.batch):
+            L = int(lens[bb])
+            if L <= mk:
+                lst = list(range(L))
+            else:
+                mid = list(range(4, L - 256, max(1, (L - 260) // 64)))[:64]
+                lst = sorted(set(range(4)) | set(mid) | set(range(L - 256, L)))
+            klen[bb] = len(lst)
+            kept[bb, :, :len(lst)] = torch.tensor(lst, dtype=torch.int32)
+        return kept.to(DEV), klen.to(DEV)
+    kls = [kept_for(c) for c in cases]
+
+    def sparse(ready):
+        outs = [pkv.sparse_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
+                                            kl[0], kl[1], c["scale"], workspace=ws, inputs_ready=ready)
+                for c, kl in zip(cases, kls)]
+        torch.cuda.synchronize()
+        return outs
+    for i, (x, y) in enumerate(zip(sparse(True), sparse(False))):
+        assert torch.equal(x, y), f"sparse layer {i}"
+        c, (kept, klen) = cases[i], kls[i]
+        rows = _sample_rows(wl.batch, wl.num_q_heads, 48, 80 + i)
+        ref = oracle.sparse_decode(bits(c["q"]), bits(c["k_cache"]), bits(c["v_cache"]),
+                                   c["block_tables"].cpu().numpy(), c["context_lens"].cpu().numpy(),
+                                   kept.cpu().numpy(), klen.cpu().numpy(), c["scale"], rows=rows)
+        assert_attn_close(x.view(-1, d)[torch.tensor(rows, device=DEV)], ref, f"sparse layer {i} (flagged)")

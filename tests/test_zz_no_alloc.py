@@ -4,20 +4,25 @@ It serves callers that cannot allocate device memory -- a plain C program or plu
 device allocator of its own, or a host runtime that owns the device heap and forbids
 cudaMalloc -- by keeping its split-K scratch in a fixed static device array inside the
 library.  These tests call it through the C ABI (ctypes on libpkv.so, no Python helper in
-between) twice in a row and compare both results with the workspace-taking entry point,
-within the same tolerance the other attention tests use.  They also check that a shape whose
-partial results do not fit the fixed scratch (G = 8 at head_dim 128) is refused.  This file is collected last, and each test builds
-its own inputs, so it passes alone in a fresh process as well as after the other tests.
+between) twice in a row and compare both results with the fp64 oracle and with the
+workspace-taking entry point, within the same tolerance the other attention tests use (the
+llama8b-sized case on a sample of rows the oracle computes one by one).  They also check that
+a shape whose partial results do not fit the fixed scratch (G = 8 at head_dim 128) is refused
+without touching the device, and that the next call still works.  This file is collected last,
+and each test builds its own inputs, so it passes alone in a fresh process as well as after the
+other tests.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_mapped_gb300 as pkv
 from paged_kv_cache_mapped_gb300 import _lib
 from paged_kv_cache_mapped_gb300 import inputs as W
-from helpers import MAX_ABS, REL_L2, attn_errors
+from helpers import MAX_ABS, REL_L2, attn_errors, bits
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -50,7 +55,7 @@ def _with_workspace(case, window=0):
     st = lib.pkv_paged_decode_attention(
         _p(out), _p(case["q"]), _p(case["k_cache"]), _p(case["v_cache"]), _p(case["block_tables"]),
         _p(case["context_lens"]), ctypes.c_float(case["scale"]), window, _p(ws), ws.numel(),
-        ctypes.byref(dims), None, stream)
+        ctypes.byref(dims), 0, None, stream)
     assert st == C["PKV_OK"]
     return out
 
@@ -61,16 +66,40 @@ def _compare(got, ref, what):
     assert mx <= MAX_ABS and rel <= REL_L2, f"{what}: max-abs {mx:.3e} rel-L2 {rel:.3e}"
 
 
+def _oracle_rows(case, rows, window):
+    return oracle.paged_decode(bits(case["q"]), bits(case["k_cache"]), bits(case["v_cache"]),
+                               case["block_tables"].cpu().numpy(), case["context_lens"].cpu().numpy(),
+                               case["scale"], window, rows=rows)
+
+
+def _rows(name, case):
+    """Every row of the tiny case; for llama8b a fixed sample (each sequence's first and last
+    query head plus 48 random rows)."""
+    B, hq = case["q"].shape[:2]
+    if name == "tiny":
+        return list(range(B * hq))
+    rng = np.random.default_rng(77)
+    rows = {b * hq for b in range(B)} | {b * hq + hq - 1 for b in range(B)}
+    rows |= set(rng.choice(B * hq, size=48, replace=False).tolist())
+    return sorted(rows)
+
+
 @pytest.mark.parametrize("name,window", [("tiny", 0), ("tiny", 50), ("llama8b", 0)])
-def test_fixed_scratch_matches_workspace_entry_point_twice(name, window):
+def test_fixed_scratch_matches_oracle_and_workspace_entry_point_twice(name, window):
     case = W.make_layer(W.WORKLOADS[name], device=DEV, device_rng=(name != "tiny"))
-    ref = _with_workspace(case, window).float()
+    rows = _rows(name, case)
+    idx = torch.tensor(rows, device=DEV)
+    d = case["q"].shape[2]
+    ref_oracle = torch.from_numpy(_oracle_rows(case, rows, window))
+    ref_ws = _with_workspace(case, window).float().view(-1, d)[idx]
     err = pkv.new_error_word(DEV)
     for call in range(2):
         out = torch.full_like(case["q"], float("nan"))
         assert _fixed(case, out, window, err) == C["PKV_OK"]
         torch.cuda.synchronize()
-        _compare(out, ref, f"{name} window={window} call {call}")
+        got = out.view(-1, d)[idx]
+        _compare(got, ref_oracle, f"{name} window={window} call {call} against the oracle")
+        _compare(got, ref_ws, f"{name} window={window} call {call} against the workspace entry point")
     assert pkv.read_error(err) == 0
 
 
@@ -84,6 +113,15 @@ def test_fixed_scratch_refuses_oversized_shapes():
     need = _lib.load().pkv_decode_workspace_bytes(ctypes.byref(_dims(case)))
     assert need > C["PKV_FIXED_SCRATCH_BYTES"]
     out = torch.zeros_like(case["q"])
-    assert _fixed(case, out) == C["PKV_ERR_WORKSPACE"]
+    err = pkv.new_error_word(DEV)
+    assert _fixed(case, out, err=err) == C["PKV_ERR_WORKSPACE"]
     torch.cuda.synchronize()
     assert torch.count_nonzero(out) == 0
+    assert pkv.read_error(err) == 0
+    # the refusal left the scratch usable: a normal call right after it is exact and clean
+    tiny = W.make_layer(W.WORKLOADS["tiny"], device=DEV)
+    out = torch.full_like(tiny["q"], float("nan"))
+    assert _fixed(tiny, out, err=err) == C["PKV_OK"]
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    _compare(out, torch.from_numpy(_oracle_rows(tiny, None, 0)), "tiny call after a refused one")

@@ -64,7 +64,7 @@ extern "C" {
 #define PKV_DEV_OK 0
 #define PKV_DEV_BAD_BLOCK_ID 1      /* block table entry outside [0, num_blocks) */
 #define PKV_DEV_BAD_SLOT 2          /* slot >= num_blocks*16 */
-#define PKV_DEV_BAD_KEPT_INDEX 3    /* kept index outside [0, context_len) */
+#define PKV_DEV_BAD_KEPT_INDEX 3    /* kept index outside [0, context_len), or not above the one before */
 #define PKV_DEV_BAD_CONTEXT_LEN 4   /* context_len < 0 or > max_blocks_per_seq*16 */
 #define PKV_DEV_WAIT_TIMEOUT 5      /* an mbarrier wait exceeded its bound (kernel gave up) */
 #define PKV_DEV_BAD_SCORE 6         /* NaN score given to top-k selection */
@@ -350,7 +350,10 @@ size_t pkv_sparse_decode_workspace_bytes(const pkv_dims* dims, int32_t max_kept)
  * attended set of (b, kv head g) = kept_index_lists[b][g][0 : kept_lens[b]], gathered row
  * by row from the full paged pool through block_tables.
  *   kept_index_lists : [B, Hkv, max_kept] int32 logical token positions, strictly
- *                      ascending, each in [0, context_lens[b]).
+ *                      ascending, each in [0, context_lens[b]).  An entry outside that range
+ *                      or not above the entry before it (a duplicate or a descent) is reported
+ *                      as PKV_DEV_BAD_KEPT_INDEX and not attended; that (b, kv head)'s rows are
+ *                      then unspecified, every other row is unaffected.
  *   kept_lens        : [B] int32 in [0, max_kept]; every kv head of b keeps that many.
  *   other arguments  : as pkv_paged_decode_attention (no window).
  */
@@ -395,7 +398,9 @@ int pkv_kv_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* s
  *   dst_block_tables         : [B, dst_max_blocks_per_seq] int32.
  *   src_*                    : the full pool and its block table, shapes per src_dims.
  *   context_lens             : [B] int32 source context lengths (for index validation).
- *   kept_index_lists, kept_lens, max_kept : as pkv_sparse_decode_attention.
+ *   kept_index_lists, kept_lens, max_kept : as pkv_sparse_decode_attention; an entry outside
+ *                              [0, L_b) or not above the one before it is reported
+ *                              (PKV_DEV_BAD_KEPT_INDEX) and its compact slot left untouched.
  * Bit-exact.
  */
 int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_block_tables,

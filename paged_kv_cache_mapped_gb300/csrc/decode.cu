@@ -483,49 +483,63 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     bt_cur = load_chunk(0);
     if (nunits > 32) bt_next = load_chunk(32);
   }
-  // Sparse: the rows of this range's units are resolved in pairs of units (lane l: row l & 15
-  // of unit 2c + l / 16) through a pipeline -- the kept index two pairs ahead of issue, the
-  // block id one pair ahead -- so an issue waits on neither dependent load.
-  int sp_t = 0, sp_b = 0, sp_g = 0;   // stage 1: kept index of pair c + 2 (valid: sp_ok1)
-  int sp_phys = 0, sp_gt = -1;        // stage 2: block id of pair c + 1; g << 4 | offset, -1 none
-  int sp_row = -1;                    // pair c: this lane's pool row, -1 when not copied
-  bool sp_ok1 = false;
-  auto sp_stage1 = [&](int pair) {    // load the kept index of `pair`
-    sp_ok1 = false;
-    const int k = 2 * pair + (lane >> 4);
+  // Sparse: the rows of this range's units are resolved in pairs of units (lane l: slot l & 15
+  // of unit 2c + l / 16) through a pipeline -- the kept entry two pairs ahead of issue, its block
+  // id one pair ahead, the pool row at issue -- so an issue waits on neither dependent load.  An
+  // entry outside [0, L) or not above the entry before it (a duplicate or a descent: each kept
+  // token is attended once) is reported and not copied.
+  Cursor sc = ic;                          // stage 1: the unit (of lanes 0-15) of the next pair
+  int sp_pair = 0;                         // stage 1: the next pair
+  int sp_t1 = -1, sp_b1 = 0, sp_g1 = 0;    // stage 1: checked position (-1: none)
+  int sp_t2 = -1, sp_g2 = 0, sp_phys2 = 0; // stage 2: position and its block id
+  int sp_row = -1;                         // pair c: this lane's pool row (-1: not copied)
+  auto sp_stage1 = [&]() {                 // load and check the kept entries of pair sp_pair
+    const int k = 2 * sp_pair + (lane >> 4);
+    Cursor c = sc;
+    if (lane >= 16 && k < nunits) advance(c, s_nb, a.B, a.Hkv);
+    int t = -1, tp = -1;
+    bool has = false, need_prev = false;
     if (k < nunits) {
-      const Cursor c = locate(u0 + k, s_start, s_nb, a.B);
-      const int pos = c.j * 16 + (lane & 15);
-      if (pos < s_len[c.b]) {
-        sp_t = __ldg(a.kept + ((size_t)c.b * a.Hkv + c.g) * a.max_kept + pos);
-        sp_b = c.b;
-        sp_g = c.g;
-        sp_ok1 = true;
+      const int e = c.j * 16 + (lane & 15);
+      if (e < s_len[c.b]) {
+        const int32_t* list = a.kept + ((size_t)c.b * a.Hkv + c.g) * a.max_kept;
+        t = __ldg(list + e);
+        has = true;
+        need_prev = e > 0;
+        if (lane == 0 && need_prev) tp = __ldg(list + e - 1);
       }
     }
-  };
-  auto sp_stage2 = [&]() {            // stage 1 -> stage 2: check the index, load its block id
-    sp_gt = -1;
-    if (sp_ok1) {
-      if (sp_t < 0 || sp_t >= s_lo[sp_b]) {
-        note_error(PKV_DEV_BAD_KEPT_INDEX);
-      } else {
-        sp_phys = __ldg(a.block_tables + (size_t)sp_b * a.MB + (sp_t >> 4));
-        sp_gt = (sp_g << 4) | (sp_t & 15);
-      }
+    // entry e - 1 of an entry e > 0 sits in the lane before (units of a segment are
+    // consecutive and full but for the last), except for lane 0
+    const int up = __shfl_up_sync(kFullMask, t, 1);
+    if (lane != 0) tp = up;
+    sp_t1 = -1;
+    if (has) {
+      if (t < 0 || t >= s_lo[c.b] || (need_prev && t <= tp)) note_error(PKV_DEV_BAD_KEPT_INDEX);
+      else sp_t1 = t;
     }
+    sp_b1 = c.b;
+    sp_g1 = c.g;
+    if (2 * sp_pair + 1 < nunits) advance(sc, s_nb, a.B, a.Hkv);
+    if (2 * sp_pair + 2 < nunits) advance(sc, s_nb, a.B, a.Hkv);
+    ++sp_pair;
   };
-  auto sp_stage3 = [&]() {            // stage 2 -> the pool row
+  auto sp_stage2 = [&]() {                 // stage 1 -> stage 2: the entry's block id
+    sp_t2 = sp_t1;
+    sp_g2 = sp_g1;
+    if (sp_t1 >= 0) sp_phys2 = __ldg(a.block_tables + (size_t)sp_b1 * a.MB + (sp_t1 >> 4));
+  };
+  auto sp_stage3 = [&]() {                 // stage 2 -> the pool row
     sp_row = -1;
-    if (sp_gt >= 0) {
-      if (sp_phys < 0 || sp_phys >= a.NB) note_error(PKV_DEV_BAD_BLOCK_ID);
-      else sp_row = (sp_phys * a.Hkv + (sp_gt >> 4)) * 16 + (sp_gt & 15);  // host checks < 2^31
+    if (sp_t2 >= 0) {
+      if (sp_phys2 < 0 || sp_phys2 >= a.NB) note_error(PKV_DEV_BAD_BLOCK_ID);
+      else sp_row = (sp_phys2 * a.Hkv + sp_g2) * 16 + (sp_t2 & 15);  // host checks < 2^31
     }
   };
   if constexpr (SPARSE) {
-    sp_stage1(0);
+    sp_stage1();
     sp_stage2();
-    sp_stage1(1);
+    sp_stage1();
   }
 
   // Issue unit k (the one `ic` names) into slot k % R.  Dense: lane 0 copies the K and V
@@ -579,7 +593,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       if ((k & 1) == 0) {  // a new pair: advance the row pipeline
         sp_stage3();
         sp_stage2();
-        sp_stage1((k >> 1) + 2);
+        sp_stage1();
       }
       const int row = __shfl_sync(kFullMask, sp_row, ((k & 1) << 4) | r);
       const bool ok = row >= 0;

@@ -181,10 +181,16 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
   const int dst_blk = __ldg(dbt + (size_t)b * dMB + (j0 >> 4));
   const int r = lane % NR;  // this lane's row of the group (lanes r, r + NR, ... share it)
   long long src_row = -1;
-  if (j0 + r < n) {
-    const int t = __ldg(kept + bg * max_kept + j0 + r);
+  // the kept entry and the one before it: a list must rise strictly (each kept token has one
+  // compact slot), so an entry not above its predecessor is reported and not copied
+  const bool has = j0 + r < n;
+  int t = -1;
+  if (has) t = __ldg(kept + bg * max_kept + j0 + r);
+  int tp = __shfl_up_sync(kFullMask, t, 1);  // entry j0 + r - 1 for r > 0
+  if (r == 0 && has && j0 > 0) tp = __ldg(kept + bg * max_kept + j0 - 1);
+  if (has) {
     const int L = __ldg(lens + b);
-    if (t < 0 || t >= L || (t >> 4) >= sMB) {
+    if (t < 0 || t >= L || (t >> 4) >= sMB || (j0 + r > 0 && t <= tp)) {
       if (lane < NR) record_error(err, PKV_DEV_BAD_KEPT_INDEX);
     } else {
       const int sb = __ldg(sbt + (size_t)b * sMB + (t >> 4));

@@ -866,21 +866,27 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
     ws_s = torch.zeros(pkv.sparse_decode_workspace_bytes(B, hq, hkv, d, src["num_blocks"],
                                                          src["max_blocks_per_seq"], K),
                        dtype=torch.uint8, device=dev)
-    gat = lambda: pkv.sparse_decode_attention(src["q"], src["k_cache"], src["v_cache"], src["block_tables"],
-                                              src["context_lens"], kept, kl, wl.scale, out=out,
-                                              workspace=ws_s, stream=cur())
+    # consecutive gather calls over unchanged pools and lists: the calls declare their inputs final
+    gat = lambda ready=True: pkv.sparse_decode_attention(src["q"], src["k_cache"], src["v_cache"],
+                                                         src["block_tables"], src["context_lens"], kept, kl,
+                                                         wl.scale, out=out, workspace=ws_s, stream=cur(),
+                                                         inputs_ready=ready)
     # each per-layer call is microseconds of device work: time it as 10 calls in one CUDA graph
     # (as a decode step runs), not as Python launches that the host would bound
     with torch.cuda.stream(gstream):
         ms_sel = _graph_time([sel] * 10, args.warmup, 5, dev, gstream) / 10
         ms_cmp = _graph_time([cmp] * 10, args.warmup, 5, dev, gstream) / 10
         ms_gat = _graph_time([gat] * 10, args.warmup, 5, dev, gstream) / 10
+        ms_gat_plain = _graph_time([lambda: gat(False)] * 10, args.warmup, 5, dev, gstream) / 10
     sel_bytes = int(scores.numel()) * 4 + B * hkv * K * 4
     cmp_bytes = B * hkv * K * d * 2 * 2 * 2
     res["sparse_layer_select_topk"] = {"ms": round(ms_sel, 4), "gbs": round(sel_bytes / (ms_sel * 1e-3) / 1e9, 1)}
     res["sparse_layer_compact"] = {"ms": round(ms_cmp, 4), "gbs": round(cmp_bytes / (ms_cmp * 1e-3) / 1e9, 1)}
     res["sparse_layer_gather_decode"] = {"ms": round(ms_gat, 4),
-                                         "gbs": round(sparse_bytes / (ms_gat * 1e-3) / 1e9, 1)}
+                                         "gbs": round(sparse_bytes / (ms_gat * 1e-3) / 1e9, 1),
+                                         "frac": round(sparse_bytes / (ms_gat * 1e-3) / 1e9 / hbm, 4),
+                                         "ms_without_inputs_ready": round(ms_gat_plain, 4),
+                                         "launch": "10 calls in one CUDA graph, inputs_ready"}
     with torch.cuda.stream(gstream):
         res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, comp[0], dbt, klens, ws, out))
     # the same layer over INT8 pools (random codes, row scales ~ Exp): compaction and rolling
@@ -896,7 +902,7 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
                                      s8["vs"], src["block_tables"], src["context_lens"], kept, kl, stream=cur())
     gat8 = lambda: pkv.sparse_decode_attention_q8(src["q"], s8["kq"], s8["vq"], s8["ks"], s8["vs"],
                                                   src["block_tables"], src["context_lens"], kept, kl, wl.scale,
-                                                  out=out, workspace=ws_s, stream=cur())
+                                                  out=out, workspace=ws_s, stream=cur(), inputs_ready=True)
     with torch.cuda.stream(gstream):
         ms_gat8 = _graph_time([gat8] * 10, args.warmup, 5, dev, gstream) / 10
         ms_cmp8 = _graph_time([cmp8] * 10, args.warmup, 5, dev, gstream) / 10
@@ -1075,7 +1081,7 @@ def run_reference(args):
 
 # ------------------------------------------------------------------- small profiling cases
 
-CASES = ("q8", "gather", "prefill", "kvops", "layers", "append")
+CASES = ("q8", "gather", "prefill", "kvops", "layers", "append", "qwen8", "qwen8_plain")
 
 
 def run_case(name: str, calls: int = 3):
@@ -1089,6 +1095,9 @@ def run_case(name: str, calls: int = 3):
       kvops    one sparse layer: kv_select_topk, kv_compact, kv_compact_q8 in turn
       layers   a qwen1p5b layer (append + decode), a full sparse layer, a compacted sparse layer
       append   llama8b layer: kv_append, kv_append_q8 in turn
+      qwen8    eight qwen1p5b layers (each with its own pools: append + decode, the calls declaring
+               their inputs ready) captured in one CUDA graph and replayed `calls` times
+      qwen8_plain  the same graph with calls that do not declare their inputs ready
     """
     import paged_kv_cache_mapped_gb300 as pkv
     from paged_kv_cache_mapped_gb300 import inputs as W
@@ -1189,6 +1198,36 @@ def run_case(name: str, calls: int = 3):
         kl = torch.full((wl.batch,), K, dtype=torch.int32, device=dev)
         for _ in range(calls):
             pkv.paged_decode_attention(q, kc, vc, dbt.to(dev), kl, wl.scale, workspace=ws)
+    elif name in ("qwen8", "qwen8_plain"):
+        wl = W.WORKLOADS["qwen1p5b"]
+        layers = [W.make_layer(wl, layer=l, device=dev, device_rng=True) for l in range(8)]
+        ws = torch.zeros(max(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                        c["num_blocks"], c["max_blocks_per_seq"]) for c in layers),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(layers[0]["q"])
+        ready = name == "qwen8"
+        s = torch.cuda.Stream(dev)
+
+        def step():
+            for c in layers:
+                pkv.paged_decode_attention_append(c["q"], c["k_cache"], c["v_cache"], c["k_new"], c["v_new"],
+                                                  c["block_tables"], c["context_lens"], c["scale"], out=out,
+                                                  workspace=ws, stream=torch.cuda.current_stream(dev),
+                                                  inputs_ready=ready)
+        with torch.cuda.stream(s):
+            step()
+            torch.cuda.synchronize(dev)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                step()
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            # the replays alone are in the profiler's range (ncu --profile-from-start off)
+            torch.cuda.cudart().cudaProfilerStart()
+            for _ in range(calls):
+                graph.replay()
+            torch.cuda.synchronize(dev)
+            torch.cuda.cudart().cudaProfilerStop()
     else:
         raise SystemExit(f"unknown case {name!r}; one of {', '.join(CASES)}")
     torch.cuda.synchronize(dev)

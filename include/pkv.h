@@ -505,11 +505,16 @@ int pkv_kv_rolling_admit_q8(void* k_codes, void* v_codes, float* k_scales, float
  *     do not fit -- G * d above 512, that is G = 8 at d = 128 -- return PKV_ERR_WORKSPACE
  *     and enqueue nothing.
  *   - The first call on a device looks up the array's device address on that device (with
- *     it current); make that first call before any stream capture.
+ *     it current); make that first call before any stream capture.  The address is kept for
+ *     the life of the process: a cudaDeviceReset after the first call (which reloads the
+ *     library's device code) is not supported by this entry point.
  *   - Every call on a device shares the one array.  Its two control words start at zero
- *     (static storage) and every call leaves them zero.  Calls whose kernels overlap on
- *     the GPU -- different streams without ordering, or several host threads -- race on
- *     it and give wrong results: serialise them.
+ *     (static storage) and every completed call leaves them zero.  If a call returns a
+ *     launch error (>= PKV_ERR_CUDA_BASE) after its first kernel was enqueued, the words may
+ *     be left non-zero: the next call then reports PKV_DEV_DIRTY_WORKSPACE, its result is
+ *     not to be used, and it clears them, so the call after it is correct again.  Calls
+ *     whose kernels overlap on the GPU -- different streams without ordering, or several
+ *     host threads -- race on it and give wrong results: serialise them.
  *   - Results equal those of pkv_paged_decode_attention up to fp32 summation order (with
  *     fewer load-balancing chunks the split-K partition may differ).
  */

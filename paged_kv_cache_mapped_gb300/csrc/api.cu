@@ -345,8 +345,9 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   const int grid = std::min(info->sm_count * per_sm, kMaxWorkers / kDecodeWarps);
   const long long workers = (long long)grid * kDecodeWarps;
   a.workers = (int)workers;
-  const int ring = q8 != nullptr ? (dims->head_dim == 128 ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
-                                 : (dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64);
+  const int ring = (sparse && dims->head_dim == 128) ? PKV_RING_SPARSE_D128
+                   : q8 != nullptr ? (dims->head_dim == 128 ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
+                                   : (dims->head_dim == 128 ? PKV_RING_D128 : PKV_RING_D64);
   // Partition settings by form (kernels.h has the measurements): the bf16 decode and its
   // score-emitting variant share one set, so their outputs agree bit for bit; the dense INT8
   // decode (issue-bound) and the gather form have their own.

@@ -65,8 +65,9 @@ struct Geo {
   static constexpr int kPitch = kRow + 16;                 // sparse: padded row pitch in smem
   static constexpr int kTile = SPARSE ? 16 * kPitch : 16 * kRow;  // bytes per tile
   static constexpr int kKSteps = D / 16;                   // k-steps of q.K, m-tiles of P.V
-  static constexpr int kRing = Q8 ? ((D == 128) ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
-                                  : ((D == 128) ? PKV_RING_D128 : PKV_RING_D64);
+  static constexpr int kRing = (SPARSE && D == 128) ? PKV_RING_SPARSE_D128
+                               : Q8 ? ((D == 128) ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
+                                    : ((D == 128) ? PKV_RING_D128 : PKV_RING_D64);
   static_assert((Q8 || kBoxes * 128 == kRow) && kRing >= 2, "head_dim must be a multiple of 64");
 };
 

@@ -90,6 +90,10 @@ constexpr int kPartFields = kPartOff + kMaxTailChunksLimit + 1;
 #define PKV_RING_Q8_D64 4
 #endif
 
+#ifndef PKV_RING_SPARSE_D128
+#define PKV_RING_SPARSE_D128 2  // gather form of the sparse decode (bf16 and INT8) at head_dim 128
+#endif
+
 #ifndef PKV_Q8_MIN_CTAS
 #define PKV_Q8_MIN_CTAS 12  // INT8 decode: resident CTAs per SM the register budget must allow (0: no bound)
 #endif

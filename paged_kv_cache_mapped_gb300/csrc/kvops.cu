@@ -239,11 +239,12 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelSmemKeys = 40960;  // candidates cached in shared memory (160 KiB)
-constexpr int kSelFilt = 4096;       // keys of the first pass's chosen bin kept for the others
-constexpr int kSelTiny = 64;         // keys of the second pass's chosen bin ranked by one warp
+constexpr int kSelBins = 4096;       // 12-bit digits (the last digit has 8 bits)
+constexpr int kSelFilt = 4096;       // keys sharing the first digit kept in a short list
+constexpr int kSelRank = kSelThreads;  // keys sharing a prefix ranked exactly, one per thread
 constexpr int kSelBatch = 16;        // score loads in flight per thread
-// dynamic shared memory: the per-warp first-pass histograms, then the cached keys
-constexpr int kSelDynSmem = (kSelWarps * 256 + kSelSmemKeys) * (int)sizeof(uint32_t);
+// dynamic shared memory: the cached keys
+constexpr int kSelDynSmem = kSelSmemKeys * (int)sizeof(uint32_t);
 
 // Order-preserving map of an fp32 score to uint32: a larger key is a larger score.  -0.0
 // is folded onto +0.0 first so the two compare equal, as the selection rule requires; NaN
@@ -303,26 +304,29 @@ __device__ __forceinline__ void block_exclusive_scan2(int a, int b, int* sums, i
 // Kept-token selection for one (sequence, kv head) per CTA ("How KV Sparsity...": sections
 // "System model" -- drop low-score KV, retain high-score and recent KV -- and "2. Attention
 // modification" -- per layer and head, the top-k tokens by accumulated score; sink tokens
-// from its introduction).  The k_top-th largest key among the candidates is found by an
-// MSD radix select over 8-bit digits: the first pass counts every candidate (one shared
-// atomic per key into its warp's histogram, while the scores load); the candidates sharing
-// the chosen top byte go to a short list when it fits, and the three other passes count over
-// that list.  Candidates above the k_top-th key are kept, and of those equal to it the lowest
-// positions fill the remainder: each thread owns a run of consecutive candidates, marks its
-// kept ones in 64-bit masks, and two block scans place them, so the kept list is written in
-// ascending position and the result is exact and unique.
+// from its introduction).  The k_top-th largest key among the candidates is found by an MSD
+// radix select over digits of 12, 12 and 8 bits: the first pass counts every candidate into a
+// 4096-bin histogram while the scores load (scores of one layer share few exponents, so bins
+// of 12 bits spread the shared-memory atomics that 8-bit bins would pile onto a few addresses).
+// Once at most kSelRank candidates share the digits chosen so far, they are gathered and every
+// thread ranks one of them against all the others (the k_top-th key x has count(> x) < need <=
+// count(>= x)), which replaces the remaining passes; a larger group goes through the next digit
+// (over a short list of the first digit's keys when it fits).  Candidates above the k_top-th
+// key are kept, and of those equal to it the lowest positions fill the remainder: each thread
+// owns a run of consecutive candidates, marks its kept ones in 64-bit masks, and one block scan
+// places them, so the kept list is written in ascending position and the result is exact and
+// unique.
 __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     int32_t* __restrict__ kept_out, int32_t* __restrict__ kept_lens_out,
     const float* __restrict__ scores, int stride, const int32_t* __restrict__ lens, int Hkv,
     int n_sink, int n_recent, int k_top, int32_t* err) {
-  extern __shared__ uint32_t s_dyn[];
-  int* whist = reinterpret_cast<int*>(s_dyn);  // [kSelWarps][256] per-warp first-pass counts
-  uint32_t* s_keys = s_dyn + kSelWarps * 256;  // kSelSmemKeys keys when the candidates fit
-  __shared__ uint32_t s_filt[kSelFilt];        // keys sharing the top byte of the k_top-th best
-  __shared__ __align__(16) int hist2[2][256];  // pass p counts into hist2[p & 1]
+  extern __shared__ __align__(16) uint32_t s_keys[];  // kSelSmemKeys keys when the candidates fit
+  __shared__ __align__(16) int hist[kSelBins];
+  __shared__ uint32_t s_filt[kSelFilt];        // keys sharing the first digit (when they fit)
+  __shared__ uint32_t s_rank[kSelRank];        // keys sharing the prefix, ranked exactly
   __shared__ int warp_sums[2 * (kSelWarps + 1)];
-  __shared__ uint32_t s_tiny[kSelTiny];         // keys sharing the top 16 bits of the k_top-th best
-  __shared__ int s_digit, s_need, s_bin, s_fcount, s_tcount;
+  __shared__ int s_digit, s_need, s_bin, s_fcount, s_rcount;
+  __shared__ uint32_t s_thr;
 
   grid_dependency_wait();
   grid_launch_dependents();
@@ -344,186 +348,206 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   const float* row = scores + (size_t)pair * stride;
   const int first = n_sink;
   const int n = L - n_recent - n_sink;  // candidates: positions first .. first + n - 1
-  if (k_top == 0) {  // no candidate is kept: sinks and the recent window only
-    for (int t = threadIdx.x; t < n_sink; t += blockDim.x) out[t] = t;
-    for (int t = threadIdx.x; t < n_recent; t += blockDim.x) out[n_sink + t] = first + n + t;
-    return;
-  }
+  // the sinks and the recent window first: their stores drain while the selection runs
+  for (int t = threadIdx.x; t < n_sink; t += blockDim.x) out[t] = t;
+  for (int t = threadIdx.x; t < n_recent; t += blockDim.x) out[n_sink + k_top + t] = first + n + t;
+  if (k_top == 0) return;  // no candidate is kept
   const bool cached = n <= kSelSmemKeys;
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  int* my_hist = whist + warp * 256;
 
-  for (int i = threadIdx.x; i < kSelWarps * 256; i += blockDim.x) whist[i] = 0;
+  for (int i = threadIdx.x; i < kSelBins; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x == 0) {
     s_fcount = 0;
-    s_tcount = 0;
+    s_rcount = 0;
   }
   __syncthreads();
-  // Scores -> order-preserving keys in shared memory, kSelBatch independent loads in flight
-  // per thread, counted by top byte on the way.
-  bool nan_seen = false;
-  for (int base = 0; base < n; base += kSelThreads * kSelBatch) {
-    float v[kSelBatch];
-#pragma unroll
-    for (int u = 0; u < kSelBatch; ++u) {
-      const int i = base + u * kSelThreads + (int)threadIdx.x;
-      v[u] = i < n ? __ldg(row + first + i) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kSelBatch; ++u) {
-      const int i = base + u * kSelThreads + (int)threadIdx.x;
-      if (i < n) {
-        const uint32_t key = score_key(v[u]);
-        nan_seen |= v[u] != v[u];
-        if (cached) s_keys[i] = key;
-        atomicAdd(&my_hist[key >> 24], 1);
-      }
-    }
-  }
-  if (nan_seen) record_error(err, PKV_DEV_BAD_SCORE);
-  __syncthreads();
-  if (threadIdx.x < 256) {
-    int c = 0;
-#pragma unroll 8
-    for (int w = 0; w < kSelWarps; ++w) c += whist[w * 256 + threadIdx.x];
-    hist2[0][threadIdx.x] = c;
-    hist2[1][threadIdx.x] = 0;
-  }
-  __syncthreads();
-  auto key_at = [&](int i) -> uint32_t { return cached ? s_keys[i] : score_key(__ldg(row + first + i)); };
-
   // The digit holding the need-th largest key among those matching the prefix so far:
-  // count(> d) < need <= count(>= d).  Lane l of warp 0 owns bins [8l, 8l + 8); suffix sums
-  // over lanes from the top.
+  // count(> d) < need <= count(>= d).  Thread t owns the 4 bins [4r, 4r + 4), r = 1023 - t, so
+  // an exclusive scan over the threads counts the keys in higher bins.
   uint32_t prefix = 0u;
   int need = k_top;
-  auto pick_digit = [&](int shift, const int* hist) {
-    if (threadIdx.x < 32) {
-      const int4 h0 = reinterpret_cast<const int4*>(hist)[2 * lane];
-      const int4 h1 = reinterpret_cast<const int4*>(hist)[2 * lane + 1];
-      const int c[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-      int own = 0;
+  auto pick_digit = [&](int shift, int bins) {
+    const int r = kSelThreads - 1 - (int)threadIdx.x;
+    int c[4] = {0, 0, 0, 0};
+    if (4 * r < bins) {
+      const int4 h = reinterpret_cast<const int4*>(hist)[r];
+      c[0] = h.x; c[1] = h.y; c[2] = h.z; c[3] = h.w;
+    }
+    const int own = c[0] + c[1] + c[2] + c[3];
+    int above, unused;
+    block_exclusive_scan2(own, 0, warp_sums, &above, &unused);
+    if (own > 0 && above < need && need <= above + own) {
+      int cum = above;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) own += c[j];
-      int suffix = own;  // sum over lanes >= lane
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_down_sync(kFullMask, suffix, o);
-        if (lane + o < 32) suffix += t;
-      }
-      const int above = suffix - own;  // keys in bins owned by higher lanes
-      if (above < need && need <= suffix) {
-        int cum = above;
-#pragma unroll
-        for (int j = 7; j >= 0; --j) {
-          if (cum + c[j] >= need) {
-            s_digit = 8 * lane + j;
-            s_need = need - cum;
-            s_bin = c[j];
-            break;
-          }
-          cum += c[j];
+      for (int j = 3; j >= 0; --j) {
+        if (cum + c[j] >= need) {
+          s_digit = 4 * r + j;
+          s_need = need - cum;
+          s_bin = c[j];
+          break;
         }
+        cum += c[j];
       }
     }
     __syncthreads();
     prefix |= (uint32_t)s_digit << shift;
     need = s_need;
   };
-  pick_digit(24, hist2[0]);
-
-  // Keys sharing the chosen top byte go to a short list when they fit: each warp counts its
-  // hits, takes its share of the list with one atomic, then writes them.
-  const bool filtered = cached && s_bin <= kSelFilt;
-  if (filtered) {
-    int cnt = 0;
-    for (int base = 0; base < n; base += kSelThreads) {
-      const int i = base + (int)threadIdx.x;
-      cnt += __popc(__ballot_sync(kFullMask, i < n && (s_keys[i] >> 24) == (prefix >> 24)));
+  bool nan_seen = false;
+  const float* cand = row + first;
+  // Scores -> order-preserving keys in shared memory, kSelBatch independent loads in flight
+  // per thread, counted by their first 12 bits on the way.
+  auto take_key = [&](float v, int i) {
+    const uint32_t key = score_key(v);
+    nan_seen |= v != v;
+    if (cached) s_keys[i] = key;
+    atomicAdd(&hist[key >> 20], 1);
+  };
+  if ((reinterpret_cast<uintptr_t>(cand) & 15u) == 0) {
+    // 16-byte loads: thread t takes candidates 4 (t + 1024 u) .. + 3, kSelBatch / 4 loads in flight
+    constexpr int V = kSelBatch / 4;
+    const int n4 = n >> 2;
+    for (int base = 0; base < n4; base += kSelThreads * V) {
+      float4 v[V];
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const int i = base + u * kSelThreads + (int)threadIdx.x;
+        v[u] = i < n4 ? __ldg(reinterpret_cast<const float4*>(cand) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const int i = base + u * kSelThreads + (int)threadIdx.x;
+        if (i < n4) {
+          const uint4 k4 = make_uint4(score_key(v[u].x), score_key(v[u].y), score_key(v[u].z), score_key(v[u].w));
+          nan_seen |= (v[u].x != v[u].x) | (v[u].y != v[u].y) | (v[u].z != v[u].z) | (v[u].w != v[u].w);
+          if (cached) reinterpret_cast<uint4*>(s_keys)[i] = k4;  // one 16-byte store
+          atomicAdd(&hist[k4.x >> 20], 1);
+          atomicAdd(&hist[k4.y >> 20], 1);
+          atomicAdd(&hist[k4.z >> 20], 1);
+          atomicAdd(&hist[k4.w >> 20], 1);
+        }
+      }
     }
-    int at = 0;
-    if (lane == 0 && cnt > 0) at = atomicAdd(&s_fcount, cnt);
-    at = __shfl_sync(kFullMask, at, 0);
-    for (int base = 0; base < n; base += kSelThreads) {
-      const int i = base + (int)threadIdx.x;
-      const uint32_t key = i < n ? s_keys[i] : 0u;
-      const bool hit = i < n && (key >> 24) == (prefix >> 24);
-      const unsigned m = __ballot_sync(kFullMask, hit);
-      if (hit) s_filt[at + __popc(m & ((1u << lane) - 1u))] = key;
-      at += __popc(m);
+    for (int i = 4 * n4 + (int)threadIdx.x; i < n; i += blockDim.x) take_key(__ldg(cand + i), i);
+  } else {
+    for (int base = 0; base < n; base += kSelThreads * kSelBatch) {
+      float v[kSelBatch];
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u) {
+        const int i = base + u * kSelThreads + (int)threadIdx.x;
+        v[u] = i < n ? __ldg(cand + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u) {
+        const int i = base + u * kSelThreads + (int)threadIdx.x;
+        if (i < n) take_key(v[u], i);
+      }
     }
   }
-  // the three other passes: over the short list (its digits spread over the bins, so a plain
-  // shared atomic per key), else over every candidate matching the prefix
-  const int m_keys = filtered ? s_bin : n;
-  if (filtered) __syncthreads();  // the short list is written
-  for (int pass = 1; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    const uint32_t hi_mask = 0xffffffffu << (shift + 8);
-    int* hist = hist2[pass & 1];  // zero since the pass before the previous one (or the start)
-    if (threadIdx.x < 256) hist2[(pass + 1) & 1][threadIdx.x] = 0;  // read last by the previous pick
-    if (filtered) {
-      for (int i = threadIdx.x; i < m_keys; i += blockDim.x) {
-        const uint32_t key = s_filt[i];
-        if ((key & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(key >> shift) & 0xffu], 1);
+  if (nan_seen) record_error(err, PKV_DEV_BAD_SCORE);
+  __syncthreads();
+  pick_digit(20, kSelBins);
+  auto key_at = [&](int i) -> uint32_t { return cached ? s_keys[i] : score_key(__ldg(row + first + i)); };
+
+  // Gathers the keys of `src` (count m) that share the prefix's top `bits` bits into dst: each
+  // warp counts its hits, takes its share of dst with one atomic, then writes them (one
+  // reservation per warp: an atomic per hit would serialise the warps on the counter).
+  auto gather = [&](const uint32_t* src, int m, int bits, uint32_t* dst, int* count) {
+    const uint32_t hi = 0xffffffffu << (32 - bits);
+    const uint32_t want = prefix & hi;
+    int cnt = 0;
+#pragma unroll 4
+    for (int base = 0; base < m; base += kSelThreads) {
+      const int i = base + (int)threadIdx.x;
+      cnt += __popc(__ballot_sync(kFullMask, i < m && (src[i] & hi) == want));
+    }
+    int at = 0;
+    if (lane == 0 && cnt > 0) at = atomicAdd(count, cnt);
+    at = __shfl_sync(kFullMask, at, 0);
+    if (cnt > 0) {
+#pragma unroll 4
+      for (int base = 0; base < m; base += kSelThreads) {
+        const int i = base + (int)threadIdx.x;
+        const uint32_t key = i < m ? src[i] : 0u;
+        const bool hit = i < m && (key & hi) == want;
+        const unsigned msk = __ballot_sync(kFullMask, hit);
+        if (hit) dst[at + __popc(msk & ((1u << lane) - 1u))] = key;
+        at += __popc(msk);
       }
-    } else {
-      for (int base = 0; base < n; base += blockDim.x) {
-        const int i = base + threadIdx.x;
-        const uint32_t key = i < n ? key_at(i) : 0u;
-        const bool hit = i < n && (key & hi_mask) == (prefix & hi_mask);
-        const int digit = (int)((key >> shift) & 0xffu);
-        // warp-aggregated increment: one atomic per distinct digit in the warp
+    }
+    __syncthreads();
+  };
+  // Counts the next digit (at `shift`, `bins` wide) of the keys sharing the prefix's top
+  // `bits` bits, from the short list or from every candidate.
+  auto count_digit = [&](const uint32_t* src, int m, int bits, int shift, int bins) {
+    for (int i = threadIdx.x; i < kSelBins; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const uint32_t hi = 0xffffffffu << (32 - bits);
+    for (int base = 0; base < m; base += blockDim.x) {
+      const int i = base + (int)threadIdx.x;
+      const uint32_t key = i < m ? (src != nullptr ? src[i] : key_at(i)) : 0u;
+      const bool hit = i < m && (key & hi) == (prefix & hi);
+      const int digit = (int)((key >> shift) & (uint32_t)(bins - 1));
+      if (src != nullptr) {
+        if (hit) atomicAdd(&hist[digit], 1);
+      } else {  // every candidate: one atomic per distinct digit of the warp
         const unsigned peers = __match_any_sync(kFullMask, hit ? digit : -1);
         if (hit && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
       }
     }
     __syncthreads();
-    pick_digit(shift, hist);
-    if (pass == 1 && filtered && s_bin <= kSelTiny) {
-      // Few keys share the top 16 bits now: gather them (each warp takes its share with one
-      // atomic) and let warp 0 rank them exactly -- the need-th largest x has
-      // count(> x) < need <= count(>= x) -- instead of two more block-wide passes.
-      for (int base = 0; base < m_keys; base += blockDim.x) {
-        const int i = base + (int)threadIdx.x;
-        const uint32_t key = i < m_keys ? s_filt[i] : 0u;
-        const bool hit = i < m_keys && (key >> 16) == (prefix >> 16);
-        const unsigned m = __ballot_sync(kFullMask, hit);
-        int at = 0;
-        if (lane == 0 && m != 0u) at = atomicAdd(&s_tcount, __popc(m));
-        at = __shfl_sync(kFullMask, at, 0);
-        if (hit) s_tiny[at + __popc(m & ((1u << lane) - 1u))] = key;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        const int mt = s_bin;  // keys in the tiny list
-        const uint32_t k0 = lane < mt ? s_tiny[lane] : 0u, k1 = lane + 32 < mt ? s_tiny[lane + 32] : 0u;
-        int gt0 = 0, ge0 = 0, gt1 = 0, ge1 = 0;
-        for (int j = 0; j < mt; ++j) {
-          const uint32_t x = __shfl_sync(kFullMask, k0, j & 31), y = __shfl_sync(kFullMask, k1, j & 31);
-          const uint32_t kj = j < 32 ? x : y;
-          gt0 += kj > k0;
-          ge0 += kj >= k0;
-          gt1 += kj > k1;
-          ge1 += kj >= k1;
-        }
-        const bool f0 = lane < mt && gt0 < need && need <= ge0;
-        const bool f1 = lane + 32 < mt && gt1 < need && need <= ge1;
-        const unsigned fm = __ballot_sync(kFullMask, f0 || f1);  // lanes holding the key (all equal)
-        const int src = __ffs(fm) - 1;
-        const uint32_t key = __shfl_sync(kFullMask, f0 ? k0 : k1, src);
-        const int rem = __shfl_sync(kFullMask, need - (f0 ? gt0 : gt1), src);
-        if (lane == 0) {
-          s_digit = (int)key;
-          s_need = rem;
+    pick_digit(shift, bins);
+  };
+  // Exact rank of the (at most kSelRank) keys sharing the prefix's top `bits` bits: the one
+  // with count(> x) < need <= count(>= x) is the k_top-th key.
+  auto rank_group = [&](const uint32_t* src, int m, int bits) {
+    gather(src, m, bits, s_rank, &s_rcount);
+    const int mr = s_rcount;
+    if ((int)threadIdx.x < mr) {
+      const uint32_t x = s_rank[threadIdx.x];
+      int gt = 0, ge = 0;
+      int j = 0;
+      for (; j + 8 <= mr; j += 8) {  // 8 independent (broadcast) loads in flight
+        uint32_t y[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) y[u] = s_rank[j + u];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          gt += y[u] > x;
+          ge += y[u] >= x;
         }
       }
-      __syncthreads();
-      prefix = (uint32_t)s_digit;
-      need = s_need;
-      break;
+      for (; j < mr; ++j) {
+        const uint32_t y = s_rank[j];
+        gt += y > x;
+        ge += y >= x;
+      }
+      if (gt < need && need <= ge) {  // every thread holding x writes the same values
+        s_thr = x;
+        s_digit = need - gt;
+      }
     }
+    __syncthreads();
+    prefix = s_thr;
+    need = s_digit;
+  };
+
+  int bits = 12;
+  if (cached && s_bin <= kSelRank) {
+    rank_group(s_keys, n, bits);
+  } else if (cached && s_bin <= kSelFilt) {
+    const int m = s_bin;
+    gather(s_keys, n, bits, s_filt, &s_fcount);
+    count_digit(s_filt, m, bits, 8, kSelBins);
+    bits = 24;
+    if (s_bin <= kSelRank) {
+      rank_group(s_filt, m, bits);
+    } else {
+      count_digit(s_filt, m, bits, 0, 256);
+    }
+  } else {  // too many keys share the first digit for the short list: passes over every key
+    count_digit(nullptr, n, bits, 8, kSelBins);
+    count_digit(nullptr, n, 24, 0, 256);
   }
   const uint32_t thr = prefix;  // key of the k_top-th best candidate
 
@@ -537,11 +561,13 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   auto masks = [&](int i0, uint32_t (&m)[4]) {  // gt lo, gt hi, eq lo, eq hi
     m[0] = m[1] = m[2] = m[3] = 0u;
     const int i1 = min(c1, i0 + 64), mid = min(i1, i0 + 32);
+#pragma unroll 8
     for (int i = i0; i < mid; ++i) {
       const uint32_t key = key_at(i);
       m[0] |= (uint32_t)(key > thr) << (i - i0);
       m[2] |= (uint32_t)(key == thr) << (i - i0);
     }
+#pragma unroll 8
     for (int i = mid; i < i1; ++i) {
       const uint32_t key = key_at(i);
       m[1] |= (uint32_t)(key > thr) << (i - i0 - 32);
@@ -579,8 +605,6 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
       }
     }
   }
-  for (int t = threadIdx.x; t < n_sink; t += blockDim.x) out[t] = t;
-  for (int t = threadIdx.x; t < n_recent; t += blockDim.x) out[n_sink + k_top + t] = first + n + t;
 }
 
 // Rolling admission of a decode step's token into a sparse layer of fixed budget ("How KV

@@ -196,3 +196,34 @@ def test_topk_uncached_long_lists_and_zero_k(k_top):
     scores = torch.empty((3, 2, 60000)).exponential_(generator=g)
     scores[0, 1, 1000:9000] = 4.0          # ties across the cut
     _assert_same_selection(*_topk_both(scores, lens, 3, 64, k_top))
+
+
+@pytest.mark.parametrize("shape", ["uniform_1_2", "block_of_equals", "all_equal", "two_values", "ties_at_cut"])
+def test_topk_digit_paths(shape):
+    """Score distributions that take each route of the radix select: few keys sharing the first
+    12-bit digit (ranked at once), a few thousand sharing it (a short list and a second digit),
+    thousands sharing 24 bits (a third digit), and every candidate sharing it (passes over every
+    key); bit-exact against the oracle, ties by lower position."""
+    g = torch.Generator().manual_seed(77)
+    B, H, S = 3, 2, 16384
+    lens = torch.tensor([16384, 15000, 9000], dtype=torch.int32)
+    if shape == "uniform_1_2":       # one exponent: 8 first-digit bins of ~2000 keys each
+        scores = 1.0 + torch.rand((B, H, S), generator=g)
+    elif shape == "block_of_equals":  # 2000 equal keys straddling the cut, inside one 24-bit group
+        scores = torch.rand((B, H, S), generator=g)
+        scores[:, :, 3000:5000] = 0.98765
+    elif shape == "all_equal":
+        scores = torch.full((B, H, S), 0.5)
+    elif shape == "ties_at_cut":      # Exp(1), with 30 more candidates set to the 512th best value
+        scores = torch.empty((B, H, S)).exponential_(generator=g)
+        for b in range(B):
+            L = int(lens[b])
+            for h in range(H):
+                cand = scores[b, h, 4:L - 1024]
+                v = torch.sort(cand, descending=True).values[511]
+                below = torch.nonzero(cand < v).flatten()
+                pick = below[torch.randperm(below.numel(), generator=g)[:30]]
+                cand[pick] = v
+    else:                             # two values: the cut falls inside the larger one's ties
+        scores = torch.where(torch.rand((B, H, S), generator=g) < 0.02, 2.0, 1.0)
+    _assert_same_selection(*_topk_both(scores, lens, 4, 1024, 512))

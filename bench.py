@@ -704,9 +704,15 @@ def _prefill_row(pkv, W, dev, stream, args, alpha=256):
     peak, kind = _tensor_peak()
     tf = flop / (ms_given * 1e-3) / 1e12
     del c, q_win, acc, lse
+    # the exponential unit's bound: one ex2 per probability on the MUFU, 16 per clock per SM
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ex2_peak = sms * 16 * 2.07e9
+    exps = pairs * hq / (ms_given * 1e-3)
     return {"ms_lse_given": round(ms_given, 4), "ms_lse_computed": round(ms_both, 4), "tflops": round(tf, 1),
             "frac": round(tf / peak, 4), "peak": peak, "peak_kind": kind, "bound": "tensor",
-            "exps_per_s": round(pairs * hq / (ms_given * 1e-3), 1),
+            "exps_per_s": round(exps, 1),
+            "ex2_roofline": {"peak_per_s": ex2_peak, "frac": round(exps / ex2_peak, 4),
+                             "what": f"MUFU ex2: {sms} SMs x 16 per clock x 2.07 GHz (maximum SM clock)"},
             "what": "16 prompts x 16384 tokens, 32/8 heads, d 128, window 256 (tcgen05 UMMA bf16 into TMEM + ex2)"}
 
 

@@ -650,6 +650,11 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   // use sl2q = sl2 over that power; o is kept in units of a V-scale reference vref that moves
   // (and rescales o) only when a unit's largest V scale exceeds it by kVrefSlack.
   float sl2q = sl2, vref = 0.f, inv_vref = 0.f;
+  // INT8 pools: K codes enter q.K as the fp16 numbers 1152 + code (no subtraction per element);
+  // each unit's S accumulator starts at -1152 sum_k q'_k of its head instead of 0, computed once
+  // per segment by the tensor core from the same q fragments (accumulator layout: rows gq, gq + 8,
+  // heads 2tq, 2tq + 1).
+  float kbias[4] = {0.f, 0.f, 0.f, 0.f};
   // Dense append mode: this step's K (lanes 0-15) or V (lanes 16-31) row chunk of the current
   // segment, to be written at token L_b - 1 (pool and tile) when its unit is consumed.
   // INT8 pools: the half-warp quantizes its row when the segment begins (the INT8 append's row
@@ -738,6 +743,14 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
       sl2q = sl2 * __int_as_float((127 - kq) << 23);
 #pragma unroll
       for (int i = 0; i < 2 * KS; ++i) qb[i] = pack_f16x2(bf16_lo_to_f32(qraw[i]) * up, bf16_hi_to_f32(qraw[i]) * up);
+      {
+        constexpr uint32_t kNeg1152 = 0xe480e480u;  // fp16x2 (-1152, -1152)
+        const uint32_t ab[4] = {kNeg1152, kNeg1152, kNeg1152, kNeg1152};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) kbias[i] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) mma_f16_m16n8k16(kbias, ab, qb[2 * ks], qb[2 * ks + 1]);
+      }
       vref = 0.f;
       inv_vref = 0.f;
     } else {
@@ -855,23 +868,23 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     }
     if (mask != 0u) {
       // -- S^T = K q^T: 16 tokens x 8 heads --------------------------------------------------
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      float c[4] = {kbias[0], kbias[1], kbias[2], kbias[3]};  // zero but for INT8 pools
       const uint32_t kbase = smem_u32(Wt.k[slot]);
       float fk0 = sl2, fk1 = sl2;  // logit factor of tokens gq and gq + 8
       if constexpr (Q8) {
         // int8 rows: one ldmatrix yields two k-steps; each lane holds 4 consecutive columns
-        // of a row per matrix, the order q was loaded in
+        // of a row per matrix, the order q was loaded in; the codes enter as 1152 + code
 #pragma unroll
         for (int pp = 0; pp < KS / 2; ++pp) {
           uint32_t r[4];
           ldsm_x4(kbase + chunk_offset<D, SPARSE, Q8>(k_row, 2 * pp + k_half), r);
           const uint32_t f0 = r[0] ^ 0x80808080u, f1 = r[1] ^ 0x80808080u;
           const uint32_t f2 = r[2] ^ 0x80808080u, f3 = r[3] ^ 0x80808080u;
-          const uint32_t a0[4] = {i8x2_to_f16x2<0x4140>(f0), i8x2_to_f16x2<0x4140>(f1),
-                                  i8x2_to_f16x2<0x4342>(f0), i8x2_to_f16x2<0x4342>(f1)};
+          const uint32_t a0[4] = {i8x2_to_biased_f16x2<0x4140>(f0), i8x2_to_biased_f16x2<0x4140>(f1),
+                                  i8x2_to_biased_f16x2<0x4342>(f0), i8x2_to_biased_f16x2<0x4342>(f1)};
           mma_f16_m16n8k16(c, a0, qb[4 * pp], qb[4 * pp + 1]);
-          const uint32_t a1[4] = {i8x2_to_f16x2<0x4140>(f2), i8x2_to_f16x2<0x4140>(f3),
-                                  i8x2_to_f16x2<0x4342>(f2), i8x2_to_f16x2<0x4342>(f3)};
+          const uint32_t a1[4] = {i8x2_to_biased_f16x2<0x4140>(f2), i8x2_to_biased_f16x2<0x4140>(f3),
+                                  i8x2_to_biased_f16x2<0x4342>(f2), i8x2_to_biased_f16x2<0x4342>(f3)};
           mma_f16_m16n8k16(c, a1, qb[4 * pp + 2], qb[4 * pp + 3]);
         }
         fk0 = warps_scales[warp].k[slot][gq] * sl2q;
@@ -904,27 +917,33 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
           if (t1 && v1) lg[a.score_stride + 8] = s11;
         }
       }
+      // lazy running max: move it only when this unit's max is well above it.  Each lane checks
+      // its own two tokens first; the unit's maxima (shuffles over the 8 token rows) are needed
+      // only when some lane's logit, or (INT8 pools) V scale, is past its reference.
       float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
-#pragma unroll
-      for (int m = 4; m <= 16; m <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, m));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, m));
-      }
-      // INT8 pools: the V scales of the attended tokens, and their largest (warp-uniform)
+      // INT8 pools: the V scales of the attended tokens, and their largest
       float vs0 = 0.f, vs1 = 0.f;
-      bool gv = false;
       float vm = 0.f;
       if constexpr (Q8) {
         vs0 = t0 ? warps_scales[warp].v[slot][gq] : 0.f;
         vs1 = t1 ? warps_scales[warp].v[slot][gq + 8] : 0.f;
         vm = fmaxf(vs0, vs1);
-#pragma unroll
-        for (int m = 4; m <= 16; m <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullMask, vm, m));
-        gv = vm > vref * kVrefSlack;
       }
-      // lazy running max: move it only when this unit's max is well above it
-      const bool g0 = mx0 > mr0 + kRescaleSlack, g1 = mx1 > mr1 + kRescaleSlack;
-      if (__any_sync(kFullMask, g0 || g1) || gv) {
+      bool g0 = mx0 > mr0 + kRescaleSlack, g1 = mx1 > mr1 + kRescaleSlack;
+      bool gv = Q8 && vm > vref * kVrefSlack;
+      if (__any_sync(kFullMask, g0 || g1 || gv)) {
+#pragma unroll
+        for (int m = 4; m <= 16; m <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, m));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, m));
+        }
+        g0 = mx0 > mr0 + kRescaleSlack;
+        g1 = mx1 > mr1 + kRescaleSlack;
+        if constexpr (Q8) {  // warp-uniform: the scales of a token are the same in its 4 lanes
+#pragma unroll
+          for (int m = 4; m <= 16; m <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullMask, vm, m));
+          gv = vm > vref * kVrefSlack;
+        }
         float al0 = 1.f, al1 = 1.f;
         if (g0) {
           al0 = exp2f(mr0 - mx0);

@@ -318,6 +318,15 @@ __device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t flipped) {
   return r;
 }
 
+// The same two codes as the fp16 numbers 1152 + code (the subtraction left to the caller: a
+// contraction over such values differs from the codes' by 1152 times the sum of the other operand).
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t i8x2_to_biased_f16x2(uint32_t flipped) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(flipped), "r"(0x64646464u), "n"(SEL));
+  return r;
+}
+
 __device__ __forceinline__ float bf16_lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 

@@ -236,7 +236,10 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
 
 // ---------------------------------------------------------------------------- top-k select
 
-constexpr int kSelThreads = 1024;
+#ifndef PKV_SEL_THREADS
+#define PKV_SEL_THREADS 1024
+#endif
+constexpr int kSelThreads = PKV_SEL_THREADS;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelSmemKeys = 40960;  // candidates cached in shared memory (160 KiB)
 constexpr int kSelBins = 4096;       // 12-bit digits (the last digit has 8 bits)
@@ -362,26 +365,31 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   }
   __syncthreads();
   // The digit holding the need-th largest key among those matching the prefix so far:
-  // count(> d) < need <= count(>= d).  Thread t owns the 4 bins [4r, 4r + 4), r = 1023 - t, so
-  // an exclusive scan over the threads counts the keys in higher bins.
+  // count(> d) < need <= count(>= d).  Thread t owns the bins [PB r, PB r + PB), r = threads - 1 - t,
+  // so an exclusive scan over the threads counts the keys in higher bins.
   uint32_t prefix = 0u;
   int need = k_top;
   auto pick_digit = [&](int shift, int bins) {
+    constexpr int PB = kSelBins / kSelThreads;  // bins per thread
     const int r = kSelThreads - 1 - (int)threadIdx.x;
-    int c[4] = {0, 0, 0, 0};
-    if (4 * r < bins) {
-      const int4 h = reinterpret_cast<const int4*>(hist)[r];
-      c[0] = h.x; c[1] = h.y; c[2] = h.z; c[3] = h.w;
+    int c[PB];
+#pragma unroll
+    for (int j = 0; j < PB; j += 4) {
+      int4 h = make_int4(0, 0, 0, 0);
+      if (PB * r + j < bins) h = reinterpret_cast<const int4*>(hist)[(PB * r + j) / 4];
+      c[j] = h.x; c[j + 1] = h.y; c[j + 2] = h.z; c[j + 3] = h.w;
     }
-    const int own = c[0] + c[1] + c[2] + c[3];
+    int own = 0;
+#pragma unroll
+    for (int j = 0; j < PB; ++j) own += c[j];
     int above, unused;
     block_exclusive_scan2(own, 0, warp_sums, &above, &unused);
     if (own > 0 && above < need && need <= above + own) {
       int cum = above;
 #pragma unroll
-      for (int j = 3; j >= 0; --j) {
+      for (int j = PB - 1; j >= 0; --j) {
         if (cum + c[j] >= need) {
-          s_digit = 4 * r + j;
+          s_digit = PB * r + j;
           s_need = need - cum;
           s_bin = c[j];
           break;

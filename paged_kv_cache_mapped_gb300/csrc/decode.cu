@@ -23,9 +23,9 @@
 //    per-slot mbarriers.  Dense mode fills them with TMA tiled copies of a 2-D tensor map
 //    over the pool (one 64-column x 16-row box per 128 bytes of row, 128-byte swizzle, L2
 //    evict-first): 4 copy operations per unit, and the swizzle puts the 8 rows an ldmatrix
-//    reads in 8 different bank groups.  Sparse mode gathers rows: each lane issues one
-//    256-byte cp.async.bulk row copy chosen through its kept index into rows stored at a
-//    272-byte pitch (again conflict-free for ldmatrix).
+//    reads in 8 different bank groups.  Sparse mode gathers rows chosen through their kept
+//    indices as 16-byte cp.async chunks (each lane one chunk of several rows) into the same
+//    swizzled layout, so both modes share the consumer.
 //  * GQA: the G <= 8 query heads sharing a kv head are processed together, so each K/V byte
 //    is read from HBM once per kv head.
 //  * Both contractions run on the tensor cores as warp-level mma.m16n8k16 (bf16 inputs,
@@ -39,8 +39,8 @@
 //    codes become fp16 in registers (a byte permute under the exponent of 1024 and one
 //    subtraction per pair), both products take fp16 operands, the K row scales multiply the
 //    logits and the V row scales enter P, relative to a per-segment reference scale, as one
-//    fp16 term.  Sparse rows are (d + 16)-byte pitched copies, their scales 4-byte copies
-//    completing on the same barrier.
+//    fp16 term.  Sparse rows arrive chunk by chunk as above, their scales as 4-byte copies
+//    completing on the K barrier.
 //  * Online softmax ("How KV Sparsity...", section "2. Attention modification", Fig. 7:
 //    running max, running sum, rescale, divide at the end) in base 2 with log2(e) folded
 //    into the scale; the running max only moves when a unit's max exceeds it by 2^8, so the
@@ -62,8 +62,7 @@ template <int D, bool SPARSE, bool Q8 = false>
 struct Geo {
   static constexpr int kRow = Q8 ? D : D * 2;              // bytes per K/V row in HBM
   static constexpr int kBoxes = Q8 ? 1 : D / 64;           // dense: 128-byte column boxes per row
-  static constexpr int kPitch = kRow + 16;                 // sparse: padded row pitch in smem
-  static constexpr int kTile = SPARSE ? 16 * kPitch : 16 * kRow;  // bytes per tile
+  static constexpr int kTile = 16 * kRow;                  // bytes per tile
   static constexpr int kKSteps = D / 16;                   // k-steps of q.K, m-tiles of P.V
   static constexpr int kRing = (SPARSE && D == 128) ? PKV_RING_SPARSE_D128
                                : Q8 ? ((D == 128) ? PKV_RING_Q8_D128 : PKV_RING_Q8_D64)
@@ -71,18 +70,16 @@ struct Geo {
   static_assert((Q8 || kBoxes * 128 == kRow) && kRing >= 2, "head_dim must be a multiple of 64");
 };
 
-// Byte offset inside a tile of the 16-byte chunk holding row r, columns [8c, 8c + 8).
-// Dense tiles are kBoxes boxes of 16 rows x 128 bytes written by TMA with the 128-byte
-// swizzle (chunk index XOR row % 8 inside each 1024-byte box); sparse tiles are plain rows
-// at the padded pitch.
-// INT8 tiles are one box of 16 rows x D bytes, written with the swizzle of the row size:
+// Byte offset inside a tile of the 16-byte chunk c of row r.
+// bf16 tiles are kBoxes boxes of 16 rows x 128 bytes, in the layout TMA writes with the 128-byte
+// swizzle (chunk index XOR row % 8 inside each 1024-byte box).
+// INT8 tiles are one box of 16 rows x D bytes, in the layout of the swizzle of the row size:
 // 128 bytes (chunk XOR row % 8) at D = 128, 64 bytes (chunk XOR (row / 2) % 4) at D = 64.
-// Either way the 8 rows an ldmatrix reads land in 8 different bank groups.
+// Either way the 8 rows an ldmatrix reads land in 8 different bank groups.  The gather form
+// writes the same layout chunk by chunk (cp.async), so both forms share one consumer.
 template <int D, bool SPARSE, bool Q8 = false>
 __device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
-  if constexpr (SPARSE) {
-    return (uint32_t)(r * Geo<D, SPARSE, Q8>::kPitch + c * 16);
-  } else if constexpr (Q8) {
+  if constexpr (Q8) {
     if constexpr (D == 128)
       return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
     else
@@ -544,7 +541,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   }
 
   // Issue unit k (the one `ic` names) into slot k % R.  Dense: lane 0 copies the K and V
-  // tiles as TMA boxes.  Sparse: lane r < 16 copies K row r, lane 16 + r V row r.
+  // tiles as TMA boxes.  Sparse: every lane copies chunks of the unit's kept rows.
   auto issue = [&](int k) {
     const int slot = k % R;
     fence_proxy_async_smem();
@@ -596,30 +593,46 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         sp_stage2();
         sp_stage1();
       }
-      const int row = __shfl_sync(kFullMask, sp_row, ((k & 1) << 4) | r);
+      const int pb = (k & 1) << 4;  // lanes of sp_row holding this unit's rows
+      const int row = __shfl_sync(kFullMask, sp_row, pb | r);
       const bool ok = row >= 0;
-      const size_t src = (size_t)(ok ? row : 0) * GE::kRow;  // bytes
       const uint32_t vmask = __ballot_sync(kFullMask, ok) & 0xffffu;  // K and V lanes agree
+      // The rows arrive as 16-byte cp.async chunks into the dense tiles' swizzled layout: lane l
+      // copies chunk l % CPR of rows l / CPR + RPI i.  These are ordinary per-lane instructions
+      // (a bulk copy per lane with its own address costs the warp one issue per lane: ~300
+      // instructions per unit, measured).  Each lane then registers its copies with the slot's
+      // barriers -- the K chunks and, over INT8 pools, both rows' scales (the softmax reads the V
+      // scales before the V rows land) with the K barrier, the V chunks with the V barrier --
+      // before lane 0's own arrivals.
+      constexpr int CPR = GE::kRow / 16;  // 16-byte chunks per row
+      constexpr int RPI = 32 / CPR;       // rows one warp instruction covers
+      const int cc = lane % CPR, r0 = lane / CPR;
+      int rows[16 / RPI];
+#pragma unroll
+      for (int i = 0; i < 16 / RPI; ++i) rows[i] = __shfl_sync(kFullMask, sp_row, pb | (r0 + RPI * i));
       if constexpr (Q8) {
-        // the row's scale (K lanes: K, V lanes: V) by a 4-byte asynchronous copy that the K
-        // barrier tracks (the softmax reads the V scales before the V rows land); every lane
-        // registers with the barrier before lane 0's expect-tx arrival below
         auto& Ws = warps_scales[warp];
         if (ok) cp_async_4(is_v ? &Ws.v[slot][r] : &Ws.k[slot][r], (is_v ? a.v_scale : a.k_scale) + row);
-        cp_async_mbar_arrive(&Wb.bar_k[slot]);
-        __syncwarp();
       }
+      const unsigned char* kb = reinterpret_cast<const unsigned char*>(a.k_cache) + cc * 16;
+      const unsigned char* vb = reinterpret_cast<const unsigned char*>(a.v_cache) + cc * 16;
+#pragma unroll
+      for (int i = 0; i < 16 / RPI; ++i)
+        if (rows[i] >= 0)
+          cp_async_16(Wt.k[slot] + chunk_offset<D, SPARSE, Q8>(r0 + RPI * i, cc), kb + (size_t)rows[i] * GE::kRow, pol);
+      cp_async_mbar_arrive(&Wb.bar_k[slot]);
+#pragma unroll
+      for (int i = 0; i < 16 / RPI; ++i)
+        if (rows[i] >= 0)
+          cp_async_16(Wt.v[slot] + chunk_offset<D, SPARSE, Q8>(r0 + RPI * i, cc), vb + (size_t)rows[i] * GE::kRow, pol);
+      cp_async_mbar_arrive(&Wb.bar_v[slot]);
+      __syncwarp();
       if (lane == 0) {
         Wb.meta[slot] = vmask;
-        mbar_arrive_expect_tx(&Wb.bar_k[slot], __popc(vmask) * GE::kRow);
-        mbar_arrive_expect_tx(&Wb.bar_v[slot], __popc(vmask) * GE::kRow);
+        mbar_arrive_expect_tx(&Wb.bar_k[slot], 0);
+        mbar_arrive_expect_tx(&Wb.bar_v[slot], 0);
       }
       __syncwarp();
-      if (ok) {
-        unsigned char* dst = (is_v ? Wt.v[slot] : Wt.k[slot]) + r * GE::kPitch;
-        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(is_v ? a.v_cache : a.k_cache) + src, GE::kRow,
-                 is_v ? &Wb.bar_v[slot] : &Wb.bar_k[slot], pol);
-      }
       advance(ic, s_nb, a.B, a.Hkv);
     }
   };
@@ -1073,6 +1086,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   }
 
   if (aborted) {  // let the copies in flight land before the CTA's shared memory goes away
+    if constexpr (SPARSE) cp_async_wait_all();
     for (int kk = k; kk < issued; ++kk) {
       (void)mbar_wait_bounded(&Wb.bar_k[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);
       (void)mbar_wait_bounded(&Wb.bar_v[kk % R], (uint32_t)(kk / R) & 1u, a.timeout_ns);

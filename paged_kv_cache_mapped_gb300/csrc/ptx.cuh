@@ -116,6 +116,17 @@ __device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src_gmem)
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 only (no L1 allocation), with an L2
+// policy; both addresses 16-byte aligned.  Completion as cp_async_4 (cp_async_mbar_arrive).
+__device__ __forceinline__ void cp_async_16(void* dst_smem, const void* src_gmem, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)),
+               "l"(src_gmem), "l"(policy)
+               : "memory");
+}
+
+// Waits until every cp.async copy this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Makes `bar` track this thread's earlier cp.async copies: its pending arrival count grows by
 // one now and an arrival follows once they have landed, so the current phase cannot complete
 // before them (call it before the phase's last ordinary arrival).

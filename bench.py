@@ -1087,7 +1087,7 @@ def run_reference(args):
 
 # ------------------------------------------------------------------- small profiling cases
 
-CASES = ("q8", "gather", "prefill", "kvops", "layers", "append", "qwen8", "qwen8_plain")
+CASES = ("q8", "gather", "gather_q8", "prefill", "kvops", "layers", "append", "qwen8", "qwen8_plain")
 
 
 def run_case(name: str, calls: int = 3):
@@ -1097,6 +1097,7 @@ def run_case(name: str, calls: int = 3):
 
       q8       llama8b-shaped layer over INT8 pools: paged_decode_attention_q8
       gather   one sparse layer: kv_select_topk, then sparse_decode_attention (gather form)
+      gather_q8  the same over INT8 pools: sparse_decode_attention_q8
       prefill  one sparse layer: prefill_window_scores with the lse computed, then given
       kvops    one sparse layer: kv_select_topk, kv_compact, kv_compact_q8 in turn
       layers   a qwen1p5b layer (append + decode), a full sparse layer, a compacted sparse layer
@@ -1135,7 +1136,7 @@ def run_case(name: str, calls: int = 3):
             else:
                 pkv.kv_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"], c["slot_mapping"])
                 pkv.kv_append_q8(kq, vq, ks, vs, c["k_new"], c["v_new"], c["slot_mapping"])
-    elif name in ("gather", "kvops"):
+    elif name in ("gather", "gather_q8", "kvops"):
         wl = W.WORKLOADS["sparse"]
         lens = W.context_lengths(wl)
         B, hkv, d, K = wl.batch, wl.num_kv_heads, wl.head_dim, wl.keep_max
@@ -1149,6 +1150,14 @@ def run_case(name: str, calls: int = 3):
             for _ in range(calls):
                 pkv.sparse_decode_attention(src["q"], src["k_cache"], src["v_cache"], src["block_tables"],
                                             src["context_lens"], kept, kl, wl.scale)
+        elif name == "gather_q8":
+            pkv.kv_select_topk(scores, src["context_lens"], wl.n_sink, wl.n_recent, wl.k_top,
+                               kept_out=kept, kept_lens_out=kl)
+            kq, vq, ks, vs = q8_pools(src["k_cache"].shape[0], hkv, d, 43, exp_scales)
+            del src["k_cache"], src["v_cache"]
+            for _ in range(calls):
+                pkv.sparse_decode_attention_q8(src["q"], kq, vq, ks, vs, src["block_tables"], src["context_lens"],
+                                               kept, kl, wl.scale)
         else:
             dbt_cpu, dnb = W.compact_tables(K, B, seed=5)
             dbt = dbt_cpu.to(dev)

@@ -245,6 +245,8 @@ constexpr int kSelSmemKeys = 40960;  // candidates cached in shared memory (160 
 constexpr int kSelBins = 4096;       // 12-bit digits (the last digit has 8 bits)
 constexpr int kSelFilt = 4096;       // keys sharing the first digit kept in a short list
 constexpr int kSelRank = kSelThreads;  // keys sharing a prefix ranked exactly, one per thread
+constexpr int kSelFast = kSelRank;     // threshold bins up to this size take the one-pass path
+constexpr int kSelRankLanes = 4;       // one-pass path: threads ranking one key of the bin
 constexpr int kSelBatch = 16;        // score loads in flight per thread
 // dynamic shared memory: the cached keys
 constexpr int kSelDynSmem = kSelSmemKeys * (int)sizeof(uint32_t);
@@ -304,6 +306,26 @@ __device__ __forceinline__ void block_exclusive_scan2(int a, int b, int* sums, i
   __syncthreads();
 }
 
+// Block-wide exclusive prefix of one int per thread with a single barrier: warps scan in
+// registers, publish their totals in `wsum` (kSelWarps ints), and every warp adds the totals of
+// the warps before it.  `wsum` must not be written again before the block's next barrier.
+__device__ __forceinline__ int block_exclusive_scan1(int a, int* wsum) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  int incl = a;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int before = lane < warp ? wsum[lane] : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(kFullMask, before, o);
+  return before + incl - a;
+}
+
 // Kept-token selection for one (sequence, kv head) per CTA ("How KV Sparsity...": sections
 // "System model" -- drop low-score KV, retain high-score and recent KV -- and "2. Attention
 // modification" -- per layer and head, the top-k tokens by accumulated score; sink tokens
@@ -319,15 +341,17 @@ __device__ __forceinline__ void block_exclusive_scan2(int a, int b, int* sums, i
 // owns a run of consecutive candidates, marks its kept ones in 64-bit masks, and one block scan
 // places them, so the kept list is written in ascending position and the result is exact and
 // unique.
-__global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
+__global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(
     int32_t* __restrict__ kept_out, int32_t* __restrict__ kept_lens_out,
     const float* __restrict__ scores, int stride, const int32_t* __restrict__ lens, int Hkv,
     int n_sink, int n_recent, int k_top, int32_t* err) {
   extern __shared__ __align__(16) uint32_t s_keys[];  // kSelSmemKeys keys when the candidates fit
   __shared__ __align__(16) int hist[kSelBins];
-  __shared__ uint32_t s_filt[kSelFilt];        // keys sharing the first digit (when they fit)
+  __shared__ __align__(16) uint32_t s_filt[kSelFilt];        // keys sharing the first digit (when they fit)
   __shared__ uint32_t s_rank[kSelRank];        // keys sharing the prefix, ranked exactly
   __shared__ int warp_sums[2 * (kSelWarps + 1)];
+  __shared__ int warp_tot[kSelWarps];          // block_exclusive_scan1's warp totals
+  __shared__ uint32_t kept_bits[kSelSmemKeys / 32];  // one-pass path: kept keys of the threshold bin
   __shared__ int s_digit, s_need, s_bin, s_fcount, s_rcount;
   __shared__ uint32_t s_thr;
 
@@ -359,6 +383,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   const int lane = threadIdx.x & 31;
 
   for (int i = threadIdx.x; i < kSelBins; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i < kSelSmemKeys / 32; i += blockDim.x) kept_bits[i] = 0u;
   if (threadIdx.x == 0) {
     s_fcount = 0;
     s_rcount = 0;
@@ -382,8 +407,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     int own = 0;
 #pragma unroll
     for (int j = 0; j < PB; ++j) own += c[j];
-    int above, unused;
-    block_exclusive_scan2(own, 0, warp_sums, &above, &unused);
+    const int above = block_exclusive_scan1(own, warp_tot);
     if (own > 0 && above < need && need <= above + own) {
       int cum = above;
 #pragma unroll
@@ -455,6 +479,105 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   if (nan_seen) record_error(err, PKV_DEV_BAD_SCORE);
   __syncthreads();
   pick_digit(20, kSelBins);
+
+  // Thread t owns candidates [t*C, t*C + C) (C odd: conflict-free shared-memory reads), at most
+  // 64 at a time as bit masks (two 32-bit halves).
+  int C = (n + blockDim.x - 1) / blockDim.x;
+  C |= 1;
+  const int c0 = min(n, (int)threadIdx.x * C);
+  const int c1 = min(n, c0 + C);
+
+  // One-pass path (the keys cached, at most kSelFast keys in the k_top-th key's first-digit bin
+  // d1): one ordered pass marks each thread's keys above bin d1 and gathers the bin's keys with
+  // their positions; each of those is ranked against the others (larger key first, then lower
+  // position) by kSelRankLanes threads, and the `need` best are set in a bitmap of kept
+  // candidates; a block scan then places every thread's kept positions, in ascending order.  The kept set is the general path's: every key above the
+  // k_top-th, then the lowest positions among the keys equal to it.
+  if (cached && s_bin <= kSelFast) {
+    const uint32_t d1 = prefix >> 20;
+    const int need1 = need;
+    // the bin's keys as (key, ~position): a larger value ranks first, so equal keys go by
+    // lower position and every value is distinct
+    unsigned long long* s_rk = reinterpret_cast<unsigned long long*>(s_filt);
+    uint32_t above[2] = {0u, 0u}, inbin[2] = {0u, 0u};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i0 = c0 + 32 * h, i1 = min(c1, i0 + 32);
+#pragma unroll 8
+      for (int i = i0; i < i1; ++i) {
+        const uint32_t dg = s_keys[i] >> 20;
+        above[h] |= (uint32_t)(dg > d1) << (i - i0);
+        inbin[h] |= (uint32_t)(dg == d1) << (i - i0);
+      }
+    }
+    // the bin's keys, one reservation per warp
+    const int nin = __popc(inbin[0]) + __popc(inbin[1]);
+    int incl = nin;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int at = 0;
+    if (lane == 31 && incl > 0) at = atomicAdd(&s_rcount, incl);
+    at = __shfl_sync(kFullMask, at, 31) + incl - nin;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t bits = inbin[h];
+      while (bits != 0u) {
+        const int i = c0 + 32 * h + __ffs(bits) - 1;
+        bits &= bits - 1u;
+        s_rk[at] = ((unsigned long long)s_keys[i] << 32) | (uint32_t)~i;
+        ++at;
+      }
+    }
+    __syncthreads();
+    const int m = s_rcount;  // == s_bin
+    constexpr int kGroups = kSelThreads / kSelRankLanes;
+    const int sub = (int)threadIdx.x & (kSelRankLanes - 1);
+    for (int j0 = 0; j0 < m; j0 += kGroups) {  // uniform trip count: the shuffles see every lane
+      const int j = j0 + (int)threadIdx.x / kSelRankLanes;
+      int r = 0;
+      unsigned long long x = 0ull;
+      if (j < m) {
+        x = s_rk[j];
+        int k = sub;
+        for (; k + 3 * kSelRankLanes < m; k += 4 * kSelRankLanes) {
+          const unsigned long long y0 = s_rk[k], y1 = s_rk[k + kSelRankLanes];
+          const unsigned long long y2 = s_rk[k + 2 * kSelRankLanes], y3 = s_rk[k + 3 * kSelRankLanes];
+          r += (int)(y0 > x) + (int)(y1 > x) + (int)(y2 > x) + (int)(y3 > x);
+        }
+        for (; k < m; k += kSelRankLanes) r += (int)(s_rk[k] > x);
+      }
+#pragma unroll
+      for (int o = 1; o < kSelRankLanes; o <<= 1) r += __shfl_xor_sync(kFullMask, r, o);
+      if (j < m && sub == 0 && r < need1) {
+        const int px = (int)~(uint32_t)x;
+        atomicOr(&kept_bits[px >> 5], 1u << (px & 31));
+      }
+    }
+    __syncthreads();
+    // the bitmap's bits of [start, start + 32), start >= 0 (bits past n are zero or unread)
+    auto bits32 = [&](int start) -> uint32_t {
+      const int w = start >> 5, sh = start & 31;
+      const uint32_t lo = kept_bits[w] >> sh;
+      return sh == 0 ? lo : lo | (kept_bits[w + 1] << (32 - sh));
+    };
+    uint32_t take[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) take[h] = above[h] | (inbin[h] != 0u ? inbin[h] & bits32(c0 + 32 * h) : 0u);
+    const int cnt = __popc(take[0]) + __popc(take[1]);
+    int w = n_sink + block_exclusive_scan1(cnt, warp_tot);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t t = take[h];
+      while (t != 0u) {
+        out[w++] = first + c0 + 32 * h + (__ffs(t) - 1);
+        t &= t - 1u;
+      }
+    }
+    return;
+  }
   auto key_at = [&](int i) -> uint32_t { return cached ? s_keys[i] : score_key(__ldg(row + first + i)); };
 
   // Gathers the keys of `src` (count m) that share the prefix's top `bits` bits into dst: each
@@ -559,13 +682,9 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
   }
   const uint32_t thr = prefix;  // key of the k_top-th best candidate
 
-  // Ordered pass: thread t owns candidates [t*C, t*C + C) (C odd: conflict-free smem reads),
-  // 64 at a time as bit masks (two 32-bit halves) of the keys above thr and equal to it.  A
-  // run of at most 64 (always, with the keys cached) keeps its masks for the write.
-  int C = (n + blockDim.x - 1) / blockDim.x;
-  C |= 1;
-  const int c0 = min(n, (int)threadIdx.x * C);
-  const int c1 = min(n, c0 + C);
+  // Ordered pass over each thread's candidates, 64 at a time as bit masks (two 32-bit halves)
+  // of the keys above thr and equal to it.  A run of at most 64 (always, with the keys cached)
+  // keeps its masks for the write.
   auto masks = [&](int i0, uint32_t (&m)[4]) {  // gt lo, gt hi, eq lo, eq hi
     m[0] = m[1] = m[2] = m[3] = 0u;
     const int i1 = min(c1, i0 + 64), mid = min(i1, i0 + 32);

@@ -635,9 +635,12 @@ def _q8_row(pkv, W, dev, stream, args, hbm):
         pkv.paged_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
                                    c["scale"], out=out, workspace=ws, stream=stream)
 
-    def q8():
+    def q8(ready=False):
         pkv.paged_decode_attention_q8(c["q"], kq, vq, ks, vs, c["block_tables"], c["context_lens"], c["scale"],
-                                      out=out, workspace=ws, stream=stream)
+                                      out=out, workspace=ws, inputs_ready=ready, stream=stream)
+
+    def q8_ready():  # consecutive calls declaring their inputs final (as the headline's steps do)
+        q8(True)
     stride = c["max_blocks_per_seq"] * 16
     acc = torch.zeros((wl.batch, wl.num_kv_heads, stride), dtype=torch.float32, device=dev)
     lse = torch.empty((wl.batch, wl.num_q_heads), dtype=torch.float32, device=dev)
@@ -656,7 +659,8 @@ def _q8_row(pkv, W, dev, stream, args, hbm):
         q8()
     steps = max(5, args.steps // 4)
     ms_plain = _time(plain, args.warmup, steps, dev, stream)
-    ms_q8 = _time(q8, args.warmup, steps, dev, stream)
+    ms_q8_plain = _time(q8, args.warmup, steps, dev, stream)
+    ms_q8 = _time(q8_ready, args.warmup, steps, dev, stream)
     ms_q8_scored = _time(q8_scored, args.warmup, steps, dev, stream)
     ms_q8_fused = _time(q8_fused, args.warmup, steps, dev, stream)
     ms_q8_two = _time(q8_two_calls, args.warmup, steps, dev, stream)
@@ -666,11 +670,15 @@ def _q8_row(pkv, W, dev, stream, args, hbm):
     nbytes = (tokens * wl.num_kv_heads * (wl.head_dim + 4) * 2 + 2 * wl.batch * wl.num_q_heads * wl.head_dim * 2
               + blocks * 4 + wl.batch * 4)  # codes + row scales of K and V, q, out, tables, lengths
     del c, kq, vq, ks, vs, ws, out, acc, logits
-    return {"ms": round(ms_q8, 4), "ms_bf16": round(ms_plain, 4), "speedup": round(ms_plain / ms_q8, 3),
-            "ms_with_scores": round(ms_q8_scored, 4), "scores_overhead": round(ms_q8_scored / ms_q8 - 1.0, 4),
+    return {"ms": round(ms_q8, 4), "ms_without_inputs_ready": round(ms_q8_plain, 4),
+            "ms_bf16": round(ms_plain, 4), "speedup": round(ms_plain / ms_q8_plain, 3),
+            "ms_with_scores": round(ms_q8_scored, 4), "scores_overhead": round(ms_q8_scored / ms_q8_plain - 1.0, 4),
             "ms_append_fused": round(ms_q8_fused, 4), "ms_append_then_decode": round(ms_q8_two, 4),
             "tokens_per_s": round(wl.batch / (ms_q8 * 1e-3), 1), "bytes": nbytes,
             "gbs": round(nbytes / (ms_q8 * 1e-3) / 1e9, 1), "frac": round(nbytes / (ms_q8 * 1e-3) / 1e9 / hbm, 4),
+            "frac_without_inputs_ready": round(nbytes / (ms_q8_plain * 1e-3) / 1e9 / hbm, 4),
+            "launch": "back-to-back calls declaring their inputs ready (ms_without_inputs_ready: the same calls "
+                      "without; ms_bf16, ms_with_scores and the append rows are undeclared calls)",
             "l2": "0.29 GB of INT8 K/V + scales per call (> L2)"}
 
 

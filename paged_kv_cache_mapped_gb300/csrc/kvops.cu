@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
 // ---------------------------------------------------------------------------- top-k select
 
 #ifndef PKV_SEL_THREADS
-#define PKV_SEL_THREADS 1024
+#define PKV_SEL_THREADS 512  // one sparse layer: 7.98 us against 8.19 us at 1024 threads (256 were slower)
 #endif
 constexpr int kSelThreads = PKV_SEL_THREADS;
 constexpr int kSelWarps = kSelThreads / 32;

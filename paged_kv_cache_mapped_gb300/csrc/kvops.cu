@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(
     atomicAdd(&hist[key >> 20], 1);
   };
   if ((reinterpret_cast<uintptr_t>(cand) & 15u) == 0) {
-    // 16-byte loads: thread t takes candidates 4 (t + 1024 u) .. + 3, kSelBatch / 4 loads in flight
+    // 16-byte loads: thread t takes candidates 4 (t + kSelThreads u) .. + 3, kSelBatch / 4 loads in flight
     constexpr int V = kSelBatch / 4;
     const int n4 = n >> 2;
     for (int base = 0; base < n4; base += kSelThreads * V) {

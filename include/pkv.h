@@ -414,8 +414,8 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
 /*
  * pkv_sparse_decode_attention_q8 -- pkv_sparse_decode_attention over INT8 pools: the attended set
  * of (b, kv head g) is its kept list, and every K and V element is read as code * scale of its
- * row (the arithmetic of pkv_paged_decode_attention_q8).  Rows are gathered one by one (the
- * codes by bulk copy, the two row scales by 4-byte asynchronous copies).
+ * row (the arithmetic of pkv_paged_decode_attention_q8).  Rows are gathered through the kept
+ * lists (the codes as 16-byte asynchronous copies, the two row scales as 4-byte ones).
  *   k_codes, v_codes, k_scales, v_scales : as pkv_paged_decode_attention_q8.
  *   other arguments    : as pkv_sparse_decode_attention (same workspace, same errors).
  */

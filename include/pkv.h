@@ -93,6 +93,23 @@ extern "C" {
  */
 #define PKV_DECODE_INPUTS_READY 1
 
+/*
+ * Flags of pkv_kv_select_topk (its `flags` argument; 0 = none).
+ *
+ * PKV_SELECT_INPUTS_READY -- the caller declares that this call's score_accum and
+ *   context_lens are not written by the work that precedes the call on its stream and may
+ *   still be running when the call's kernel starts (with programmatic dependent launch, the
+ *   kernel enqueued just before the call and whatever that kernel lets run alongside it).
+ *   The selection then loads and counts its scores before that work has ended, and waits for
+ *   it only before it writes kept_out, kept_lens_out or error_word -- which the preceding
+ *   kernel may therefore still read or write.  This is the case of the selections of a
+ *   model's layers made one after another, each from its own layer's final scores ("How KV
+ *   Sparsity...", section "2. Attention modification": the scores of a layer and head are
+ *   accumulated first, the top-k taken after).  Results are identical with and without the
+ *   flag.  Unknown flag bits are refused with PKV_ERR_ARGUMENT.
+ */
+#define PKV_SELECT_INPUTS_READY 1
+
 /* Shape record shared by the calls. */
 typedef struct pkv_dims {
   int32_t batch;              /* B: sequences in this decode step */
@@ -381,10 +398,11 @@ int pkv_sparse_decode_attention(void* out, const void* q, const void* k_cache,
  * [n_sink, L_b - n_recent), ordered by score descending, equal scores by lower position
  * first (-0.0 equals +0.0); the first k_top candidates are kept.  Bit-exact.  NaN scores are
  * invalid (PKV_DEV_BAD_SCORE).  Supports score_stride <= 262144.
+ *   flags          : 0 or PKV_SELECT_INPUTS_READY (see there).
  */
 int pkv_kv_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* score_accum,
                        int32_t score_stride, const int32_t* context_lens, int32_t n_sink,
-                       int32_t n_recent, int32_t k_top, const pkv_dims* dims,
+                       int32_t n_recent, int32_t k_top, const pkv_dims* dims, uint32_t flags,
                        int32_t* error_word, void* stream);
 
 /*

@@ -30,6 +30,7 @@ __all__ = [
 
 BLOCK_SIZE = 16
 _INPUTS_READY = header_constants()["PKV_DECODE_INPUTS_READY"]
+_SELECT_READY = header_constants()["PKV_SELECT_INPUTS_READY"]
 
 
 def _ptr(t):
@@ -468,11 +469,13 @@ def sparse_decode_attention(q, k_cache, v_cache, block_tables, context_lens, kep
 
 
 def kv_select_topk(score_accum, context_lens, n_sink, n_recent, k_top, *, kept_out=None,
-                   kept_lens_out=None, error_word=None, stream=None):
+                   kept_lens_out=None, error_word=None, inputs_ready=False, stream=None):
     """Kept positions per (sequence, kv head): sinks, top-k by score, recent window.
 
     score_accum [B, Hkv, S] fp32 -> (kept [B, Hkv, n_sink+k_top+n_recent] int32 ascending,
     kept_lens [B] int32); entries past kept_lens[b] are left as they were (-1 when allocated here).
+    inputs_ready: PKV_SELECT_INPUTS_READY (the scores and lengths are final before the work
+    enqueued just before this call ends; results are identical).
     """
     _need(score_accum, "score_accum", torch.float32, 3)
     dev = score_accum.device
@@ -492,8 +495,8 @@ def kv_select_topk(score_accum, context_lens, n_sink, n_recent, k_top, *, kept_o
     dims = _dims(B, hkv, hkv, 128, 0, 0)
     check("pkv_kv_select_topk", load().pkv_kv_select_topk(
         _ptr(kept_out), _ptr(kept_lens_out), _ptr(score_accum), stride, _ptr(context_lens),
-        int(n_sink), int(n_recent), int(k_top), ctypes.byref(dims), _ptr(error_word),
-        _stream(stream, dev)))
+        int(n_sink), int(n_recent), int(k_top), ctypes.byref(dims), _SELECT_READY if inputs_ready else 0,
+        _ptr(error_word), _stream(stream, dev)))
     return kept_out, kept_lens_out
 
 

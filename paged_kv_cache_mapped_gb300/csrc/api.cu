@@ -582,9 +582,10 @@ int pkv_sparse_decode_attention_q8(void* out, const void* q, const void* k_codes
 
 int pkv_kv_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* score_accum,
                        int32_t score_stride, const int32_t* context_lens, int32_t n_sink,
-                       int32_t n_recent, int32_t k_top, const pkv_dims* dims, int32_t* error_word,
-                       void* stream) {
+                       int32_t n_recent, int32_t k_top, const pkv_dims* dims, uint32_t flags,
+                       int32_t* error_word, void* stream) {
   if (dims == nullptr) return PKV_ERR_NULL_POINTER;
+  if ((flags & ~(uint32_t)PKV_SELECT_INPUTS_READY) != 0) return PKV_ERR_ARGUMENT;
   if (dims->batch < 0 || dims->num_kv_heads <= 0) return PKV_ERR_DIMS;
   if (n_sink < 0 || n_recent < 0 || k_top < 0 || score_stride < 0 || score_stride > 262144)
     return PKV_ERR_ARGUMENT;
@@ -595,8 +596,8 @@ int pkv_kv_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* s
   if (!device_info(&st)) return st;
   return cuda_status(launch_select_topk(kept_out, kept_lens_out, score_accum, score_stride,
                                         context_lens, dims->batch, dims->num_kv_heads, n_sink,
-                                        n_recent, k_top, error_word,
-                                        static_cast<cudaStream_t>(stream)));
+                                        n_recent, k_top, (flags & PKV_SELECT_INPUTS_READY) ? 1 : 0,
+                                        error_word, static_cast<cudaStream_t>(stream)));
 }
 
 int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_block_tables,

@@ -210,7 +210,7 @@ cudaError_t launch_kv_rolling_admit_q8(void* k_cache, void* v_cache, float* k_sc
                                        int n_recent, int32_t* err, cudaStream_t stream);
 cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* scores,
                                int stride, const int32_t* lens, int B, int Hkv, int n_sink,
-                               int n_recent, int k_top, int32_t* err, cudaStream_t stream);
+                               int n_recent, int k_top, int early, int32_t* err, cudaStream_t stream);
 
 // Prefill-window score (prefill.cu).  The window's queries and the pool are read through
 // tensor maps; lse is [B, Hq, alpha] natural-log, scores [B, Hkv, score_stride].

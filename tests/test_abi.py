@@ -88,7 +88,10 @@ def test_host_validation_codes(lib):
                              ctypes.byref(_dims()), None, None) == c["PKV_ERR_NULL_POINTER"]
     # selection
     assert lib.pkv_kv_select_topk(P(0x1000), P(0x1000), P(0x1000), 100, P(0x1000), -1, 4, 4,
-                                  ctypes.byref(_dims()), None, None) == c["PKV_ERR_ARGUMENT"]
+                                  ctypes.byref(_dims()), 0, None, None) == c["PKV_ERR_ARGUMENT"]
+    # unknown flag bits are refused before anything else is looked at
+    assert lib.pkv_kv_select_topk(P(0x1000), P(0x1000), P(0x1000), 100, P(0x1000), 4, 4, 4,
+                                  ctypes.byref(_dims()), 2, None, None) == c["PKV_ERR_ARGUMENT"]
     # score-emitting decode
     def scores(lse=0x30000, acc=0x40000, logits=0x50000, stride=64, k_new=None, v_new=None):
         return lib.pkv_paged_decode_attention_scores(

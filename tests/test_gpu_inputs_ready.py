@@ -6,7 +6,9 @@ The flag changes when inputs are read, never what is computed: every flagged res
 against the fp64 oracle and, bit for bit, against the same call without the flag.  The calls run
 back to back on one stream with no synchronisation between them -- the case the flag exists for:
 consecutive layers of one decode step, each over its own pools, where a layer's split kernel starts
-while the previous layer's kernels finish -- eagerly and captured in a CUDA graph."""
+while the previous layer's kernels finish -- eagerly and captured in a CUDA graph.  The last tests
+do the same for kv_select_topk with PKV_SELECT_INPUTS_READY (the scores and lengths final, so the
+selection loads and counts them before the preceding work ends)."""
 import numpy as np
 import pytest
 import torch
@@ -329,3 +331,73 @@ def test_int8_scores_and_sparse_forms_flagged_equal_plain():
                                    c["block_tables"].cpu().numpy(), c["context_lens"].cpu().numpy(),
                                    kept.cpu().numpy(), klen.cpu().numpy(), c["scale"], rows=rows)
         assert_attn_close(x.view(-1, d)[torch.tensor(rows, device=DEV)], ref, f"sparse layer {i} (flagged)")
+
+
+# ---------------------------------------------------------------- kv_select_topk with the flag
+
+def test_select_layers_back_to_back_against_oracle():
+    """PKV_SELECT_INPUTS_READY: the selections of several layers, each from its own final scores
+    (Exp(1), ties, ragged lengths, short lists), run back to back on one stream with no
+    synchronisation, writing into one shared pair of output buffers after each layer's copy;
+    every layer's kept lists equal the oracle's and the unflagged call's, bit for bit."""
+    g = torch.Generator().manual_seed(71)
+    B, hkv, S = 5, 3, 6000
+    lens = torch.tensor([6000, 5000, 40, 0, 3333], dtype=torch.int32)
+    n_sink, n_recent, k_top = 3, 64, 300
+    layers = [torch.empty((B, hkv, S)).exponential_(generator=g) for _ in range(3)]
+    layers.append(torch.round(torch.empty((B, hkv, S)).exponential_(generator=g) * 4) / 4)  # ties
+    dl = lens.to(DEV)
+    kmax = n_sink + k_top + n_recent
+    kept = torch.empty((B, hkv, kmax), dtype=torch.int32, device=DEV)
+    kl = torch.empty(B, dtype=torch.int32, device=DEV)
+    err = pkv.new_error_word(DEV)
+    got = []
+    for sc in layers:
+        pkv.kv_select_topk(sc.to(DEV), dl, n_sink, n_recent, k_top, kept_out=kept, kept_lens_out=kl,
+                           error_word=err, inputs_ready=True)
+        got.append((kept.clone(), kl.clone()))  # the copies queue behind the flagged call
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    for sc, (k, n) in zip(layers, got):
+        okept, okl = oracle.select_topk(sc.numpy(), lens.numpy(), n_sink, n_recent, k_top)
+        assert np.array_equal(n.cpu().numpy(), okl)
+        kc = k.cpu().numpy()
+        for b in range(B):
+            assert np.array_equal(kc[b, :, :okl[b]], okept[b, :, :okl[b]])
+        pk, pl = pkv.kv_select_topk(sc.to(DEV), dl, n_sink, n_recent, k_top)
+        torch.cuda.synchronize()
+        assert torch.equal(pl, n)
+        for b in range(B):
+            assert torch.equal(pk[b, :, :int(okl[b])], k[b, :, :int(okl[b])])
+
+
+def test_select_flagged_in_graph_and_errors_after_the_wait():
+    """Flagged selections captured in a CUDA graph equal the eager unflagged ones; a length out of
+    range found before the wait is recorded once the call may write (PKV_DEV_BAD_CONTEXT_LEN)."""
+    g = torch.Generator().manual_seed(72)
+    B, hkv, S = 4, 2, 3000
+    lens = torch.tensor([3000, 2999, 700, 1], dtype=torch.int32, device=DEV)
+    scores = [torch.empty((B, hkv, S)).exponential_(generator=g).to(DEV) for _ in range(4)]
+    outs = [(torch.empty((B, hkv, 4 + 50 + 200), dtype=torch.int32, device=DEV),
+             torch.empty(B, dtype=torch.int32, device=DEV)) for _ in scores]
+    s = torch.cuda.Stream(DEV)
+    with torch.cuda.stream(s):
+        pkv.kv_select_topk(scores[0], lens, 4, 200, 50, stream=s)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            for sc, (k, n) in zip(scores, outs):
+                pkv.kv_select_topk(sc, lens, 4, 200, 50, kept_out=k, kept_lens_out=n, inputs_ready=True, stream=s)
+        gr.replay()
+        torch.cuda.synchronize()
+    for sc, (k, n) in zip(scores, outs):
+        pk, pl = pkv.kv_select_topk(sc, lens, 4, 200, 50)
+        torch.cuda.synchronize()
+        assert torch.equal(pl, n)
+        for b in range(B):
+            assert torch.equal(pk[b, :, :int(pl[b])], k[b, :, :int(pl[b])])
+    err = pkv.new_error_word(DEV)
+    bad = torch.tensor([3000, S + 1, 700, 1], dtype=torch.int32, device=DEV)
+    pkv.kv_select_topk(scores[1], bad, 4, 200, 50, error_word=err, inputs_ready=True)
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == pkv.header_constants()["PKV_DEV_BAD_CONTEXT_LEN"]

@@ -401,3 +401,29 @@ def test_select_flagged_in_graph_and_errors_after_the_wait():
     pkv.kv_select_topk(scores[1], bad, 4, 200, 50, error_word=err, inputs_ready=True)
     torch.cuda.synchronize()
     assert pkv.read_error(err) == pkv.header_constants()["PKV_DEV_BAD_CONTEXT_LEN"]
+
+
+@pytest.mark.parametrize("S", [16387, 50003])
+def test_select_flagged_long_and_odd_rows(S):
+    """Flagged selections over rows that fill the key cache (a row length that is not a multiple
+    of 4: the cache rounds up and the loads are unaligned) and rows longer than the cache (the
+    general path reads the scores again), each against the oracle and the unflagged call."""
+    g = torch.Generator().manual_seed(73 + S)
+    B, hkv = 3, 2
+    lens = torch.tensor([S, S - 5, 9000], dtype=torch.int32)
+    n_sink, n_recent, k_top = 4, 128, 700
+    layers = [torch.empty((B, hkv, S)).exponential_(generator=g) for _ in range(2)]
+    err = pkv.new_error_word(DEV)
+    got = [pkv.kv_select_topk(sc.to(DEV), lens.to(DEV), n_sink, n_recent, k_top, error_word=err, inputs_ready=True)
+           for sc in layers]
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    for sc, (k, n) in zip(layers, got):
+        okept, okl = oracle.select_topk(sc.numpy(), lens.numpy(), n_sink, n_recent, k_top)
+        assert np.array_equal(n.cpu().numpy(), okl)
+        pk, _ = pkv.kv_select_topk(sc.to(DEV), lens.to(DEV), n_sink, n_recent, k_top)
+        torch.cuda.synchronize()
+        kc, pc = k.cpu().numpy(), pk.cpu().numpy()
+        for b in range(B):
+            assert np.array_equal(kc[b, :, :okl[b]], okept[b, :, :okl[b]])
+            assert np.array_equal(pc[b, :, :okl[b]], kc[b, :, :okl[b]])

@@ -110,6 +110,27 @@ extern "C" {
  */
 #define PKV_SELECT_INPUTS_READY 1
 
+/*
+ * Flags of pkv_kv_compact and pkv_kv_compact_q8 (their `flags` argument; 0 = none).
+ *
+ * PKV_COMPACT_INPUTS_READY -- the caller declares that this call's source pools (for INT8 also
+ *   their scales), src_block_tables, context_lens, kept_index_lists, kept_lens and
+ *   dst_block_tables are not written by the work that precedes the call on its stream and may
+ *   still be running when the call's kernel starts (with programmatic dependent launch, the
+ *   kernel enqueued just before the call and whatever that kernel lets run alongside it).  The
+ *   compaction then reads all of them, the kept rows included, before that work has ended, and
+ *   waits for it only before it writes the destination pools or error_word -- which the
+ *   preceding kernel may therefore still read or write.  This is the case of the compactions of
+ *   a model's sparse layers made one after another, each from its own pool through kept lists
+ *   that are already final ("How KV Sparsity...", section "Key technique 1": every layer gets its
+ *   own compact block table).  The first compaction after the selections that wrote the kept
+ *   lists is made without the flag: a flagged selection lets the selections before it run
+ *   alongside it, so the lists may still be in flight when it is the preceding work.  Results
+ *   are identical with and without the flag.  Unknown flag bits are refused with
+ *   PKV_ERR_ARGUMENT.
+ */
+#define PKV_COMPACT_INPUTS_READY 1
+
 /* Shape record shared by the calls. */
 typedef struct pkv_dims {
   int32_t batch;              /* B: sequences in this decode step */
@@ -419,6 +440,7 @@ int pkv_kv_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* s
  *   kept_index_lists, kept_lens, max_kept : as pkv_sparse_decode_attention; an entry outside
  *                              [0, L_b) or not above the one before it is reported
  *                              (PKV_DEV_BAD_KEPT_INDEX) and its compact slot left untouched.
+ *   flags                    : 0 or PKV_COMPACT_INPUTS_READY (see there).
  * Bit-exact.
  */
 int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_block_tables,
@@ -426,8 +448,8 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
                    const void* src_k_cache, const void* src_v_cache,
                    const int32_t* src_block_tables, const int32_t* context_lens,
                    const int32_t* kept_index_lists, const int32_t* kept_lens,
-                   int32_t max_kept, const pkv_dims* src_dims, int32_t* error_word,
-                   void* stream);
+                   int32_t max_kept, const pkv_dims* src_dims, uint32_t flags,
+                   int32_t* error_word, void* stream);
 
 /*
  * pkv_sparse_decode_attention_q8 -- pkv_sparse_decode_attention over INT8 pools: the attended set
@@ -456,7 +478,7 @@ int pkv_kv_compact_q8(void* dst_k_codes, void* dst_v_codes, float* dst_k_scales,
                       const void* src_k_codes, const void* src_v_codes, const float* src_k_scales,
                       const float* src_v_scales, const int32_t* src_block_tables, const int32_t* context_lens,
                       const int32_t* kept_index_lists, const int32_t* kept_lens, int32_t max_kept,
-                      const pkv_dims* src_dims, int32_t* error_word, void* stream);
+                      const pkv_dims* src_dims, uint32_t flags, int32_t* error_word, void* stream);
 
 /*
  * pkv_kv_rolling_admit -- admit one decode step's token into each sequence's sparse-layer cache

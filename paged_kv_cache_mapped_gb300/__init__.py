@@ -31,6 +31,7 @@ __all__ = [
 BLOCK_SIZE = 16
 _INPUTS_READY = header_constants()["PKV_DECODE_INPUTS_READY"]
 _SELECT_READY = header_constants()["PKV_SELECT_INPUTS_READY"]
+_COMPACT_READY = header_constants()["PKV_COMPACT_INPUTS_READY"]
 
 
 def _ptr(t):
@@ -502,8 +503,12 @@ def kv_select_topk(score_accum, context_lens, n_sink, n_recent, k_top, *, kept_o
 
 def kv_compact(dst_k_cache, dst_v_cache, dst_block_tables, src_k_cache, src_v_cache,
                src_block_tables, context_lens, kept_index_lists, kept_lens, *, error_word=None,
-               stream=None):
-    """Copy each (sequence, kv head)'s kept tokens into consecutive slots of the dst pool."""
+               inputs_ready=False, stream=None):
+    """Copy each (sequence, kv head)'s kept tokens into consecutive slots of the dst pool.
+
+    inputs_ready=True sets PKV_COMPACT_INPUTS_READY: the caller declares the source pools and
+    tables, the lengths, the kept lists and dst_block_tables final before the preceding work on
+    the stream (not written by it), so the call reads the kept rows before that work ends."""
     snb, hkv, d = _pool_dims(src_k_cache, src_v_cache)
     dnb, dhkv, dd = _pool_dims(dst_k_cache, dst_v_cache)
     if (dhkv, dd) != (hkv, d):
@@ -522,13 +527,14 @@ def kv_compact(dst_k_cache, dst_v_cache, dst_block_tables, src_k_cache, src_v_ca
         _ptr(dst_k_cache), _ptr(dst_v_cache), _ptr(dst_block_tables), dnb, dst_block_tables.shape[1],
         _ptr(src_k_cache), _ptr(src_v_cache), _ptr(src_block_tables), _ptr(context_lens),
         _ptr(kept_index_lists), _ptr(kept_lens), kept_index_lists.shape[2], ctypes.byref(dims),
-        _ptr(error_word), _stream(stream, dev)))
+        _COMPACT_READY if inputs_ready else 0, _ptr(error_word), _stream(stream, dev)))
 
 
 def kv_compact_q8(dst_k_codes, dst_v_codes, dst_k_scales, dst_v_scales, dst_block_tables, src_k_codes,
                   src_v_codes, src_k_scales, src_v_scales, src_block_tables, context_lens, kept_index_lists,
-                  kept_lens, *, error_word=None, stream=None):
-    """kv_compact over INT8 pools: each kept row's codes and row scale move together."""
+                  kept_lens, *, error_word=None, inputs_ready=False, stream=None):
+    """kv_compact over INT8 pools: each kept row's codes and row scale move together
+    (inputs_ready as kv_compact)."""
     snb, hkv, d = _q8_pool_dims(src_k_codes, src_v_codes, src_k_scales, src_v_scales)
     dnb, dhkv, dd = _q8_pool_dims(dst_k_codes, dst_v_codes, dst_k_scales, dst_v_scales)
     if (dhkv, dd) != (hkv, d):
@@ -549,4 +555,5 @@ def kv_compact_q8(dst_k_codes, dst_v_codes, dst_k_scales, dst_v_scales, dst_bloc
         _ptr(dst_k_codes), _ptr(dst_v_codes), _ptr(dst_k_scales), _ptr(dst_v_scales), _ptr(dst_block_tables), dnb,
         dst_block_tables.shape[1], _ptr(src_k_codes), _ptr(src_v_codes), _ptr(src_k_scales), _ptr(src_v_scales),
         _ptr(src_block_tables), _ptr(context_lens), _ptr(kept_index_lists), _ptr(kept_lens),
-        kept_index_lists.shape[2], ctypes.byref(dims), _ptr(error_word), _stream(stream, dev)))
+        kept_index_lists.shape[2], ctypes.byref(dims), _COMPACT_READY if inputs_ready else 0, _ptr(error_word),
+        _stream(stream, dev)))

@@ -605,7 +605,8 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
                    const void* src_v_cache, const int32_t* src_block_tables,
                    const int32_t* context_lens, const int32_t* kept_index_lists,
                    const int32_t* kept_lens, int32_t max_kept, const pkv_dims* src_dims,
-                   int32_t* error_word, void* stream) {
+                   uint32_t flags, int32_t* error_word, void* stream) {
+  if ((flags & ~(uint32_t)PKV_COMPACT_INPUTS_READY) != 0) return PKV_ERR_ARGUMENT;
   int st = check_dims(src_dims, false);
   if (st != PKV_OK) return st;
   if (dst_num_blocks < 0 || dst_max_blocks_per_seq < 0 || max_kept < 0) return PKV_ERR_DIMS;
@@ -622,7 +623,8 @@ int pkv_kv_compact(void* dst_k_cache, void* dst_v_cache, const int32_t* dst_bloc
                                        src_block_tables, context_lens, kept_index_lists, kept_lens,
                                        max_kept, src_dims->batch, src_dims->num_kv_heads,
                                        src_dims->head_dim, src_dims->num_blocks,
-                                       src_dims->max_blocks_per_seq, error_word,
+                                       src_dims->max_blocks_per_seq,
+                                       (flags & PKV_COMPACT_INPUTS_READY) ? 1 : 0, error_word,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -631,7 +633,8 @@ int pkv_kv_compact_q8(void* dst_k_codes, void* dst_v_codes, float* dst_k_scales,
                       const void* src_k_codes, const void* src_v_codes, const float* src_k_scales,
                       const float* src_v_scales, const int32_t* src_block_tables, const int32_t* context_lens,
                       const int32_t* kept_index_lists, const int32_t* kept_lens, int32_t max_kept,
-                      const pkv_dims* src_dims, int32_t* error_word, void* stream) {
+                      const pkv_dims* src_dims, uint32_t flags, int32_t* error_word, void* stream) {
+  if ((flags & ~(uint32_t)PKV_COMPACT_INPUTS_READY) != 0) return PKV_ERR_ARGUMENT;
   int st = check_dims(src_dims, false);
   if (st != PKV_OK) return st;
   if (dst_num_blocks < 0 || dst_max_blocks_per_seq < 0 || max_kept < 0) return PKV_ERR_DIMS;
@@ -648,7 +651,8 @@ int pkv_kv_compact_q8(void* dst_k_codes, void* dst_v_codes, float* dst_k_scales,
       dst_k_codes, dst_v_codes, dst_k_scales, dst_v_scales, dst_block_tables, dst_num_blocks, dst_max_blocks_per_seq,
       src_k_codes, src_v_codes, src_k_scales, src_v_scales, src_block_tables, context_lens, kept_index_lists,
       kept_lens, max_kept, src_dims->batch, src_dims->num_kv_heads, src_dims->head_dim, src_dims->num_blocks,
-      src_dims->max_blocks_per_seq, error_word, static_cast<cudaStream_t>(stream)));
+      src_dims->max_blocks_per_seq, (flags & PKV_COMPACT_INPUTS_READY) ? 1 : 0, error_word,
+      static_cast<cudaStream_t>(stream)));
 }
 
 int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tables,

@@ -190,7 +190,7 @@ cudaError_t launch_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, f
 cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, int dMB,
                               const void* sk, const void* sv, const int32_t* sbt,
                               const int32_t* lens, const int32_t* kept, const int32_t* kept_lens,
-                              int max_kept, int B, int Hkv, int D, int sNB, int sMB,
+                              int max_kept, int B, int Hkv, int D, int sNB, int sMB, int early,
                               int32_t* err, cudaStream_t stream);
 cudaError_t launch_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* bt, int NB, int MB,
                                     int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
@@ -202,7 +202,7 @@ cudaError_t launch_kv_compact_q8(void* dk, void* dv, float* dks, float* dvs, con
                                  int dMB, const void* sk, const void* sv, const float* sks, const float* svs,
                                  const int32_t* sbt, const int32_t* lens, const int32_t* kept,
                                  const int32_t* kept_lens, int max_kept, int B, int Hkv, int D, int sNB,
-                                 int sMB, int32_t* err, cudaStream_t stream);
+                                 int sMB, int early, int32_t* err, cudaStream_t stream);
 cudaError_t launch_kv_rolling_admit_q8(void* k_cache, void* v_cache, float* k_scales, float* v_scales,
                                        const int32_t* bt, int NB, int MB, int32_t* slot_pos, float* slot_score,
                                        int32_t* kept_lens, const int32_t* lens, const void* k_new,

@@ -145,12 +145,23 @@ __global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ 
 // row scales move with them when SCALES.  One warp per (b, g, compact_rows(RB) consecutive
 // compact positions inside one destination block): the lanes resolve the group's positions to source
 // rows (kept index, then source block id: one chain of dependent loads for the group instead
-// of one per row), then every lane loads its 16-byte chunks of the group's K and V rows before
-// any is stored, and the stores fill consecutive rows of the destination block.
+// of one per row), then every lane loads its 16-byte chunks of the group's K and V rows (and
+// the row scales) before any is stored, and the stores fill consecutive rows of the destination
+// block.  EARLY (the caller declared every input final before the preceding work): the warp
+// reads all of it before waiting for that work, and waits on every path before its first write
+// -- the error word included -- so that the call also ends after the work it follows.
 // positions per warp (a divisor of 16): 4 for 256-byte rows, 8 for shorter ones (measured)
 __host__ __device__ constexpr int compact_rows(int rb) { return rb >= 256 ? 4 : 8; }
 
-template <int RB, bool SCALES>
+// the last step of a compaction warp: wait for the preceding work if it was not waited for at the
+// start, then record this lane's error (0: none)
+template <bool EARLY>
+__device__ __forceinline__ void compact_finish(int32_t* err, int code) {
+  if constexpr (EARLY) grid_dependency_wait();
+  if (code != 0) record_error(err, code);
+}
+
+template <int RB, bool SCALES, bool EARLY>
 __global__ void __launch_bounds__(256) kv_compact_kernel(
     unsigned char* __restrict__ dk, unsigned char* __restrict__ dv, float* __restrict__ dks,
     float* __restrict__ dvs, const int32_t* __restrict__ dbt, int dNB, int dMB,
@@ -165,24 +176,31 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
   static_assert(16 % NR == 0 && NR * CPR >= 32, "a group fills the warp's lanes");
   const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  grid_dependency_wait();
+  if constexpr (!EARLY) grid_dependency_wait();
   grid_launch_dependents();
   const int groups = (max_kept + NR - 1) / NR;
-  if (item >= (int64_t)B * Hkv * groups) return;
+  if (item >= (int64_t)B * Hkv * groups) {
+    compact_finish<EARLY>(err, 0);
+    return;
+  }
   const int jb = (int)(item % groups);
   const int64_t bg = item / groups;
   const int b = (int)(bg / Hkv);
   const int g = (int)(bg - (int64_t)b * Hkv);
   const int n = __ldg(kept_lens + b);
   const int j0 = jb * NR;
-  if (j0 >= n) return;
+  if (j0 >= n) {
+    compact_finish<EARLY>(err, 0);
+    return;
+  }
   if (n > max_kept || n > dMB * 16) {
-    if (lane == 0) record_error(err, PKV_DEV_BAD_KEPT_INDEX);
+    compact_finish<EARLY>(err, lane == 0 ? PKV_DEV_BAD_KEPT_INDEX : 0);
     return;
   }
   const int dst_blk = __ldg(dbt + (size_t)b * dMB + (j0 >> 4));
   const int r = lane % NR;  // this lane's row of the group (lanes r, r + NR, ... share it)
   long long src_row = -1;
+  int code = 0;  // this lane's error
   // the kept entry and the one before it: a list must rise strictly (each kept token has one
   // compact slot), so an entry not above its predecessor is reported and not copied
   const bool has = j0 + r < n;
@@ -193,17 +211,18 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
   if (has) {
     const int L = __ldg(lens + b);
     if (t < 0 || t >= L || (t >> 4) >= sMB || (j0 + r > 0 && t <= tp)) {
-      if (lane < NR) record_error(err, PKV_DEV_BAD_KEPT_INDEX);
+      if (lane < NR) code = PKV_DEV_BAD_KEPT_INDEX;
     } else {
       const int sb = __ldg(sbt + (size_t)b * sMB + (t >> 4));
       if (sb < 0 || sb >= sNB) {
-        if (lane < NR) record_error(err, PKV_DEV_BAD_BLOCK_ID);
+        if (lane < NR) code = PKV_DEV_BAD_BLOCK_ID;
       } else {
         src_row = ((long long)sb * Hkv + g) * 16 + (t & 15);
       }
     }
   }
   if (dst_blk < 0 || dst_blk >= dNB) {
+    compact_finish<EARLY>(err, code);
     if (lane == 0) record_error(err, PKV_DEV_BAD_BLOCK_ID);
     return;
   }
@@ -220,6 +239,11 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
       vbuf[i] = __ldg(reinterpret_cast<const uint4*>(sv + sr * RB) + c % CPR);
     }
   }
+  float scl = 0.f;  // lanes 0..NR-1: the K row scale of row r; NR..2NR-1: the V row scale
+  if constexpr (SCALES) {
+    if (lane < 2 * NR && src_row >= 0) scl = lane < NR ? __ldg(sks + src_row) : __ldg(svs + src_row);
+  }
+  compact_finish<EARLY>(err, code);
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int c = i * 32 + lane;
@@ -230,8 +254,8 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
   }
   if constexpr (SCALES) {
     if (lane < 2 * NR && src_row >= 0) {
-      if (lane < NR) dks[dst0 + r] = __ldg(sks + src_row);
-      else dvs[dst0 + r] = __ldg(svs + src_row);
+      if (lane < NR) dks[dst0 + r] = scl;
+      else dvs[dst0 + r] = scl;
     }
   }
 }
@@ -932,17 +956,17 @@ cudaError_t launch_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, f
 cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, int dMB,
                               const void* sk, const void* sv, const int32_t* sbt,
                               const int32_t* lens, const int32_t* kept, const int32_t* kept_lens,
-                              int max_kept, int B, int Hkv, int D, int sNB, int sMB,
+                              int max_kept, int B, int Hkv, int D, int sNB, int sMB, int early,
                               int32_t* err, cudaStream_t stream) {
   return launch_kv_compact_q8(dk, dv, nullptr, nullptr, dbt, dNB, dMB, sk, sv, nullptr, nullptr, sbt, lens,
-                              kept, kept_lens, max_kept, B, Hkv, D, sNB, sMB, err, stream);
+                              kept, kept_lens, max_kept, B, Hkv, D, sNB, sMB, early, err, stream);
 }
 
 cudaError_t launch_kv_compact_q8(void* dk, void* dv, float* dks, float* dvs, const int32_t* dbt, int dNB,
                                  int dMB, const void* sk, const void* sv, const float* sks, const float* svs,
                                  const int32_t* sbt, const int32_t* lens, const int32_t* kept,
                                  const int32_t* kept_lens, int max_kept, int B, int Hkv, int D, int sNB,
-                                 int sMB, int32_t* err, cudaStream_t stream) {
+                                 int sMB, int early, int32_t* err, cudaStream_t stream) {
   const int nr = compact_rows(dks != nullptr ? D : 2 * D);
   const int64_t warps = (int64_t)B * Hkv * ((max_kept + nr - 1) / nr);
   if (warps == 0) return cudaSuccess;
@@ -954,9 +978,16 @@ cudaError_t launch_kv_compact_q8(void* dk, void* dv, float* dks, float* dvs, con
   void* args[] = {&a, &c, &dks, &dvs, &dbt, &dNB, &dMB, &s1, &s2, &sks, &svs, &sbt, &lens, &kept, &kept_lens,
                   &max_kept, &B, &Hkv, &sNB, &sMB, &err};
   const bool q8 = dks != nullptr;
-  const void* fn = q8 ? (D == 128 ? (const void*)kv_compact_kernel<128, true> : (const void*)kv_compact_kernel<64, true>)
-                      : (D == 128 ? (const void*)kv_compact_kernel<256, false>
-                                  : (const void*)kv_compact_kernel<128, false>);
+  const void* fn;
+  if (early)
+    fn = q8 ? (D == 128 ? (const void*)kv_compact_kernel<128, true, true> : (const void*)kv_compact_kernel<64, true, true>)
+            : (D == 128 ? (const void*)kv_compact_kernel<256, false, true>
+                        : (const void*)kv_compact_kernel<128, false, true>);
+  else
+    fn = q8 ? (D == 128 ? (const void*)kv_compact_kernel<128, true, false>
+                        : (const void*)kv_compact_kernel<64, true, false>)
+            : (D == 128 ? (const void*)kv_compact_kernel<256, false, false>
+                        : (const void*)kv_compact_kernel<128, false, false>);
   return launch_pdl(fn, dim3(grid), dim3(256), 0, stream, args);
 }
 

@@ -160,14 +160,19 @@ def test_host_validation_codes(lib):
     assert q8_sparse(vs=0x40008) == c["PKV_ERR_ALIGNMENT"]
     assert q8_sparse() == c["PKV_ERR_WORKSPACE"]                      # 16-byte workspace
 
-    def q8_compact(dks=0x30000, max_kept=8):
+    def q8_compact(dks=0x30000, max_kept=8, flags=0):
         return lib.pkv_kv_compact_q8(P(0x10000), P(0x10000), P(dks), P(0x40000), P(0x50000), 8, 4, P(0x10000),
                                      P(0x10000), P(0x30000), P(0x40000), P(0x50000), P(0x60000), P(0x70000),
-                                     P(0x80000), max_kept, ctypes.byref(_dims()), None, None)
+                                     P(0x80000), max_kept, ctypes.byref(_dims()), flags, None, None)
     assert q8_compact(dks=0) == c["PKV_ERR_NULL_POINTER"]
     assert q8_compact(dks=0x30004) == c["PKV_ERR_ALIGNMENT"]
     assert q8_compact(max_kept=-1) == c["PKV_ERR_DIMS"]
     assert q8_compact(max_kept=0) == c["PKV_OK"]
+    assert q8_compact(max_kept=0, flags=c["PKV_COMPACT_INPUTS_READY"]) == c["PKV_OK"]
+    assert q8_compact(flags=2) == c["PKV_ERR_ARGUMENT"]                # unknown flag bit
+    assert lib.pkv_kv_compact(P(0x10000), P(0x10000), P(0x50000), 8, 4, P(0x10000), P(0x10000), P(0x50000),
+                              P(0x60000), P(0x70000), P(0x80000), 8, ctypes.byref(_dims()), 4, None,
+                              None) == c["PKV_ERR_ARGUMENT"]
 
     def q8_admit(cap=60, n_sink=4, n_recent=32, ks=0x30000):
         return lib.pkv_kv_rolling_admit_q8(P(0x10000), P(0x10000), P(ks), P(0x40000), P(0x10000), P(0x30000),

@@ -8,7 +8,9 @@ back to back on one stream with no synchronisation between them -- the case the 
 consecutive layers of one decode step, each over its own pools, where a layer's split kernel starts
 while the previous layer's kernels finish -- eagerly and captured in a CUDA graph.  The last tests
 do the same for kv_select_topk with PKV_SELECT_INPUTS_READY (the scores and lengths final, so the
-selection loads and counts them before the preceding work ends)."""
+selection loads and counts them before the preceding work ends) and for kv_compact / kv_compact_q8
+with PKV_COMPACT_INPUTS_READY (pools, tables and kept lists final, so the compaction reads the kept
+rows before the preceding work ends)."""
 import numpy as np
 import pytest
 import torch
@@ -427,3 +429,147 @@ def test_select_flagged_long_and_odd_rows(S):
         for b in range(B):
             assert np.array_equal(kc[b, :, :okl[b]], okept[b, :, :okl[b]])
             assert np.array_equal(pc[b, :, :okl[b]], kc[b, :, :okl[b]])
+
+
+def _compact_layer(B, hkv, d, lens, max_kept, seed, q8):
+    """One layer's source pool (bf16, or INT8 codes with Exp row scales), its shuffled block table
+    and strictly rising kept lists (min(L_b, max_kept) tokens, one list a ragged 17)."""
+    rng = np.random.default_rng(seed)
+    lens = np.array(lens, dtype=np.int32)
+    smb = int((lens.max() + 15) // 16)
+    snb = B * smb + 5
+    sbt = rng.permutation(snb)[: B * smb].reshape(B, smb).astype(np.int32)
+    kl = np.minimum(lens, max_kept).astype(np.int32)
+    kl[1] = min(17, lens[1])
+    kept = np.full((B, hkv, max_kept), -1, dtype=np.int32)
+    for b in range(B):
+        for g in range(hkv):
+            if kl[b]:
+                kept[b, g, :kl[b]] = np.sort(rng.choice(lens[b], size=kl[b], replace=False))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    c = {"sbt": t(sbt), "lens": t(lens), "kept": t(kept), "kl": t(kl)}
+    if q8:
+        for name in ("sk", "sv"):
+            c[name] = t(rng.integers(-127, 128, size=(snb, hkv, 16, d)).astype(np.int8))
+            c[name + "s"] = t(rng.exponential(size=(snb, hkv, 16)).astype(np.float32))
+    else:
+        for name in ("sk", "sv"):
+            c[name] = t(rng.integers(0, 1 << 16, size=(snb, hkv, 16, d)).astype(np.uint16)).view(torch.bfloat16)
+    return c
+
+
+def _compact_dst(B, hkv, d, max_kept, seed, q8):
+    """A destination pool filled with noise (slots the copy does not address keep it) and its table."""
+    rng = np.random.default_rng(seed)
+    dmb = (max_kept + 15) // 16
+    dnb = B * dmb + 3
+    dbt = torch.from_numpy(rng.permutation(dnb)[: B * dmb].reshape(B, dmb).astype(np.int32)).to(DEV)
+    if q8:
+        pools = [torch.from_numpy(rng.integers(-127, 128, size=(dnb, hkv, 16, d)).astype(np.int8)).to(DEV)
+                 for _ in range(2)]
+        pools += [torch.from_numpy(rng.exponential(size=(dnb, hkv, 16)).astype(np.float32)).to(DEV) for _ in range(2)]
+    else:
+        pools = [torch.from_numpy(rng.integers(0, 1 << 16, size=(dnb, hkv, 16, d)).astype(np.uint16)).to(DEV)
+                 .view(torch.bfloat16) for _ in range(2)]
+    return pools, dbt
+
+
+def _compact_call(c, pools, dbt, q8, ready, err=None, stream=None):
+    if q8:
+        pkv.kv_compact_q8(pools[0], pools[1], pools[2], pools[3], dbt, c["sk"], c["sv"], c["sks"], c["svs"],
+                          c["sbt"], c["lens"], c["kept"], c["kl"], error_word=err, inputs_ready=ready, stream=stream)
+    else:
+        pkv.kv_compact(pools[0], pools[1], dbt, c["sk"], c["sv"], c["sbt"], c["lens"], c["kept"], c["kl"],
+                       error_word=err, inputs_ready=ready, stream=stream)
+
+
+def _np(t):
+    return (t.view(torch.uint16) if t.dtype == torch.bfloat16 else t).cpu().numpy()
+
+
+def _compact_oracle(c, pools, dbt, q8):
+    """The destination pools after one compaction, by the oracle (numpy copies of `pools`)."""
+    n = lambda k: _np(c[k])
+    if q8:
+        return list(oracle.compact_q8(*pools, _np(dbt), n("sk"), n("sv"), n("sks"), n("svs"), n("sbt"), n("lens"),
+                                      n("kept"), n("kl")))
+    return list(oracle.compact(*pools, _np(dbt), n("sk"), n("sv"), n("sbt"), n("lens"), n("kept"), n("kl")))
+
+
+@pytest.mark.parametrize("q8,d", [(False, 128), (False, 64), (True, 128), (True, 64)])
+def test_compact_layers_back_to_back_against_oracle(q8, d):
+    """PKV_COMPACT_INPUTS_READY: the compactions of several layers, each from its own pool through
+    final kept lists, run back to back into one shared destination pool with a copy of that pool
+    queued after each (the next flagged call may read before the copy ends and must write after
+    it); every copy equals the oracle's chain of compactions and the unflagged chain, bit for bit."""
+    B, hkv, max_kept = 4, 3, 300
+    layers = [_compact_layer(B, hkv, d, [900, 33, 0, 1500], max_kept, 80 + l, q8) for l in range(3)]
+    pools, dbt = _compact_dst(B, hkv, d, max_kept, 90, q8)
+    start = [p.clone() for p in pools]
+    err = pkv.new_error_word(DEV)
+    torch.cuda.synchronize()
+    snaps = []
+    for c in layers:
+        _compact_call(c, pools, dbt, q8, True, err)
+        snaps.append([p.clone() for p in pools])
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    want = [_np(p) for p in start]
+    for c, snap in zip(layers, snaps):
+        want = _compact_oracle(c, want, dbt, q8)
+        for w, g in zip(want, snap):
+            assert np.array_equal(_np(g), w)
+    plain = [p.clone() for p in start]
+    for c, snap in zip(layers, snaps):
+        _compact_call(c, plain, dbt, q8, False)
+        torch.cuda.synchronize()
+        for p, g in zip(plain, snap):
+            assert torch.equal(_np_t(p), _np_t(g))
+
+
+def _np_t(t):
+    return t.view(torch.uint16) if t.dtype == torch.bfloat16 else t
+
+
+@pytest.mark.parametrize("q8", [False, True])
+def test_compact_flagged_in_graph_and_errors_after_the_wait(q8):
+    """Flagged compactions of four layers into four pools, captured in a CUDA graph, equal the eager
+    unflagged ones; a kept entry past its context, a source block id and a destination block id
+    outside their pools, found before the wait, are recorded once the call may write."""
+    B, hkv, d, max_kept = 3, 2, 128, 200
+    layers = [_compact_layer(B, hkv, d, [700, 40, 2000], max_kept, 100 + l, q8) for l in range(4)]
+    dsts = [_compact_dst(B, hkv, d, max_kept, 110 + l, q8) for l in range(4)]
+    start = [[p.clone() for p in pools] for pools, _ in dsts]
+    s = torch.cuda.Stream(DEV)
+    with torch.cuda.stream(s):
+        _compact_call(layers[0], [p.clone() for p in start[0]], dsts[0][1], q8, False, stream=s)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            for c, (pools, dbt) in zip(layers, dsts):
+                _compact_call(c, pools, dbt, q8, True, stream=s)
+        gr.replay()
+        torch.cuda.synchronize()
+    for c, (pools, dbt), st in zip(layers, dsts, start):
+        _compact_call(c, st, dbt, q8, False)
+        torch.cuda.synchronize()
+        for p, g in zip(st, pools):
+            assert torch.equal(_np_t(p), _np_t(g))
+    C = pkv.header_constants()
+    for field, where, value, code in (("kept", (1, 1, 5), 40, "PKV_DEV_BAD_KEPT_INDEX"),
+                                      ("sbt", (2, int(layers[1]["kept"][2, 0, 0]) >> 4), 10 ** 6,
+                                       "PKV_DEV_BAD_BLOCK_ID"),  # the block of a kept token
+                                      ("dbt", (0, 2), 10 ** 6, "PKV_DEV_BAD_BLOCK_ID")):
+        c = dict(layers[1])
+        pools, dbt = dsts[1]
+        if field == "dbt":
+            dbt = dbt.clone()
+            dbt[where] = value
+        else:
+            c[field] = c[field].clone()
+            c[field][where] = value
+        err = pkv.new_error_word(DEV)
+        torch.cuda.synchronize()
+        _compact_call(c, pools, dbt, q8, True, err)
+        torch.cuda.synchronize()
+        assert pkv.read_error(err) == C[code], field

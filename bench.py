@@ -604,8 +604,8 @@ def _append_row(pkv, W, dev, stream, args):
     c = W.make_layer(wl, device=dev, device_rng=True)
     nb, hkv, _, d = c["k_cache"].shape
     g = torch.Generator(device=dev).manual_seed(43)
-    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
-    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
+    kq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.uint8)
+    vq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.uint8)
     ks = torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g) * 0.02
     vs = torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g) * 0.02
     ws = torch.zeros(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
@@ -655,8 +655,8 @@ def _q8_row(pkv, W, dev, stream, args, hbm):
     c = W.make_layer(wl, device=dev, device_rng=True)
     nb, hkv, _, d = c["k_cache"].shape
     g = torch.Generator(device=dev).manual_seed(41)
-    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
-    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
+    kq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.uint8)
+    vq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.uint8)
     ks = torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g) * 0.02
     vs = torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g) * 0.02
     ws = torch.zeros(pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
@@ -800,7 +800,7 @@ def _qwen_step(pkv, W, dev, stream, args, hbm):
     pools8 = []
     for c in layers:
         nb = c["num_blocks"]
-        codes = lambda: torch.randint(-127, 128, (nb, hkv, 16, d), generator=g8, device=dev, dtype=torch.int8)
+        codes = lambda: torch.randint(1, 256, (nb, hkv, 16, d), generator=g8, device=dev, dtype=torch.uint8)
         rs = lambda: torch.empty((nb, hkv, 16), device=dev).exponential_(generator=g8) * 0.02
         pools8.append((codes(), codes(), rs(), rs()))
 
@@ -875,7 +875,7 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
     gq8 = torch.Generator(device=dev).manual_seed(47)
 
     def q8_pools(nblocks):
-        codes = lambda: torch.randint(-127, 128, (nblocks, hkv, 16, d), generator=gq8, device=dev, dtype=torch.int8)
+        codes = lambda: torch.randint(1, 256, (nblocks, hkv, 16, d), generator=gq8, device=dev, dtype=torch.uint8)
         rs = lambda: torch.empty((nblocks, hkv, 16), device=dev).exponential_(generator=gq8) * 0.02
         return codes(), codes(), rs(), rs()
     full8 = [q8_pools(c["num_blocks"]) for c in full]
@@ -964,7 +964,7 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
         res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, comp[0], dbt, klens, ws, out))
     # the same layer over INT8 pools (random codes, row scales ~ Exp): compaction and rolling
     gq = torch.Generator(device=dev).manual_seed(43)
-    codes = lambda n: torch.randint(-127, 128, (n, hkv, 16, d), generator=gq, device=dev, dtype=torch.int8)
+    codes = lambda n: torch.randint(1, 256, (n, hkv, 16, d), generator=gq, device=dev, dtype=torch.uint8)
     rscales = lambda n: torch.empty((n, hkv, 16), device=dev).exponential_(generator=gq) * 0.02
     snb = src["k_cache"].shape[0]
     s8 = {"kq": codes(snb), "vq": codes(snb), "ks": rscales(snb), "vs": rscales(snb)}
@@ -1190,7 +1190,7 @@ def run_case(name: str, calls: int = 3):
 
     def q8_pools(nb, hkv, d, seed, scale_fn):
         g = torch.Generator(device=dev).manual_seed(seed)
-        codes = [torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.int8)
+        codes = [torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=dev, dtype=torch.uint8)
                  for _ in range(2)]
         return codes + [scale_fn(g, (nb, hkv, 16)) for _ in range(2)]
     exp_scales = lambda g, shape: torch.empty(shape, device=dev).exponential_(generator=g) * 0.02

@@ -237,12 +237,14 @@ int pkv_paged_decode_attention_append(void* out, const void* q, void* k_cache, v
  * quantization per (token, kv head) row: scale s = max|x| / 127 (fp32), codes
  * c = round_half_even(x / s) clamped to [-127, 127] (single-precision IEEE division and
  * rounding), value c * s.  A zero row has s = 0 and codes 0.
- * Code pools are [NB, Hkv, 16, d] int8 (the bf16 layout, one byte per element); scale pools
- * are [NB, Hkv, 16] fp32 (one scale per row: 4/d bytes per element more, 3.1 % at d = 128).
+ * Code pools are [NB, Hkv, 16, d] uint8 (the bf16 layout, one byte per element) holding each
+ * code c as the byte c + 128 (1..255 for the codes this rule makes; a byte b is read as the
+ * code b - 128); scale pools are [NB, Hkv, 16] fp32 (one scale per row: 4/d bytes per element
+ * more, 3.1 % at d = 128).
  *
  * pkv_kv_append_q8 -- pkv_kv_append into INT8 pools: each new K and V row is quantized into
  * its slot.
- *   k_codes, v_codes   : [NB, Hkv, 16, d] int8, updated in place.
+ *   k_codes, v_codes   : [NB, Hkv, 16, d] uint8, updated in place.
  *   k_scales, v_scales : [NB, Hkv, 16] fp32, updated in place.
  *   k, v, slot_mapping, num_tokens, dims : as pkv_kv_append.
  *   error_word         : optional; PKV_DEV_BAD_SLOT, or PKV_DEV_BAD_VALUE for a token whose K or
@@ -256,7 +258,7 @@ int pkv_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_sca
 /*
  * pkv_paged_decode_attention_q8 -- pkv_paged_decode_attention over INT8 pools: every K and V
  * element is read as code * scale of its row.  Reads half the K/V bytes (plus the scales).
- *   k_codes, v_codes   : [NB, Hkv, 16, d] int8.
+ *   k_codes, v_codes   : [NB, Hkv, 16, d] uint8.
  *   k_scales, v_scales : [NB, Hkv, 16] fp32, 16-byte aligned; rows of tokens outside the
  *                        attended set are never used.
  *   other arguments    : as pkv_paged_decode_attention; the same workspace
@@ -469,7 +471,7 @@ int pkv_sparse_decode_attention_q8(void* out, const void* q, const void* k_codes
 /*
  * pkv_kv_compact_q8 -- pkv_kv_compact over INT8 pools: each kept row's codes and its fp32 row
  * scale move together, so the compact pool holds the same values (code * scale).
- *   dst_k_codes, dst_v_codes, src_k_codes, src_v_codes : [NB, Hkv, 16, d] int8 pools.
+ *   dst_k_codes, dst_v_codes, src_k_codes, src_v_codes : [NB, Hkv, 16, d] uint8 pools.
  *   dst_k_scales, dst_v_scales, src_k_scales, src_v_scales : [NB, Hkv, 16] fp32 row scales.
  *   other arguments : as pkv_kv_compact.  All pool pointers 16-byte aligned.  Bit-exact.
  */
@@ -516,7 +518,7 @@ int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tabl
 /*
  * pkv_kv_rolling_admit_q8 -- pkv_kv_rolling_admit into INT8 pools: the same choice of slot,
  * and the new token's K and V rows quantized into it by the row rule of pkv_kv_append_q8.
- *   k_codes, v_codes   : [NB, Hkv, 16, d] int8 compact pools, updated in place.
+ *   k_codes, v_codes   : [NB, Hkv, 16, d] uint8 compact pools, updated in place.
  *   k_scales, v_scales : [NB, Hkv, 16] fp32 row scales, updated in place.
  *   other arguments    : as pkv_kv_rolling_admit.
  *   error_word         : as pkv_kv_rolling_admit, plus PKV_DEV_BAD_VALUE for a (b, g) whose new K

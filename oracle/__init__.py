@@ -306,21 +306,22 @@ def rolling_admit(k_cache, v_cache, block_tables, slot_pos, slot_score, kept_len
 
 
 def quantize_rows(x):
-    """INT8 quantization of the last axis of x (bf16 bits): (codes int8 x.shape, scales fp32 x.shape[:-1])."""
+    """INT8 quantization of the last axis of x (bf16 bits): (codes x.shape as stored, each code c as the
+    byte c + 128 (uint8), scales fp32 x.shape[:-1])."""
     x = _arr(x, np.uint16)
     d = x.shape[-1]
     n = x.size // d if d else 0
-    codes = np.zeros(x.shape, dtype=np.int8)
+    codes = np.zeros(x.shape, dtype=np.uint8)
     scales = np.zeros(x.shape[:-1], dtype=np.float32)
     _check(_load().oracle_quantize_rows(_ptr(codes), _ptr(scales), _ptr(x), n, d), "quantize_rows")
     return codes, scales
 
 
 def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k, v, slot_mapping):
-    """Return copies of the INT8 pools ([NB,Hkv,16,d] int8 codes, [NB,Hkv,16] fp32 scales)
+    """Return copies of the INT8 pools ([NB,Hkv,16,d] uint8 codes c stored as c + 128, [NB,Hkv,16] fp32 scales)
     after quantizing k, v [T,Hkv,d] (bf16 bits) into the slots."""
-    kc = np.array(_arr(k_codes, np.int8), copy=True)
-    vc = np.array(_arr(v_codes, np.int8), copy=True)
+    kc = np.array(_arr(k_codes, np.uint8), copy=True)
+    vc = np.array(_arr(v_codes, np.uint8), copy=True)
     ks = np.array(_arr(k_scales, np.float32), copy=True)
     vs = np.array(_arr(v_scales, np.float32), copy=True)
     k = _arr(k, np.uint16)
@@ -338,8 +339,8 @@ def paged_decode_q8(q, k_codes, k_scales, v_codes, v_scales, block_tables, conte
                     rows=None):
     """fp64 attention over INT8 pools (values code * scale).  Shapes as paged_decode."""
     q = _arr(q, np.uint16)
-    kc = _arr(k_codes, np.int8)
-    vc = _arr(v_codes, np.int8)
+    kc = _arr(k_codes, np.uint8)
+    vc = _arr(v_codes, np.uint8)
     ks = _arr(k_scales, np.float32)
     vs = _arr(v_scales, np.float32)
     bt = _arr(block_tables, np.int32)
@@ -389,7 +390,7 @@ def prefill_scores(q_win, k_cache, block_tables, context_lens, alpha, scale, lse
 def decode_scores_q8(q, k_codes, k_scales, block_tables, context_lens, scale, window=0, stride=None, segs=None):
     """decode_scores over an INT8 K pool (values code * scale); same returns."""
     q = _arr(q, np.uint16)
-    kc = _arr(k_codes, np.int8)
+    kc = _arr(k_codes, np.uint8)
     ks = _arr(k_scales, np.float32)
     bt = _arr(block_tables, np.int32)
     lens = _arr(context_lens, np.int32)
@@ -418,13 +419,13 @@ def decode_scores_q8(q, k_codes, k_scales, block_tables, context_lens, scale, wi
 def compact_q8(dst_k, dst_v, dst_ks, dst_vs, dst_block_tables, src_k, src_v, src_ks, src_vs, src_block_tables,
                context_lens, kept, kept_lens):
     """INT8 compaction; returns copies (dst_k, dst_v, dst_ks, dst_vs) of the destination pools."""
-    dk = np.array(_arr(dst_k, np.int8), copy=True)
-    dv = np.array(_arr(dst_v, np.int8), copy=True)
+    dk = np.array(_arr(dst_k, np.uint8), copy=True)
+    dv = np.array(_arr(dst_v, np.uint8), copy=True)
     dks = np.array(_arr(dst_ks, np.float32), copy=True)
     dvs = np.array(_arr(dst_vs, np.float32), copy=True)
     dbt = _arr(dst_block_tables, np.int32)
-    sk = _arr(src_k, np.int8)
-    sv = _arr(src_v, np.int8)
+    sk = _arr(src_k, np.uint8)
+    sv = _arr(src_v, np.uint8)
     sks = _arr(src_ks, np.float32)
     svs = _arr(src_vs, np.float32)
     sbt = _arr(src_block_tables, np.int32)
@@ -445,8 +446,8 @@ def rolling_admit_q8(k_codes, v_codes, k_scales, v_scales, block_tables, slot_po
                      context_lens, k_new, v_new, n_sink, n_recent):
     """rolling_admit into INT8 pools; returns updated copies (k_codes, v_codes, k_scales,
     v_scales, slot_pos, slot_score, kept_lens)."""
-    kc = np.array(_arr(k_codes, np.int8), copy=True)
-    vc = np.array(_arr(v_codes, np.int8), copy=True)
+    kc = np.array(_arr(k_codes, np.uint8), copy=True)
+    vc = np.array(_arr(v_codes, np.uint8), copy=True)
     ks = np.array(_arr(k_scales, np.float32), copy=True)
     vs = np.array(_arr(v_scales, np.float32), copy=True)
     bt = _arr(block_tables, np.int32)
@@ -470,8 +471,8 @@ def sparse_decode_q8(q, k_codes, k_scales, v_codes, v_scales, block_tables, cont
                      rows=None):
     """sparse_decode over INT8 pools (values code * scale).  Shapes as sparse_decode."""
     q = _arr(q, np.uint16)
-    kc = _arr(k_codes, np.int8)
-    vc = _arr(v_codes, np.int8)
+    kc = _arr(k_codes, np.uint8)
+    vc = _arr(v_codes, np.uint8)
     ks = _arr(k_scales, np.float32)
     vs = _arr(v_scales, np.float32)
     bt = _arr(block_tables, np.int32)

@@ -53,19 +53,19 @@ static float bf16_to_float(uint16_t bits) {
 }
 
 /*
- * A K or V pool as the decode reads it: bf16 elements, or INT8 codes with one fp32 scale per
- * (block, kv head, token) row, whose values are code * scale (exact in fp64).
+ * A K or V pool as the decode reads it: bf16 elements, or INT8 codes (bytes code + 128) with one
+ * fp32 scale per (block, kv head, token) row, whose values are code * scale (exact in fp64).
  * Row r = (physical block * Hkv + kv head) * 16 + offset; element e of row r is at r * d + e.
  */
 typedef struct {
   const uint16_t* bf16;
-  const int8_t* codes;
+  const uint8_t* codes;
   const float* scales;
 } pool_t;
 
 static double pool_value(const pool_t* p, int64_t row, int head_dim, int e) {
   if (p->bf16) return bf16_to_double(p->bf16[row * head_dim + e]);
-  return (double)p->codes[row * head_dim + e] * (double)p->scales[row];
+  return (double)((int)p->codes[row * head_dim + e] - 128) * (double)p->scales[row];
 }
 
 int oracle_num_threads(void) {
@@ -263,8 +263,10 @@ int oracle_paged_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
  * and the row's values are c_e * s.  The division and the rounding are single-precision
  * IEEE operations: they decide an integer, so they are taken in the precision the kernel
  * takes them in.  A row of zeros gets s = 0 and codes 0; a non-finite element is refused.
+ * A code c is stored as the byte c + 128 (the library's pool format); a byte b reads as the
+ * code b - 128.
  */
-static int quantize_row(int8_t* codes, float* scale, const uint16_t* x, int head_dim) {
+static int quantize_row(uint8_t* codes, float* scale, const uint16_t* x, int head_dim) {
   float amax = 0.0f;
   for (int e = 0; e < head_dim; ++e) {
     float v = bf16_to_float(x[e]);
@@ -275,19 +277,19 @@ static int quantize_row(int8_t* codes, float* scale, const uint16_t* x, int head
   *scale = s;
   for (int e = 0; e < head_dim; ++e) {
     if (s == 0.0f) {
-      codes[e] = 0;
+      codes[e] = 128;  /* code 0 */
       continue;
     }
     float c = rintf(bf16_to_float(x[e]) / s);
     if (c > 127.0f) c = 127.0f;
     if (c < -127.0f) c = -127.0f;
-    codes[e] = (int8_t)c;
+    codes[e] = (uint8_t)((int)c + 128);
   }
   return ORC_OK;
 }
 
 /* Quantize n_rows rows of d bf16 values: codes [n_rows][d], scales [n_rows]. */
-int oracle_quantize_rows(int8_t* codes, float* scales, const uint16_t* x, int64_t n_rows,
+int oracle_quantize_rows(uint8_t* codes, float* scales, const uint16_t* x, int64_t n_rows,
                          int head_dim) {
   if (n_rows < 0 || head_dim <= 0) return ORC_ERR_ARG;
   for (int64_t r = 0; r < n_rows; ++r) {
@@ -299,9 +301,10 @@ int oracle_quantize_rows(int8_t* codes, float* scales, const uint16_t* x, int64_
 
 /*
  * Append into INT8 pools: as oracle_kv_append, with each (token, kv head) row of K and of V
- * quantized on the way in.  Code pools are [NB][Hkv][16][d] int8, scale pools [NB][Hkv][16].
+ * quantized on the way in.  Code pools are [NB][Hkv][16][d] bytes (code + 128), scale pools
+ * [NB][Hkv][16].
  */
-int oracle_kv_append_q8(int8_t* k_codes, int8_t* v_codes, float* k_scales, float* v_scales,
+int oracle_kv_append_q8(uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales,
                         const uint16_t* k, const uint16_t* v, const int64_t* slot_mapping,
                         int64_t num_tokens, int num_kv_heads, int head_dim, int64_t num_blocks) {
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return ORC_ERR_ARG;
@@ -326,8 +329,8 @@ int oracle_kv_append_q8(int8_t* k_codes, int8_t* v_codes, float* k_scales, float
  * Paged decode attention over INT8 pools: oracle_paged_decode with every K and V element
  * dequantized (code * scale, exact in fp64) where it is used.
  */
-int oracle_paged_decode_q8(double* out, const uint16_t* q, const int8_t* k_codes,
-                           const float* k_scales, const int8_t* v_codes, const float* v_scales,
+int oracle_paged_decode_q8(double* out, const uint16_t* q, const uint8_t* k_codes,
+                           const float* k_scales, const uint8_t* v_codes, const float* v_scales,
                            const int32_t* block_tables, const int32_t* context_lens, int batch,
                            int num_q_heads, int num_kv_heads, int head_dim, int64_t num_blocks,
                            int max_blocks_per_seq, double scale, int window,
@@ -406,8 +409,8 @@ int oracle_sparse_decode(double* out, const uint16_t* q, const uint16_t* k_cache
 }
 
 /* Sparse decode attention over INT8 pools: every K and V element read as code * row scale. */
-int oracle_sparse_decode_q8(double* out, const uint16_t* q, const int8_t* k_codes,
-                            const float* k_scales, const int8_t* v_codes, const float* v_scales,
+int oracle_sparse_decode_q8(double* out, const uint16_t* q, const uint8_t* k_codes,
+                            const float* k_scales, const uint8_t* v_codes, const float* v_scales,
                             const int32_t* block_tables, const int32_t* context_lens,
                             const int32_t* kept, const int32_t* kept_lens, int max_kept,
                             int batch, int num_q_heads, int num_kv_heads, int head_dim,
@@ -540,7 +543,7 @@ int oracle_decode_scores(double* score_add, double* lse, const uint16_t* q,
 
 /* The decode score over an INT8 K pool: every K element read as code * scale of its row. */
 int oracle_decode_scores_q8(double* score_add, double* lse, const uint16_t* q,
-                            const int8_t* k_codes, const float* k_scales,
+                            const uint8_t* k_codes, const float* k_scales,
                             const int32_t* block_tables, const int32_t* context_lens, int batch,
                             int num_q_heads, int num_kv_heads, int head_dim, int64_t num_blocks,
                             int max_blocks_per_seq, double scale, int window, int64_t stride,
@@ -769,9 +772,9 @@ int oracle_compact(uint16_t* dst_k, uint16_t* dst_v, const int32_t* dst_block_ta
  * Compaction of INT8 pools: the kept rows' codes and their row scales move together, so the
  * compact pool holds the same values (code * scale) at the new positions.
  */
-int oracle_compact_q8(int8_t* dst_k, int8_t* dst_v, float* dst_ks, float* dst_vs,
+int oracle_compact_q8(uint8_t* dst_k, uint8_t* dst_v, float* dst_ks, float* dst_vs,
                       const int32_t* dst_block_tables, int64_t dst_num_blocks,
-                      int dst_max_blocks_per_seq, const int8_t* src_k, const int8_t* src_v,
+                      int dst_max_blocks_per_seq, const uint8_t* src_k, const uint8_t* src_v,
                       const float* src_ks, const float* src_vs, const int32_t* src_block_tables,
                       const int32_t* context_lens, const int32_t* kept, const int32_t* kept_lens,
                       int max_kept, int batch, int num_kv_heads, int head_dim,
@@ -792,8 +795,8 @@ int oracle_compact_q8(int8_t* dst_k, int8_t* dst_v, float* dst_ks, float* dst_vs
 typedef struct {
   uint16_t* k_bf16;
   uint16_t* v_bf16;
-  int8_t* k_codes;
-  int8_t* v_codes;
+  uint8_t* k_codes;
+  uint8_t* v_codes;
   float* k_scales;
   float* v_scales;
 } wpool_t;
@@ -805,8 +808,8 @@ static int write_row(const wpool_t* p, int64_t r, const uint16_t* k, const uint1
     memcpy(p->v_bf16 + r * head_dim, v, (size_t)head_dim * sizeof(uint16_t));
     return ORC_OK;
   }
-  int8_t* kc = (int8_t*)malloc((size_t)head_dim);
-  int8_t* vc = (int8_t*)malloc((size_t)head_dim);
+  uint8_t* kc = (uint8_t*)malloc((size_t)head_dim);
+  uint8_t* vc = (uint8_t*)malloc((size_t)head_dim);
   float ks = 0.0f, vs = 0.0f;
   int st = (kc && vc) ? ORC_OK : ORC_ERR_MEM;
   if (st == ORC_OK) st = quantize_row(kc, &ks, k, head_dim);
@@ -904,7 +907,7 @@ int oracle_rolling_admit(uint16_t* k_cache, uint16_t* v_cache, const int32_t* bl
  * Rolling admission into INT8 pools: the same choice of slot; the new token's K and V rows
  * are quantized into it (codes and row scale, as oracle_kv_append_q8 does).
  */
-int oracle_rolling_admit_q8(int8_t* k_codes, int8_t* v_codes, float* k_scales, float* v_scales,
+int oracle_rolling_admit_q8(uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales,
                             const int32_t* block_tables, int64_t num_blocks,
                             int max_blocks_per_seq, int32_t* slot_pos, float* slot_score,
                             int32_t* kept_lens, const int32_t* context_lens,

@@ -102,9 +102,9 @@ def kv_append(k_cache, v_cache, k, v, slot_mapping, *, error_word=None, stream=N
 
 
 def _q8_pool_dims(k_codes, v_codes, k_scales, v_scales):
-    _need(k_codes, "k_codes", torch.int8, 4)
+    _need(k_codes, "k_codes", torch.uint8, 4)
     dev = k_codes.device
-    _need(v_codes, "v_codes", torch.int8, 4, dev)
+    _need(v_codes, "v_codes", torch.uint8, 4, dev)
     _need(k_scales, "k_scales", torch.float32, 3, dev)
     _need(v_scales, "v_scales", torch.float32, 3, dev)
     if v_codes.shape != k_codes.shape:
@@ -119,7 +119,8 @@ def _q8_pool_dims(k_codes, v_codes, k_scales, v_scales):
 
 def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k, v, slot_mapping, *, error_word=None, stream=None):
     """Quantize k, v [T, Hkv, d] (bf16) into the INT8 pools at slot_mapping [T] (int64):
-    codes [NB, Hkv, 16, d] int8 and one fp32 scale per row, [NB, Hkv, 16]."""
+    codes [NB, Hkv, 16, d] uint8 (each code c stored as the byte c + 128) and one fp32 scale per
+    row, [NB, Hkv, 16]."""
     nb, hkv, d = _q8_pool_dims(k_codes, v_codes, k_scales, v_scales)
     dev = k_codes.device
     _need(k, "k", torch.bfloat16, 3, dev)
@@ -399,7 +400,7 @@ def kv_rolling_admit(k_cache, v_cache, block_tables, slot_pos, slot_score, kept_
 
 def kv_rolling_admit_q8(k_codes, v_codes, k_scales, v_scales, block_tables, slot_pos, slot_score, kept_lens,
                         context_lens, k_new, v_new, n_sink, n_recent, *, error_word=None, stream=None):
-    """kv_rolling_admit into INT8 compact pools (codes [NB, Hkv, 16, d] int8, row scales
+    """kv_rolling_admit into INT8 compact pools (codes [NB, Hkv, 16, d] uint8 as code + 128, row scales
     [NB, Hkv, 16] fp32): the same slot choice, the new rows quantized into the slot."""
     nb, hkv, d = _q8_pool_dims(k_codes, v_codes, k_scales, v_scales)
     dims = _rolling_dims(nb, hkv, d, k_codes.device, block_tables, slot_pos, slot_score, kept_lens, context_lens,

@@ -35,9 +35,9 @@
 //    operand by an in-register 8x8 transpose (movmatrix); it is carried as bf16 hi + lo
 //    parts so P keeps ~16 significant bits.  This replaces ~870 CUDA-core instructions per
 //    unit with ~100, leaving the warps waiting on memory rather than on issue slots.
-//  * INT8 pools (one code byte per element plus one fp32 scale per row and kv head): the
-//    codes become fp16 in registers (a byte permute under the exponent of 1024 and one
-//    subtraction per pair), both products take fp16 operands, the K row scales multiply the
+//  * INT8 pools (one byte per element, the code + 128, plus one fp32 scale per row and kv
+//    head): the codes become fp16 in registers (a byte permute under the exponent of 1024,
+//    and for V one subtraction per pair), both products take fp16 operands, the K row scales multiply the
 //    logits and the V row scales enter P, relative to a per-segment reference scale, as one
 //    fp16 term.  Sparse rows arrive chunk by chunk as above, their scales as 4-byte copies
 //    completing on the K barrier.
@@ -801,7 +801,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         for (int i = 0; i < 8; ++i) {
           int cd = 0;
           if (new_scale != 0.f) cd = max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], new_scale))));
-          pk[i / 4] |= (uint32_t)(cd & 0xff) << (8 * (i % 4));
+          pk[i / 4] |= (uint32_t)(cd + 128) << (8 * (i % 4));  // stored as code + 128
         }
         new_codes = make_uint2(pk[0], pk[1]);
       }
@@ -891,8 +891,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         for (int pp = 0; pp < KS / 2; ++pp) {
           uint32_t r[4];
           ldsm_x4(kbase + chunk_offset<D, SPARSE, Q8>(k_row, 2 * pp + k_half), r);
-          const uint32_t f0 = r[0] ^ 0x80808080u, f1 = r[1] ^ 0x80808080u;
-          const uint32_t f2 = r[2] ^ 0x80808080u, f3 = r[3] ^ 0x80808080u;
+          const uint32_t f0 = r[0], f1 = r[1], f2 = r[2], f3 = r[3];  // bytes code + 128
           const uint32_t a0[4] = {i8x2_to_biased_f16x2<0x4140>(f0), i8x2_to_biased_f16x2<0x4140>(f1),
                                   i8x2_to_biased_f16x2<0x4342>(f0), i8x2_to_biased_f16x2<0x4342>(f1)};
           mma_f16_m16n8k16(c, a0, qb[4 * pp], qb[4 * pp + 1]);
@@ -1051,8 +1050,7 @@ decode_split_kernel(const __grid_constant__ DecodeArgs a) {
         for (int pp = 0; pp < KS / 2; ++pp) {
           uint32_t r[4];
           ldsm_x4_trans(vbase + chunk_offset<D, SPARSE, Q8>(k_row, 2 * pp + k_half), r);
-          const uint32_t f0 = r[0] ^ 0x80808080u, f1 = r[1] ^ 0x80808080u;
-          const uint32_t f2 = r[2] ^ 0x80808080u, f3 = r[3] ^ 0x80808080u;
+          const uint32_t f0 = r[0], f1 = r[1], f2 = r[2], f3 = r[3];  // bytes code + 128
           const uint32_t a0[4] = {i8x2_to_f16x2<0x4240>(f0), i8x2_to_f16x2<0x4341>(f0),
                                   i8x2_to_f16x2<0x4240>(f1), i8x2_to_f16x2<0x4341>(f1)};
           mma_f16_m16n8k16(o[2 * pp], a0, bh0, bh1);

@@ -39,7 +39,7 @@ struct DecodeArgs {
   float2* part_ml;               // [2 ranges, G] (running max in log2 units, running sum)
   float* part_o;                 // [2 ranges, G, D] unnormalised partial outputs
   const float* k_scale;          // INT8 pools: [NB, Hkv, 16] fp32 scale of each K row
-  const float* v_scale;          //   (likewise V); the pools then hold int8 codes
+  const float* v_scale;          //   (likewise V); the pools then hold INT8 codes (bytes code + 128)
   float* k_scale_out;            // INT8 append mode: the scale pools again, writable
   float* v_scale_out;
   float* logits;                 // scores mode: [B, Hq, score_stride] base-2 logits of attended keys
@@ -197,7 +197,7 @@ cudaError_t launch_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t*
                                     const int32_t* lens, const void* k_new, const void* v_new, int B,
                                     int Hkv, int D, int capacity, int n_sink, int n_recent, int32_t* err,
                                     cudaStream_t stream);
-// INT8 pools: codes [NB, Hkv, 16, D] int8 with row scales [NB, Hkv, 16] fp32 moving with them.
+// INT8 pools: codes [NB, Hkv, 16, D] (bytes code + 128) with row scales [NB, Hkv, 16] fp32 moving with them.
 cudaError_t launch_kv_compact_q8(void* dk, void* dv, float* dks, float* dvs, const int32_t* dbt, int dNB,
                                  int dMB, const void* sk, const void* sv, const float* sks, const float* svs,
                                  const int32_t* sbt, const int32_t* lens, const int32_t* kept,

@@ -53,12 +53,13 @@ __global__ void __launch_bounds__(256) kv_append_kernel(__nv_bfloat16* __restric
 // INT8 row rule (the KV-cache primer's INT8 cache, section 4.2): each (token, kv head) row of
 // d values gets one fp32 scale s = max|x| / 127 and codes round_half_even(x / s), clamped to
 // [-127, 127]; a zero row gets s = 0 and codes 0.  The division and rounding are IEEE single
-// precision (they decide the codes).  A warp quantizes one token's K row (lanes 0-15) and V
+// precision (they decide the codes).  A code c is stored as the byte c + 128 (so the decode's
+// int8-to-fp16 conversion needs no sign flip).  A warp quantizes one token's K row (lanes 0-15) and V
 // row (lanes 16-31), D/16 elements a lane, and stores codes and scales at the given rows; if
 // either row holds a non-finite value it stores nothing and returns false.  Every lane of the
 // warp calls it.
 template <int D>
-__device__ __forceinline__ bool quantize_kv_rows(int8_t* kq_row, int8_t* vq_row, float* ks_at, float* vs_at,
+__device__ __forceinline__ bool quantize_kv_rows(uint8_t* kq_row, uint8_t* vq_row, float* ks_at, float* vs_at,
                                                  const __nv_bfloat16* k_src, const __nv_bfloat16* v_src,
                                                  int lane) {
   constexpr int E = D / 16;  // elements per lane
@@ -100,9 +101,9 @@ __device__ __forceinline__ bool quantize_kv_rows(int8_t* kq_row, int8_t* vq_row,
   for (int i = 0; i < E; ++i) {
     int c = 0;
     if (sc != 0.f) c = max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], sc))));
-    packed[i / 4] |= (uint32_t)(c & 0xff) << (8 * (i % 4));
+    packed[i / 4] |= (uint32_t)(c + 128) << (8 * (i % 4));
   }
-  int8_t* dst = (lane < 16 ? kq_row : vq_row) + h * E;
+  uint8_t* dst = (lane < 16 ? kq_row : vq_row) + h * E;
   if constexpr (E == 8)
     *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
   else
@@ -114,7 +115,7 @@ __device__ __forceinline__ bool quantize_kv_rows(int8_t* kq_row, int8_t* vq_row,
 // INT8 append: the new token's K and V rows quantized into INT8 pools by the row rule above.
 // One warp per (token, kv head).  A non-finite element skips the token's rows and is reported.
 template <int D>
-__global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ kq, int8_t* __restrict__ vq,
+__global__ void __launch_bounds__(256) kv_append_q8_kernel(uint8_t* __restrict__ kq, uint8_t* __restrict__ vq,
                                                            float* __restrict__ ks, float* __restrict__ vs,
                                                            const __nv_bfloat16* __restrict__ k,
                                                            const __nv_bfloat16* __restrict__ v,
@@ -894,7 +895,7 @@ __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
         const size_t src = ((size_t)b * Hkv + g) * D;
         bool written = true;
         if constexpr (Q8) {
-          written = quantize_kv_rows<D>(static_cast<int8_t*>(kc) + row * D, static_cast<int8_t*>(vc) + row * D,
+          written = quantize_kv_rows<D>(static_cast<uint8_t*>(kc) + row * D, static_cast<uint8_t*>(vc) + row * D,
                                         ks + row, vs + row, k_new + src, v_new + src, lane);
           if (!written && lane == 0) record_error(err, PKV_DEV_BAD_VALUE);
         } else {
@@ -944,8 +945,8 @@ cudaError_t launch_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, f
   const int64_t warps = T * Hkv;
   if (warps == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
-  auto* kq = static_cast<int8_t*>(k_codes);
-  auto* vq = static_cast<int8_t*>(v_codes);
+  auto* kq = static_cast<uint8_t*>(k_codes);
+  auto* vq = static_cast<uint8_t*>(v_codes);
   auto* kk = static_cast<const __nv_bfloat16*>(k);
   auto* vv = static_cast<const __nv_bfloat16*>(v);
   void* args[] = {&kq, &vq, &k_scales, &v_scales, &kk, &vv, &slots, &T, &Hkv, &NB, &err};

@@ -317,14 +317,14 @@ __device__ __forceinline__ float f16_hi_to_f32(uint32_t w) {
   return f;
 }
 
-// Two int8 codes of a word as an exact f16x2.  `flipped` is the word with every byte's sign
-// bit inverted (byte = code + 128); SEL names the two bytes (low result half first) in the
-// form 0x4j4i.  Byte u under the exponent byte 0x64 is the fp16 number 1024 + u (fp16 holds
-// every integer below 2048), so subtracting 1152 leaves the code itself.
+// Two INT8 codes of a word as an exact f16x2.  The word holds four stored bytes, each code + 128;
+// SEL names the two bytes (low result half first) in the form 0x4j4i.  Byte u under the
+// exponent byte 0x64 is the fp16 number 1024 + u (fp16 holds every integer below 2048), so
+// subtracting 1152 leaves the code itself.
 template <uint32_t SEL>
-__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t flipped) {
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t w) {
   uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(flipped), "r"(0x64646464u), "n"(SEL));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(0x64646464u), "n"(SEL));
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r) : "r"(0x64806480u));
   return r;
 }
@@ -332,9 +332,9 @@ __device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t flipped) {
 // The same two codes as the fp16 numbers 1152 + code (the subtraction left to the caller: a
 // contraction over such values differs from the codes' by 1152 times the sum of the other operand).
 template <uint32_t SEL>
-__device__ __forceinline__ uint32_t i8x2_to_biased_f16x2(uint32_t flipped) {
+__device__ __forceinline__ uint32_t i8x2_to_biased_f16x2(uint32_t w) {
   uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(flipped), "r"(0x64646464u), "n"(SEL));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(0x64646464u), "n"(SEL));
   return r;
 }
 

@@ -25,6 +25,23 @@ def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().to(torch.float64).numpy()
 
 
+def stored_codes(codes) -> np.ndarray:
+    """INT8 codes (integers in [-128, 127]) as the pools store them: the byte code + 128."""
+    return (np.asarray(codes, dtype=np.int32) + 128).astype(np.uint8)
+
+
+def code_values(stored) -> np.ndarray:
+    """The INT8 codes of stored pool bytes (numpy or torch): byte - 128, as int32."""
+    if isinstance(stored, torch.Tensor):
+        stored = stored.cpu().numpy()
+    return np.asarray(stored).astype(np.int32) - 128
+
+
+def rand_code_pool(shape, gen, device=None) -> torch.Tensor:
+    """A pool of random INT8 codes in [-127, 127], stored as bytes code + 128 (uint8)."""
+    return torch.randint(1, 256, shape, generator=gen, device=device, dtype=torch.uint8)
+
+
 def paged_from_contiguous(k, v, lens, num_blocks, gen, max_blocks=None, fill=None):
     """Scatter contiguous k, v [B, Lmax, Hkv, d] (bf16) into shuffled pools.
 

@@ -91,7 +91,7 @@ def test_fixed_scratch_out():
 
 def _q8_pools(nb, hkv, d, seed):
     g = torch.Generator(device=DEV).manual_seed(seed)
-    codes = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    codes = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
     scales = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     return codes, scales
 
@@ -103,8 +103,8 @@ def test_int8_append_decode_pools_and_out():
     B = len(lens)
     kq0, ks0 = _q8_pools(nb, hkv, d, 5)
     vq0, vs0 = _q8_pools(nb, hkv, d, 6)
-    kq = Guarded(kq0.shape, torch.int8, init=kq0)
-    vq = Guarded(vq0.shape, torch.int8, init=vq0)
+    kq = Guarded(kq0.shape, torch.uint8, init=kq0)
+    vq = Guarded(vq0.shape, torch.uint8, init=vq0)
     ks = Guarded(ks0.shape, torch.float32, init=ks0)
     vs = Guarded(vs0.shape, torch.float32, init=vs0)
     out = Guarded((B, hq, d), torch.bfloat16)
@@ -154,7 +154,7 @@ def test_sparse_select_compact_gather_and_rolling():
     # INT8 forms of the compaction and the gather decode
     skq, sks = _q8_pools(nb, hkv, d, 11)
     svq, svs = _q8_pools(nb, hkv, d, 12)
-    dkq = Guarded((dnb, hkv, 16, d), torch.int8, init=0)
+    dkq = Guarded((dnb, hkv, 16, d), torch.uint8, init=0)
     dks = Guarded((dnb, hkv, 16), torch.float32, init=0)
     pkv.kv_compact_q8(dkq.t, dkq.t.clone(), dks.t, dks.t.clone(), dbt, skq, svq, sks, svs, c["block_tables"],
                       c["context_lens"], kept.t, kl.t, error_word=err)

@@ -18,7 +18,7 @@ import torch
 import oracle
 import paged_kv_cache_mapped_gb300 as pkv
 from paged_kv_cache_mapped_gb300 import inputs as W
-from helpers import assert_attn_close, bits, paged_from_contiguous, rand_bf16
+from helpers import assert_attn_close, bits, code_values, paged_from_contiguous, rand_bf16, stored_codes
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -255,7 +255,7 @@ def test_errors_found_before_the_wait_are_recorded():
 
 def _q8_pools(nb, hkv, d, seed):
     g = torch.Generator(device=DEV).manual_seed(seed)
-    codes = lambda: torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    codes = lambda: torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
     scales = lambda: torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     return codes(), codes(), scales(), scales()
 
@@ -450,7 +450,7 @@ def _compact_layer(B, hkv, d, lens, max_kept, seed, q8):
     c = {"sbt": t(sbt), "lens": t(lens), "kept": t(kept), "kl": t(kl)}
     if q8:
         for name in ("sk", "sv"):
-            c[name] = t(rng.integers(-127, 128, size=(snb, hkv, 16, d)).astype(np.int8))
+            c[name] = t(stored_codes(rng.integers(-127, 128, size=(snb, hkv, 16, d))))
             c[name + "s"] = t(rng.exponential(size=(snb, hkv, 16)).astype(np.float32))
     else:
         for name in ("sk", "sv"):
@@ -465,7 +465,7 @@ def _compact_dst(B, hkv, d, max_kept, seed, q8):
     dnb = B * dmb + 3
     dbt = torch.from_numpy(rng.permutation(dnb)[: B * dmb].reshape(B, dmb).astype(np.int32)).to(DEV)
     if q8:
-        pools = [torch.from_numpy(rng.integers(-127, 128, size=(dnb, hkv, 16, d)).astype(np.int8)).to(DEV)
+        pools = [torch.from_numpy(stored_codes(rng.integers(-127, 128, size=(dnb, hkv, 16, d)))).to(DEV)
                  for _ in range(2)]
         pools += [torch.from_numpy(rng.exponential(size=(dnb, hkv, 16)).astype(np.float32)).to(DEV) for _ in range(2)]
     else:

@@ -203,7 +203,7 @@ def test_compaction_rejects_duplicates_and_descents(q8):
     err = pkv.new_error_word(DEV)
     dv = lambda t: t.to(DEV)
     if q8:
-        z = lambda: torch.zeros((dnb, hkv, 16, d), dtype=torch.int8)
+        z = lambda: torch.zeros((dnb, hkv, 16, d), dtype=torch.uint8)
         zs = lambda: torch.zeros((dnb, hkv, 16), dtype=torch.float32)
         dst = [z(), z(), zs(), zs()]
         ref = oracle.compact_q8(dst[0].numpy(), dst[1].numpy(), dst[2].numpy(), dst[3].numpy(), dbt.numpy(),

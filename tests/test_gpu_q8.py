@@ -10,7 +10,7 @@ import torch
 import oracle
 import paged_kv_cache_mapped_gb300 as pkv
 from paged_kv_cache_mapped_gb300 import inputs as W
-from helpers import assert_attn_close, bits, paged_from_contiguous, rand_bf16
+from helpers import assert_attn_close, bits, code_values, paged_from_contiguous, rand_bf16, stored_codes
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -72,8 +72,8 @@ def test_append_q8_bit_exact(d):
     k[6, 2] = 0.0                                  # a zero row
     slots = torch.from_numpy(rng.choice(nb * 16, size=T, replace=False).astype(np.int64))
     slots[7] = -1
-    kq0 = torch.from_numpy(rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8))
-    vq0 = torch.from_numpy(rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8))
+    kq0 = torch.from_numpy(stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d))))
+    vq0 = torch.from_numpy(stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d))))
     ks0 = torch.rand((nb, hkv, 16), generator=g)
     vs0 = torch.rand((nb, hkv, 16), generator=g)
     ref = oracle.kv_append_q8(kq0.numpy(), vq0.numpy(), ks0.numpy(), vs0.numpy(), bits(k), bits(v), slots.numpy())
@@ -91,7 +91,7 @@ def test_append_q8_non_finite_reported_and_skipped():
     v = torch.ones((3, hkv, d), dtype=torch.bfloat16)
     v[1, 0, 9] = float("inf")
     slots = torch.tensor([0, 17, 33], dtype=torch.int64)
-    kq = torch.zeros((nb, hkv, 16, d), dtype=torch.int8, device=DEV)
+    kq = torch.zeros((nb, hkv, 16, d), dtype=torch.uint8, device=DEV)
     vq = torch.zeros_like(kq)
     ks = torch.full((nb, hkv, 16), 7.0, device=DEV)
     vs = torch.full((nb, hkv, 16), 7.0, device=DEV)
@@ -99,8 +99,9 @@ def test_append_q8_non_finite_reported_and_skipped():
     pkv.kv_append_q8(kq, vq, ks, vs, k.to(DEV), v.to(DEV), slots.to(DEV), error_word=err)
     assert pkv.read_error(err) == pkv.header_constants()["PKV_DEV_BAD_VALUE"]
     assert ks[1, 0, 1].item() == 7.0 and torch.all(kq[1, 0, 1] == 0)     # token 1, kv head 0 skipped
-    assert ks[1, 1, 1].item() == pytest.approx(1 / 127) and torch.all(kq[1, 1, 1] == 127)  # head 1 written
-    assert torch.all(kq[0, :, 0] == 127) and torch.all(kq[2, :, 1] == 127)
+    # written rows of ones: code 127 everywhere, stored as the byte 255
+    assert ks[1, 1, 1].item() == pytest.approx(1 / 127) and np.all(code_values(kq[1, 1, 1]) == 127)  # head 1
+    assert np.all(code_values(kq[0, :, 0]) == 127) and np.all(code_values(kq[2, :, 1]) == 127)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -154,8 +155,8 @@ def test_llama8b_full_size_sampled_rows():
     mb = int((lens.max() + 15) // 16)
     nb = B * mb + 64
     g = torch.Generator(device=DEV).manual_seed(31)
-    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
-    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    kq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
+    vq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
     ks = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     vs = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     bt = torch.randperm(nb, device=DEV, generator=g)[: B * mb].view(B, mb).to(torch.int32)
@@ -180,8 +181,8 @@ def test_long_contexts_with_tail_chunks_sampled_rows():
     mb = int((lens.max() + 15) // 16)
     nb = B * mb + 64
     g = torch.Generator(device=DEV).manual_seed(33)
-    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
-    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    kq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
+    vq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
     ks = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     vs = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     bt = torch.randperm(nb, device=DEV, generator=g)[: B * mb].view(B, mb).to(torch.int32)
@@ -251,7 +252,8 @@ def test_fused_append_q8_non_finite_row_is_reported_and_skipped():
     for k in ("kq", "vq", "ks", "vs"):
         assert torch.equal(c[k][blk1, 1, off1], before[k][blk1, 1, off1]), k   # (1, 1): not written
     blk0, off0 = int(c["bt"][0, 39 // 16]), 39 % 16
-    assert torch.all(c["kq"][blk0, :, off0] == 127) and torch.all(c["kq"][blk1, 0, off1] == 127)
+    # rows of ones: code 127 everywhere (stored as the byte 255)
+    assert np.all(code_values(c["kq"][blk0, :, off0]) == 127) and np.all(code_values(c["kq"][blk1, 0, off1]) == 127)
 
 
 def test_fused_append_q8_llama8b_full_size_sampled_rows():
@@ -261,8 +263,8 @@ def test_fused_append_q8_llama8b_full_size_sampled_rows():
     mb = int((lens.max() + 15) // 16)
     nb = B * mb + 64
     g = torch.Generator(device=DEV).manual_seed(93)
-    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
-    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    kq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
+    vq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
     ks = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     vs = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     bt = torch.randperm(nb, device=DEV, generator=g)[: B * mb].view(B, mb).to(torch.int32)

@@ -17,7 +17,7 @@ import torch
 import oracle
 import paged_kv_cache_mapped_gb300 as pkv
 from paged_kv_cache_mapped_gb300 import inputs as W
-from helpers import assert_attn_close, bits, paged_from_contiguous, rand_bf16
+from helpers import assert_attn_close, bits, code_values, paged_from_contiguous, rand_bf16, stored_codes
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -138,8 +138,8 @@ def test_scores_q8_llama8b_full_size_sampled_segments():
     mb = int((lens.max() + 15) // 16)
     nb = B * mb + 64
     g = torch.Generator(device=DEV).manual_seed(41)
-    kq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
-    vq = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    kq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
+    vq = torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
     ks = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     vs = torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     bt = torch.randperm(nb, device=DEV, generator=g)[: B * mb].view(B, mb).to(torch.int32)
@@ -162,7 +162,7 @@ def test_scores_q8_llama8b_full_size_sampled_segments():
 
 def _q8_pool(nb, hkv, d, seed):
     rng = np.random.default_rng(seed)
-    codes = torch.from_numpy(rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8))
+    codes = torch.from_numpy(stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d))))
     scales = torch.from_numpy(rng.exponential(size=(nb, hkv, 16)).astype(np.float32))
     return codes.to(DEV), scales.to(DEV)
 
@@ -287,9 +287,10 @@ def test_rolling_admit_q8_non_finite_row_leaves_its_head_unchanged():
     assert int(st["slot_pos"][1, 0, 0]) == -1                   # (b=1, g=0): nothing written
     assert np.array_equal(_n(st["kq"])[blk1, 0, 0], before[0][blk1, 0, 0])
     assert float(st["ks"][blk1, 0, 0]) == float(before[2][blk1, 0, 0])
-    assert int(st["slot_pos"][1, 1, 0]) == 0 and torch.all(st["kq"][blk1, 1, 0] == 127)   # (1, 1) admitted
+    # (1, 1) admitted: a row of ones is code 127 everywhere (stored as the byte 255)
+    assert int(st["slot_pos"][1, 1, 0]) == 0 and np.all(code_values(st["kq"][blk1, 1, 0]) == 127)
     blk0 = int(st["bt"][0, 0])
-    assert torch.all(st["kq"][blk0, :, 0] == 127) and torch.all(st["slot_pos"][0, :, 0] == 0)
+    assert np.all(code_values(st["kq"][blk0, :, 0]) == 127) and torch.all(st["slot_pos"][0, :, 0] == 0)
 
 
 def test_int8_sparse_layer_chain_matches_the_oracle_chain():
@@ -371,7 +372,7 @@ def test_compact_q8_sparse_workload_full_size_bit_exact():
     mb = int((lens.max() + 15) // 16)
     snb = B * mb + 16
     g = torch.Generator(device=DEV).manual_seed(71)
-    codes = lambda n: torch.randint(-127, 128, (n, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    codes = lambda n: torch.randint(1, 256, (n, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
     scales = lambda n: torch.empty((n, hkv, 16), device=DEV).exponential_(generator=g)
     sk, sv, sks, svs = codes(snb), codes(snb), scales(snb), scales(snb)
     sbt = torch.randperm(snb, device=DEV, generator=g)[: B * mb].view(B, mb).to(torch.int32)
@@ -480,7 +481,7 @@ def test_sparse_q8_sparse_workload_full_size_sampled_rows():
     mb = int((lens.max() + 15) // 16)
     nb = B * mb + 16
     g = torch.Generator(device=DEV).manual_seed(113)
-    codes = lambda: torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.int8)
+    codes = lambda: torch.randint(1, 256, (nb, hkv, 16, d), generator=g, device=DEV, dtype=torch.uint8)
     scales = lambda: torch.empty((nb, hkv, 16), device=DEV).exponential_(generator=g) * 0.02
     c = {"q": torch.randn((B, hq, d), generator=g, device=DEV).to(torch.bfloat16), "kq": codes(), "vq": codes(),
          "ks": scales(), "vs": scales(),

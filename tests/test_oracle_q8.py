@@ -1,6 +1,7 @@
 """Pins of the oracle's INT8 KV cache (oracle.quantize_rows, kv_append_q8, paged_decode_q8) to
 facts outside it.
 
+  Codes are checked as the pools store them: each code c as the byte c + 128.
   * exact round trips: a row whose values are integer codes times a power-of-two scale (one
     code of magnitude 127) quantizes back to exactly those codes and that scale;
   * hand-worked half-way ties (scale 1): round half to even;
@@ -16,7 +17,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import bits, from_bits, paged_from_contiguous, rand_bf16
+from helpers import bits, code_values, from_bits, paged_from_contiguous, rand_bf16, stored_codes
 
 
 def _bf16_bits_of(values: np.ndarray) -> np.ndarray:
@@ -29,11 +30,11 @@ def _bf16_bits_of(values: np.ndarray) -> np.ndarray:
 def test_codes_times_power_of_two_round_trip_exactly():
     rng = np.random.default_rng(1)
     for d, e in ((64, -9), (128, -3), (128, 0), (64, 4)):
-        codes = rng.integers(-127, 128, size=(20, d)).astype(np.int8)
+        codes = rng.integers(-127, 128, size=(20, d))
         codes[np.arange(20), rng.integers(0, d, size=20)] = rng.choice([-127, 127], size=20)
         x = codes.astype(np.float32) * np.float32(2.0 ** e)
         c, s = oracle.quantize_rows(_bf16_bits_of(x))
-        assert np.array_equal(c, codes)
+        assert c.dtype == np.uint8 and np.array_equal(code_values(c), codes)
         assert np.all(s == np.float32(2.0 ** e))
 
 
@@ -45,16 +46,17 @@ def test_half_way_ties_round_to_even():
     x[0, :len(row)] = row
     c, s = oracle.quantize_rows(_bf16_bits_of(x))
     assert s[0] == np.float32(1.0)
-    assert c[0, :len(want)].tolist() == want
+    assert code_values(c)[0, :len(want)].tolist() == want
 
 
 def test_rounding_bound_and_absmax_code():
     g = torch.Generator().manual_seed(2)
     x = rand_bf16((64, 128), g) * torch.logspace(-6, 6, 64).view(-1, 1).to(torch.bfloat16)
     c, s = oracle.quantize_rows(bits(x))
+    c = code_values(c)
     xf = x.to(torch.float64).numpy()
     deq = c.astype(np.float64) * s.astype(np.float64)[:, None]
-    assert np.all(np.abs(c.astype(np.int32)) <= 127)
+    assert np.all(np.abs(c) <= 127)
     # half a step, plus the fp32 quotient's rounding (half an ulp of a value below 128: 2^-18)
     assert np.all(np.abs(xf - deq) <= s.astype(np.float64)[:, None] * (0.5 + 2.0 ** -17))
     amax_at = np.argmax(np.abs(xf), axis=1)
@@ -65,7 +67,7 @@ def test_rounding_bound_and_absmax_code():
 
 def test_zero_rows_and_non_finite_refused():
     c, s = oracle.quantize_rows(np.zeros((3, 64), dtype=np.uint16))
-    assert np.all(c == 0) and np.all(s == 0.0)
+    assert np.all(code_values(c) == 0) and np.all(c == 128) and np.all(s == 0.0)
     for bad in (np.inf, -np.inf, np.nan):
         x = np.ones((2, 64), dtype=np.float32)
         x[1, 7] = bad
@@ -78,8 +80,8 @@ def test_append_q8_writes_quantized_rows_at_their_slots():
     nb, hkv, d, T = 6, 3, 64, 9
     g = torch.Generator().manual_seed(3)
     rng = np.random.default_rng(3)
-    kc = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
-    vc = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
+    kc = stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d)))
+    vc = stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d)))
     ks = rng.random((nb, hkv, 16)).astype(np.float32)
     vs = rng.random((nb, hkv, 16)).astype(np.float32)
     k = bits(rand_bf16((T, hkv, d), g))
@@ -111,10 +113,10 @@ def _pow2_q8_pools(nb, hkv, d, seed):
     rng = np.random.default_rng(seed)
     pools = []
     for _ in range(2):
-        codes = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
+        codes = rng.integers(-127, 128, size=(nb, hkv, 16, d))
         scales = (2.0 ** rng.integers(-9, 2, size=(nb, hkv, 16))).astype(np.float32)
         vals = codes.astype(np.float32) * scales[..., None]
-        pools.append((codes, scales, _bf16_bits_of(vals)))
+        pools.append((stored_codes(codes), scales, _bf16_bits_of(vals)))
     return pools
 
 
@@ -146,8 +148,8 @@ def test_q8_decode_matches_sdpa_on_dequantized_values():
     scale = d ** -0.5
     for window in (0, 20):
         got = oracle.paged_decode_q8(bits(q), kq, ks, vq, vs, bt.numpy(), np.array(lens, np.int32), scale, window)
-        kd = torch.from_numpy(kq.astype(np.float64) * ks.astype(np.float64)[..., None])
-        vd = torch.from_numpy(vq.astype(np.float64) * vs.astype(np.float64)[..., None])
+        kd = torch.from_numpy(code_values(kq).astype(np.float64) * ks.astype(np.float64)[..., None])
+        vd = torch.from_numpy(code_values(vq).astype(np.float64) * vs.astype(np.float64)[..., None])
         for b, L in enumerate(lens):
             s0 = max(0, L - window) if window else 0
             idx = torch.arange(s0, L)

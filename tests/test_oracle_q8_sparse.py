@@ -17,7 +17,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import bits, paged_from_contiguous, rand_bf16
+from helpers import bits, code_values, paged_from_contiguous, rand_bf16, stored_codes
 
 
 def _bf16_bits_of(values: np.ndarray) -> np.ndarray:
@@ -27,14 +27,15 @@ def _bf16_bits_of(values: np.ndarray) -> np.ndarray:
 
 
 def _pow2_pool(nb, hkv, d, rng):
-    """INT8 codes and power-of-two row scales, and the bf16 pool of the same values."""
-    codes = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
+    """INT8 codes (stored as code + 128) and power-of-two row scales, and the bf16 pool of the
+    same values."""
+    codes = rng.integers(-127, 128, size=(nb, hkv, 16, d))
     scales = (2.0 ** rng.integers(-9, 2, size=(nb, hkv, 16))).astype(np.float32)
-    return codes, scales, _bf16_bits_of(codes.astype(np.float32) * scales[..., None])
+    return stored_codes(codes), scales, _bf16_bits_of(codes.astype(np.float32) * scales[..., None])
 
 
-def _dequant(codes, scales):
-    return codes.astype(np.float64) * scales.astype(np.float64)[..., None]
+def _dequant(stored, scales):
+    return code_values(stored).astype(np.float64) * scales.astype(np.float64)[..., None]
 
 
 @pytest.mark.parametrize("hq,hkv,d,window", [(8, 2, 64, 0), (12, 2, 128, 0), (8, 8, 64, 21), (32, 8, 128, 0)])
@@ -100,8 +101,8 @@ def _compact_case(rng, d, nb_src=40, nb_dst=24):
             n = kept_lens[b]
             kept[b, g, :n] = np.sort(rng.choice(lens[b], size=n, replace=False)) if n else []
     dbt = rng.permutation(nb_dst)[: B * 3].reshape(B, 3).astype(np.int32)
-    dk = rng.integers(-127, 128, size=(nb_dst, hkv, 16, d)).astype(np.int8)
-    dv = rng.integers(-127, 128, size=(nb_dst, hkv, 16, d)).astype(np.int8)
+    dk = stored_codes(rng.integers(-127, 128, size=(nb_dst, hkv, 16, d)))
+    dv = stored_codes(rng.integers(-127, 128, size=(nb_dst, hkv, 16, d)))
     dks = rng.random((nb_dst, hkv, 16)).astype(np.float32)
     dvs = rng.random((nb_dst, hkv, 16)).astype(np.float32)
     return dict(dk=dk, dv=dv, dks=dks, dvs=dvs, dbt=dbt, sk=sk, sv=sv, sks=sks, svs=svs, sbt=sbt,
@@ -167,8 +168,8 @@ def test_rolling_admit_q8_follows_the_bf16_admission():
     B, hkv, d, cap, n_sink, n_recent = 3, 2, 64, 24, 2, 4
     nb = 10
     bt = rng.permutation(nb)[: B * 2].reshape(B, 2).astype(np.int32)
-    kc = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
-    vc = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
+    kc = stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d)))
+    vc = stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d)))
     ks = rng.random((nb, hkv, 16)).astype(np.float32)
     vs = rng.random((nb, hkv, 16)).astype(np.float32)
     kb = bits(rand_bf16((nb, hkv, 16, d), g))
@@ -210,7 +211,7 @@ def test_rolling_admit_q8_follows_the_bf16_admission():
 
 def test_rolling_admit_q8_refuses_a_non_finite_row():
     B, hkv, d, cap = 1, 1, 64, 16
-    kc = np.zeros((2, hkv, 16, d), np.int8)
+    kc = np.zeros((2, hkv, 16, d), np.uint8)
     ks = np.zeros((2, hkv, 16), np.float32)
     x = np.ones((B, hkv, d), np.float32)
     x[0, 0, 5] = np.inf
@@ -253,8 +254,8 @@ def test_sparse_q8_with_every_token_kept_equals_paged_q8():
     rng = np.random.default_rng(11)
     lens = [37, 64, 1]
     hq, hkv, d, nb = 8, 2, 64, 20
-    kc = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
-    vc = rng.integers(-127, 128, size=(nb, hkv, 16, d)).astype(np.int8)
+    kc = stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d)))
+    vc = stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d)))
     ks = rng.random((nb, hkv, 16)).astype(np.float32)
     vs = rng.random((nb, hkv, 16)).astype(np.float32)
     g = torch.Generator().manual_seed(12)

@@ -389,10 +389,13 @@ def run_ours(args):
 
 
 def run_e2e(pkv, copies, host0, dev, stream, ws, args):
-    """Same step through the public API with the step's inputs copied from pinned host
-    memory and the result read back, inside the timed region.  The step's inputs (q, the new
-    K/V rows, block tables, lengths) sit in one pinned host buffer at 256-byte aligned offsets
-    and cross in one copy; the call takes views into its device copy."""
+    """Same step through the public API with the step's inputs taken from pinned host memory
+    and the result returned to pinned host memory, inside the timed region, the steps in order.
+    The step's inputs (q, the new K/V rows, block tables, lengths) sit in one pinned host buffer
+    at 256-byte aligned offsets.  The figure: the call reads them there and writes out into a
+    pinned host buffer, its kernels crossing the host link (NVLink-C2C) in place, so no copy
+    separates one step's kernels from the next.  Beside it (`copies`): one host-to-device copy of
+    the packed inputs, the call on views into the device copy, one device-to-host copy of out."""
     names = ("q", "k_new", "v_new", "block_tables", "context_lens")
     offs, at = {}, 0
     for n in names:
@@ -423,7 +426,7 @@ def run_e2e(pkv, copies, host0, dev, stream, ws, args):
     h2d = sum(host0[n].numel() * host0[n].element_size() for n in names)
     d2h = out.numel() * out.element_size()
 
-    def one(i):
+    def one_copies(i):
         c, di = copies[i % ROTATE], dev_in[i % 2]
         dev_buf[i % 2].copy_(hosts[i % ROTATE], non_blocking=True)
         pkv.paged_decode_attention_append(di["q"], c["k_cache"], c["v_cache"], di["k_new"], di["v_new"],
@@ -431,31 +434,58 @@ def run_e2e(pkv, copies, host0, dev, stream, ws, args):
                                           workspace=ws, stream=stream)
         out_h.copy_(out, non_blocking=True)
 
-    for i in range(args.warmup):
-        one(i)
-    torch.cuda.synchronize(dev)
-    # the K steps in 5 consecutive blocks, each between two events; the median block is the
-    # figure (one stall of the shared host inside a block moves only that block)
-    nblk = 5 if args.steps >= 10 else 1
-    per = [args.steps // nblk + (1 if b < args.steps % nblk else 0) for b in range(nblk)]
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nblk + 1)]
-    ev[0].record(stream)
-    i = 0
-    for b in range(nblk):
-        for _ in range(per[b]):
+    # in place: the call reads the pinned input buffer and writes a pinned output buffer (two,
+    # alternating); its inputs are final before the previous step (that step appended into
+    # another pool copy), so it declares them ready like the device-timed steps
+    host_in = [views(h) for h in hosts]
+    outs_h = [torch.empty((copies[0]["q"].shape), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+
+    def one_in_place(i):
+        c, hv = copies[i % ROTATE], host_in[i % ROTATE]
+        pkv.paged_decode_attention_append(hv["q"], c["k_cache"], c["v_cache"], hv["k_new"], hv["v_new"],
+                                          hv["block_tables"], hv["context_lens"], c["scale"], out=outs_h[i % 2],
+                                          workspace=ws, stream=stream, inputs_ready=True)
+
+    def timed(one):
+        for i in range(args.warmup):
             one(i)
-            i += 1
-        ev[b + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        # the K steps in 5 consecutive blocks, each between two events; the median block is the
+        # figure (one stall of the shared host inside a block moves only that block)
+        nblk = 5 if args.steps >= 10 else 1
+        per = [args.steps // nblk + (1 if b < args.steps % nblk else 0) for b in range(nblk)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(nblk + 1)]
+        ev[0].record(stream)
+        i = 0
+        for b in range(nblk):
+            for _ in range(per[b]):
+                one(i)
+                i += 1
+            ev[b + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        blocks = [ev[b].elapsed_time(ev[b + 1]) / per[b] for b in range(nblk)]
+        return (statistics.median(blocks), ev[0].elapsed_time(ev[nblk]) / args.steps, blocks,
+                f"median of {nblk} consecutive blocks of the {args.steps} steps")
+
+    ms_c, mean_c, blocks_c, how = timed(one_copies)
+    ms, mean, blocks, how = timed(one_in_place)
+    # the in-place step's result equals the copy path's for the same inputs (the append rewrites
+    # the same rows, so repeating a step leaves the pools as they were)
+    one_copies(0)
+    one_in_place(0)
     torch.cuda.synchronize(dev)
-    blocks = [ev[b].elapsed_time(ev[b + 1]) / per[b] for b in range(nblk)]
-    ms = statistics.median(blocks)
-    mean = ev[0].elapsed_time(ev[nblk]) / args.steps
+    if not torch.equal(outs_h[0], out_h):
+        raise RuntimeError("the in-place end-to-end step differs from the copy path")
     B = copies[0]["q"].shape[0]
     return {"value": round(B / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step_mean": round(mean, 5), "blocks_ms": [round(x, 5) for x in blocks],
-            "timing": f"median of {nblk} consecutive blocks of the {args.steps} steps",
-            "copies_per_step": "one host-to-device copy of the packed inputs, one device-to-host copy of out"}
+            "ms_per_step_mean": round(mean, 5), "blocks_ms": [round(x, 5) for x in blocks], "timing": how,
+            "transfers_per_step": "the kernels read the step's inputs from the pinned host buffer and write out "
+                                  "into a pinned host buffer over the host link (NVLink-C2C), in place",
+            "copies": {"value": round(B / (ms_c * 1e-3), 1), "ms_per_step": round(ms_c, 5),
+                       "ms_per_step_mean": round(mean_c, 5), "blocks_ms": [round(x, 5) for x in blocks_c],
+                       "transfers_per_step": "one host-to-device copy of the packed inputs, one device-to-host "
+                                             "copy of out, the call between them on the device copy"}}
 
 
 def cpu_model() -> str:

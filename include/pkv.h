@@ -568,6 +568,24 @@ int pkv_paged_decode_attention_fixed_scratch(void* out, const void* q, const voi
                                              int32_t* error_word, void* stream);
 
 /*
+ * pkv_device_alias -- the device address of pinned (page-locked) host memory, for the decode
+ * calls' arguments that their kernels reach with ordinary loads and stores: q, k_new, v_new,
+ * block_tables, context_lens and out of every *_decode_attention* call may be pinned host
+ * memory passed by this address (not the K/V pools, read through tensor maps, nor the
+ * workspace, error_word or score buffers).  The kernels then read and write that memory in
+ * place over the host link (NVLink-C2C on a Grace-Blackwell node), so a step's inputs need no
+ * copy to the device and its output none back, and consecutive calls stay adjacent on the
+ * stream.  The memory must stay pinned and unchanged by the host until the calls that use it
+ * have completed.
+ *   host_ptr   : an address inside memory allocated with cudaHostAlloc / cudaMallocHost (or
+ *                registered with cudaHostRegister, mapped).
+ *   device_ptr : receives the device address (on unified-addressing systems the same value).
+ * Returns PKV_OK, PKV_ERR_NULL_POINTER, or PKV_ERR_ARGUMENT when the memory is not pinned and
+ * mapped for the current device (*device_ptr is then NULL).  Host only; no device work.
+ */
+int pkv_device_alias(const void* host_ptr, void** device_ptr);
+
+/*
  * pkv_read_error -- synchronise `stream`, then return the device error word's value
  * (PKV_DEV_*), or a negative host status if it cannot be read.  If `clear` is non-zero
  * the word is reset to 0 afterwards.  Diagnostic; not for the hot loop.

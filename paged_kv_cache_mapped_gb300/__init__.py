@@ -35,7 +35,14 @@ _COMPACT_READY = header_constants()["PKV_COMPACT_INPUTS_READY"]
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    if t is None:
+        return None
+    if not t.is_cuda:  # pinned host memory (admitted by _need): its device address
+        base = t.untyped_storage().data_ptr()
+        d = ctypes.c_void_p()
+        check("pkv_device_alias", load().pkv_device_alias(ctypes.c_void_p(base), ctypes.byref(d)))
+        return ctypes.c_void_p(d.value + (t.data_ptr() - base))
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream, device):
@@ -43,18 +50,21 @@ def _stream(stream, device):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _need(t, name, dtype, ndim, device=None):
+def _need(t, name, dtype, ndim, device=None, host_ok=False):
+    """host_ok: the argument may also be pinned host memory, which the kernels reach in place."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must live on a CUDA device (the library has no CPU path)")
+    on_host = host_ok and not t.is_cuda and t.is_pinned()
+    if not t.is_cuda and not on_host:
+        where = "a CUDA device or pinned host memory" if host_ok else "a CUDA device"
+        raise ValueError(f"{name} must live on {where} (the library has no CPU path)")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
-    if device is not None and t.device != device:
+    if device is not None and not on_host and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
@@ -162,9 +172,9 @@ def _flags(inputs_ready: bool) -> int:
 def _decode_inputs(q, k_cache, v_cache, block_tables, context_lens):
     nb, hkv, d = _pool_dims(k_cache, v_cache)
     dev = k_cache.device
-    _need(q, "q", torch.bfloat16, 3, dev)
-    _need(block_tables, "block_tables", torch.int32, 2, dev)
-    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(q, "q", torch.bfloat16, 3, dev, host_ok=True)
+    _need(block_tables, "block_tables", torch.int32, 2, dev, host_ok=True)
+    _need(context_lens, "context_lens", torch.int32, 1, dev, host_ok=True)
     B, hq, dq = q.shape
     if dq != d:
         raise ValueError("q head_dim differs from the pools'")
@@ -173,17 +183,18 @@ def _decode_inputs(q, k_cache, v_cache, block_tables, context_lens):
     return _dims(B, hq, hkv, d, nb, block_tables.shape[1]), dev
 
 
-def _out_ws(q, out, workspace, nbytes):
+def _out_ws(q, out, workspace, nbytes, dev):
+    """out (given: on dev or in pinned host memory; else allocated on dev) and the workspace."""
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=dev)
     else:
-        _need(out, "out", torch.bfloat16, 3, q.device)
+        _need(out, "out", torch.bfloat16, 3, dev, host_ok=True)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
     if workspace is None:
-        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
     else:
-        _need(workspace, "workspace", torch.uint8, 1, q.device)
+        _need(workspace, "workspace", torch.uint8, 1, dev)
     return out, workspace
 
 
@@ -192,7 +203,7 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     """softmax(scale * q K^T) V over the paged cache; returns out [B, Hq, d] bf16."""
     dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
-    out, workspace = _out_ws(q, out, workspace, nbytes)
+    out, workspace = _out_ws(q, out, workspace, nbytes, dev)
     check("pkv_paged_decode_attention", load().pkv_paged_decode_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
@@ -203,9 +214,9 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
 def _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens):
     nb, hkv, d = _q8_pool_dims(k_codes, v_codes, k_scales, v_scales)
     dev = k_codes.device
-    _need(q, "q", torch.bfloat16, 3, dev)
-    _need(block_tables, "block_tables", torch.int32, 2, dev)
-    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(q, "q", torch.bfloat16, 3, dev, host_ok=True)
+    _need(block_tables, "block_tables", torch.int32, 2, dev, host_ok=True)
+    _need(context_lens, "context_lens", torch.int32, 1, dev, host_ok=True)
     B, hq, dq = q.shape
     if dq != d:
         raise ValueError("q head_dim differs from the pools'")
@@ -219,7 +230,7 @@ def paged_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_tab
     """paged_decode_attention over INT8 pools (each element code * its row's scale)."""
     dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
-    out, workspace = _out_ws(q, out, workspace, nbytes)
+    out, workspace = _out_ws(q, out, workspace, nbytes, dev)
     check("pkv_paged_decode_attention_q8", load().pkv_paged_decode_attention_q8(
         _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_tables),
         _ptr(context_lens), float(scale), int(window), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
@@ -267,12 +278,12 @@ def paged_decode_attention_append(q, k_cache, v_cache, k_new, v_new, block_table
     (context_lens[b] - 1, through the block table) and attend, in one kernel.  Same result as
     kv_append followed by paged_decode_attention for that slot layout."""
     dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
-    _need(k_new, "k_new", torch.bfloat16, 3, dev)
-    _need(v_new, "v_new", torch.bfloat16, 3, dev)
+    _need(k_new, "k_new", torch.bfloat16, 3, dev, host_ok=True)
+    _need(v_new, "v_new", torch.bfloat16, 3, dev, host_ok=True)
     if k_new.shape != (dims.batch, dims.num_kv_heads, dims.head_dim) or v_new.shape != k_new.shape:
         raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
-    out, workspace = _out_ws(q, out, workspace, nbytes)
+    out, workspace = _out_ws(q, out, workspace, nbytes, dev)
     check("pkv_paged_decode_attention_append", load().pkv_paged_decode_attention_append(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
         _ptr(block_tables), _ptr(context_lens), float(scale), int(window), _ptr(workspace),
@@ -315,12 +326,12 @@ def paged_decode_attention_scores(q, k_cache, v_cache, block_tables, context_len
     if (k_new is None) != (v_new is None):
         raise ValueError("give both k_new and v_new, or neither")
     if k_new is not None:
-        _need(k_new, "k_new", torch.bfloat16, 3, dev)
-        _need(v_new, "v_new", torch.bfloat16, 3, dev)
+        _need(k_new, "k_new", torch.bfloat16, 3, dev, host_ok=True)
+        _need(v_new, "v_new", torch.bfloat16, 3, dev, host_ok=True)
         if k_new.shape != (dims.batch, dims.num_kv_heads, dims.head_dim) or v_new.shape != k_new.shape:
             raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
-    out, workspace = _out_ws(q, out, workspace, nbytes)
+    out, workspace = _out_ws(q, out, workspace, nbytes, dev)
     check("pkv_paged_decode_attention_scores", load().pkv_paged_decode_attention_scores(
         _ptr(out), _ptr(lse), _ptr(score_accum), _ptr(logits), int(stride), _ptr(q), _ptr(k_cache),
         _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(context_lens), float(scale),
@@ -335,12 +346,12 @@ def paged_decode_attention_append_q8(q, k_codes, v_codes, k_scales, v_scales, k_
     """kv_append_q8 of k_new/v_new [B, Hkv, d] (bf16) at each sequence's position L_b - 1, fused
     into paged_decode_attention_q8 over the updated INT8 pools."""
     dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
-    _need(k_new, "k_new", torch.bfloat16, 3, dev)
-    _need(v_new, "v_new", torch.bfloat16, 3, dev)
+    _need(k_new, "k_new", torch.bfloat16, 3, dev, host_ok=True)
+    _need(v_new, "v_new", torch.bfloat16, 3, dev, host_ok=True)
     if k_new.shape != (dims.batch, dims.num_kv_heads, dims.head_dim) or v_new.shape != k_new.shape:
         raise ValueError("k_new/v_new must be [B, Hkv, head_dim]")
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
-    out, workspace = _out_ws(q, out, workspace, nbytes)
+    out, workspace = _out_ws(q, out, workspace, nbytes, dev)
     check("pkv_paged_decode_attention_append_q8", load().pkv_paged_decode_attention_append_q8(
         _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(k_new), _ptr(v_new),
         _ptr(block_tables), _ptr(context_lens), float(scale), int(window), _ptr(workspace), workspace.numel(),
@@ -359,7 +370,7 @@ def sparse_decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, block_ta
         raise ValueError("kept_index_lists must be [B, Hkv, max_kept] and kept_lens [B]")
     max_kept = kept_index_lists.shape[2]
     nbytes = int(load().pkv_sparse_decode_workspace_bytes(ctypes.byref(dims), max_kept))
-    out, workspace = _out_ws(q, out, workspace, nbytes)
+    out, workspace = _out_ws(q, out, workspace, nbytes, dev)
     check("pkv_sparse_decode_attention_q8", load().pkv_sparse_decode_attention_q8(
         _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_tables),
         _ptr(context_lens), _ptr(kept_index_lists), _ptr(kept_lens), max_kept, float(scale), _ptr(workspace),
@@ -375,7 +386,7 @@ def paged_decode_attention_scores_q8(q, k_codes, v_codes, k_scales, v_scales, bl
     dims, dev = _q8_decode_inputs(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens)
     stride, lse, logits = _score_buffers(dims, dev, score_accum, lse, logits)
     nbytes = int(load().pkv_decode_workspace_bytes(ctypes.byref(dims)))
-    out, workspace = _out_ws(q, out, workspace, nbytes)
+    out, workspace = _out_ws(q, out, workspace, nbytes, dev)
     check("pkv_paged_decode_attention_scores_q8", load().pkv_paged_decode_attention_scores_q8(
         _ptr(out), _ptr(lse), _ptr(score_accum), _ptr(logits), int(stride), _ptr(q), _ptr(k_codes), _ptr(v_codes),
         _ptr(k_scales), _ptr(v_scales), _ptr(block_tables), _ptr(context_lens), float(scale), int(window),
@@ -417,8 +428,8 @@ def _rolling_dims(nb, hkv, d, dev, block_tables, slot_pos, slot_score, kept_lens
     _need(slot_score, "slot_score", torch.float32, 3, dev)
     _need(kept_lens, "kept_lens", torch.int32, 1, dev)
     _need(context_lens, "context_lens", torch.int32, 1, dev)
-    _need(k_new, "k_new", torch.bfloat16, 3, dev)
-    _need(v_new, "v_new", torch.bfloat16, 3, dev)
+    _need(k_new, "k_new", torch.bfloat16, 3, dev, host_ok=True)
+    _need(v_new, "v_new", torch.bfloat16, 3, dev, host_ok=True)
     B = slot_pos.shape[0]
     if slot_pos.shape[1] != hkv or slot_score.shape != slot_pos.shape:
         raise ValueError("slot_pos and slot_score must be [B, Hkv, capacity]")
@@ -462,7 +473,7 @@ def sparse_decode_attention(q, k_cache, v_cache, block_tables, context_lens, kep
         raise ValueError("kept_index_lists must be [B, Hkv, max_kept]")
     max_kept = kept_index_lists.shape[2]
     nbytes = int(load().pkv_sparse_decode_workspace_bytes(ctypes.byref(dims), max_kept))
-    out, workspace = _out_ws(q, out, workspace, nbytes)
+    out, workspace = _out_ws(q, out, workspace, nbytes, dev)
     check("pkv_sparse_decode_attention", load().pkv_sparse_decode_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         _ptr(kept_index_lists), _ptr(kept_lens), max_kept, float(scale), _ptr(workspace),

@@ -89,6 +89,7 @@ def load():
             "pkv_kv_compact": (I32, [P, P, P, I32, I32, P, P, P, P, P, P, I32, D, U32, P, P]),
             "pkv_paged_decode_attention_fixed_scratch": (I32, [P, P, P, P, P, P, F32, I32, D, P, P]),
             "pkv_read_error": (I32, [P, I32, P]),
+            "pkv_device_alias": (I32, [P, ctypes.POINTER(ctypes.c_void_p)]),
             "pkv_status_string": (ctypes.c_char_p, [I32]),
             "pkv_device_error_string": (ctypes.c_char_p, [I32]),
         }

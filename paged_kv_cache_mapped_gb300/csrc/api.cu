@@ -702,6 +702,25 @@ int pkv_kv_rolling_admit_q8(void* k_codes, void* v_codes, float* k_scales, float
       n_sink, n_recent, error_word, static_cast<cudaStream_t>(stream)));
 }
 
+int pkv_device_alias(const void* host_ptr, void** device_ptr) {
+  if (host_ptr == nullptr || device_ptr == nullptr) return PKV_ERR_NULL_POINTER;
+  *device_ptr = nullptr;
+  // pinned (page-locked) host memory only: a system whose GPU reaches pageable memory too (a
+  // Grace-Blackwell node) would map that as well, but its pages may move or be swapped out
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, host_ptr) != cudaSuccess || at.type != cudaMemoryTypeHost) {
+    (void)cudaGetLastError();  // a host error, not a sticky one
+    return PKV_ERR_ARGUMENT;
+  }
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void*>(host_ptr), 0) != cudaSuccess || d == nullptr) {
+    (void)cudaGetLastError();
+    return PKV_ERR_ARGUMENT;
+  }
+  *device_ptr = d;
+  return PKV_OK;
+}
+
 int pkv_read_error(int32_t* error_word, int32_t clear, void* stream) {
   if (error_word == nullptr) return PKV_ERR_NULL_POINTER;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

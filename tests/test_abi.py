@@ -21,7 +21,7 @@ def _dims(B=4, hq=32, hkv=8, d=128, bs=16, nb=1000, mb=64):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _lib.header_functions()
-    assert len(declared) == 22
+    assert len(declared) == 23
     nm = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     for name in declared:
@@ -211,3 +211,16 @@ def test_binding_rejects_cpu_tensors():
     lens = torch.ones(2, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         pkv.paged_decode_attention(q, kc, kc, bt, lens, 0.125)
+
+
+def test_device_alias_refuses_null_and_unpinned_memory(lib):
+    """pkv_device_alias: NULL arguments, and host memory that is not pinned (here: ordinary
+    ctypes memory, or no device at all), come back as host errors with the output cleared; no
+    device work is done."""
+    c = _lib.header_constants()
+    d = ctypes.c_void_p(0x1234)
+    assert lib.pkv_device_alias(None, ctypes.byref(d)) == c["PKV_ERR_NULL_POINTER"]
+    buf = ctypes.create_string_buffer(64)
+    assert lib.pkv_device_alias(ctypes.cast(buf, ctypes.c_void_p), None) == c["PKV_ERR_NULL_POINTER"]
+    assert lib.pkv_device_alias(ctypes.cast(buf, ctypes.c_void_p), ctypes.byref(d)) == c["PKV_ERR_ARGUMENT"]
+    assert d.value is None

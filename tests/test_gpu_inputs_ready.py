@@ -573,3 +573,91 @@ def test_compact_flagged_in_graph_and_errors_after_the_wait(q8):
         _compact_call(c, pools, dbt, q8, True, err)
         torch.cuda.synchronize()
         assert pkv.read_error(err) == C[code], field
+
+
+def test_llama8b_headline_graph_full_size():
+    """The headline's launch configuration: llama8b-shaped layers (full size) over four pool
+    copies, fused append + decode declaring inputs ready, captured in one CUDA graph: every
+    output equal bit for bit to the eager undeclared call, pools holding the appended rows, and
+    sampled rows of one layer within the gate of the oracle."""
+    wl = W.WORKLOADS["llama8b"]
+    cases = [W.make_layer(wl, layer=r, device=DEV, device_rng=True) for r in range(4)]
+    need = pkv.decode_workspace_bytes(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                      cases[0]["num_blocks"], cases[0]["max_blocks_per_seq"])
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    pools0 = [(c["k_cache"].clone(), c["v_cache"].clone()) for c in cases]
+    eager = [_append_call(c, torch.empty_like(c["q"]), ws, False).clone() for c in cases]
+    torch.cuda.synchronize()
+    appended = [(c["k_cache"].clone(), c["v_cache"].clone()) for c in cases]
+    for c, (k0, v0) in zip(cases, pools0):
+        c["k_cache"].copy_(k0)
+        c["v_cache"].copy_(v0)
+    outs = [torch.full_like(c["q"], float("nan")) for c in cases]
+    s = torch.cuda.Stream(DEV)
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for c, o in zip(cases, outs):
+                _append_call(c, o, ws, True, stream=s)
+        graph.replay()
+        torch.cuda.synchronize()
+    for i, (c, o, e, (ka, va)) in enumerate(zip(cases, outs, eager, appended)):
+        assert torch.equal(o, e), f"copy {i}"
+        assert torch.equal(c["k_cache"], ka) and torch.equal(c["v_cache"], va)
+    rows = _sample_rows(wl.batch, wl.num_q_heads, 24, seed=61)
+    ref = _oracle(cases[2], rows=rows, kc=bits(appended[2][0]), vc=bits(appended[2][1]))
+    assert_attn_close(outs[2].view(-1, wl.head_dim)[torch.tensor(rows, device=DEV)], ref, "llama8b graph, copy 2")
+
+
+def test_sparse_layers_flagged_pipeline_full_size():
+    """Two sparse layers of the layer-wise sparse workload at full size, as the bench runs them:
+    the selections declaring their scores ready back to back, the first compaction undeclared
+    (it follows the selections) and the second declared, and each layer's gather decode
+    declared; every result equal bit for bit to the undeclared pipeline, the kept lists to the
+    oracle's, and sampled rows of the second layer within the gate of the oracle."""
+    wl = W.WORKLOADS["sparse"]
+    lens = W.context_lengths(wl)
+    layers = [W.make_layer(wl, layer=l, device=DEV, device_rng=True) for l in (4, 5)]
+    scores = [W.make_scores(wl, l, lens, device=DEV, device_rng=True) for l in (4, 5)]
+    dbt, dnb = W.compact_tables(wl.keep_max, wl.batch, seed=5)
+    dbt = dbt.to(DEV)
+    K, hkv, d = wl.keep_max, wl.num_kv_heads, wl.head_dim
+    ws = torch.zeros(pkv.sparse_decode_workspace_bytes(wl.batch, wl.num_q_heads, hkv, d, layers[0]["num_blocks"],
+                                                       layers[0]["max_blocks_per_seq"], K),
+                     dtype=torch.uint8, device=DEV)
+
+    def pipeline(flagged):
+        err = pkv.new_error_word(DEV)
+        kept = [pkv.kv_select_topk(sc, c["context_lens"], wl.n_sink, wl.n_recent, wl.k_top, error_word=err,
+                                   inputs_ready=flagged) for sc, c in zip(scores, layers)]
+        comp = []
+        for i, (c, (kp, kl)) in enumerate(zip(layers, kept)):
+            dk = torch.zeros((dnb, hkv, 16, d), dtype=torch.bfloat16, device=DEV)  # untouched slots stay 0
+            dv = torch.zeros_like(dk)
+            pkv.kv_compact(dk, dv, dbt, c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"], kp, kl,
+                           error_word=err, inputs_ready=flagged and i > 0)
+            comp.append((dk, dv))
+        outs = [pkv.sparse_decode_attention(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["context_lens"],
+                                            kp, kl, wl.scale, workspace=ws, error_word=err, inputs_ready=flagged)
+                .clone() for c, (kp, kl) in zip(layers, kept)]
+        torch.cuda.synchronize()
+        assert pkv.read_error(err) == 0
+        return kept, comp, outs
+
+    kf, cf, of = pipeline(True)
+    kp_, cp_, op_ = pipeline(False)
+    for i in range(2):
+        okl = kp_[i][1].cpu().numpy()
+        for b in range(wl.batch):
+            assert torch.equal(kf[i][0][b, :, :int(okl[b])], kp_[i][0][b, :, :int(okl[b])])
+        assert torch.equal(kf[i][1], kp_[i][1])
+        assert torch.equal(cf[i][0], cp_[i][0]) and torch.equal(cf[i][1], cp_[i][1])
+        assert torch.equal(of[i], op_[i])
+    okept, okl = oracle.select_topk(scores[1].cpu().numpy(), lens.numpy(), wl.n_sink, wl.n_recent, wl.k_top)
+    assert np.array_equal(kf[1][0].cpu().numpy(), okept) and np.array_equal(kf[1][1].cpu().numpy(), okl)
+    rows = sorted({0, 31, 257, 511} | set(range(16 * 32 - 3, 16 * 32)))
+    c = layers[1]
+    ref = oracle.sparse_decode(bits(c["q"]), bits(c["k_cache"]), bits(c["v_cache"]), c["block_tables"].cpu().numpy(),
+                               lens.numpy(), okept, okl, wl.scale, rows=rows)
+    assert_attn_close(of[1].view(-1, d)[torch.tensor(rows, device=DEV)], ref, "sparse layer 5, flagged gather")

@@ -449,9 +449,9 @@ def paged_decode_attention_fixed_scratch(q, k_cache, v_cache, block_tables, cont
     given, is allocated here by torch; pass it to allocate nothing.)"""
     dims, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=dev)
     else:
-        _need(out, "out", torch.bfloat16, 3, dev)
+        _need(out, "out", torch.bfloat16, 3, dev, host_ok=True)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
     check("pkv_paged_decode_attention_fixed_scratch",

@@ -170,3 +170,19 @@ def test_pageable_host_memory_refused():
     assert lib.pkv_device_alias(ctypes.cast(buf, ctypes.c_void_p), ctypes.byref(d)) == \
         pkv.header_constants()["PKV_ERR_ARGUMENT"]
     assert d.value is None
+
+
+def test_fixed_scratch_with_host_inputs():
+    """The no-workspace entry point with pinned host inputs: out allocated on the device when not
+    given, or a pinned host out; both equal to the device-input call bit for bit."""
+    c = _case([600, 33, 1], 16, 4, 128, seed=17)
+    d, h = _placed(c, "device"), _placed(c, "host")
+    ref = pkv.paged_decode_attention_fixed_scratch(d["q"], c["k_cache"], c["v_cache"], d["block_tables"],
+                                                   d["context_lens"], c["scale"])
+    got = pkv.paged_decode_attention_fixed_scratch(h["q"], c["k_cache"], c["v_cache"], h["block_tables"],
+                                                   h["context_lens"], c["scale"])
+    got_h = pkv.paged_decode_attention_fixed_scratch(h["q"], c["k_cache"], c["v_cache"], h["block_tables"],
+                                                     h["context_lens"], c["scale"], out=_out(c, "host"))
+    torch.cuda.synchronize()
+    assert got.is_cuda and not got_h.is_cuda
+    assert torch.equal(bits_t(got), bits_t(ref)) and torch.equal(bits_t(got_h), bits_t(ref.cpu()))

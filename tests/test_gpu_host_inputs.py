@@ -3,8 +3,9 @@
 result is bit-identical to the same call on device copies of those tensors -- which the other
 test files check against the fp64 oracle -- and within the gate of the oracle itself here.
 Covered: the fused append + decode (bf16 and INT8 pools; the pools end identical), the plain
-decode with a window, the gather form of the sparse decode, calls declaring their inputs ready
-back to back and captured in a CUDA graph, and the refusal of pageable host memory."""
+decode with a window, the gather form of the sparse decode, the no-workspace entry point, calls
+declaring their inputs ready back to back and captured in a CUDA graph, and the refusal of
+pageable host memory."""
 import numpy as np
 import pytest
 import torch

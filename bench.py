@@ -991,7 +991,7 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
                                          "ms_without_inputs_ready": round(ms_gat_plain, 4),
                                          "launch": "10 calls in one CUDA graph, inputs_ready"}
     with torch.cuda.stream(gstream):
-        res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, comp[0], dbt, klens, ws, out))
+        res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, comp[:4], dbt, klens, ws, out))
     # the same layer over INT8 pools (random codes, row scales ~ Exp): compaction and rolling
     gq = torch.Generator(device=dev).manual_seed(43)
     codes = lambda n: torch.randint(1, 256, (n, hkv, 16, d), generator=gq, device=dev, dtype=torch.uint8)
@@ -1005,7 +1005,7 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
     # INT8 compactions as the bf16 ones: n_cmp layers, each its own source and compact pools
     s8l = [s8] + [{"kq": codes(snb), "vq": codes(snb), "ks": rscales(snb), "vs": rscales(snb)}
                   for _ in range(n_cmp - 1)]
-    d8l = [d8] + [{"kq": codes(dnb), "vq": codes(dnb), "ks": rscales(dnb), "vs": rscales(dnb)}
+    d8l = [d8] + [{"q": d8["q"], "kq": codes(dnb), "vq": codes(dnb), "ks": rscales(dnb), "vs": rscales(dnb)}
                   for _ in range(n_cmp - 1)]
     cmp8_layer = [lambda s_=s_, d_=d_, t_=t_, r=r: pkv.kv_compact_q8(d_["kq"], d_["vq"], d_["ks"], d_["vs"], dbt,
                                                                      s_["kq"], s_["vq"], s_["ks"], s_["vs"], t_[0],
@@ -1018,7 +1018,7 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
         ms_gat8 = _graph_time([gat8] * 10, args.warmup, 5, dev, gstream) / 10
         ms_cmp8 = _graph_time(cmp8_layer[:n_cmp] * 3, args.warmup, 5, dev, gstream) / (3 * n_cmp)
         ms_cmp8_plain = _graph_time(cmp8_layer[n_cmp:] * 3, args.warmup, 5, dev, gstream) / (3 * n_cmp)
-        res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, d8, dbt, klens, ws, out, q8=True))
+        res.update(_rolling_rows(pkv, wl, dev, gstream, lens, scores, d8l, dbt, klens, ws, out, q8=True))
     cmp8_bytes = B * hkv * K * (d + 4) * 2 * 2
     gat8_bytes = B * hkv * K * (d + 4) * 2 + 2 * B * hq * d * 2
     res["sparse_layer_gather_decode_int8"] = {"ms": round(ms_gat8, 4), "bytes": gat8_bytes,
@@ -1032,13 +1032,16 @@ def _sparse_step(pkv, W, dev, stream, args, hbm):
     return res
 
 
-def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, calls=10, trials=5, q8=False):
-    """One sparse layer kept at its fixed budget by rolling admission.  The state is a top-k
-    selection over the first L - 1 tokens; call i admits token L - 1 + i (its own row of context
-    lengths), then, in the layer step, attends over the compact pool with the scores added to
-    the slot scores.  Admission changes the state, so the `calls` calls are one CUDA graph
-    replayed once per trial from a restored state.  q8: the compact pool is INT8 (c holds
-    kq, vq, ks, vs) and the rows are named *_int8."""
+def _rolling_rows(pkv, wl, dev, gstream, lens, scores, pools, dbt, klens, ws, out, calls=10, trials=5, q8=False):
+    """Sparse layers kept at their fixed budget by rolling admission, stepped as a decode step
+    steps them: `pools` are the layers' compact pools (each its own; q8: kq, vq, ks, vs), each
+    layer's state a top-k selection over the first L - 1 tokens.  Step i admits token L - 1 + i
+    (its own row of context lengths) into every layer, then, in the layer step, attends over
+    that layer's compact pool with the scores added to its slot scores.  The admissions declare
+    their inputs ready: a layer's slot state was last written by its own score pass of the
+    previous step, with the other layers' work in between (the undeclared calls beside).
+    Admission changes the state, so the calls are one CUDA graph replayed once per trial from a
+    restored state.  Rows named *_int8 for q8."""
     B, hq, hkv, d, K = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.keep_max
     prev = (lens - 1).to(dev)
     kept = torch.empty((B, hkv, K), dtype=torch.int32, device=dev)
@@ -1049,25 +1052,28 @@ def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, c
     sc0 = torch.gather(scores, 2, kept.to(torch.int64))
     kl0 = kl.clone()
     g = torch.Generator(device=dev).manual_seed(11)
-    k_new = torch.randn((B, hkv, d), generator=g, device=dev).to(torch.bfloat16)
-    v_new = torch.randn((B, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    n_layers = len(pools)
+    news = [(torch.randn((B, hkv, d), generator=g, device=dev).to(torch.bfloat16),
+             torch.randn((B, hkv, d), generator=g, device=dev).to(torch.bfloat16)) for _ in pools]
     lens_rows = (lens.to(dev).view(1, B) + torch.arange(calls, dtype=torch.int32, device=dev).view(-1, 1)).contiguous()
-    pos, sc, kls = pos0.clone(), sc0.clone(), kl0.clone()
+    states = [(pos0.clone(), sc0.clone(), kl0.clone()) for _ in pools]
     lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
     logits = torch.empty((B, hq, K), dtype=torch.float32, device=dev)
     err = pkv.new_error_word(dev)
 
     cur = lambda: torch.cuda.current_stream(dev)
 
-    def admit(i):
+    def admit(i, l, ready):
+        c, (pos, sc, kls), (k_new, v_new) = pools[l], states[l], news[l]
         if q8:
             pkv.kv_rolling_admit_q8(c["kq"], c["vq"], c["ks"], c["vs"], dbt, pos, sc, kls, lens_rows[i], k_new,
-                                    v_new, wl.n_sink, wl.n_recent, error_word=err, stream=cur())
+                                    v_new, wl.n_sink, wl.n_recent, error_word=err, inputs_ready=ready, stream=cur())
         else:
             pkv.kv_rolling_admit(c["k_cache"], c["v_cache"], dbt, pos, sc, kls, lens_rows[i], k_new, v_new,
-                                 wl.n_sink, wl.n_recent, error_word=err, stream=cur())
+                                 wl.n_sink, wl.n_recent, error_word=err, inputs_ready=ready, stream=cur())
 
-    def decode_scores():
+    def decode_scores(l):
+        c, sc = pools[l], states[l][1]
         if q8:
             pkv.paged_decode_attention_scores_q8(c["q"], c["kq"], c["vq"], c["ks"], c["vs"], dbt, klens, wl.scale,
                                                  sc, out=out, lse=lse, logits=logits, workspace=ws, error_word=err,
@@ -1077,7 +1083,8 @@ def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, c
                                               out=out, lse=lse, logits=logits, workspace=ws, error_word=err,
                                               stream=cur())
 
-    def plain():
+    def plain(l):
+        c = pools[l]
         if q8:
             pkv.paged_decode_attention_q8(c["q"], c["kq"], c["vq"], c["ks"], c["vs"], dbt, klens, wl.scale, out=out,
                                           workspace=ws, stream=cur())
@@ -1086,19 +1093,23 @@ def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, c
                                        workspace=ws, stream=cur())
 
     def restore():
-        pos.copy_(pos0)
-        sc.copy_(sc0)
-        kls.copy_(kl0)
+        for pos, sc, kls in states:
+            pos.copy_(pos0)
+            sc.copy_(sc0)
+            kls.copy_(kl0)
         torch.cuda.synchronize(dev)
 
     def series(body):
+        """body(i, l) enqueues layer l's work of step i; returns ms per (step, layer)."""
         restore()
-        body(0)                              # one eager call: any lazy setup happens outside the capture
+        for l in range(n_layers):            # one eager pass: any lazy setup happens outside the capture
+            body(0, l)
         restore()
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=gstream):
             for i in range(calls):
-                body(i)
+                for l in range(n_layers):
+                    body(i, l)
         times = []
         for _ in range(trials + 1):          # the first replay is a warm-up
             restore()
@@ -1108,11 +1119,13 @@ def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, c
             gr.replay()
             e1.record(gstream)
             torch.cuda.synchronize(dev)
-            times.append(e0.elapsed_time(e1) / calls)
+            times.append(e0.elapsed_time(e1) / (calls * n_layers))
         return sorted(times[1:])[trials // 2]
-    ms_adm = series(admit)
-    ms_layer = series(lambda i: (admit(i), decode_scores()))
-    ms_plain = series(lambda i: plain())
+    ms_adm = series(lambda i, l: admit(i, l, True))
+    ms_adm_plain = series(lambda i, l: admit(i, l, False))
+    ms_layer = series(lambda i, l: (admit(i, l, True), decode_scores(l)))
+    ms_layer_plain = series(lambda i, l: (admit(i, l, False), decode_scores(l)))
+    ms_plain = series(lambda i, l: plain(l))
     if pkv.read_error(err) != 0:
         raise RuntimeError(f"rolling admission reported device error {pkv.read_error(err)}")
     segs = B * hkv
@@ -1124,13 +1137,18 @@ def _rolling_rows(pkv, wl, dev, gstream, lens, scores, c, dbt, klens, ws, out, c
     else:
         kv = decode_bytes(klens.cpu(), B, hq, hkv, d)
     sfx = "_int8" if q8 else ""
+    launch = (f"{calls} steps of {n_layers} layers (each its own pool and state) in one CUDA graph, median of "
+              f"{trials}; admissions declaring their inputs ready")
     return {"sparse_layer_rolling_admit" + sfx: {"ms": round(ms_adm, 4), "bytes": adm_bytes,
-                                                 "gbs": round(adm_bytes / (ms_adm * 1e-3) / 1e9, 1)},
+                                                 "gbs": round(adm_bytes / (ms_adm * 1e-3) / 1e9, 1),
+                                                 "ms_without_inputs_ready": round(ms_adm_plain, 4),
+                                                 "launch": launch},
             "sparse_layer_rolling_step" + sfx: {
-                "ms": round(ms_layer, 4), "ms_plain_compact_decode": round(ms_plain, 4),
+                "ms": round(ms_layer, 4), "ms_without_inputs_ready": round(ms_layer_plain, 4),
+                "ms_plain_compact_decode": round(ms_plain, 4),
                 "gbs": round((kv + adm_bytes) / (ms_layer * 1e-3) / 1e9, 1),
                 "what": "admit + score-emitting decode over 1540 slots per (b, kv head)",
-                "launch": f"{calls} layer steps in one CUDA graph, median of {trials}"}}
+                "launch": launch}}
 
 
 def _time(fn, warmup, steps, dev, stream):

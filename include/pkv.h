@@ -131,6 +131,24 @@ extern "C" {
  */
 #define PKV_COMPACT_INPUTS_READY 1
 
+/*
+ * Flags of pkv_kv_rolling_admit and pkv_kv_rolling_admit_q8 (their `flags` argument; 0 = none).
+ *
+ * PKV_ADMIT_INPUTS_READY -- the caller declares that this call's slot_pos, slot_score,
+ *   kept_lens, context_lens and block_tables are not written by the work that precedes the call
+ *   on its stream and may still be running when the call's kernel starts (with programmatic
+ *   dependent launch, the kernel enqueued just before the call and whatever that kernel lets run
+ *   alongside it).  The admission then scans the slots and chooses each (sequence, kv head)'s
+ *   slot before that work has ended, and waits for it only before it reads k_new and v_new and
+ *   before any write (the pool, the slot state, kept_lens, error_word) -- so the preceding
+ *   kernel may still produce k_new / v_new.  This is the case of a decode step's sparse layers:
+ *   a layer's slot scores were last updated by its own score pass of the previous step, and
+ *   only the new token's K and V come from the work just before ("How KV Sparsity...",
+ *   section "System model").  Results are identical with and without the flag.  Unknown flag
+ *   bits are refused with PKV_ERR_ARGUMENT.
+ */
+#define PKV_ADMIT_INPUTS_READY 1
+
 /* Shape record shared by the calls. */
 typedef struct pkv_dims {
   int32_t batch;              /* B: sequences in this decode step */
@@ -505,6 +523,7 @@ int pkv_kv_compact_q8(void* dst_k_codes, void* dst_v_codes, float* dst_k_scales,
  *   kept_lens        : [B] int32 slots in use (updated).
  *   context_lens     : [B] int32 L_b counting the new token (>= 1).
  *   k_new, v_new     : [B, Hkv, d] bf16.
+ *   flags            : 0 or PKV_ADMIT_INPUTS_READY (see there).
  *   error_word       : optional; PKV_DEV_BAD_SCORE (a NaN score), PKV_DEV_BAD_KEPT_INDEX (the
  *                      leaving token is in no slot), PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT_LEN;
  *                      that (b, g) (or b) is then left unchanged.
@@ -513,7 +532,7 @@ int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tabl
                          int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
                          const int32_t* context_lens, const void* k_new, const void* v_new,
                          int32_t capacity, int32_t n_sink, int32_t n_recent, const pkv_dims* dims,
-                         int32_t* error_word, void* stream);
+                         uint32_t flags, int32_t* error_word, void* stream);
 
 /*
  * pkv_kv_rolling_admit_q8 -- pkv_kv_rolling_admit into INT8 pools: the same choice of slot,
@@ -529,8 +548,8 @@ int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tabl
 int pkv_kv_rolling_admit_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
                             const int32_t* block_tables, int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
                             const int32_t* context_lens, const void* k_new, const void* v_new, int32_t capacity,
-                            int32_t n_sink, int32_t n_recent, const pkv_dims* dims, int32_t* error_word,
-                            void* stream);
+                            int32_t n_sink, int32_t n_recent, const pkv_dims* dims, uint32_t flags,
+                            int32_t* error_word, void* stream);
 
 /*
  * pkv_paged_decode_attention_fixed_scratch -- pkv_paged_decode_attention for callers that

@@ -32,6 +32,7 @@ BLOCK_SIZE = 16
 _INPUTS_READY = header_constants()["PKV_DECODE_INPUTS_READY"]
 _SELECT_READY = header_constants()["PKV_SELECT_INPUTS_READY"]
 _COMPACT_READY = header_constants()["PKV_COMPACT_INPUTS_READY"]
+_ADMIT_READY = header_constants()["PKV_ADMIT_INPUTS_READY"]
 
 
 def _ptr(t):
@@ -395,31 +396,36 @@ def paged_decode_attention_scores_q8(q, k_codes, v_codes, k_scales, v_scales, bl
 
 
 def kv_rolling_admit(k_cache, v_cache, block_tables, slot_pos, slot_score, kept_lens, context_lens, k_new,
-                     v_new, n_sink, n_recent, *, error_word=None, stream=None):
+                     v_new, n_sink, n_recent, *, error_word=None, inputs_ready=False, stream=None):
     """Admit this step's token (k_new/v_new [B, Hkv, d], position context_lens[b] - 1) into each
     sequence's fixed-budget sparse cache: the compact pool [NB, Hkv, 16, d] with its tables,
     slot_pos [B, Hkv, C] int32 and slot_score [B, Hkv, C] fp32 (C = n_sink + k_top + n_recent
-    slots) and kept_lens [B] int32, all updated in place.  See pkv_kv_rolling_admit."""
+    slots) and kept_lens [B] int32, all updated in place.  See pkv_kv_rolling_admit.
+    inputs_ready=True sets PKV_ADMIT_INPUTS_READY: the slot state, lengths and tables are final
+    before the preceding work on the stream, so the slots are chosen before that work ends."""
     nb, hkv, d = _pool_dims(k_cache, v_cache)
     dims = _rolling_dims(nb, hkv, d, k_cache.device, block_tables, slot_pos, slot_score, kept_lens, context_lens,
                          k_new, v_new)
     check("pkv_kv_rolling_admit", load().pkv_kv_rolling_admit(
         _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(slot_pos), _ptr(slot_score), _ptr(kept_lens),
         _ptr(context_lens), _ptr(k_new), _ptr(v_new), slot_pos.shape[2], int(n_sink), int(n_recent),
-        ctypes.byref(dims), _ptr(error_word), _stream(stream, k_cache.device)))
+        ctypes.byref(dims), _ADMIT_READY if inputs_ready else 0, _ptr(error_word), _stream(stream, k_cache.device)))
 
 
 def kv_rolling_admit_q8(k_codes, v_codes, k_scales, v_scales, block_tables, slot_pos, slot_score, kept_lens,
-                        context_lens, k_new, v_new, n_sink, n_recent, *, error_word=None, stream=None):
+                        context_lens, k_new, v_new, n_sink, n_recent, *, error_word=None, inputs_ready=False,
+                        stream=None):
     """kv_rolling_admit into INT8 compact pools (codes [NB, Hkv, 16, d] uint8 as code + 128, row scales
-    [NB, Hkv, 16] fp32): the same slot choice, the new rows quantized into the slot."""
+    [NB, Hkv, 16] fp32): the same slot choice, the new rows quantized into the slot (inputs_ready as
+    kv_rolling_admit)."""
     nb, hkv, d = _q8_pool_dims(k_codes, v_codes, k_scales, v_scales)
     dims = _rolling_dims(nb, hkv, d, k_codes.device, block_tables, slot_pos, slot_score, kept_lens, context_lens,
                          k_new, v_new)
     check("pkv_kv_rolling_admit_q8", load().pkv_kv_rolling_admit_q8(
         _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_tables), _ptr(slot_pos),
         _ptr(slot_score), _ptr(kept_lens), _ptr(context_lens), _ptr(k_new), _ptr(v_new), slot_pos.shape[2],
-        int(n_sink), int(n_recent), ctypes.byref(dims), _ptr(error_word), _stream(stream, k_codes.device)))
+        int(n_sink), int(n_recent), ctypes.byref(dims), _ADMIT_READY if inputs_ready else 0, _ptr(error_word),
+        _stream(stream, k_codes.device)))
 
 
 def _rolling_dims(nb, hkv, d, dev, block_tables, slot_pos, slot_score, kept_lens, context_lens, k_new, v_new):

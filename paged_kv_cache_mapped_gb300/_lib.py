@@ -75,14 +75,14 @@ def load():
             "pkv_paged_decode_attention_append": (I32, [P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, U32, P, P]),
             "pkv_paged_decode_attention_scores": (I32, [P, P, P, P, I32, P, P, P, P, P, P, P, F32, I32, P, SZ,
                                                         D, U32, P, P]),
-            "pkv_kv_rolling_admit": (I32, [P, P, P, P, P, P, P, P, P, I32, I32, I32, D, P, P]),
+            "pkv_kv_rolling_admit": (I32, [P, P, P, P, P, P, P, P, P, I32, I32, I32, D, U32, P, P]),
             "pkv_paged_decode_attention_scores_q8": (I32, [P, P, P, P, I32, P, P, P, P, P, P, P, F32, I32, P,
                                                            SZ, D, U32, P, P]),
             "pkv_paged_decode_attention_append_q8": (I32, [P, P, P, P, P, P, P, P, P, P, F32, I32, P, SZ, D, U32,
                                                            P, P]),
             "pkv_sparse_decode_attention_q8": (I32, [P, P, P, P, P, P, P, P, P, P, I32, F32, P, SZ, D, U32, P, P]),
             "pkv_kv_compact_q8": (I32, [P, P, P, P, P, I32, I32, P, P, P, P, P, P, P, P, I32, D, U32, P, P]),
-            "pkv_kv_rolling_admit_q8": (I32, [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, D, P, P]),
+            "pkv_kv_rolling_admit_q8": (I32, [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, D, U32, P, P]),
             "pkv_sparse_decode_workspace_bytes": (SZ, [D, I32]),
             "pkv_sparse_decode_attention": (I32, [P, P, P, P, P, P, P, P, I32, F32, P, SZ, D, U32, P, P]),
             "pkv_kv_select_topk": (I32, [P, P, P, I32, P, I32, I32, I32, D, U32, P, P]),

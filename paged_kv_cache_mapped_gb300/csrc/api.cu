@@ -659,7 +659,8 @@ int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tabl
                          int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
                          const int32_t* context_lens, const void* k_new, const void* v_new,
                          int32_t capacity, int32_t n_sink, int32_t n_recent, const pkv_dims* dims,
-                         int32_t* error_word, void* stream) {
+                         uint32_t flags, int32_t* error_word, void* stream) {
+  if ((flags & ~(uint32_t)PKV_ADMIT_INPUTS_READY) != 0) return PKV_ERR_ARGUMENT;
   int st = check_dims(dims, false);
   if (st != PKV_OK) return st;
   if (capacity <= 0 || n_sink < 0 || n_recent < 0 || (long long)n_sink + n_recent > capacity)
@@ -675,14 +676,15 @@ int pkv_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* block_tabl
   return cuda_status(launch_kv_rolling_admit(
       k_cache, v_cache, block_tables, dims->num_blocks, dims->max_blocks_per_seq, slot_pos, slot_score,
       kept_lens, context_lens, k_new, v_new, dims->batch, dims->num_kv_heads, dims->head_dim, capacity,
-      n_sink, n_recent, error_word, static_cast<cudaStream_t>(stream)));
+      n_sink, n_recent, (flags & PKV_ADMIT_INPUTS_READY) ? 1 : 0, error_word, static_cast<cudaStream_t>(stream)));
 }
 
 int pkv_kv_rolling_admit_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
                             const int32_t* block_tables, int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
                             const int32_t* context_lens, const void* k_new, const void* v_new, int32_t capacity,
-                            int32_t n_sink, int32_t n_recent, const pkv_dims* dims, int32_t* error_word,
-                            void* stream) {
+                            int32_t n_sink, int32_t n_recent, const pkv_dims* dims, uint32_t flags,
+                            int32_t* error_word, void* stream) {
+  if ((flags & ~(uint32_t)PKV_ADMIT_INPUTS_READY) != 0) return PKV_ERR_ARGUMENT;
   int st = check_dims(dims, false);
   if (st != PKV_OK) return st;
   if (capacity <= 0 || n_sink < 0 || n_recent < 0 || (long long)n_sink + n_recent > capacity)
@@ -699,7 +701,7 @@ int pkv_kv_rolling_admit_q8(void* k_codes, void* v_codes, float* k_scales, float
   return cuda_status(launch_kv_rolling_admit_q8(
       k_codes, v_codes, k_scales, v_scales, block_tables, dims->num_blocks, dims->max_blocks_per_seq, slot_pos,
       slot_score, kept_lens, context_lens, k_new, v_new, dims->batch, dims->num_kv_heads, dims->head_dim, capacity,
-      n_sink, n_recent, error_word, static_cast<cudaStream_t>(stream)));
+      n_sink, n_recent, (flags & PKV_ADMIT_INPUTS_READY) ? 1 : 0, error_word, static_cast<cudaStream_t>(stream)));
 }
 
 int pkv_device_alias(const void* host_ptr, void** device_ptr) {

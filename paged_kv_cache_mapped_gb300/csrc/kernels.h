@@ -195,8 +195,8 @@ cudaError_t launch_kv_compact(void* dk, void* dv, const int32_t* dbt, int dNB, i
 cudaError_t launch_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* bt, int NB, int MB,
                                     int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
                                     const int32_t* lens, const void* k_new, const void* v_new, int B,
-                                    int Hkv, int D, int capacity, int n_sink, int n_recent, int32_t* err,
-                                    cudaStream_t stream);
+                                    int Hkv, int D, int capacity, int n_sink, int n_recent, int early,
+                                    int32_t* err, cudaStream_t stream);
 // INT8 pools: codes [NB, Hkv, 16, D] (bytes code + 128) with row scales [NB, Hkv, 16] fp32 moving with them.
 cudaError_t launch_kv_compact_q8(void* dk, void* dv, float* dks, float* dvs, const int32_t* dbt, int dNB,
                                  int dMB, const void* sk, const void* sv, const float* sks, const float* svs,
@@ -207,7 +207,7 @@ cudaError_t launch_kv_rolling_admit_q8(void* k_cache, void* v_cache, float* k_sc
                                        const int32_t* bt, int NB, int MB, int32_t* slot_pos, float* slot_score,
                                        int32_t* kept_lens, const int32_t* lens, const void* k_new,
                                        const void* v_new, int B, int Hkv, int D, int capacity, int n_sink,
-                                       int n_recent, int32_t* err, cudaStream_t stream);
+                                       int n_recent, int early, int32_t* err, cudaStream_t stream);
 cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const float* scores,
                                int stride, const int32_t* lens, int B, int Hkv, int n_sink,
                                int n_recent, int k_top, int early, int32_t* err, cudaStream_t stream);

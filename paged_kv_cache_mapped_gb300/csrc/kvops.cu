@@ -797,11 +797,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(
 // weakest (score, position) pair across its lanes, then copies the rows (lanes 0-15 K,
 // 16-31 V; with Q8 the rows are quantized into INT8 pools by the row rule of the INT8 append,
 // and a non-finite row leaves its (b, g) unchanged).  The slot count is updated after every
-// head is done.
+// head is done.  EARLY (the caller declared the slot state, lengths and block table final before
+// the preceding work): the warps scan and choose their slots before waiting for that work, and
+// wait before the step's rows are read and before any write -- the error word included.
 constexpr int kAdmitWarps = 8;
 constexpr int kAdmitUnroll = 4;  // 16-byte slot loads in flight per lane and per array
 
-template <int D, bool Q8>
+template <int D, bool Q8, bool EARLY>
 __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
     void* __restrict__ kc, void* __restrict__ vc, float* __restrict__ ks, float* __restrict__ vs,
     const int32_t* __restrict__ bt, int NB, int MB, int32_t* __restrict__ slot_pos, float* __restrict__ slot_score,
@@ -810,12 +812,14 @@ __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  grid_dependency_wait();
+  if constexpr (!EARLY) grid_dependency_wait();
   grid_launch_dependents();
   const int L = lens[b];
   const int used = kept_lens[b];
   const bool valid = L >= 1 && used >= 0 && used <= capacity;
-  if (!valid && threadIdx.x == 0) record_error(err, PKV_DEV_BAD_CONTEXT_LEN);
+  if constexpr (!EARLY) {
+    if (!valid && threadIdx.x == 0) record_error(err, PKV_DEV_BAD_CONTEXT_LEN);
+  }
   const bool full = used == capacity;
   for (int g = warp; valid && g < Hkv; g += kAdmitWarps) {
     int32_t* pos = slot_pos + ((size_t)b * Hkv + g) * capacity;
@@ -879,6 +883,7 @@ __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
       }
       nan = __any_sync(kFullMask, nan);
       if (nan || s_out < 0) {
+        if constexpr (EARLY) grid_dependency_wait();
         if (lane == 0) record_error(err, nan ? PKV_DEV_BAD_SCORE : PKV_DEV_BAD_KEPT_INDEX);
         ok = false;
       } else {
@@ -888,6 +893,7 @@ __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
     }
     if (ok) {
       const int blk = target / 16 < MB ? bt[(size_t)b * MB + target / 16] : -1;
+      if constexpr (EARLY) grid_dependency_wait();  // the step's rows, and every write, after it
       if (blk < 0 || blk >= NB) {
         if (lane == 0) record_error(err, PKV_DEV_BAD_BLOCK_ID);
       } else {
@@ -908,6 +914,10 @@ __global__ void __launch_bounds__(kAdmitWarps * 32) kv_rolling_admit_kernel(
         }
       }
     }
+  }
+  if constexpr (EARLY) {  // every thread waits, so the call also ends after the work it follows
+    grid_dependency_wait();
+    if (!valid && threadIdx.x == 0) record_error(err, PKV_DEV_BAD_CONTEXT_LEN);
   }
   __syncthreads();
   if (threadIdx.x == 0 && valid && !full) kept_lens[b] = used + 1;
@@ -1011,28 +1021,35 @@ cudaError_t launch_select_topk(int32_t* kept_out, int32_t* kept_lens_out, const 
 cudaError_t launch_kv_rolling_admit(void* k_cache, void* v_cache, const int32_t* bt, int NB, int MB,
                                     int32_t* slot_pos, float* slot_score, int32_t* kept_lens,
                                     const int32_t* lens, const void* k_new, const void* v_new, int B,
-                                    int Hkv, int D, int capacity, int n_sink, int n_recent, int32_t* err,
-                                    cudaStream_t stream) {
+                                    int Hkv, int D, int capacity, int n_sink, int n_recent, int early,
+                                    int32_t* err, cudaStream_t stream) {
   return launch_kv_rolling_admit_q8(k_cache, v_cache, nullptr, nullptr, bt, NB, MB, slot_pos, slot_score,
-                                    kept_lens, lens, k_new, v_new, B, Hkv, D, capacity, n_sink, n_recent, err,
-                                    stream);
+                                    kept_lens, lens, k_new, v_new, B, Hkv, D, capacity, n_sink, n_recent, early,
+                                    err, stream);
 }
 
 cudaError_t launch_kv_rolling_admit_q8(void* k_cache, void* v_cache, float* k_scales, float* v_scales,
                                        const int32_t* bt, int NB, int MB, int32_t* slot_pos, float* slot_score,
                                        int32_t* kept_lens, const int32_t* lens, const void* k_new,
                                        const void* v_new, int B, int Hkv, int D, int capacity, int n_sink,
-                                       int n_recent, int32_t* err, cudaStream_t stream) {
+                                       int n_recent, int early, int32_t* err, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   auto* kn = static_cast<const __nv_bfloat16*>(k_new);
   auto* vn = static_cast<const __nv_bfloat16*>(v_new);
   void* args[] = {&k_cache, &v_cache, &k_scales, &v_scales, &bt, &NB, &MB, &slot_pos, &slot_score, &kept_lens,
                   &lens, &kn, &vn, &Hkv, &capacity, &n_sink, &n_recent, &err};
   const bool q8 = k_scales != nullptr;
-  const void* fn = q8 ? (D == 128 ? (const void*)kv_rolling_admit_kernel<128, true>
-                                  : (const void*)kv_rolling_admit_kernel<64, true>)
-                      : (D == 128 ? (const void*)kv_rolling_admit_kernel<128, false>
-                                  : (const void*)kv_rolling_admit_kernel<64, false>);
+  const void* fn;
+  if (early)
+    fn = q8 ? (D == 128 ? (const void*)kv_rolling_admit_kernel<128, true, true>
+                        : (const void*)kv_rolling_admit_kernel<64, true, true>)
+            : (D == 128 ? (const void*)kv_rolling_admit_kernel<128, false, true>
+                        : (const void*)kv_rolling_admit_kernel<64, false, true>);
+  else
+    fn = q8 ? (D == 128 ? (const void*)kv_rolling_admit_kernel<128, true, false>
+                        : (const void*)kv_rolling_admit_kernel<64, true, false>)
+            : (D == 128 ? (const void*)kv_rolling_admit_kernel<128, false, false>
+                        : (const void*)kv_rolling_admit_kernel<64, false, false>);
   return launch_pdl(fn, dim3(B), dim3(kAdmitWarps * 32), 0, stream, args);
 }
 

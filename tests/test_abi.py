@@ -104,15 +104,17 @@ def test_host_validation_codes(lib):
     assert scores(k_new=0x60000) == c["PKV_ERR_NULL_POINTER"]        # k_new without v_new
     assert scores() == c["PKV_ERR_WORKSPACE"]                         # 16-byte workspace
     # rolling admission
-    def admit(cap=60, n_sink=4, n_recent=32, slot_pos=0x30000, dims=None):
+    def admit(cap=60, n_sink=4, n_recent=32, slot_pos=0x30000, dims=None, flags=0):
         return lib.pkv_kv_rolling_admit(P(0x10000), P(0x10000), P(0x10000), P(slot_pos), P(0x40000),
                                         P(0x50000), P(0x60000), P(0x70000), P(0x80000), cap, n_sink,
-                                        n_recent, ctypes.byref(dims or _dims()), None, None)
+                                        n_recent, ctypes.byref(dims or _dims()), flags, None, None)
     assert admit(cap=0) == c["PKV_ERR_ARGUMENT"]
     assert admit(n_sink=40, n_recent=32) == c["PKV_ERR_ARGUMENT"]     # sinks + recent > capacity
     assert admit(cap=64 * 16 + 1) == c["PKV_ERR_DIMS"]                # more slots than the tables
     assert admit(slot_pos=0) == c["PKV_ERR_NULL_POINTER"]
     assert admit(dims=_dims(B=0)) == c["PKV_OK"]
+    assert admit(dims=_dims(B=0), flags=c["PKV_ADMIT_INPUTS_READY"]) == c["PKV_OK"]
+    assert admit(flags=2) == c["PKV_ERR_ARGUMENT"]                     # unknown flag bit
     # INT8 pools
     def q8_append(ks=0x30000, n=4):
         return lib.pkv_kv_append_q8(P(0x10000), P(0x10000), P(ks), P(0x40000), P(0x10000), P(0x10000),
@@ -174,14 +176,15 @@ def test_host_validation_codes(lib):
                               P(0x60000), P(0x70000), P(0x80000), 8, ctypes.byref(_dims()), 4, None,
                               None) == c["PKV_ERR_ARGUMENT"]
 
-    def q8_admit(cap=60, n_sink=4, n_recent=32, ks=0x30000):
+    def q8_admit(cap=60, n_sink=4, n_recent=32, ks=0x30000, flags=0):
         return lib.pkv_kv_rolling_admit_q8(P(0x10000), P(0x10000), P(ks), P(0x40000), P(0x10000), P(0x30000),
                                            P(0x40000), P(0x50000), P(0x60000), P(0x70000), P(0x80000), cap,
-                                           n_sink, n_recent, ctypes.byref(_dims()), None, None)
+                                           n_sink, n_recent, ctypes.byref(_dims()), flags, None, None)
     assert q8_admit(cap=0) == c["PKV_ERR_ARGUMENT"]
     assert q8_admit(cap=64 * 16 + 1) == c["PKV_ERR_DIMS"]
     assert q8_admit(ks=0) == c["PKV_ERR_NULL_POINTER"]
     assert q8_admit(ks=0x30004) == c["PKV_ERR_ALIGNMENT"]
+    assert q8_admit(flags=4) == c["PKV_ERR_ARGUMENT"]                  # unknown flag bit
     # prefill-window score
     def prefill(alpha=16, stride=64, lse=0x30000, qw=0x10000, dims=None):
         return lib.pkv_prefill_window_scores(P(0x40000), stride, P(lse), 0, P(qw), P(0x10000), P(0x10000),

@@ -661,3 +661,127 @@ def test_sparse_layers_flagged_pipeline_full_size():
     ref = oracle.sparse_decode(bits(c["q"]), bits(c["k_cache"]), bits(c["v_cache"]), c["block_tables"].cpu().numpy(),
                                lens.numpy(), okept, okl, wl.scale, rows=rows)
     assert_attn_close(of[1].view(-1, d)[torch.tensor(rows, device=DEV)], ref, "sparse layer 5, flagged gather")
+
+
+def _admit_layer_state(B, hkv, d, cap, seed, q8):
+    """One sparse layer's rolling state: a compact pool (bf16, or INT8 codes and scales) with
+    noise in unused slots, its shuffled table, and empty slot arrays."""
+    rng = np.random.default_rng(seed)
+    mb = (cap + 15) // 16
+    nb = B * mb + 5
+    st = {"bt": torch.from_numpy(rng.permutation(nb)[: B * mb].reshape(B, mb).astype(np.int32)).to(DEV),
+          "slot_pos": torch.full((B, hkv, cap), -1, dtype=torch.int32, device=DEV),
+          "slot_score": torch.zeros((B, hkv, cap), dtype=torch.float32, device=DEV),
+          "kept_lens": torch.zeros(B, dtype=torch.int32, device=DEV)}
+    if q8:
+        for name in ("kq", "vq"):
+            st[name] = torch.from_numpy(stored_codes(rng.integers(-127, 128, size=(nb, hkv, 16, d)))).to(DEV)
+        for name in ("ks", "vs"):
+            st[name] = torch.from_numpy(rng.exponential(size=(nb, hkv, 16)).astype(np.float32)).to(DEV)
+    else:
+        for name in ("kc", "vc"):
+            st[name] = torch.from_numpy(rng.integers(0, 1 << 16, size=(nb, hkv, 16, d)).astype(np.uint16)).to(DEV) \
+                .view(torch.bfloat16)
+    return st
+
+
+_POOL_KEYS = {False: ("kc", "vc"), True: ("kq", "vq", "ks", "vs")}
+_SLOT_KEYS = ("slot_pos", "slot_score", "kept_lens")
+
+
+def _admit_gpu(st, lens, kn, vn, n_sink, n_recent, q8, ready, err=None):
+    if q8:
+        pkv.kv_rolling_admit_q8(st["kq"], st["vq"], st["ks"], st["vs"], st["bt"], st["slot_pos"], st["slot_score"],
+                                st["kept_lens"], lens, kn, vn, n_sink, n_recent, error_word=err, inputs_ready=ready)
+    else:
+        pkv.kv_rolling_admit(st["kc"], st["vc"], st["bt"], st["slot_pos"], st["slot_score"], st["kept_lens"], lens,
+                             kn, vn, n_sink, n_recent, error_word=err, inputs_ready=ready)
+
+
+def _admit_oracle(ref, bt, lens, kn, vn, n_sink, n_recent, q8):
+    """The oracle's admission on numpy state `ref` (pool arrays then the slot arrays), in place."""
+    if q8:
+        out = oracle.rolling_admit_q8(*(ref[k] for k in ("kq", "vq", "ks", "vs")), bt, ref["slot_pos"],
+                                      ref["slot_score"], ref["kept_lens"], lens, kn, vn, n_sink, n_recent)
+        keys = ("kq", "vq", "ks", "vs") + _SLOT_KEYS
+    else:
+        out = oracle.rolling_admit(ref["kc"], ref["vc"], bt, ref["slot_pos"], ref["slot_score"], ref["kept_lens"],
+                                   lens, kn, vn, n_sink, n_recent)
+        keys = ("kc", "vc") + _SLOT_KEYS
+    ref.update(zip(keys, out))
+
+
+@pytest.mark.parametrize("q8,d", [(False, 128), (False, 64), (True, 128)])
+def test_admissions_of_interleaved_layers_flagged_against_oracle(q8, d):
+    """PKV_ADMIT_INPUTS_READY: three sparse layers, each with its own rolling state, stepped from
+    empty to full and past it with no synchronisation: per step, each layer's admission (flagged)
+    and then that layer's score update (a torch add standing in for its score pass), so each
+    admission's preceding work is the previous layer's update, never its own state's writer.  The
+    final state of every layer equals the oracle's chain bit for bit."""
+    B, hkv, n_sink, k_top, n_recent = 3, 4, 4, 24, 32
+    cap = n_sink + k_top + n_recent
+    layers = [_admit_layer_state(B, hkv, d, cap, 90 + 7 * l, q8) for l in range(3)]
+    rng = np.random.default_rng(5 + d)
+    g = torch.Generator().manual_seed(6 + d)
+    steps = 110
+    kns = [[rand_bf16((B, hkv, d), g) for _ in layers] for _ in range(steps)]
+    vns = [[rand_bf16((B, hkv, d), g) for _ in layers] for _ in range(steps)]
+    incs = [[rng.choice([0.0, 0.25, 0.5, 1.0], size=(B, hkv, cap)).astype(np.float32) for _ in layers]
+            for _ in range(steps)]
+    lens = [torch.full((B,), L, dtype=torch.int32, device=DEV) for L in range(1, steps + 1)]
+    refs = [{k: v.cpu().numpy().copy() if v.dtype != torch.bfloat16 else bits(v) for k, v in st.items() if k != "bt"}
+            for st in layers]
+    dk = [[(kns[i][l].to(DEV), vns[i][l].to(DEV), torch.from_numpy(incs[i][l]).to(DEV)) for l in range(3)]
+          for i in range(steps)]
+    err = pkv.new_error_word(DEV)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        for l, st in enumerate(layers):
+            kn, vn, inc = dk[i][l]
+            _admit_gpu(st, lens[i], kn, vn, n_sink, n_recent, q8, True, err)
+            st["slot_score"].add_(inc)
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == 0
+    for l, (st, ref) in enumerate(zip(layers, refs)):
+        bt = st["bt"].cpu().numpy()
+        for i in range(steps):
+            _admit_oracle(ref, bt, lens[i].cpu().numpy(), bits(kns[i][l]), bits(vns[i][l]), n_sink, n_recent, q8)
+            ref["slot_score"] = ref["slot_score"] + incs[i][l]
+        for name in _POOL_KEYS[q8] + _SLOT_KEYS:
+            got = st[name]
+            got = bits(got) if got.dtype == torch.bfloat16 else got.cpu().numpy()
+            assert np.array_equal(got, ref[name]), f"layer {l} {name}"
+
+
+def test_admission_flagged_errors_after_the_wait():
+    """A NaN slot score and a context length of 0, found before the wait by flagged admissions,
+    are recorded once the calls may write; the (b, g) with the NaN and the sequence with the bad
+    length are left unchanged."""
+    B, hkv, d, n_sink, k_top, n_recent = 2, 2, 64, 2, 4, 6
+    cap = n_sink + k_top + n_recent
+    st = _admit_layer_state(B, hkv, d, cap, 31, False)
+    g = torch.Generator().manual_seed(31)
+    for L in range(1, cap + 1):  # fill the budget
+        _admit_gpu(st, torch.full((B,), L, dtype=torch.int32, device=DEV), rand_bf16((B, hkv, d), g).to(DEV),
+                   rand_bf16((B, hkv, d), g).to(DEV), n_sink, n_recent, False, False)
+    torch.cuda.synchronize()
+    st["slot_score"][1, 0, 5] = float("nan")
+    before = {k: st[k].clone() for k in ("slot_pos", "slot_score", "kept_lens")}
+    err = pkv.new_error_word(DEV)
+    torch.cuda.synchronize()
+    _admit_gpu(st, torch.full((B,), cap + 1, dtype=torch.int32, device=DEV), rand_bf16((B, hkv, d), g).to(DEV),
+               rand_bf16((B, hkv, d), g).to(DEV), n_sink, n_recent, False, True, err)
+    torch.cuda.synchronize()
+    C = pkv.header_constants()
+    assert pkv.read_error(err, clear=True) == C["PKV_DEV_BAD_SCORE"]
+    assert torch.equal(st["slot_pos"][1, 0], before["slot_pos"][1, 0])
+    assert not torch.equal(st["slot_pos"][0, 0], before["slot_pos"][0, 0])   # the others admitted
+    st["slot_score"][1, 0, 5] = 0.0
+    before = {k: st[k].clone() for k in ("slot_pos", "slot_score", "kept_lens")}
+    torch.cuda.synchronize()
+    bad = torch.tensor([cap + 2, 0], dtype=torch.int32, device=DEV)
+    _admit_gpu(st, bad, rand_bf16((B, hkv, d), g).to(DEV), rand_bf16((B, hkv, d), g).to(DEV), n_sink, n_recent,
+               False, True, err)
+    torch.cuda.synchronize()
+    assert pkv.read_error(err) == C["PKV_DEV_BAD_CONTEXT_LEN"]
+    assert torch.equal(st["slot_pos"][1], before["slot_pos"][1]) and torch.equal(st["kept_lens"], before["kept_lens"])
